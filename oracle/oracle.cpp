@@ -1,0 +1,357 @@
+// CPU oracle for the DominoTree drafting-round tree builder.
+//
+// TEST INFRASTRUCTURE. Only the test suite, the smoke check and the bench's CPU-baseline leg load this library.
+// The CUDA product path never calls it, and the two share no code: this file has its own bf16 decoding, its own
+// GRU, its own correction and softmax, its own heap.
+//
+// Plain and slow on purpose: fp64 everywhere, one loop per formula, library sort and heap, no blocking or fusion.
+// Inputs are read in their storage form (fp32, or bf16 bit patterns) and widened exactly to double.
+//
+// What it computes follows three web pages about the paper "DominoTree: Conditional Tree-Structured Drafting with
+// Domino for Speculative Decoding" (arXiv 2607.08642):
+//   [S] blog.captcha.la summary      - "Methodology — deep read", "Technical innovations", "Key findings"
+//   [Z] zhichai.top blog (Chinese)   - "两条路线的困境", "DominoTree 的破局"
+//   [G] gist.science explainer (fr)  - "Résumé Technique / Méthodologie / Composants Clés", "Vérification"
+// Where the pages are silent the reading taken is stated next to the code it governs.
+//
+// Parity status of each function (what pins it, all in the CPU test suite):
+//   orc_topm        - pinned: full lexicographic sort of every row (brute force).
+//   orc_gru_step    - pinned: torch.nn.GRUCell in fp64 on the same weights.
+//   orc_child_logp  - pinned: with M = V equals torch.log_softmax of the full-vocabulary corrected row.
+//   orc_build_trees - pinned: brute-force enumeration of the depth-limited M-ary tree on tiny inputs; the
+//                     W_c = 0 factorised closed form; the M = 1 / max_depth = 1 / n = 1 special cases.
+//   orc_rescore     - pinned: must reproduce orc_build_trees' own scores on its own trees, and the brute-force
+//                     path scores.
+//   The GRU gate layout (rows r|z|n, PyTorch convention) and the order "add correction, then divide by T" are
+//   readings; against the real Domino checkpoint the semantics are parity unpinned (no equations on the pages).
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <limits>
+#include <numeric>
+#include <queue>
+#include <vector>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+namespace {
+
+enum { ORC_F32 = 0, ORC_BF16 = 1 };
+
+enum {
+  ORC_OK = 0,
+  ORC_ERR_ARG = 1,      // inconsistent sizes or a null pointer
+  ORC_ERR_NAN = 2,      // a NaN among the logits
+  ORC_ERR_BUDGET = 3,   // fewer than n nodes exist within max_depth
+  ORC_ERR_TREE = 4,     // orc_rescore: the given tree is not a valid draft tree over the candidates
+};
+
+// Exact widening of one stored element to double.
+double load(const void* base, int dtype, size_t i) {
+  if (dtype == ORC_F32) return static_cast<double>(static_cast<const float*>(base)[i]);
+  const uint32_t bits = static_cast<uint32_t>(static_cast<const uint16_t*>(base)[i]) << 16;
+  float f;
+  std::memcpy(&f, &bits, sizeof f);
+  return static_cast<double>(f);
+}
+
+struct Weights {
+  int H, E, dtype;
+  const void* emb;   // [V,E]
+  const void* w_ih;  // [3H,E], gate rows r|z|n
+  const void* w_hh;  // [3H,H], gate rows r|z|n
+  const void* b_ih;  // [3H] or null (zero)
+  const void* b_hh;  // [3H] or null (zero)
+  const void* w_c;   // [V,H] correction rows
+};
+
+double bias(const void* b, int dtype, size_t i) { return b ? load(b, dtype, i) : 0.0; }
+
+// ---------------------------------------------------------------------------------------------------------------
+// Top-M candidate restriction. [S] "Methodology — deep read" and "Technical innovations": at every block position
+// the children may only be the M tokens with the highest marginal logit. [G] "Composants Clés — Restriction de
+// Candidats". Order: value descending, then id ascending (so -0.0 and +0.0 tie and the id decides).
+int topm_row(const void* logits, int dtype, size_t row_off, int V, int M, int32_t* ids, double* vals) {
+  std::vector<double> v(static_cast<size_t>(V));
+  for (int i = 0; i < V; ++i) {
+    v[i] = load(logits, dtype, row_off + static_cast<size_t>(i));
+    if (std::isnan(v[i])) return ORC_ERR_NAN;
+  }
+  std::vector<int> order(static_cast<size_t>(V));
+  std::iota(order.begin(), order.end(), 0);
+  std::partial_sort(order.begin(), order.begin() + M, order.end(), [&](int a, int b) {
+    if (v[a] != v[b]) return v[a] > v[b];
+    return a < b;
+  });
+  for (int m = 0; m < M; ++m) {
+    ids[m] = order[m];
+    vals[m] = v[order[m]];
+  }
+  return ORC_OK;
+}
+
+// ---------------------------------------------------------------------------------------------------------------
+// One step of the Domino GRU along a draft path. [S] "Methodology — deep read": the hidden state is carried and
+// updated along each candidate path. [G] "Composants Clés": only the light GRU correction is recomputed per node.
+// Reading: the pages give no equations, so the cell is PyTorch's GRUCell with gate rows r|z|n:
+//   r = sigmoid(W_ir x + b_ir + W_hr h + b_hr)
+//   u = sigmoid(W_iz x + b_iz + W_hz h + b_hz)          (the update gate, "z" in PyTorch's notation)
+//   g = tanh(W_in x + b_in + r * (W_hn h + b_hn))
+//   h' = (1 - u) * g + u * h
+void gru_step(const Weights& w, const double* x, const double* h, double* out) {
+  const int H = w.H, E = w.E;
+  for (int k = 0; k < H; ++k) {
+    double in_side[3], hid_side[3];
+    for (int gate = 0; gate < 3; ++gate) {
+      const size_t row = static_cast<size_t>(gate) * H + k;
+      double a = bias(w.b_ih, w.dtype, row);
+      for (int e = 0; e < E; ++e) a += load(w.w_ih, w.dtype, row * E + e) * x[e];
+      double c = bias(w.b_hh, w.dtype, row);
+      for (int j = 0; j < H; ++j) c += load(w.w_hh, w.dtype, row * H + j) * h[j];
+      in_side[gate] = a;
+      hid_side[gate] = c;
+    }
+    const double r = 1.0 / (1.0 + std::exp(-(in_side[0] + hid_side[0])));
+    const double u = 1.0 / (1.0 + std::exp(-(in_side[1] + hid_side[1])));
+    const double g = std::tanh(in_side[2] + r * hid_side[2]);
+    out[k] = (1.0 - u) * g + u * h[k];
+  }
+}
+
+// ---------------------------------------------------------------------------------------------------------------
+// Conditional log-probabilities of the M candidates of one block position, given the hidden state h of the node
+// being expanded. [S] "Methodology — deep read": the correction is applied only to the top-M slice, by fetching
+// the matching rows of the correction matrix and of the base logits. [G] "Composants Clés": the base marginal
+// logit L_base is corrected by Delta L (the GRU head's output) on that slice.
+// Reading: Delta L_m = W_c[ids_m] . h; the corrected logit is divided by the temperature (T_eff = 1 when T = 0,
+// greedy decoding, where a softmax is undefined), then log-softmax over the M candidates only.
+void child_logp(const Weights& w, const int32_t* ids, const double* base, int M, double T_eff, const double* h,
+                double* logp) {
+  const int H = w.H;
+  std::vector<double> z(static_cast<size_t>(M));
+  for (int m = 0; m < M; ++m) {
+    double s = 0.0;
+    for (int k = 0; k < H; ++k) s += load(w.w_c, w.dtype, static_cast<size_t>(ids[m]) * H + k) * h[k];
+    z[m] = (base[m] + s) / T_eff;
+  }
+  double mx = z[0];
+  for (int m = 1; m < M; ++m) mx = std::max(mx, z[m]);
+  double sum = 0.0;
+  for (int m = 0; m < M; ++m) sum += std::exp(z[m] - mx);
+  const double lse = std::log(sum);
+  for (int m = 0; m < M; ++m) logp[m] = (z[m] - mx) - lse;
+}
+
+// ---------------------------------------------------------------------------------------------------------------
+// Best-first tree growth. [S] "Methodology — deep read": DDTree's best-first search with a max-priority queue keyed
+// by the cumulative conditional log-probability, expanded until the node budget n (or the depth limit) is reached;
+// the tree is prefix-closed. [G] "Tas de Recherche de Premier Choix à Score Conditionnel".
+// Readings: the root is the last accepted token, has score 0 and hidden state h0 (no GRU step); its children sit
+// at depth 1 and use block position 0, and in general a node at depth d expands into block position d. The budget
+// counts draft nodes only. Ties in the queue: higher score first, then lower token id, then earlier insertion
+// (children are inserted in candidate order m = 0..M-1, the root's first). The n-th pop is not expanded.
+struct Cand {
+  double score;
+  int token;
+  int parent;  // index of the parent among the popped nodes, -1 for a child of the root
+  int depth;
+  long long seq;
+};
+struct RanksBelow {  // a ranks below b in the queue
+  bool operator()(const Cand& a, const Cand& b) const {
+    if (a.score != b.score) return a.score < b.score;
+    if (a.token != b.token) return a.token > b.token;
+    return a.seq > b.seq;
+  }
+};
+
+// Number of nodes of the depth-limited M-ary tree, saturated at `cap`.
+long long tree_size(int M, int max_depth, long long cap) {
+  long long total = 0, level = 1;
+  for (int d = 1; d <= max_depth; ++d) {
+    level = (level > cap / std::max(M, 1)) ? cap : level * M;
+    total = std::min(cap, total + level);
+  }
+  return total;
+}
+
+int build_one(const Weights& w, const int32_t* ids, const double* vals, int M, int n, int max_depth, double T,
+              const double* h0, int32_t* tokens, int32_t* parents, int32_t* depth, double* scores, uint8_t* mask,
+              double* gaps) {
+  const int H = w.H, E = w.E;
+  const double T_eff = T > 0.0 ? T : 1.0;
+  std::priority_queue<Cand, std::vector<Cand>, RanksBelow> frontier;
+  std::vector<double> hs(static_cast<size_t>(n) * H);  // hidden state of every popped, expanded node
+  std::vector<double> logp(static_cast<size_t>(M)), x(static_cast<size_t>(E));
+  long long seq = 0;
+
+  auto expand = [&](const double* h, int parent, int d, double score) {
+    child_logp(w, ids + static_cast<size_t>(d) * M, vals + static_cast<size_t>(d) * M, M, T_eff, h, logp.data());
+    for (int m = 0; m < M; ++m)
+      frontier.push(Cand{score + logp[m], ids[static_cast<size_t>(d) * M + m], parent, d + 1, seq++});
+  };
+
+  expand(h0, -1, 0, 0.0);
+  for (int i = 0; i < n; ++i) {
+    if (frontier.empty()) return ORC_ERR_BUDGET;
+    const Cand u = frontier.top();
+    frontier.pop();
+    gaps[i] = frontier.empty() ? std::numeric_limits<double>::infinity() : u.score - frontier.top().score;
+    tokens[i] = u.token;
+    parents[i] = u.parent;
+    depth[i] = u.depth;
+    scores[i] = u.score;
+    if (i + 1 < n && u.depth < max_depth) {
+      const double* hp = u.parent < 0 ? h0 : &hs[static_cast<size_t>(u.parent) * H];
+      for (int e = 0; e < E; ++e) x[e] = load(w.emb, w.dtype, static_cast<size_t>(u.token) * E + e);
+      gru_step(w, x.data(), hp, &hs[static_cast<size_t>(i) * H]);
+      expand(&hs[static_cast<size_t>(i) * H], i, u.depth, u.score);
+    }
+  }
+  // Ancestor-only attention mask ([S] "Methodology — deep read"; [G] "Vérification"): row i sees itself and its
+  // ancestors. The root (the accepted prefix) is always visible and has no column.
+  for (int i = 0; i < n; ++i) {
+    for (int j = 0; j < n; ++j) mask[static_cast<size_t>(i) * n + j] = 0;
+    for (int j = i; j >= 0; j = parents[j]) mask[static_cast<size_t>(i) * n + j] = 1;
+  }
+  return ORC_OK;
+}
+
+// Scores of a given tree (for instance one built elsewhere), recomputed along each node's path.
+int rescore_one(const Weights& w, const int32_t* ids, const double* vals, int M, int n, int max_depth, double T,
+                const double* h0, const int32_t* tokens, const int32_t* parents, const int32_t* depth,
+                double* scores) {
+  const int H = w.H, E = w.E;
+  const double T_eff = T > 0.0 ? T : 1.0;
+  std::vector<double> hs(static_cast<size_t>(n) * H);
+  std::vector<char> has_h(static_cast<size_t>(n), 0);
+  std::vector<double> logp(static_cast<size_t>(M)), x(static_cast<size_t>(E));
+  for (int i = 0; i < n; ++i) {
+    const int p = parents[i];
+    if (p < -1 || p >= i) return ORC_ERR_TREE;
+    const int d = depth[i];
+    if (d != (p < 0 ? 1 : depth[p] + 1) || d < 1 || d > max_depth) return ORC_ERR_TREE;
+    const double* hp = h0;
+    double base_score = 0.0;
+    if (p >= 0) {
+      if (!has_h[p]) {
+        const double* hpp = parents[p] < 0 ? h0 : &hs[static_cast<size_t>(parents[p]) * H];
+        for (int e = 0; e < E; ++e) x[e] = load(w.emb, w.dtype, static_cast<size_t>(tokens[p]) * E + e);
+        gru_step(w, x.data(), hpp, &hs[static_cast<size_t>(p) * H]);
+        has_h[p] = 1;
+      }
+      hp = &hs[static_cast<size_t>(p) * H];
+      base_score = scores[p];
+    }
+    const size_t pos = static_cast<size_t>(d - 1) * M;
+    child_logp(w, ids + pos, vals + pos, M, T_eff, hp, logp.data());
+    int found = -1;
+    for (int m = 0; m < M; ++m)
+      if (ids[pos + m] == tokens[i]) { found = m; break; }
+    if (found < 0) return ORC_ERR_TREE;
+    scores[i] = base_score + logp[found];
+  }
+  return ORC_OK;
+}
+
+int threads_or_default(int threads) {
+#ifdef _OPENMP
+  return threads > 0 ? threads : omp_get_max_threads();
+#else
+  (void)threads;
+  return 1;
+#endif
+}
+
+}  // namespace
+
+extern "C" {
+
+// Top-M of every row of logits [B,K,V] -> ids [B,K,M], vals [B,K,M] (fp64, exact widening of the stored value).
+int orc_topm(const void* logits, int dtype, int B, int K, int V, int M, int32_t* ids, double* vals, int threads) {
+  if (!logits || !ids || !vals || B < 0 || K < 1 || V < 1 || M < 1 || M > V) return ORC_ERR_ARG;
+  const long long rows = static_cast<long long>(B) * K;
+  int status = ORC_OK;
+#pragma omp parallel for schedule(dynamic) num_threads(threads_or_default(threads))
+  for (long long r = 0; r < rows; ++r) {
+    const int s = topm_row(logits, dtype, static_cast<size_t>(r) * V, V, M, ids + r * M, vals + r * M);
+    if (s != ORC_OK) {
+#pragma omp critical
+      status = s;
+    }
+  }
+  return status;
+}
+
+int orc_gru_step(int H, int E, int wdtype, const void* w_ih, const void* w_hh, const void* b_ih, const void* b_hh,
+                 const double* x, const double* h, double* out) {
+  if (!w_ih || !w_hh || !x || !h || !out || H < 1 || E < 1) return ORC_ERR_ARG;
+  const Weights w{H, E, wdtype, nullptr, w_ih, w_hh, b_ih, b_hh, nullptr};
+  gru_step(w, x, h, out);
+  return ORC_OK;
+}
+
+int orc_child_logp(int H, int wdtype, const void* w_c, const int32_t* ids, const double* base, int M, double T,
+                   const double* h, double* logp) {
+  if (!w_c || !ids || !base || !h || !logp || H < 1 || M < 1 || !(T >= 0.0)) return ORC_ERR_ARG;
+  const Weights w{H, 0, wdtype, nullptr, nullptr, nullptr, nullptr, nullptr, w_c};
+  child_logp(w, ids, base, M, T > 0.0 ? T : 1.0, h, logp);
+  return ORC_OK;
+}
+
+// Best-first conditional trees for B independent requests. ids/vals are the top-M per position ([B,K,M]),
+// h0 is [B,H] (fp64). Outputs: tokens/parents/depth [B,n], scores [B,n], mask [B,n,n], and gaps [B,n] = the popped
+// node's score minus the best remaining frontier score at the time of that pop (+inf if the frontier is empty).
+int orc_build_trees(int B, int K, int M, int n, int max_depth, double T, const int32_t* ids, const double* vals,
+                    const double* h0, int H, int E, int wdtype, const void* emb, const void* w_ih, const void* w_hh,
+                    const void* b_ih, const void* b_hh, const void* w_c, int32_t* tokens, int32_t* parents,
+                    int32_t* depth, double* scores, uint8_t* mask, double* gaps, int threads) {
+  if (!ids || !vals || !h0 || !emb || !w_ih || !w_hh || !w_c || !tokens || !parents || !depth || !scores || !mask ||
+      !gaps || B < 0 || K < 1 || M < 1 || n < 1 || max_depth < 1 || max_depth > K || H < 1 || E < 1 || !(T >= 0.0))
+    return ORC_ERR_ARG;
+  if (tree_size(M, max_depth, n) < n) return ORC_ERR_BUDGET;
+  const Weights w{H, E, wdtype, emb, w_ih, w_hh, b_ih, b_hh, w_c};
+  int status = ORC_OK;
+#pragma omp parallel for schedule(dynamic) num_threads(threads_or_default(threads))
+  for (int b = 0; b < B; ++b) {
+    const size_t kb = static_cast<size_t>(b) * K * M, nb = static_cast<size_t>(b) * n;
+    const int s = build_one(w, ids + kb, vals + kb, M, n, max_depth, T, h0 + static_cast<size_t>(b) * H,
+                            tokens + nb, parents + nb, depth + nb, scores + nb, mask + nb * n, gaps + nb);
+    if (s != ORC_OK) {
+#pragma omp critical
+      status = s;
+    }
+  }
+  return status;
+}
+
+// Scores of given trees (tokens/parents/depth [B,n], in any valid prefix order), recomputed in fp64.
+int orc_rescore(int B, int K, int M, int n, int max_depth, double T, const int32_t* ids, const double* vals,
+                const double* h0, int H, int E, int wdtype, const void* emb, const void* w_ih, const void* w_hh,
+                const void* b_ih, const void* b_hh, const void* w_c, const int32_t* tokens, const int32_t* parents,
+                const int32_t* depth, double* scores, int threads) {
+  if (!ids || !vals || !h0 || !emb || !w_ih || !w_hh || !w_c || !tokens || !parents || !depth || !scores || B < 0 ||
+      K < 1 || M < 1 || n < 1 || max_depth < 1 || max_depth > K || H < 1 || E < 1 || !(T >= 0.0))
+    return ORC_ERR_ARG;
+  const Weights w{H, E, wdtype, emb, w_ih, w_hh, b_ih, b_hh, w_c};
+  int status = ORC_OK;
+#pragma omp parallel for schedule(dynamic) num_threads(threads_or_default(threads))
+  for (int b = 0; b < B; ++b) {
+    const size_t kb = static_cast<size_t>(b) * K * M, nb = static_cast<size_t>(b) * n;
+    const int s = rescore_one(w, ids + kb, vals + kb, M, n, max_depth, T, h0 + static_cast<size_t>(b) * H,
+                              tokens + nb, parents + nb, depth + nb, scores + nb);
+    if (s != ORC_OK) {
+#pragma omp critical
+      status = s;
+    }
+  }
+  return status;
+}
+
+long long orc_tree_size(int M, int max_depth, long long cap) { return tree_size(M, max_depth, cap); }
+
+}  // extern "C"

@@ -1,0 +1,350 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Each pin takes an oracle ctypes handle ``L`` (so the mutation test can run the same pins on deliberately broken
+copies of the oracle) and raises AssertionError (or the oracle's own error) when the oracle is wrong.
+
+What each pin leans on, outside the oracle:
+  * top-M             - a full lexicographic sort of every row (numpy lexsort), i.e. brute force;
+  * GRU step          - torch.nn.GRUCell in fp64 (library routine);
+  * restricted softmax- with M = V it must equal torch.log_softmax over the full-vocabulary corrected row
+                        computed with a dense matmul (no gather);
+  * W_c = 0           - the factorised DDTree closed form: the sum of per-position log-softmaxes of the marginals;
+  * best-first search - brute-force enumeration of every node of the depth-limited M-ary tree, ranked by score;
+  * special cases     - M = 1 (a chain with all scores 0), max_depth = 1, n = 1;
+  * golden fixtures   - hand-derived trees with closed-form scores (tests/golden);
+  * invariants        - prefix closure, depths, monotone scores, ancestor-mask closure.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import torch
+
+from speculative_decoding_tree_top_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def widen(a):
+    """Exact fp64 value of a stored array (uint16 = bf16 bit patterns, or float32)."""
+    if a is None:
+        return None
+    if a.dtype == np.uint16:
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
+
+
+def tiny_inputs(seed, dtype="f32", biases=True, **kw):
+    base = dict(B=1, V=512, K=4, M=6, H=16, E=24, n=12, max_depth=4, T=0.0, dtype=dtype, logit_scale=3.0,
+                boost_count=8, boost_lo=2.0, boost_hi=6.0, name="pin")
+    base.update(kw)
+    return synth.make_inputs(synth.Shape(**base), device="cpu", seed=seed, biases=biases)
+
+
+def host(inp):
+    from oracle import oracle as orc
+    return (synth.host_array(inp.logits), synth.host_array(inp.h0).astype(np.float64), orc.weights_of(inp))
+
+
+# ----------------------------------------------------------------------------------------------------------------
+def pin_topm_bruteforce(L):
+    from oracle import oracle as orc
+    rng = np.random.default_rng(7)
+    for dtype in ("f32", "bf16"):
+        B, K, V = 2, 3, 777
+        x = (rng.standard_normal((B, K, V)) * 3).astype(np.float32)
+        x[0, 0, :50] = 1.5                       # a block of ties
+        x[0, 1, 10], x[0, 1, 11] = -0.0, 0.0     # signed zeros tie
+        x[0, 1, 12:20] = 0.0
+        x[1, 2, 5], x[1, 2, 6] = np.inf, -np.inf
+        x[1, 0, :] = 0.25                        # a whole row of ties
+        arr = x if dtype == "f32" else synth.bits_u16(torch.from_numpy(x).to(torch.bfloat16))
+        full = widen(arr)
+        for M in (1, 37, V):
+            ids, vals = orc.topm(arr, M, L=L)
+            for b in range(B):
+                for k in range(K):
+                    order = np.lexsort((np.arange(V), -full[b, k]))[:M]
+                    assert np.array_equal(ids[b, k], order), (dtype, M, b, k)
+                    assert np.array_equal(vals[b, k], full[b, k][order]), (dtype, M, b, k)
+
+
+def _grucell(w_ih, w_hh, b_ih, b_hh):
+    H, E = w_hh.shape[1], w_ih.shape[1]
+    cell = torch.nn.GRUCell(E, H, bias=True, dtype=torch.float64)
+    with torch.no_grad():
+        cell.weight_ih.copy_(torch.from_numpy(widen(w_ih)))
+        cell.weight_hh.copy_(torch.from_numpy(widen(w_hh)))
+        cell.bias_ih.copy_(torch.from_numpy(widen(b_ih)) if b_ih is not None else torch.zeros(3 * H))
+        cell.bias_hh.copy_(torch.from_numpy(widen(b_hh)) if b_hh is not None else torch.zeros(3 * H))
+    return cell
+
+
+def pin_gru_vs_grucell(L):
+    from oracle import oracle as orc
+    for dtype in ("f32", "bf16"):
+        for biases in (True, False):
+            inp = tiny_inputs(11, dtype=dtype, biases=biases, H=20, E=36)
+            _, _, w = host(inp)
+            cell = _grucell(w["w_ih"], w["w_hh"], w["b_ih"], w["b_hh"])
+            rng = np.random.default_rng(3)
+            for tok in (0, 17, 511):
+                x = widen(w["emb"])[tok]
+                h = rng.standard_normal(20)
+                got = orc.gru_step(w["w_ih"], w["w_hh"], w["b_ih"], w["b_hh"], x, h, L=L)
+                with torch.no_grad():
+                    ref = cell(torch.from_numpy(x)[None], torch.from_numpy(h)[None])[0].numpy()
+                assert np.max(np.abs(got - ref)) < 1e-12, (dtype, biases, tok, np.max(np.abs(got - ref)))
+
+
+def pin_full_vocab_softmax(L):
+    """M = V: the restricted log-softmax over the gathered slice equals the full conditional over the vocabulary."""
+    from oracle import oracle as orc
+    inp = synth.make_inputs(0, device="cpu")
+    logits, _, w = host(inp)
+    V = logits.shape[2]
+    ids, vals = orc.topm(logits, V, L=L)
+    Wc = torch.from_numpy(widen(w["w_c"]))
+    rng = np.random.default_rng(5)
+    for p in range(logits.shape[1]):
+        h = rng.standard_normal(Wc.shape[1])
+        full_row = torch.from_numpy(widen(logits)[0, p])
+        for T in (0.0, 0.5, 1.0, 2.5):
+            Te = T if T > 0 else 1.0
+            ref = torch.log_softmax((full_row + Wc @ torch.from_numpy(h)) / Te, dim=0).numpy()
+            got = orc.child_logp(w["w_c"], ids[0, p], vals[0, p], T, h, L=L)
+            assert np.max(np.abs(got - ref[ids[0, p]])) < 1e-12, (p, T)
+            assert abs(math.fsum(np.exp(got)) - 1.0) < 1e-12
+
+
+def brute_force_nodes(ids, vals, h0, w, max_depth, T):
+    """Every node of the depth-limited M-ary tree with its score, walking each path (torch, fp64)."""
+    Te = T if T > 0 else 1.0
+    M = ids.shape[1]
+    cell = _grucell(w["w_ih"], w["w_hh"], w["b_ih"], w["b_hh"])
+    Wc = torch.from_numpy(widen(w["w_c"]))
+    emb = torch.from_numpy(widen(w["emb"]))
+    paths = [()]
+    scores = torch.zeros(1, dtype=torch.float64)
+    hid = torch.from_numpy(np.asarray(h0, np.float64))[None]
+    nodes = {}
+    with torch.no_grad():
+        for d in range(max_depth):
+            cand = torch.from_numpy(ids[d].astype(np.int64))
+            base = torch.from_numpy(np.asarray(vals[d], np.float64))
+            logp = torch.log_softmax((base[None, :] + hid @ Wc[cand].T) / Te, dim=1)
+            child_scores = (scores[:, None] + logp).reshape(-1)
+            child_paths = [p + (int(t),) for p in paths for t in ids[d]]
+            nodes.update(zip(child_paths, child_scores.tolist()))
+            if d + 1 < max_depth:
+                hid = cell(emb[cand].repeat(len(paths), 1), hid.repeat_interleave(M, dim=0))
+            paths, scores = child_paths, child_scores
+    return nodes
+
+
+def tree_paths(tokens, parents):
+    paths = []
+    for i, t in enumerate(tokens):
+        p = parents[i]
+        paths.append((paths[p] if p >= 0 else ()) + (int(t),))
+    return paths
+
+
+def check_against_bruteforce(tree, nodes, n, sep=1e-9):
+    paths = tree_paths(tree["tokens"], tree["parents"])
+    for i, pth in enumerate(paths):
+        assert pth in nodes, ("not a node of the candidate tree", pth)
+        assert abs(nodes[pth] - tree["scores"][i]) < 1e-12, (i, nodes[pth], tree["scores"][i])
+    ranked = sorted(nodes.items(), key=lambda kv: (-kv[1], kv[0][-1]))
+    bf_scores = np.array([s for _, s in ranked])
+    assert np.max(np.abs(bf_scores[:n] - np.asarray(tree["scores"]))) < 1e-12
+    if len(ranked) == n or bf_scores[n - 1] - bf_scores[n] > sep:
+        assert set(paths) == {p for p, _ in ranked[:n]}
+    for i in range(n):
+        lo_ok = i == 0 or bf_scores[i - 1] - bf_scores[i] > sep
+        hi_ok = i + 1 >= len(ranked) or bf_scores[i] - bf_scores[i + 1] > sep
+        if lo_ok and hi_ok:
+            assert paths[i] == ranked[i][0], (i, paths[i], ranked[i][0])
+
+
+def pin_bruteforce_tree(L):
+    from oracle import oracle as orc
+    cases = [
+        (0, {}, None),                                           # the tiny oracle-check workload itself
+        (21, dict(M=3, n=30, max_depth=4, T=0.5), "f32"),
+        (22, dict(M=5, n=40, max_depth=3, T=1.0, H=12, E=20), "bf16"),
+        (23, dict(M=4, n=60, max_depth=4, T=2.0, logit_scale=0.3), "f32"),
+        (24, dict(M=2, n=14, max_depth=4, T=0.0), "bf16"),
+    ]
+    for seed, kw, dtype in cases:
+        inp = synth.make_inputs(0, device="cpu") if dtype is None else tiny_inputs(seed, dtype=dtype, **kw)
+        s = inp.shape
+        logits, h0, w = host(inp)
+        ids, vals = orc.topm(logits, s.M, L=L)
+        tree = orc.build_trees(ids, vals, h0, w, s.n, s.max_depth, s.T, L=L)
+        nodes = brute_force_nodes(ids[0], vals[0], h0[0], w, s.max_depth, s.T)
+        one = {k: tree[k][0] for k in ("tokens", "parents", "scores")}
+        check_against_bruteforce(one, nodes, s.n)
+
+
+def pin_factorised_closed_form(L):
+    """W_c = 0: each score is the sum over its path of log-softmax(top-M marginals / T) (DDTree's scoring)."""
+    from oracle import oracle as orc
+    for T in (0.0, 0.5, 1.0):
+        inp = tiny_inputs(31, M=5, n=25, max_depth=4, T=T)
+        logits, h0, w = host(inp)
+        w = dict(w)
+        w["w_c"] = np.zeros_like(w["w_c"])
+        ids, vals = orc.topm(logits, 5, L=L)
+        tree = orc.build_trees(ids, vals, h0, w, 25, 4, T, L=L)
+        Te = T if T > 0 else 1.0
+        marg = torch.log_softmax(torch.from_numpy(vals[0]) / Te, dim=1).numpy()   # [K, M]
+        paths = tree_paths(tree["tokens"][0], tree["parents"][0])
+        for i, pth in enumerate(paths):
+            ref = math.fsum(marg[d][list(ids[0, d]).index(t)] for d, t in enumerate(pth))
+            assert abs(ref - tree["scores"][0, i]) < 1e-12, (T, i)
+        # and the factorised tree is the n best paths of the product of marginals
+        nodes = {}
+        for pth in _all_paths(ids[0], 4):
+            nodes[pth] = math.fsum(marg[d][list(ids[0, d]).index(t)] for d, t in enumerate(pth))
+        check_against_bruteforce({k: tree[k][0] for k in ("tokens", "parents", "scores")}, nodes, 25)
+
+
+def _all_paths(ids, max_depth):
+    out, level = [], [()]
+    for d in range(max_depth):
+        level = [p + (int(t),) for p in level for t in ids[d]]
+        out += level
+    return out
+
+
+def pin_special_cases(L):
+    from oracle import oracle as orc
+    # M = 1: every restricted log-softmax is exactly 0; the tree is the chain of top-1 tokens.
+    inp = tiny_inputs(41, M=1, n=4, max_depth=4, K=4)
+    logits, h0, w = host(inp)
+    ids, vals = orc.topm(logits, 1, L=L)
+    tree = orc.build_trees(ids, vals, h0, w, 4, 4, 0.0, L=L)
+    assert np.array_equal(tree["tokens"][0], ids[0, :, 0])
+    assert np.array_equal(tree["parents"][0], [-1, 0, 1, 2])
+    assert np.array_equal(tree["depth"][0], [1, 2, 3, 4])
+    assert np.all(tree["scores"][0] == 0.0)
+    # max_depth = 1: the n best children of the root, by conditional log-prob then token id.
+    inp = tiny_inputs(42, M=7, n=5, max_depth=1, T=0.7)
+    logits, h0, w = host(inp)
+    ids, vals = orc.topm(logits, 7, L=L)
+    tree = orc.build_trees(ids, vals, h0, w, 5, 1, 0.7, L=L)
+    z = (torch.from_numpy(vals[0, 0]) + torch.from_numpy(widen(w["w_c"])[ids[0, 0]]) @ torch.from_numpy(h0[0])) / 0.7
+    lp = torch.log_softmax(z, dim=0).numpy()
+    order = sorted(range(7), key=lambda m: (-lp[m], ids[0, 0, m]))[:5]
+    assert np.array_equal(tree["tokens"][0], ids[0, 0, order])
+    assert np.all(tree["parents"][0] == -1) and np.all(tree["depth"][0] == 1)
+    assert np.max(np.abs(tree["scores"][0] - lp[order])) < 1e-12
+    # n = 1: the arg-max child of the root.
+    tree1 = orc.build_trees(ids, vals, h0, w, 1, 1, 0.7, L=L)
+    assert tree1["tokens"][0, 0] == ids[0, 0, order[0]] and tree1["mask"][0, 0, 0] == 1
+
+
+def _eval_expr(e):
+    ns = {"log": math.log, "tanh": math.tanh, "sigmoid": lambda v: 1.0 / (1.0 + math.exp(-v)), "__builtins__": {}}
+    return float(eval(str(e), ns))  # fixture strings are closed forms over numbers and log/tanh/sigmoid only
+
+
+def _fill(spec, shape_):
+    a = np.zeros(shape_, np.float32)
+    if isinstance(spec, list):
+        for r, c, v in spec:
+            a[r, c] = _eval_expr(v)
+    return a
+
+
+def load_golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        g = json.load(f)
+    V, K, H, E = g["V"], g["K"], g["H"], g["E"]
+    logits = np.full((1, K, V), g["logit_default"], np.float32)
+    for k, v, val in g["logits"]:
+        logits[0, k, v] = _eval_expr(val)
+    w = {"emb": _fill(g["emb"], (V, E)), "w_ih": _fill(g["w_ih"], (3 * H, E)), "w_hh": _fill(g["w_hh"], (3 * H, H)),
+         "b_ih": _fill(g["b_ih"], (1, 3 * H))[0], "b_hh": _fill(g["b_hh"], (1, 3 * H))[0],
+         "w_c": _fill(g["w_c"], (V, H))}
+    h0 = np.asarray(g["h0"], np.float64)[None]
+    return g, logits, h0, w
+
+
+def pin_golden(L):
+    from oracle import oracle as orc
+    for name in ("handworked_factorised.json", "handworked_gru_path.json"):
+        g, logits, h0, w = load_golden(name)
+        ids, vals = orc.topm(logits, g["M"], L=L)
+        tree = orc.build_trees(ids, vals, h0, w, g["n"], g["max_depth"], g["T"], L=L)
+        ex = g["expected"]
+        assert list(tree["tokens"][0]) == ex["tokens"], (name, tree["tokens"][0])
+        assert list(tree["parents"][0]) == ex["parents"], (name, tree["parents"][0])
+        assert list(tree["depth"][0]) == ex["depth"], name
+        want = np.array([_eval_expr(e) for e in ex["scores"]])
+        assert np.max(np.abs(tree["scores"][0] - want)) < g["tolerance"], (name, tree["scores"][0], want)
+
+
+def check_invariants(tokens, parents, depth, scores, mask, n, max_depth):
+    """Properties every draft tree has, whatever its arithmetic."""
+    assert len(tokens) == n
+    for i in range(n):
+        p = parents[i]
+        assert -1 <= p < i, ("not prefix-closed", i, p)
+        assert depth[i] == (1 if p < 0 else depth[p] + 1), ("depth", i)
+        assert 1 <= depth[i] <= max_depth
+        if p >= 0:
+            assert scores[i] <= scores[p], ("child scores above parent", i)
+        anc = set()
+        j = i
+        while j >= 0:
+            anc.add(j)
+            j = parents[j]
+        row = mask[i]
+        assert all((row[j] == 1) == (j in anc) for j in range(n)), ("mask is not the ancestor closure", i)
+    paths = tree_paths(tokens, parents)
+    assert len(set(paths)) == n, "a node appears twice"
+
+
+def pin_invariants(L):
+    from oracle import oracle as orc
+    for seed, kw in ((51, dict(M=8, n=60, max_depth=4)), (52, dict(M=3, n=20, max_depth=4, T=1.0)),
+                     (53, dict(M=6, n=12, max_depth=2, T=0.5))):
+        inp = tiny_inputs(seed, B=3, **kw)
+        s = inp.shape
+        logits, h0, w = host(inp)
+        ids, vals = orc.topm(logits, s.M, L=L)
+        tree = orc.build_trees(ids, vals, h0, w, s.n, s.max_depth, s.T, L=L)
+        for b in range(s.B):
+            check_invariants(tree["tokens"][b], tree["parents"][b], tree["depth"][b], tree["scores"][b],
+                             tree["mask"][b], s.n, s.max_depth)
+            assert np.all(np.diff(tree["scores"][b]) <= 0), "pops are not best-first"
+            assert np.all(tree["gaps"][b] >= 0)
+
+
+def pin_rescore(L):
+    from oracle import oracle as orc
+    inp = tiny_inputs(61, B=2, M=5, n=30, max_depth=4, T=0.5)
+    s = inp.shape
+    logits, h0, w = host(inp)
+    ids, vals = orc.topm(logits, s.M, L=L)
+    tree = orc.build_trees(ids, vals, h0, w, s.n, s.max_depth, s.T, L=L)
+    again = orc.rescore(ids, vals, h0, w, tree["tokens"], tree["parents"], tree["depth"], s.max_depth, s.T, L=L)
+    assert np.max(np.abs(again - tree["scores"])) < 1e-12
+    # a tree in another valid order (breadth-first by depth) gets the brute-force path scores
+    nodes = brute_force_nodes(ids[0], vals[0], h0[0], w, s.max_depth, s.T)
+    chosen = sorted(nodes, key=lambda p: (len(p), p))[:s.n]
+    index = {p: i for i, p in enumerate(chosen)}
+    tok = np.array([[p[-1] for p in chosen]], np.int32)
+    par = np.array([[index[p[:-1]] if len(p) > 1 else -1 for p in chosen]], np.int32)
+    dep = np.array([[len(p) for p in chosen]], np.int32)
+    sc = orc.rescore(ids[:1], vals[:1], h0[:1], w, tok, par, dep, s.max_depth, s.T, L=L)
+    assert np.max(np.abs(sc[0] - [nodes[p] for p in chosen])) < 1e-12
+
+
+ALL_PINS = [pin_topm_bruteforce, pin_gru_vs_grucell, pin_full_vocab_softmax, pin_golden, pin_special_cases,
+            pin_factorised_closed_form, pin_bruteforce_tree, pin_invariants, pin_rescore]

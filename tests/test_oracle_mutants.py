@@ -1,0 +1,66 @@
+"""Plants one plausible mistake at a time in a copy of the oracle (on the CPU) and checks that the pins catch it.
+
+Each mutant is the oracle source with one substring replaced; it is compiled to a temporary library and run
+through the pin suite. A mutant that passes every pin would mean the pins cannot tell that mistake apart.
+"""
+import os
+import subprocess
+
+import pytest
+
+import pins
+from oracle import oracle as orc
+
+MUTANTS = {
+    "topm-order-reversed": ("if (v[a] != v[b]) return v[a] > v[b];", "if (v[a] != v[b]) return v[a] < v[b];"),
+    "topm-id-tiebreak-reversed": ("    return a < b;\n  });", "    return a > b;\n  });"),
+    "gru-drops-b_hh": ("double c = bias(w.b_hh, w.dtype, row);", "double c = 0.0;"),
+    "gru-reset-gate-wrong-row": ("in_side[2] + r * hid_side[2]", "in_side[2] + r * hid_side[1]"),
+    "gru-update-gate-swapped": ("out[k] = (1.0 - u) * g + u * h[k];", "out[k] = u * g + (1.0 - u) * h[k];"),
+    "gru-sigmoid-sign": ("1.0 / (1.0 + std::exp(-(in_side[0] + hid_side[0])))",
+                         "1.0 / (1.0 + std::exp(in_side[0] + hid_side[0]))"),
+    "correction-columns-reversed": ("static_cast<size_t>(ids[m]) * H + k] ", "XX"),
+    "correction-after-temperature": ("z[m] = (base[m] + s) / T_eff;", "z[m] = base[m] / T_eff + s;"),
+    "softmax-drops-normaliser": ("logp[m] = (z[m] - mx) - lse;", "logp[m] = z[m] - mx;"),
+    "position-off-by-one": ("child_logp(w, ids + static_cast<size_t>(d) * M, vals + static_cast<size_t>(d) * M,",
+                            "child_logp(w, ids + static_cast<size_t>(d > 0 ? d - 1 : 0) * M, "
+                            "vals + static_cast<size_t>(d > 0 ? d - 1 : 0) * M,"),
+    "heap-token-tiebreak-reversed": ("if (a.token != b.token) return a.token > b.token;",
+                                     "if (a.token != b.token) return a.token < b.token;"),
+    "heap-seq-tiebreak-reversed": ("return a.seq > b.seq;", "return a.seq < b.seq;"),
+    "hidden-state-not-carried": ("const double* hp = u.parent < 0 ? h0 : &hs[static_cast<size_t>(u.parent) * H];",
+                                 "const double* hp = h0;"),
+    "score-not-cumulative": ("frontier.push(Cand{score + logp[m],", "frontier.push(Cand{logp[m],"),
+    "mask-self-only": ("for (int j = i; j >= 0; j = parents[j]) mask", "for (int j = i; j == i; j = parents[j]) mask"),
+    "embedding-of-parent": ("load(w.emb, w.dtype, static_cast<size_t>(u.token) * E + e)",
+                            "load(w.emb, w.dtype, static_cast<size_t>(u.parent < 0 ? u.token : tokens[u.parent]) * E + e)"),
+}
+
+
+def _mutant_source(name):
+    src = orc.SRC.read_text()
+    old, new = MUTANTS[name]
+    if name == "correction-columns-reversed":
+        old = "load(w.w_c, w.dtype, static_cast<size_t>(ids[m]) * H + k)"
+        new = "load(w.w_c, w.dtype, static_cast<size_t>(ids[m]) * H + (H - 1 - k))"
+    assert src.count(old) >= 1, f"mutation site of {name} not found"
+    return src.replace(old, new)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path):
+    src = tmp_path / "mutant.cpp"
+    src.write_text(_mutant_source(name))
+    out = tmp_path / "libmutant.so"
+    cmd = orc.compile_command(src, out)
+    cmd[1] = "-O1"
+    subprocess.run(cmd, check=True)
+    L = orc.load(out)
+    caught = None
+    for pin in pins.ALL_PINS:
+        try:
+            pin(L)
+        except (AssertionError, orc.OracleError, ValueError, IndexError) as e:
+            caught = (pin.__name__, type(e).__name__)
+            break
+    assert caught is not None, f"no pin detects the planted mistake {name!r}"
