@@ -1,0 +1,389 @@
+#!/usr/bin/env python
+"""Throughput of one DominoTree drafting round on GB300: dt_topm + dt_build_trees, trees per second.
+
+A step is one whole round over one batch of synthetic inputs already resident in HBM: the top-M of every
+(request, position) row over the full vocabulary, then the best-first conditional tree of every request. The default
+workload is the Qwen3-4B-shaped single request (B=1, V=151936, K=16, M=64, E=2560, H=512, n=16, T=0).
+
+Timing: W untimed warm-up steps; then K steps, each timed with CUDA events on the launching stream around the two
+kernels (per-kernel events too); L2 is flushed between steps by a 256 MB memset outside the events; barrier +
+synchronize on both sides; max over ranks. ``e2e`` runs the same rounds through the host-buffer API (pinned logits
+and h0 copied in, the tree copied out, every step). The SM clock is sampled through NVML during the timed region.
+
+``--impl reference`` times the CPU oracle (fp64, the plain restatement of the method) on the same workload.
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PAGES_MS_PER_ROUND = 2.31   # the pages' CUDA-graph builder, n=16, M=64, Qwen3-4B, RTX 5080 / A6000 (context only)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=1, help="workload index (1 = the headline single request)")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--reference-budget", type=float, default=150.0, help="seconds for the whole reference arm")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ---------------------------------------------------------------------------------------------------------------
+class ClockSampler:
+    """SM clock and throttle reasons of one GPU, sampled by NVML in a thread (read-only queries)."""
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+               0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+    def __init__(self, index: int, period_s: float = 0.002):
+        self.period = period_s
+        self.samples = []
+        self.reasons = 0
+        self.max_mhz = None
+        self.ok = False
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            if self.nvml.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(self.h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if self.nvml.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self.ok = True
+        except OSError:
+            pass
+
+    def _run(self):
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nvml.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk)) == 0:
+                self.samples.append(clk.value)
+            if self.nvml.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(rs)) == 0:
+                self.reasons |= rs.value & ~0x1
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self._stop = threading.Event()
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0, "source": "unavailable"}
+        s = sorted(self.samples)
+        return {"sm_mhz": s[len(s) // 2], "sm_max_mhz": self.max_mhz,
+                "reasons": [v for k, v in self.REASONS.items() if self.reasons & k], "samples": len(s),
+                "source": "nvml"}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs"), "measured"
+    return 6800.0, "fallback"
+
+
+def source_sha(name: str) -> str:
+    path = os.path.join(ROOT, "speculative_decoding_tree_top_gb300", "csrc", name)
+    h = hashlib.sha256()
+    for p in (path, os.path.join(ROOT, "speculative_decoding_tree_top_gb300", "csrc", "dt_internal.cuh")):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, source: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current source of the kernel."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel, {}).get(workload)
+    if not e or e.get("source_sha") != source_sha(source):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------------------------------------------
+def algorithmic_bytes(shape, tokens, parents, depth):
+    """Bytes a launch must move at least once (HBM roofline numerators), from the trees actually built.
+
+    dt_topm: the logits once + the ids/values written.
+    dt_build_trees: per request, the W_c rows of every block position it expanded (M rows of H per position; nodes of
+    the same depth share them), one embedding row per GRU step, the GRU weights once (shared by the batch), the
+    top-M ids/values and h0 read, the tree written."""
+    s = 4 if shape.dtype == "f32" else 2
+    B, K, V, M, H, E, n = shape.B, shape.K, shape.V, shape.M, shape.H, shape.E, shape.n
+    topm = B * K * V * s + B * K * M * 8
+    wc = emb = 0
+    for b in range(B):
+        expanded = {0}   # the root expands into position 0
+        gru = 0
+        for i in range(n - 1):
+            if depth[b, i] < shape.max_depth:
+                expanded.add(int(depth[b, i]))
+                gru += 1
+        wc += len(expanded) * M * H * s
+        emb += gru * E * s
+    gru_w = 3 * H * (E + H) * s + 6 * H * s
+    build = wc + emb + gru_w + B * K * M * 8 + B * H * 4 + B * n * 16 + B * n * n
+    return topm, build, dict(w_c_rows=wc, emb_rows=emb, gru_weights=gru_w)
+
+
+# ---------------------------------------------------------------------------------------------------------------
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+    from speculative_decoding_tree_top_gb300 import dominotree as dt, synth
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    s = synth.shape(args.config)
+    inp = synth.make_inputs(args.config, device=dev, seed=1234 + 100 * args.config + 7919 * rank)
+    w = dt.Weights.of(inp)
+    rnd = dt.Round(s.B, s.K, s.V, s.M, s.n, s.max_depth, s.T, w, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(evs=None):
+        flush.zero_()
+        if evs:
+            evs[0].record(stream)
+        dt.dt_topm(inp.logits, s.M, rnd.ids, rnd.vals, rnd.workspace, stream)
+        if evs:
+            evs[1].record(stream)
+        dt.dt_build_trees(rnd.ids, rnd.vals, inp.h0, w, s.n, s.max_depth, s.T, rnd.out, rnd.workspace, stream)
+        if evs:
+            evs[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    rnd.check()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier()
+    with ClockSampler(local) as clocks:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            step(evs[i])
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    barrier()
+    rnd.check()
+    topm_ms = np.array([a.elapsed_time(b) for a, b, _ in evs])
+    build_ms = np.array([b.elapsed_time(c) for _, b, c in evs])
+    round_ms = topm_ms + build_ms
+    total_s = float(round_ms.sum()) / 1e3
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_s], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_s = float(t.item())
+    value = world * s.B * args.steps / total_s
+
+    out = {k: v.cpu().numpy() for k, v in rnd.out.items()}
+    topm_b, build_b, parts = algorithmic_bytes(s, out["tokens"], out["parents"], out["depth"])
+    peak, peak_src = measured_peaks()
+    kernels = {
+        "dt_topm": dict(us=float(topm_ms.mean() * 1e3), bytes=topm_b, gbps=topm_b / (topm_ms.mean() * 1e6),
+                        source="topm.cu"),
+        "dt_build_trees": dict(us=float(build_ms.mean() * 1e3), bytes=build_b,
+                               gbps=build_b / (build_ms.mean() * 1e6), source="build_trees.cu"),
+    }
+    dom = max(kernels, key=lambda k: kernels[k]["us"])
+    kd = kernels[dom]
+    traffic = ncu_traffic(dom, kd["source"], s.name)
+    roofline = {"kernel": dom, "bound": "hbm", "achieved": round(kd["gbps"], 1), "peak": peak, "unit": "GB/s",
+                "frac": round(kd["gbps"] / peak, 4), "traffic": traffic, "peak_source": peak_src,
+                "algorithmic_bytes_per_launch": kd["bytes"], "bytes_breakdown": parts if dom == "dt_build_trees"
+                else {"logits": s.B * s.K * s.V * (4 if s.dtype == "f32" else 2)}}
+
+    e2e = None
+    if not args.no_e2e:
+        hr = dt.HostRound(s.B, s.K, s.V, s.M, s.n, s.max_depth, s.T, w, inp.logits.dtype, device=dev)
+        h_logits = dt.pinned_like(inp.logits)
+        h_logits.copy_(inp.logits)
+        h_h0 = dt.pinned_like(inp.h0)
+        h_h0.copy_(inp.h0)
+        for _ in range(args.warmup):
+            hr.run(h_logits, h_h0)
+        torch.cuda.synchronize()
+        ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        barrier()
+        for i in range(args.steps):
+            flush.zero_()
+            ev2[i][0].record(stream)
+            hr.run(h_logits, h_h0)
+            ev2[i][1].record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        hr.check()
+        assert np.array_equal(hr.host_out["tokens"].numpy(), out["tokens"]), "host-buffer round differs"
+        e2e_s = sum(a.elapsed_time(b) for a, b in ev2) / 1e3
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        e2e = {"value": round(world * s.B * args.steps / e2e_s, 2), "unit": "trees/s",
+               "h2d_bytes_per_step": hr.h2d_bytes(), "d2h_bytes_per_step": hr.d2h_bytes(),
+               "us_per_round": round(e2e_s / args.steps * 1e6, 2)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(inp, args.cpu_budget)
+
+    if rank != 0:
+        return None
+    return {
+        "metric": "trees_per_sec", "value": round(value, 2), "unit": "trees/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_s / args.steps * 1e3, 5),
+        "us_per_round": round(total_s / args.steps * 1e6, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": round(value / (1e3 / PAGES_MS_PER_ROUND), 3) if args.config == 1 else None,
+        "dtype": "f32", "inputs_dtype": s.dtype, "data": "synthetic",
+        "config": {"workload": s.describe(), "B_per_gpu": s.B,
+                   "l2": "flushed between steps (256 MB memset outside the timed events)"},
+        "kernels": {k: {kk: (round(vv, 3) if isinstance(vv, float) else vv) for kk, vv in d.items()}
+                    for k, d in kernels.items()},
+        "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": 2 * args.steps,
+        "clocks": clocks.summary(), "wall_s_timed_loop": round(t_wall, 4),
+    }
+
+
+def cpu_baseline(inp, budget_s):
+    """The oracle as it stands, on whole rounds of the same workload, for about ``budget_s`` seconds."""
+    import numpy as np
+    from oracle import oracle as orc
+    from speculative_decoding_tree_top_gb300.synth import host_array
+    s = inp.shape
+    logits = host_array(inp.logits)
+    h0 = host_array(inp.h0).astype(np.float64)
+    w = orc.weights_of(inp)
+    threads = len(os.sched_getaffinity(0))
+    rounds, t0 = 0, time.perf_counter()
+    while True:
+        ids, vals = orc.topm(logits, s.M, threads=threads)
+        orc.build_trees(ids, vals, h0, w, s.n, s.max_depth, s.T, threads=threads)
+        rounds += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": round(rounds * s.B / el, 3), "unit": "trees/s", "cores": threads, "kind": "oracle",
+            "sample": f"{rounds} whole rounds of {s.name} (B={s.B}) in {el:.1f} s, OpenMP over rows and requests"}
+
+
+def run_reference(args, world, rank):
+    """The CPU oracle timed as the reference arm, on the same workload, metric and unit."""
+    import numpy as np
+    import torch
+    from oracle import oracle as orc
+    from speculative_decoding_tree_top_gb300 import synth
+    from speculative_decoding_tree_top_gb300.synth import host_array
+    if rank != 0:
+        return None
+    s = synth.shape(args.config)
+    inp = synth.make_inputs(args.config, device="cuda" if torch.cuda.is_available() else "cpu")
+    logits = host_array(inp.logits)
+    h0 = host_array(inp.h0).astype(np.float64)
+    w = orc.weights_of(inp)
+    threads = len(os.sched_getaffinity(0))
+
+    def one(frac):
+        # a bounded sample of one round: the top-M of a share of the rows and the tree with a share of the pops
+        rows = max(1, math.ceil(s.K * frac))
+        n = max(1, math.ceil(s.n * frac))
+        ids, vals = orc.topm(np.ascontiguousarray(logits[:, :rows]), s.M, threads=threads)
+        if rows < s.K:
+            full_ids = np.zeros((s.B, s.K, s.M), np.int32)
+            full_vals = np.zeros((s.B, s.K, s.M), np.float64)
+            full_ids[:, :rows], full_vals[:, :rows] = ids, vals
+            full_ids[:, rows:], full_vals[:, rows:] = ids[:, -1:], vals[:, -1:]
+            ids, vals = full_ids, full_vals
+        orc.build_trees(ids, vals, h0, w, n, s.max_depth, s.T, threads=threads)
+        return min(rows / s.K, n / s.n)
+
+    t0 = time.perf_counter()
+    one(1.0)
+    est = time.perf_counter() - t0
+    frac = min(1.0, args.reference_budget / max(1e-9, (args.steps + args.warmup) * est))
+    for _ in range(max(0, args.warmup - 1)):
+        one(frac)
+    t0 = time.perf_counter()
+    done = 0.0
+    for _ in range(args.steps):
+        done += one(frac)
+    el = time.perf_counter() - t0
+    value = done * s.B / el
+    sample = (f"each step: one whole round of {s.name}" if frac >= 1.0 else
+              f"each step: top-M of {max(1, math.ceil(s.K * frac))}/{s.K} rows and {max(1, math.ceil(s.n * frac))}"
+              f"/{s.n} pops of one round, counted as that share of a tree")
+    return {"impl": "reference", "metric": "trees_per_sec", "value": round(value, 3), "unit": "trees/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": s.describe(), "B_per_gpu": s.B},
+            "cpu_baseline": {"value": round(value, 3), "unit": "trees/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": "trees/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, world, rank)
+    else:
+        res = run_ours(args, world, rank, local)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,146 @@
+/*
+ * dominotree.h — C ABI of the GB300 (sm_103a) drafting-round tree builder of DominoTree.
+ *
+ * One drafting round of the method described in "DominoTree: Conditional Tree-Structured Drafting with Domino for
+ * Speculative Decoding" (arXiv 2607.08642), as summarised by blog.captcha.la ("Methodology — deep read",
+ * "Technical innovations"), zhichai.top ("DominoTree 的破局", "GPU 原生树构建器") and gist.science ("Résumé
+ * Technique — Composants Clés"):
+ *
+ *   dt_topm         top-M candidates at each of the K block positions, from the drafter's marginal logits over
+ *                   the full vocabulary ("top-M candidate restriction");
+ *   dt_build_trees  best-first growth of a prefix-closed draft tree keyed by cumulative conditional
+ *                   log-probability: per expanded node one GRU step along its path, the correction W_c[ids]·h on
+ *                   the gathered top-M slice, a temperature-scaled log-softmax restricted to those M; emits tokens,
+ *                   parents, depths, scores and the ancestor-only attention mask of the verify pass.
+ *
+ * Conventions for every call below
+ *   - All array pointers are DEVICE pointers owned by the caller; the library allocates nothing and keeps no
+ *     pointer after a call returns. Arrays are dense, row-major, with the shapes given in brackets, and must start
+ *     on a 16-byte boundary.
+ *   - Calls are asynchronous on `stream`; a round is dt_topm then dt_build_trees on the same stream.
+ *   - Argument errors are detected on the host before anything is launched and return DT_ERR_INVALID_ARG (or
+ *     DT_ERR_UNSUPPORTED for sizes outside the supported envelope); nothing is written then. A failed launch
+ *     returns DT_ERR_CUDA. Problems found on the device (a barrier wait that ran out, a NaN among the logits) are
+ *     recorded in the workspace's status word and read with dt_get_error.
+ *   - The workspace is caller-allocated device memory of at least the size the matching *_workspace_bytes call
+ *     returns, zeroed once (dt_workspace_init) before its first use; each call leaves it ready for the next one.
+ *     dt_build_trees keeps its own region after the one dt_topm uses, so a workspace of
+ *     dt_build_workspace_bytes(...) bytes serves both calls of a round when they are ordered on one stream. Two
+ *     calls that may run concurrently need two workspaces.
+ *   - No C++ exception crosses this boundary. The calls are thread-safe for distinct workspaces.
+ */
+#ifndef DOMINOTREE_H
+#define DOMINOTREE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DT_ABI_VERSION 1
+
+typedef enum {
+  DT_OK = 0,
+  DT_ERR_INVALID_ARG = 1, /* a null or misaligned pointer, or sizes that contradict each other         */
+  DT_ERR_UNSUPPORTED = 2, /* valid, but outside the envelope the kernels are built for (limits below)    */
+  DT_ERR_CUDA = 3,        /* a CUDA runtime call failed (launch, attribute query)                        */
+  DT_ERR_TIMEOUT = 4,     /* device: a grid-barrier wait ran out of its time budget; the kernel returned  */
+  DT_ERR_NUMERIC = 5      /* device: a NaN was found among the logits                                    */
+} dt_status;
+
+typedef enum { DT_F32 = 0, DT_BF16 = 1 } dt_dtype;
+
+/* Supported envelope of dt_build_trees (DT_ERR_UNSUPPORTED beyond). */
+#define DT_MAX_M 1024      /* candidates per position                */
+#define DT_MAX_N 1024      /* node budget                            */
+#define DT_MAX_H 2048      /* GRU hidden width                       */
+#define DT_MAX_E 16384     /* token-embedding width                  */
+
+/* Drafter correction weights, shared by every request of a round. `dtype` is the storage type of all of them.
+ * The GRU follows PyTorch's GRUCell layout: gate rows r | z | n (reset, update, new), each block H rows. */
+typedef struct {
+  int H;              /* GRU hidden width, a multiple of 8                                           */
+  int E;              /* token-embedding width, a multiple of 8                                      */
+  dt_dtype dtype;     /* DT_BF16 or DT_F32                                                           */
+  const void* emb;    /* [V,E]   token embeddings fed to the GRU                                     */
+  const void* w_ih;   /* [3H,E]  input-to-hidden weights                                             */
+  const void* w_hh;   /* [3H,H]  hidden-to-hidden weights                                            */
+  const void* b_ih;   /* [3H]    input bias, or NULL for zero                                        */
+  const void* b_hh;   /* [3H]    hidden bias, or NULL for zero                                       */
+  const void* w_c;    /* [V,H]   correction head: the corrected logit of token v is base_v + w_c[v]·h */
+} dt_weights;
+
+/* Zero a workspace before its first use (cudaMemsetAsync on `stream`). */
+dt_status dt_workspace_init(void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------------------------------------
+ * dt_topm — top-M candidate restriction.
+ * Source: blog.captcha.la, "Methodology — deep read" and "Technical innovations" (the per-node correction only
+ * sees the M tokens with the highest marginal at each depth, M = 64 in the experiments); gist.science,
+ * "Composants Clés — Restriction de Candidats".
+ *
+ *   logits    [B,K,V] of `dtype` (DT_BF16 or DT_F32): the drafter's marginal logits, one row per (request,
+ *             block position). V·sizeof(dtype) need not be a multiple of 16, but the base must be 16-byte aligned.
+ *   out_ids   [B,K,M] int32: candidate token ids of each row, ordered by logit descending, ties by id ascending
+ *             (-0.0 and +0.0 compare equal; -0.0 is returned as +0.0).
+ *   out_vals  [B,K,M] fp32: the candidates' logits, exact copies of the stored values.
+ *   1 <= M <= V, M <= DT_MAX_M. A NaN among the logits sets DT_ERR_NUMERIC on the device (the ids of that row are
+ *   then unspecified but in range).
+ * ------------------------------------------------------------------------------------------------------------- */
+size_t dt_topm_workspace_bytes(int B, int K, int V, int M);
+dt_status dt_topm(const void* logits, dt_dtype dtype, int B, int K, int V, int M, int32_t* out_ids,
+                  float* out_vals, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------------------------------------
+ * dt_build_trees — conditional best-first draft trees for B independent requests.
+ * Source: blog.captcha.la, "Methodology — deep read" (DDTree's best-first max-priority queue keyed by cumulative
+ * conditional log-probability; GRU state carried along each root-to-node path; correction applied only to the
+ * gathered top-M rows; fixed node budget n or max depth; prefix-closed tree verified with the ancestor-only
+ * causal mask); gist.science, "Composants Clés" and "Vérification".
+ *
+ * Semantics (fp32 arithmetic, fp32 accumulation over bf16 or fp32 weights):
+ *   root: score 0, hidden state h0[b], depth 0. A node u at depth d < max_depth is expanded into block position
+ *   d: if u is not the root, h_u = GRUCell(emb[token_u], h_parent(u)); then for m < M
+ *       z_m    = (topm_vals[b,d,m] + w_c[topm_ids[b,d,m]]·h_u) / T_eff,   T_eff = T if T > 0 else 1
+ *       logp_m = z_m - max(z) - log(sum_j exp(z_j - max(z)))
+ *   and the children (token topm_ids[b,d,m], score score_u + logp_m) join the frontier. n nodes are popped, best
+ *   first: higher score, then lower token id, then earlier insertion (children enter in m order). The n-th pop is
+ *   not expanded.
+ *
+ *   topm_ids, topm_vals  [B,K,M] from dt_topm.
+ *   h0                   [B,H] fp32, the hidden state that summarises each request's accepted prefix.
+ *   out_tokens           [B,n] int32, nodes in pop order (scores non-increasing).
+ *   out_parents          [B,n] int32, index of the parent node, -1 for children of the root.
+ *   out_depth            [B,n] int32, in 1..max_depth.
+ *   out_scores           [B,n] fp32, cumulative conditional log-probability of the node's path.
+ *   out_mask             [B,n,n] uint8, 1 where column j is row i itself or one of its ancestors (the root, i.e.
+ *                        the accepted prefix, is visible to every node and has no column).
+ *   Requires 1 <= M <= V, 1 <= max_depth <= K, 1 <= n <= number of nodes of the depth-limited M-ary tree,
+ *   T finite and >= 0, and the limits DT_MAX_*.
+ * ------------------------------------------------------------------------------------------------------------- */
+size_t dt_build_workspace_bytes(int B, int K, int V, int M, int n, int H, int E);
+dt_status dt_build_trees(int B, int K, int V, int M, int n, int max_depth, float T, const int32_t* topm_ids,
+                         const float* topm_vals, const float* h0, const dt_weights* w, int32_t* out_tokens,
+                         int32_t* out_parents, int32_t* out_depth, float* out_scores, uint8_t* out_mask,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Synchronises `stream`, then reads and clears the status word the device wrote into `workspace`. Returns DT_OK
+ * when no device-side problem was recorded. After DT_ERR_TIMEOUT the workspace must be re-initialised. */
+dt_status dt_get_error(void* workspace, cudaStream_t stream);
+
+/* Time budget of every grid-barrier wait inside dt_build_trees, in nanoseconds (default 2 s). A test hook: with a
+ * budget of 0 the first wait gives up at once, the kernel records DT_ERR_TIMEOUT and returns. Process-wide. */
+void dt_set_barrier_timeout_ns(uint64_t ns);
+
+const char* dt_status_string(dt_status s);
+int dt_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DOMINOTREE_H */

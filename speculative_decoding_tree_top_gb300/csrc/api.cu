@@ -1,0 +1,51 @@
+// Status strings, workspace initialisation, device status word, process-wide settings of libdominotree.
+#include <atomic>
+
+#include <cuda_runtime.h>
+
+#include "dt_internal.cuh"
+
+namespace dt {
+namespace {
+std::atomic<uint64_t> g_barrier_timeout_ns{2000000000ull};
+}
+uint64_t barrier_timeout_ns() { return g_barrier_timeout_ns.load(std::memory_order_relaxed); }
+}  // namespace dt
+
+extern "C" const char* dt_status_string(dt_status s) {
+  switch (s) {
+    case DT_OK: return "ok";
+    case DT_ERR_INVALID_ARG: return "invalid argument";
+    case DT_ERR_UNSUPPORTED: return "outside the supported envelope";
+    case DT_ERR_CUDA: return "CUDA runtime error";
+    case DT_ERR_TIMEOUT: return "grid-barrier wait ran out of its time budget";
+    case DT_ERR_NUMERIC: return "NaN among the logits";
+  }
+  return "unknown status";
+}
+
+extern "C" int dt_abi_version(void) { return DT_ABI_VERSION; }
+
+extern "C" void dt_set_barrier_timeout_ns(uint64_t ns) {
+  dt::g_barrier_timeout_ns.store(ns, std::memory_order_relaxed);
+}
+
+extern "C" dt_status dt_workspace_init(void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!workspace || workspace_bytes < sizeof(dt::WsHeader) || !dt::aligned16(workspace)) return DT_ERR_INVALID_ARG;
+  return dt::cuda_status(cudaMemsetAsync(workspace, 0, workspace_bytes, stream));
+}
+
+extern "C" dt_status dt_get_error(void* workspace, cudaStream_t stream) {
+  if (!workspace || !dt::aligned16(workspace)) return DT_ERR_INVALID_ARG;
+  unsigned status = 0;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&status, workspace, sizeof status, cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return DT_ERR_CUDA;
+  if (status != 0) {
+    e = cudaMemsetAsync(workspace, 0, sizeof status, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return DT_ERR_CUDA;
+  }
+  return static_cast<dt_status>(status);
+}

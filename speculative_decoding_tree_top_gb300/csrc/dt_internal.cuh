@@ -1,0 +1,202 @@
+// Internal helpers shared by the CUDA translation units of libdominotree (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dominotree.h"
+
+namespace dt {
+
+// Every workspace starts with this 256-byte header. It is zeroed once (dt_workspace_init); kernels leave it zeroed
+// again except for `status`, which holds the first device-side problem until dt_get_error clears it.
+struct WsHeader {
+  unsigned status;     // dt_status of the first device-side problem, 0 if none
+  unsigned reserved0;
+  unsigned bar_count;  // grid barrier: CTAs arrived at the current barrier
+  unsigned bar_gen;    // grid barrier: generation, bumped by the last CTA to arrive
+  unsigned reserved[60];
+};
+static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
+
+constexpr size_t kAlign = 256;
+__host__ __device__ inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
+
+__device__ __forceinline__ void record_error(WsHeader* hdr, unsigned code) { atomicCAS(&hdr->status, 0u, code); }
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Grid-wide barrier of a cooperative launch. Every wait is bounded: when the budget runs out, or when another CTA
+// has already recorded a problem, the CTA records DT_ERR_TIMEOUT (first problem wins) and the barrier returns
+// false in every thread of the CTA, which must then leave the kernel. Memory written before the barrier by any CTA
+// is visible after it (release by the arrivals and the last arrival, acquire by the waiters).
+__device__ __forceinline__ bool grid_barrier(WsHeader* hdr, unsigned nblocks, uint64_t timeout_ns, int* s_flag) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    const unsigned gen = ld_acquire_gpu(&hdr->bar_gen);
+    const unsigned arrived = atom_add_acq_rel_gpu(&hdr->bar_count, 1u) + 1u;
+    if (arrived == nblocks) {
+      atomicExch(&hdr->bar_count, 0u);
+      st_release_gpu(&hdr->bar_gen, gen + 1u);
+    } else if (timeout_ns == 0) {  // test hook: a zero budget gives up at the first wait
+      record_error(hdr, DT_ERR_TIMEOUT);
+      ok = 0;
+    } else {
+      const uint64_t t0 = global_timer_ns();
+      unsigned polls = 0;
+      while (ld_acquire_gpu(&hdr->bar_gen) == gen) {
+        if ((++polls & 15u) == 0u) {
+          if (ld_acquire_gpu(&hdr->status) != 0u || global_timer_ns() - t0 > timeout_ns) {
+            record_error(hdr, DT_ERR_TIMEOUT);
+            ok = 0;
+            break;
+          }
+        }
+      }
+    }
+    *s_flag = ok;
+  }
+  __syncthreads();
+  return *s_flag != 0;
+}
+
+// ---- order-preserving unsigned keys of logits -------------------------------------------------------------------
+// Larger key <=> larger value. -0.0 is folded onto +0.0 so that both compare equal (the id then decides). Every
+// non-padding element gets a key >= 1, so key 0 marks "no element".
+__device__ __forceinline__ uint32_t key_of_bf16(uint32_t bits) {
+  bits &= 0xFFFFu;
+  if (bits == 0x8000u) bits = 0u;
+  const uint32_t k = (bits & 0x8000u) ? (~bits & 0xFFFFu) : (bits | 0x8000u);
+  return k > 1u ? k : 1u;
+}
+__device__ __forceinline__ uint32_t key_of_f32(uint32_t bits) {
+  if (bits == 0x80000000u) bits = 0u;
+  const uint32_t k = (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
+  return k > 1u ? k : 1u;
+}
+__device__ __forceinline__ bool is_nan_bf16(uint32_t bits) { return (bits & 0x7FFFu) > 0x7F80u; }
+__device__ __forceinline__ bool is_nan_f32(uint32_t bits) { return (bits & 0x7FFFFFFFu) > 0x7F800000u; }
+
+__device__ __forceinline__ float value_of_key_bf16(uint32_t k) {
+  const uint32_t bits = (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu);
+  return __uint_as_float(bits << 16);
+}
+__device__ __forceinline__ float value_of_key_f32(uint32_t k) {
+  const uint32_t bits = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
+  return __uint_as_float(bits);
+}
+
+// A candidate as one 64-bit word: key in the high half, bit-inverted id in the low half, so that the larger word is
+// the larger value and, among equal values, the smaller id. Distinct ids make every word distinct; 0 = empty.
+__device__ __forceinline__ uint64_t pack_candidate(uint32_t key, uint32_t id) {
+  return (static_cast<uint64_t>(key) << 32) | static_cast<uint64_t>(~id);
+}
+__device__ __forceinline__ uint32_t candidate_id(uint64_t c) { return ~static_cast<uint32_t>(c); }
+__device__ __forceinline__ uint32_t candidate_key(uint64_t c) { return static_cast<uint32_t>(c >> 32); }
+
+// ---- block-wide helpers (blockDim.x == 32 * kWarps) -------------------------------------------------------------
+template <int kWarps>
+__device__ __forceinline__ int block_sum(int v, int* s_warp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = __reduce_add_sync(0xFFFFFFFFu, v);
+  if (lane == 0) s_warp[warp] = v;
+  __syncthreads();
+  int t = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) t += s_warp[w];
+  __syncthreads();
+  return t;
+}
+
+template <int kWarps>
+__device__ __forceinline__ int block_exclusive_scan(int v, int* total, int* s_warp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  int base = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const int s = s_warp[w];
+    base += (w < warp) ? s : 0;
+    tot += s;
+  }
+  __syncthreads();
+  *total = tot;
+  return base + incl - v;
+}
+
+template <int kWarps>
+__device__ __forceinline__ uint64_t block_max_u64(uint64_t v, uint64_t* s_warp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint64_t y = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    v = y > v ? y : v;
+  }
+  if (lane == 0) s_warp[warp] = v;
+  __syncthreads();
+  uint64_t m = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) m = s_warp[w] > m ? s_warp[w] : m;
+  __syncthreads();
+  return m;
+}
+
+// Streaming 16-byte load that does not allocate in L1 (the logits are read exactly once).
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+inline dt_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DT_OK : DT_ERR_CUDA; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Workspace layout of dt_topm: header | per-row tickets | per-(row, chunk) candidate lists. dt_build_trees puts its
+// own region after this one, so that one workspace can serve both calls of a round.
+constexpr int kTopmChunk = 8192;  // logits per top-M CTA
+struct TopmLayout {
+  size_t tickets, lists, bytes;
+  int chunks;
+};
+inline TopmLayout topm_layout(int B, int K, int V, int M) {
+  TopmLayout L{};
+  const size_t rows = static_cast<size_t>(B) * static_cast<size_t>(K);
+  L.chunks = (V + kTopmChunk - 1) / kTopmChunk;
+  L.tickets = sizeof(WsHeader);
+  L.lists = align_up(L.tickets + sizeof(unsigned) * rows);
+  const size_t list_bytes = L.chunks > 1 ? sizeof(uint64_t) * rows * static_cast<size_t>(L.chunks) * M : 0;
+  L.bytes = align_up(L.lists + list_bytes);
+  return L;
+}
+
+// Host-side process-wide setting (dt_set_barrier_timeout_ns).
+uint64_t barrier_timeout_ns();
+
+}  // namespace dt

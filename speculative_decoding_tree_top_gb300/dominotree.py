@@ -1,0 +1,265 @@
+"""Python binding of libdominotree (include/dominotree.h): argument marshalling only.
+
+Every function here checks its torch tensors (device, dtype, shape, contiguity), passes their device pointers and
+the current CUDA stream to the C ABI function of the same name, and raises DTError on a non-OK status. All the work
+runs in the library's CUDA kernels; there is no fallback of any kind: without the compiled library the import of
+``lib()`` fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import enum
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import buildlib
+
+
+class Status(enum.IntEnum):
+    OK = 0
+    INVALID_ARG = 1
+    UNSUPPORTED = 2
+    CUDA = 3
+    TIMEOUT = 4
+    NUMERIC = 5
+
+
+F32, BF16 = 0, 1
+
+
+class DTError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = Status(status)
+        super().__init__(f"{where}: {self.status.name} ({_LIB.dt_status_string(int(status)).decode() if _LIB else ''})")
+
+
+class _Weights(ctypes.Structure):
+    _fields_ = [("H", ctypes.c_int), ("E", ctypes.c_int), ("dtype", ctypes.c_int), ("emb", ctypes.c_void_p),
+                ("w_ih", ctypes.c_void_p), ("w_hh", ctypes.c_void_p), ("b_ih", ctypes.c_void_p),
+                ("b_hh", ctypes.c_void_p), ("w_c", ctypes.c_void_p)]
+
+
+_P, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+_LIB: Optional[ctypes.CDLL] = None
+
+# Every symbol the header declares, with its ctypes signature (restype, argtypes).
+SIGNATURES = {
+    "dt_workspace_init": (_I, [_P, _SZ, _P]),
+    "dt_topm_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
+    "dt_topm": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]),
+    "dt_build_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "dt_build_trees": (_I, [_I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _P, ctypes.POINTER(_Weights), _P, _P,
+                            _P, _P, _P, _P, _SZ, _P]),
+    "dt_get_error": (_I, [_P, _P]),
+    "dt_set_barrier_timeout_ns": (None, [ctypes.c_uint64]),
+    "dt_status_string": (ctypes.c_char_p, [_I]),
+    "dt_abi_version": (_I, []),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library. Raises if it has not been built (``__graft_entry__.build()``)."""
+    global _LIB
+    if _LIB is None:
+        if not buildlib.LIB.exists():
+            raise RuntimeError(f"{buildlib.LIB} is missing: the CUDA library must be built first "
+                               "(python -c 'import __graft_entry__ as g; g.build()')")
+        L = ctypes.CDLL(str(buildlib.LIB))
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _LIB = L
+    return _LIB
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise DTError(status, where)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, shape=None) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, not {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, not {tuple(t.shape)}")
+    return t.data_ptr()
+
+
+def _code(dtype: torch.dtype) -> int:
+    if dtype == torch.bfloat16:
+        return BF16
+    if dtype == torch.float32:
+        return F32
+    raise TypeError(f"unsupported dtype {dtype}: bf16 or fp32")
+
+
+def dt_topm_workspace_bytes(B: int, K: int, V: int, M: int) -> int:
+    return int(lib().dt_topm_workspace_bytes(B, K, V, M))
+
+
+def dt_build_workspace_bytes(B: int, K: int, V: int, M: int, n: int, H: int, E: int) -> int:
+    """Workspace of a whole round (the top-M region, then the builder's own)."""
+    return int(lib().dt_build_workspace_bytes(B, K, V, M, n, H, E))
+
+
+def dt_workspace_init(workspace: torch.Tensor, stream=None):
+    _check(lib().dt_workspace_init(_dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream)),
+           "dt_workspace_init")
+
+
+def new_workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """A zero-initialised workspace of at least ``nbytes`` bytes (a uint8 tensor)."""
+    ws = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    dt_workspace_init(ws)
+    return ws
+
+
+def dt_get_error(workspace: torch.Tensor, stream=None) -> Status:
+    return Status(lib().dt_get_error(_dev(workspace, "workspace", torch.uint8), _stream(stream)))
+
+
+def dt_set_barrier_timeout_ns(ns: int):
+    lib().dt_set_barrier_timeout_ns(int(ns))
+
+
+def dt_topm(logits: torch.Tensor, M: int, out_ids: Optional[torch.Tensor] = None,
+            out_vals: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None, stream=None):
+    """Top-M candidates of every row of logits [B,K,V] -> (ids [B,K,M] int32, vals [B,K,M] fp32)."""
+    B, K, V = logits.shape
+    if out_ids is None:
+        out_ids = torch.empty((B, K, M), dtype=torch.int32, device=logits.device)
+    if out_vals is None:
+        out_vals = torch.empty((B, K, M), dtype=torch.float32, device=logits.device)
+    if workspace is None:
+        workspace = new_workspace(dt_topm_workspace_bytes(B, K, V, M), logits.device)
+    _check(lib().dt_topm(_dev(logits, "logits"), _code(logits.dtype), B, K, V, M,
+                         _dev(out_ids, "out_ids", torch.int32, (B, K, M)),
+                         _dev(out_vals, "out_vals", torch.float32, (B, K, M)),
+                         _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream)), "dt_topm")
+    return out_ids, out_vals
+
+
+@dataclass
+class Weights:
+    """The drafter's correction weights (shared by all requests): GRU (gate rows r|z|n), embeddings, W_c."""
+    emb: torch.Tensor                 # [V,E]
+    w_ih: torch.Tensor                # [3H,E]
+    w_hh: torch.Tensor                # [3H,H]
+    b_ih: Optional[torch.Tensor]      # [3H] or None
+    b_hh: Optional[torch.Tensor]      # [3H] or None
+    w_c: torch.Tensor                 # [V,H]
+
+    @property
+    def H(self) -> int:
+        return self.w_hh.shape[1]
+
+    @property
+    def E(self) -> int:
+        return self.w_ih.shape[1]
+
+    def struct(self) -> _Weights:
+        dt = self.w_ih.dtype
+        H, E, V = self.H, self.E, self.emb.shape[0]
+        opt = lambda t, n: _dev(t, n, dt, (3 * H,)) if t is not None else None
+        return _Weights(H, E, _code(dt), _dev(self.emb, "emb", dt, (V, E)), _dev(self.w_ih, "w_ih", dt, (3 * H, E)),
+                        _dev(self.w_hh, "w_hh", dt, (3 * H, H)), opt(self.b_ih, "b_ih"), opt(self.b_hh, "b_hh"),
+                        _dev(self.w_c, "w_c", dt, (V, H)))
+
+    @classmethod
+    def of(cls, inputs) -> "Weights":
+        return cls(inputs.emb, inputs.w_ih, inputs.w_hh, inputs.b_ih, inputs.b_hh, inputs.w_c)
+
+
+def dt_build_trees(topm_ids: torch.Tensor, topm_vals: torch.Tensor, h0: torch.Tensor, weights: Weights, n: int,
+                   max_depth: int, T: float, out: Optional[dict] = None, workspace: Optional[torch.Tensor] = None,
+                   stream=None) -> dict:
+    """Best-first conditional trees -> dict of tokens/parents/depth [B,n] int32, scores [B,n] fp32,
+    mask [B,n,n] uint8."""
+    B, K, M = topm_ids.shape
+    V = weights.emb.shape[0]
+    dev = topm_ids.device
+    if out is None:
+        out = alloc_tree_outputs(B, n, dev)
+    if workspace is None:
+        workspace = new_workspace(dt_build_workspace_bytes(B, K, V, M, n, weights.H, weights.E), dev)
+    w = weights.struct()
+    _check(lib().dt_build_trees(
+        B, K, V, M, n, max_depth, float(T), _dev(topm_ids, "topm_ids", torch.int32, (B, K, M)),
+        _dev(topm_vals, "topm_vals", torch.float32, (B, K, M)), _dev(h0, "h0", torch.float32, (B, weights.H)),
+        ctypes.byref(w), _dev(out["tokens"], "out_tokens", torch.int32, (B, n)),
+        _dev(out["parents"], "out_parents", torch.int32, (B, n)), _dev(out["depth"], "out_depth", torch.int32, (B, n)),
+        _dev(out["scores"], "out_scores", torch.float32, (B, n)),
+        _dev(out["mask"], "out_mask", torch.uint8, (B, n, n)), _dev(workspace, "workspace", torch.uint8),
+        workspace.numel(), _stream(stream)), "dt_build_trees")
+    return out
+
+
+def alloc_tree_outputs(B: int, n: int, device) -> dict:
+    return dict(tokens=torch.empty((B, n), dtype=torch.int32, device=device),
+                parents=torch.empty((B, n), dtype=torch.int32, device=device),
+                depth=torch.empty((B, n), dtype=torch.int32, device=device),
+                scores=torch.empty((B, n), dtype=torch.float32, device=device),
+                mask=torch.empty((B, n, n), dtype=torch.uint8, device=device))
+
+
+class Round:
+    """Preallocated buffers for one drafting round of a fixed shape: dt_topm then dt_build_trees on one stream."""
+
+    def __init__(self, B, K, V, M, n, max_depth, T, weights: Weights, device="cuda"):
+        self.B, self.K, self.V, self.M, self.n, self.max_depth, self.T = B, K, V, M, n, max_depth, T
+        self.weights = weights
+        self.ids = torch.empty((B, K, M), dtype=torch.int32, device=device)
+        self.vals = torch.empty((B, K, M), dtype=torch.float32, device=device)
+        self.out = alloc_tree_outputs(B, n, device)
+        self.workspace = new_workspace(dt_build_workspace_bytes(B, K, V, M, n, weights.H, weights.E), device)
+
+    def __call__(self, logits: torch.Tensor, h0: torch.Tensor, stream=None) -> dict:
+        dt_topm(logits, self.M, self.ids, self.vals, self.workspace, stream)
+        dt_build_trees(self.ids, self.vals, h0, self.weights, self.n, self.max_depth, self.T, self.out,
+                       self.workspace, stream)
+        return self.out
+
+    def check(self, stream=None):
+        _check(int(dt_get_error(self.workspace, stream)), "device status")
+
+
+def pinned_like(t: torch.Tensor) -> torch.Tensor:
+    return torch.empty(t.shape, dtype=t.dtype, device="cpu", pin_memory=True)
+
+
+class HostRound(Round):
+    """A round whose inputs and outputs live in (pinned) host memory: each call copies the logits and h0 to the
+    device, runs dt_topm and dt_build_trees, and copies the tree back, all on one stream."""
+
+    def __init__(self, B, K, V, M, n, max_depth, T, weights: Weights, logits_dtype, device="cuda"):
+        super().__init__(B, K, V, M, n, max_depth, T, weights, device)
+        self.d_logits = torch.empty((B, K, V), dtype=logits_dtype, device=device)
+        self.d_h0 = torch.empty((B, weights.H), dtype=torch.float32, device=device)
+        self.host_out = {k: pinned_like(v) for k, v in self.out.items()}
+
+    def h2d_bytes(self) -> int:
+        return self.d_logits.numel() * self.d_logits.element_size() + self.d_h0.numel() * 4
+
+    def d2h_bytes(self) -> int:
+        return sum(v.numel() * v.element_size() for v in self.host_out.values())
+
+    def run(self, host_logits: torch.Tensor, host_h0: torch.Tensor, stream=None) -> dict:
+        self.d_logits.copy_(host_logits, non_blocking=True)
+        self.d_h0.copy_(host_h0, non_blocking=True)
+        out = self(self.d_logits, self.d_h0, stream)
+        for k, v in out.items():
+            self.host_out[k].copy_(v, non_blocking=True)
+        return self.host_out

@@ -128,28 +128,43 @@ def _distinct_ids(rows: int, count: int, V: int, device, seed: int) -> torch.Ten
     return out.to(device)
 
 
-def make_inputs(config_or_shape, device="cpu", seed: Optional[int] = None, biases: bool = True,
-                **overrides) -> Inputs:
-    """Draw one round's inputs for a workload (an index into CONFIGS, or a Shape)."""
-    if isinstance(config_or_shape, Shape):
-        s = replace(config_or_shape, **overrides)
-        cfg_idx = 0
-    else:
-        cfg_idx = int(config_or_shape)
-        s = shape(cfg_idx, **overrides)
-    if seed is None:
-        seed = 1234 + 100 * cfg_idx
-    device = torch.device(device)
-    B, V, K, H, E = s.B, s.V, s.K, s.H, s.E
-
+def _logits_f32(s: Shape, device, seed: int) -> torch.Tensor:
+    B, K, V = s.B, s.K, s.V
     logits = _normal((B, K, V), s.logit_scale, device, seed, "logits")
     if s.boost_count > 0:
         ids = _distinct_ids(B * K, s.boost_count, V, device, seed)
         g = _gen(device, seed, "boost_vals")
         boost = torch.rand((B * K, s.boost_count), generator=g, device=device, dtype=torch.float32)
         boost = boost * (s.boost_hi - s.boost_lo) + s.boost_lo
-        flat = logits.view(B * K, V)
-        flat.scatter_add_(1, ids, boost)
+        logits.view(B * K, V).scatter_add_(1, ids, boost)
+    return logits
+
+
+def _resolve(config_or_shape, seed, overrides):
+    if isinstance(config_or_shape, Shape):
+        s = replace(config_or_shape, **overrides)
+        cfg_idx = 0
+    else:
+        cfg_idx = int(config_or_shape)
+        s = shape(cfg_idx, **overrides)
+    return s, (1234 + 100 * cfg_idx if seed is None else seed)
+
+
+def make_logits(config_or_shape, device="cpu", seed: Optional[int] = None, **overrides) -> torch.Tensor:
+    """Only the marginal logits [B,K,V] of a workload (same values as make_inputs draws)."""
+    s, seed = _resolve(config_or_shape, seed, overrides)
+    logits = _logits_f32(s, torch.device(device), seed)
+    return logits.to(s.torch_dtype).contiguous()
+
+
+def make_inputs(config_or_shape, device="cpu", seed: Optional[int] = None, biases: bool = True,
+                **overrides) -> Inputs:
+    """Draw one round's inputs for a workload (an index into CONFIGS, or a Shape)."""
+    s, seed = _resolve(config_or_shape, seed, overrides)
+    device = torch.device(device)
+    B, V, H, E = s.B, s.V, s.H, s.E
+
+    logits = _logits_f32(s, device, seed)
     h0 = _normal((B, H), 1.0, device, seed, "h0")
     w_ih = _normal((3 * H, E), 1.0 / math.sqrt(E), device, seed, "w_ih")
     w_hh = _normal((3 * H, H), 1.0 / math.sqrt(H), device, seed, "w_hh")

@@ -1,0 +1,116 @@
+"""The C-ABI library loads, exports every symbol the header declares, and rejects bad arguments on the host
+before anything is launched (no GPU needed: validation runs before the first CUDA call)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "dominotree.h")
+
+OK, INVALID, UNSUPPORTED = 0, 1, 2
+A = 1 << 20  # a 16-byte-aligned fake device address: validation must reject before any dereference
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return set(re.findall(r"\b(dt_[a-z_0-9]+)\s*\(", text))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    assert {"dt_topm", "dt_build_trees", "dt_topm_workspace_bytes", "dt_build_workspace_bytes", "dt_get_error",
+            "dt_workspace_init", "dt_status_string"} <= names
+
+
+def test_library_exports_every_declared_symbol(dtlib):
+    L = dtlib.lib()
+    names = declared_functions()
+    assert names == set(dtlib.SIGNATURES), "binding signatures and header declarations diverge"
+    for name in names:
+        assert getattr(L, name) is not None
+    nm = subprocess.run(["nm", "-D", "--defined-only", str(dtlib.buildlib.LIB)], capture_output=True, text=True)
+    exported = set(re.findall(r"\b(dt_[a-z_0-9]+)\b", nm.stdout))
+    assert names <= exported
+    assert L.dt_abi_version() == 1
+
+
+def test_status_strings(dtlib):
+    L = dtlib.lib()
+    for s in range(6):
+        assert L.dt_status_string(s)
+    assert L.dt_status_string(99) == b"unknown status"
+
+
+def test_workspace_sizes(dtlib):
+    t = dtlib.dt_topm_workspace_bytes
+    assert t(1, 4, 1024, 8) >= 256 and t(1, 4, 1024, 8) % 256 == 0
+    # one chunk per row needs no candidate lists; more chunks need [rows][chunks][M] 8-byte words
+    assert t(1, 16, 151936, 64) >= 256 + 16 * 19 * 64 * 8
+    assert t(256, 16, 151936, 128) > t(64, 16, 151936, 64)
+    b = dtlib.dt_build_workspace_bytes
+    assert b(32, 16, 151936, 64, 32, 1024, 4096) >= 32 * 32 * 1024 * 4 + t(32, 16, 151936, 64)
+    # the round's workspace holds the top-M region first, then the builder's own region
+    assert b(2, 4, 20000, 8, 16, 64, 64) > t(2, 4, 20000, 8)
+    assert t(-1, 1, 1, 1) == 0 and b(1, 1, 1, 1, 0, 8, 8) == 0
+
+
+def _topm(L, logits=A, dtype=1, B=1, K=2, V=100, M=5, ids=A, vals=A, ws=A, wsb=1 << 30):
+    return L.dt_topm(logits, dtype, B, K, V, M, ids, vals, ws, wsb, None)
+
+
+def test_topm_rejects_bad_arguments(dtlib):
+    L = dtlib.lib()
+    assert _topm(L, M=0) == INVALID
+    assert _topm(L, M=101) == INVALID
+    assert _topm(L, K=0) == INVALID
+    assert _topm(L, B=-1) == INVALID
+    assert _topm(L, dtype=7) == INVALID
+    assert _topm(L, logits=None) == INVALID
+    assert _topm(L, logits=A + 8) == INVALID          # misaligned
+    assert _topm(L, ws=A + 4) == INVALID
+    assert _topm(L, wsb=16) == INVALID                # workspace too small
+    assert _topm(L, V=5000, M=2000) == UNSUPPORTED    # M above DT_MAX_M
+    assert _topm(L, B=0) == OK                        # nothing to do, nothing launched
+
+
+def _weights(dtlib, H=32, E=32, dtype=1, b_ih=None, emb=A):
+    return dtlib._Weights(H, E, dtype, emb, A, A, b_ih, None, A)
+
+
+def _build(dtlib, B=1, K=4, V=100, M=4, n=8, max_depth=3, T=0.0, w=None, ws=A, wsb=1 << 30):
+    w = w or _weights(dtlib)
+    return dtlib.lib().dt_build_trees(B, K, V, M, n, max_depth, T, A, A, A, ctypes.byref(w), A, A, A, A, A, ws, wsb,
+                                      None)
+
+
+def test_build_rejects_bad_arguments(dtlib):
+    assert _build(dtlib, max_depth=5) == INVALID                 # deeper than the block
+    assert _build(dtlib, M=2, max_depth=2, n=7) == INVALID       # 2 + 4 = 6 nodes exist
+    assert _build(dtlib, M=2, max_depth=2, n=6, B=0) == OK       # exactly the whole tree is allowed
+    assert _build(dtlib, T=-0.5) == INVALID
+    assert _build(dtlib, T=float("nan")) == INVALID
+    assert _build(dtlib, T=float("inf")) == INVALID
+    assert _build(dtlib, w=_weights(dtlib, H=30)) == INVALID     # H not a multiple of 8
+    assert _build(dtlib, w=_weights(dtlib, E=12)) == INVALID
+    assert _build(dtlib, w=_weights(dtlib, dtype=3)) == INVALID
+    assert _build(dtlib, w=_weights(dtlib, emb=None)) == INVALID
+    assert _build(dtlib, w=_weights(dtlib, b_ih=A + 2)) == INVALID
+    assert _build(dtlib, M=0) == INVALID
+    assert _build(dtlib, M=200, V=100) == INVALID
+    assert _build(dtlib, n=0) == INVALID
+    assert _build(dtlib, wsb=64) == INVALID
+    assert _build(dtlib, w=_weights(dtlib, H=4096)) == UNSUPPORTED
+    assert _build(dtlib, M=2000, V=5000) == UNSUPPORTED
+    assert dtlib.lib().dt_build_trees(1, 4, 100, 4, 8, 3, 0.0, A, A, A, None, A, A, A, A, A, A, 1 << 30,
+                                      None) == INVALID
+    assert _build(dtlib, B=0) == OK
+
+
+def test_binding_refuses_host_tensors(dtlib):
+    import torch
+    with pytest.raises(TypeError):
+        dtlib.dt_topm(torch.zeros(1, 2, 64), 4, out_ids=torch.zeros(1, 2, 4, dtype=torch.int32),
+                      out_vals=torch.zeros(1, 2, 4), workspace=torch.zeros(4096, dtype=torch.uint8))

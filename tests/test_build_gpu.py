@@ -1,0 +1,124 @@
+"""dt_build_trees on the GPU against the CPU oracle: structure bit-exact up to the first near-tie (gap <= 1e-3),
+scores within 1e-3 of the oracle's fp64 rescoring of the GPU's own tree, tree invariants everywhere."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import compare
+from speculative_decoding_tree_top_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-3
+
+
+# The stricter pass: two pops count as a near-tie only when the oracle's gap is <= 5e-5, eight times the largest
+# fp32-vs-fp64 score difference seen on these workloads (6e-6); beyond that the builders must decide alike.
+STRICT = 5e-5
+
+
+def run_both(dtlib, orc, inp):
+    s = inp.shape
+    w = dtlib.Weights.of(inp)
+    rnd = dtlib.Round(s.B, s.K, s.V, s.M, s.n, s.max_depth, s.T, w, device="cuda")
+    out = rnd(inp.logits, inp.h0)
+    torch.cuda.synchronize()
+    rnd.check()
+    ora = orc.round_(inp)
+    assert np.array_equal(rnd.ids.cpu().numpy(), ora["ids"])
+    gpu = {k: v.cpu().numpy() for k, v in out.items()}
+    h0 = synth.host_array(inp.h0).astype(np.float64)
+    resc = orc.rescore(ora["ids"], ora["vals"], h0, orc.weights_of(inp), gpu["tokens"], gpu["parents"],
+                       gpu["depth"], s.max_depth, s.T)
+    rep = compare.compare_round(gpu, ora, resc, s.n, s.max_depth, TOL)
+    strict = compare.compare_round(gpu, ora, resc, s.n, s.max_depth, TOL, struct_tol=STRICT)
+    rep["compared_pops_strict"] = strict["compared_pops"]
+    return rep, gpu, ora, rnd
+
+
+@pytest.mark.parametrize("config", [0, 1, 2, 3, 4])
+def test_build_parity_workloads(dtlib, orc, config):
+    inp = synth.make_inputs(config, device="cuda")
+    rep, *_ = run_both(dtlib, orc, inp)
+    print(config, rep)
+    # not vacuous: under the stricter pass most pops are compared bit-exactly (the rest follow a genuine
+    # near-tie of the oracle, where either choice is correct)
+    assert rep["compared_pops"] >= 0.5 and rep["compared_pops_strict"] >= 0.8
+
+
+def tiny(seed, **kw):
+    base = dict(B=2, V=600, K=5, M=6, H=16, E=24, n=12, max_depth=4, T=0.0, dtype="f32", logit_scale=3.0,
+                boost_count=8, boost_lo=2.0, boost_hi=6.0, name="edge")
+    base.update(kw)
+    return synth.make_inputs(synth.Shape(**base), device="cuda", seed=seed)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(M=1, n=4, max_depth=4),                         # a chain, all scores 0
+    dict(max_depth=1, n=5),                              # the best children of the root
+    dict(n=1),                                           # the arg-max
+    dict(M=2, n=30, max_depth=4, K=4),                   # the whole depth-limited tree (2+4+8+16)
+    dict(B=300, n=10),                                   # more requests than SMs
+    dict(H=24, E=40, n=20, T=0.5),                       # widths that are not multiples of the tile
+    dict(dtype="bf16", n=25, T=2.0),
+    dict(dtype="bf16", M=40, n=64, max_depth=5, K=5),    # a wide, deep frontier
+    dict(B=3, V=9000, M=100, n=40, T=1.0, logit_scale=0.5),
+])
+def test_build_edge_cases(dtlib, orc, kw):
+    inp = tiny(abs(hash(str(sorted(kw.items())))) % 10000, **kw)
+    run_both(dtlib, orc, inp)
+
+
+def test_build_without_biases(dtlib, orc):
+    s = synth.Shape(B=2, V=600, K=4, M=5, H=16, E=16, n=15, max_depth=4, T=0.0, dtype="bf16", name="nobias")
+    inp = synth.make_inputs(s, device="cuda", seed=5, biases=False)
+    run_both(dtlib, orc, inp)
+
+
+def test_build_deterministic(dtlib, orc):
+    inp = synth.make_inputs(2, device="cuda")
+    s = inp.shape
+    rnd = dtlib.Round(s.B, s.K, s.V, s.M, s.n, s.max_depth, s.T, dtlib.Weights.of(inp))
+    a = {k: v.clone() for k, v in rnd(inp.logits, inp.h0).items()}
+    b = rnd(inp.logits, inp.h0)
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_barrier_timeout_is_reported_and_recoverable(dtlib, orc):
+    """With a zero wait budget the first barrier wait gives up at once: the kernel records DT_ERR_TIMEOUT and
+    returns (no hang, no fault); after re-initialising the workspace the next round is correct."""
+    inp = synth.make_inputs(0, device="cuda")
+    s = inp.shape
+    rnd = dtlib.Round(s.B, s.K, s.V, s.M, s.n, s.max_depth, s.T, dtlib.Weights.of(inp))
+    try:
+        dtlib.dt_set_barrier_timeout_ns(0)
+        rnd(inp.logits, inp.h0)
+        assert dtlib.dt_get_error(rnd.workspace) == dtlib.Status.TIMEOUT
+    finally:
+        dtlib.dt_set_barrier_timeout_ns(2_000_000_000)
+    dtlib.dt_workspace_init(rnd.workspace)
+    out = rnd(inp.logits, inp.h0)
+    torch.cuda.synchronize()
+    rnd.check()
+    ora = orc.round_(inp)
+    assert np.array_equal(out["tokens"].cpu().numpy(), ora["tokens"])
+
+
+def test_rounds_reuse_one_workspace(dtlib, orc):
+    """Consecutive rounds on one workspace (top-M region then the builder's region): no state leaks between calls."""
+    s = synth.shape(2, B=8)
+    inputs = [synth.make_inputs(s, device="cuda", seed=seed) for seed in (1, 2)]
+    rnd = dtlib.Round(s.B, s.K, s.V, s.M, s.n, s.max_depth, s.T, dtlib.Weights.of(inputs[0]))
+    expect = [orc.round_(inp) for inp in inputs]
+    for i in (0, 1, 0, 1, 1, 0):
+        inp = inputs[i]
+        rnd.weights = dtlib.Weights.of(inp)
+        out = rnd(inp.logits, inp.h0)
+        torch.cuda.synchronize()
+        rnd.check()
+        assert np.array_equal(rnd.ids.cpu().numpy(), expect[i]["ids"])
+        gpu = {k: v.cpu().numpy() for k, v in out.items()}
+        h0 = synth.host_array(inp.h0).astype(np.float64)
+        resc = orc.rescore(expect[i]["ids"], expect[i]["vals"], h0, orc.weights_of(inp), gpu["tokens"],
+                           gpu["parents"], gpu["depth"], s.max_depth, s.T)
+        compare.compare_round(gpu, expect[i], resc, s.n, s.max_depth, TOL, struct_tol=STRICT)
