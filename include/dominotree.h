@@ -128,6 +128,31 @@ dt_status dt_build_trees(int B, int K, int V, int M, int n, int max_depth, float
                          int32_t* out_parents, int32_t* out_depth, float* out_scores, uint8_t* out_mask,
                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------------------------------------------
+ * dt_topm_static — dt_topm for callers that cannot allocate device memory.
+ * No counterpart in the paper: this is a deployment variant of dt_topm, with the same arguments minus the
+ * workspace and bit-identical results.
+ *
+ * Some callers cannot call cudaMalloc or receive a scratch buffer: a backend or plugin whose host framework owns all
+ * device memory and hands it only inputs and outputs, or a latency-critical path that cannot afford the implicit
+ * device synchronisation of an allocation. This entry point allocates nothing (no cudaMalloc, no cudaFree, no
+ * allocating library call): its scratch is one library-wide device array of DT_TOPM_STATIC_SCRATCH_BYTES bytes,
+ * which every GPU that loads the library holds until the process exits. The caller still passes the logits and the
+ * output arrays.
+ *   - Sizes whose scratch (dt_topm_workspace_bytes(B,K,V,M)) exceeds the array return DT_ERR_UNSUPPORTED before
+ *     any launch. For V = 151936 the array holds up to 1723 rows (B·K) at M = 64 and 862 rows at M = 128; one
+ *     request of 16 positions at M = 64 needs 156 KB of it.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress, with that device
+ *     current) and caches it; make that first call before any stream capture.
+ *   - Every call shares the array and it keeps the previous call's contents; each call clears the part that must
+ *     start at zero (a cudaMemsetAsync on `stream`). Calls that may overlap on the GPU (other streams, other host
+ *     threads) race on the array and must be serialised by the caller.
+ *   - A NaN among the logits is not reported (there is no caller-visible status word); use dt_topm to detect it.
+ * ------------------------------------------------------------------------------------------------------------- */
+#define DT_TOPM_STATIC_SCRATCH_BYTES (16u << 20)
+dt_status dt_topm_static(const void* logits, dt_dtype dtype, int B, int K, int V, int M, int32_t* out_ids,
+                         float* out_vals, cudaStream_t stream);
+
 /* Synchronises `stream`, then reads and clears the status word the device wrote into `workspace`. Returns DT_OK
  * when no device-side problem was recorded. After DT_ERR_TIMEOUT the workspace must be re-initialised. */
 dt_status dt_get_error(void* workspace, cudaStream_t stream);

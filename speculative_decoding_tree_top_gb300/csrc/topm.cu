@@ -19,6 +19,8 @@
 // words instead; slower, same result.
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "dt_internal.cuh"
 
 namespace dt {
@@ -276,6 +278,69 @@ extern "C" dt_status dt_topm(const void* logits, dt_dtype dtype, int B, int K, i
   const long long rows = static_cast<long long>(B) * K;
   if (rows > 65535) return DT_ERR_UNSUPPORTED;  // grid.y limit of one launch
   char* ws = static_cast<char*>(workspace);
+  auto* hdr = reinterpret_cast<WsHeader*>(ws);
+  auto* tickets = reinterpret_cast<unsigned*>(ws + L.tickets);
+  auto* lists = reinterpret_cast<uint64_t*>(ws + L.lists);
+  const size_t esize = dtype == DT_BF16 ? 2 : 4;
+  const bool vec_ok = (static_cast<size_t>(V) * esize) % 16 == 0;
+  const dim3 grid(static_cast<unsigned>(L.chunks), static_cast<unsigned>(rows));
+  if (dtype == DT_BF16)
+    topm_kernel<true><<<grid, kThreads, 0, stream>>>(logits, V, M, L.chunks, vec_ok, lists, tickets, out_ids,
+                                                     out_vals, hdr);
+  else
+    topm_kernel<false><<<grid, kThreads, 0, stream>>>(logits, V, M, L.chunks, vec_ok, lists, tickets, out_ids,
+                                                      out_vals, hdr);
+  return cuda_status(cudaGetLastError());
+}
+
+// ---- dt_topm_static: the same top-M with no caller workspace ----------------------------------------------------
+// For callers that cannot call cudaMalloc (see dominotree.h). Its scratch is this file-scope device array: every GPU
+// that loads the library holds it until the process exits. Host code must not pass `g_topm_scratch` itself to a
+// kernel (on the host that name is only a stand-in); the device address comes from cudaGetSymbolAddress, taken once
+// per device with that device current, on the first call made on it.
+namespace dt {
+namespace {
+__device__ __align__(256) unsigned char g_topm_scratch[DT_TOPM_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+dt_status static_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DT_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return DT_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_topm_scratch) != cudaSuccess || !p) return DT_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return DT_OK;
+}
+}  // namespace
+}  // namespace dt
+
+extern "C" dt_status dt_topm_static(const void* logits, dt_dtype dtype, int B, int K, int V, int M,
+                                    int32_t* out_ids, float* out_vals, cudaStream_t stream) {
+  using namespace dt;
+  if (B < 0 || K < 1 || V < 1 || M < 1 || M > V) return DT_ERR_INVALID_ARG;
+  if (dtype != DT_F32 && dtype != DT_BF16) return DT_ERR_INVALID_ARG;
+  if (M > DT_MAX_M) return DT_ERR_UNSUPPORTED;
+  if (B == 0) return DT_OK;
+  if (!logits || !out_ids || !out_vals) return DT_ERR_INVALID_ARG;
+  if (!aligned16(logits) || !aligned16(out_ids) || !aligned16(out_vals)) return DT_ERR_INVALID_ARG;
+  const TopmLayout L = topm_layout(B, K, V, M);
+  if (L.bytes > DT_TOPM_STATIC_SCRATCH_BYTES) return DT_ERR_UNSUPPORTED;  // beyond the fixed scratch array
+  const long long rows = static_cast<long long>(B) * K;
+  if (rows > 65535) return DT_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  const dt_status st = static_scratch(&scratch);
+  if (st != DT_OK) return st;
+  char* ws = static_cast<char*>(scratch);
+  // The array keeps the previous call's contents: the header and the per-row tickets must start at zero.
+  if (cudaMemsetAsync(ws, 0, L.lists, stream) != cudaSuccess) return DT_ERR_CUDA;
   auto* hdr = reinterpret_cast<WsHeader*>(ws);
   auto* tickets = reinterpret_cast<unsigned*>(ws + L.tickets);
   auto* lists = reinterpret_cast<uint64_t*>(ws + L.lists);

@@ -52,6 +52,7 @@ SIGNATURES = {
     "dt_build_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "dt_build_trees": (_I, [_I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _P, ctypes.POINTER(_Weights), _P, _P,
                             _P, _P, _P, _P, _SZ, _P]),
+    "dt_topm_static": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "dt_get_error": (_I, [_P, _P]),
     "dt_set_barrier_timeout_ns": (None, [ctypes.c_uint64]),
     "dt_status_string": (ctypes.c_char_p, [_I]),
@@ -149,6 +150,21 @@ def dt_topm(logits: torch.Tensor, M: int, out_ids: Optional[torch.Tensor] = None
                          _dev(out_ids, "out_ids", torch.int32, (B, K, M)),
                          _dev(out_vals, "out_vals", torch.float32, (B, K, M)),
                          _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream)), "dt_topm")
+    return out_ids, out_vals
+
+
+def dt_topm_static(logits: torch.Tensor, M: int, out_ids: Optional[torch.Tensor] = None,
+                   out_vals: Optional[torch.Tensor] = None, stream=None):
+    """dt_topm without a workspace: the library's fixed device scratch array instead (see dominotree.h)."""
+    B, K, V = logits.shape
+    if out_ids is None:
+        out_ids = torch.empty((B, K, M), dtype=torch.int32, device=logits.device)
+    if out_vals is None:
+        out_vals = torch.empty((B, K, M), dtype=torch.float32, device=logits.device)
+    _check(lib().dt_topm_static(_dev(logits, "logits"), _code(logits.dtype), B, K, V, M,
+                                _dev(out_ids, "out_ids", torch.int32, (B, K, M)),
+                                _dev(out_vals, "out_vals", torch.float32, (B, K, M)), _stream(stream)),
+           "dt_topm_static")
     return out_ids, out_vals
 
 
