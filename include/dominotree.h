@@ -45,7 +45,8 @@ extern "C" {
 
 typedef enum {
   DT_OK = 0,
-  DT_ERR_INVALID_ARG = 1, /* a null or misaligned pointer, or sizes that contradict each other         */
+  DT_ERR_INVALID_ARG = 1, /* a null or misaligned pointer, sizes that contradict each other; from the
+                             device (dt_get_error): a candidate id outside [0, V) given to dt_build_trees  */
   DT_ERR_UNSUPPORTED = 2, /* valid, but outside the envelope the kernels are built for (limits below)    */
   DT_ERR_CUDA = 3,        /* a CUDA runtime call failed (launch, attribute query)                        */
   DT_ERR_TIMEOUT = 4,     /* device: a grid-barrier wait ran out of its time budget; the kernel returned  */
@@ -140,8 +141,8 @@ dt_status dt_build_trees(int B, int K, int V, int M, int n, int max_depth, float
  * which every GPU that loads the library holds until the process exits. The caller still passes the logits and the
  * output arrays.
  *   - Sizes whose scratch (dt_topm_workspace_bytes(B,K,V,M)) exceeds the array return DT_ERR_UNSUPPORTED before
- *     any launch. For V = 151936 the array holds up to 1723 rows (B·K) at M = 64 and 862 rows at M = 128; one
- *     request of 16 positions at M = 64 needs 156 KB of it.
+ *     any launch. For V = 151936 the array holds up to 3274 rows (B·K) at M = 64 and 1637 rows at M = 128; one
+ *     request of 16 positions at M = 64 needs 83 KB of it.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress, with that device
  *     current) and caches it; make that first call before any stream capture.
  *   - Every call shares the array and it keeps the previous call's contents; each call clears the part that must

@@ -42,7 +42,7 @@ extern "C" dt_status dt_get_error(void* workspace, cudaStream_t stream) {
   if (e == cudaSuccess) e = cudaMemcpyAsync(&status, workspace, sizeof status, cudaMemcpyDeviceToHost, stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return DT_ERR_CUDA;
-  if (status != 0) {
+  if (status != 0) {  // clear the status word (the abort word stays until the workspace is re-initialised)
     e = cudaMemsetAsync(workspace, 0, sizeof status, stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return DT_ERR_CUDA;

@@ -93,6 +93,16 @@ __device__ __forceinline__ float ldw(const void* p, bool bf16, size_t i) {
 
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
 
+// Candidate ids come from the caller (normally dt_topm); one outside [0, V) is recorded as DT_ERR_INVALID_ARG and
+// replaced by 0, so that no gather ever leaves the weight arrays.
+__device__ __forceinline__ int valid_id(const Params& p, int id) {
+  if (static_cast<unsigned>(id) >= static_cast<unsigned>(p.V)) {
+    record_error(p.hdr, DT_ERR_INVALID_ARG);
+    return 0;
+  }
+  return id;
+}
+
 // ---- phase A: GRU step of every request whose last pop is expanded --------------------------------------------
 __device__ void gru_phase(const Params& p, int node, float* smem) {
   float* xs = smem;                  // [kTB][kPad]
@@ -252,7 +262,7 @@ __device__ void frontier_phase(const Params& p, int s, float* smem) {
       __syncthreads();
       const size_t pos = (static_cast<size_t>(b) * p.K + node_depth) * M;
       for (int m = warp; m < M; m += kWarps) {
-        const int id = __ldg(p.ids + pos + m);
+        const int id = valid_id(p, __ldg(p.ids + pos + m));
         const float d = warp_row_dot(p.w_c, p.bf16, id, h, H);
         if (lane == 0) z[m] = (__ldg(p.vals + pos + m) + d) / p.T_eff;
       }
@@ -276,7 +286,7 @@ __device__ void frontier_phase(const Params& p, int s, float* smem) {
       for (int m = t; m < M; m += kThreads) {
         Entry e;
         e.score = node_score + ((z[m] - mx) - lse);
-        e.token = __ldg(p.ids + pos + m);
+        e.token = valid_id(p, __ldg(p.ids + pos + m));
         e.parent = static_cast<short>(parent_idx);
         e.depth = static_cast<short>(node_depth + 1);
         e.seq = st.seq_next + m;

@@ -12,7 +12,7 @@ namespace dt {
 // again except for `status`, which holds the first device-side problem until dt_get_error clears it.
 struct WsHeader {
   unsigned status;     // dt_status of the first device-side problem, 0 if none
-  unsigned reserved0;
+  unsigned abort;      // set when a barrier wait ran out: every CTA leaves at its next barrier
   unsigned bar_count;  // grid barrier: CTAs arrived at the current barrier
   unsigned bar_gen;    // grid barrier: generation, bumped by the last CTA to arrive
   unsigned reserved[60];
@@ -43,10 +43,11 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-// Grid-wide barrier of a cooperative launch. Every wait is bounded: when the budget runs out, or when another CTA
-// has already recorded a problem, the CTA records DT_ERR_TIMEOUT (first problem wins) and the barrier returns
-// false in every thread of the CTA, which must then leave the kernel. Memory written before the barrier by any CTA
-// is visible after it (release by the arrivals and the last arrival, acquire by the waiters).
+// Grid-wide barrier of a cooperative launch. Every wait is bounded: when the budget runs out, or when another CTA's
+// wait already ran out (the header's abort word), the CTA records DT_ERR_TIMEOUT (first problem wins), raises the
+// abort word, and the barrier returns false in every thread of the CTA, which must then leave the kernel. Other
+// recorded problems do not stop the kernel. Memory written before the barrier by any CTA is visible after it
+// (release by the arrivals and the last arrival, acquire by the waiters).
 __device__ __forceinline__ bool grid_barrier(WsHeader* hdr, unsigned nblocks, uint64_t timeout_ns, int* s_flag) {
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -57,20 +58,21 @@ __device__ __forceinline__ bool grid_barrier(WsHeader* hdr, unsigned nblocks, ui
       atomicExch(&hdr->bar_count, 0u);
       st_release_gpu(&hdr->bar_gen, gen + 1u);
     } else if (timeout_ns == 0) {  // test hook: a zero budget gives up at the first wait
-      record_error(hdr, DT_ERR_TIMEOUT);
       ok = 0;
     } else {
       const uint64_t t0 = global_timer_ns();
       unsigned polls = 0;
       while (ld_acquire_gpu(&hdr->bar_gen) == gen) {
-        if ((++polls & 15u) == 0u) {
-          if (ld_acquire_gpu(&hdr->status) != 0u || global_timer_ns() - t0 > timeout_ns) {
-            record_error(hdr, DT_ERR_TIMEOUT);
-            ok = 0;
-            break;
-          }
+        if ((++polls & 15u) == 0u &&
+            (ld_acquire_gpu(&hdr->abort) != 0u || global_timer_ns() - t0 > timeout_ns)) {
+          ok = 0;
+          break;
         }
       }
+    }
+    if (!ok) {
+      record_error(hdr, DT_ERR_TIMEOUT);
+      atomicExch(&hdr->abort, 1u);
     }
     *s_flag = ok;
   }
@@ -180,15 +182,21 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 // Workspace layout of dt_topm: header | per-row tickets | per-(row, chunk) candidate lists. dt_build_trees puts its
 // own region after this one, so that one workspace can serve both calls of a round.
-constexpr int kTopmChunk = 8192;  // logits per top-M CTA
+// A top-M CTA reads one chunk of 16384 logits of a row (256 threads x 64).
+inline int topm_chunk(int B, int K) {
+  (void)B;
+  (void)K;
+  return 16384;
+}
 struct TopmLayout {
   size_t tickets, lists, bytes;
-  int chunks;
+  int chunks, chunk;
 };
 inline TopmLayout topm_layout(int B, int K, int V, int M) {
   TopmLayout L{};
   const size_t rows = static_cast<size_t>(B) * static_cast<size_t>(K);
-  L.chunks = (V + kTopmChunk - 1) / kTopmChunk;
+  L.chunk = topm_chunk(B, K);
+  L.chunks = (V + L.chunk - 1) / L.chunk;
   L.tickets = sizeof(WsHeader);
   L.lists = align_up(L.tickets + sizeof(unsigned) * rows);
   const size_t list_bytes = L.chunks > 1 ? sizeof(uint64_t) * rows * static_cast<size_t>(L.chunks) * M : 0;

@@ -122,3 +122,18 @@ def test_rounds_reuse_one_workspace(dtlib, orc):
         resc = orc.rescore(expect[i]["ids"], expect[i]["vals"], h0, orc.weights_of(inp), gpu["tokens"],
                            gpu["parents"], gpu["depth"], s.max_depth, s.T)
         compare.compare_round(gpu, expect[i], resc, s.n, s.max_depth, TOL, struct_tol=STRICT)
+
+
+def test_out_of_range_ids_are_reported_not_gathered(dtlib):
+    """Candidate ids are caller input: one outside [0, V) must come back as a device status, never as a gather
+    outside the weight arrays (the kernel range-checks every id before using it)."""
+    inp = synth.make_inputs(0, device="cuda")
+    s = inp.shape
+    ids, vals = dtlib.dt_topm(inp.logits, s.M)
+    ids[0, 0, 3] = s.V + 1000
+    ids[0, 1, 0] = -7
+    ws = dtlib.new_workspace(dtlib.dt_build_workspace_bytes(s.B, s.K, s.V, s.M, s.n, s.H, s.E))
+    out = dtlib.dt_build_trees(ids, vals, inp.h0, dtlib.Weights.of(inp), s.n, s.max_depth, s.T, workspace=ws)
+    assert dtlib.dt_get_error(ws) == dtlib.Status.INVALID_ARG
+    tok = out["tokens"].cpu().numpy()
+    assert tok.min() >= 0 and tok.max() < s.V
