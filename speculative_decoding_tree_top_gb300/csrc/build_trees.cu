@@ -20,7 +20,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
-#include "dt_internal.cuh"
+#include "build_common.cuh"
 
 namespace dt {
 namespace {
@@ -31,77 +31,6 @@ constexpr int kTB = 16;   // requests per GRU tile
 constexpr int kTU = 16;   // hidden units per GRU tile
 constexpr int kKC = 64;   // K-chunk of the GRU tile
 constexpr int kPad = kKC + 1;
-
-struct Entry {  // a frontier node; 16 bytes
-  float score;
-  int token;
-  short parent;  // index of the parent among the popped nodes, -1 for a child of the root
-  short depth;
-  int seq;       // insertion order
-};
-
-// Pop order: higher score, then lower token id, then earlier insertion.
-__device__ __forceinline__ bool before(const Entry& a, const Entry& b) {
-  if (a.score != b.score) return a.score > b.score;
-  if (a.token != b.token) return a.token < b.token;
-  return a.seq < b.seq;
-}
-
-struct NodeState {  // the node popped last by a request, as phase A of the next step needs it
-  int token;
-  int parent;
-  int depth;
-  int expand;  // 1 if the node is expanded in the next step
-  float score;
-  int seq_next;
-  int fcount;  // entries in the request's frontier
-  int pad;
-};
-
-struct Params {
-  int B, K, V, M, n, max_depth, H, E;
-  float T_eff;
-  bool bf16;
-  const int32_t* ids;
-  const float* vals;
-  const float* h0;
-  const void* emb;
-  const void* w_ih;
-  const void* w_hh;
-  const void* b_ih;
-  const void* b_hh;
-  const void* w_c;
-  int32_t* tokens;
-  int32_t* parents;
-  int32_t* depth;
-  float* scores;
-  uint8_t* mask;
-  WsHeader* hdr;
-  NodeState* state;
-  Entry* frontier;  // [B][n]
-  float* hs;        // [B][n][H]
-  uint64_t timeout_ns;
-};
-
-__device__ __forceinline__ float ldw(const void* p, bool bf16, size_t i) {
-  if (bf16) {
-    const unsigned short u = __ldg(static_cast<const unsigned short*>(p) + i);
-    return __uint_as_float(static_cast<uint32_t>(u) << 16);
-  }
-  return __ldg(static_cast<const float*>(p) + i);
-}
-
-__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
-
-// Candidate ids come from the caller (normally dt_topm); one outside [0, V) is recorded as DT_ERR_INVALID_ARG and
-// replaced by 0, so that no gather ever leaves the weight arrays.
-__device__ __forceinline__ int valid_id(const Params& p, int id) {
-  if (static_cast<unsigned>(id) >= static_cast<unsigned>(p.V)) {
-    record_error(p.hdr, DT_ERR_INVALID_ARG);
-    return 0;
-  }
-  return id;
-}
 
 // ---- phase A: GRU step of every request whose last pop is expanded --------------------------------------------
 __device__ void gru_phase(const Params& p, int node, float* smem) {
@@ -189,36 +118,6 @@ __device__ void gru_phase(const Params& p, int node, float* smem) {
       p.hs[(static_cast<size_t>(b) * p.n + node) * p.H + k] = (1.f - u) * g + u * hprev;
     }
   }
-}
-
-// One warp: w_c[row] . h (h in shared memory), lanes over 16-byte groups, fixed-order shuffle reduction.
-__device__ __forceinline__ float warp_row_dot(const void* w, bool bf16, int row, const float* h, int H) {
-  const int lane = threadIdx.x & 31;
-  float acc = 0.f;
-  if (bf16) {
-    const uint4* r = reinterpret_cast<const uint4*>(static_cast<const unsigned short*>(w) + static_cast<size_t>(row) * H);
-    for (int g = lane; g < H / 8; g += 32) {
-      const uint4 v = __ldg(r + g);
-      const uint32_t q[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        acc = fmaf(__uint_as_float(q[e] << 16), h[g * 8 + 2 * e], acc);
-        acc = fmaf(__uint_as_float(q[e] & 0xFFFF0000u), h[g * 8 + 2 * e + 1], acc);
-      }
-    }
-  } else {
-    const float4* r = reinterpret_cast<const float4*>(static_cast<const float*>(w) + static_cast<size_t>(row) * H);
-    for (int g = lane; g < H / 4; g += 32) {
-      const float4 v = __ldg(r + g);
-      acc = fmaf(v.x, h[g * 4 + 0], acc);
-      acc = fmaf(v.y, h[g * 4 + 1], acc);
-      acc = fmaf(v.z, h[g * 4 + 2], acc);
-      acc = fmaf(v.w, h[g * 4 + 3], acc);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-  return acc;
 }
 
 // ---- phase B: expand, merge, pop (one CTA per request) ----------------------------------------------------------
@@ -344,19 +243,6 @@ __global__ void __launch_bounds__(kThreads, 1) build_kernel(Params p) {
   }
 }
 
-struct BuildLayout {
-  size_t state, frontier, hs, bytes;
-};
-
-BuildLayout build_layout(int B, int K, int V, int M, int n, int H) {
-  BuildLayout L{};
-  L.state = topm_layout(B, K, V, M).bytes;  // after the top-M region: one workspace serves the whole round
-  L.frontier = align_up(L.state + sizeof(NodeState) * static_cast<size_t>(B));
-  L.hs = align_up(L.frontier + sizeof(Entry) * static_cast<size_t>(B) * n);
-  L.bytes = align_up(L.hs + sizeof(float) * static_cast<size_t>(B) * n * H);
-  return L;
-}
-
 size_t smem_bytes(int M, int n, int H) {
   const size_t a = sizeof(float) * (kTB * kPad + 3 * kTU * kPad);
   const size_t b = sizeof(float) * (H + ((M + 3) & ~3)) + 2 * sizeof(Entry) * static_cast<size_t>(n + M);
@@ -414,6 +300,7 @@ extern "C" dt_status dt_build_trees(int B, int K, int V, int M, int n, int max_d
   p.state = reinterpret_cast<NodeState*>(ws + L.state);
   p.frontier = reinterpret_cast<Entry*>(ws + L.frontier);
   p.hs = reinterpret_cast<float*>(ws + L.hs);
+  p.acc = B <= kSmallMaxB ? reinterpret_cast<long long*>(ws + L.acc) : nullptr;
   p.timeout_ns = barrier_timeout_ns();
 
   const size_t smem = smem_bytes(M, n, H);
@@ -421,6 +308,9 @@ extern "C" dt_status dt_build_trees(int B, int K, int V, int M, int n, int max_d
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+  if (e != cudaSuccess) return DT_ERR_CUDA;
+  if (!coop) return DT_ERR_UNSUPPORTED;
+  if (small_builder_fits(p, sms)) return cuda_status(launch_small_builder(p, stream));
   if (e == cudaSuccess) e = cudaFuncSetAttribute(build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  static_cast<int>(smem));
   if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, build_kernel, kThreads, smem);

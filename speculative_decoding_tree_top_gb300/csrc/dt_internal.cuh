@@ -15,7 +15,8 @@ struct WsHeader {
   unsigned abort;      // set when a barrier wait ran out: every CTA leaves at its next barrier
   unsigned bar_count;  // grid barrier: CTAs arrived at the current barrier
   unsigned bar_gen;    // grid barrier: generation, bumped by the last CTA to arrive
-  unsigned reserved[60];
+  unsigned long long sync_count;  // step barrier: arrivals ever made (monotonic, never reset)
+  unsigned reserved[58];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 
@@ -63,6 +64,50 @@ __device__ __forceinline__ bool grid_barrier(WsHeader* hdr, unsigned nblocks, ui
       const uint64_t t0 = global_timer_ns();
       unsigned polls = 0;
       while (ld_acquire_gpu(&hdr->bar_gen) == gen) {
+        if ((++polls & 15u) == 0u &&
+            (ld_acquire_gpu(&hdr->abort) != 0u || global_timer_ns() - t0 > timeout_ns)) {
+          ok = 0;
+          break;
+        }
+      }
+    }
+    if (!ok) {
+      record_error(hdr, DT_ERR_TIMEOUT);
+      atomicExch(&hdr->abort, 1u);
+    }
+    *s_flag = ok;
+  }
+  __syncthreads();
+  return *s_flag != 0;
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// One-hop grid barrier for a launch that crosses many barriers: every CTA adds 1 to a monotonic 64-bit counter
+// with a release reduction (no round trip) and waits until the counter reaches `target` = base + G * k for its k-th
+// crossing, base being the counter's value read by every CTA before the launch's first grid_barrier (no CTA can
+// arrive here before all have read it). Bounded like grid_barrier: a run-out budget or the abort word stops it.
+__device__ __forceinline__ bool counter_barrier(WsHeader* hdr, unsigned long long target, uint64_t timeout_ns,
+                                                int* s_flag) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(&hdr->sync_count) : "memory");
+    if (timeout_ns == 0) {
+      ok = 0;
+    } else {
+      const uint64_t t0 = global_timer_ns();
+      unsigned polls = 0;
+      while (ld_acquire_gpu_u64(&hdr->sync_count) < target) {
         if ((++polls & 15u) == 0u &&
             (ld_acquire_gpu(&hdr->abort) != 0u || global_timer_ns() - t0 > timeout_ns)) {
           ok = 0;
