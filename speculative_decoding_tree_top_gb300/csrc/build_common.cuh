@@ -114,7 +114,7 @@ __device__ __forceinline__ float warp_row_dot(const void* w, bool bf16, int row,
 
 // Builder region of the workspace, after the top-M region (one workspace serves the whole round): per-request
 // last-pop state, pruned frontiers [B][n], hidden states [B][n][H] fp32, and for small batches the per-step
-// fixed-point correction accumulators [n][B][M] int64.
+// fixed-point correction accumulators [n][B][M] int64 and the hidden-state publication counters [B][n].
 struct BuildLayout {
   size_t state, frontier, hs, acc, bytes;
 };
@@ -125,7 +125,10 @@ inline BuildLayout build_layout(int B, int K, int V, int M, int n, int H) {
   L.frontier = align_up(L.state + sizeof(NodeState) * static_cast<size_t>(B));
   L.hs = align_up(L.frontier + sizeof(Entry) * static_cast<size_t>(B) * n);
   L.acc = align_up(L.hs + sizeof(float) * static_cast<size_t>(B) * n * H);
-  const size_t acc_bytes = B <= kSmallMaxB ? sizeof(long long) * static_cast<size_t>(n) * B * M : 0;
+  // per-step per-candidate accumulators [n][B][M] int64, then per-node publication counters [B][n] int32
+  const size_t acc_bytes =
+      B <= kSmallMaxB ? sizeof(long long) * (static_cast<size_t>(n) * B * M + (static_cast<size_t>(B) * n + 1) / 2)
+                      : 0;
   L.bytes = align_up(L.acc + acc_bytes);
   return L;
 }

@@ -1,4 +1,4 @@
-// dt_build_trees for small batches (B <= 8): every SM works on every request, one grid barrier per step.
+// dt_build_trees for small batches (B <= 8): every SM works on every request; no grid barrier between steps.
 //
 // Method: blog.captcha.la, "Methodology — deep read" (best-first max-priority queue keyed by cumulative conditional
 // log-probability; GRU state carried along each root-to-node path; correction only on the gathered top-M rows);
@@ -9,16 +9,22 @@
 //   * weight-stationary: CTA j of the G = min(#SMs, H) CTAs owns hidden units [j*H/G, (j+1)*H/G) and keeps the
 //     3 gate rows of W_ih and W_hh of those units in shared memory for the whole launch (9.4 MB of GRU weights
 //     spread over 152 SMs: ~62 KB each at E=2560, H=512), plus the same units' columns of W_c for every candidate
-//     of every position (gathered once at launch);
-//   * per step each CTA runs its slice of the GRU for the popped node (one warp per gate row, 16-byte shared-memory
-//     reads, fp32 accumulation), then its units' share of every candidate's correction W_c[id]·h, added into a
-//     per-step accumulator as a fixed-point integer (int64, scale 2^32): integer addition is associative, so the
-//     reduction over CTAs is exact and bit-identical run to run whatever the arrival order;
-//   * one grid barrier; then every CTA redundantly finishes the step for every request: corrected logits,
-//     restricted log-softmax (one warp), merge of the children into the frontier kept in shared memory (rank by
-//     counting spread over the whole CTA, pruned to the n - s that can still be popped), pop. All CTAs reach the
-//     same pop, so no second barrier is needed to publish it; CTA 0 writes the outputs;
+//     of every position, the candidate ids and base logits (gathered once at launch);
+//   * per step each CTA runs its slice of the GRU for the popped node (K-split over 512 threads: each thread reads its
+//     slice of the input once and applies it to all gate rows; a recursive-halving shuffle reduce-scatter finishes
+//     the sums), then its units' share of every candidate's correction W_c[id]·h;
+//   * that share goes into a per-step, per-candidate 64-bit accumulator as ((fixed-point value << 8) + 1): integer
+//     addition is associative (the reduction over CTAs is exact and bit-identical run to run) and never carries into
+//     the low byte, which therefore counts the contributions. A CTA knows the correction of candidate m is complete
+//     when that count reaches G: the slot is its own barrier, so there is no grid barrier between steps;
+//   * every CTA then finishes the step for every request: corrected logits, restricted log-softmax (one warp), merge
+//     of the children into the frontier kept in shared memory (rank by counting spread over the CTA, pruned to the
+//     n - s that can still be popped), pop. All CTAs reach the same pop, so nothing needs publishing; CTA 0 writes the
+//     outputs. The embedding row of the popped token is fetched with cp.async as soon as the pop is known;
+//   * the new node's hidden state, written unit by unit by all CTAs, is published unit by unit with release
+//     reductions on a counter and pulled into every CTA's shared-memory cache with cp.async, off the critical path;
 //   * the embedding rows of all candidates are prefetched into L2 at launch.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <type_traits>
@@ -28,8 +34,10 @@
 namespace dt {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
+constexpr int kMaxRows = 16;  // gate rows per CTA handled by the K-split GEMV (3 * units <= 16)
+constexpr int kRowPad = 8;    // elements of padding per shared-memory weight row (16 bytes)
 
 struct ReqState {  // a request's frontier bookkeeping, replicated in every CTA
   int fcount;
@@ -45,7 +53,7 @@ struct ReqState {  // a request's frontier bookkeeping, replicated in every CTA
 // Shared-memory plan of one CTA (identical on host and device).
 struct Plan {
   int G, umax, R;
-  size_t wih, whh, bias, wc, x, gates, hnew, req, fr, scr, z, red, ids, vals, par, hc, bytes;
+  size_t wih, whh, bias, wc, xe, xh, req, fr, scr, z, hb, gates, red, ids, vals, par, hc, bytes;
 };
 
 __host__ __device__ inline size_t take(size_t& o, size_t bytes) {
@@ -60,17 +68,18 @@ __host__ __device__ inline Plan make_plan(int B, int M, int n, int max_depth, in
   P.umax = (H + G - 1) / G;
   P.R = 3 * P.umax;
   size_t o = 0;
-  P.wih = take(o, static_cast<size_t>(esize) * P.R * E);
-  P.whh = take(o, static_cast<size_t>(esize) * P.R * H);
+  P.wih = take(o, static_cast<size_t>(esize) * P.R * (E + kRowPad));
+  P.whh = take(o, static_cast<size_t>(esize) * P.R * (H + kRowPad));
   P.bias = take(o, sizeof(float) * 2 * P.R);
   P.wc = take(o, static_cast<size_t>(esize) * B * max_depth * M * P.umax);
-  P.x = take(o, sizeof(float) * (E + H));
-  P.gates = take(o, sizeof(float) * 2 * P.R);
-  P.hnew = take(o, sizeof(float) * B * P.umax);
+  P.xe = take(o, static_cast<size_t>(esize) * B * E);  // embedding row of each request's popped token, as stored
+  P.xh = take(o, sizeof(float) * H);                   // parent hidden state of the request being stepped
   P.req = take(o, sizeof(ReqState) * B);
   P.fr = take(o, sizeof(Entry) * B * n);
   P.scr = take(o, sizeof(Entry) * 2 * (n + M));
   P.z = take(o, sizeof(float) * M);
+  P.hb = take(o, sizeof(float) * P.umax);
+  P.gates = take(o, sizeof(float) * 2 * P.R);
   P.red = take(o, sizeof(float) * kWarps * 32);
   P.ids = take(o, sizeof(int) * B * max_depth * M);
   P.vals = take(o, sizeof(float) * B * max_depth * M);
@@ -89,64 +98,49 @@ struct WT {
   }
 };
 
-// Copies `bytes` (a multiple of 16) from global to shared memory with 16-byte loads.
-__device__ __forceinline__ void copy16(void* dst, const void* src, size_t bytes) {
-  const uint4* s = static_cast<const uint4*>(src);
-  uint4* d = static_cast<uint4*>(dst);
-#pragma unroll 8
-  for (size_t i = threadIdx.x; i < bytes / 16; i += kThreads) d[i] = __ldg(s + i);
+// Asynchronous global -> shared copy of `bytes` (a multiple of 16, both ends 16-byte aligned), L2 only.
+__device__ __forceinline__ void copy16_async(void* dst, const void* src, size_t bytes) {
+  for (size_t i = threadIdx.x; i < bytes / 16; i += kThreads) {
+    const unsigned d = static_cast<unsigned>(__cvta_generic_to_shared(static_cast<char*>(dst) + 16 * i));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(static_cast<const char*>(src) + 16 * i)
+                 : "memory");
+  }
 }
 
-// a . x over `len` elements: weights in shared memory, x (fp32) in shared memory; one warp, 16-byte weight reads.
-template <bool kBf16>
-__device__ __forceinline__ float warp_dot(const typename WT<kBf16>::T* w, const float* x, int len) {
-  const int lane = threadIdx.x & 31;
-  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;  // independent chains: the loop is latency-, not issue-bound
-  if (kBf16) {
-#pragma unroll 2
-    for (int c = lane; c < len / 8; c += 32) {
-      const uint4 q = *reinterpret_cast<const uint4*>(w + c * 8);
-      const float4 a = *reinterpret_cast<const float4*>(x + c * 8);
-      const float4 b = *reinterpret_cast<const float4*>(x + c * 8 + 4);
-      a0 = fmaf(__uint_as_float(q.x << 16), a.x, a0);
-      a1 = fmaf(__uint_as_float(q.x & 0xFFFF0000u), a.y, a1);
-      a2 = fmaf(__uint_as_float(q.y << 16), a.z, a2);
-      a3 = fmaf(__uint_as_float(q.y & 0xFFFF0000u), a.w, a3);
-      a0 = fmaf(__uint_as_float(q.z << 16), b.x, a0);
-      a1 = fmaf(__uint_as_float(q.z & 0xFFFF0000u), b.y, a1);
-      a2 = fmaf(__uint_as_float(q.w << 16), b.z, a2);
-      a3 = fmaf(__uint_as_float(q.w & 0xFFFF0000u), b.w, a3);
-    }
-  } else {
-#pragma unroll 2
-    for (int c = lane; c < len / 4; c += 32) {
-      const float4 q = *reinterpret_cast<const float4*>(w + c * 4);
-      const float4 a = *reinterpret_cast<const float4*>(x + c * 4);
-      a0 = fmaf(q.x, a.x, a0);
-      a1 = fmaf(q.y, a.y, a1);
-      a2 = fmaf(q.z, a.z, a2);
-      a3 = fmaf(q.w, a.w, a3);
+__device__ __forceinline__ long long ld_relaxed_s64(const long long* p) {
+  long long v;
+  asm volatile("ld.relaxed.gpu.global.s64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Polls until `pred(load())` holds, within the launch's time budget; false (and the abort word raised) when the
+// budget runs out or another CTA already gave up.
+template <typename Load, typename Pred>
+__device__ __forceinline__ bool poll(const Params& p, Load load, Pred pred) {
+  if (pred(load())) return true;
+  const uint64_t t0 = global_timer_ns();
+  unsigned polls = 0;
+  while (true) {
+    if (pred(load())) return true;
+    if ((++polls & 15u) == 0u &&
+        (ld_acquire_gpu(&p.hdr->abort) != 0u || global_timer_ns() - t0 > p.timeout_ns || p.timeout_ns == 0)) {
+      record_error(p.hdr, DT_ERR_TIMEOUT);
+      atomicExch(&p.hdr->abort, 1u);
+      return false;
     }
   }
-  float acc = (a0 + a1) + (a2 + a3);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-  return acc;
 }
 
-constexpr int kMaxRows = 16;  // gate rows per CTA handled by the K-split GEMV (3 * units <= 16)
-
 template <bool kBf16>
-__device__ __forceinline__ void dot8_rows(const typename WT<kBf16>::T* w, size_t row_stride, int col, int R,
-                                          const float* x8, float (&acc)[kMaxRows]) {
-  constexpr int kPer = kBf16 ? 8 : 4;
+__device__ __forceinline__ void dot_rows(const typename WT<kBf16>::T* w, size_t row_stride, int col, int R,
+                                         const float* x8, float (&acc)[kMaxRows]) {
 #pragma unroll
   for (int r = 0; r < kMaxRows; ++r) {
     if (r < R) {
       const typename WT<kBf16>::T* wr = w + static_cast<size_t>(r) * row_stride + col;
+      float a = acc[r];
       if (kBf16) {
         const uint4 q = *reinterpret_cast<const uint4*>(wr);
-        float a = acc[r];
         a = fmaf(__uint_as_float(q.x << 16), x8[0], a);
         a = fmaf(__uint_as_float(q.x & 0xFFFF0000u), x8[1], a);
         a = fmaf(__uint_as_float(q.y << 16), x8[2], a);
@@ -155,23 +149,20 @@ __device__ __forceinline__ void dot8_rows(const typename WT<kBf16>::T* w, size_t
         a = fmaf(__uint_as_float(q.z & 0xFFFF0000u), x8[5], a);
         a = fmaf(__uint_as_float(q.w << 16), x8[6], a);
         a = fmaf(__uint_as_float(q.w & 0xFFFF0000u), x8[7], a);
-        acc[r] = a;
       } else {
         const float4 q = *reinterpret_cast<const float4*>(wr);
-        float a = acc[r];
         a = fmaf(q.x, x8[0], a);
         a = fmaf(q.y, x8[1], a);
         a = fmaf(q.z, x8[2], a);
         a = fmaf(q.w, x8[3], a);
-        acc[r] = a;
       }
+      acc[r] = a;
     }
   }
-  (void)kPer;
 }
 
-// Sums 32 per-thread values over a warp by recursive halving: after the call, lane l holds the warp total of
-// value l (31 shuffles instead of 32 x 5).
+// Sums 32 per-thread values over a warp by recursive halving: afterwards lane l holds the warp total of value l
+// (31 shuffles instead of 32 x 5).
 __device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32]) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
@@ -187,35 +178,43 @@ __device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32]) {
   return v[0];
 }
 
-constexpr float kFix = 4294967296.0f;          // 2^32: fixed-point scale of the correction accumulators
+// Correction accumulators: every CTA adds (round(v * 2^32) << 8) + 1 to the slot of each candidate. The upper 56
+// bits hold the exact fixed-point sum, the low byte the number of contributions (G < 256).
+constexpr float kFix = 4294967296.0f;              // 2^32
 constexpr float kUnfix = 2.3283064365386963e-10f;  // 2^-32
+constexpr float kMaxShare = 32768.0f;              // |share| bound: 255 shares still fit in 56 bits
 
-__device__ __forceinline__ void add_fixed(const Params& p, long long* slot, float v) {
-  if (!(fabsf(v) < 2147483648.0f)) {  // also catches NaN: the accumulator would overflow
+__device__ __forceinline__ void add_share(const Params& p, long long* slot, float v) {
+  if (!(fabsf(v) < kMaxShare)) {  // also catches NaN
     record_error(p.hdr, DT_ERR_NUMERIC);
     v = 0.f;
   }
-  atomicAdd(reinterpret_cast<unsigned long long*>(slot), static_cast<unsigned long long>(__float2ll_rn(v * kFix)));
+  const unsigned long long c = (static_cast<unsigned long long>(__float2ll_rn(v * kFix)) << 8) + 1ull;
+  atomicAdd(reinterpret_cast<unsigned long long*>(slot), c);
 }
 
 template <bool kBf16>
 __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
   using T = typename WT<kBf16>::T;
   extern __shared__ __align__(16) unsigned char smem[];
-  T* wih = reinterpret_cast<T*>(smem + P.wih);      // [R][E], row g*umax + u
-  T* whh = reinterpret_cast<T*>(smem + P.whh);      // [R][H]
-  float* bias = reinterpret_cast<float*>(smem + P.bias);  // [R][2]: b_ih, b_hh
-  T* wc = reinterpret_cast<T*>(smem + P.wc);        // [B][max_depth][M][umax]
-  float* xs = reinterpret_cast<float*>(smem + P.x);        // [E + H]: emb row, then parent state
-  float* gates = reinterpret_cast<float*>(smem + P.gates);  // [R][2]: input side, hidden side
-  float* hnew = reinterpret_cast<float*>(smem + P.hnew);    // [B][umax]
+  T* wih = reinterpret_cast<T*>(smem + P.wih);               // [R][E + pad], row g*umax + u
+  T* whh = reinterpret_cast<T*>(smem + P.whh);               // [R][H + pad]
+  float* bias = reinterpret_cast<float*>(smem + P.bias);     // [R][2]: b_ih, b_hh
+  T* wc = reinterpret_cast<T*>(smem + P.wc);                 // [B][max_depth][M][umax]
+  T* xe = reinterpret_cast<T*>(smem + P.xe);                 // [B][E]
+  float* xh = reinterpret_cast<float*>(smem + P.xh);         // [H]
   ReqState* rs = reinterpret_cast<ReqState*>(smem + P.req);  // [B]
-  Entry* fr = reinterpret_cast<Entry*>(smem + P.fr);        // [B][n]
-  float* red = reinterpret_cast<float*>(smem + P.red);       // [warps][32]: GEMV reduction
+  Entry* fr = reinterpret_cast<Entry*>(smem + P.fr);         // [B][n]
+  Entry* cand = reinterpret_cast<Entry*>(smem + P.scr);      // [n + M]
+  Entry* sorted = cand + (p.n + p.M);                        // [n + M]
+  float* z = reinterpret_cast<float*>(smem + P.z);           // [M]
+  float* red = reinterpret_cast<float*>(smem + P.red);       // [warps][32]
+  float* hb = reinterpret_cast<float*>(smem + P.hb);         // [umax]: the new hidden state of the owned units
+  float* gates = reinterpret_cast<float*>(smem + P.gates);   // [R][2]: input side, hidden side
   int* ids_s = reinterpret_cast<int*>(smem + P.ids);         // [B][max_depth][M] candidate ids (range-checked)
   float* vals_s = reinterpret_cast<float*>(smem + P.vals);   // [B][max_depth][M] candidate base logits
   short* par_s = reinterpret_cast<short*>(smem + P.par);     // [B][n]: parent of every popped node
-  float* hc = reinterpret_cast<float*>(smem + P.hc);         // [B][n][H]: hidden state of every popped node
+  float* hc = reinterpret_cast<float*>(smem + P.hc);         // [B][n][H]: hidden state of every expanded node
   __shared__ int s_flag;
 
   const int B = p.B, K = p.K, M = p.M, n = p.n, H = p.H, E = p.E, maxd = p.max_depth;
@@ -224,14 +223,18 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
   const int u0 = static_cast<int>((static_cast<long long>(j) * H) / G);
   const int nu = static_cast<int>((static_cast<long long>(j + 1) * H) / G) - u0;
   const size_t esize = kBf16 ? 2 : 4;
+  int* hs_count = reinterpret_cast<int*>(p.acc + static_cast<size_t>(n) * B * M);  // [B][n]
 
-  // ---- launch: weights of the owned units, W_c columns of the candidates, L2 prefetch, zeroed accumulators ----
-  for (int g = 0; g < 3; ++g) {
-    copy16(wih + static_cast<size_t>(g * umax) * E,
-           static_cast<const char*>(p.w_ih) + (static_cast<size_t>(g) * H + u0) * E * esize, esize * nu * E);
-    copy16(whh + static_cast<size_t>(g * umax) * H,
-           static_cast<const char*>(p.w_hh) + (static_cast<size_t>(g) * H + u0) * H * esize, esize * nu * H);
+  // ---- launch: weights of the owned units, W_c columns / ids / base logits of the candidates, L2 prefetch ----
+  const int SE = E + kRowPad, SH = H + kRowPad;  // shared-memory row strides of W_ih and W_hh
+  for (int q = 0; q < 3 * nu; ++q) {
+    const int g = q / nu, u = q % nu, r = g * umax + u;
+    const size_t row = static_cast<size_t>(g) * H + u0 + u;
+    // asynchronous copies: every row in flight at once (waited for at the top of the first step)
+    copy16_async(wih + static_cast<size_t>(r) * SE, static_cast<const char*>(p.w_ih) + row * E * esize, esize * E);
+    copy16_async(whh + static_cast<size_t>(r) * SH, static_cast<const char*>(p.w_hh) + row * H * esize, esize * H);
   }
+  asm volatile("cp.async.commit_group;" ::: "memory");
   for (int i = t; i < 3 * umax; i += kThreads) {
     const int g = i / umax, u = i % umax;
     const size_t row = static_cast<size_t>(g) * H + u0 + u;
@@ -253,9 +256,9 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
     const size_t lines = (row_bytes + 127) / 128;
     const size_t total = static_cast<size_t>(B) * maxd * M * lines;
     for (size_t i = static_cast<size_t>(j) * kThreads + t; i < total; i += static_cast<size_t>(G) * kThreads) {
-      const size_t cand = i / lines, line = i % lines;
-      const int b = static_cast<int>(cand / (maxd * M)), pos = static_cast<int>((cand / M) % maxd);
-      const int m = static_cast<int>(cand % M);
+      const size_t c = i / lines, line = i % lines;
+      const int b = static_cast<int>(c / (maxd * M)), pos = static_cast<int>((c / M) % maxd);
+      const int m = static_cast<int>(c % M);
       const int id = __ldg(p.ids + (static_cast<size_t>(b) * K + pos) * M + m);
       if (static_cast<unsigned>(id) < static_cast<unsigned>(p.V)) {
         const char* a = static_cast<const char*>(p.emb) + static_cast<size_t>(id) * row_bytes + line * 128;
@@ -263,71 +266,71 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
       }
     }
   }
-  for (size_t i = static_cast<size_t>(j) * kThreads + t; i < static_cast<size_t>(n) * B * M;
-       i += static_cast<size_t>(G) * kThreads)
+  // every step's accumulators and the hidden-state counters start at zero; one grid barrier orders that
+  const size_t zero_words = static_cast<size_t>(n) * B * M + (static_cast<size_t>(B) * n + 1) / 2;
+  for (size_t i = static_cast<size_t>(j) * kThreads + t; i < zero_words; i += static_cast<size_t>(G) * kThreads)
     p.acc[i] = 0;
-  for (int b = t; b < B; b += kThreads) {
-    ReqState r{};
-    rs[b] = r;
-  }
-  __shared__ unsigned long long s_base;
-  if (t == 0) s_base = ld_relaxed_gpu_u64(&p.hdr->sync_count);  // before anyone can pass the first barrier
+  for (int b = t; b < B; b += kThreads) rs[b] = ReqState{};
   if (!grid_barrier(p.hdr, G, p.timeout_ns, &s_flag)) return;
-  const unsigned long long sync_base = s_base;
 
   for (int s = 0; s < n; ++s) {
-    asm volatile("cp.async.wait_all;" ::: "memory");  // this thread's cache copies of the previous step
+    asm volatile("cp.async.wait_all;" ::: "memory");  // this thread's cache and embedding copies
     __syncthreads();                                   // ... and everyone else's
     long long* acc_s = p.acc + static_cast<size_t>(s) * B * M;
+
     // ---- phase A: this CTA's share of the GRU and of the correction of every expanding request ----
     for (int b = 0; b < B; ++b) {
       const bool root = s == 0;
       if (!root && !rs[b].expand) continue;  // uniform across the CTA (replicated state)
       const int pos = root ? 0 : rs[b].depth;
-      float* hb = hnew + b * umax;
       if (root) {
         for (int u = t; u < nu; u += kThreads) hb[u] = __ldg(p.h0 + static_cast<size_t>(b) * H + u0 + u);
       } else {
-        const int tok = rs[b].token, par = rs[b].parent;
-        const uint4* erow = reinterpret_cast<const uint4*>(static_cast<const char*>(p.emb) +
-                                                           static_cast<size_t>(tok) * E * esize);
-        constexpr int kPer16 = kBf16 ? 8 : 4;
-#pragma unroll 4
-        for (int c = t; c < E / kPer16; c += kThreads) {  // 16-byte loads, all in flight together
-          const uint4 q = __ldg(erow + c);
-          float* d = xs + c * kPer16;
-          if (kBf16) {
-            *reinterpret_cast<float4*>(d) = make_float4(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xFFFF0000u),
-                                                        __uint_as_float(q.y << 16), __uint_as_float(q.y & 0xFFFF0000u));
-            *reinterpret_cast<float4*>(d + 4) =
-                make_float4(__uint_as_float(q.z << 16), __uint_as_float(q.z & 0xFFFF0000u),
-                            __uint_as_float(q.w << 16), __uint_as_float(q.w & 0xFFFF0000u));
-          } else {
-            *reinterpret_cast<uint4*>(d) = q;
-          }
+        const int par = rs[b].parent;
+        const float* xhp = xh;  // the parent's hidden state: the cached copy, or h0 staged for a child of the root
+        if (par < 0) {
+          for (int k = t; k < H / 4; k += kThreads)
+            reinterpret_cast<float4*>(xh)[k] =
+                __ldg(reinterpret_cast<const float4*>(p.h0 + static_cast<size_t>(b) * H) + k);
+          __syncthreads();
+        } else {
+          xhp = hc + (static_cast<size_t>(b) * n + par) * H;
         }
-        const float* hp = par < 0 ? nullptr : hc + (static_cast<size_t>(b) * n + par) * H;
-        for (int k = t; k < H / 4; k += kThreads)
-          reinterpret_cast<float4*>(xs + E)[k] =
-              par < 0 ? __ldg(reinterpret_cast<const float4*>(p.h0 + static_cast<size_t>(b) * H) + k)
-                      : reinterpret_cast<const float4*>(hp)[k];
-        __syncthreads();
-        {  // K-split GEMV: each thread reads its slice of x once and applies it to every gate row of this CTA
+        const T* xeb = xe + static_cast<size_t>(b) * E;
+        const int R = 3 * umax;
+        {
+          // K-split GEMV on the CUDA cores: each thread reads its slice of x once and applies it to every gate row;
+          // a recursive-halving shuffle reduce-scatter finishes the warp's sums. (Legacy mma.sync was measured
+          // slower here: a 12-row GEMV is latency-bound, not throughput-bound.)
           constexpr int kPer = kBf16 ? 8 : 4;
-          const int R = 3 * umax, EG = E / kPer, KG = (E + H) / kPer;
+          const int EG = E / kPer, KG = (E + H) / kPer;
           float ai[kMaxRows], ah[kMaxRows];
 #pragma unroll
           for (int r = 0; r < kMaxRows; ++r) ai[r] = ah[r] = 0.f;
           for (int f = t; f < KG; f += kThreads) {
             float x8[8];
-            const float4 a = *reinterpret_cast<const float4*>(xs + f * kPer);
-            x8[0] = a.x; x8[1] = a.y; x8[2] = a.z; x8[3] = a.w;
-            if (kBf16) {
-              const float4 b4 = *reinterpret_cast<const float4*>(xs + f * kPer + 4);
-              x8[4] = b4.x; x8[5] = b4.y; x8[6] = b4.z; x8[7] = b4.w;
+            if (f < EG) {
+              if (kBf16) {
+                const uint4 q = *reinterpret_cast<const uint4*>(xeb + f * kPer);
+                x8[0] = __uint_as_float(q.x << 16); x8[1] = __uint_as_float(q.x & 0xFFFF0000u);
+                x8[2] = __uint_as_float(q.y << 16); x8[3] = __uint_as_float(q.y & 0xFFFF0000u);
+                x8[4] = __uint_as_float(q.z << 16); x8[5] = __uint_as_float(q.z & 0xFFFF0000u);
+                x8[6] = __uint_as_float(q.w << 16); x8[7] = __uint_as_float(q.w & 0xFFFF0000u);
+              } else {
+                const float4 q = *reinterpret_cast<const float4*>(xeb + f * kPer);
+                x8[0] = q.x; x8[1] = q.y; x8[2] = q.z; x8[3] = q.w;
+              }
+              dot_rows<kBf16>(wih, SE, f * kPer, R, x8, ai);
+            } else {
+              const int c = (f - EG) * kPer;
+              const float4 a = *reinterpret_cast<const float4*>(xhp + c);
+              x8[0] = a.x; x8[1] = a.y; x8[2] = a.z; x8[3] = a.w;
+              if (kBf16) {
+                const float4 b4 = *reinterpret_cast<const float4*>(xhp + c + 4);
+                x8[4] = b4.x; x8[5] = b4.y; x8[6] = b4.z; x8[7] = b4.w;
+              }
+              dot_rows<kBf16>(whh, SH, c, R, x8, ah);
             }
-            if (f < EG) dot8_rows<kBf16>(wih, E, f * kPer, R, x8, ai);
-            else dot8_rows<kBf16>(whh, H, (f - EG) * kPer, R, x8, ah);
           }
           float v[32];
 #pragma unroll
@@ -336,91 +339,80 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
             v[kMaxRows + r] = ah[r];
           }
           red[warp * 32 + lane] = warp_reduce_scatter32(v);
-          __syncthreads();
-          if (t < 2 * R) {  // value t: input side of row t (t < kMaxRows) or hidden side of row t - kMaxRows
-            const int vi = t < R ? t : kMaxRows + (t - R);
-            float sum = 0.f;
+        }
+        __syncthreads();
+        if (t < 2 * R) {  // value t: input side of row t (t < R) or hidden side of row t - R, summed over the warps
+          const int vi = t < R ? t : kMaxRows + (t - R);
+          float q[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) sum += red[w * 32 + vi];
-            const int r = t < R ? t : t - R;
-            gates[2 * r + (t < R ? 0 : 1)] = sum;
-          }
+          for (int w = 0; w < kWarps; ++w) q[w & 3] += red[w * 32 + vi];
+          const int r = t < R ? t : t - R;
+          gates[2 * r + (t < R ? 0 : 1)] = (q[0] + q[1]) + (q[2] + q[3]);
         }
         __syncthreads();
         for (int u = t; u < nu; u += kThreads) {
           const int rr = u, rz = umax + u, rn = 2 * umax + u;
           const float r = sigmoidf_(gates[2 * rr] + bias[2 * rr] + gates[2 * rr + 1] + bias[2 * rr + 1]);
-          const float z = sigmoidf_(gates[2 * rz] + bias[2 * rz] + gates[2 * rz + 1] + bias[2 * rz + 1]);
+          const float zg = sigmoidf_(gates[2 * rz] + bias[2 * rz] + gates[2 * rz + 1] + bias[2 * rz + 1]);
           const float g = tanhf(gates[2 * rn] + bias[2 * rn] + r * (gates[2 * rn + 1] + bias[2 * rn + 1]));
-          const float h = (1.f - z) * g + z * xs[E + u0 + u];
-          hb[u] = h;
-          p.hs[(static_cast<size_t>(b) * n + (s - 1)) * H + u0 + u] = h;
+          hb[u] = (1.f - zg) * g + zg * xhp[u0 + u];
         }
       }
       __syncthreads();
+      if (!root && warp == kWarps - 1) {  // publish the new units (the last warp polls nothing in phase C)
+        for (int u = lane; u < nu; u += 32) {
+          p.hs[(static_cast<size_t>(b) * n + (s - 1)) * H + u0 + u] = hb[u];
+          // a release reduction orders the store above before the count (H units in all)
+          asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(hs_count + static_cast<size_t>(b) * n + (s - 1))
+                       : "memory");
+        }
+      }
       // this CTA's units' part of W_c[id]·h for the M candidates of position pos
       const T* wcp = wc + (static_cast<size_t>(b) * maxd + pos) * M * umax;
       for (int m = t; m < M; m += kThreads) {
         float v = 0.f;
         for (int u = 0; u < nu; ++u) v = fmaf(WT<kBf16>::f(wcp[static_cast<size_t>(m) * umax + u]), hb[u], v);
-        if (nu > 0) add_fixed(p, acc_s + static_cast<size_t>(b) * M + m, v);
+        add_share(p, acc_s + static_cast<size_t>(b) * M + m, v);
       }
-    }
-    if (!counter_barrier(p.hdr, sync_base + static_cast<unsigned long long>(G) * (s + 1), p.timeout_ns, &s_flag))
-      return;
-
-    // hidden states of the nodes expanded this step (written unit by unit by all CTAs) into this CTA's cache, as
-    // asynchronous global->shared copies that overlap phase C (waited for before the next phase A)
-    if (s > 0) {
-      for (int b = 0; b < B; ++b) {
-        if (!rs[b].expand) continue;
-        const float* src = p.hs + (static_cast<size_t>(b) * n + (s - 1)) * H;
-        float* dst = hc + (static_cast<size_t>(b) * n + (s - 1)) * H;
-        for (int k = t; k < H / 4; k += kThreads) {
-          const unsigned d = static_cast<unsigned>(__cvta_generic_to_shared(dst + 4 * k));
-          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src + 4 * k) : "memory");
-        }
-      }
-      asm volatile("cp.async.commit_group;" ::: "memory");
+      if (B > 1) __syncthreads();  // red / xh are reused by the next request
     }
 
     // ---- phase C: every CTA finishes the step for every request (the whole CTA on one request at a time) ----
-    Entry* cand = reinterpret_cast<Entry*>(smem + P.scr);  // [n + M]
-    Entry* sorted = cand + (n + M);                          // [n + M]
-    float* z = reinterpret_cast<float*>(smem + P.z);         // [M]
-    __shared__ float s_red[2];
     for (int b = 0; b < B; ++b) {
       const ReqState st = rs[b];
       const int F = st.fcount;
       const bool expanded = s == 0 || st.expand;
       const int C = expanded ? M : 0;
       const int pos = s == 0 ? 0 : st.depth;
-      const size_t off = (static_cast<size_t>(b) * maxd + pos) * M;  // into the staged ids/vals
+      const size_t off = (static_cast<size_t>(b) * maxd + pos) * M;  // into the staged ids / base logits
       for (int i = t; i < F; i += kThreads) cand[i] = fr[static_cast<size_t>(b) * n + i];
-      if (expanded) {
-        for (int m = t; m < M; m += kThreads) {
-          const long long a = __ldcg(acc_s + static_cast<size_t>(b) * M + m);
-          z[m] = (vals_s[off + m] + __ll2float_rn(a) * kUnfix) / p.T_eff;
+      int ok = 1;
+      if (expanded && warp == 0) {
+        // All G shares of every candidate: lane 0 polls a sentinel slot (every CTA issues the shares of all
+        // candidates together, so the others are then complete or nearly so), then each lane reads its slots once and
+        // re-polls only a slot still short. Light polling traffic on the lines the shares are landing in.
+        auto complete = [&](long long v) { return (v & 0xFF) == (G & 0xFF); };
+        const long long* slots = acc_s + static_cast<size_t>(b) * M;
+        if (lane == 0) ok &= poll(p, [&] { return ld_relaxed_s64(slots + (M - 1)); }, complete);
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        float mx = -INFINITY;
+        for (int m = lane; ok && m < M; m += 32) {
+          long long a = 0;
+          ok &= poll(p, [&] { return a = ld_relaxed_s64(slots + m); }, complete);
+          const float v = (vals_s[off + m] + __ll2float_rn(a >> 8) * kUnfix) / p.T_eff;
+          z[m] = v;
+          mx = fmaxf(mx, v);
         }
-        __syncthreads();
-        if (warp == 0) {  // restricted log-softmax statistics
-          float mx = -INFINITY;
-          for (int m = lane; m < M; m += 32) mx = fmaxf(mx, z[m]);
+        // restricted log-softmax of this node's children, in the warp
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-          float sum = 0.f;
-          for (int m = lane; m < M; m += 32) sum += expf(z[m] - mx);
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+        float sum = 0.f;
+        for (int m = lane; m < M; m += 32) sum += expf(z[m] - mx);
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-          if (lane == 0) {
-            s_red[0] = mx;
-            s_red[1] = logf(sum);
-          }
-        }
-        __syncthreads();
-        const float mx = s_red[0], lse = s_red[1];
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+        const float lse = logf(sum);
         const float base_score = s == 0 ? 0.f : st.score;
-        for (int m = t; m < M; m += kThreads) {
+        for (int m = lane; m < M; m += 32) {
           Entry e;
           e.score = base_score + ((z[m] - mx) - lse);
           e.token = ids_s[off + m];
@@ -430,7 +422,25 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
           cand[F + m] = e;
         }
       }
-      __syncthreads();
+      if (expanded && s > 0 && warp == kWarps - 1) {
+        // the expanded node's full hidden state (published unit by unit by every CTA) into this CTA's cache,
+        // asynchronously (waited for at the next step)
+        const int* cnt = hs_count + static_cast<size_t>(b) * n + (s - 1);
+        if (lane == 0)
+          ok &= poll(p, [&] { return static_cast<long long>(ld_acquire_gpu(reinterpret_cast<const unsigned*>(cnt))); },
+                     [&](long long v) { return v >= H; });
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        if (ok) {
+          const float* src = p.hs + (static_cast<size_t>(b) * n + (s - 1)) * H;
+          float* dst = hc + (static_cast<size_t>(b) * n + (s - 1)) * H;
+          for (int k = lane; k < H / 4; k += 32) {
+            const unsigned d = static_cast<unsigned>(__cvta_generic_to_shared(dst + 4 * k));
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src + 4 * k) : "memory");
+          }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+      }
+      if (!__syncthreads_and(ok)) return;
       // Keep the R = n - s best (nothing ranked below them can be popped in the n - s pops left). Rank by
       // counting, tpe threads per entry, each counting a stride of the others, combined with shuffles.
       const int N = F + C;
@@ -455,15 +465,18 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
       }
       __syncthreads();
       const Entry pop = sorted[0];
+      const bool will_expand = (s + 1 < n) && (pop.depth < maxd);
+      if (will_expand)  // its embedding row, for the next step's GRU
+        copy16_async(xe + static_cast<size_t>(b) * E,
+                     static_cast<const char*>(p.emb) + static_cast<size_t>(pop.token) * E * esize, esize * E);
+      asm volatile("cp.async.commit_group;" ::: "memory");
       for (int i = t + 1; i < R; i += kThreads) fr[static_cast<size_t>(b) * n + i - 1] = sorted[i];
       short* pb = par_s + static_cast<size_t>(b) * n;
-      if (t == 0) pb[s] = pop.parent;
-      __syncthreads();
       if (j == 0) {
         const size_t o = static_cast<size_t>(b) * n + s;
         uint8_t* mrow = p.mask + o * n;
         for (int c = t; c < n; c += kThreads) {  // ancestor test by walking s's parent chain (parents come first)
-          int a = s;
+          int a = c < s ? pop.parent : s;
           while (a > c) a = pb[a];
           mrow[c] = a == c;
         }
@@ -474,7 +487,8 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
           p.scores[o] = pop.score;
         }
       }
-      if (t == 0) {
+      if (t == 0) {  // read by others only after the next barrier
+        pb[s] = pop.parent;
         ReqState ns = st;
         ns.fcount = R - 1;
         ns.seq_next += C;
@@ -482,12 +496,11 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
         ns.parent = pop.parent;
         ns.depth = pop.depth;
         ns.score = pop.score;
-        ns.expand = (s + 1 < n) && (pop.depth < maxd);
+        ns.expand = will_expand;
         rs[b] = ns;
       }
-      __syncthreads();
+      if (b + 1 < B) __syncthreads();  // the next request reuses the scratch entries
     }
-    __syncthreads();
   }
 }
 
@@ -501,11 +514,12 @@ Plan plan_for(const Params& p, int sms) {
 
 bool small_builder_fits(const Params& p, int sms) {
   if (p.B > kSmallMaxB || p.B < 1 || !p.acc) return false;
-  if (3 * plan_for(p, sms).umax > kMaxRows) return false;  // more gate rows per CTA than the GEMV holds
+  const Plan P = plan_for(p, sms);
+  if (3 * P.umax > kMaxRows || P.G > 255) return false;  // GEMV rows per CTA; contribution count in one byte
   int dev = 0, optin = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return false;
-  return plan_for(p, sms).bytes <= static_cast<size_t>(optin);
+  return P.bytes <= static_cast<size_t>(optin);
 }
 
 cudaError_t launch_small_builder(const Params& p, cudaStream_t stream) {
