@@ -60,6 +60,7 @@ struct Params {
   float* hs;        // [B][n][H]
   long long* acc;   // [n][B][M] fixed-point correction accumulators (small-batch builder)
   uint64_t timeout_ns;
+  bool rows_smem;   // large-batch builder: the M gathered correction rows of a node are staged in shared memory
 };
 
 __device__ __forceinline__ float ldw(const void* p, bool bf16, size_t i) {
@@ -101,6 +102,36 @@ __device__ __forceinline__ float warp_row_dot(const void* w, bool bf16, int row,
     const float4* r = reinterpret_cast<const float4*>(static_cast<const float*>(w) + static_cast<size_t>(row) * H);
     for (int g = lane; g < H / 4; g += 32) {
       const float4 v = __ldg(r + g);
+      acc = fmaf(v.x, h[g * 4 + 0], acc);
+      acc = fmaf(v.y, h[g * 4 + 1], acc);
+      acc = fmaf(v.z, h[g * 4 + 2], acc);
+      acc = fmaf(v.w, h[g * 4 + 3], acc);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+  return acc;
+}
+
+// The same dot product with the row in shared memory (plain loads: ld.global.nc does not apply to shared memory).
+__device__ __forceinline__ float warp_row_dot_shared(const void* rows, bool bf16, int row, const float* h, int H) {
+  const int lane = threadIdx.x & 31;
+  float acc = 0.f;
+  if (bf16) {
+    const uint4* r = reinterpret_cast<const uint4*>(static_cast<const unsigned short*>(rows) + static_cast<size_t>(row) * H);
+    for (int g = lane; g < H / 8; g += 32) {
+      const uint4 v = r[g];
+      const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc = fmaf(__uint_as_float(q[e] << 16), h[g * 8 + 2 * e], acc);
+        acc = fmaf(__uint_as_float(q[e] & 0xFFFF0000u), h[g * 8 + 2 * e + 1], acc);
+      }
+    }
+  } else {
+    const float4* r = reinterpret_cast<const float4*>(static_cast<const float*>(rows) + static_cast<size_t>(row) * H);
+    for (int g = lane; g < H / 4; g += 32) {
+      const float4 v = r[g];
       acc = fmaf(v.x, h[g * 4 + 0], acc);
       acc = fmaf(v.y, h[g * 4 + 1], acc);
       acc = fmaf(v.z, h[g * 4 + 2], acc);

@@ -96,12 +96,17 @@ __device__ __forceinline__ unsigned long long ld_relaxed_gpu_u64(const unsigned 
 // with a release reduction (no round trip) and waits until the counter reaches `target` = base + G * k for its k-th
 // crossing, base being the counter's value read by every CTA before the launch's first grid_barrier (no CTA can
 // arrive here before all have read it). Bounded like grid_barrier: a run-out budget or the abort word stops it.
-__device__ __forceinline__ bool counter_barrier(WsHeader* hdr, unsigned long long target, uint64_t timeout_ns,
-                                                int* s_flag) {
-  __syncthreads();
+__device__ __forceinline__ void counter_arrive(WsHeader* hdr) {
+  __syncthreads();  // every thread of the CTA is done with the phase; thread 0 releases their writes
+  if (threadIdx.x == 0) asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(&hdr->sync_count) : "memory");
+}
+
+// Waiting half: thread 0 polls (acquire) until `target` arrivals, then the whole CTA proceeds. Between the two halves
+// a CTA may do work that reads nothing the other CTAs write in the phase (prefetches).
+__device__ __forceinline__ bool counter_wait(WsHeader* hdr, unsigned long long target, uint64_t timeout_ns,
+                                             int* s_flag) {
   if (threadIdx.x == 0) {
     int ok = 1;
-    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(&hdr->sync_count) : "memory");
     if (timeout_ns == 0) {
       ok = 0;
     } else {
@@ -123,6 +128,12 @@ __device__ __forceinline__ bool counter_barrier(WsHeader* hdr, unsigned long lon
   }
   __syncthreads();
   return *s_flag != 0;
+}
+
+__device__ __forceinline__ bool counter_barrier(WsHeader* hdr, unsigned long long target, uint64_t timeout_ns,
+                                                int* s_flag) {
+  counter_arrive(hdr);
+  return counter_wait(hdr, target, timeout_ns, s_flag);
 }
 
 // ---- order-preserving unsigned keys of logits -------------------------------------------------------------------
