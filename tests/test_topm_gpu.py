@@ -95,3 +95,32 @@ def test_topm_empty_batch(dtlib):
     x = torch.empty((0, 4, 1024), device="cuda", dtype=torch.bfloat16)
     ids, vals = dtlib.dt_topm(x, 8)
     assert ids.shape == (0, 4, 8)
+
+
+# bf16 rows whose length is a multiple of 8 logits with M <= 128 take the streaming kernel (persistent CTAs, a
+# running threshold per row segment); the cases below reach its buffer-overflow, exact-bisection, compaction and
+# split-row merge paths.
+@pytest.mark.parametrize("M", [1, 64, 128])
+def test_topm_streaming_ties_and_extremes(dtlib, orc, M):
+    V = 3 * 16384 + 80
+    x = torch.randn((1, 7, V), device="cuda") * 2
+    x[0, 0] = 0.5                                   # all ties: the first stage overflows, the exact path decides
+    x[0, 1, ::2] = -0.0
+    x[0, 1, 1::2] = 0.0
+    x[0, 2, 100] = float("inf")
+    x[0, 2, 20000] = float("-inf")
+    x[0, 3] = torch.round(x[0, 3] * 4) / 4          # heavy ties everywhere
+    x[0, 4, :] = -1.0
+    x[0, 4, 16384 * 2 + 5:] = 3.0                   # all the winners in the last stage
+    stage = torch.arange(V, device="cuda") // 16384
+    x[0, 5] = torch.randn(V, device="cuda") + 10.0 * stage   # every stage beats all earlier ones
+    x[0, 6] = torch.where(torch.arange(V, device="cuda") % 16384 < 40, 7.0, -7.0)
+    ids, _ = _check(dtlib, orc, x.to(torch.bfloat16), M)
+    assert np.array_equal(ids[0, 0].cpu().numpy(), np.arange(M))
+
+
+def test_topm_streaming_rows_split_across_ctas(dtlib, orc):
+    """160 rows of 3 stages over at most 2 CTAs per SM: segments start and end inside rows."""
+    g = torch.Generator(device="cuda").manual_seed(11)
+    x = (torch.randn((4, 40, 40000), generator=g, device="cuda") * 3).to(torch.bfloat16)
+    _check(dtlib, orc, x, 64)
