@@ -141,12 +141,12 @@ dt_status dt_build_trees(int B, int K, int V, int M, int n, int max_depth, float
  * which every GPU that loads the library holds until the process exits. The caller still passes the logits and the
  * output arrays.
  *   - Sizes whose scratch (dt_topm_workspace_bytes(B,K,V,M)) exceeds the array return DT_ERR_UNSUPPORTED before
- *     any launch. For V = 151936 the array holds up to 3274 rows (B·K) at M = 64 and 1637 rows at M = 128; one
- *     request of 16 positions at M = 64 needs 83 KB of it.
+ *     any launch. For V = 151936 the array holds up to 817 rows (B·K) at M = 64 and 409 rows at M = 128; one
+ *     request of 16 positions at M = 64 needs 321 KB of it.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress, with that device
  *     current) and caches it; make that first call before any stream capture.
- *   - Every call shares the array and it keeps the previous call's contents; each call clears the part that must
- *     start at zero (a cudaMemsetAsync on `stream`). Calls that may overlap on the GPU (other streams, other host
+ *   - Every call shares the array and it keeps the previous call's contents; each call clears its header and
+ *     per-row bounds (a cudaMemsetAsync on `stream`, 256 bytes plus 4 per row). Calls that may overlap on the GPU (other streams, other host
  *     threads) race on the array and must be serialised by the caller.
  *   - A NaN among the logits is not reported (there is no caller-visible status word); use dt_topm to detect it.
  * ------------------------------------------------------------------------------------------------------------- */

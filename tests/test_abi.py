@@ -47,8 +47,8 @@ def test_status_strings(dtlib):
 def test_workspace_sizes(dtlib):
     t = dtlib.dt_topm_workspace_bytes
     assert t(1, 4, 1024, 8) >= 256 and t(1, 4, 1024, 8) % 256 == 0
-    # one chunk per row needs no candidate lists; more chunks need [rows][chunks][M] 8-byte words
-    assert t(1, 16, 151936, 64) >= 256 + 16 * 10 * 64 * 8   # 10 chunks of 16384 logits per row
+    # per (row, chunk of 16384 logits): a candidate count and room for max(64, 4M) 8-byte candidate words
+    assert t(1, 16, 151936, 64) >= 256 + 16 * 10 * (4 + 256 * 8)   # 10 chunks of 16384 logits per row
     assert t(256, 16, 151936, 128) > t(64, 16, 151936, 64)
     b = dtlib.dt_build_workspace_bytes
     assert b(32, 16, 151936, 64, 32, 1024, 4096) >= 32 * 32 * 1024 * 4 + t(32, 16, 151936, 64)
