@@ -236,8 +236,8 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
 inline dt_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DT_OK : DT_ERR_CUDA; }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Workspace layout of dt_topm: header | per-row bound of the row's M-th largest key (zero between calls) |
-// per-(row, chunk) candidate counts | per-(row, chunk) candidate words, room for `cap` 8-byte words each. dt_build_trees puts its own region after this one, so that one workspace can serve
+// Workspace layout of dt_topm: header | per-row bound of the row's M-th largest key | per-row ticket (both zero
+// between calls) | per-(row, chunk) candidate counts | per-(row, chunk) candidate words, room for `cap` 8-byte words each. dt_build_trees puts its own region after this one, so that one workspace can serve
 // both calls of a round. A filter CTA reads one chunk of 16384 logits of a row (256 threads x 64).
 inline int topm_chunk(int B, int K) {
   (void)B;
@@ -248,7 +248,7 @@ inline int topm_chunk(int B, int K) {
 // them (M <= 256; at least 64), else exactly its top M.
 inline int topm_cap(int M) { return M <= 256 ? (4 * M < 64 ? 64 : 4 * M) : M; }
 struct TopmLayout {
-  size_t bounds, counts, words, bytes;
+  size_t bounds, tickets, counts, words, bytes;
   int chunks, chunk, cap;
 };
 inline TopmLayout topm_layout(int B, int K, int V, int M) {
@@ -258,7 +258,8 @@ inline TopmLayout topm_layout(int B, int K, int V, int M) {
   L.chunks = (V + L.chunk - 1) / L.chunk;
   L.cap = topm_cap(M);
   L.bounds = sizeof(WsHeader);
-  L.counts = align_up(L.bounds + sizeof(uint32_t) * rows);
+  L.tickets = align_up(L.bounds + sizeof(uint32_t) * rows);
+  L.counts = align_up(L.tickets + sizeof(uint32_t) * rows);
   L.words = align_up(L.counts + sizeof(int) * rows * static_cast<size_t>(L.chunks));
   L.bytes = align_up(L.words + sizeof(uint64_t) * rows * static_cast<size_t>(L.chunks) * L.cap);
   return L;

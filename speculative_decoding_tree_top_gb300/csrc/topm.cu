@@ -155,16 +155,26 @@ struct Topm {
   // Bit k of the result is set when 16-byte group k of this thread holds a logit >= the threshold value (NaN never
   // does; padding may, and is dropped by index later). Fully unrolled, the logits stay in registers; for bf16 one
   // packed compare covers two logits and the common "nothing here" group costs five instructions.
-  __device__ __forceinline__ unsigned group_mask(uint32_t thr_bits) const {
+  // With kNan (bf16), the same pass also folds the groups into a NaN-propagating maximum and sets `nan` when a NaN
+  // is present: one pass over the chunk when the bound is known in advance.
+  template <bool kNan = false>
+  __device__ __forceinline__ unsigned group_mask(uint32_t thr_bits, bool* nan = nullptr) const {
     unsigned sel = 0;
     if (kBf16) {
       const __nv_bfloat162 th = as_bf2(thr_bits | (thr_bits << 16));
+      __nv_bfloat162 mx = as_bf2(0xFF80FF80u);
 #pragma unroll
       for (int k = 0; k < kGroups; ++k) {
         const uint4 v = g_(k);
         const unsigned any = __hge2_mask(as_bf2(v.x), th) | __hge2_mask(as_bf2(v.y), th) |
                              __hge2_mask(as_bf2(v.z), th) | __hge2_mask(as_bf2(v.w), th);
         sel |= (any != 0u) << k;
+        if (kNan)
+          mx = __hmax2_nan(mx, __hmax2_nan(__hmax2_nan(as_bf2(v.x), as_bf2(v.y)), __hmax2_nan(as_bf2(v.z), as_bf2(v.w))));
+      }
+      if (kNan) {
+        const uint32_t w = as_u32(mx);
+        *nan |= is_nan_bf16(w) | is_nan_bf16(w >> 16);
       }
     } else {
       const float th = __uint_as_float(thr_bits);
@@ -280,183 +290,38 @@ constexpr int kFThreads = 256;
 constexpr int kCandMax = 1024;  // >= topm_cap(M) for every supported M
 constexpr size_t kChunkSmem = static_cast<size_t>(kFThreads) * 16 * 16;  // 64 KB: the staged chunk
 
-template <bool kBf16>
-__global__ void __launch_bounds__(kFThreads, 3)
-    topm_filter_kernel(const void* __restrict__ logits, int V, int M, int chunks, int cap, bool vec_ok,
-                       uint32_t* __restrict__ bounds, void* __restrict__ words, int* __restrict__ counts,
-                       WsHeader* hdr) {
-  using T = Topm<kBf16, kFThreads>;
-  using CWord = typename T::CWord;
-  constexpr int kWarps = kFThreads / 32;
-  constexpr int kHalf = T::kGroups / 2;  // groups per 64-bit mask word
-  constexpr uint32_t kNegInf = kBf16 ? 0xFF80u : 0xFF800000u;
-  constexpr uint32_t kMinKey = kBf16 ? 0x7Fu : 0x7FFFFFu;  // key of -inf: every real logit has a key >= it
-  extern __shared__ uint4 chunk_s[];
-  __shared__ CWord cand[kCandMax];
-  __shared__ uint32_t tmax[kFThreads];
-  __shared__ int s_warp[kWarps];
-  __shared__ uint32_t s_theta;
-  __shared__ int s_n;
-  // rows vary fastest: a row's first chunk runs (and publishes the row's bound) before its later chunks start
-  const int row = blockIdx.x, chunk = blockIdx.y, t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const long long row_off = static_cast<long long>(row) * V;
-  const int c0 = chunk * T::kChunk;
-  const int len = min(T::kChunk, V - c0);
-
-  T x{chunk_s};
-  x.stage(logits, row_off, c0, len, vec_ok);
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
-  __syncthreads();
-  bool nan = kBf16 ? false : x.any_nan_f32();
-  tmax[t] = x.max_key(nan);
-  if (t == 0) {
-    s_n = 0;
-    // Any chunk's lane-maximum bound is a lower bound of the whole row's M-th largest: a later chunk of the row
-    // takes the largest one published so far instead of computing its own.
-    s_theta = M <= kFThreads ? *reinterpret_cast<volatile uint32_t*>(bounds + row) : 0u;
-  }
-  if (__syncthreads_or(nan) && t == 0) record_error(hdr, DT_ERR_NUMERIC);
-  if (s_theta == 0u && M <= kFThreads) {  // uniform: s_theta was written before the barrier
-    __syncthreads();                      // everyone has read s_theta
-    if (warp == 0) {
-      const uint32_t th = warp_kth_key<T::kKeyBits, kFThreads>(tmax, M);
-      if (lane == 0) {
-        s_theta = th;
-        atomicMax(bounds + row, th);
-      }
-    }
-    __syncthreads();
-  }
-
-  // bit pattern of the smallest value whose key is >= key
-  auto thr_of = [&](uint32_t key) -> uint32_t {
-    if (key <= kMinKey) return kNegInf;
-    return kBf16 ? ((key & 0x8000u) ? (key & 0x7FFFu) : (~key & 0xFFFFu))
-                 : ((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
-  };
-  // Appends the elements whose bits are set in e0 (groups 0..7) and e1 (groups 8..15), kPer16 bits per group. One
-  // shared atomic per warp reserves the warp's slots; slots past cap are dropped (and show up as s_n > cap). The
-  // chunk is in shared memory, so groups are visited by run-time index (no unrolling, few registers).
-  auto append = [&](uint64_t e0, uint64_t e1) {
-    const int cnt = __popcll(e0) + __popcll(e1);
-    int incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    const int wtotal = __shfl_sync(0xFFFFFFFFu, incl, 31);
-    if (wtotal == 0) return;
-    int base = 0;
-    if (lane == 31) base = atomicAdd(&s_n, wtotal);
-    int pos = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt;
-    constexpr uint32_t kGroupBits = (1u << T::kPer16) - 1u;
-    unsigned gm = 0;  // groups that hold candidates
-#pragma unroll
-    for (int k = 0; k < T::kGroups; ++k)
-      gm |= static_cast<unsigned>(((k < kHalf ? e0 : e1) >> (T::kPer16 * (k % kHalf))) & kGroupBits ? 1u : 0u) << k;
-#pragma unroll 1
-    for (; gm; gm &= gm - 1u) {
-      const int k = __ffs(gm) - 1;
-      uint32_t m = static_cast<uint32_t>((k < kHalf ? e0 : e1) >> (T::kPer16 * (k % kHalf))) & kGroupBits;
-      const int li0 = (t + kFThreads * k) * T::kPer16;
-      for (; m; m &= m - 1u, ++pos) {
-        const int e = __ffs(m) - 1;
-        if (pos < cap) cand[pos] = T::cword(x.element_bits(k, e), li0 + e);
-      }
-    }
-  };
-  // e0 / e1 of the elements at or above (kEq: equal to) thr in the groups whose bits are set in sel.
-  auto masks = [&](unsigned sel, uint32_t thr, bool eq, uint64_t& e0, uint64_t& e1) {
-    e0 = e1 = 0;
-#pragma unroll 1
-    for (; sel; sel &= sel - 1u) {
-      const int k = __ffs(sel) - 1;
-      const uint64_t m = eq ? x.template elem_mask<true>(k, thr, len) : x.template elem_mask<false>(k, thr, len);
-      if (k < kHalf) e0 |= m << (T::kPer16 * k);
-      else e1 |= m << (T::kPer16 * (k - kHalf));
-    }
-  };
-  constexpr unsigned kAllGroups = (1u << T::kGroups) - 1u;
-
-  {
-    const uint32_t thr = thr_of(s_theta);
-    uint64_t e0, e1;
-    masks(x.group_mask(thr), thr, false, e0, e1);  // cheap "anything here" test first
-    append(e0, e1);
-  }
-  __syncthreads();
-  int n = s_n;
-  if (n > cap) {
-    // Exactly the top M. kth: the largest key with at least M elements at or above it (bisection, counts from the
-    // staged chunk); then all elements above kth and the lowest-index ties at kth, layer by layer in index order.
-    auto count_ge = [&](uint32_t key) {
-      const uint32_t thr = thr_of(key);
-      int c = 0;
-#pragma unroll 1
-      for (int k = 0; k < T::kGroups; ++k) c += __popc(x.template elem_mask<false>(k, thr, len));
-      return c;
-    };
-    uint32_t kth = 0;
-    for (int bit = T::kKeyBits - 1; bit >= 0; --bit) {
-      const uint32_t cnd = kth | (1u << bit);
-      if (block_sum<kWarps>(count_ge(cnd), s_warp) >= M) kth = cnd;
-    }
-    int need = M - block_sum<kWarps>(count_ge(kth + 1u), s_warp);  // ties at kth still to take (>= 1)
-    if (t == 0) s_n = 0;
-    __syncthreads();
-    {
-      uint64_t e0, e1;
-      masks(kAllGroups, thr_of(kth + 1u), false, e0, e1);
-      append(e0, e1);
-    }
-    const uint32_t thr_eq = thr_of(kth);
-#pragma unroll 1
-    for (int k = 0; k < T::kGroups; ++k) {  // layer k holds indices [k * kThreads * kPer16, (k + 1) * ...)
-      if (need <= 0) break;                  // uniform
-      uint32_t m = x.template elem_mask<true>(k, thr_eq, len);
-      int layer = 0;
-      const int before = block_exclusive_scan<kWarps>(__popc(m), &layer, s_warp);
-      const int take = max(0, min(__popc(m), need - before));
-      for (int i = __popc(m) - take; i > 0; --i) m &= ~(1u << (31 - __clz(m)));  // keep the `take` lowest
-      const uint64_t em = static_cast<uint64_t>(m) << (T::kPer16 * (k % kHalf));
-      append(k < kHalf ? em : 0ull, k < kHalf ? 0ull : em);
-      need -= layer;
-    }
-    __syncthreads();
-    n = s_n;
-  }
-  CWord* out = static_cast<CWord*>(words) + (static_cast<size_t>(row) * chunks + chunk) * cap;
-  for (int i = t; i < n; i += kFThreads) out[i] = cand[i];
-  if (t == 0) counts[static_cast<size_t>(row) * chunks + chunk] = n;
-}
-
-// ---- kernel 2: select ---------------------------------------------------------------------------------------------
-// One CTA per row: the row's candidates (a few hundred words) as 64-bit words (value key, inverted row index), the
-// exact M-th largest word by radix select (8-bit digits from the top, 256-bin shared histograms; stops as soon as a
-// digit's bin is taken whole), then the M words at or above it ranked by counting and written out in order.
-constexpr int kSelThreads = 256;
-constexpr int kSelCap = 4096;  // candidate words of a row kept in shared memory (more are re-read from L2)
+// ---- the row's final selection (run by the row's last filter CTA) -----------------------------------------------
+// The row's candidates (a few hundred words) as 64-bit words (value key, inverted row index), the exact M-th largest
+// word by radix select (8-bit digits from the top, 256-bin shared histograms; stops once a digit's bin is taken
+// whole, or once the key digits are fixed and the ties fit the ranking buffer), then the words at or above it
+// ranked by counting and the first M written out in order. Candidates written by other CTAs are read through L2.
+constexpr int kSelThreads = kFThreads;
+constexpr int kSelCap = 4096;                 // candidate words of a row kept in shared memory (more: re-read)
+constexpr int kMaxChunks = 4 * kSelThreads;   // chunk offsets kept in shared memory up to this many chunks
+struct SelectSmem {                           // lives in the filter's 64 KB chunk buffer
+  uint64_t w[kSelCap];
+  uint64_t top[DT_MAX_M];
+  int off[kMaxChunks + 1];
+  unsigned hist[256];
+  unsigned sel[2];
+};
+static_assert(sizeof(SelectSmem) <= kChunkSmem, "the selection fits the chunk buffer");
 
 template <bool kBf16>
-__global__ void __launch_bounds__(kSelThreads) topm_select_kernel(const void* __restrict__ words,
-                                                                  const int* __restrict__ counts, int chunks, int cap,
-                                                                  int M, uint32_t* __restrict__ bounds,
-                                                                  int32_t* __restrict__ out_ids,
-                                                                  float* __restrict__ out_vals) {
+__device__ void select_row(int row, const void* __restrict__ words, const int* __restrict__ counts, int chunks,
+                           int cap, int M, int32_t* __restrict__ out_ids, float* __restrict__ out_vals,
+                           SelectSmem& S, int* s_warp, int* s_n_ptr) {
   using T = Topm<kBf16, kFThreads>;
   using CWord = typename T::CWord;
   constexpr int kWarps = kSelThreads / 32;
   constexpr int kTopDigit = kBf16 ? 5 : 7;  // bf16 keys are 16 bits: word bits 48..63 are zero
-  constexpr int kMaxChunks = 4 * kSelThreads;  // chunk offsets kept in shared memory up to this many chunks
-  __shared__ uint64_t w[kSelCap];
-  __shared__ uint64_t top[DT_MAX_M];
-  __shared__ int s_off[kMaxChunks + 1];
-  __shared__ unsigned hist[256];
-  __shared__ unsigned sel[2];
-  __shared__ int s_warp[kWarps];
-  __shared__ int s_n;
-  const int row = blockIdx.x, t = threadIdx.x, lane = t & 31;
+  uint64_t* w = S.w;
+  uint64_t* top = S.top;
+  int* s_off = S.off;
+  unsigned* hist = S.hist;
+  unsigned* sel = S.sel;
+  int& s_n = *s_n_ptr;
+  const int t = threadIdx.x, lane = t & 31;
   const CWord* base = static_cast<const CWord*>(words) + static_cast<size_t>(row) * chunks * cap;
   const int* cnt = counts + static_cast<size_t>(row) * chunks;
   const bool few = chunks <= kMaxChunks;
@@ -466,7 +331,7 @@ __global__ void __launch_bounds__(kSelThreads) topm_select_kernel(const void* __
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int c = 4 * t + j;
-      c4[j] = c < chunks ? cnt[c] : 0;
+      c4[j] = c < chunks ? __ldcg(cnt + c) : 0;
       mine += c4[j];
     }
     int off = block_exclusive_scan<kWarps>(mine, &total, s_warp);
@@ -478,13 +343,10 @@ __global__ void __launch_bounds__(kSelThreads) topm_select_kernel(const void* __
     }
   } else {
     int mine = 0;
-    for (int c = t; c < chunks; c += kSelThreads) mine += cnt[c];
+    for (int c = t; c < chunks; c += kSelThreads) mine += __ldcg(cnt + c);
     total = block_sum<kWarps>(mine, s_warp);
   }
-  if (t == 0) {
-    s_n = 0;
-    bounds[row] = 0u;  // the row's bound served this call's filter (which has finished): zero for the next call
-  }
+  if (t == 0) s_n = 0;
   __syncthreads();
   const bool in_smem = few && total <= kSelCap;
   if (in_smem) {
@@ -495,7 +357,7 @@ __global__ void __launch_bounds__(kSelThreads) topm_select_kernel(const void* __
         if (s_off[mid] <= i) lo = mid;
         else hi = mid - 1;
       }
-      w[i] = T::global_word(base[static_cast<size_t>(lo) * cap + (i - s_off[lo])], lo * T::kChunk);
+      w[i] = T::global_word(__ldcg(base + static_cast<size_t>(lo) * cap + (i - s_off[lo])), lo * T::kChunk);
     }
   }
   __syncthreads();
@@ -504,8 +366,9 @@ __global__ void __launch_bounds__(kSelThreads) topm_select_kernel(const void* __
       for (int i = t; i < total; i += kSelThreads) f(w[i]);
     } else {
       for (int c = 0; c < chunks; ++c) {
-        const int nc = cnt[c];
-        for (int i = t; i < nc; i += kSelThreads) f(T::global_word(base[static_cast<size_t>(c) * cap + i], c * T::kChunk));
+        const int nc = __ldcg(cnt + c);
+        for (int i = t; i < nc; i += kSelThreads)
+          f(T::global_word(__ldcg(base + static_cast<size_t>(c) * cap + i), c * T::kChunk));
       }
     }
   };
@@ -569,41 +432,236 @@ __global__ void __launch_bounds__(kSelThreads) topm_select_kernel(const void* __
   emit_final<kBf16, kSelThreads>(sorted, M, out_ids + row_out, out_vals + row_out);
 }
 
+// kFuse: the row's last CTA (ticket) runs the selection itself: one launch, best for small grids; with many rows
+// the per-CTA fence and ticket cost more than a second launch (topm_select_kernel).
+template <bool kBf16, bool kFuse>
+__global__ void __launch_bounds__(kFThreads, 3)
+    topm_filter_kernel(const void* __restrict__ logits, int V, int M, int chunks, int cap, bool vec_ok,
+                       uint32_t* __restrict__ bounds, unsigned* __restrict__ tickets, void* __restrict__ words,
+                       int* __restrict__ counts, int32_t* __restrict__ out_ids, float* __restrict__ out_vals,
+                       WsHeader* hdr) {
+  using T = Topm<kBf16, kFThreads>;
+  using CWord = typename T::CWord;
+  constexpr int kWarps = kFThreads / 32;
+  constexpr int kHalf = T::kGroups / 2;  // groups per 64-bit mask word
+  constexpr uint32_t kNegInf = kBf16 ? 0xFF80u : 0xFF800000u;
+  constexpr uint32_t kMinKey = kBf16 ? 0x7Fu : 0x7FFFFFu;  // key of -inf: every real logit has a key >= it
+  extern __shared__ uint4 chunk_s[];
+  __shared__ CWord cand[kCandMax];
+  __shared__ uint32_t tmax[kFThreads];
+  __shared__ int s_warp[kWarps];
+  __shared__ uint32_t s_theta;
+  __shared__ int s_n;
+  // rows vary fastest: a row's first chunk runs (and publishes the row's bound) before its later chunks start
+  const int row = blockIdx.x, chunk = blockIdx.y, t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const long long row_off = static_cast<long long>(row) * V;
+  const int c0 = chunk * T::kChunk;
+  const int len = min(T::kChunk, V - c0);
+
+  T x{chunk_s};
+  x.stage(logits, row_off, c0, len, vec_ok);
+  // Any chunk's lane-maximum bound is a lower bound of the whole row's M-th largest: a later chunk of the row takes
+  // the largest one published so far instead of computing its own. Read while the chunk is in flight.
+  if (t == 0) {
+    s_n = 0;
+    s_theta = M <= kFThreads ? *reinterpret_cast<volatile uint32_t*>(bounds + row) : 0u;
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  __syncthreads();
+  bool nan = kBf16 ? false : x.any_nan_f32();
+  const bool known = s_theta != 0u;  // uniform: written by thread 0 before the barrier
+  if (!known) {  // this chunk computes (and publishes) the bound
+    tmax[t] = x.max_key(nan);
+    __syncthreads();  // every thread has read s_theta, tmax is complete
+    if (warp == 0) {
+      const uint32_t th = M <= kFThreads ? warp_kth_key<T::kKeyBits, kFThreads>(tmax, M) : 0u;
+      if (lane == 0) {
+        s_theta = th;
+        if (th) atomicMax(bounds + row, th);
+      }
+    }
+    __syncthreads();
+  }
+  // bit pattern of the smallest value whose key is >= key
+  auto thr_of = [&](uint32_t key) -> uint32_t {
+    if (key <= kMinKey) return kNegInf;
+    return kBf16 ? ((key & 0x8000u) ? (key & 0x7FFFu) : (~key & 0xFFFFu))
+                 : ((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+  };
+  // Appends the elements whose bits are set in e0 (groups 0..7) and e1 (groups 8..15), kPer16 bits per group. One
+  // shared atomic per warp reserves the warp's slots; slots past cap are dropped (and show up as s_n > cap). The
+  // chunk is in shared memory, so groups are visited by run-time index (no unrolling, few registers).
+  auto append = [&](uint64_t e0, uint64_t e1) {
+    const int cnt = __popcll(e0) + __popcll(e1);
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int wtotal = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    if (wtotal == 0) return;
+    int base = 0;
+    if (lane == 31) base = atomicAdd(&s_n, wtotal);
+    int pos = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt;
+    constexpr uint32_t kGroupBits = (1u << T::kPer16) - 1u;
+    unsigned gm = 0;  // groups that hold candidates
+#pragma unroll
+    for (int k = 0; k < T::kGroups; ++k)
+      gm |= static_cast<unsigned>(((k < kHalf ? e0 : e1) >> (T::kPer16 * (k % kHalf))) & kGroupBits ? 1u : 0u) << k;
+#pragma unroll 1
+    for (; gm; gm &= gm - 1u) {
+      const int k = __ffs(gm) - 1;
+      uint32_t m = static_cast<uint32_t>((k < kHalf ? e0 : e1) >> (T::kPer16 * (k % kHalf))) & kGroupBits;
+      const int li0 = (t + kFThreads * k) * T::kPer16;
+      for (; m; m &= m - 1u, ++pos) {
+        const int e = __ffs(m) - 1;
+        if (pos < cap) cand[pos] = T::cword(x.element_bits(k, e), li0 + e);
+      }
+    }
+  };
+  // e0 / e1 of the elements at or above (kEq: equal to) thr in the groups whose bits are set in sel.
+  auto masks = [&](unsigned sel, uint32_t thr, bool eq, uint64_t& e0, uint64_t& e1) {
+    e0 = e1 = 0;
+#pragma unroll 1
+    for (; sel; sel &= sel - 1u) {
+      const int k = __ffs(sel) - 1;
+      const uint64_t m = eq ? x.template elem_mask<true>(k, thr, len) : x.template elem_mask<false>(k, thr, len);
+      if (k < kHalf) e0 |= m << (T::kPer16 * k);
+      else e1 |= m << (T::kPer16 * (k - kHalf));
+    }
+  };
+  constexpr unsigned kAllGroups = (1u << T::kGroups) - 1u;
+
+  {
+    const uint32_t thr = thr_of(s_theta);
+    uint64_t e0, e1;
+    // cheap "anything here" test first; with a known bound it is the only pass and also looks for NaNs
+    const unsigned sel = known && kBf16 ? x.template group_mask<true>(thr, &nan) : x.group_mask(thr);
+    masks(sel, thr, false, e0, e1);
+    append(e0, e1);
+  }
+  if (__syncthreads_or(nan) && t == 0) record_error(hdr, DT_ERR_NUMERIC);
+  int n = s_n;
+  if (n > cap) {
+    // Exactly the top M. kth: the largest key with at least M elements at or above it (bisection, counts from the
+    // staged chunk); then all elements above kth and the lowest-index ties at kth, layer by layer in index order.
+    auto count_ge = [&](uint32_t key) {
+      const uint32_t thr = thr_of(key);
+      int c = 0;
+#pragma unroll 1
+      for (int k = 0; k < T::kGroups; ++k) c += __popc(x.template elem_mask<false>(k, thr, len));
+      return c;
+    };
+    uint32_t kth = 0;
+    for (int bit = T::kKeyBits - 1; bit >= 0; --bit) {
+      const uint32_t cnd = kth | (1u << bit);
+      if (block_sum<kWarps>(count_ge(cnd), s_warp) >= M) kth = cnd;
+    }
+    int need = M - block_sum<kWarps>(count_ge(kth + 1u), s_warp);  // ties at kth still to take (>= 1)
+    if (t == 0) s_n = 0;
+    __syncthreads();
+    {
+      uint64_t e0, e1;
+      masks(kAllGroups, thr_of(kth + 1u), false, e0, e1);
+      append(e0, e1);
+    }
+    const uint32_t thr_eq = thr_of(kth);
+#pragma unroll 1
+    for (int k = 0; k < T::kGroups; ++k) {  // layer k holds indices [k * kThreads * kPer16, (k + 1) * ...)
+      if (need <= 0) break;                  // uniform
+      uint32_t m = x.template elem_mask<true>(k, thr_eq, len);
+      int layer = 0;
+      const int before = block_exclusive_scan<kWarps>(__popc(m), &layer, s_warp);
+      const int take = max(0, min(__popc(m), need - before));
+      for (int i = __popc(m) - take; i > 0; --i) m &= ~(1u << (31 - __clz(m)));  // keep the `take` lowest
+      const uint64_t em = static_cast<uint64_t>(m) << (T::kPer16 * (k % kHalf));
+      append(k < kHalf ? em : 0ull, k < kHalf ? 0ull : em);
+      need -= layer;
+    }
+    __syncthreads();
+    n = s_n;
+  }
+  CWord* out = static_cast<CWord*>(words) + (static_cast<size_t>(row) * chunks + chunk) * cap;
+  for (int i = t; i < n; i += kFThreads) out[i] = cand[i];
+  if (t == 0) counts[static_cast<size_t>(row) * chunks + chunk] = n;
+  if (!kFuse) return;
+
+  // The last CTA of the row to finish selects the row's top M. The barrier orders every thread's writes before
+  // thread 0's fence, which publishes them at device scope before the ticket.
+  __syncthreads();
+  if (t == 0) {
+    __threadfence();
+    s_theta = atomicAdd(tickets + row, 1u) == static_cast<unsigned>(chunks - 1) ? 1u : 0u;
+  }
+  __syncthreads();
+  if (s_theta == 0u) return;
+  if (t == 0) {
+    __threadfence();
+    tickets[row] = 0u;  // both zero for the next call
+    bounds[row] = 0u;
+  }
+  select_row<kBf16>(row, words, counts, chunks, cap, M, out_ids, out_vals,
+                    *reinterpret_cast<SelectSmem*>(chunk_s), s_warp, &s_n);
+}
+
+template <bool kBf16>
+__global__ void __launch_bounds__(kSelThreads) topm_select_kernel(const void* __restrict__ words,
+                                                                  const int* __restrict__ counts, int chunks, int cap,
+                                                                  int M, uint32_t* __restrict__ bounds,
+                                                                  int32_t* __restrict__ out_ids,
+                                                                  float* __restrict__ out_vals) {
+  extern __shared__ uint4 smem_u4[];
+  __shared__ int s_warp[kSelThreads / 32];
+  __shared__ int s_n;
+  if (threadIdx.x == 0) bounds[blockIdx.x] = 0u;  // the filter launch has finished with it: zero for the next call
+  select_row<kBf16>(blockIdx.x, words, counts, chunks, cap, M, out_ids, out_vals,
+                    *reinterpret_cast<SelectSmem*>(smem_u4), s_warp, &s_n);
+}
+
 dt_status launch_topm(const void* logits, dt_dtype dtype, int B, int K, int V, int M, int32_t* out_ids,
                       float* out_vals, char* ws, const TopmLayout& L, cudaStream_t stream) {
   const long long rows = static_cast<long long>(B) * K;
   auto* hdr = reinterpret_cast<WsHeader*>(ws);
   auto* bounds = reinterpret_cast<uint32_t*>(ws + L.bounds);
+  auto* tickets = reinterpret_cast<unsigned*>(ws + L.tickets);
   auto* counts = reinterpret_cast<int*>(ws + L.counts);
   void* words = ws + L.words;
   const size_t esize = dtype == DT_BF16 ? 2 : 4;
   const bool vec_ok = (static_cast<size_t>(V) * esize) % 16 == 0;
-  // the staged chunk is above the default 48 KB of dynamic shared memory: allowed once per process and device
-  static std::once_flag attr[2];
-  std::call_once(attr[0], [] {
-    cudaFuncSetAttribute(topm_filter_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(kChunkSmem));
+  // the staged chunk (and the selection's buffers) exceed the default 48 KB of dynamic shared memory: raised once
+  static std::once_flag attr;
+  std::call_once(attr, [] {
+    const int bytes = static_cast<int>(kChunkSmem), sel = static_cast<int>(sizeof(SelectSmem));
+    cudaFuncSetAttribute(topm_filter_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    cudaFuncSetAttribute(topm_filter_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    cudaFuncSetAttribute(topm_filter_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    cudaFuncSetAttribute(topm_filter_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    cudaFuncSetAttribute(topm_select_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, sel);
+    cudaFuncSetAttribute(topm_select_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, sel);
   });
-  std::call_once(attr[1], [] {
-    cudaFuncSetAttribute(topm_filter_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(kChunkSmem));
-  });
-  if (dtype == DT_BF16) {
-    constexpr int kChunk = Topm<true, kFThreads>::kChunk;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return DT_ERR_CUDA;
+  auto run = [&](auto bf16_tag) {
+    constexpr bool kB = decltype(bf16_tag)::value;
+    constexpr int kChunk = Topm<kB, kFThreads>::kChunk;
     const int chunks = (V + kChunk - 1) / kChunk;  // <= L.chunks: the layout is sized for the smaller fp32 chunk
-    topm_filter_kernel<true><<<dim3(static_cast<unsigned>(rows), chunks), kFThreads, kChunkSmem, stream>>>(
-        logits, V, M, chunks, L.cap, vec_ok, bounds, words, counts, hdr);
-    topm_select_kernel<true><<<static_cast<unsigned>(rows), kSelThreads, 0, stream>>>(words, counts, chunks, L.cap,
-                                                                                      M, bounds, out_ids, out_vals);
-  } else {
-    constexpr int kChunk = Topm<false, kFThreads>::kChunk;
-    const int chunks = (V + kChunk - 1) / kChunk;
-    topm_filter_kernel<false><<<dim3(static_cast<unsigned>(rows), chunks), kFThreads, kChunkSmem, stream>>>(
-        logits, V, M, chunks, L.cap, vec_ok, bounds, words, counts, hdr);
-    topm_select_kernel<false><<<static_cast<unsigned>(rows), kSelThreads, 0, stream>>>(words, counts, chunks,
-                                                                                       L.cap, M, bounds, out_ids,
-                                                                                       out_vals);
-  }
+    const dim3 grid(static_cast<unsigned>(rows), static_cast<unsigned>(chunks));
+    // about two waves of three CTAs per SM or fewer: fuse the selection into the launch
+    const bool fuse = rows * chunks <= 6LL * sms;
+    if (fuse) {
+      topm_filter_kernel<kB, true><<<grid, kFThreads, kChunkSmem, stream>>>(
+          logits, V, M, chunks, L.cap, vec_ok, bounds, tickets, words, counts, out_ids, out_vals, hdr);
+    } else {
+      topm_filter_kernel<kB, false><<<grid, kFThreads, kChunkSmem, stream>>>(
+          logits, V, M, chunks, L.cap, vec_ok, bounds, tickets, words, counts, out_ids, out_vals, hdr);
+      topm_select_kernel<kB><<<static_cast<unsigned>(rows), kSelThreads, sizeof(SelectSmem), stream>>>(
+          words, counts, chunks, L.cap, M, bounds, out_ids, out_vals);
+    }
+  };
+  if (dtype == DT_BF16) run(std::true_type{});
+  else run(std::false_type{});
   return cuda_status(cudaGetLastError());
 }
 
