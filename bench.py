@@ -119,29 +119,43 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def source_sha(name: str) -> str:
-    path = os.path.join(ROOT, "speculative_decoding_tree_top_gb300", "csrc", name)
+# The sources each C-ABI call is built from: a committed ncu figure counts only while they are unchanged.
+CALL_SOURCES = {
+    "dt_topm": ["topm.cu", "dt_internal.cuh"],
+    "dt_build_trees": ["build_trees.cu", "build_small.cu", "build_common.cuh", "dt_internal.cuh"],
+}
+
+
+def source_sha(call: str) -> str:
     h = hashlib.sha256()
-    for p in (path, os.path.join(ROOT, "speculative_decoding_tree_top_gb300", "csrc", "dt_internal.cuh")):
-        with open(p, "rb") as f:
+    for name in CALL_SOURCES[call]:
+        with open(os.path.join(ROOT, "speculative_decoding_tree_top_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str, source: str, workload: str):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current source of the kernel."""
+def ncu_traffic(call: str, workload: str):
+    """DRAM bytes per call from a committed ncu summary, if it was taken on the current sources of the call."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    e = d.get(kernel, {}).get(workload)
-    if not e or e.get("source_sha") != source_sha(source):
+    e = d.get(call, {}).get(workload)
+    if not e or e.get("source_sha") != source_sha(call):
         return None
-    return e.get("dram_bytes_per_launch")
+    return e.get("dram_bytes_per_call")
 
 
 # ---------------------------------------------------------------------------------------------------------------
+def topm_launches(shape, sms: int) -> int:
+    """Kernels one dt_topm call launches: the filter, plus a selection launch unless the grid is about two waves or
+    fewer (then the filter's last CTA of each row selects)."""
+    chunk = 16384 if shape.dtype == "f32" else 32768
+    chunks = -(-shape.V // chunk)
+    return 1 if shape.B * shape.K * chunks <= 6 * sms else 2
+
+
 def algorithmic_bytes(shape, tokens, parents, depth):
     """Bytes a launch must move at least once (HBM roofline numerators), from the trees actually built.
 
@@ -233,13 +247,13 @@ def run_ours(args, world, rank, local):
     peak, peak_src = measured_peaks()
     kernels = {
         "dt_topm": dict(us=float(topm_ms.mean() * 1e3), bytes=topm_b, gbps=topm_b / (topm_ms.mean() * 1e6),
-                        source="topm.cu"),
+                        sources=CALL_SOURCES["dt_topm"]),
         "dt_build_trees": dict(us=float(build_ms.mean() * 1e3), bytes=build_b,
-                               gbps=build_b / (build_ms.mean() * 1e6), source="build_trees.cu"),
+                               gbps=build_b / (build_ms.mean() * 1e6), sources=CALL_SOURCES["dt_build_trees"]),
     }
     dom = max(kernels, key=lambda k: kernels[k]["us"])
     kd = kernels[dom]
-    traffic = ncu_traffic(dom, kd["source"], s.name)
+    traffic = ncu_traffic(dom, s.name)
     roofline = {"kernel": dom, "bound": "hbm", "achieved": round(kd["gbps"], 1), "peak": peak, "unit": "GB/s",
                 "frac": round(kd["gbps"] / peak, 4), "traffic": traffic, "peak_source": peak_src,
                 "algorithmic_bytes_per_launch": kd["bytes"], "bytes_breakdown": parts if dom == "dt_build_trees"
@@ -293,7 +307,7 @@ def run_ours(args, world, rank, local):
                    "l2": "flushed between steps (256 MB memset outside the timed events)"},
         "kernels": {k: {kk: (round(vv, 3) if isinstance(vv, float) else vv) for kk, vv in d.items()}
                     for k, d in kernels.items()},
-        "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": 2 * args.steps,
+        "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": (topm_launches(s, torch.cuda.get_device_properties(dev).multi_processor_count) + 1) * args.steps,
         "clocks": clocks.summary(), "wall_s_timed_loop": round(t_wall, 4),
     }
 
