@@ -83,64 +83,64 @@ __device__ __forceinline__ int valid_id(const Params& p, int id) {
   return id;
 }
 
-// One warp: w_c[row] . h (h in shared memory), lanes over 16-byte groups, fixed-order shuffle reduction.
-__device__ __forceinline__ float warp_row_dot(const void* w, bool bf16, int row, const float* h, int H) {
+// One warp: the dot products of 8 consecutive rows m0 .. m0 + 7 (those < M) with h, for the rows of a gathered slice
+// in shared memory (`rows`, [M][H]) or, when rows == nullptr, the correction rows w[ids[m]] in global memory. The
+// lane's share of h is loaded once and used for all 8 rows, whose sums are 8 independent chains (same per-lane order
+// and shuffle tree as one row at a time, so the results are identical). out[j] is valid in every lane.
+__device__ __forceinline__ void warp_dot_rows8(const void* rows, const void* w, const int* ids, bool bf16, int m0,
+                                               int M, const float* h, int H, float (&out)[8]) {
   const int lane = threadIdx.x & 31;
-  float acc = 0.f;
-  if (bf16) {
-    const uint4* r = reinterpret_cast<const uint4*>(static_cast<const unsigned short*>(w) + static_cast<size_t>(row) * H);
-    for (int g = lane; g < H / 8; g += 32) {
-      const uint4 v = __ldg(r + g);
-      const uint32_t q[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        acc = fmaf(__uint_as_float(q[e] << 16), h[g * 8 + 2 * e], acc);
-        acc = fmaf(__uint_as_float(q[e] & 0xFFFF0000u), h[g * 8 + 2 * e + 1], acc);
+  for (int j = 0; j < 8; ++j) out[j] = 0.f;
+  if (bf16) {
+    const int G = H / 8;  // 16-byte groups per row
+    for (int g = lane; g < G; g += 32) {
+      const float4 ha = *reinterpret_cast<const float4*>(h + g * 8), hb = *reinterpret_cast<const float4*>(h + g * 8 + 4);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int m = m0 + j;
+        if (m >= M) break;
+        const uint4 v = rows ? reinterpret_cast<const uint4*>(static_cast<const unsigned short*>(rows) +
+                                                              static_cast<size_t>(m) * H)[g]
+                             : __ldg(reinterpret_cast<const uint4*>(static_cast<const unsigned short*>(w) +
+                                                                    static_cast<size_t>(ids[m]) * H) + g);
+        float a = out[j];
+        a = fmaf(__uint_as_float(v.x << 16), ha.x, a);
+        a = fmaf(__uint_as_float(v.x & 0xFFFF0000u), ha.y, a);
+        a = fmaf(__uint_as_float(v.y << 16), ha.z, a);
+        a = fmaf(__uint_as_float(v.y & 0xFFFF0000u), ha.w, a);
+        a = fmaf(__uint_as_float(v.z << 16), hb.x, a);
+        a = fmaf(__uint_as_float(v.z & 0xFFFF0000u), hb.y, a);
+        a = fmaf(__uint_as_float(v.w << 16), hb.z, a);
+        a = fmaf(__uint_as_float(v.w & 0xFFFF0000u), hb.w, a);
+        out[j] = a;
       }
     }
   } else {
-    const float4* r = reinterpret_cast<const float4*>(static_cast<const float*>(w) + static_cast<size_t>(row) * H);
-    for (int g = lane; g < H / 4; g += 32) {
-      const float4 v = __ldg(r + g);
-      acc = fmaf(v.x, h[g * 4 + 0], acc);
-      acc = fmaf(v.y, h[g * 4 + 1], acc);
-      acc = fmaf(v.z, h[g * 4 + 2], acc);
-      acc = fmaf(v.w, h[g * 4 + 3], acc);
-    }
-  }
+    const int G = H / 4;
+    for (int g = lane; g < G; g += 32) {
+      const float4 hv = *reinterpret_cast<const float4*>(h + g * 4);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-  return acc;
-}
-
-// The same dot product with the row in shared memory (plain loads: ld.global.nc does not apply to shared memory).
-__device__ __forceinline__ float warp_row_dot_shared(const void* rows, bool bf16, int row, const float* h, int H) {
-  const int lane = threadIdx.x & 31;
-  float acc = 0.f;
-  if (bf16) {
-    const uint4* r = reinterpret_cast<const uint4*>(static_cast<const unsigned short*>(rows) + static_cast<size_t>(row) * H);
-    for (int g = lane; g < H / 8; g += 32) {
-      const uint4 v = r[g];
-      const uint32_t q[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        acc = fmaf(__uint_as_float(q[e] << 16), h[g * 8 + 2 * e], acc);
-        acc = fmaf(__uint_as_float(q[e] & 0xFFFF0000u), h[g * 8 + 2 * e + 1], acc);
+      for (int j = 0; j < 8; ++j) {
+        const int m = m0 + j;
+        if (m >= M) break;
+        const float4 v = rows ? reinterpret_cast<const float4*>(static_cast<const float*>(rows) +
+                                                                static_cast<size_t>(m) * H)[g]
+                              : __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(w) +
+                                                                      static_cast<size_t>(ids[m]) * H) + g);
+        float a = out[j];
+        a = fmaf(v.x, hv.x, a);
+        a = fmaf(v.y, hv.y, a);
+        a = fmaf(v.z, hv.z, a);
+        a = fmaf(v.w, hv.w, a);
+        out[j] = a;
       }
     }
-  } else {
-    const float4* r = reinterpret_cast<const float4*>(static_cast<const float*>(rows) + static_cast<size_t>(row) * H);
-    for (int g = lane; g < H / 4; g += 32) {
-      const float4 v = r[g];
-      acc = fmaf(v.x, h[g * 4 + 0], acc);
-      acc = fmaf(v.y, h[g * 4 + 1], acc);
-      acc = fmaf(v.z, h[g * 4 + 2], acc);
-      acc = fmaf(v.w, h[g * 4 + 3], acc);
-    }
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-  return acc;
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) out[j] += __shfl_xor_sync(0xFFFFFFFFu, out[j], o);
 }
 
 // Builder region of the workspace, after the top-M region (one workspace serves the whole round): per-request

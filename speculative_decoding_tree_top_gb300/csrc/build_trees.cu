@@ -163,10 +163,11 @@ __device__ __forceinline__ void prefetch_l2(const void* src, unsigned bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
-template <int kRT, int kUT>
+template <int kRT, int kUT, int kKcT, int kStagesT>
 struct GemmTile {
   static constexpr int kCols = 4 * kUT;   // r | z | n_in | n_h, kUT units each
-  static constexpr int kKc = 128;         // K columns per pipeline stage: one k16 step per warp
+  static constexpr int kKc = kKcT;        // K columns per pipeline stage
+  static constexpr int kSteps = kKc / 16 / kWarps;  // k16 steps of each warp in every chunk
   static constexpr int kXS = kKc + 8;     // shared row stride of a bf16 chunk (elements): conflict-free fragments
   static constexpr int kHS = kKc + 8;     // shared row stride of an fp32 chunk (elements): conflict-free per half-warp
   static constexpr int kMT = kRT / 16;    // m16 tiles
@@ -175,19 +176,28 @@ struct GemmTile {
   static constexpr int kXBytes = kRT * kHS * 4;  // the fp32 hidden-side chunk is the larger of the two inputs
   static constexpr int kWBytes = kCols * kXS * 2;
   static constexpr int kStage = kXBytes + kWBytes;
-  static constexpr int kStages = kRT == 32 ? 7 : 4;
+  static constexpr int kStages = kStagesT;
   static constexpr int kRS = kCols + 8;   // row stride of a warp's partial tile (floats): conflict-free float2 stores
   static constexpr int kRedBytes = kWarps * kRT * kRS * 4;
   static constexpr int kRing = kStages * kStage > kRedBytes ? kStages * kStage : kRedBytes;
   static constexpr int kInfo = kRT * 4 * 4;  // token, parent, expand per request (+ pad)
   static constexpr size_t kBytes = static_cast<size_t>(kRing) + kInfo;
   static_assert(kUT % 8 == 0 && kRT % 16 == 0, "whole mma tiles");
-  static_assert(kKc / 16 == kWarps, "one k16 step per warp per chunk");
+  static_assert(kSteps >= 1 && kSteps * 16 * kWarps == kKc, "whole k16 steps per warp per chunk");
+
 };
 
-template <int kRT, int kUT>
+// Tile shapes: 32 requests x 8 units with K chunks of 256 (B < 128; chunks of 128 through a deeper ring when the
+// widths are not multiples of 256), 64 x 16 with chunks of 128 (B >= 128).
+using TileS = GemmTile<32, 8, 256, 4>;
+using TileS128 = GemmTile<32, 8, 128, 7>;
+using TileL = GemmTile<64, 16, 128, 4>;
+
+// Operand chunks of kKc columns stream from L2 through a ring of kStages shared-memory stages filled by 16-byte
+// cp.async (one cp.async group per chunk). (Bulk copies of the 256- to 1024-byte row pieces measured 2x slower here:
+// each chunk is ~56 small copies.)
+template <typename GT, int kRT, int kUT>
 __device__ void gemm_gru_phase(const Params& p, int node, unsigned char* smem) {
-  using GT = GemmTile<kRT, kUT>;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int g = lane >> 2, tig = lane & 3;
   const int E = p.E, H = p.H, B = p.B, n = p.n;
@@ -220,9 +230,8 @@ __device__ void gemm_gru_phase(const Params& p, int node, unsigned char* smem) {
         const int row = i / (GT::kKc / 8), piece = i % (GT::kKc / 8);
         const int gate = row / kUT, uu = row % kUT, u = u0 + uu;
         const int set = (gate == 2 && !in) ? 3 : gate;
-        if (u < H)
-          cp_async16(wdst + (set * kUT + uu) * GT::kXS + piece * 8,
-                     wsrc + (static_cast<size_t>(gate) * H + u) * K + k0 + piece * 8);
+        cp_async16(wdst + (set * kUT + uu) * GT::kXS + piece * 8,
+                   wsrc + (static_cast<size_t>(gate) * H + u) * K + k0 + piece * 8);
       }
       if (in) {  // the requests' embedding rows, bf16
         unsigned short* xdst = reinterpret_cast<unsigned short*>(st);
@@ -260,7 +269,6 @@ __device__ void gemm_gru_phase(const Params& p, int node, unsigned char* smem) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[a][b][q] = 0.f;
 
-    const int k = warp * 16 + tig * 2;  // this warp's k16 step inside every chunk
     for (int c = 0; c < GT::kStages - 1; ++c) issue_or_empty(c);
     for (int c = 0; c < nc; ++c) {
       asm volatile("cp.async.wait_group %0;" ::"n"(GT::kStages - 2) : "memory");  // chunk c has landed
@@ -269,49 +277,54 @@ __device__ void gemm_gru_phase(const Params& p, int node, unsigned char* smem) {
       const bool in = c < nin;
       const unsigned char* st = smem + (c % GT::kStages) * GT::kStage;
       const unsigned short* wsm = reinterpret_cast<const unsigned short*>(st + GT::kXBytes);
-      // column sets: r, z on both sides; n_in (set 2) only on the input side, n_h (set 3) only on the hidden side
-      uint32_t bfr[GT::kNT][2];
 #pragma unroll
-      for (int nt = 0; nt < GT::kNT; ++nt) {
-        const int col = nt * 8 + g;
-        bfr[nt][0] = lds32(wsm + col * GT::kXS + k);
-        bfr[nt][1] = lds32(wsm + col * GT::kXS + k + 8);
-      }
-      if (in) {
-        const unsigned short* xsm = reinterpret_cast<const unsigned short*>(st);
+      for (int j = 0; j < GT::kSteps; ++j) {
+        const int k = (j * kWarps + warp) * 16 + tig * 2;  // this warp's j-th k16 step inside the chunk
+        // column sets: r, z on both sides; n_in (set 2) only on the input side, n_h (set 3) only on the hidden side
+        uint32_t bfr[GT::kNT][2];
 #pragma unroll
-        for (int mt = 0; mt < GT::kMT; ++mt) {
-          const int r0 = mt * 16 + g;
-          const uint32_t a0 = lds32(xsm + r0 * GT::kXS + k), a1 = lds32(xsm + (r0 + 8) * GT::kXS + k);
-          const uint32_t a2 = lds32(xsm + r0 * GT::kXS + k + 8), a3 = lds32(xsm + (r0 + 8) * GT::kXS + k + 8);
-#pragma unroll
-          for (int nt = 0; nt < 3 * GT::kNS; ++nt) mma_bf16_16816(acc[mt][nt], a0, a1, a2, a3, bfr[nt][0], bfr[nt][1]);
+        for (int nt = 0; nt < GT::kNT; ++nt) {
+          const int col = nt * 8 + g;
+          bfr[nt][0] = lds32(wsm + col * GT::kXS + k);
+          bfr[nt][1] = lds32(wsm + col * GT::kXS + k + 8);
         }
-      } else {
-        const float* xsm = reinterpret_cast<const float*>(st);
+        if (in) {
+          const unsigned short* xsm = reinterpret_cast<const unsigned short*>(st);
 #pragma unroll
-        for (int mt = 0; mt < GT::kMT; ++mt) {
-          const int r0 = mt * 16 + g;
-          const float2 p0 = *reinterpret_cast<const float2*>(xsm + r0 * GT::kHS + k);
-          const float2 p1 = *reinterpret_cast<const float2*>(xsm + (r0 + 8) * GT::kHS + k);
-          const float2 p2 = *reinterpret_cast<const float2*>(xsm + r0 * GT::kHS + k + 8);
-          const float2 p3 = *reinterpret_cast<const float2*>(xsm + (r0 + 8) * GT::kHS + k + 8);
-          uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
-          split_bf16x2(p0.x, p0.y, h0, l0);
-          split_bf16x2(p1.x, p1.y, h1, l1);
-          split_bf16x2(p2.x, p2.y, h2, l2);
-          split_bf16x2(p3.x, p3.y, h3, l3);
+          for (int mt = 0; mt < GT::kMT; ++mt) {
+            const int r0 = mt * 16 + g;
+            const uint32_t a0 = lds32(xsm + r0 * GT::kXS + k), a1 = lds32(xsm + (r0 + 8) * GT::kXS + k);
+            const uint32_t a2 = lds32(xsm + r0 * GT::kXS + k + 8), a3 = lds32(xsm + (r0 + 8) * GT::kXS + k + 8);
 #pragma unroll
-          for (int nt = 0; nt < GT::kNT; ++nt) {
-            if (nt / GT::kNS == 2) continue;  // n_in has no hidden side
-            mma_bf16_16816(acc[mt][nt], h0, h1, h2, h3, bfr[nt][0], bfr[nt][1]);
-            mma_bf16_16816(acc[mt][nt], l0, l1, l2, l3, bfr[nt][0], bfr[nt][1]);
+            for (int nt = 0; nt < 3 * GT::kNS; ++nt)
+              mma_bf16_16816(acc[mt][nt], a0, a1, a2, a3, bfr[nt][0], bfr[nt][1]);
+          }
+        } else {
+          const float* xsm = reinterpret_cast<const float*>(st);
+#pragma unroll
+          for (int mt = 0; mt < GT::kMT; ++mt) {
+            const int r0 = mt * 16 + g;
+            const float2 p0 = *reinterpret_cast<const float2*>(xsm + r0 * GT::kHS + k);
+            const float2 p1 = *reinterpret_cast<const float2*>(xsm + (r0 + 8) * GT::kHS + k);
+            const float2 p2 = *reinterpret_cast<const float2*>(xsm + r0 * GT::kHS + k + 8);
+            const float2 p3 = *reinterpret_cast<const float2*>(xsm + (r0 + 8) * GT::kHS + k + 8);
+            uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
+            split_bf16x2(p0.x, p0.y, h0, l0);
+            split_bf16x2(p1.x, p1.y, h1, l1);
+            split_bf16x2(p2.x, p2.y, h2, l2);
+            split_bf16x2(p3.x, p3.y, h3, l3);
+#pragma unroll
+            for (int nt = 0; nt < GT::kNT; ++nt) {
+              if (nt / GT::kNS == 2) continue;  // n_in has no hidden side
+              mma_bf16_16816(acc[mt][nt], h0, h1, h2, h3, bfr[nt][0], bfr[nt][1]);
+              mma_bf16_16816(acc[mt][nt], l0, l1, l2, l3, bfr[nt][0], bfr[nt][1]);
+            }
           }
         }
       }
     }
     cp_async_wait_all();
-    __syncthreads();  // the ring is free: it now holds the warps' partial tiles
+    __syncthreads();  // the ring is free (every chunk consumed): it now holds the warps' partial tiles
     // partial tile of this warp -> red[warp]: thread holds rows g, g + 8 and columns tig*2, tig*2 + 1 of each tile
 #pragma unroll
     for (int mt = 0; mt < GT::kMT; ++mt)
@@ -436,10 +449,12 @@ __device__ void frontier_phase(const Params& p, int s, unsigned char* smem, Owne
         cp_async_wait_all();
         __syncthreads();
       }
-      for (int m = warp; m < M; m += kWarps) {
-        const float d = rows_in_smem ? warp_row_dot_shared(rows, p.bf16, m, h, H)
-                                     : warp_row_dot(p.w_c, p.bf16, ids[m], h, H);
-        if (lane == 0) z[m] = (vals[m] + d) / p.T_eff;
+      for (int m0 = warp * 8; m0 < M; m0 += kWarps * 8) {  // each warp: 8 consecutive rows at a time
+        float d[8];
+        warp_dot_rows8(rows_in_smem ? rows : nullptr, p.w_c, ids, p.bf16, m0, M, h, H, d);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (lane == j && m0 + j < M) z[m0 + j] = (vals[m0 + j] + d[j]) / p.T_eff;
       }
       __syncthreads();
       if (warp == 0) {
@@ -537,8 +552,8 @@ __device__ void prefetch_next(const Params& p, const OwnedState* own) {
   }
 }
 
-// kGemm: 0 = CUDA-core GRU tiles (fp32 weights or widths not multiples of 128), 1 = tensor cores with tiles of
-// 32 requests x 8 units, 2 = tensor cores with tiles of 64 requests x 16 units.
+// kGemm: 0 = CUDA-core GRU tiles (fp32 weights or widths not multiples of 128), tensor cores with 1 = TileS,
+// 2 = TileL, 3 = TileS128.
 template <int kGemm>
 __global__ void __launch_bounds__(kThreads, 1) build_kernel(Params p) {
   extern __shared__ float4 smem_f4[];
@@ -552,8 +567,9 @@ __global__ void __launch_bounds__(kThreads, 1) build_kernel(Params p) {
   unsigned long long target = s_base;
   for (int s = 0; s < p.n; ++s) {
     if (s > 0) {
-      if (kGemm == 1) gemm_gru_phase<32, 8>(p, s - 1, smem);
-      else if (kGemm == 2) gemm_gru_phase<64, 16>(p, s - 1, smem);
+      if (kGemm == 1) gemm_gru_phase<TileS, 32, 8>(p, s - 1, smem);
+      else if (kGemm == 2) gemm_gru_phase<TileL, 64, 16>(p, s - 1, smem);
+      else if (kGemm == 3) gemm_gru_phase<TileS128, 32, 8>(p, s - 1, smem);
       else gru_phase(p, s - 1, reinterpret_cast<float*>(smem));
       target += G;
       if (!counter_barrier(p.hdr, target, p.timeout_ns, &s_flag)) return;
@@ -572,8 +588,9 @@ __global__ void __launch_bounds__(kThreads, 1) build_kernel(Params p) {
 // cap and the device's opt-in limit (`rows_smem` reports the choice).
 size_t smem_bytes(int gemm, int M, int n, int H, size_t esize, size_t optin, bool* rows_smem) {
   size_t a = sizeof(float) * (kTB * kPad + 3 * kTU * kPad);
-  if (gemm == 1) a = GemmTile<32, 8>::kBytes;
-  if (gemm == 2) a = GemmTile<64, 16>::kBytes;
+  if (gemm == 1) a = TileS::kBytes;
+  if (gemm == 2) a = TileL::kBytes;
+  if (gemm == 3) a = TileS128::kBytes;
   const size_t rows = static_cast<size_t>(M) * H * esize;
   const size_t base = frontier_rows_offset(M, n, H);
   *rows_smem = rows <= kFrontierRowsCap && base + rows <= optin;
@@ -636,9 +653,12 @@ extern "C" dt_status dt_build_trees(int B, int K, int V, int M, int n, int max_d
   p.timeout_ns = barrier_timeout_ns();
 
   // phase A: tensor cores for bf16 weights whose widths are multiples of the 128-column pipeline chunk
-  const bool tc = p.bf16 && E % GemmTile<32, 8>::kKc == 0 && H % GemmTile<32, 8>::kKc == 0;
-  const int gemm = !tc ? 0 : (B >= 128 ? 2 : 1);
+  const int gemm = !p.bf16 ? 0
+                   : B >= 128 ? (E % TileL::kKc == 0 && H % TileL::kKc == 0 ? 2 : 0)
+                   : E % TileS::kKc == 0 && H % TileS::kKc == 0 ? 1
+                   : E % TileS128::kKc == 0 && H % TileS128::kKc == 0 ? 3 : 0;
   const void* fn = gemm == 0 ? reinterpret_cast<const void*>(build_kernel<0>)
+                             : gemm == 3 ? reinterpret_cast<const void*>(build_kernel<3>)
                              : gemm == 1 ? reinterpret_cast<const void*>(build_kernel<1>)
                                          : reinterpret_cast<const void*>(build_kernel<2>);
   int dev = 0, sms = 0, coop = 0, per_sm = 0, optin = 0;
