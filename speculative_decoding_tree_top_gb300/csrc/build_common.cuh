@@ -58,7 +58,8 @@ struct Params {
   NodeState* state;
   Entry* frontier;  // [B][n]
   float* hs;        // [B][n][H]
-  long long* acc;   // [n][B][M] fixed-point correction accumulators (small-batch builder)
+  long long* acc;   // [n][B][M] fixed-point correction accumulators, acc_stride words apart (small-batch builder)
+  int acc_stride;
   uint64_t timeout_ns;
   bool rows_smem;   // large-batch builder: the M gathered correction rows of a node are staged in shared memory
 };
@@ -150,15 +151,23 @@ struct BuildLayout {
   size_t state, frontier, hs, acc, bytes;
 };
 
+// Words between two correction accumulators: one 128-byte line each, so that the shares of a step (every SM adds
+// one to every candidate's slot) spread over the L2 slices, unless that takes more than 64 MB.
+__host__ __device__ inline int acc_stride(int B, int M, int n) {
+  return static_cast<size_t>(n) * B * M * 128u <= (64u << 20) ? 16 : 1;
+}
+
 inline BuildLayout build_layout(int B, int K, int V, int M, int n, int H) {
   BuildLayout L{};
   L.state = topm_layout(B, K, V, M).bytes;
   L.frontier = align_up(L.state + sizeof(NodeState) * static_cast<size_t>(B));
   L.hs = align_up(L.frontier + sizeof(Entry) * static_cast<size_t>(B) * n);
   L.acc = align_up(L.hs + sizeof(float) * static_cast<size_t>(B) * n * H);
-  // per-step per-candidate accumulators [n][B][M] int64, then per-node publication counters [B][n] int32
+  // per-step per-candidate accumulators [n][B][M] int64 (acc_stride words apart), then per-node publication
+  // counters [B][n] int32
   const size_t acc_bytes =
-      B <= kSmallMaxB ? sizeof(long long) * (static_cast<size_t>(n) * B * M + (static_cast<size_t>(B) * n + 1) / 2)
+      B <= kSmallMaxB ? sizeof(long long) * (static_cast<size_t>(n) * B * M * acc_stride(B, M, n) +
+                                             (static_cast<size_t>(B) * n + 1) / 2)
                       : 0;
   L.bytes = align_up(L.acc + acc_bytes);
   return L;

@@ -36,7 +36,8 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kMaxRows = 16;  // gate rows per CTA handled by the K-split GEMV (3 * units <= 16)
+constexpr uint64_t kCopyBudgetNs = 4000000000ull;  // the weight copies take microseconds: this stops a lost one
+constexpr int kMaxRows = 16;  // gate rows per CTA, one warp each (3 * units <= 16 warps)
 constexpr int kRowPad = 8;    // elements of padding per shared-memory weight row (16 bytes)
 
 struct ReqState {  // a request's frontier bookkeeping, replicated in every CTA
@@ -53,7 +54,7 @@ struct ReqState {  // a request's frontier bookkeeping, replicated in every CTA
 // Shared-memory plan of one CTA (identical on host and device).
 struct Plan {
   int G, umax, R;
-  size_t wih, whh, bias, wc, xe, xh, req, fr, scr, z, hb, gates, red, ids, vals, par, hc, bytes;
+  size_t wih, whh, bias, wc, xe, xh, req, fr, scr, z, hb, gates, ids, vals, par, hc, bytes;
 };
 
 __host__ __device__ inline size_t take(size_t& o, size_t bytes) {
@@ -80,7 +81,6 @@ __host__ __device__ inline Plan make_plan(int B, int M, int n, int max_depth, in
   P.z = take(o, sizeof(float) * M);
   P.hb = take(o, sizeof(float) * P.umax);
   P.gates = take(o, sizeof(float) * 2 * P.R);
-  P.red = take(o, sizeof(float) * kWarps * 32);
   P.ids = take(o, sizeof(int) * B * max_depth * M);
   P.vals = take(o, sizeof(float) * B * max_depth * M);
   P.par = take(o, sizeof(short) * B * n);
@@ -131,53 +131,6 @@ __device__ __forceinline__ bool poll(const Params& p, Load load, Pred pred) {
   }
 }
 
-template <bool kBf16>
-__device__ __forceinline__ void dot_rows(const typename WT<kBf16>::T* w, size_t row_stride, int col, int R,
-                                         const float* x8, float (&acc)[kMaxRows]) {
-#pragma unroll
-  for (int r = 0; r < kMaxRows; ++r) {
-    if (r < R) {
-      const typename WT<kBf16>::T* wr = w + static_cast<size_t>(r) * row_stride + col;
-      float a = acc[r];
-      if (kBf16) {
-        const uint4 q = *reinterpret_cast<const uint4*>(wr);
-        a = fmaf(__uint_as_float(q.x << 16), x8[0], a);
-        a = fmaf(__uint_as_float(q.x & 0xFFFF0000u), x8[1], a);
-        a = fmaf(__uint_as_float(q.y << 16), x8[2], a);
-        a = fmaf(__uint_as_float(q.y & 0xFFFF0000u), x8[3], a);
-        a = fmaf(__uint_as_float(q.z << 16), x8[4], a);
-        a = fmaf(__uint_as_float(q.z & 0xFFFF0000u), x8[5], a);
-        a = fmaf(__uint_as_float(q.w << 16), x8[6], a);
-        a = fmaf(__uint_as_float(q.w & 0xFFFF0000u), x8[7], a);
-      } else {
-        const float4 q = *reinterpret_cast<const float4*>(wr);
-        a = fmaf(q.x, x8[0], a);
-        a = fmaf(q.y, x8[1], a);
-        a = fmaf(q.z, x8[2], a);
-        a = fmaf(q.w, x8[3], a);
-      }
-      acc[r] = a;
-    }
-  }
-}
-
-// Sums 32 per-thread values over a warp by recursive halving: afterwards lane l holds the warp total of value l
-// (31 shuffles instead of 32 x 5).
-__device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32]) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int w = 16; w >= 1; w >>= 1) {
-    const bool upper = lane & w;
-#pragma unroll
-    for (int i = 0; i < w; ++i) {
-      const float send = upper ? v[i] : v[i + w];
-      const float keep = upper ? v[i + w] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, w);
-    }
-  }
-  return v[0];
-}
-
 // Correction accumulators: every CTA adds (round(v * 2^32) << 8) + 1 to the slot of each candidate. The upper 56
 // bits hold the exact fixed-point sum, the low byte the number of contributions (G < 256).
 constexpr float kFix = 4294967296.0f;              // 2^32
@@ -208,7 +161,6 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
   Entry* cand = reinterpret_cast<Entry*>(smem + P.scr);      // [n + M]
   Entry* sorted = cand + (p.n + p.M);                        // [n + M]
   float* z = reinterpret_cast<float*>(smem + P.z);           // [M]
-  float* red = reinterpret_cast<float*>(smem + P.red);       // [warps][32]
   float* hb = reinterpret_cast<float*>(smem + P.hb);         // [umax]: the new hidden state of the owned units
   float* gates = reinterpret_cast<float*>(smem + P.gates);   // [R][2]: input side, hidden side
   int* ids_s = reinterpret_cast<int*>(smem + P.ids);         // [B][max_depth][M] candidate ids (range-checked)
@@ -216,6 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
   short* par_s = reinterpret_cast<short*>(smem + P.par);     // [B][n]: parent of every popped node
   float* hc = reinterpret_cast<float*>(smem + P.hc);         // [B][n][H]: hidden state of every expanded node
   __shared__ int s_flag;
+  __shared__ uint64_t wbar;  // completion of the weight rows' bulk copies
 
   const int B = p.B, K = p.K, M = p.M, n = p.n, H = p.H, E = p.E, maxd = p.max_depth;
   const int G = P.G, umax = P.umax;
@@ -223,33 +176,57 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
   const int u0 = static_cast<int>((static_cast<long long>(j) * H) / G);
   const int nu = static_cast<int>((static_cast<long long>(j + 1) * H) / G) - u0;
   const size_t esize = kBf16 ? 2 : 4;
-  int* hs_count = reinterpret_cast<int*>(p.acc + static_cast<size_t>(n) * B * M);  // [B][n]
+  const int AS = p.acc_stride;
+  int* hs_count = reinterpret_cast<int*>(p.acc + static_cast<size_t>(n) * B * M * AS);  // [B][n]
 
   // ---- launch: weights of the owned units, W_c columns / ids / base logits of the candidates, L2 prefetch ----
   const int SE = E + kRowPad, SH = H + kRowPad;  // shared-memory row strides of W_ih and W_hh
-  for (int q = 0; q < 3 * nu; ++q) {
-    const int g = q / nu, u = q % nu, r = g * umax + u;
-    const size_t row = static_cast<size_t>(g) * H + u0 + u;
-    // asynchronous copies: every row in flight at once (waited for at the top of the first step)
-    copy16_async(wih + static_cast<size_t>(r) * SE, static_cast<const char*>(p.w_ih) + row * E * esize, esize * E);
-    copy16_async(whh + static_cast<size_t>(r) * SH, static_cast<const char*>(p.w_hh) + row * H * esize, esize * H);
+  // The 3 * nu rows of W_ih and of W_hh as bulk copies (1 to 8 KB each) completing on one mbarrier, issued by warp 0;
+  // waited for at the top of the first step.
+  if (t == 0) {
+    mbar_init(&wbar, 1);
+    mbar_fence_init();
   }
-  asm volatile("cp.async.commit_group;" ::: "memory");
+  __syncthreads();
+  if (warp == 0) {
+    if (lane == 0) mbar_expect_tx(&wbar, static_cast<unsigned>(3 * nu * (E + H) * esize));
+    __syncwarp();
+    for (int q = lane; q < 6 * nu; q += 32) {
+      const bool hid = q >= 3 * nu;
+      const int qq = hid ? q - 3 * nu : q, g = qq / nu, u = qq % nu, r = g * umax + u;
+      const size_t row = static_cast<size_t>(g) * H + u0 + u;
+      if (hid)
+        bulk_g2s(whh + static_cast<size_t>(r) * SH, static_cast<const char*>(p.w_hh) + row * H * esize,
+                 static_cast<unsigned>(esize * H), &wbar);
+      else
+        bulk_g2s(wih + static_cast<size_t>(r) * SE, static_cast<const char*>(p.w_ih) + row * E * esize,
+                 static_cast<unsigned>(esize * E), &wbar);
+    }
+  }
+  // A return before the first step leaves no copy in flight: this waits (bounded) for the weights.
+  auto drain = [&]() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    mbar_wait(&wbar, 0, kCopyBudgetNs);
+  };
   for (int i = t; i < 3 * umax; i += kThreads) {
     const int g = i / umax, u = i % umax;
     const size_t row = static_cast<size_t>(g) * H + u0 + u;
     bias[2 * i] = (u < nu && p.b_ih) ? ldw(p.b_ih, kBf16, row) : 0.f;
     bias[2 * i + 1] = (u < nu && p.b_hh) ? ldw(p.b_hh, kBf16, row) : 0.f;
   }
-#pragma unroll 4
+  // candidate ids and base logits of every (request, position) first, then the owned units' W_c columns of every
+  // candidate, all independent loads
   for (int i = t; i < B * maxd * M; i += kThreads) {
     const int b = i / (maxd * M), pos = (i / M) % maxd, m = i % M;
     const size_t gi = (static_cast<size_t>(b) * K + pos) * M + m;
-    const int id = valid_id(p, __ldg(p.ids + gi));
-    ids_s[i] = id;
+    ids_s[i] = valid_id(p, __ldg(p.ids + gi));
     vals_s[i] = __ldg(p.vals + gi);
-    const T* src = static_cast<const T*>(p.w_c) + static_cast<size_t>(id) * H + u0;
-    for (int u = 0; u < umax; ++u) wc[static_cast<size_t>(i) * umax + u] = u < nu ? src[u] : T(0);
+  }
+  __syncthreads();
+#pragma unroll 8
+  for (int q = t; q < B * maxd * M * umax; q += kThreads) {
+    const int i = q / umax, u = q % umax;
+    wc[q] = u < nu ? static_cast<const T*>(p.w_c)[static_cast<size_t>(ids_s[i]) * H + u0 + u] : T(0);
   }
   {
     const size_t row_bytes = static_cast<size_t>(E) * esize;
@@ -267,16 +244,20 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
     }
   }
   // every step's accumulators and the hidden-state counters start at zero; one grid barrier orders that
-  const size_t zero_words = static_cast<size_t>(n) * B * M + (static_cast<size_t>(B) * n + 1) / 2;
+  const size_t zero_words = static_cast<size_t>(n) * B * M * AS + (static_cast<size_t>(B) * n + 1) / 2;
   for (size_t i = static_cast<size_t>(j) * kThreads + t; i < zero_words; i += static_cast<size_t>(G) * kThreads)
     p.acc[i] = 0;
   for (int b = t; b < B; b += kThreads) rs[b] = ReqState{};
-  if (!grid_barrier(p.hdr, G, p.timeout_ns, &s_flag)) return;
+  if (!grid_barrier(p.hdr, G, p.timeout_ns, &s_flag)) {
+    drain();
+    return;
+  }
 
+  if (!mbar_wait(&wbar, 0, kCopyBudgetNs)) record_error(p.hdr, DT_ERR_TIMEOUT);  // the weight rows (bounded)
   for (int s = 0; s < n; ++s) {
     asm volatile("cp.async.wait_all;" ::: "memory");  // this thread's cache and embedding copies
     __syncthreads();                                   // ... and everyone else's
-    long long* acc_s = p.acc + static_cast<size_t>(s) * B * M;
+    long long* acc_s = p.acc + static_cast<size_t>(s) * B * M * AS;
 
     // ---- phase A: this CTA's share of the GRU and of the correction of every expanding request ----
     for (int b = 0; b < B; ++b) {
@@ -298,56 +279,69 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
         }
         const T* xeb = xe + static_cast<size_t>(b) * E;
         const int R = 3 * umax;
-        {
-          // K-split GEMV on the CUDA cores: each thread reads its slice of x once and applies it to every gate row;
-          // a recursive-halving shuffle reduce-scatter finishes the warp's sums. (Legacy mma.sync was measured
-          // slower here: a 12-row GEMV is latency-bound, not throughput-bound.)
+        if (warp < R) {
+          // One warp per gate row (R <= 16 rows, 16 warps): the lanes stride over K with four independent
+          // accumulators per side, then one shuffle tree per side. The row's input side (over E) and hidden side
+          // (over H) stay apart: the n gate needs them separately.
+          const int r = warp;
           constexpr int kPer = kBf16 ? 8 : 4;
-          const int EG = E / kPer, KG = (E + H) / kPer;
-          float ai[kMaxRows], ah[kMaxRows];
-#pragma unroll
-          for (int r = 0; r < kMaxRows; ++r) ai[r] = ah[r] = 0.f;
-          for (int f = t; f < KG; f += kThreads) {
-            float x8[8];
-            if (f < EG) {
-              if (kBf16) {
-                const uint4 q = *reinterpret_cast<const uint4*>(xeb + f * kPer);
-                x8[0] = __uint_as_float(q.x << 16); x8[1] = __uint_as_float(q.x & 0xFFFF0000u);
-                x8[2] = __uint_as_float(q.y << 16); x8[3] = __uint_as_float(q.y & 0xFFFF0000u);
-                x8[4] = __uint_as_float(q.z << 16); x8[5] = __uint_as_float(q.z & 0xFFFF0000u);
-                x8[6] = __uint_as_float(q.w << 16); x8[7] = __uint_as_float(q.w & 0xFFFF0000u);
-              } else {
-                const float4 q = *reinterpret_cast<const float4*>(xeb + f * kPer);
-                x8[0] = q.x; x8[1] = q.y; x8[2] = q.z; x8[3] = q.w;
-              }
-              dot_rows<kBf16>(wih, SE, f * kPer, R, x8, ai);
+          float ai[4] = {0.f, 0.f, 0.f, 0.f}, ah[4] = {0.f, 0.f, 0.f, 0.f};
+          const T* wr = wih + static_cast<size_t>(r) * SE;
+#pragma unroll 4
+          for (int f = lane; f < E / kPer; f += 32) {
+            const int c = f * kPer;
+            if (kBf16) {
+              const uint4 w = *reinterpret_cast<const uint4*>(wr + c), q = *reinterpret_cast<const uint4*>(xeb + c);
+              ai[0] = fmaf(__uint_as_float(w.x << 16), __uint_as_float(q.x << 16), ai[0]);
+              ai[1] = fmaf(__uint_as_float(w.x & 0xFFFF0000u), __uint_as_float(q.x & 0xFFFF0000u), ai[1]);
+              ai[2] = fmaf(__uint_as_float(w.y << 16), __uint_as_float(q.y << 16), ai[2]);
+              ai[3] = fmaf(__uint_as_float(w.y & 0xFFFF0000u), __uint_as_float(q.y & 0xFFFF0000u), ai[3]);
+              ai[0] = fmaf(__uint_as_float(w.z << 16), __uint_as_float(q.z << 16), ai[0]);
+              ai[1] = fmaf(__uint_as_float(w.z & 0xFFFF0000u), __uint_as_float(q.z & 0xFFFF0000u), ai[1]);
+              ai[2] = fmaf(__uint_as_float(w.w << 16), __uint_as_float(q.w << 16), ai[2]);
+              ai[3] = fmaf(__uint_as_float(w.w & 0xFFFF0000u), __uint_as_float(q.w & 0xFFFF0000u), ai[3]);
             } else {
-              const int c = (f - EG) * kPer;
-              const float4 a = *reinterpret_cast<const float4*>(xhp + c);
-              x8[0] = a.x; x8[1] = a.y; x8[2] = a.z; x8[3] = a.w;
-              if (kBf16) {
-                const float4 b4 = *reinterpret_cast<const float4*>(xhp + c + 4);
-                x8[4] = b4.x; x8[5] = b4.y; x8[6] = b4.z; x8[7] = b4.w;
-              }
-              dot_rows<kBf16>(whh, SH, c, R, x8, ah);
+              const float4 w = *reinterpret_cast<const float4*>(wr + c), q = *reinterpret_cast<const float4*>(xeb + c);
+              ai[0] = fmaf(w.x, q.x, ai[0]);
+              ai[1] = fmaf(w.y, q.y, ai[1]);
+              ai[2] = fmaf(w.z, q.z, ai[2]);
+              ai[3] = fmaf(w.w, q.w, ai[3]);
             }
           }
-          float v[32];
-#pragma unroll
-          for (int r = 0; r < kMaxRows; ++r) {
-            v[r] = ai[r];
-            v[kMaxRows + r] = ah[r];
+          const T* hr = whh + static_cast<size_t>(r) * SH;
+#pragma unroll 4
+          for (int f = lane; f < H / kPer; f += 32) {
+            const int c = f * kPer;
+            const float4 x0 = *reinterpret_cast<const float4*>(xhp + c);
+            if (kBf16) {
+              const float4 x1 = *reinterpret_cast<const float4*>(xhp + c + 4);
+              const uint4 w = *reinterpret_cast<const uint4*>(hr + c);
+              ah[0] = fmaf(__uint_as_float(w.x << 16), x0.x, ah[0]);
+              ah[1] = fmaf(__uint_as_float(w.x & 0xFFFF0000u), x0.y, ah[1]);
+              ah[2] = fmaf(__uint_as_float(w.y << 16), x0.z, ah[2]);
+              ah[3] = fmaf(__uint_as_float(w.y & 0xFFFF0000u), x0.w, ah[3]);
+              ah[0] = fmaf(__uint_as_float(w.z << 16), x1.x, ah[0]);
+              ah[1] = fmaf(__uint_as_float(w.z & 0xFFFF0000u), x1.y, ah[1]);
+              ah[2] = fmaf(__uint_as_float(w.w << 16), x1.z, ah[2]);
+              ah[3] = fmaf(__uint_as_float(w.w & 0xFFFF0000u), x1.w, ah[3]);
+            } else {
+              const float4 w = *reinterpret_cast<const float4*>(hr + c);
+              ah[0] = fmaf(w.x, x0.x, ah[0]);
+              ah[1] = fmaf(w.y, x0.y, ah[1]);
+              ah[2] = fmaf(w.z, x0.z, ah[2]);
+              ah[3] = fmaf(w.w, x0.w, ah[3]);
+            }
           }
-          red[warp * 32 + lane] = warp_reduce_scatter32(v);
-        }
-        __syncthreads();
-        if (t < 2 * R) {  // value t: input side of row t (t < R) or hidden side of row t - R, summed over the warps
-          const int vi = t < R ? t : kMaxRows + (t - R);
-          float q[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains
+          float si = (ai[0] + ai[1]) + (ai[2] + ai[3]), sh = (ah[0] + ah[1]) + (ah[2] + ah[3]);
 #pragma unroll
-          for (int w = 0; w < kWarps; ++w) q[w & 3] += red[w * 32 + vi];
-          const int r = t < R ? t : t - R;
-          gates[2 * r + (t < R ? 0 : 1)] = (q[0] + q[1]) + (q[2] + q[3]);
+          for (int o = 16; o > 0; o >>= 1) {
+            si += __shfl_xor_sync(0xFFFFFFFFu, si, o);
+            sh += __shfl_xor_sync(0xFFFFFFFFu, sh, o);
+          }
+          if (lane == 0) {
+            gates[2 * r] = si;
+            gates[2 * r + 1] = sh;
+          }
         }
         __syncthreads();
         for (int u = t; u < nu; u += kThreads) {
@@ -372,9 +366,9 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
       for (int m = t; m < M; m += kThreads) {
         float v = 0.f;
         for (int u = 0; u < nu; ++u) v = fmaf(WT<kBf16>::f(wcp[static_cast<size_t>(m) * umax + u]), hb[u], v);
-        add_share(p, acc_s + static_cast<size_t>(b) * M + m, v);
+        add_share(p, acc_s + (static_cast<size_t>(b) * M + m) * AS, v);
       }
-      if (B > 1) __syncthreads();  // red / xh are reused by the next request
+      if (B > 1) __syncthreads();  // gates / xh are reused by the next request
     }
 
     // ---- phase C: every CTA finishes the step for every request (the whole CTA on one request at a time) ----
@@ -388,21 +382,41 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
       for (int i = t; i < F; i += kThreads) cand[i] = fr[static_cast<size_t>(b) * n + i];
       int ok = 1;
       if (expanded && warp == 0) {
-        // All G shares of every candidate: lane 0 polls a sentinel slot (every CTA issues the shares of all
-        // candidates together, so the others are then complete or nearly so), then each lane reads its slots once and
-        // re-polls only a slot still short. Light polling traffic on the lines the shares are landing in.
+        // All G shares of every candidate: each lane polls its slots (each on its own cache line) until all are
+        // complete, every slot read of a round in flight together, then takes the corrected logits.
         auto complete = [&](long long v) { return (v & 0xFF) == (G & 0xFF); };
-        const long long* slots = acc_s + static_cast<size_t>(b) * M;
-        if (lane == 0) ok &= poll(p, [&] { return ld_relaxed_s64(slots + (M - 1)); }, complete);
-        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        const long long* slots = acc_s + static_cast<size_t>(b) * M * AS;
         float mx = -INFINITY;
-        for (int m = lane; ok && m < M; m += 32) {
-          long long a = 0;
-          ok &= poll(p, [&] { return a = ld_relaxed_s64(slots + m); }, complete);
-          const float v = (vals_s[off + m] + __ll2float_rn(a >> 8) * kUnfix) / p.T_eff;
-          z[m] = v;
-          mx = fmaxf(mx, v);
+        for (int m0 = lane; m0 < M; m0 += 128) {
+          long long a[4];
+          bool done = false;
+          const uint64_t t0 = global_timer_ns();
+          for (unsigned polls = 0; !done; ++polls) {
+            done = true;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int m = m0 + 32 * j;
+              a[j] = m < M ? ld_relaxed_s64(slots + static_cast<size_t>(m) * AS) : static_cast<long long>(G & 0xFF);
+              done &= complete(a[j]);
+            }
+            if (!done && (polls & 15u) == 15u &&
+                (ld_acquire_gpu(&p.hdr->abort) != 0u || global_timer_ns() - t0 > p.timeout_ns)) {
+              record_error(p.hdr, DT_ERR_TIMEOUT);
+              atomicExch(&p.hdr->abort, 1u);
+              ok = 0;
+              break;
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int m = m0 + 32 * j;
+            if (m >= M) break;
+            const float v = (vals_s[off + m] + __ll2float_rn(a[j] >> 8) * kUnfix) / p.T_eff;
+            z[m] = v;
+            mx = fmaxf(mx, v);
+          }
         }
+        ok = __all_sync(0xFFFFFFFFu, ok);
         // restricted log-softmax of this node's children, in the warp
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
@@ -440,7 +454,10 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
       }
-      if (!__syncthreads_and(ok)) return;
+      if (!__syncthreads_and(ok)) {  // a wait ran out (recorded): leave with no copy in flight
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        return;
+      }
       // Keep the R = n - s best (nothing ranked below them can be popped in the n - s pops left). Rank by
       // counting, tpe threads per entry, each counting a stride of the others, combined with shuffles.
       const int N = F + C;

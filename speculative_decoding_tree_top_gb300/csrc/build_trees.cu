@@ -650,6 +650,7 @@ extern "C" dt_status dt_build_trees(int B, int K, int V, int M, int n, int max_d
   p.frontier = reinterpret_cast<Entry*>(ws + L.frontier);
   p.hs = reinterpret_cast<float*>(ws + L.hs);
   p.acc = B <= kSmallMaxB ? reinterpret_cast<long long*>(ws + L.acc) : nullptr;
+  p.acc_stride = acc_stride(B, M, n);
   p.timeout_ns = barrier_timeout_ns();
 
   // phase A: tensor cores for bf16 weights whose widths are multiples of the 128-column pipeline chunk
