@@ -84,6 +84,46 @@ __device__ __forceinline__ int valid_id(const Params& p, int id) {
   return id;
 }
 
+// Keeps the first R entries, in pop order, of the union of a request's frontier and a node's new children:
+// cand[0, F) is the frontier, already in pop order (it was written that way), cand[F, F + C) the children in any
+// order. The children are ranked among themselves by counting (tpe threads per child), then every entry's place in
+// the union is its place in its own list plus a binary search in the other one: O((F + C) log) instead of counting
+// every pair. `before` is a strict total order, so the places are distinct. sc[0, C) is scratch; sorted[0, R) the
+// result. Called by the whole block (kThreads threads); ends synchronised.
+template <int kThreads>
+__device__ void merge_rank(const Entry* cand, int F, int C, int R, Entry* sc, Entry* sorted) {
+  const int t = threadIdx.x;
+  int tpe = 1;
+  while (tpe < 32 && tpe * 2 * C <= kThreads) tpe *= 2;
+  for (int base = 0; base < C * tpe; base += kThreads) {  // uniform bounds: every lane reaches the shuffles
+    const int slot = base + t, i = slot / tpe, part = slot % tpe;
+    int r = 0;
+    Entry ei{};
+    if (i < C) {
+      ei = cand[F + i];
+#pragma unroll 4
+      for (int q = part; q < C; q += tpe) r += before(cand[F + q], ei);
+    }
+    for (int o = 1; o < tpe; o <<= 1) r += __shfl_xor_sync(0xFFFFFFFFu, r, o);
+    if (i < C && part == 0) sc[r] = ei;
+  }
+  __syncthreads();
+  for (int k = t; k < F + C; k += kThreads) {
+    const bool old = k < F;
+    const Entry e = old ? cand[k] : sc[k - F];
+    const Entry* other = old ? sc : cand;
+    int lo = 0, hi = old ? C : F;  // entries of the other list that come before e
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (before(other[mid], e)) lo = mid + 1;
+      else hi = mid;
+    }
+    const int r = (old ? k : k - F) + lo;
+    if (r < R) sorted[r] = e;
+  }
+  __syncthreads();
+}
+
 // One warp: the dot products of 8 consecutive rows m0 .. m0 + 7 (those < M) with h, for the rows of a gathered slice
 // in shared memory (`rows`, [M][H]) or, when rows == nullptr, the correction rows w[ids[m]] in global memory. The
 // lane's share of h is loaded once and used for all 8 rows, whose sums are 8 independent chains (same per-lane order

@@ -458,24 +458,11 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
         asm volatile("cp.async.wait_all;" ::: "memory");
         return;
       }
-      // Keep the R = n - s best (nothing ranked below them can be popped in the n - s pops left). Rank by
-      // counting, tpe threads per entry, each counting a stride of the others, combined with shuffles.
+      // Keep the R = n - s best (nothing ranked below them can be popped in the n - s pops left): the sorted
+      // frontier merged with the ranked children.
       const int N = F + C;
       const int R = min(n - s, N);
-      int tpe = 1;
-      while (tpe < 32 && tpe * 2 * N <= kThreads) tpe *= 2;
-      for (int base = 0; base < N * tpe; base += kThreads) {
-        const int slot = base + t, i = slot / tpe, part = slot % tpe;
-        int r = 0;
-        Entry ei{};
-        if (i < N) {
-          ei = cand[i];
-#pragma unroll 4
-          for (int q = part; q < N; q += tpe) r += before(cand[q], ei);
-        }
-        for (int o = 1; o < tpe; o <<= 1) r += __shfl_xor_sync(0xFFFFFFFFu, r, o);
-        if (i < N && part == 0 && r < R) sorted[r] = ei;
-      }
+      merge_rank<kThreads>(cand, F, C, R, sorted + n, sorted);
       if (N == 0 && t == 0) {  // unreachable when n <= the size of the depth-limited tree (checked on the host)
         record_error(p.hdr, DT_ERR_INVALID_ARG);
         sorted[0] = Entry{-INFINITY, 0, -1, 1, 0};

@@ -484,25 +484,11 @@ __device__ void frontier_phase(const Params& p, int s, unsigned char* smem, Owne
       }
     }
     __syncthreads();
-    // Keep the R = n - s best: nothing ranked below them can be popped in the n - s pops left. Rank by counting,
-    // tpe threads per entry, each counting a stride of the others, combined with shuffles.
+    // Keep the R = n - s best (nothing ranked below them can be popped in the n - s pops left): the sorted
+    // frontier merged with the ranked children (sorted[n, n + M) is free: R <= n).
     const int N = F + C;
     const int R = min(n - s, N);
-    int tpe = 1;
-    while (tpe < 32 && tpe * 2 * N <= kThreads) tpe *= 2;
-    for (int base = 0; base < N * tpe; base += kThreads) {
-      const int slot_i = base + t, i = slot_i / tpe, part = slot_i % tpe;
-      int r = 0;
-      Entry ei{};
-      if (i < N) {
-        ei = cand[i];
-#pragma unroll 4
-        for (int q = part; q < N; q += tpe) r += before(cand[q], ei);
-      }
-      for (int o = 1; o < tpe; o <<= 1) r += __shfl_xor_sync(0xFFFFFFFFu, r, o);
-      if (i < N && part == 0 && r < R) sorted[r] = ei;
-    }
-    __syncthreads();
+    merge_rank<kThreads>(cand, F, C, R, sorted + n, sorted);
     const Entry pop = sorted[0];
     for (int i = t + 1; i < R; i += kThreads) fr[i - 1] = sorted[i];
     const size_t o = static_cast<size_t>(b) * n + s;
