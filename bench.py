@@ -203,10 +203,10 @@ def run_ours(args, world, rank, local):
         flush.zero_()
         if evs:
             evs[0].record(stream)
-        dt.dt_topm(inp.logits, s.M, rnd.ids, rnd.vals, rnd.workspace, stream)
+        rnd.topm(inp.logits, stream)
         if evs:
             evs[1].record(stream)
-        dt.dt_build_trees(rnd.ids, rnd.vals, inp.h0, w, s.n, s.max_depth, s.T, rnd.out, rnd.workspace, stream)
+        rnd.build(inp.h0, stream)
         if evs:
             evs[2].record(stream)
 

@@ -162,6 +162,15 @@ dt_status dt_get_error(void* workspace, cudaStream_t stream);
  * budget of 0 the first wait gives up at once, the kernel records DT_ERR_TIMEOUT and returns. Process-wide. */
 void dt_set_barrier_timeout_ns(uint64_t ns);
 
+/* Lookahead width of dt_build_trees: how many nodes of one request may be expanded together in one wave (their GRU
+ * steps and children's scores computed at once), process-wide. 0 (the default) lets the library choose; k >= 1 caps
+ * it (the small-batch builder also caps B·k at its wave size). The pops stay strictly best-first: a node joins the
+ * frontier only when its parent is popped, so every width gives bit-identical outputs and only the time changes.
+ * Returns DT_ERR_INVALID_ARG for k < 0 or k > DT_MAX_LOOKAHEAD. A tuning and test hook; no counterpart in the paper,
+ * whose builder expands one popped node at a time (blog.captcha.la, "Methodology — deep read"). */
+#define DT_MAX_LOOKAHEAD 8
+dt_status dt_set_lookahead(int k);
+
 const char* dt_status_string(dt_status s);
 int dt_abi_version(void);
 

@@ -1,5 +1,7 @@
 // Status strings, workspace initialisation, device status word, process-wide settings of libdominotree.
 #include <atomic>
+#include <mutex>
+#include <vector>
 
 #include <cuda_runtime.h>
 
@@ -8,8 +10,60 @@
 namespace dt {
 namespace {
 std::atomic<uint64_t> g_barrier_timeout_ns{2000000000ull};
+std::atomic<int> g_lookahead{0};
 }
 uint64_t barrier_timeout_ns() { return g_barrier_timeout_ns.load(std::memory_order_relaxed); }
+int lookahead_setting() { return g_lookahead.load(std::memory_order_relaxed); }
+
+namespace {
+std::mutex g_cache_mu;
+std::vector<DeviceInfo> g_devices;
+struct SmemSetting {
+  int dev;
+  const void* fn;
+  size_t bytes;
+};
+std::vector<SmemSetting> g_smem;
+}  // namespace
+
+cudaError_t current_device_info(DeviceInfo* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  {
+    std::lock_guard<std::mutex> lock(g_cache_mu);
+    for (const DeviceInfo& d : g_devices)
+      if (d.dev == dev) {
+        *out = d;
+        return cudaSuccess;
+      }
+  }
+  DeviceInfo d{dev, 0, 0, 0};
+  e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.coop, cudaDevAttrCooperativeLaunch, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  g_devices.push_back(d);
+  *out = d;
+  return cudaSuccess;
+}
+
+cudaError_t ensure_dynamic_smem(const void* fn, size_t bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  SmemSetting* have = nullptr;
+  for (SmemSetting& sset : g_smem)
+    if (sset.dev == dev && sset.fn == fn) have = &sset;
+  if (have && have->bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e != cudaSuccess) return e;
+  if (have) have->bytes = bytes;
+  else g_smem.push_back(SmemSetting{dev, fn, bytes});
+  return cudaSuccess;
+}
 }  // namespace dt
 
 extern "C" const char* dt_status_string(dt_status s) {
@@ -28,6 +82,12 @@ extern "C" int dt_abi_version(void) { return DT_ABI_VERSION; }
 
 extern "C" void dt_set_barrier_timeout_ns(uint64_t ns) {
   dt::g_barrier_timeout_ns.store(ns, std::memory_order_relaxed);
+}
+
+extern "C" dt_status dt_set_lookahead(int k) {
+  if (k < 0 || k > DT_MAX_LOOKAHEAD) return DT_ERR_INVALID_ARG;
+  dt::g_lookahead.store(k, std::memory_order_relaxed);
+  return DT_OK;
 }
 
 extern "C" dt_status dt_workspace_init(void* workspace, size_t workspace_bytes, cudaStream_t stream) {

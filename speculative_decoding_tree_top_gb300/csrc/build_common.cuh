@@ -9,6 +9,12 @@
 namespace dt {
 
 constexpr int kSmallMaxB = 8;  // batches up to this size use the all-SM, one-barrier-per-step builder
+constexpr int kWaveJobs = 8;   // small-batch builder: expansions per wave over the whole batch
+constexpr int kSpareSlots = 16;  // expansion slots per request beyond the n that best-first needs (speculation)
+
+// Expansion slots of a request: the root (slot 0) and every node whose children were computed, speculatively or
+// not. Best-first needs at most n (the root and the first n - 1 pops); the rest bound the speculative waste.
+__host__ __device__ inline int expansion_slots(int n) { return n + kSpareSlots; }
 
 struct alignas(16) Entry {  // a frontier node; 16 bytes
   float score;
@@ -23,6 +29,251 @@ __device__ __forceinline__ bool before(const Entry& a, const Entry& b) {
   const bool seq_first = a.seq < b.seq;
   const bool tok_first = (a.token < b.token) | ((a.token == b.token) & seq_first);
   return (a.score > b.score) | ((a.score == b.score) & tok_first);
+}
+
+// A known node of the lookahead builders: an entry of a request's frontier, or of the children list of an expanded
+// node that has not been popped yet; 16 bytes.
+struct alignas(16) Node {
+  float score;
+  int token;
+  int seq;      // insertion order; in the children list of an unpopped node: the candidate index m
+  short pslot;  // expansion slot of the parent (0 = the root)
+  short xslot;  // expansion slot of this node, -1 while its children are unknown
+};
+
+__device__ __forceinline__ bool before(const Node& a, const Node& b) {
+  const bool seq_first = a.seq < b.seq;
+  const bool tok_first = (a.token < b.token) | ((a.token == b.token) & seq_first);
+  return (a.score > b.score) | ((a.score == b.score) & tok_first);
+}
+
+// One expansion: the GRU step of a node (unless it is the root) and its children's scores.
+struct Job {
+  int b;        // request
+  int xslot;    // the node's expansion slot: where its hidden state and children go
+  int pslot;    // its parent's slot (-1 for the root, whose hidden state is h0)
+  int token;    // its token: the GRU input
+  int depth;    // its depth: the children take block position `depth`
+  float score;  // its cumulative score
+  int pad[2];
+};
+
+// Warp-wide best of one candidate per lane (`has` false: none), in pop order: higher score (-0.0 equal to +0.0),
+// then lower token, then lower insertion index, then lower lane. Three warp reductions and one ballot pick the lane;
+// returns it (-1 if no lane has a candidate) and leaves its node in `e` in every lane.
+__device__ __forceinline__ int warp_best(bool has, Node& e) {
+  const uint32_t sk = has ? key_of_f32(__float_as_uint(e.score)) : 0u;  // keys of real scores are >= 1
+  const uint32_t ms = __reduce_max_sync(0xFFFFFFFFu, sk);
+  if (ms == 0u) return -1;
+  const bool c1 = sk == ms;
+  const uint32_t mt = __reduce_min_sync(0xFFFFFFFFu, c1 ? static_cast<uint32_t>(e.token) : 0xFFFFFFFFu);
+  const bool c2 = c1 && static_cast<uint32_t>(e.token) == mt;
+  const uint32_t mq = __reduce_min_sync(0xFFFFFFFFu, c2 ? static_cast<uint32_t>(e.seq) : 0xFFFFFFFFu);
+  const bool c3 = c2 && static_cast<uint32_t>(e.seq) == mq;
+  const int wl = __ffs(__ballot_sync(0xFFFFFFFFu, c3)) - 1;
+  e.score = __shfl_sync(0xFFFFFFFFu, e.score, wl);
+  e.token = __shfl_sync(0xFFFFFFFFu, e.token, wl);
+  e.seq = __shfl_sync(0xFFFFFFFFu, e.seq, wl);
+  e.pslot = static_cast<short>(__shfl_sync(0xFFFFFFFFu, static_cast<int>(e.pslot), wl));
+  e.xslot = static_cast<short>(__shfl_sync(0xFFFFFFFFu, static_cast<int>(e.xslot), wl));
+  return wl;
+}
+
+// A request's best-first bookkeeping.
+struct ReqCtl {
+  int s;          // nodes popped
+  int fb;         // which buffer of the merged list is current
+  int seq_next;   // insertion index of the next child that joins the frontier
+  int next_slot;  // expansion slots in use (the root holds slot 0)
+  int njobs;      // expansions picked for the next wave
+  int pad[3];
+};
+
+// The frontier of a request is the union of up to 32 sorted sources, one per lane of the warp that works on it:
+// lane 0 walks the merged list, lane l > 0 the ranked children list of a popped node (slot `src`), whose entry m
+// has insertion index base + m. An idle lane has src = -1.
+struct LaneSrc {
+  int src;   // -2: the merged list, -1: none, >= 0: the children list of that slot
+  int idx;   // next entry
+  int cnt;   // entries
+  int base;  // insertion index of the list's candidate 0
+};
+
+struct PopRec {  // a popped node, as the outputs need it
+  int token;
+  int parent;
+  int depth;
+  float score;
+};
+
+// One request's state as the warp that pops and picks sees it (shared memory).
+struct ReqView {
+  ReqCtl* ctl;
+  LaneSrc* lanes;  // [32]
+  Node* merged;    // [2][n]
+  Node* kids;      // [X][KM] ranked children of every expanded slot
+  int* kcount;     // [X] entries kept in each children list
+  int* popidx;     // [X] pop index of the slot's node (-1: the root, -2: not popped)
+  int* sdepth;     // [X] depth of the slot's node
+  PopRec* pops;    // [n]
+};
+
+__device__ __forceinline__ bool lane_head(const ReqView& R, const LaneSrc& q, const Node* mg, int KM, Node& h) {
+  if (q.src == -1 || q.idx >= q.cnt) return false;
+  if (q.src == -2) {
+    h = mg[q.idx];
+  } else {
+    h = R.kids[static_cast<size_t>(q.src) * KM + q.idx];
+    h.seq += q.base;
+  }
+  return true;
+}
+
+// Called by one whole warp for request b once its wave's expansions are known. Pops best-first while the best node
+// of the frontier needs no expansion (a leaf of the depth limit, or the n-th pop) or is already expanded; then walks
+// on in the order best-first would follow on what is known (the frontier, plus the children of nodes expanded but
+// not popped yet, with the insertion indices they would get) and picks up to `kla` unexpanded nodes for the next
+// wave, the blocked best first. A pick takes an expansion slot; picks after the first keep enough slots free for
+// every pop still to come. The pops are exact whatever the picks: a pick only decides when children become known.
+__device__ inline void request_step(const ReqView& R, int b, int n, int M, int maxd, int X, int KM, int kla,
+                                    Job* jobs_out, WsHeader* hdr) {
+  const int lane = threadIdx.x & 31;
+  ReqCtl st = *R.ctl;
+  LaneSrc ls = R.lanes[lane];
+  if (ls.src >= 0 && ls.cnt < 0) ls.cnt = R.kcount[ls.src];  // the root's list, attached at launch, filled in wave 0
+  Node* mg = R.merged + static_cast<size_t>(st.fb) * n;
+  Node hd{};
+  bool has = lane_head(R, ls, mg, KM, hd);
+  while (st.s < n) {
+    Node e = hd;
+    const int wl = warp_best(has, e);
+    if (wl < 0) {  // unreachable when n <= the size of the depth-limited tree (checked on the host)
+      if (lane == 0) record_error(hdr, DT_ERR_INVALID_ARG);
+      break;
+    }
+    const int depth = R.sdepth[e.pslot] + 1;
+    const bool need = (st.s + 1 < n) && (depth < maxd);
+    if (need && e.xslot < 0) break;  // its children are not known yet: the next wave expands it
+    if (lane == 0) R.pops[st.s] = PopRec{e.token, R.popidx[e.pslot], depth, e.score};
+    if (lane == wl) {
+      ++ls.idx;
+      has = lane_head(R, ls, mg, KM, hd);
+    }
+    if (need) {
+      const int x = e.xslot;
+      if (lane == 0) R.popidx[x] = st.s;
+      const int kc = R.kcount[x];
+      if (kc > 0) {
+        unsigned idle = __ballot_sync(0xFFFFFFFFu, lane > 0 && !has);
+        if (idle == 0u) {
+          // Every lane walks a live list: fold the shortest into the merged list, keeping what can still be popped.
+          const unsigned rem = lane > 0 ? static_cast<unsigned>(ls.cnt - ls.idx) : 0xFFFFFFFFu;
+          const unsigned key = __reduce_min_sync(0xFFFFFFFFu, lane > 0 ? (rem << 5) | lane : 0xFFFFFFFFu);
+          const int L = static_cast<int>(key & 31u);
+          const int i0 = __shfl_sync(0xFFFFFFFFu, ls.idx, 0), c0 = __shfl_sync(0xFFFFFFFFu, ls.cnt, 0);
+          const int sL = __shfl_sync(0xFFFFFFFFu, ls.src, L), iL = __shfl_sync(0xFFFFFFFFu, ls.idx, L);
+          const int cL = __shfl_sync(0xFFFFFFFFu, ls.cnt, L), bL = __shfl_sync(0xFFFFFFFFu, ls.base, L);
+          const Node* la = mg + i0;
+          const Node* lb = R.kids + static_cast<size_t>(sL) * KM + iL;
+          const int na = c0 - i0, nb = cL - iL, limit = n - st.s - 1;
+          Node* out = R.merged + static_cast<size_t>(st.fb ^ 1) * n;
+          for (int k = lane; k < na + nb; k += 32) {
+            Node v;
+            int lo = 0, hi, pos;
+            if (k < na) {
+              v = la[k];
+              hi = nb;
+              while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                Node c = lb[mid];
+                c.seq += bL;
+                if (before(c, v)) lo = mid + 1;
+                else hi = mid;
+              }
+              pos = k + lo;
+            } else {
+              v = lb[k - na];
+              v.seq += bL;
+              hi = na;
+              while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (before(la[mid], v)) lo = mid + 1;
+                else hi = mid;
+              }
+              pos = (k - na) + lo;
+            }
+            if (pos < limit) out[pos] = v;
+          }
+          __syncwarp();
+          st.fb ^= 1;
+          mg = out;
+          if (lane == 0) ls = LaneSrc{-2, 0, min(na + nb, limit), 0};
+          if (lane == L) ls.src = -1;
+          if (lane == 0 || lane == L) has = lane_head(R, ls, mg, KM, hd);
+          idle = __ballot_sync(0xFFFFFFFFu, lane > 0 && !has);
+        }
+        const int nl = __ffs(idle) - 1;
+        if (lane == nl) {
+          ls = LaneSrc{x, 0, kc, st.seq_next};
+          has = lane_head(R, ls, mg, KM, hd);
+        }
+      }
+      st.seq_next += M;
+    }
+    ++st.s;
+  }
+  R.lanes[lane] = ls;
+  // lookahead: the same walk on a copy of the lanes, taking unexpanded nodes as picks instead of stopping there
+  int njobs = 0;
+  if (st.s < n) {
+    LaneSrc ss = ls;
+    Node sh = hd;
+    bool shas = has;
+    int sseq = st.seq_next;
+    for (int sim = st.s; sim < n - 1 && njobs < kla; ++sim) {
+      Node e = sh;
+      const int wl = warp_best(shas, e);
+      if (wl < 0) break;
+      const int depth = R.sdepth[e.pslot] + 1;
+      if (depth < maxd && e.xslot < 0) {
+        const bool allowed = njobs == 0 || st.next_slot + 1 + (n - 1 - st.s) <= X;
+        if (!allowed || st.next_slot >= X) break;
+        const int x = st.next_slot++;
+        if (lane == wl) {  // mark the node as expanded in the list it lives in
+          Node* at = ss.src == -2 ? mg + ss.idx : R.kids + static_cast<size_t>(ss.src) * KM + ss.idx;
+          at->xslot = static_cast<short>(x);
+        }
+        if (lane == 0) {
+          R.sdepth[x] = depth;
+          R.popidx[x] = -2;
+          R.kcount[x] = 0;
+          jobs_out[njobs] = Job{b, x, e.pslot, e.token, depth, e.score, {0, 0}};
+        }
+        ++njobs;
+      }
+      if (lane == wl) {
+        ++ss.idx;
+        shas = lane_head(R, ss, mg, KM, sh);
+      }
+      if (depth < maxd && e.xslot >= 0) {  // expanded but not popped: its children join the walk
+        const int kc = R.kcount[e.xslot];
+        if (kc > 0) {
+          const unsigned idle = __ballot_sync(0xFFFFFFFFu, lane > 0 && !shas);
+          if (idle == 0u) break;
+          const int nl = __ffs(idle) - 1;
+          if (lane == nl) {
+            ss = LaneSrc{e.xslot, 0, kc, sseq};
+            shas = lane_head(R, ss, mg, KM, sh);
+          }
+        }
+        sseq += M;
+      }
+    }
+  }
+  if (st.s < n && njobs == 0 && lane == 0) record_error(hdr, DT_ERR_INVALID_ARG);  // no slot left (unreachable)
+  st.njobs = njobs;
+  __syncwarp();
+  if (lane == 0) *R.ctl = st;
 }
 
 struct NodeState {  // the node popped last by a request, as phase A of the next step needs it
@@ -62,6 +313,9 @@ struct Params {
   int acc_stride;
   uint64_t timeout_ns;
   bool rows_smem;   // large-batch builder: the M gathered correction rows of a node are staged in shared memory
+  int lookahead;    // expansions a request may run per wave (1 = one pop at a time)
+  int xslots;       // expansion slots per request (expansion_slots(n))
+  int* hs_count;    // [B][xslots] units of each slot's hidden state published (small-batch builder)
 };
 
 __device__ __forceinline__ float ldw(const void* p, bool bf16, size_t i) {
@@ -188,13 +442,13 @@ __device__ __forceinline__ void warp_dot_rows8(const void* rows, const void* w, 
 // last-pop state, pruned frontiers [B][n], hidden states [B][n][H] fp32, and for small batches the per-step
 // fixed-point correction accumulators [n][B][M] int64 and the hidden-state publication counters [B][n].
 struct BuildLayout {
-  size_t state, frontier, hs, acc, bytes;
+  size_t state, frontier, hs, acc, hs_count, bytes;
 };
 
-// Words between two correction accumulators: one 128-byte line each, so that the shares of a step (every SM adds
+// Words between two correction accumulators: one 128-byte line each, so that the shares of a wave (every SM adds
 // one to every candidate's slot) spread over the L2 slices, unless that takes more than 64 MB.
-__host__ __device__ inline int acc_stride(int B, int M, int n) {
-  return static_cast<size_t>(n) * B * M * 128u <= (64u << 20) ? 16 : 1;
+__host__ __device__ inline int acc_stride(int M, int n) {
+  return static_cast<size_t>(expansion_slots(n)) * kWaveJobs * M * 128u <= (64u << 20) ? 16 : 1;
 }
 
 inline BuildLayout build_layout(int B, int K, int V, int M, int n, int H) {
@@ -202,21 +456,20 @@ inline BuildLayout build_layout(int B, int K, int V, int M, int n, int H) {
   L.state = topm_layout(B, K, V, M).bytes;
   L.frontier = align_up(L.state + sizeof(NodeState) * static_cast<size_t>(B));
   L.hs = align_up(L.frontier + sizeof(Entry) * static_cast<size_t>(B) * n);
-  L.acc = align_up(L.hs + sizeof(float) * static_cast<size_t>(B) * n * H);
-  // per-step per-candidate accumulators [n][B][M] int64 (acc_stride words apart), then per-node publication
-  // counters [B][n] int32
-  const size_t acc_bytes =
-      B <= kSmallMaxB ? sizeof(long long) * (static_cast<size_t>(n) * B * M * acc_stride(B, M, n) +
-                                             (static_cast<size_t>(B) * n + 1) / 2)
-                      : 0;
-  L.bytes = align_up(L.acc + acc_bytes);
+  const size_t X = static_cast<size_t>(expansion_slots(n));
+  L.acc = align_up(L.hs + sizeof(float) * static_cast<size_t>(B) * X * H);
+  // small batches: per-wave per-job per-candidate accumulators [X][kWaveJobs][M] int64 (acc_stride words apart),
+  // then per-slot publication counters [B][X] int32
+  const size_t acc_bytes = B <= kSmallMaxB ? sizeof(long long) * X * kWaveJobs * M * acc_stride(M, n) : 0;
+  L.hs_count = align_up(L.acc + acc_bytes);
+  L.bytes = align_up(L.hs_count + (B <= kSmallMaxB ? sizeof(int) * static_cast<size_t>(B) * X : 0));
   return L;
 }
 
 
 // The small-batch builder (build_small.cu). Returns false when its shared-memory plan does not fit this device
 // (the caller then uses the general builder).
-bool small_builder_fits(const Params& p, int sms);
-cudaError_t launch_small_builder(const Params& p, cudaStream_t stream);
+bool small_builder_fits(const Params& p, const DeviceInfo& di);
+cudaError_t launch_small_builder(const Params& p, const DeviceInfo& di, cudaStream_t stream);
 
 }  // namespace dt

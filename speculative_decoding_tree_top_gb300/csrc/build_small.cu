@@ -1,29 +1,33 @@
-// dt_build_trees for small batches (B <= 8): every SM works on every request; no grid barrier between steps.
+// dt_build_trees for small batches (B <= 8): every SM works on every request; no grid barrier between waves.
 //
 // Method: blog.captcha.la, "Methodology — deep read" (best-first max-priority queue keyed by cumulative conditional
 // log-probability; GRU state carried along each root-to-node path; correction only on the gathered top-M rows);
 // gist.science, "Composants Clés" (only the light GRU correction and its head are recomputed per node).
 //
-// GB300 design. With one or a few requests the round is a chain of n dependent steps (pop -> GRU -> correction ->
-// softmax -> pop), so the design minimises the latency of one step, not the bytes:
+// GB300 design. With one or a few requests the round is a chain of dependent steps (pop -> GRU -> correction ->
+// softmax -> pop), so the design shortens the chain rather than the bytes:
+//   * lookahead waves. The expansion of a node (its GRU step and its children's scores) depends only on its own path,
+//     never on the pop order, so any frontier node can be expanded before it is popped. A wave expands up to k
+//     nodes of each request at once: the node that blocks the next pop, then the next unexpanded nodes in the order
+//     best-first would reach them given what is known (the frontier, plus the children of nodes already expanded but
+//     not yet popped). The pops themselves stay strictly best-first and exact: a node is popped only from the true
+//     frontier, and its children join it only when it is popped. A wrong guess costs an unused expansion, never a
+//     different tree; the outputs are bit-identical for every k. The trees of the drafting workloads are wide and
+//     shallow, so k = 8 turns 16 dependent steps into 3 to 5 waves;
 //   * weight-stationary: CTA j of the G = min(#SMs, H) CTAs owns hidden units [j*H/G, (j+1)*H/G) and keeps the
 //     3 gate rows of W_ih and W_hh of those units in shared memory for the whole launch (9.4 MB of GRU weights
 //     spread over 152 SMs: ~62 KB each at E=2560, H=512), plus the same units' columns of W_c for every candidate
 //     of every position, the candidate ids and base logits (gathered once at launch);
-//   * per step each CTA runs its slice of the GRU for the popped node (K-split over 512 threads: each thread reads its
-//     slice of the input once and applies it to all gate rows; a recursive-halving shuffle reduce-scatter finishes
-//     the sums), then its units' share of every candidate's correction W_c[id]·h;
-//   * that share goes into a per-step, per-candidate 64-bit accumulator as ((fixed-point value << 8) + 1): integer
-//     addition is associative (the reduction over CTAs is exact and bit-identical run to run) and never carries into
-//     the low byte, which therefore counts the contributions. A CTA knows the correction of candidate m is complete
-//     when that count reaches G: the slot is its own barrier, so there is no grid barrier between steps;
-//   * every CTA then finishes the step for every request: corrected logits, restricted log-softmax (one warp), merge
-//     of the children into the frontier kept in shared memory (rank by counting spread over the CTA, pruned to the
-//     n - s that can still be popped), pop. All CTAs reach the same pop, so nothing needs publishing; CTA 0 writes the
-//     outputs. The embedding row of the popped token is fetched with cp.async as soon as the pop is known;
-//   * the new node's hidden state, written unit by unit by all CTAs, is published unit by unit with release
-//     reductions on a counter and pulled into every CTA's shared-memory cache with cp.async, off the critical path;
-//   * the embedding rows of all candidates are prefetched into L2 at launch.
+//   * per wave each CTA runs its slice of the GRU for every job (one warp per gate row, all jobs against the row at
+//     once), publishes its units of each new hidden state, then adds its units' share of every candidate's
+//     correction W_c[id]·h into a per-wave, per-job, per-candidate 64-bit accumulator as ((fixed-point value << 8)
+//     + 1): integer addition is associative (the reduction over CTAs is exact and bit-identical run to run) and never
+//     carries into the low byte, which therefore counts the contributions. A CTA knows a candidate's correction is
+//     complete when that count reaches G: the slot is its own barrier;
+//   * every CTA then finishes the wave redundantly: corrected logits, restricted log-softmax and the ranked children
+//     list of every job, then one warp per request pops (merging a popped node's children into the frontier, pruned
+//     to what can still be popped) and picks the next wave's jobs. All CTAs reach the same decisions, so nothing is
+//     exchanged but the hidden states and the correction sums; CTA 0 writes the outputs at the end.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -39,22 +43,14 @@ constexpr int kWarps = kThreads / 32;
 constexpr uint64_t kCopyBudgetNs = 4000000000ull;  // the weight copies take microseconds: this stops a lost one
 constexpr int kMaxRows = 16;  // gate rows per CTA, one warp each (3 * units <= 16 warps)
 constexpr int kRowPad = 8;    // elements of padding per shared-memory weight row (16 bytes)
-
-struct ReqState {  // a request's frontier bookkeeping, replicated in every CTA
-  int fcount;
-  int seq_next;
-  int token;   // the node popped last
-  int parent;
-  int depth;
-  int expand;
-  float score;
-  int pad;
-};
+constexpr int kJ = kWaveJobs;
+static_assert(kJ == 8, "a wave's jobs are the n8 tile of the GRU MMA");
 
 // Shared-memory plan of one CTA (identical on host and device).
 struct Plan {
-  int G, umax, R;
-  size_t wih, whh, bias, wc, xe, xh, req, fr, scr, z, hb, gates, ids, vals, par, hc, bytes;
+  int G, umax, R, kmax;
+  size_t wih, whh, bias, wc, ids, vals, xe, xh, gates, hb, z, kraw, kkey, red, jobs, ctl, lanes, merged, kids, kcount,
+      popidx, sdepth, pops, bytes;
 };
 
 __host__ __device__ inline size_t take(size_t& o, size_t bytes) {
@@ -68,23 +64,32 @@ __host__ __device__ inline Plan make_plan(int B, int M, int n, int max_depth, in
   P.G = G;
   P.umax = (H + G - 1) / G;
   P.R = 3 * P.umax;
+  P.kmax = M < n ? M : n;  // children kept per expanded node: at most n can ever be popped
+  const size_t X = static_cast<size_t>(expansion_slots(n));
   size_t o = 0;
   P.wih = take(o, static_cast<size_t>(esize) * P.R * (E + kRowPad));
   P.whh = take(o, static_cast<size_t>(esize) * P.R * (H + kRowPad));
   P.bias = take(o, sizeof(float) * 2 * P.R);
   P.wc = take(o, static_cast<size_t>(esize) * B * max_depth * M * P.umax);
-  P.xe = take(o, static_cast<size_t>(esize) * B * E);  // embedding row of each request's popped token, as stored
-  P.xh = take(o, sizeof(float) * H);                   // parent hidden state of the request being stepped
-  P.req = take(o, sizeof(ReqState) * B);
-  P.fr = take(o, sizeof(Entry) * B * n);
-  P.scr = take(o, sizeof(Entry) * 2 * (n + M));
-  P.z = take(o, sizeof(float) * M);
-  P.hb = take(o, sizeof(float) * P.umax);
-  P.gates = take(o, sizeof(float) * 2 * P.R);
   P.ids = take(o, sizeof(int) * B * max_depth * M);
   P.vals = take(o, sizeof(float) * B * max_depth * M);
-  P.par = take(o, sizeof(short) * B * n);
-  P.hc = take(o, sizeof(float) * B * n * H);
+  P.xe = take(o, static_cast<size_t>(esize) * kJ * (E + kRowPad));  // embedding rows of the wave's jobs, as stored
+  P.xh = take(o, sizeof(float) * kJ * H);                          // their parents' hidden states
+  P.gates = take(o, sizeof(float) * kJ * P.R * 2);
+  P.hb = take(o, sizeof(float) * kJ * P.umax);
+  P.z = take(o, sizeof(float) * kJ * M);
+  P.kraw = take(o, sizeof(Node) * kJ * M);
+  P.kkey = take(o, sizeof(unsigned long long) * kJ * M);
+  P.red = take(o, sizeof(float) * kWarps * 2 * kMaxRows * kJ);  // per-warp partial GRU tiles (tensor-core path)
+  P.jobs = take(o, sizeof(Job) * kJ);
+  P.ctl = take(o, sizeof(ReqCtl) * B);
+  P.lanes = take(o, sizeof(LaneSrc) * B * 32);
+  P.merged = take(o, sizeof(Node) * B * 2 * n);
+  P.kids = take(o, sizeof(Node) * B * X * P.kmax);
+  P.kcount = take(o, sizeof(int) * B * X);
+  P.popidx = take(o, sizeof(int) * B * X);
+  P.sdepth = take(o, sizeof(int) * B * X);
+  P.pops = take(o, sizeof(PopRec) * B * n);
   P.bytes = o;
   return P;
 }
@@ -98,37 +103,10 @@ struct WT {
   }
 };
 
-// Asynchronous global -> shared copy of `bytes` (a multiple of 16, both ends 16-byte aligned), L2 only.
-__device__ __forceinline__ void copy16_async(void* dst, const void* src, size_t bytes) {
-  for (size_t i = threadIdx.x; i < bytes / 16; i += kThreads) {
-    const unsigned d = static_cast<unsigned>(__cvta_generic_to_shared(static_cast<char*>(dst) + 16 * i));
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(static_cast<const char*>(src) + 16 * i)
-                 : "memory");
-  }
-}
-
 __device__ __forceinline__ long long ld_relaxed_s64(const long long* p) {
   long long v;
   asm volatile("ld.relaxed.gpu.global.s64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
-}
-
-// Polls until `pred(load())` holds, within the launch's time budget; false (and the abort word raised) when the
-// budget runs out or another CTA already gave up.
-template <typename Load, typename Pred>
-__device__ __forceinline__ bool poll(const Params& p, Load load, Pred pred) {
-  if (pred(load())) return true;
-  const uint64_t t0 = global_timer_ns();
-  unsigned polls = 0;
-  while (true) {
-    if (pred(load())) return true;
-    if ((++polls & 15u) == 0u &&
-        (ld_acquire_gpu(&p.hdr->abort) != 0u || global_timer_ns() - t0 > p.timeout_ns || p.timeout_ns == 0)) {
-      record_error(p.hdr, DT_ERR_TIMEOUT);
-      atomicExch(&p.hdr->abort, 1u);
-      return false;
-    }
-  }
 }
 
 // Correction accumulators: every CTA adds (round(v * 2^32) << 8) + 1 to the slot of each candidate. The upper 56
@@ -146,6 +124,30 @@ __device__ __forceinline__ void add_share(const Params& p, long long* slot, floa
   atomicAdd(reinterpret_cast<unsigned long long*>(slot), c);
 }
 
+// Sibling order as one 64-bit key (larger first): score, then lower token. Ties of both (only with repeated ids
+// among a row's candidates) fall to the lower candidate index, as in the pop order.
+__device__ __forceinline__ unsigned long long sibling_key(const Node& e) {
+  return (static_cast<unsigned long long>(key_of_f32(__float_as_uint(e.score))) << 32) |
+         static_cast<unsigned long long>(~static_cast<uint32_t>(e.token));
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// fp32 pair -> bf16x2 high part and bf16x2 remainder (x = hi + lo to 2^-16 relative)
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
+  const __nv_bfloat16 l0 = __float2bfloat16_rn(x0 - __bfloat162float(h0));
+  const __nv_bfloat16 l1 = __float2bfloat16_rn(x1 - __bfloat162float(h1));
+  hi = static_cast<uint32_t>(__bfloat16_as_ushort(h0)) | (static_cast<uint32_t>(__bfloat16_as_ushort(h1)) << 16);
+  lo = static_cast<uint32_t>(__bfloat16_as_ushort(l0)) | (static_cast<uint32_t>(__bfloat16_as_ushort(l1)) << 16);
+}
+
 template <bool kBf16>
 __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
   using T = typename WT<kBf16>::T;
@@ -154,37 +156,45 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
   T* whh = reinterpret_cast<T*>(smem + P.whh);               // [R][H + pad]
   float* bias = reinterpret_cast<float*>(smem + P.bias);     // [R][2]: b_ih, b_hh
   T* wc = reinterpret_cast<T*>(smem + P.wc);                 // [B][max_depth][M][umax]
-  T* xe = reinterpret_cast<T*>(smem + P.xe);                 // [B][E]
-  float* xh = reinterpret_cast<float*>(smem + P.xh);         // [H]
-  ReqState* rs = reinterpret_cast<ReqState*>(smem + P.req);  // [B]
-  Entry* fr = reinterpret_cast<Entry*>(smem + P.fr);         // [B][n]
-  Entry* cand = reinterpret_cast<Entry*>(smem + P.scr);      // [n + M]
-  Entry* sorted = cand + (p.n + p.M);                        // [n + M]
-  float* z = reinterpret_cast<float*>(smem + P.z);           // [M]
-  float* hb = reinterpret_cast<float*>(smem + P.hb);         // [umax]: the new hidden state of the owned units
-  float* gates = reinterpret_cast<float*>(smem + P.gates);   // [R][2]: input side, hidden side
   int* ids_s = reinterpret_cast<int*>(smem + P.ids);         // [B][max_depth][M] candidate ids (range-checked)
   float* vals_s = reinterpret_cast<float*>(smem + P.vals);   // [B][max_depth][M] candidate base logits
-  short* par_s = reinterpret_cast<short*>(smem + P.par);     // [B][n]: parent of every popped node
-  float* hc = reinterpret_cast<float*>(smem + P.hc);         // [B][n][H]: hidden state of every expanded node
-  __shared__ int s_flag;
+  T* xe = reinterpret_cast<T*>(smem + P.xe);                 // [kJ][E + pad]
+  float* xh = reinterpret_cast<float*>(smem + P.xh);         // [kJ][H]
+  float* gates = reinterpret_cast<float*>(smem + P.gates);   // [kJ][R][2]: input side, hidden side
+  float* hb = reinterpret_cast<float*>(smem + P.hb);         // [kJ][umax]: the jobs' new owned units
+  float* z = reinterpret_cast<float*>(smem + P.z);           // [kJ][M]
+  Node* kraw = reinterpret_cast<Node*>(smem + P.kraw);       // [kJ][M] children, unsorted
+  unsigned long long* kkey = reinterpret_cast<unsigned long long*>(smem + P.kkey);  // [kJ][M] their sibling keys
+  float* red = reinterpret_cast<float*>(smem + P.red);       // [kWarps][2][16 rows][kJ jobs]
+  Job* jobs = reinterpret_cast<Job*>(smem + P.jobs);         // [kJ]
+  ReqCtl* ctl = reinterpret_cast<ReqCtl*>(smem + P.ctl);     // [B]
+  LaneSrc* lanes = reinterpret_cast<LaneSrc*>(smem + P.lanes);  // [B][32]
+  Node* merged = reinterpret_cast<Node*>(smem + P.merged);   // [B][2][n]
+  Node* kids = reinterpret_cast<Node*>(smem + P.kids);       // [B][X][kmax] ranked children of each slot
+  int* kcount = reinterpret_cast<int*>(smem + P.kcount);     // [B][X]
+  int* popidx = reinterpret_cast<int*>(smem + P.popidx);     // [B][X] pop index of the slot's node (-1 root, -2 not yet)
+  int* sdepth = reinterpret_cast<int*>(smem + P.sdepth);     // [B][X] depth of the slot's node
+  PopRec* pops = reinterpret_cast<PopRec*>(smem + P.pops);   // [B][n]
+  __shared__ int s_flag, s_J;
   __shared__ uint64_t wbar;  // completion of the weight rows' bulk copies
+  __shared__ uint64_t jbar;  // completion of a wave's input copies (embedding rows, parents' states)
 
   const int B = p.B, K = p.K, M = p.M, n = p.n, H = p.H, E = p.E, maxd = p.max_depth;
-  const int G = P.G, umax = P.umax;
+  const int G = P.G, umax = P.umax, KM = P.kmax, X = p.xslots;
+  const int kla = p.lookahead;
   const int j = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int u0 = static_cast<int>((static_cast<long long>(j) * H) / G);
   const int nu = static_cast<int>((static_cast<long long>(j + 1) * H) / G) - u0;
   const size_t esize = kBf16 ? 2 : 4;
   const int AS = p.acc_stride;
-  int* hs_count = reinterpret_cast<int*>(p.acc + static_cast<size_t>(n) * B * M * AS);  // [B][n]
+  const int SE = E + kRowPad, SH = H + kRowPad;  // shared-memory row strides of W_ih / xe and of W_hh
 
   // ---- launch: weights of the owned units, W_c columns / ids / base logits of the candidates, L2 prefetch ----
-  const int SE = E + kRowPad, SH = H + kRowPad;  // shared-memory row strides of W_ih and W_hh
   // The 3 * nu rows of W_ih and of W_hh as bulk copies (1 to 8 KB each) completing on one mbarrier, issued by warp 0;
-  // waited for at the top of the first step.
+  // waited for before the first GRU step.
   if (t == 0) {
     mbar_init(&wbar, 1);
+    mbar_init(&jbar, 1);
     mbar_fence_init();
   }
   __syncthreads();
@@ -203,11 +213,8 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
                  static_cast<unsigned>(esize * E), &wbar);
     }
   }
-  // A return before the first step leaves no copy in flight: this waits (bounded) for the weights.
-  auto drain = [&]() {
-    asm volatile("cp.async.wait_all;" ::: "memory");
-    mbar_wait(&wbar, 0, kCopyBudgetNs);
-  };
+  // A return before the first GRU step leaves no copy in flight: this waits (bounded) for the weights.
+  auto drain = [&]() { mbar_wait(&wbar, 0, kCopyBudgetNs); };
   for (int i = t; i < 3 * umax; i += kThreads) {
     const int g = i / umax, u = i % umax;
     const size_t row = static_cast<size_t>(g) * H + u0 + u;
@@ -243,267 +250,383 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
       }
     }
   }
-  // every step's accumulators and the hidden-state counters start at zero; one grid barrier orders that
-  const size_t zero_words = static_cast<size_t>(n) * B * M * AS + (static_cast<size_t>(B) * n + 1) / 2;
-  for (size_t i = static_cast<size_t>(j) * kThreads + t; i < zero_words; i += static_cast<size_t>(G) * kThreads)
-    p.acc[i] = 0;
-  for (int b = t; b < B; b += kThreads) rs[b] = ReqState{};
+  // every wave's accumulators and the slots' publication counters start at zero; one grid barrier orders that
+  {
+    const size_t acc_words = static_cast<size_t>(X) * kJ * M * AS;
+    for (size_t i = static_cast<size_t>(j) * kThreads + t; i < acc_words; i += static_cast<size_t>(G) * kThreads)
+      p.acc[i] = 0;
+    for (size_t i = static_cast<size_t>(j) * kThreads + t; i < static_cast<size_t>(B) * X;
+         i += static_cast<size_t>(G) * kThreads)
+      p.hs_count[i] = 0;
+  }
+  // control state, identical in every CTA: the root of every request is expanded in wave 0
+  for (int b = t; b < B; b += kThreads) {
+    ctl[b] = ReqCtl{0, 0, M, 1, 0, {0, 0, 0}};  // the root's children take insertion indices 0 .. M - 1
+    jobs[b] = Job{b, 0, -1, 0, 0, 0.f, {0, 0}};
+  }
+  for (int i = t; i < B * n; i += kThreads) pops[i] = PopRec{0, -1, 0, -INFINITY};
+  for (int i = t; i < B * 32; i += kThreads) {  // lane 0: the merged list (empty), lane 1: the root's children
+    const int l = i % 32;
+    lanes[i] = l == 0 ? LaneSrc{-2, 0, 0, 0} : l == 1 ? LaneSrc{0, 0, -1, 0} : LaneSrc{-1, 0, 0, 0};
+  }
+  for (int i = t; i < B * X; i += kThreads) {
+    kcount[i] = 0;
+    popidx[i] = (i % X) == 0 ? -1 : -2;
+    sdepth[i] = 0;
+  }
+  if (t == 0) s_J = B;
   if (!grid_barrier(p.hdr, G, p.timeout_ns, &s_flag)) {
     drain();
     return;
   }
-
   if (!mbar_wait(&wbar, 0, kCopyBudgetNs)) record_error(p.hdr, DT_ERR_TIMEOUT);  // the weight rows (bounded)
-  for (int s = 0; s < n; ++s) {
-    asm volatile("cp.async.wait_all;" ::: "memory");  // this thread's cache and embedding copies
-    __syncthreads();                                   // ... and everyone else's
-    long long* acc_s = p.acc + static_cast<size_t>(s) * B * M * AS;
 
-    // ---- phase A: this CTA's share of the GRU and of the correction of every expanding request ----
-    for (int b = 0; b < B; ++b) {
-      const bool root = s == 0;
-      if (!root && !rs[b].expand) continue;  // uniform across the CTA (replicated state)
-      const int pos = root ? 0 : rs[b].depth;
-      if (root) {
-        for (int u = t; u < nu; u += kThreads) hb[u] = __ldg(p.h0 + static_cast<size_t>(b) * H + u0 + u);
-      } else {
-        const int par = rs[b].parent;
-        const float* xhp = xh;  // the parent's hidden state: the cached copy, or h0 staged for a child of the root
-        if (par < 0) {
-          for (int k = t; k < H / 4; k += kThreads)
-            reinterpret_cast<float4*>(xh)[k] =
-                __ldg(reinterpret_cast<const float4*>(p.h0 + static_cast<size_t>(b) * H) + k);
-          __syncthreads();
-        } else {
-          xhp = hc + (static_cast<size_t>(b) * n + par) * H;
+  for (int w = 0;; ++w) {
+    __syncthreads();
+    const int J = s_J;
+    if (J == 0) break;
+    // the jobs' inputs, copied at the end of the previous wave (wave 0 expands the roots and reads none)
+    if (w > 0 && !mbar_wait(&jbar, (w - 1) & 1, kCopyBudgetNs)) {
+      record_error(p.hdr, DT_ERR_TIMEOUT);
+      atomicExch(&p.hdr->abort, 1u);
+      return;
+    }
+    long long* acc_w = p.acc + static_cast<size_t>(w) * kJ * M * AS;
+    const bool roots = w == 0;  // wave 0 expands the roots (h = h0, no GRU step); later waves never do
+
+    // ---- phase A: this CTA's units of every job's GRU step, then its share of every job's correction ----
+    const bool mma = kBf16 && E % 16 == 0 && H % 16 == 0;  // the tensor-core GRU (else the CUDA-core one below)
+    if (!roots && mma) {
+      // Tensor cores, mma.sync m16n8k16 (bf16 in, fp32 accumulate): D[16 gate rows][8 jobs] = W[rows][K] X[K][jobs],
+      // the warps splitting the k16 steps. A = this CTA's gate rows (rows past R repeat row R - 1: their outputs are
+      // not used), B = the jobs' embedding rows (input side) and the parents' fp32 states as bf16 hi + lo pairs
+      // (hidden side); each side has its own accumulator, the n gate needs them apart. A job's column never mixes
+      // with another's, so its sums do not depend on which jobs share the wave.
+      const int g = lane >> 2, tg = lane & 3, R = 3 * umax;
+      float din[4] = {0.f, 0.f, 0.f, 0.f}, dh[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const unsigned short* a_lo = reinterpret_cast<const unsigned short*>(wih) + static_cast<size_t>(min(g, R - 1)) * SE;
+        const unsigned short* a_hi = reinterpret_cast<const unsigned short*>(wih) + static_cast<size_t>(min(g + 8, R - 1)) * SE;
+        const unsigned short* bx = reinterpret_cast<const unsigned short*>(xe) + static_cast<size_t>(g) * SE;
+#pragma unroll 2
+        for (int ks = warp; ks < E / 16; ks += kWarps) {
+          const int k = ks * 16 + tg * 2;
+          mma_bf16_16816(din, *reinterpret_cast<const uint32_t*>(a_lo + k), *reinterpret_cast<const uint32_t*>(a_hi + k),
+                         *reinterpret_cast<const uint32_t*>(a_lo + k + 8), *reinterpret_cast<const uint32_t*>(a_hi + k + 8),
+                         *reinterpret_cast<const uint32_t*>(bx + k), *reinterpret_cast<const uint32_t*>(bx + k + 8));
         }
-        const T* xeb = xe + static_cast<size_t>(b) * E;
-        const int R = 3 * umax;
-        if (warp < R) {
-          // One warp per gate row (R <= 16 rows, 16 warps): the lanes stride over K with four independent
-          // accumulators per side, then one shuffle tree per side. The row's input side (over E) and hidden side
-          // (over H) stay apart: the n gate needs them separately.
-          const int r = warp;
-          constexpr int kPer = kBf16 ? 8 : 4;
-          float ai[4] = {0.f, 0.f, 0.f, 0.f}, ah[4] = {0.f, 0.f, 0.f, 0.f};
-          const T* wr = wih + static_cast<size_t>(r) * SE;
-#pragma unroll 4
-          for (int f = lane; f < E / kPer; f += 32) {
-            const int c = f * kPer;
-            if (kBf16) {
-              const uint4 w = *reinterpret_cast<const uint4*>(wr + c), q = *reinterpret_cast<const uint4*>(xeb + c);
-              ai[0] = fmaf(__uint_as_float(w.x << 16), __uint_as_float(q.x << 16), ai[0]);
-              ai[1] = fmaf(__uint_as_float(w.x & 0xFFFF0000u), __uint_as_float(q.x & 0xFFFF0000u), ai[1]);
-              ai[2] = fmaf(__uint_as_float(w.y << 16), __uint_as_float(q.y << 16), ai[2]);
-              ai[3] = fmaf(__uint_as_float(w.y & 0xFFFF0000u), __uint_as_float(q.y & 0xFFFF0000u), ai[3]);
-              ai[0] = fmaf(__uint_as_float(w.z << 16), __uint_as_float(q.z << 16), ai[0]);
-              ai[1] = fmaf(__uint_as_float(w.z & 0xFFFF0000u), __uint_as_float(q.z & 0xFFFF0000u), ai[1]);
-              ai[2] = fmaf(__uint_as_float(w.w << 16), __uint_as_float(q.w << 16), ai[2]);
-              ai[3] = fmaf(__uint_as_float(w.w & 0xFFFF0000u), __uint_as_float(q.w & 0xFFFF0000u), ai[3]);
-            } else {
-              const float4 w = *reinterpret_cast<const float4*>(wr + c), q = *reinterpret_cast<const float4*>(xeb + c);
-              ai[0] = fmaf(w.x, q.x, ai[0]);
-              ai[1] = fmaf(w.y, q.y, ai[1]);
-              ai[2] = fmaf(w.z, q.z, ai[2]);
-              ai[3] = fmaf(w.w, q.w, ai[3]);
-            }
-          }
-          const T* hr = whh + static_cast<size_t>(r) * SH;
-#pragma unroll 4
-          for (int f = lane; f < H / kPer; f += 32) {
-            const int c = f * kPer;
-            const float4 x0 = *reinterpret_cast<const float4*>(xhp + c);
-            if (kBf16) {
-              const float4 x1 = *reinterpret_cast<const float4*>(xhp + c + 4);
-              const uint4 w = *reinterpret_cast<const uint4*>(hr + c);
-              ah[0] = fmaf(__uint_as_float(w.x << 16), x0.x, ah[0]);
-              ah[1] = fmaf(__uint_as_float(w.x & 0xFFFF0000u), x0.y, ah[1]);
-              ah[2] = fmaf(__uint_as_float(w.y << 16), x0.z, ah[2]);
-              ah[3] = fmaf(__uint_as_float(w.y & 0xFFFF0000u), x0.w, ah[3]);
-              ah[0] = fmaf(__uint_as_float(w.z << 16), x1.x, ah[0]);
-              ah[1] = fmaf(__uint_as_float(w.z & 0xFFFF0000u), x1.y, ah[1]);
-              ah[2] = fmaf(__uint_as_float(w.w << 16), x1.z, ah[2]);
-              ah[3] = fmaf(__uint_as_float(w.w & 0xFFFF0000u), x1.w, ah[3]);
-            } else {
-              const float4 w = *reinterpret_cast<const float4*>(hr + c);
-              ah[0] = fmaf(w.x, x0.x, ah[0]);
-              ah[1] = fmaf(w.y, x0.y, ah[1]);
-              ah[2] = fmaf(w.z, x0.z, ah[2]);
-              ah[3] = fmaf(w.w, x0.w, ah[3]);
-            }
-          }
-          float si = (ai[0] + ai[1]) + (ai[2] + ai[3]), sh = (ah[0] + ah[1]) + (ah[2] + ah[3]);
+      }
+      {
+        const unsigned short* a_lo = reinterpret_cast<const unsigned short*>(whh) + static_cast<size_t>(min(g, R - 1)) * SH;
+        const unsigned short* a_hi = reinterpret_cast<const unsigned short*>(whh) + static_cast<size_t>(min(g + 8, R - 1)) * SH;
+        const float* bh = xh + static_cast<size_t>(g) * H;
+        for (int ks = warp; ks < H / 16; ks += kWarps) {
+          const int k = ks * 16 + tg * 2;
+          const uint32_t a0 = *reinterpret_cast<const uint32_t*>(a_lo + k), a1 = *reinterpret_cast<const uint32_t*>(a_hi + k);
+          const uint32_t a2 = *reinterpret_cast<const uint32_t*>(a_lo + k + 8), a3 = *reinterpret_cast<const uint32_t*>(a_hi + k + 8);
+          const float2 x0 = *reinterpret_cast<const float2*>(bh + k), x1 = *reinterpret_cast<const float2*>(bh + k + 8);
+          uint32_t h0, l0, h1, l1;
+          split_bf16x2(x0.x, x0.y, h0, l0);
+          split_bf16x2(x1.x, x1.y, h1, l1);
+          mma_bf16_16816(dh, a0, a1, a2, a3, h0, h1);
+          mma_bf16_16816(dh, a0, a1, a2, a3, l0, l1);
+        }
+      }
+      // this warp's partial tiles: the thread holds rows g, g + 8 and job columns 2 tg, 2 tg + 1
+      float* rw = red + warp * 2 * kMaxRows * kJ;
+      *reinterpret_cast<float2*>(rw + g * kJ + 2 * tg) = make_float2(din[0], din[1]);
+      *reinterpret_cast<float2*>(rw + (g + 8) * kJ + 2 * tg) = make_float2(din[2], din[3]);
+      *reinterpret_cast<float2*>(rw + (kMaxRows + g) * kJ + 2 * tg) = make_float2(dh[0], dh[1]);
+      *reinterpret_cast<float2*>(rw + (kMaxRows + g + 8) * kJ + 2 * tg) = make_float2(dh[2], dh[3]);
+    }
+    if (!roots && !mma && warp < 3 * umax) {
+      // One warp per gate row (R <= 16 rows, 16 warps), every job against the row: the lanes stride over K, one
+      // accumulator per job and side, then one shuffle tree each. A job's sums do not depend on the other jobs.
+      // The row's input side (over E) and hidden side (over H) stay apart: the n gate needs them separately.
+      const int r = warp;
+      constexpr int kPer = kBf16 ? 8 : 4;
+      float ai[kJ], ah[kJ];
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            si += __shfl_xor_sync(0xFFFFFFFFu, si, o);
-            sh += __shfl_xor_sync(0xFFFFFFFFu, sh, o);
+      for (int q = 0; q < kJ; ++q) ai[q] = ah[q] = 0.f;
+      const T* wr = wih + static_cast<size_t>(r) * SE;
+      for (int f = lane; f < E / kPer; f += 32) {
+        const int c = f * kPer;
+        if (kBf16) {
+          const uint4 wv = *reinterpret_cast<const uint4*>(wr + c);
+          const float w0 = __uint_as_float(wv.x << 16), w1 = __uint_as_float(wv.x & 0xFFFF0000u);
+          const float w2 = __uint_as_float(wv.y << 16), w3 = __uint_as_float(wv.y & 0xFFFF0000u);
+          const float w4 = __uint_as_float(wv.z << 16), w5 = __uint_as_float(wv.z & 0xFFFF0000u);
+          const float w6 = __uint_as_float(wv.w << 16), w7 = __uint_as_float(wv.w & 0xFFFF0000u);
+#pragma unroll
+          for (int q = 0; q < kJ; ++q) {
+            if (q >= J) break;
+            const uint4 xv = *reinterpret_cast<const uint4*>(xe + static_cast<size_t>(q) * SE + c);
+            float a = ai[q];
+            a = fmaf(w0, __uint_as_float(xv.x << 16), a);
+            a = fmaf(w1, __uint_as_float(xv.x & 0xFFFF0000u), a);
+            a = fmaf(w2, __uint_as_float(xv.y << 16), a);
+            a = fmaf(w3, __uint_as_float(xv.y & 0xFFFF0000u), a);
+            a = fmaf(w4, __uint_as_float(xv.z << 16), a);
+            a = fmaf(w5, __uint_as_float(xv.z & 0xFFFF0000u), a);
+            a = fmaf(w6, __uint_as_float(xv.w << 16), a);
+            a = fmaf(w7, __uint_as_float(xv.w & 0xFFFF0000u), a);
+            ai[q] = a;
           }
-          if (lane == 0) {
-            gates[2 * r] = si;
-            gates[2 * r + 1] = sh;
+        } else {
+          const float4 wv = *reinterpret_cast<const float4*>(wr + c);
+#pragma unroll
+          for (int q = 0; q < kJ; ++q) {
+            if (q >= J) break;
+            const float4 xv = *reinterpret_cast<const float4*>(xe + static_cast<size_t>(q) * SE + c);
+            float a = ai[q];
+            a = fmaf(wv.x, xv.x, a);
+            a = fmaf(wv.y, xv.y, a);
+            a = fmaf(wv.z, xv.z, a);
+            a = fmaf(wv.w, xv.w, a);
+            ai[q] = a;
           }
-        }
-        __syncthreads();
-        for (int u = t; u < nu; u += kThreads) {
-          const int rr = u, rz = umax + u, rn = 2 * umax + u;
-          const float r = sigmoidf_(gates[2 * rr] + bias[2 * rr] + gates[2 * rr + 1] + bias[2 * rr + 1]);
-          const float zg = sigmoidf_(gates[2 * rz] + bias[2 * rz] + gates[2 * rz + 1] + bias[2 * rz + 1]);
-          const float g = tanhf(gates[2 * rn] + bias[2 * rn] + r * (gates[2 * rn + 1] + bias[2 * rn + 1]));
-          hb[u] = (1.f - zg) * g + zg * xhp[u0 + u];
         }
       }
-      __syncthreads();
-      if (!root && warp == kWarps - 1) {  // publish the new units (the last warp polls nothing in phase C)
-        for (int u = lane; u < nu; u += 32) {
-          p.hs[(static_cast<size_t>(b) * n + (s - 1)) * H + u0 + u] = hb[u];
-          // a release reduction orders the store above before the count (H units in all)
-          asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(hs_count + static_cast<size_t>(b) * n + (s - 1))
-                       : "memory");
+      const T* hr = whh + static_cast<size_t>(r) * SH;
+      for (int f = lane; f < H / kPer; f += 32) {
+        const int c = f * kPer;
+        if (kBf16) {
+          const uint4 wv = *reinterpret_cast<const uint4*>(hr + c);
+          const float w0 = __uint_as_float(wv.x << 16), w1 = __uint_as_float(wv.x & 0xFFFF0000u);
+          const float w2 = __uint_as_float(wv.y << 16), w3 = __uint_as_float(wv.y & 0xFFFF0000u);
+          const float w4 = __uint_as_float(wv.z << 16), w5 = __uint_as_float(wv.z & 0xFFFF0000u);
+          const float w6 = __uint_as_float(wv.w << 16), w7 = __uint_as_float(wv.w & 0xFFFF0000u);
+#pragma unroll
+          for (int q = 0; q < kJ; ++q) {
+            if (q >= J) break;
+            const float4 x0 = *reinterpret_cast<const float4*>(xh + static_cast<size_t>(q) * H + c);
+            const float4 x1 = *reinterpret_cast<const float4*>(xh + static_cast<size_t>(q) * H + c + 4);
+            float a = ah[q];
+            a = fmaf(w0, x0.x, a);
+            a = fmaf(w1, x0.y, a);
+            a = fmaf(w2, x0.z, a);
+            a = fmaf(w3, x0.w, a);
+            a = fmaf(w4, x1.x, a);
+            a = fmaf(w5, x1.y, a);
+            a = fmaf(w6, x1.z, a);
+            a = fmaf(w7, x1.w, a);
+            ah[q] = a;
+          }
+        } else {
+          const float4 wv = *reinterpret_cast<const float4*>(hr + c);
+#pragma unroll
+          for (int q = 0; q < kJ; ++q) {
+            if (q >= J) break;
+            const float4 xv = *reinterpret_cast<const float4*>(xh + static_cast<size_t>(q) * H + c);
+            float a = ah[q];
+            a = fmaf(wv.x, xv.x, a);
+            a = fmaf(wv.y, xv.y, a);
+            a = fmaf(wv.z, xv.z, a);
+            a = fmaf(wv.w, xv.w, a);
+            ah[q] = a;
+          }
         }
       }
-      // this CTA's units' part of W_c[id]·h for the M candidates of position pos
-      const T* wcp = wc + (static_cast<size_t>(b) * maxd + pos) * M * umax;
-      for (int m = t; m < M; m += kThreads) {
+#pragma unroll
+      for (int q = 0; q < kJ; ++q) {
+        if (q >= J) break;
+        float si = ai[q], sh = ah[q];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          si += __shfl_xor_sync(0xFFFFFFFFu, si, o);
+          sh += __shfl_xor_sync(0xFFFFFFFFu, sh, o);
+        }
+        if (lane == 0) {
+          gates[(q * 3 * umax + r) * 2] = si;
+          gates[(q * 3 * umax + r) * 2 + 1] = sh;
+        }
+      }
+    }
+    __syncthreads();
+    if (!roots && mma) {  // the partial tiles summed over the warps in a fixed order
+      for (int i = t; i < 2 * 3 * umax * J; i += kThreads) {
+        const int side = i / (3 * umax * J), r = (i / J) % (3 * umax), q = i % J;
         float v = 0.f;
-        for (int u = 0; u < nu; ++u) v = fmaf(WT<kBf16>::f(wcp[static_cast<size_t>(m) * umax + u]), hb[u], v);
-        add_share(p, acc_s + (static_cast<size_t>(b) * M + m) * AS, v);
+#pragma unroll
+        for (int w2 = 0; w2 < kWarps; ++w2) v += red[(w2 * 2 + side) * kMaxRows * kJ + r * kJ + q];
+        gates[(q * 3 * umax + r) * 2 + side] = v;
       }
-      if (B > 1) __syncthreads();  // gates / xh are reused by the next request
+    }
+    __syncthreads();
+    // the GRU pointwise of the owned units (root jobs: h0), published unit by unit: a release reduction orders the
+    // store before the count (H units in all)
+    for (int i = t; i < J * umax; i += kThreads) {
+      const int q = i / umax, u = i % umax;
+      if (u >= nu) continue;
+      const Job jb = jobs[q];
+      float hn;
+      if (roots) {
+        hn = __ldg(p.h0 + static_cast<size_t>(jb.b) * H + u0 + u);
+      } else {
+        const float* gq = gates + q * 3 * umax * 2;
+        const int rr = u, rz = umax + u, rn = 2 * umax + u;
+        const float r = sigmoidf_(gq[2 * rr] + bias[2 * rr] + gq[2 * rr + 1] + bias[2 * rr + 1]);
+        const float zg = sigmoidf_(gq[2 * rz] + bias[2 * rz] + gq[2 * rz + 1] + bias[2 * rz + 1]);
+        const float g = tanhf(gq[2 * rn] + bias[2 * rn] + r * (gq[2 * rn + 1] + bias[2 * rn + 1]));
+        hn = (1.f - zg) * g + zg * xh[static_cast<size_t>(q) * H + u0 + u];
+      }
+      hb[q * umax + u] = hn;
+      const size_t slot = static_cast<size_t>(jb.b) * X + jb.xslot;
+      p.hs[slot * H + u0 + u] = hn;
+      asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p.hs_count + slot) : "memory");
+    }
+    __syncthreads();
+    // this CTA's units' part of W_c[id]·h for the M candidates of each job's block position
+    for (int i = t; i < J * M; i += kThreads) {
+      const int q = i / M, m = i % M;
+      const Job jb = jobs[q];
+      const T* wcp = wc + ((static_cast<size_t>(jb.b) * maxd + jb.depth) * M + m) * umax;
+      float v = 0.f;
+      for (int u = 0; u < nu; ++u) v = fmaf(WT<kBf16>::f(wcp[u]), hb[q * umax + u], v);
+      add_share(p, acc_w + (static_cast<size_t>(q) * M + m) * AS, v);
     }
 
-    // ---- phase C: every CTA finishes the step for every request (the whole CTA on one request at a time) ----
-    for (int b = 0; b < B; ++b) {
-      const ReqState st = rs[b];
-      const int F = st.fcount;
-      const bool expanded = s == 0 || st.expand;
-      const int C = expanded ? M : 0;
-      const int pos = s == 0 ? 0 : st.depth;
-      const size_t off = (static_cast<size_t>(b) * maxd + pos) * M;  // into the staged ids / base logits
-      for (int i = t; i < F; i += kThreads) cand[i] = fr[static_cast<size_t>(b) * n + i];
-      int ok = 1;
-      if (expanded && warp == 0) {
-        // All G shares of every candidate: each lane polls its slots (each on its own cache line) until all are
-        // complete, every slot read of a round in flight together, then takes the corrected logits.
-        auto complete = [&](long long v) { return (v & 0xFF) == (G & 0xFF); };
-        const long long* slots = acc_s + static_cast<size_t>(b) * M * AS;
-        float mx = -INFINITY;
-        for (int m0 = lane; m0 < M; m0 += 128) {
-          long long a[4];
-          bool done = false;
-          const uint64_t t0 = global_timer_ns();
-          for (unsigned polls = 0; !done; ++polls) {
-            done = true;
+    // ---- phase C: every CTA finishes the wave (replicated) ----
+    // (1) one warp per job: all G shares of every candidate (each lane polls its slots, every read of a round in
+    //     flight together) and the job's published hidden state, then the restricted log-softmax and the children
+    int ok = 1;
+    if (warp < J) {
+      const int q = warp;
+      const Job jb = jobs[q];
+      const size_t off = (static_cast<size_t>(jb.b) * maxd + jb.depth) * M;  // staged ids / base logits
+      auto complete = [&](long long v) { return (v & 0xFF) == (G & 0xFF); };
+      const long long* slots = acc_w + static_cast<size_t>(q) * M * AS;
+      const unsigned* hcnt = reinterpret_cast<const unsigned*>(p.hs_count) + static_cast<size_t>(jb.b) * X + jb.xslot;
+      float mx = -INFINITY;
+      for (int m0 = lane; m0 < M; m0 += 128) {
+        long long a[4];
+        bool done = false;
+        const uint64_t t0 = global_timer_ns();
+        for (unsigned polls = 0; !done; ++polls) {
+          done = true;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int m = m0 + 32 * j;
-              a[j] = m < M ? ld_relaxed_s64(slots + static_cast<size_t>(m) * AS) : static_cast<long long>(G & 0xFF);
-              done &= complete(a[j]);
-            }
-            if (!done && (polls & 15u) == 15u &&
-                (ld_acquire_gpu(&p.hdr->abort) != 0u || global_timer_ns() - t0 > p.timeout_ns)) {
-              record_error(p.hdr, DT_ERR_TIMEOUT);
-              atomicExch(&p.hdr->abort, 1u);
-              ok = 0;
-              break;
-            }
+          for (int jj = 0; jj < 4; ++jj) {
+            const int m = m0 + 32 * jj;
+            a[jj] = m < M ? ld_relaxed_s64(slots + static_cast<size_t>(m) * AS) : static_cast<long long>(G & 0xFF);
+            done &= complete(a[jj]);
           }
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int m = m0 + 32 * j;
-            if (m >= M) break;
-            const float v = (vals_s[off + m] + __ll2float_rn(a[j] >> 8) * kUnfix) / p.T_eff;
-            z[m] = v;
-            mx = fmaxf(mx, v);
+          if (lane == 0 && m0 == 0) done &= ld_acquire_gpu(hcnt) >= static_cast<unsigned>(H);
+          if (!done && (polls & 15u) == 15u &&
+              (ld_acquire_gpu(&p.hdr->abort) != 0u || global_timer_ns() - t0 > p.timeout_ns)) {
+            record_error(p.hdr, DT_ERR_TIMEOUT);
+            atomicExch(&p.hdr->abort, 1u);
+            ok = 0;
+            break;
           }
         }
-        ok = __all_sync(0xFFFFFFFFu, ok);
-        // restricted log-softmax of this node's children, in the warp
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-        float sum = 0.f;
-        for (int m = lane; m < M; m += 32) sum += expf(z[m] - mx);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-        const float lse = logf(sum);
-        const float base_score = s == 0 ? 0.f : st.score;
-        for (int m = lane; m < M; m += 32) {
-          Entry e;
-          e.score = base_score + ((z[m] - mx) - lse);
-          e.token = ids_s[off + m];
-          e.parent = static_cast<short>(s == 0 ? -1 : s - 1);
-          e.depth = static_cast<short>(pos + 1);
-          e.seq = st.seq_next + m;
-          cand[F + m] = e;
+        for (int jj = 0; jj < 4; ++jj) {
+          const int m = m0 + 32 * jj;
+          if (m >= M) break;
+          const float v = (vals_s[off + m] + __ll2float_rn(a[jj] >> 8) * kUnfix) / p.T_eff;
+          z[q * M + m] = v;
+          mx = fmaxf(mx, v);
         }
       }
-      if (expanded && s > 0 && warp == kWarps - 1) {
-        // the expanded node's full hidden state (published unit by unit by every CTA) into this CTA's cache,
-        // asynchronously (waited for at the next step)
-        const int* cnt = hs_count + static_cast<size_t>(b) * n + (s - 1);
-        if (lane == 0)
-          ok &= poll(p, [&] { return static_cast<long long>(ld_acquire_gpu(reinterpret_cast<const unsigned*>(cnt))); },
-                     [&](long long v) { return v >= H; });
-        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-        if (ok) {
-          const float* src = p.hs + (static_cast<size_t>(b) * n + (s - 1)) * H;
-          float* dst = hc + (static_cast<size_t>(b) * n + (s - 1)) * H;
-          for (int k = lane; k < H / 4; k += 32) {
-            const unsigned d = static_cast<unsigned>(__cvta_generic_to_shared(dst + 4 * k));
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src + 4 * k) : "memory");
+      ok = __all_sync(0xFFFFFFFFu, ok);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+      float sum = 0.f;
+      for (int m = lane; m < M; m += 32) sum += expf(z[q * M + m] - mx);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+      const float lse = logf(sum);
+      for (int m = lane; m < M; m += 32) {
+        Node e;
+        e.score = jb.score + ((z[q * M + m] - mx) - lse);
+        e.token = ids_s[off + m];
+        e.seq = m;  // the candidate index until the node is popped
+        e.pslot = static_cast<short>(jb.xslot);
+        e.xslot = -1;
+        kraw[q * M + m] = e;
+        kkey[q * M + m] = sibling_key(e);
+      }
+    }
+    if (!__syncthreads_and(ok)) return;  // a wait ran out (recorded); no copy is in flight
+    // (2) every job's children ranked among themselves by their sibling keys (tpe threads per child), the first kc
+    //     kept: at most n - s - 1 of them can still be popped after the job's node itself (n for the root's)
+    {
+      int tpe = 1;
+      while (tpe < 32 && tpe * 2 * J * M <= kThreads) tpe *= 2;
+      for (int base = 0; base < J * M * tpe; base += kThreads) {  // uniform bounds: every lane reaches the shuffles
+        const int slot = base + t, i = slot / tpe, part = slot % tpe;
+        const int q = i / M, mi = i % M;
+        int r = 0;
+        if (i < J * M) {
+          const unsigned long long ki = kkey[i];
+          const unsigned long long* sib = kkey + q * M;
+#pragma unroll 8
+          for (int c = part; c < M; c += tpe) {
+            const unsigned long long kc = sib[c];
+            r += (kc > ki) | ((kc == ki) & (c < mi));
           }
         }
-        asm volatile("cp.async.commit_group;" ::: "memory");
+        for (int o = 1; o < tpe; o <<= 1) r += __shfl_xor_sync(0xFFFFFFFFu, r, o);
+        if (i < J * M && part == 0) {
+          const Job jb = jobs[q];
+          const int rem = roots ? n : n - ctl[jb.b].s - 1;
+          const int kc = min(min(M, KM), rem);
+          if (r < kc) kids[(static_cast<size_t>(jb.b) * X + jb.xslot) * KM + r] = kraw[i];
+          if (r == 0) kcount[jb.b * X + jb.xslot] = kc;
+        }
       }
-      if (!__syncthreads_and(ok)) {  // a wait ran out (recorded): leave with no copy in flight
-        asm volatile("cp.async.wait_all;" ::: "memory");
-        return;
-      }
-      // Keep the R = n - s best (nothing ranked below them can be popped in the n - s pops left): the sorted
-      // frontier merged with the ranked children.
-      const int N = F + C;
-      const int R = min(n - s, N);
-      merge_rank<kThreads>(cand, F, C, R, sorted + n, sorted);
-      if (N == 0 && t == 0) {  // unreachable when n <= the size of the depth-limited tree (checked on the host)
+    }
+    __syncthreads();
+    // (3) one warp per request: pops, then the next wave's picks
+    if (warp < B) {
+      const int b = warp;
+      const ReqView R{ctl + b, lanes + b * 32, merged + static_cast<size_t>(b) * 2 * n,
+                      kids + static_cast<size_t>(b) * X * KM, kcount + b * X, popidx + b * X, sdepth + b * X,
+                      pops + static_cast<size_t>(b) * n};
+      request_step(R, b, n, M, maxd, X, KM, kla, jobs + b * kla, p.hdr);
+    }
+    __syncthreads();
+    // the next wave's jobs, packed in request order; their inputs (embedding rows, parents' hidden states) in flight
+    // the next wave's jobs, packed in request order, and their inputs (embedding rows, parents' hidden states) as
+    // one bulk copy each, completing on jbar; every slot a wave can use was checked against X when it was taken
+    if (t == 0) {
+      int J2 = 0;
+      for (int b = 0; b < B; ++b)
+        for (int q = 0; q < ctl[b].njobs; ++q) jobs[J2++] = jobs[b * kla + q];
+      if (J2 > 0 && w + 1 >= X) {  // cannot happen: every wave expands at least one of a request's X slots
         record_error(p.hdr, DT_ERR_INVALID_ARG);
-        sorted[0] = Entry{-INFINITY, 0, -1, 1, 0};
+        J2 = 0;
       }
-      __syncthreads();
-      const Entry pop = sorted[0];
-      const bool will_expand = (s + 1 < n) && (pop.depth < maxd);
-      if (will_expand)  // its embedding row, for the next step's GRU
-        copy16_async(xe + static_cast<size_t>(b) * E,
-                     static_cast<const char*>(p.emb) + static_cast<size_t>(pop.token) * E * esize, esize * E);
-      asm volatile("cp.async.commit_group;" ::: "memory");
-      for (int i = t + 1; i < R; i += kThreads) fr[static_cast<size_t>(b) * n + i - 1] = sorted[i];
-      short* pb = par_s + static_cast<size_t>(b) * n;
-      if (j == 0) {
-        const size_t o = static_cast<size_t>(b) * n + s;
-        uint8_t* mrow = p.mask + o * n;
-        for (int c = t; c < n; c += kThreads) {  // ancestor test by walking s's parent chain (parents come first)
-          int a = c < s ? pop.parent : s;
-          while (a > c) a = pb[a];
-          mrow[c] = a == c;
-        }
-        if (t == 0) {
-          p.tokens[o] = pop.token;
-          p.parents[o] = pop.parent;
-          p.depth[o] = pop.depth;
-          p.scores[o] = pop.score;
+      if (J2 > 0) {
+        const unsigned erow = static_cast<unsigned>(E * esize), hrow = static_cast<unsigned>(H * sizeof(float));
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // phase A's reads of xe / xh came first
+        mbar_expect_tx(&jbar, static_cast<unsigned>(J2) * (erow + hrow));
+        for (int q = 0; q < J2; ++q) {
+          const Job jb = jobs[q];
+          bulk_g2s(xe + static_cast<size_t>(q) * SE, static_cast<const char*>(p.emb) + static_cast<size_t>(jb.token) * erow,
+                   erow, &jbar);
+          bulk_g2s(xh + static_cast<size_t>(q) * H, p.hs + (static_cast<size_t>(jb.b) * X + jb.pslot) * H, hrow, &jbar);
         }
       }
-      if (t == 0) {  // read by others only after the next barrier
-        pb[s] = pop.parent;
-        ReqState ns = st;
-        ns.fcount = R - 1;
-        ns.seq_next += C;
-        ns.token = pop.token;
-        ns.parent = pop.parent;
-        ns.depth = pop.depth;
-        ns.score = pop.score;
-        ns.expand = will_expand;
-        rs[b] = ns;
-      }
-      if (b + 1 < B) __syncthreads();  // the next request reuses the scratch entries
+      s_J = J2;
+    }
+  }
+
+  // ---- outputs (CTA 0): nodes in pop order, and the ancestor mask by walking each node's parent chain ----
+  if (j == 0) {
+    for (int i = t; i < B * n; i += kThreads) {
+      const PopRec r = pops[i];
+      p.tokens[i] = r.token;
+      p.parents[i] = r.parent;
+      p.depth[i] = r.depth;
+      p.scores[i] = r.score;
+    }
+    for (size_t i = t; i < static_cast<size_t>(B) * n * n; i += kThreads) {
+      const int b = static_cast<int>(i / (static_cast<size_t>(n) * n));
+      const int row = static_cast<int>((i / n) % n), c = static_cast<int>(i % n);
+      int a = row;
+      for (int hops = 0; a > c && hops < n; ++hops) a = pops[b * n + a].parent;  // parents precede their children
+      p.mask[i] = a == c;
     }
   }
 }
@@ -516,30 +639,22 @@ Plan plan_for(const Params& p, int sms) {
 
 }  // namespace
 
-bool small_builder_fits(const Params& p, int sms) {
+bool small_builder_fits(const Params& p, const DeviceInfo& di) {
   if (p.B > kSmallMaxB || p.B < 1 || !p.acc) return false;
-  const Plan P = plan_for(p, sms);
+  if (p.B * p.lookahead > kWaveJobs) return false;
+  const Plan P = plan_for(p, di.sms);
   if (3 * P.umax > kMaxRows || P.G > 255) return false;  // GEMV rows per CTA; contribution count in one byte
-  int dev = 0, optin = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return false;
-  return P.bytes <= static_cast<size_t>(optin);
+  return P.bytes <= static_cast<size_t>(di.optin);
 }
 
-cudaError_t launch_small_builder(const Params& p, cudaStream_t stream) {
-  int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
-  const Plan P = plan_for(p, sms);
+// One CTA per SM at most (launch bounds of 512 threads, one block), so the shared-memory plan alone decides that the
+// G CTAs are co-resident; the cooperative launch checks it again.
+cudaError_t launch_small_builder(const Params& p, const DeviceInfo& di, cudaStream_t stream) {
+  const Plan P = plan_for(p, di.sms);
   const void* fn = p.bf16 ? reinterpret_cast<const void*>(small_builder<true>)
                           : reinterpret_cast<const void*>(small_builder<false>);
-  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(P.bytes));
+  cudaError_t e = ensure_dynamic_smem(fn, P.bytes);
   if (e != cudaSuccess) return e;
-  int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, P.bytes);
-  if (e != cudaSuccess) return e;
-  if (per_sm < 1) return cudaErrorInvalidConfiguration;
   Params pp = p;
   Plan PP = P;
   void* args[] = {&pp, &PP};

@@ -636,8 +636,15 @@ extern "C" dt_status dt_build_trees(int B, int K, int V, int M, int n, int max_d
   p.frontier = reinterpret_cast<Entry*>(ws + L.frontier);
   p.hs = reinterpret_cast<float*>(ws + L.hs);
   p.acc = B <= kSmallMaxB ? reinterpret_cast<long long*>(ws + L.acc) : nullptr;
-  p.acc_stride = acc_stride(B, M, n);
+  p.hs_count = B <= kSmallMaxB ? reinterpret_cast<int*>(ws + L.hs_count) : nullptr;
+  p.acc_stride = acc_stride(M, n);
+  p.xslots = expansion_slots(n);
   p.timeout_ns = barrier_timeout_ns();
+  {  // expansions per request per wave: the setting, else as many as the small-batch builder's wave holds
+    const int k = lookahead_setting();
+    const int fit = kWaveJobs / (B < kWaveJobs ? B : kWaveJobs);
+    p.lookahead = k > 0 ? (k < fit ? k : fit) : fit;
+  }
 
   // phase A: tensor cores for bf16 weights whose widths are multiples of the 128-column pipeline chunk
   const int gemm = !p.bf16 ? 0
@@ -648,23 +655,16 @@ extern "C" dt_status dt_build_trees(int B, int K, int V, int M, int n, int max_d
                              : gemm == 3 ? reinterpret_cast<const void*>(build_kernel<3>)
                              : gemm == 1 ? reinterpret_cast<const void*>(build_kernel<1>)
                                          : reinterpret_cast<const void*>(build_kernel<2>);
-  int dev = 0, sms = 0, coop = 0, per_sm = 0, optin = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  if (e != cudaSuccess) return DT_ERR_CUDA;
-  if (!coop) return DT_ERR_UNSUPPORTED;
-  if (small_builder_fits(p, sms)) return cuda_status(launch_small_builder(p, stream));
-  // static shared memory of the kernel (flags, reductions) is well under 1 KB
-  const size_t smem = smem_bytes(gemm, M, n, H, p.bf16 ? 2 : 4, static_cast<size_t>(optin) - 1024, &p.rows_smem);
-  if (smem + 1024 > static_cast<size_t>(optin)) return DT_ERR_UNSUPPORTED;
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem);
-  if (e != cudaSuccess) return DT_ERR_CUDA;
-  if (per_sm < 1) return DT_ERR_UNSUPPORTED;
-  const unsigned grid = static_cast<unsigned>(sms);  // one CTA per SM; co-resident under a cooperative launch
+  DeviceInfo di{};
+  if (current_device_info(&di) != cudaSuccess) return DT_ERR_CUDA;
+  if (!di.coop) return DT_ERR_UNSUPPORTED;
+  if (small_builder_fits(p, di)) return cuda_status(launch_small_builder(p, di, stream));
+  // static shared memory of the kernel (flags, reductions) is well under 1 KB; one CTA per SM (launch bounds), so
+  // the shared memory alone decides whether a CTA fits
+  const size_t smem = smem_bytes(gemm, M, n, H, p.bf16 ? 2 : 4, static_cast<size_t>(di.optin) - 1024, &p.rows_smem);
+  if (smem + 1024 > static_cast<size_t>(di.optin)) return DT_ERR_UNSUPPORTED;
+  if (ensure_dynamic_smem(fn, smem) != cudaSuccess) return DT_ERR_CUDA;
+  const unsigned grid = static_cast<unsigned>(di.sms);  // one CTA per SM; co-resident under a cooperative launch
   void* args[] = {&p};
-  e = cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kThreads), args, smem, stream);
-  return cuda_status(e);
+  return cuda_status(cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kThreads), args, smem, stream));
 }

@@ -301,7 +301,17 @@ inline TopmLayout topm_layout(int B, int K, int V, int M) {
   return L;
 }
 
-// Host-side process-wide setting (dt_set_barrier_timeout_ns).
+// Host-side process-wide settings (dt_set_barrier_timeout_ns, dt_set_lookahead).
 uint64_t barrier_timeout_ns();
+int lookahead_setting();  // 0 = automatic
+
+// Attributes of the current device, queried once per device and cached (a launch then costs one runtime call).
+struct DeviceInfo {
+  int dev, sms, coop, optin;
+};
+cudaError_t current_device_info(DeviceInfo* out);
+// Raises the dynamic shared-memory limit of kernel `fn` on the current device to at least `bytes`; the runtime is
+// called only when a larger size than any set before for this (device, kernel) is asked for.
+cudaError_t ensure_dynamic_smem(const void* fn, size_t bytes);
 
 }  // namespace dt

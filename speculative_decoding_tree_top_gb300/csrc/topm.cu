@@ -629,20 +629,10 @@ dt_status launch_topm(const void* logits, dt_dtype dtype, int B, int K, int V, i
   void* words = ws + L.words;
   const size_t esize = dtype == DT_BF16 ? 2 : 4;
   const bool vec_ok = (static_cast<size_t>(V) * esize) % 16 == 0;
-  // the staged chunk (and the selection's buffers) exceed the default 48 KB of dynamic shared memory: raised once
-  static std::once_flag attr;
-  std::call_once(attr, [] {
-    const int bytes = static_cast<int>(kChunkSmem), sel = static_cast<int>(sizeof(SelectSmem));
-    cudaFuncSetAttribute(topm_filter_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    cudaFuncSetAttribute(topm_filter_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    cudaFuncSetAttribute(topm_filter_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    cudaFuncSetAttribute(topm_filter_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    cudaFuncSetAttribute(topm_select_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, sel);
-    cudaFuncSetAttribute(topm_select_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, sel);
-  });
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return DT_ERR_CUDA;
+  // the staged chunk (and the selection's buffers) exceed the default 48 KB of dynamic shared memory
+  DeviceInfo di{};
+  if (current_device_info(&di) != cudaSuccess) return DT_ERR_CUDA;
+  const int sms = di.sms;
   auto run = [&](auto bf16_tag) {
     constexpr bool kB = decltype(bf16_tag)::value;
     constexpr int kChunk = Topm<kB, kFThreads>::kChunk;
@@ -650,6 +640,10 @@ dt_status launch_topm(const void* logits, dt_dtype dtype, int B, int K, int V, i
     const dim3 grid(static_cast<unsigned>(rows), static_cast<unsigned>(chunks));
     // about two waves of three CTAs per SM or fewer: fuse the selection into the launch
     const bool fuse = rows * chunks <= 6LL * sms;
+    if (ensure_dynamic_smem(reinterpret_cast<const void*>(topm_filter_kernel<kB, true>), kChunkSmem) != cudaSuccess ||
+        ensure_dynamic_smem(reinterpret_cast<const void*>(topm_filter_kernel<kB, false>), kChunkSmem) != cudaSuccess ||
+        ensure_dynamic_smem(reinterpret_cast<const void*>(topm_select_kernel<kB>), sizeof(SelectSmem)) != cudaSuccess)
+      return false;
     if (fuse) {
       topm_filter_kernel<kB, true><<<grid, kFThreads, kChunkSmem, stream>>>(
           logits, V, M, chunks, L.cap, vec_ok, bounds, tickets, words, counts, out_ids, out_vals, hdr);
@@ -659,9 +653,10 @@ dt_status launch_topm(const void* logits, dt_dtype dtype, int B, int K, int V, i
       topm_select_kernel<kB><<<static_cast<unsigned>(rows), kSelThreads, sizeof(SelectSmem), stream>>>(
           words, counts, chunks, L.cap, M, bounds, out_ids, out_vals);
     }
+    return true;
   };
-  if (dtype == DT_BF16) run(std::true_type{});
-  else run(std::false_type{});
+  const bool ok = dtype == DT_BF16 ? run(std::true_type{}) : run(std::false_type{});
+  if (!ok) return DT_ERR_CUDA;
   return cuda_status(cudaGetLastError());
 }
 

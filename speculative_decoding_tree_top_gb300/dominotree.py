@@ -55,6 +55,7 @@ SIGNATURES = {
     "dt_topm_static": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "dt_get_error": (_I, [_P, _P]),
     "dt_set_barrier_timeout_ns": (None, [ctypes.c_uint64]),
+    "dt_set_lookahead": (_I, [_I]),
     "dt_status_string": (ctypes.c_char_p, [_I]),
     "dt_abi_version": (_I, []),
 }
@@ -134,6 +135,11 @@ def dt_get_error(workspace: torch.Tensor, stream=None) -> Status:
 
 def dt_set_barrier_timeout_ns(ns: int):
     lib().dt_set_barrier_timeout_ns(int(ns))
+
+
+def dt_set_lookahead(k: int):
+    """Expansions per request per wave in dt_build_trees (0 = the library's choice); outputs do not depend on it."""
+    _check(lib().dt_set_lookahead(int(k)), "dt_set_lookahead")
 
 
 def dt_topm(logits: torch.Tensor, M: int, out_ids: Optional[torch.Tensor] = None,
@@ -242,11 +248,47 @@ class Round:
         self.out = alloc_tree_outputs(B, n, device)
         self.workspace = new_workspace(dt_build_workspace_bytes(B, K, V, M, n, weights.H, weights.E), device)
 
-    def __call__(self, logits: torch.Tensor, h0: torch.Tensor, stream=None) -> dict:
-        dt_topm(logits, self.M, self.ids, self.vals, self.workspace, stream)
-        dt_build_trees(self.ids, self.vals, h0, self.weights, self.n, self.max_depth, self.T, self.out,
-                       self.workspace, stream)
+        self._topm_key = self._build_key = None
+
+    def topm(self, logits: torch.Tensor, stream=None):
+        """dt_topm into this round's ids/vals. The marshalled arguments are kept while the logits tensor (address,
+        shape, dtype) and the stream stay the same, so a repeated call costs one C call."""
+        st = _stream(stream)
+        key = (logits.data_ptr(), tuple(logits.shape), logits.dtype, st)
+        if key != self._topm_key:
+            B, K, V = logits.shape
+            if (B, K, V) != (self.B, self.K, self.V):
+                raise ValueError(f"logits must have shape {(self.B, self.K, self.V)}, not {(B, K, V)}")
+            self._topm_args = (_dev(logits, "logits"), _code(logits.dtype), B, K, V, self.M,
+                               _dev(self.ids, "out_ids"), _dev(self.vals, "out_vals"),
+                               _dev(self.workspace, "workspace", torch.uint8), self.workspace.numel(), st)
+            self._topm_key = key
+        _check(lib().dt_topm(*self._topm_args), "dt_topm")
+        return self.ids, self.vals
+
+    def build(self, h0: torch.Tensor, stream=None) -> dict:
+        """dt_build_trees from this round's ids/vals into its outputs (arguments kept like ``topm``'s, also keyed
+        by the weights' tensors)."""
+        st = _stream(stream)
+        w = self.weights
+        key = (h0.data_ptr(), tuple(h0.shape), h0.dtype, st, id(w),
+               *(t.data_ptr() if t is not None else 0 for t in (w.emb, w.w_ih, w.w_hh, w.b_ih, w.b_hh, w.w_c)))
+        if key != self._build_key:
+            self._wstruct = w.struct()
+            o = self.out
+            self._build_args = (
+                self.B, self.K, self.V, self.M, self.n, self.max_depth, float(self.T), _dev(self.ids, "topm_ids"),
+                _dev(self.vals, "topm_vals"), _dev(h0, "h0", torch.float32, (self.B, w.H)),
+                ctypes.byref(self._wstruct), _dev(o["tokens"], "out_tokens"), _dev(o["parents"], "out_parents"),
+                _dev(o["depth"], "out_depth"), _dev(o["scores"], "out_scores"), _dev(o["mask"], "out_mask"),
+                _dev(self.workspace, "workspace", torch.uint8), self.workspace.numel(), st)
+            self._build_key = key
+        _check(lib().dt_build_trees(*self._build_args), "dt_build_trees")
         return self.out
+
+    def __call__(self, logits: torch.Tensor, h0: torch.Tensor, stream=None) -> dict:
+        self.topm(logits, stream)
+        return self.build(h0, stream)
 
     def check(self, stream=None):
         _check(int(dt_get_error(self.workspace, stream)), "device status")

@@ -114,3 +114,11 @@ def test_binding_refuses_host_tensors(dtlib):
     with pytest.raises(TypeError):
         dtlib.dt_topm(torch.zeros(1, 2, 64), 4, out_ids=torch.zeros(1, 2, 4, dtype=torch.int32),
                       out_vals=torch.zeros(1, 2, 4), workspace=torch.zeros(4096, dtype=torch.uint8))
+
+
+def test_lookahead_setting_is_validated(dtlib):
+    L = dtlib.lib()
+    assert L.dt_set_lookahead(-1) == INVALID
+    assert L.dt_set_lookahead(9) == INVALID
+    for k in (1, 8, 0):
+        assert L.dt_set_lookahead(k) == OK

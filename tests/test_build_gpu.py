@@ -137,3 +137,36 @@ def test_out_of_range_ids_are_reported_not_gathered(dtlib):
     assert dtlib.dt_get_error(ws) == dtlib.Status.INVALID_ARG
     tok = out["tokens"].cpu().numpy()
     assert tok.min() >= 0 and tok.max() < s.V
+
+
+@pytest.mark.parametrize("case", [
+    dict(config=1),                                                    # one request, the bench workload
+    dict(config=0),                                                    # tiny, fp32
+    dict(config=2, B=2),                                               # two requests share a wave
+    dict(config=3, B=2),                                               # deeper trees (T = 0.5)
+    dict(tiny=dict(dtype="bf16", M=40, n=64, max_depth=5, K=5, B=1)),  # wide and deep
+    dict(tiny=dict(M=1, n=4, max_depth=4, B=1)),                       # a chain: nothing to look ahead at
+])
+def test_lookahead_width_does_not_change_the_tree(dtlib, case):
+    """Expanding several frontier nodes per wave only changes when children become known, never the pop order:
+    every lookahead width gives bit-identical outputs."""
+    if "tiny" in case:
+        inp = tiny(11, **case["tiny"])
+    else:
+        inp = synth.make_inputs(synth.shape(case["config"], **{k: v for k, v in case.items() if k != "config"}),
+                                device="cuda")
+    s = inp.shape
+    rnd = dtlib.Round(s.B, s.K, s.V, s.M, s.n, s.max_depth, s.T, dtlib.Weights.of(inp))
+    outs = []
+    try:
+        for k in (1, 2, 3, 8, 0):
+            dtlib.dt_set_lookahead(k)
+            out = rnd(inp.logits, inp.h0)
+            torch.cuda.synchronize()
+            rnd.check()
+            outs.append({key: v.clone() for key, v in out.items()})
+    finally:
+        dtlib.dt_set_lookahead(0)
+    for o in outs[1:]:
+        for key in o:
+            assert torch.equal(o[key], outs[0][key]), key
