@@ -16,21 +16,6 @@ constexpr int kSpareSlots = 16;  // expansion slots per request beyond the n tha
 // not. Best-first needs at most n (the root and the first n - 1 pops); the rest bound the speculative waste.
 __host__ __device__ inline int expansion_slots(int n) { return n + kSpareSlots; }
 
-struct alignas(16) Entry {  // a frontier node; 16 bytes
-  float score;
-  int token;
-  short parent;  // index of the parent among the popped nodes, -1 for a child of the root
-  short depth;
-  int seq;       // insertion order
-};
-
-// Pop order: higher score, then lower token id, then earlier insertion (branch-free).
-__device__ __forceinline__ bool before(const Entry& a, const Entry& b) {
-  const bool seq_first = a.seq < b.seq;
-  const bool tok_first = (a.token < b.token) | ((a.token == b.token) & seq_first);
-  return (a.score > b.score) | ((a.score == b.score) & tok_first);
-}
-
 // A known node of the lookahead builders: an entry of a request's frontier, or of the children list of an expanded
 // node that has not been popped yet; 16 bytes.
 struct alignas(16) Node {
@@ -276,17 +261,6 @@ __device__ inline void request_step(const ReqView& R, int b, int n, int M, int m
   if (lane == 0) *R.ctl = st;
 }
 
-struct NodeState {  // the node popped last by a request, as phase A of the next step needs it
-  int token;
-  int parent;
-  int depth;
-  int expand;  // 1 if the node is expanded in the next step
-  float score;
-  int seq_next;
-  int fcount;  // entries in the request's frontier
-  int pad;
-};
-
 struct Params {
   int B, K, V, M, n, max_depth, H, E;
   float T_eff;
@@ -306,11 +280,12 @@ struct Params {
   float* scores;
   uint8_t* mask;
   WsHeader* hdr;
-  NodeState* state;
-  Entry* frontier;  // [B][n]
-  float* hs;        // [B][n][H]
-  long long* acc;   // [n][B][M] fixed-point correction accumulators, acc_stride words apart (small-batch builder)
+  float* hs;        // [B][xslots][H] hidden state of every expansion slot (slot 0: h0)
+  long long* acc;   // [xslots][kWaveJobs][M] fixed-point correction accumulators, acc_stride words apart (small)
   int acc_stride;
+  unsigned char* rstate;  // [B] per-request best-first state blocks of req_layout(...).bytes (large-batch builder)
+  Job* joblist;     // [2][B * lookahead] the expansions of a wave, packed (large-batch builder)
+  int* jobcount;    // [xslots + 2] expansions per wave (large-batch builder)
   uint64_t timeout_ns;
   bool rows_smem;   // large-batch builder: the M gathered correction rows of a node are staged in shared memory
   int lookahead;    // expansions a request may run per wave (1 = one pop at a time)
@@ -336,46 +311,6 @@ __device__ __forceinline__ int valid_id(const Params& p, int id) {
     return 0;
   }
   return id;
-}
-
-// Keeps the first R entries, in pop order, of the union of a request's frontier and a node's new children:
-// cand[0, F) is the frontier, already in pop order (it was written that way), cand[F, F + C) the children in any
-// order. The children are ranked among themselves by counting (tpe threads per child), then every entry's place in
-// the union is its place in its own list plus a binary search in the other one: O((F + C) log) instead of counting
-// every pair. `before` is a strict total order, so the places are distinct. sc[0, C) is scratch; sorted[0, R) the
-// result. Called by the whole block (kThreads threads); ends synchronised.
-template <int kThreads>
-__device__ void merge_rank(const Entry* cand, int F, int C, int R, Entry* sc, Entry* sorted) {
-  const int t = threadIdx.x;
-  int tpe = 1;
-  while (tpe < 32 && tpe * 2 * C <= kThreads) tpe *= 2;
-  for (int base = 0; base < C * tpe; base += kThreads) {  // uniform bounds: every lane reaches the shuffles
-    const int slot = base + t, i = slot / tpe, part = slot % tpe;
-    int r = 0;
-    Entry ei{};
-    if (i < C) {
-      ei = cand[F + i];
-#pragma unroll 4
-      for (int q = part; q < C; q += tpe) r += before(cand[F + q], ei);
-    }
-    for (int o = 1; o < tpe; o <<= 1) r += __shfl_xor_sync(0xFFFFFFFFu, r, o);
-    if (i < C && part == 0) sc[r] = ei;
-  }
-  __syncthreads();
-  for (int k = t; k < F + C; k += kThreads) {
-    const bool old = k < F;
-    const Entry e = old ? cand[k] : sc[k - F];
-    const Entry* other = old ? sc : cand;
-    int lo = 0, hi = old ? C : F;  // entries of the other list that come before e
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (before(other[mid], e)) lo = mid + 1;
-      else hi = mid;
-    }
-    const int r = (old ? k : k - F) + lo;
-    if (r < R) sorted[r] = e;
-  }
-  __syncthreads();
 }
 
 // One warp: the dot products of 8 consecutive rows m0 .. m0 + 7 (those < M) with h, for the rows of a gathered slice
@@ -438,11 +373,46 @@ __device__ __forceinline__ void warp_dot_rows8(const void* rows, const void* w, 
     for (int j = 0; j < 8; ++j) out[j] += __shfl_xor_sync(0xFFFFFFFFu, out[j], o);
 }
 
-// Builder region of the workspace, after the top-M region (one workspace serves the whole round): per-request
-// last-pop state, pruned frontiers [B][n], hidden states [B][n][H] fp32, and for small batches the per-step
-// fixed-point correction accumulators [n][B][M] int64 and the hidden-state publication counters [B][n].
+// A request's best-first state as one contiguous block (the large-batch builder keeps it in the workspace between
+// waves and works on it in shared memory; offsets are multiples of 16 so the block moves as one bulk copy).
+struct ReqLayout {
+  size_t ctl, lanes, jobs, merged, kids, kcount, popidx, sdepth, pops, bytes;
+};
+__host__ __device__ inline ReqLayout req_layout(int n, int X, int KM, int kla) {
+  ReqLayout L{};
+  size_t o = 0;
+  auto take = [&o](size_t bytes) {
+    const size_t at = o;
+    o = (o + bytes + 15) / 16 * 16;
+    return at;
+  };
+  L.ctl = take(sizeof(ReqCtl));
+  L.lanes = take(sizeof(LaneSrc) * 32);
+  L.jobs = take(sizeof(Job) * kla);
+  L.merged = take(sizeof(Node) * 2 * static_cast<size_t>(n));
+  L.kids = take(sizeof(Node) * static_cast<size_t>(X) * KM);
+  L.kcount = take(sizeof(int) * X);
+  L.popidx = take(sizeof(int) * X);
+  L.sdepth = take(sizeof(int) * X);
+  L.pops = take(sizeof(PopRec) * static_cast<size_t>(n));
+  L.bytes = o;
+  return L;
+}
+__host__ __device__ inline ReqView req_view(unsigned char* base, const ReqLayout& L) {
+  return ReqView{reinterpret_cast<ReqCtl*>(base + L.ctl), reinterpret_cast<LaneSrc*>(base + L.lanes),
+                 reinterpret_cast<Node*>(base + L.merged), reinterpret_cast<Node*>(base + L.kids),
+                 reinterpret_cast<int*>(base + L.kcount), reinterpret_cast<int*>(base + L.popidx),
+                 reinterpret_cast<int*>(base + L.sdepth), reinterpret_cast<PopRec*>(base + L.pops)};
+}
+constexpr int kLargeLookahead = 8;  // the large-batch builder's most expansions per request and wave
+constexpr int kLargeDefault = 4;    // ... and its default
+
+// Builder region of the workspace, after the top-M region (one workspace serves the whole round): the hidden states
+// of every expansion slot [B][X][H] fp32; for small batches the per-wave fixed-point correction accumulators and the
+// per-slot publication counters; for larger ones the per-request state blocks, the packed job lists of two waves and
+// the per-wave job counts.
 struct BuildLayout {
-  size_t state, frontier, hs, acc, hs_count, bytes;
+  size_t hs, acc, hs_count, rstate, joblist, jobcount, bytes;
 };
 
 // Words between two correction accumulators: one 128-byte line each, so that the shares of a wave (every SM adds
@@ -453,16 +423,17 @@ __host__ __device__ inline int acc_stride(int M, int n) {
 
 inline BuildLayout build_layout(int B, int K, int V, int M, int n, int H) {
   BuildLayout L{};
-  L.state = topm_layout(B, K, V, M).bytes;
-  L.frontier = align_up(L.state + sizeof(NodeState) * static_cast<size_t>(B));
-  L.hs = align_up(L.frontier + sizeof(Entry) * static_cast<size_t>(B) * n);
   const size_t X = static_cast<size_t>(expansion_slots(n));
-  L.acc = align_up(L.hs + sizeof(float) * static_cast<size_t>(B) * X * H);
-  // small batches: per-wave per-job per-candidate accumulators [X][kWaveJobs][M] int64 (acc_stride words apart),
-  // then per-slot publication counters [B][X] int32
+  const int KM = M < n ? M : n;
+  L.hs = topm_layout(B, K, V, M).bytes;
   const size_t acc_bytes = B <= kSmallMaxB ? sizeof(long long) * X * kWaveJobs * M * acc_stride(M, n) : 0;
+  L.acc = align_up(L.hs + sizeof(float) * static_cast<size_t>(B) * X * H);
   L.hs_count = align_up(L.acc + acc_bytes);
-  L.bytes = align_up(L.hs_count + (B <= kSmallMaxB ? sizeof(int) * static_cast<size_t>(B) * X : 0));
+  L.rstate = align_up(L.hs_count + (B <= kSmallMaxB ? sizeof(int) * static_cast<size_t>(B) * X : 0));
+  // both builders may run for small batches (the small one needs shared memory the device may not have)
+  L.joblist = align_up(L.rstate + req_layout(n, static_cast<int>(X), KM, kLargeLookahead).bytes * B);
+  L.jobcount = align_up(L.joblist + sizeof(Job) * 2 * static_cast<size_t>(B) * kLargeLookahead);
+  L.bytes = align_up(L.jobcount + sizeof(int) * (X + 2));
   return L;
 }
 

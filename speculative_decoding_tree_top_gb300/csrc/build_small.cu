@@ -600,6 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
       if (J2 > 0) {
         const unsigned erow = static_cast<unsigned>(E * esize), hrow = static_cast<unsigned>(H * sizeof(float));
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // phase A's reads of xe / xh came first
+        asm volatile("fence.proxy.async.global;" ::: "memory");      // the states were stored by the generic proxy
         mbar_expect_tx(&jbar, static_cast<unsigned>(J2) * (erow + hrow));
         for (int q = 0; q < J2; ++q) {
           const Job jb = jobs[q];

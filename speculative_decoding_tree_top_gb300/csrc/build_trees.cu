@@ -6,17 +6,22 @@
 // gist.science, "Composants Clés" (only the light GRU correction and correction head are recomputed per node).
 //
 // GB300 design. The pages' builder replays a CUDA graph per node while a host-side heap decides the next pop
-// (gist.science, "Constructeur Natif GPU"); here the whole round is one launch with no host round-trip:
-//   * all B requests advance in lockstep: step s pops the s-th node of every request;
-//   * phase A (all CTAs): the GRU step of the nodes popped in the previous step, as tiles of
-//     [16 requests x 16 hidden units] over K = E (embedding row) then K = H (parent state), fp32 accumulation;
+// (gist.science, "Constructeur Natif GPU"); here the whole round is one launch with no host round-trip, and all B
+// requests advance in lockstep waves:
+//   * a wave expands up to k nodes of every request (lookahead: the node that blocks the request's next pop, then
+//     the next unexpanded nodes in the order best-first would reach them; the pops themselves stay exact, see
+//     request_step), so a round takes a few waves rather than n steps;
+//   * phase A (all CTAs): the GRU step of every expansion of the wave as one GEMM, rows = the packed expansions,
+//     columns = the r, z, n_in, n_h gate sets of the hidden units, tensor cores (mma.sync) for bf16 weights;
 //   * grid barrier;
-//   * phase B (one CTA per request): gather the M correction rows of the node's block position and dot them with
-//     h (one warp per row), restricted log-softmax (warp reductions), merge the children into the request's
-//     frontier keeping only the n - s entries that can still be popped, pop the best, write the node's output row
-//     and its ancestor-mask row;
-//   * grid barrier; next step.
-// Every reduction has a fixed order (no floating-point atomics), so the output is bit-identical run to run.
+//   * phase B (the CTA that owns the request): its best-first state comes into shared memory as one bulk copy; for
+//     each expansion, the M correction rows of the node's block position dotted with its new hidden state, the
+//     restricted log-softmax, the children ranked; then one warp pops and picks the next wave's expansions, which
+//     join the packed list of the next wave; the state goes back as one bulk copy; a finished request writes its
+//     outputs and ancestor mask;
+//   * grid barrier; next wave (none when no request added an expansion).
+// Every reduction has a fixed order (no floating-point atomics), so the output is bit-identical run to run and
+// does not depend on the lookahead width or on where an expansion sits in the packed list.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -28,39 +33,42 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr uint64_t kCopyBudgetNs = 4000000000ull;
 constexpr int kTB = 16;   // requests per GRU tile
 constexpr int kTU = 16;   // hidden units per GRU tile
 constexpr int kKC = 64;   // K-chunk of the GRU tile
 constexpr int kPad = kKC + 1;
 
-// ---- phase A: GRU step of every request whose last pop is expanded --------------------------------------------
-__device__ void gru_phase(const Params& p, int node, float* smem) {
+// ---- phase A: GRU step of every expansion of the wave (CUDA cores: fp32 weights, or widths that are not
+// multiples of the tensor-core tile) ------------------------------------------------------------------------------
+__device__ void gru_phase(const Params& p, const Job* jl, int rows, float* smem) {
   float* xs = smem;                  // [kTB][kPad]
   float* ws = smem + kTB * kPad;     // [3][kTU][kPad]
-  __shared__ int s_tok[kTB], s_par[kTB], s_exp[kTB];
+  __shared__ int s_tok[kTB], s_b[kTB], s_ps[kTB], s_xs[kTB];
   const int t = threadIdx.x, lb = t / kTU, lu = t % kTU;
+  const int X = p.xslots;
   const int ublocks = (p.H + kTU - 1) / kTU;
-  const int rblocks = (p.B + kTB - 1) / kTB;
+  const int rblocks = (rows + kTB - 1) / kTB;
   const int tiles = ublocks * rblocks;
   for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
     const int rb = tile / ublocks, ub = tile % ublocks;
     __syncthreads();
     if (t < kTB) {
-      const int b = rb * kTB + t;
-      const bool ok = b < p.B && p.state[b].expand;
-      s_exp[t] = ok;
-      s_tok[t] = ok ? p.state[b].token : 0;
-      s_par[t] = ok ? p.state[b].parent : -1;
+      const int r = rb * kTB + t;
+      const bool ok = r < rows;
+      s_tok[t] = ok ? jl[r].token : -1;
+      s_b[t] = ok ? jl[r].b : 0;
+      s_ps[t] = ok ? jl[r].pslot : 0;
+      s_xs[t] = ok ? jl[r].xslot : 0;
     }
     __syncthreads();
-    if (!__syncthreads_or(t < kTB && s_exp[t])) continue;
-    const int b = rb * kTB + lb, k = ub * kTU + lu;
+    const int r = rb * kTB + lb, k = ub * kTU + lu;
     float acc_r = 0.f, acc_u = 0.f, acc_ni = 0.f, acc_nh = 0.f;
     // input side: W_ih[gate rows] . emb[token]
     for (int e0 = 0; e0 < p.E; e0 += kKC) {
       for (int i = t; i < kTB * kKC; i += kThreads) {
-        const int r = i / kKC, c = i % kKC, e = e0 + c;
-        xs[r * kPad + c] = (s_exp[r] && e < p.E) ? ldw(p.emb, p.bf16, static_cast<size_t>(s_tok[r]) * p.E + e) : 0.f;
+        const int q = i / kKC, c = i % kKC, e = e0 + c;
+        xs[q * kPad + c] = (s_tok[q] >= 0 && e < p.E) ? ldw(p.emb, p.bf16, static_cast<size_t>(s_tok[q]) * p.E + e) : 0.f;
       }
       for (int i = t; i < 3 * kTU * kKC; i += kThreads) {
         const int g = i / (kTU * kKC), u = (i / kKC) % kTU, c = i % kKC, e = e0 + c, kk = ub * kTU + u;
@@ -80,15 +88,9 @@ __device__ void gru_phase(const Params& p, int node, float* smem) {
     // hidden side: W_hh[gate rows] . h_parent
     for (int j0 = 0; j0 < p.H; j0 += kKC) {
       for (int i = t; i < kTB * kKC; i += kThreads) {
-        const int r = i / kKC, c = i % kKC, j = j0 + c;
-        float v = 0.f;
-        if (s_exp[r] && j < p.H) {
-          const int bb = rb * kTB + r, par = s_par[r];
-          const float* hp = par < 0 ? p.h0 + static_cast<size_t>(bb) * p.H
-                                    : p.hs + (static_cast<size_t>(bb) * p.n + par) * p.H;
-          v = par < 0 ? __ldg(hp + j) : hp[j];
-        }
-        xs[r * kPad + c] = v;
+        const int q = i / kKC, c = i % kKC, j = j0 + c;
+        xs[q * kPad + c] = (s_tok[q] >= 0 && j < p.H)
+                               ? __ldcg(p.hs + (static_cast<size_t>(s_b[q]) * X + s_ps[q]) * p.H + j) : 0.f;
       }
       for (int i = t; i < 3 * kTU * kKC; i += kThreads) {
         const int g = i / (kTU * kKC), u = (i / kKC) % kTU, c = i % kKC, j = j0 + c, kk = ub * kTU + u;
@@ -105,18 +107,17 @@ __device__ void gru_phase(const Params& p, int node, float* smem) {
       }
       __syncthreads();
     }
-    if (b < p.B && k < p.H && s_exp[lb]) {
+    if (r < rows && k < p.H) {
       const size_t g0 = k, g1 = static_cast<size_t>(p.H) + k, g2 = 2 * static_cast<size_t>(p.H) + k;
       const float bir = p.b_ih ? ldw(p.b_ih, p.bf16, g0) : 0.f, bhr = p.b_hh ? ldw(p.b_hh, p.bf16, g0) : 0.f;
       const float biu = p.b_ih ? ldw(p.b_ih, p.bf16, g1) : 0.f, bhu = p.b_hh ? ldw(p.b_hh, p.bf16, g1) : 0.f;
       const float bin = p.b_ih ? ldw(p.b_ih, p.bf16, g2) : 0.f, bhn = p.b_hh ? ldw(p.b_hh, p.bf16, g2) : 0.f;
-      const float r = sigmoidf_(acc_r + bir + bhr);
+      const float rg = sigmoidf_(acc_r + bir + bhr);
       const float u = sigmoidf_(acc_u + biu + bhu);
-      const float g = tanhf((acc_ni + bin) + r * (acc_nh + bhn));
-      const int par = s_par[lb];
-      const float hprev = par < 0 ? __ldg(p.h0 + static_cast<size_t>(b) * p.H + k)
-                                  : p.hs[(static_cast<size_t>(b) * p.n + par) * p.H + k];
-      p.hs[(static_cast<size_t>(b) * p.n + node) * p.H + k] = (1.f - u) * g + u * hprev;
+      const float g = tanhf((acc_ni + bin) + rg * (acc_nh + bhn));
+      const size_t b = s_b[lb];
+      const float hprev = __ldcg(p.hs + (b * X + s_ps[lb]) * p.H + k);
+      p.hs[(b * X + s_xs[lb]) * p.H + k] = (1.f - u) * g + u * hprev;
     }
   }
 }
@@ -197,26 +198,26 @@ using TileL = GemmTile<64, 16, 128, 4>;
 // cp.async (one cp.async group per chunk). (Bulk copies of the 256- to 1024-byte row pieces measured 2x slower here:
 // each chunk is ~56 small copies.)
 template <typename GT, int kRT, int kUT>
-__device__ void gemm_gru_phase(const Params& p, int node, unsigned char* smem) {
+__device__ void gemm_gru_phase(const Params& p, const Job* jl, int rows, unsigned char* smem) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int g = lane >> 2, tig = lane & 3;
-  const int E = p.E, H = p.H, B = p.B, n = p.n;
+  const int E = p.E, H = p.H, X = p.xslots;
   float* red = reinterpret_cast<float*>(smem);                // [kWarps][kRT][kRS], after the main loop
-  int* info = reinterpret_cast<int*>(smem + GT::kRing);        // [kRT][4]
-  const int rtiles = (B + kRT - 1) / kRT, utiles = (H + kUT - 1) / kUT;
+  int* info = reinterpret_cast<int*>(smem + GT::kRing);        // [kRT][4]: token (-1: no row), request, parent slot, slot
+  const int rtiles = (rows + kRT - 1) / kRT, utiles = (H + kUT - 1) / kUT;
   const int nin = E / GT::kKc, nc = nin + H / GT::kKc;  // chunks: input side, then hidden side
   for (int tile = blockIdx.x; tile < rtiles * utiles; tile += gridDim.x) {
     const int b0 = (tile / utiles) * kRT, u0 = (tile % utiles) * kUT;
     __syncthreads();  // the previous tile is done with the shared buffers
     for (int r = t; r < kRT; r += kThreads) {
-      const int b = b0 + r;
-      const bool ok = b < B && p.state[b].expand;
-      info[4 * r] = ok ? p.state[b].token : 0;
-      info[4 * r + 1] = ok ? p.state[b].parent : -1;
-      info[4 * r + 2] = ok;
+      const int row = b0 + r;
+      const bool ok = row < rows;
+      info[4 * r] = ok ? jl[row].token : -1;
+      info[4 * r + 1] = ok ? jl[row].b : 0;
+      info[4 * r + 2] = ok ? jl[row].pslot : 0;
+      info[4 * r + 3] = ok ? jl[row].xslot : 0;
     }
     __syncthreads();
-    if (!__syncthreads_or(t < kRT && info[4 * t + 2])) continue;
 
     auto issue = [&](int c) {  // chunk c -> stage c % kStages
       unsigned char* st = smem + (c % GT::kStages) * GT::kStage;
@@ -237,7 +238,7 @@ __device__ void gemm_gru_phase(const Params& p, int node, unsigned char* smem) {
         unsigned short* xdst = reinterpret_cast<unsigned short*>(st);
         for (int i = t; i < kRT * (GT::kKc / 8); i += kThreads) {
           const int r = i / (GT::kKc / 8), piece = i % (GT::kKc / 8);
-          if (info[4 * r + 2])
+          if (info[4 * r] >= 0)
             cp_async16(xdst + r * GT::kXS + piece * 8,
                        static_cast<const unsigned short*>(p.emb) + static_cast<size_t>(info[4 * r]) * E + k0 +
                            piece * 8);
@@ -246,10 +247,8 @@ __device__ void gemm_gru_phase(const Params& p, int node, unsigned char* smem) {
         float* xdst = reinterpret_cast<float*>(st);
         for (int i = t; i < kRT * (GT::kKc / 4); i += kThreads) {
           const int r = i / (GT::kKc / 4), piece = i % (GT::kKc / 4);
-          if (info[4 * r + 2]) {
-            const int b = b0 + r, par = info[4 * r + 1];
-            const float* src = par < 0 ? p.h0 + static_cast<size_t>(b) * H
-                                       : p.hs + (static_cast<size_t>(b) * n + par) * H;
+          if (info[4 * r] >= 0) {
+            const float* src = p.hs + (static_cast<size_t>(info[4 * r + 1]) * X + info[4 * r + 2]) * H;
             cp_async16(xdst + r * GT::kHS + piece * 4, src + k0 + piece * 4);
           }
         }
@@ -337,8 +336,8 @@ __device__ void gemm_gru_phase(const Params& p, int node, unsigned char* smem) {
       }
     __syncthreads();
     for (int i = t; i < kRT * kUT; i += kThreads) {  // the GRU pointwise, one (request, unit) per thread
-      const int r = i / kUT, uu = i % kUT, b = b0 + r, u = u0 + uu;
-      if (b >= B || u >= H || !info[4 * r + 2]) continue;
+      const int r = i / kUT, uu = i % kUT, u = u0 + uu;
+      if (u >= H || info[4 * r] < 0) continue;
       float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {  // fixed order: bit-identical run to run
@@ -353,101 +352,109 @@ __device__ void gemm_gru_phase(const Params& p, int node, unsigned char* smem) {
       const float rg = sigmoidf_(d[0] + bir + bhr);
       const float zg = sigmoidf_(d[1] + biz + bhz);
       const float ng = tanhf(d[2] + bin + rg * (d[3] + bhn));
-      const int par = info[4 * r + 1];
-      const float hprev = par < 0 ? __ldg(p.h0 + static_cast<size_t>(b) * H + u)
-                                  : __ldcg(p.hs + (static_cast<size_t>(b) * n + par) * H + u);
-      p.hs[(static_cast<size_t>(b) * n + node) * H + u] = (1.f - zg) * ng + zg * hprev;
+      const size_t b = static_cast<size_t>(info[4 * r + 1]);
+      const float hprev = __ldcg(p.hs + (b * X + info[4 * r + 2]) * H + u);
+      p.hs[(b * X + info[4 * r + 3]) * H + u] = (1.f - zg) * ng + zg * hprev;
     }
   }
 }
 
-// ---- phase B: expand, merge, pop (one CTA per request) ----------------------------------------------------------
-// A CTA owns requests blockIdx.x, blockIdx.x + G, ... for the whole launch; the states of its first kSlots requests
-// stay in shared memory between steps, and after each step it asks L2 for what the next step of those requests
-// reads (the popped token's embedding row, the correction rows of the popped node's block position) while it waits
-// at the grid barrier.
-constexpr int kSlots = 8;
-
-struct OwnedState {
-  NodeState st[kSlots];
-  int pf_token[kSlots];  // embedding row to prefetch, -1 for none
-  int pf_pos[kSlots];    // offset of the candidate row in ids/vals to prefetch the correction rows of, -1 for none
-};
-
-// Shared memory of the frontier phase: [H] hidden state, [M4] logits, [M4] base logits, [M4] ids, 2 x [n + M]
-// entries, then (when it fits) the node's M gathered W_c rows.
+// ---- phase B: the expansions' children, then pops and picks (the CTA that owns the request) ---------------------
+// Shared memory of the phase: the request's state block, then per expansion [H] hidden state, [M4] logits,
+// [M4] base logits, [M4] ids, [M] sibling keys, [M] children, then (when it fits) the M gathered W_c rows.
 __host__ __device__ inline int round4(int x) { return (x + 3) & ~3; }
-__host__ __device__ inline size_t frontier_rows_offset(int M, int n, int H) {
-  return align_up(sizeof(float) * (H + 3 * round4(M)) + 2 * sizeof(Entry) * static_cast<size_t>(n + M), 16);
+struct FrontierSmem {
+  size_t h, z, vals, ids, keys, kraw, rows, bytes;
+};
+__host__ __device__ inline FrontierSmem frontier_smem(size_t state_bytes, int M, int H) {
+  FrontierSmem F{};
+  size_t o = (state_bytes + 15) / 16 * 16;
+  auto take = [&o](size_t bytes) {
+    const size_t at = o;
+    o = (o + bytes + 15) / 16 * 16;
+    return at;
+  };
+  F.h = take(sizeof(float) * H);
+  F.z = take(sizeof(float) * round4(M));
+  F.vals = take(sizeof(float) * round4(M));
+  F.ids = take(sizeof(int) * round4(M));
+  F.keys = take(sizeof(unsigned long long) * M);
+  F.kraw = take(sizeof(Node) * M);
+  F.rows = o;
+  F.bytes = o;
+  return F;
 }
 constexpr size_t kFrontierRowsCap = 160 * 1024;  // gathered rows kept in shared memory up to this size
 
-__device__ void frontier_phase(const Params& p, int s, unsigned char* smem, OwnedState* own) {
+__device__ __forceinline__ void bulk_s2g(void* gdst, const void* ssrc, unsigned bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(ssrc)), "r"(bytes)
+               : "memory");
+}
+
+// Returns false when a bulk-copy wait ran out (recorded); the caller leaves the kernel.
+__device__ bool frontier_phase(const Params& p, int w, unsigned char* smem, uint64_t* bar, unsigned& bar_uses) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int M = p.M, n = p.n, H = p.H, M4 = round4(M);
+  const int M = p.M, n = p.n, H = p.H, X = p.xslots, KM = M < n ? M : n, kla = p.lookahead;
   const size_t esize = p.bf16 ? 2 : 4;
-  float* h = reinterpret_cast<float*>(smem);                   // [H]
-  float* z = h + H;                                            // [M4]
-  float* vals = z + M4;                                        // [M4]
-  int* ids = reinterpret_cast<int*>(vals + M4);                // [M4]
-  Entry* cand = reinterpret_cast<Entry*>(ids + M4);            // [n + M]
-  Entry* sorted = cand + (n + M);                              // [n + M]
-  unsigned char* rows = smem + frontier_rows_offset(M, n, H);  // [M][H]
+  const ReqLayout RL = req_layout(n, X, KM, kla);
+  const FrontierSmem FS = frontier_smem(RL.bytes, M, H);
+  const ReqView R = req_view(smem, RL);
+  Job* jobs = reinterpret_cast<Job*>(smem + RL.jobs);
+  float* h = reinterpret_cast<float*>(smem + FS.h);
+  float* z = reinterpret_cast<float*>(smem + FS.z);
+  float* vals = reinterpret_cast<float*>(smem + FS.vals);
+  int* ids = reinterpret_cast<int*>(smem + FS.ids);
+  unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem + FS.keys);
+  Node* kraw = reinterpret_cast<Node*>(smem + FS.kraw);
+  unsigned char* rows = smem + FS.rows;
   const bool rows_in_smem = p.rows_smem;
+  Job* next = p.joblist + static_cast<size_t>((w + 1) & 1) * p.B * kla;
   __shared__ float s_red[2];
-  int slot = 0;
-  for (int b = blockIdx.x; b < p.B; b += gridDim.x, ++slot) {
-    __syncthreads();
-    NodeState st;
-    bool expand;
-    int node_depth, parent_idx;
-    float node_score;
-    const float* hsrc;
-    if (s == 0) {
-      expand = true;
-      node_depth = 0;
-      parent_idx = -1;
-      node_score = 0.f;
-      hsrc = p.h0 + static_cast<size_t>(b) * H;
-      st.seq_next = 0;
-      st.fcount = 0;
-    } else {
-      st = slot < kSlots ? own->st[slot] : p.state[b];
-      expand = st.expand != 0;
-      node_depth = st.depth;
-      parent_idx = s - 1;
-      node_score = st.score;
-      hsrc = p.hs + (static_cast<size_t>(b) * n + (s - 1)) * H;
+  __shared__ int s_off;
+  auto wait_bar = [&]() -> bool {  // bulk copies take microseconds: the budget only stops a lost one
+    const bool ok = mbar_wait(bar, bar_uses & 1u, kCopyBudgetNs);
+    ++bar_uses;
+    if (!ok) {
+      record_error(p.hdr, DT_ERR_TIMEOUT);
+      atomicExch(&p.hdr->abort, 1u);
     }
-    const int F = st.fcount;
-    const int C = expand ? M : 0;
-    Entry* fr = p.frontier + static_cast<size_t>(b) * n;
-    const size_t pos = (static_cast<size_t>(b) * p.K + node_depth) * M;
-    // first wave: everything whose address is known (state, ids, base logits, frontier), one latency
-    for (int i = t; i < F; i += kThreads) cp_async16(cand + i, fr + i);
-    if (expand) {
-      for (int k = t; k < H / 4; k += kThreads) cp_async16(h + 4 * k, hsrc + 4 * k);
-      for (int m = t; m < M; m += kThreads) {
-        cp_async4(ids + m, p.ids + pos + m);
-        cp_async4(vals + m, p.vals + pos + m);
+    return ok;
+  };
+  for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
+    unsigned char* gstate = p.rstate + static_cast<size_t>(b) * RL.bytes;
+    __syncthreads();  // the previous request (or phase) is done with the shared buffers
+    if (t == 0) {
+      mbar_expect_tx(bar, static_cast<unsigned>(RL.bytes));
+      bulk_g2s(smem, gstate, static_cast<unsigned>(RL.bytes), bar);
+    }
+    if (!__syncthreads_and(wait_bar())) return false;
+    const ReqCtl st0 = *R.ctl;
+    if (st0.s >= n) continue;  // finished in an earlier wave
+    // each expansion of the wave: correction on the gathered slice, restricted log-softmax, children ranked
+    for (int q = 0; q < st0.njobs; ++q) {
+      const Job jb = jobs[q];
+      const size_t pos = (static_cast<size_t>(b) * p.K + jb.depth) * M;
+      const float* hsrc = p.hs + (static_cast<size_t>(b) * X + jb.xslot) * H;
+      if (t == 0) {  // the node's hidden state (written by the GRU phase through the generic proxy): a bulk copy
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        mbar_expect_tx(bar, static_cast<unsigned>(H * 4));
+        bulk_g2s(h, hsrc, static_cast<unsigned>(H * 4), bar);
       }
-    }
-    cp_async_commit();
-    cp_async_wait_all();
-    __syncthreads();
-    if (expand) {
-      for (int m = t; m < M; m += kThreads) ids[m] = valid_id(p, ids[m]);
-      __syncthreads();
-      if (rows_in_smem) {  // second wave: the M correction rows (L2 hits when the previous step prefetched them)
-        const int pieces = static_cast<int>(H * esize / 16);
-        for (int i = t; i < M * pieces; i += kThreads) {
-          const int m = i / pieces, q = i % pieces;
-          cp_async16(rows + (static_cast<size_t>(m) * pieces + q) * 16,
-                     static_cast<const char*>(p.w_c) + (static_cast<size_t>(ids[m]) * pieces + q) * 16);
+      for (int m = t; m < M; m += kThreads) {  // ids and base logits of its block position (any M: plain loads)
+        ids[m] = valid_id(p, __ldg(p.ids + pos + m));
+        vals[m] = __ldg(p.vals + pos + m);
+      }
+      if (!__syncthreads_and(wait_bar())) return false;
+      if (rows_in_smem) {  // the M correction rows, one bulk copy each (issued by warp 0's lanes)
+        const unsigned rb = static_cast<unsigned>(H * esize);
+        if (warp == 0) {
+          if (lane == 0) mbar_expect_tx(bar, rb * static_cast<unsigned>(M));
+          __syncwarp();
+          for (int m = lane; m < M; m += 32)
+            bulk_g2s(rows + static_cast<size_t>(m) * rb, static_cast<const char*>(p.w_c) + static_cast<size_t>(ids[m]) * rb,
+                     rb, bar);
         }
-        cp_async_commit();
-        cp_async_wait_all();
-        __syncthreads();
+        if (!__syncthreads_and(wait_bar())) return false;
       }
       for (int m0 = warp * 8; m0 < M; m0 += kWarps * 8) {  // each warp: 8 consecutive rows at a time
         float d[8];
@@ -474,68 +481,95 @@ __device__ void frontier_phase(const Params& p, int s, unsigned char* smem, Owne
       __syncthreads();
       const float mx = s_red[0], lse = s_red[1];
       for (int m = t; m < M; m += kThreads) {
-        Entry e;
-        e.score = node_score + ((z[m] - mx) - lse);
+        Node e;
+        e.score = jb.score + ((z[m] - mx) - lse);
         e.token = ids[m];
-        e.parent = static_cast<short>(parent_idx);
-        e.depth = static_cast<short>(node_depth + 1);
-        e.seq = st.seq_next + m;
-        cand[F + m] = e;
+        e.seq = m;  // the candidate index until the node is popped
+        e.pslot = static_cast<short>(jb.xslot);
+        e.xslot = -1;
+        kraw[m] = e;
+        keys[m] = (static_cast<unsigned long long>(key_of_f32(__float_as_uint(e.score))) << 32) |
+                  static_cast<unsigned long long>(~static_cast<uint32_t>(e.token));
+      }
+      __syncthreads();
+      // rank among siblings (score, then token, then candidate index); keep the first kc: at most n - s - 1 of them
+      // can still be popped after the node itself (n for the root's)
+      const int kc = min(KM, jb.pslot < 0 ? n : n - st0.s - 1);
+      for (int i = t; i < M; i += kThreads) {
+        const unsigned long long ki = keys[i];
+        int r = 0;
+#pragma unroll 8
+        for (int c = 0; c < M; ++c) {
+          const unsigned long long kk = keys[c];
+          r += (kk > ki) | ((kk == ki) & (c < i));
+        }
+        if (r < kc) R.kids[static_cast<size_t>(jb.xslot) * KM + r] = kraw[i];
+      }
+      if (t == 0) R.kcount[jb.xslot] = kc;
+      __syncthreads();
+    }
+    // pops and the next wave's picks (one warp), then the picks join the next wave's packed list
+    if (warp == 0) request_step(R, b, n, M, p.max_depth, X, KM, kla, jobs, p.hdr);
+    __syncthreads();
+    const ReqCtl st = *R.ctl;
+    if (t == 0) s_off = st.njobs > 0 ? atomicAdd(p.jobcount + w + 1, st.njobs) : 0;
+    __syncthreads();
+    for (int q = t; q < st.njobs; q += kThreads) next[s_off + q] = jobs[q];
+    if (st.s >= n) {  // finished: the outputs, and each node's ancestor-mask row by walking its parent chain
+      const size_t o = static_cast<size_t>(b) * n;
+      for (int i = t; i < n; i += kThreads) {
+        const PopRec r = R.pops[i];
+        p.tokens[o + i] = r.token;
+        p.parents[o + i] = r.parent;
+        p.depth[o + i] = r.depth;
+        p.scores[o + i] = r.score;
+      }
+      for (int i = t; i < n * n; i += kThreads) {
+        const int row = i / n, c = i % n;
+        int a = row;
+        for (int hops = 0; a > c && hops < n; ++hops) a = R.pops[a].parent;  // parents precede their children
+        p.mask[(o + row) * n + c] = a == c;
       }
     }
+    // the state block goes back (one bulk copy; complete before the shared buffers are reused)
     __syncthreads();
-    // Keep the R = n - s best (nothing ranked below them can be popped in the n - s pops left): the sorted
-    // frontier merged with the ranked children (sorted[n, n + M) is free: R <= n).
-    const int N = F + C;
-    const int R = min(n - s, N);
-    merge_rank<kThreads>(cand, F, C, R, sorted + n, sorted);
-    const Entry pop = sorted[0];
-    for (int i = t + 1; i < R; i += kThreads) fr[i - 1] = sorted[i];
-    const size_t o = static_cast<size_t>(b) * n + s;
-    uint8_t* mrow = p.mask + o * n;
-    const uint8_t* prow = pop.parent >= 0 ? p.mask + (static_cast<size_t>(b) * n + pop.parent) * n : nullptr;
-    for (int j = t; j < n; j += kThreads) mrow[j] = (j == s) ? 1 : ((j < s && prow) ? prow[j] : 0);
     if (t == 0) {
-      p.tokens[o] = pop.token;
-      p.parents[o] = pop.parent;
-      p.depth[o] = pop.depth;
-      p.scores[o] = pop.score;
-      NodeState ns;
-      ns.token = pop.token;
-      ns.parent = pop.parent;
-      ns.depth = pop.depth;
-      ns.expand = (s + 1 < n) && (pop.depth < p.max_depth);
-      ns.score = pop.score;
-      ns.seq_next = st.seq_next + C;
-      ns.fcount = R - 1;
-      ns.pad = 0;
-      p.state[b] = ns;
-      if (slot < kSlots) {
-        own->st[slot] = ns;
-        own->pf_token[slot] = ns.expand ? ns.token : -1;
-        own->pf_pos[slot] = ns.expand ? static_cast<int>((static_cast<size_t>(b) * p.K + ns.depth) * M) : -1;
-      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      bulk_s2g(gstate, smem, static_cast<unsigned>(RL.bytes));
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
   }
+  return true;
 }
 
-// Runs between arriving at and waiting on the grid barrier that ends step s: the owned requests' next reads go to
-// L2 (warps 1.., so that thread 0 can poll the barrier). Pure hints: nothing waits for them.
-__device__ void prefetch_next(const Params& p, const OwnedState* own) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int owned = p.B > static_cast<int>(blockIdx.x) ? (p.B - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
-  const unsigned esize = p.bf16 ? 2u : 4u;
-  for (int slot = warp - 1; slot >= 0 && slot < min(owned, kSlots); slot += kWarps - 1) {
-    const int tok = own->pf_token[slot], pos = own->pf_pos[slot];
-    if (pos < 0) continue;
-    if (lane == 0)
-      prefetch_l2(static_cast<const char*>(p.emb) + static_cast<size_t>(tok) * p.E * esize, p.E * esize);
-    for (int m = lane; m < p.M; m += 32) {
-      const int id = __ldg(p.ids + pos + m);
-      if (static_cast<unsigned>(id) < static_cast<unsigned>(p.V))
-        prefetch_l2(static_cast<const char*>(p.w_c) + static_cast<size_t>(id) * p.H * esize, p.H * esize);
+// Before the first wave: every owned request's state block (the root expanded in wave 0 with h0, which becomes
+// slot 0's hidden state), and every wave's job count at zero.
+__device__ void init_requests(const Params& p, unsigned char* smem) {
+  const int t = threadIdx.x;
+  const int M = p.M, n = p.n, H = p.H, X = p.xslots, KM = M < n ? M : n;
+  const ReqLayout RL = req_layout(n, X, KM, p.lookahead);
+  for (int i = blockIdx.x * kThreads + t; i < X + 2; i += gridDim.x * kThreads) p.jobcount[i] = 0;
+  for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
+    const ReqView R = req_view(p.rstate + static_cast<size_t>(b) * RL.bytes, RL);
+    Job* jobs = reinterpret_cast<Job*>(p.rstate + static_cast<size_t>(b) * RL.bytes + RL.jobs);
+    if (t == 0) {
+      *R.ctl = ReqCtl{0, 0, M, 1, 1, {0, 0, 0}};  // the root's children take insertion indices 0 .. M - 1
+      jobs[0] = Job{b, 0, -1, 0, 0, 0.f, {0, 0}};
     }
+    if (t < 32) R.lanes[t] = t == 0 ? LaneSrc{-2, 0, 0, 0} : t == 1 ? LaneSrc{0, 0, -1, 0} : LaneSrc{-1, 0, 0, 0};
+    for (int i = t; i < X; i += kThreads) {
+      R.kcount[i] = 0;
+      R.popidx[i] = i == 0 ? -1 : -2;
+      R.sdepth[i] = 0;
+    }
+    for (int i = t; i < n; i += kThreads) R.pops[i] = PopRec{0, -1, 0, -INFINITY};
+    for (int i = t; i < H; i += kThreads)
+      p.hs[static_cast<size_t>(b) * X * H + i] = __ldg(p.h0 + static_cast<size_t>(b) * H + i);
   }
+  // the state blocks are read back through the async proxy (bulk copies)
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  (void)smem;
 }
 
 // kGemm: 0 = CUDA-core GRU tiles (fp32 weights or widths not multiples of 128), tensor cores with 1 = TileS,
@@ -546,41 +580,47 @@ __global__ void __launch_bounds__(kThreads, 1) build_kernel(Params p) {
   unsigned char* smem = reinterpret_cast<unsigned char*>(smem_f4);
   __shared__ int s_flag;
   __shared__ unsigned long long s_base;
-  __shared__ OwnedState own;
+  __shared__ uint64_t bar;  // completion of the frontier phase's bulk copies
+  unsigned bar_uses = 0;
   const unsigned G = gridDim.x;
-  if (threadIdx.x == 0) s_base = ld_relaxed_gpu_u64(&p.hdr->sync_count);  // before anyone can pass this barrier
+  if (threadIdx.x == 0) {
+    s_base = ld_relaxed_gpu_u64(&p.hdr->sync_count);  // before anyone can pass this barrier
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+  }
+  init_requests(p, smem);
   if (!grid_barrier(p.hdr, G, p.timeout_ns, &s_flag)) return;
   unsigned long long target = s_base;
-  for (int s = 0; s < p.n; ++s) {
-    if (s > 0) {
-      if (kGemm == 1) gemm_gru_phase<TileS, 32, 8>(p, s - 1, smem);
-      else if (kGemm == 2) gemm_gru_phase<TileL, 64, 16>(p, s - 1, smem);
-      else if (kGemm == 3) gemm_gru_phase<TileS128, 32, 8>(p, s - 1, smem);
-      else gru_phase(p, s - 1, reinterpret_cast<float*>(smem));
+  for (int w = 0; w < p.xslots; ++w) {
+    if (w > 0) {
+      const int rows = __ldcg(p.jobcount + w);
+      if (rows == 0) break;  // every request is finished (the same count in every CTA)
+      const Job* jl = p.joblist + static_cast<size_t>(w & 1) * p.B * p.lookahead;
+      if (kGemm == 1) gemm_gru_phase<TileS, 32, 8>(p, jl, rows, smem);
+      else if (kGemm == 2) gemm_gru_phase<TileL, 64, 16>(p, jl, rows, smem);
+      else if (kGemm == 3) gemm_gru_phase<TileS128, 32, 8>(p, jl, rows, smem);
+      else gru_phase(p, jl, rows, reinterpret_cast<float*>(smem));
       target += G;
       if (!counter_barrier(p.hdr, target, p.timeout_ns, &s_flag)) return;
     }
-    frontier_phase(p, s, smem, &own);
-    if (s + 1 < p.n) {
-      counter_arrive(p.hdr);
-      prefetch_next(p, &own);
-      target += G;
-      if (!counter_wait(p.hdr, target, p.timeout_ns, &s_flag)) return;
-    }
+    if (!frontier_phase(p, w, smem, &bar, bar_uses)) return;
+    target += G;
+    if (!counter_barrier(p.hdr, target, p.timeout_ns, &s_flag)) return;
   }
 }
 
 // Dynamic shared memory of the large-batch kernel; the gathered rows are staged only when they fit under both the
 // cap and the device's opt-in limit (`rows_smem` reports the choice).
-size_t smem_bytes(int gemm, int M, int n, int H, size_t esize, size_t optin, bool* rows_smem) {
+size_t smem_bytes(int gemm, int M, int n, int H, int kla, size_t esize, size_t optin, bool* rows_smem) {
   size_t a = sizeof(float) * (kTB * kPad + 3 * kTU * kPad);
   if (gemm == 1) a = TileS::kBytes;
   if (gemm == 2) a = TileL::kBytes;
   if (gemm == 3) a = TileS128::kBytes;
+  const int X = expansion_slots(n), KM = M < n ? M : n;
+  const FrontierSmem F = frontier_smem(req_layout(n, X, KM, kla).bytes, M, H);
   const size_t rows = static_cast<size_t>(M) * H * esize;
-  const size_t base = frontier_rows_offset(M, n, H);
-  *rows_smem = rows <= kFrontierRowsCap && base + rows <= optin;
-  const size_t b = base + (*rows_smem ? rows : 0);
+  *rows_smem = rows <= kFrontierRowsCap && F.bytes + rows <= optin;
+  const size_t b = F.bytes + (*rows_smem ? rows : 0);
   return a > b ? a : b;
 }
 
@@ -632,36 +672,43 @@ extern "C" dt_status dt_build_trees(int B, int K, int V, int M, int n, int max_d
   p.emb = w->emb; p.w_ih = w->w_ih; p.w_hh = w->w_hh; p.b_ih = w->b_ih; p.b_hh = w->b_hh; p.w_c = w->w_c;
   p.tokens = out_tokens; p.parents = out_parents; p.depth = out_depth; p.scores = out_scores; p.mask = out_mask;
   p.hdr = reinterpret_cast<WsHeader*>(ws);
-  p.state = reinterpret_cast<NodeState*>(ws + L.state);
-  p.frontier = reinterpret_cast<Entry*>(ws + L.frontier);
   p.hs = reinterpret_cast<float*>(ws + L.hs);
   p.acc = B <= kSmallMaxB ? reinterpret_cast<long long*>(ws + L.acc) : nullptr;
   p.hs_count = B <= kSmallMaxB ? reinterpret_cast<int*>(ws + L.hs_count) : nullptr;
+  p.rstate = reinterpret_cast<unsigned char*>(ws + L.rstate);
+  p.joblist = reinterpret_cast<Job*>(ws + L.joblist);
+  p.jobcount = reinterpret_cast<int*>(ws + L.jobcount);
   p.acc_stride = acc_stride(M, n);
   p.xslots = expansion_slots(n);
   p.timeout_ns = barrier_timeout_ns();
-  {  // expansions per request per wave: the setting, else as many as the small-batch builder's wave holds
-    const int k = lookahead_setting();
+  DeviceInfo di{};
+  if (current_device_info(&di) != cudaSuccess) return DT_ERR_CUDA;
+  if (!di.coop) return DT_ERR_UNSUPPORTED;
+  // expansions per request per wave: the setting, capped by what the builder's wave holds; by default all of the
+  // small-batch builder's wave, and kLargeDefault for the large-batch builder
+  const int k_set = lookahead_setting();
+  {
     const int fit = kWaveJobs / (B < kWaveJobs ? B : kWaveJobs);
-    p.lookahead = k > 0 ? (k < fit ? k : fit) : fit;
+    p.lookahead = k_set > 0 ? (k_set < fit ? k_set : fit) : fit;
   }
+  if (small_builder_fits(p, di)) return cuda_status(launch_small_builder(p, di, stream));
+  p.lookahead = k_set > 0 ? (k_set < kLargeLookahead ? k_set : kLargeLookahead) : kLargeDefault;
 
-  // phase A: tensor cores for bf16 weights whose widths are multiples of the 128-column pipeline chunk
+  // phase A: tensor cores for bf16 weights whose widths are multiples of the pipeline chunk; the larger tile once a
+  // wave can hold 128 expansions or more
+  const long long max_rows = static_cast<long long>(B) * p.lookahead;
   const int gemm = !p.bf16 ? 0
-                   : B >= 128 ? (E % TileL::kKc == 0 && H % TileL::kKc == 0 ? 2 : 0)
+                   : max_rows >= 128 ? (E % TileL::kKc == 0 && H % TileL::kKc == 0 ? 2 : 0)
                    : E % TileS::kKc == 0 && H % TileS::kKc == 0 ? 1
                    : E % TileS128::kKc == 0 && H % TileS128::kKc == 0 ? 3 : 0;
   const void* fn = gemm == 0 ? reinterpret_cast<const void*>(build_kernel<0>)
                              : gemm == 3 ? reinterpret_cast<const void*>(build_kernel<3>)
                              : gemm == 1 ? reinterpret_cast<const void*>(build_kernel<1>)
                                          : reinterpret_cast<const void*>(build_kernel<2>);
-  DeviceInfo di{};
-  if (current_device_info(&di) != cudaSuccess) return DT_ERR_CUDA;
-  if (!di.coop) return DT_ERR_UNSUPPORTED;
-  if (small_builder_fits(p, di)) return cuda_status(launch_small_builder(p, di, stream));
   // static shared memory of the kernel (flags, reductions) is well under 1 KB; one CTA per SM (launch bounds), so
   // the shared memory alone decides whether a CTA fits
-  const size_t smem = smem_bytes(gemm, M, n, H, p.bf16 ? 2 : 4, static_cast<size_t>(di.optin) - 1024, &p.rows_smem);
+  const size_t smem = smem_bytes(gemm, M, n, H, p.lookahead, p.bf16 ? 2 : 4, static_cast<size_t>(di.optin) - 1024,
+                                 &p.rows_smem);
   if (smem + 1024 > static_cast<size_t>(di.optin)) return DT_ERR_UNSUPPORTED;
   if (ensure_dynamic_smem(fn, smem) != cudaSuccess) return DT_ERR_CUDA;
   const unsigned grid = static_cast<unsigned>(di.sms);  // one CTA per SM; co-resident under a cooperative launch

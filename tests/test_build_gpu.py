@@ -146,6 +146,10 @@ def test_out_of_range_ids_are_reported_not_gathered(dtlib):
     dict(config=3, B=2),                                               # deeper trees (T = 0.5)
     dict(tiny=dict(dtype="bf16", M=40, n=64, max_depth=5, K=5, B=1)),  # wide and deep
     dict(tiny=dict(M=1, n=4, max_depth=4, B=1)),                       # a chain: nothing to look ahead at
+    dict(config=2, B=16),                                              # the large-batch builder
+    dict(config=3, B=12),                                              # ... deeper trees, H = 1024
+    dict(config=4, B=12),                                              # ... M = 128, n = 64
+    dict(tiny=dict(B=20, M=6, n=30, max_depth=4)),                     # ... fp32, CUDA-core GRU tiles
 ])
 def test_lookahead_width_does_not_change_the_tree(dtlib, case):
     """Expanding several frontier nodes per wave only changes when children become known, never the pop order:
