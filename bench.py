@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--builder", choices=["conditional", "marginal"], default="conditional",
+                    help="conditional: dt_build_trees (the method); marginal: dt_build_trees_marginal (DDTree scoring)")
     ap.add_argument("--reference-budget", type=float, default=150.0, help="seconds for the whole reference arm")
     return ap.parse_args()
 
@@ -198,6 +200,7 @@ def run_ours(args, world, rank, local):
     rnd = dt.Round(s.B, s.K, s.V, s.M, s.n, s.max_depth, s.T, w, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+    marginal = args.builder == "marginal"
 
     def step(evs=None):
         flush.zero_()
@@ -206,7 +209,10 @@ def run_ours(args, world, rank, local):
         rnd.topm(inp.logits, stream)
         if evs:
             evs[1].record(stream)
-        rnd.build(inp.h0, stream)
+        if marginal:
+            rnd.build_marginal(stream)
+        else:
+            rnd.build(inp.h0, stream)
         if evs:
             evs[2].record(stream)
 
@@ -244,6 +250,9 @@ def run_ours(args, world, rank, local):
 
     out = {k: v.cpu().numpy() for k, v in rnd.out.items()}
     topm_b, build_b, parts = algorithmic_bytes(s, out["tokens"], out["parents"], out["depth"])
+    if marginal:  # no GRU, no correction rows: the candidates' ids and values read, the tree written
+        build_b = s.B * s.K * s.M * 8 + s.B * s.n * 16 + s.B * s.n * s.n
+        parts = dict(ids_vals=s.B * s.K * s.M * 8)
     peak, peak_src = measured_peaks()
     kernels = {
         "dt_topm": dict(us=float(topm_ms.mean() * 1e3), bytes=topm_b, gbps=topm_b / (topm_ms.mean() * 1e6),
@@ -260,7 +269,7 @@ def run_ours(args, world, rank, local):
                 else {"logits": s.B * s.K * s.V * (4 if s.dtype == "f32" else 2)}}
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not marginal:
         hr = dt.HostRound(s.B, s.K, s.V, s.M, s.n, s.max_depth, s.T, w, inp.logits.dtype, device=dev)
         h_logits = dt.pinned_like(inp.logits)
         h_logits.copy_(inp.logits)
@@ -292,7 +301,7 @@ def run_ours(args, world, rank, local):
                "us_per_round": round(e2e_s / args.steps * 1e6, 2)}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not marginal:
         cpu = cpu_baseline(inp, args.cpu_budget)
 
     if rank != 0:
@@ -303,7 +312,7 @@ def run_ours(args, world, rank, local):
         "us_per_round": round(total_s / args.steps * 1e6, 2), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": round(value / (1e3 / PAGES_MS_PER_ROUND), 3) if args.config == 1 else None,
         "dtype": "f32", "inputs_dtype": s.dtype, "data": "synthetic",
-        "config": {"workload": s.describe(), "B_per_gpu": s.B,
+        "config": {"workload": s.describe() + (" marginal-scoring" if marginal else ""), "B_per_gpu": s.B,
                    "l2": "flushed between steps (256 MB memset outside the timed events)"},
         "kernels": {k: {kk: (round(vv, 3) if isinstance(vv, float) else vv) for kk, vv in d.items()}
                     for k, d in kernels.items()},

@@ -130,6 +130,25 @@ dt_status dt_build_trees(int B, int K, int V, int M, int n, int max_depth, float
                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------------------------------------------
+ * dt_build_trees_marginal — the same best-first draft trees scored by DDTree's factorised marginals.
+ * Source: blog.captcha.la, "Methodology — deep read" (DDTree scores tree nodes by factorised marginal
+ * log-probabilities) and "Key findings" (the ablation that changes only the scoring function: conditional scoring
+ * +9.2% throughput over marginal scoring); zhichai.top, "两条路线的困境"; gist.science, "Énoncé du Problème" (in the
+ * factorised formulations a token's score depends only on its position).
+ *
+ * Semantics: dt_build_trees with no correction and no hidden state: a child at block position d scores
+ *     score_parent + logp_m,   logp_m = z_m - max(z) - log(sum_j exp(z_j - max(z))),   z_m = topm_vals[b,d,m] / T_eff
+ * with the same pops, ties, budget, depth limit and outputs (and, on the GPU, the same fp32 arithmetic as
+ * dt_build_trees with w_c = 0, so the trees are identical to those). Arguments as dt_build_trees, without h0 and
+ * weights; `workspace` needs only its 256-byte header (the status word; a round's workspace serves). One CTA per
+ * request keeps the request's state in shared memory: sizes whose state does not fit return DT_ERR_UNSUPPORTED.
+ * ------------------------------------------------------------------------------------------------------------- */
+dt_status dt_build_trees_marginal(int B, int K, int V, int M, int n, int max_depth, float T, const int32_t* topm_ids,
+                                  const float* topm_vals, int32_t* out_tokens, int32_t* out_parents,
+                                  int32_t* out_depth, float* out_scores, uint8_t* out_mask, void* workspace,
+                                  size_t workspace_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------------------------------------
  * dt_topm_static — dt_topm for callers that cannot allocate device memory.
  * No counterpart in the paper: this is a deployment variant of dt_topm, with the same arguments minus the
  * workspace and bit-identical results.

@@ -57,6 +57,8 @@ def load(path=None) -> ctypes.CDLL:
                                     _P, _P, _P, _P, _P, _P, _I]
     lib.orc_rescore.argtypes = [_I, _I, _I, _I, _I, _D, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P,
                                 _P, _P, _P, _P, _I]
+    lib.orc_build_trees_marginal.argtypes = [_I, _I, _I, _I, _I, _D, _P, _P, _P, _P, _P, _P, _P, _P, _I]
+    lib.orc_build_trees_marginal.restype = _I
     lib.orc_tree_size.argtypes = [_I, _I, ctypes.c_longlong]
     lib.orc_tree_size.restype = ctypes.c_longlong
     for f in (lib.orc_topm, lib.orc_gru_step, lib.orc_child_logp, lib.orc_build_trees, lib.orc_rescore):
@@ -147,6 +149,21 @@ def build_trees(ids, vals, h0, w: dict, n: int, max_depth: int, T: float, thread
     _check(L.orc_build_trees(B, K, M, n, max_depth, float(T), _ptr(ids), _ptr(vals), _ptr(h0), H, E, wd, emb, wih,
                              whh, bih, bhh, wc, _ptr(out["tokens"]), _ptr(out["parents"]), _ptr(out["depth"]),
                              _ptr(out["scores"]), _ptr(out["mask"]), _ptr(out["gaps"]), threads))
+    return out
+
+
+def build_trees_marginal(ids, vals, n: int, max_depth: int, T: float, threads: int = 0, L=None) -> dict:
+    """DDTree's factorised best-first trees from top-M candidates (no GRU, no correction)."""
+    L = L or lib()
+    B, K, M = ids.shape
+    ids = np.ascontiguousarray(ids, np.int32)
+    vals = np.ascontiguousarray(vals, np.float64)
+    out = dict(tokens=np.empty((B, n), np.int32), parents=np.empty((B, n), np.int32),
+               depth=np.empty((B, n), np.int32), scores=np.empty((B, n), np.float64),
+               mask=np.empty((B, n, n), np.uint8), gaps=np.empty((B, n), np.float64))
+    _check(L.orc_build_trees_marginal(B, K, M, n, max_depth, float(T), _ptr(ids), _ptr(vals), _ptr(out["tokens"]),
+                                      _ptr(out["parents"]), _ptr(out["depth"]), _ptr(out["scores"]),
+                                      _ptr(out["mask"]), _ptr(out["gaps"]), threads))
     return out
 
 

@@ -53,6 +53,8 @@ SIGNATURES = {
     "dt_build_trees": (_I, [_I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _P, ctypes.POINTER(_Weights), _P, _P,
                             _P, _P, _P, _P, _SZ, _P]),
     "dt_topm_static": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "dt_build_trees_marginal": (_I, [_I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                                     _P]),
     "dt_get_error": (_I, [_P, _P]),
     "dt_set_barrier_timeout_ns": (None, [ctypes.c_uint64]),
     "dt_set_lookahead": (_I, [_I]),
@@ -229,6 +231,26 @@ def dt_build_trees(topm_ids: torch.Tensor, topm_vals: torch.Tensor, h0: torch.Te
     return out
 
 
+def dt_build_trees_marginal(topm_ids: torch.Tensor, topm_vals: torch.Tensor, V: int, n: int, max_depth: int,
+                            T: float, out: Optional[dict] = None, workspace: Optional[torch.Tensor] = None,
+                            stream=None) -> dict:
+    """DDTree's factorised best-first trees (no GRU, no correction) -> the same outputs as dt_build_trees."""
+    B, K, M = topm_ids.shape
+    dev = topm_ids.device
+    if out is None:
+        out = alloc_tree_outputs(B, n, dev)
+    if workspace is None:
+        workspace = new_workspace(256, dev)
+    _check(lib().dt_build_trees_marginal(
+        B, K, V, M, n, max_depth, float(T), _dev(topm_ids, "topm_ids", torch.int32, (B, K, M)),
+        _dev(topm_vals, "topm_vals", torch.float32, (B, K, M)), _dev(out["tokens"], "out_tokens", torch.int32, (B, n)),
+        _dev(out["parents"], "out_parents", torch.int32, (B, n)), _dev(out["depth"], "out_depth", torch.int32, (B, n)),
+        _dev(out["scores"], "out_scores", torch.float32, (B, n)),
+        _dev(out["mask"], "out_mask", torch.uint8, (B, n, n)), _dev(workspace, "workspace", torch.uint8),
+        workspace.numel(), _stream(stream)), "dt_build_trees_marginal")
+    return out
+
+
 def alloc_tree_outputs(B: int, n: int, device) -> dict:
     return dict(tokens=torch.empty((B, n), dtype=torch.int32, device=device),
                 parents=torch.empty((B, n), dtype=torch.int32, device=device),
@@ -284,6 +306,20 @@ class Round:
                 _dev(self.workspace, "workspace", torch.uint8), self.workspace.numel(), st)
             self._build_key = key
         _check(lib().dt_build_trees(*self._build_args), "dt_build_trees")
+        return self.out
+
+    def build_marginal(self, stream=None) -> dict:
+        """dt_build_trees_marginal (DDTree's factorised scoring) from this round's ids/vals into its outputs."""
+        st = _stream(stream)
+        if getattr(self, "_marg_key", None) != st:
+            o = self.out
+            self._marg_args = (self.B, self.K, self.V, self.M, self.n, self.max_depth, float(self.T),
+                               _dev(self.ids, "topm_ids"), _dev(self.vals, "topm_vals"), _dev(o["tokens"], "out_tokens"),
+                               _dev(o["parents"], "out_parents"), _dev(o["depth"], "out_depth"),
+                               _dev(o["scores"], "out_scores"), _dev(o["mask"], "out_mask"),
+                               _dev(self.workspace, "workspace", torch.uint8), self.workspace.numel(), st)
+            self._marg_key = st
+        _check(lib().dt_build_trees_marginal(*self._marg_args), "dt_build_trees_marginal")
         return self.out
 
     def __call__(self, logits: torch.Tensor, h0: torch.Tensor, stream=None) -> dict:

@@ -213,6 +213,34 @@ def pin_factorised_closed_form(L):
         check_against_bruteforce({k: tree[k][0] for k in ("tokens", "parents", "scores")}, nodes, 25)
 
 
+def pin_marginal_builder(L):
+    """DDTree's marginal-scored trees: the n best nodes of the depth-limited tree under the product of the
+    per-position marginals (log-softmax by torch, exhaustive enumeration), and the conditional builder at W_c = 0."""
+    from oracle import oracle as orc
+    cases = [(51, dict(M=5, n=25, max_depth=4, T=0.0)), (52, dict(M=3, n=30, max_depth=4, T=0.5)),
+             (53, dict(M=4, n=12, max_depth=3, T=2.0, logit_scale=0.2)), (54, dict(M=1, n=4, max_depth=4, K=4))]
+    for seed, kw in cases:
+        inp = tiny_inputs(seed, **kw)
+        s = inp.shape
+        logits, h0, w = host(inp)
+        ids, vals = orc.topm(logits, s.M, L=L)
+        tree = orc.build_trees_marginal(ids, vals, s.n, s.max_depth, s.T, L=L)
+        Te = s.T if s.T > 0 else 1.0
+        marg = torch.log_softmax(torch.from_numpy(vals[0]) / Te, dim=1).numpy()
+        nodes = {pth: math.fsum(marg[d][list(ids[0, d]).index(t)] for d, t in enumerate(pth))
+                 for pth in _all_paths(ids[0], s.max_depth)}
+        one = {k: tree[k][0] for k in ("tokens", "parents", "scores")}
+        check_against_bruteforce(one, nodes, s.n)
+        check_invariants(tree["tokens"][0], tree["parents"][0], tree["depth"][0], tree["scores"][0], tree["mask"][0],
+                         s.n, s.max_depth)
+        w0 = dict(w)
+        w0["w_c"] = np.zeros_like(w["w_c"])
+        cond = orc.build_trees(ids, vals, h0, w0, s.n, s.max_depth, s.T, L=L)
+        for k in ("tokens", "parents", "depth", "mask"):
+            assert np.array_equal(cond[k], tree[k]), k
+        assert np.max(np.abs(cond["scores"] - tree["scores"])) < 1e-12
+
+
 def _all_paths(ids, max_depth):
     out, level = [], [()]
     for d in range(max_depth):
@@ -347,4 +375,4 @@ def pin_rescore(L):
 
 
 ALL_PINS = [pin_topm_bruteforce, pin_gru_vs_grucell, pin_full_vocab_softmax, pin_golden, pin_special_cases,
-            pin_factorised_closed_form, pin_bruteforce_tree, pin_invariants, pin_rescore]
+            pin_factorised_closed_form, pin_bruteforce_tree, pin_invariants, pin_rescore, pin_marginal_builder]

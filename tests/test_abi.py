@@ -122,3 +122,23 @@ def test_lookahead_setting_is_validated(dtlib):
     assert L.dt_set_lookahead(9) == INVALID
     for k in (1, 8, 0):
         assert L.dt_set_lookahead(k) == OK
+
+
+def test_marginal_rejects_bad_arguments(dtlib):
+    L = dtlib.lib()
+    f = L.dt_build_trees_marginal
+    good = dict(B=1, K=4, V=100, M=5, n=8, max_depth=4, T=0.0)
+
+    def call(**kw):
+        a = dict(good, **kw)
+        return f(a["B"], a["K"], a["V"], a["M"], a["n"], a["max_depth"], a["T"], A, A, A, A, A, A, A, A,
+                 kw.get("wsb", 1 << 20), None)
+    assert call(M=0) == INVALID
+    assert call(M=101) == INVALID
+    assert call(max_depth=5) == INVALID
+    assert call(T=-1.0) == INVALID
+    assert call(n=10 ** 6, M=2, max_depth=2) == INVALID     # more nodes than the depth-limited tree has
+    assert call(wsb=16) == INVALID                           # no room for the status word
+    assert call(M=2000, V=5000) == UNSUPPORTED
+    assert f(1, 4, 100, 5, 8, 4, 0.0, A, A, A, A, A, A, A + 8, A, 1 << 20, None) == INVALID  # misaligned
+    assert call(B=0) == OK

@@ -1,0 +1,80 @@
+"""dt_build_trees_marginal (DDTree's factorised scoring) on the GPU: parity with the CPU oracle's marginal builder
+(structure bit-exact up to the first near-tie, scores within 1e-3 of the oracle's fp64 rescoring of the GPU's own
+tree), and bit-identity with dt_build_trees when the correction head is zero."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import compare
+from speculative_decoding_tree_top_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-3
+
+
+def zero_correction(dtlib, inp):
+    w = dtlib.Weights.of(inp)
+    return dtlib.Weights(w.emb, w.w_ih, w.w_hh, w.b_ih, w.b_hh, torch.zeros_like(w.w_c))
+
+
+def run_marginal(dtlib, orc, inp):
+    s = inp.shape
+    ids, vals = dtlib.dt_topm(inp.logits, s.M)
+    ws = dtlib.new_workspace(256)
+    out = dtlib.dt_build_trees_marginal(ids, vals, s.V, s.n, s.max_depth, s.T, workspace=ws)
+    torch.cuda.synchronize()
+    assert dtlib.dt_get_error(ws) == dtlib.Status.OK
+    ids_h, vals_h = ids.cpu().numpy(), vals.cpu().numpy().astype(np.float64)
+    ora = orc.build_trees_marginal(ids_h, vals_h, s.n, s.max_depth, s.T)
+    gpu = {k: v.cpu().numpy() for k, v in out.items()}
+    # fp64 scores of the GPU's own tree under the factorised scoring: the conditional oracle with W_c = 0
+    w = orc.weights_of(inp)
+    w["w_c"] = np.zeros_like(w["w_c"])
+    h0 = synth.host_array(inp.h0).astype(np.float64)
+    resc = orc.rescore(ids_h, vals_h, h0, w, gpu["tokens"], gpu["parents"], gpu["depth"], s.max_depth, s.T)
+    rep = compare.compare_round(gpu, ora, resc, s.n, s.max_depth, TOL)
+    return rep, out, (ids, vals)
+
+
+@pytest.mark.parametrize("config", [0, 1, 2, 3, 4])
+def test_marginal_parity_workloads(dtlib, orc, config):
+    inp = synth.make_inputs(config, device="cuda")
+    rep, *_ = run_marginal(dtlib, orc, inp)
+    print(config, rep)
+    # marginals of bf16 logits tie exactly and often (equal logits, equal log-probabilities), so the structure is
+    # compared bit-exactly only up to the first tie; the bit-exact check of the whole tree is the one against the
+    # conditional builder at W_c = 0 below
+    assert rep["compared_pops"] > 0 and rep["max_err_own"] < TOL
+
+
+@pytest.mark.parametrize("kw", [
+    dict(M=1, n=4, max_depth=4),            # a chain, all scores 0
+    dict(max_depth=1, n=5),                 # the best children of the root
+    dict(n=1),                              # the arg-max
+    dict(M=2, n=30, max_depth=4, K=4),      # the whole depth-limited tree
+    dict(B=300, n=10),                      # more requests than SMs
+    dict(M=40, n=64, max_depth=5, K=5),     # wide and deep
+])
+def test_marginal_edge_cases(dtlib, orc, kw):
+    base = dict(B=2, V=600, K=5, M=6, H=16, E=24, n=12, max_depth=4, T=0.5, dtype="f32", logit_scale=3.0,
+                boost_count=8, boost_lo=2.0, boost_hi=6.0, name="edge")
+    base.update(kw)
+    inp = synth.make_inputs(synth.Shape(**base), device="cuda", seed=7)
+    run_marginal(dtlib, orc, inp)
+
+
+@pytest.mark.parametrize("config,B", [(1, 1), (2, 64), (0, 1), (4, 16)])
+def test_marginal_equals_conditional_at_zero_correction(dtlib, config, B):
+    """The factorised tree is the conditional one with W_c = 0, to the bit (both builders share the per-node
+    arithmetic: a zero correction adds exactly 0.0)."""
+    inp = synth.make_inputs(synth.shape(config, B=B), device="cuda")
+    s = inp.shape
+    rnd = dtlib.Round(s.B, s.K, s.V, s.M, s.n, s.max_depth, s.T, zero_correction(dtlib, inp))
+    cond = {k: v.clone() for k, v in rnd(inp.logits, inp.h0).items()}
+    torch.cuda.synchronize()
+    rnd.check()
+    marg = dtlib.dt_build_trees_marginal(rnd.ids, rnd.vals, s.V, s.n, s.max_depth, s.T, workspace=rnd.workspace)
+    torch.cuda.synchronize()
+    rnd.check()
+    for k in cond:
+        assert torch.equal(cond[k], marg[k]), k
