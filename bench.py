@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--with-accept", action="store_true",
+                    help="also time dt_accept_paths on the round's trees (synthetic target tokens), reported apart")
     ap.add_argument("--builder", choices=["conditional", "marginal"], default="conditional",
                     help="conditional: dt_build_trees (the method); marginal: dt_build_trees_marginal (DDTree scoring)")
     ap.add_argument("--reference-budget", type=float, default=150.0, help="seconds for the whole reference arm")
@@ -267,6 +269,34 @@ def run_ours(args, world, rank, local):
                 "frac": round(kd["gbps"] / peak, 4), "traffic": traffic, "peak_source": peak_src,
                 "algorithmic_bytes_per_launch": kd["bytes"], "bytes_breakdown": parts if dom == "dt_build_trees"
                 else {"logits": s.B * s.K * s.V * (4 if s.dtype == "f32" else 2)}}
+
+    if args.with_accept:  # the step after verification, timed on its own (inputs resident, after the timed loop)
+        tn = torch.from_numpy(synth.make_target_next(out["tokens"], out["parents"], s.V, 0.9, seed=rank)).to(dev)
+        acc_out = dt.dt_accept_paths(rnd.out["tokens"], rnd.out["parents"], tn, stream=stream)
+        for _ in range(args.warmup):
+            dt.dt_accept_paths(rnd.out["tokens"], rnd.out["parents"], tn, acc_out, stream)
+        # a launch of one warp per request is shorter than its host-side call, so the calls are captured in a CUDA
+        # graph and replayed: the events then time the GPU, not the Python caller
+        reps = 32
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side), torch.cuda.graph(graph, stream=side):
+            for _ in range(reps):
+                dt.dt_accept_paths(rnd.out["tokens"], rnd.out["parents"], tn, acc_out, side)
+        stream.wait_stream(side)
+        graph.replay()
+        ea = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        for a, b in ea:
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        acc_ms = np.array([a.elapsed_time(b) for a, b in ea]) / reps
+        kernels["dt_accept_paths"] = dict(us=float(acc_ms.mean() * 1e3), bytes=s.B * s.n * 8 + s.B * (s.n + 1) * 4,
+                                          mean_accept_len=float(acc_out["accept_len"].float().mean().item()),
+                                          sources=["accept.cu"])
 
     e2e = None
     if not args.no_e2e and not marginal:

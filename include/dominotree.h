@@ -149,6 +149,27 @@ dt_status dt_build_trees_marginal(int B, int K, int V, int M, int n, int max_dep
                                   size_t workspace_bytes, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------------------------------------------
+ * dt_accept_paths — the accepted path of each draft tree after the target model's verify pass.
+ * Source: blog.captcha.la, "Methodology — deep read" (one target forward pass over the tree with the ancestor-only
+ * mask; the longest accepted root-to-leaf path is kept) and "Threat model" (lossless up to floating-point ties);
+ * gist.science, "Composants Clés — Vérification", "Résultats Expérimentaux" (output equal to serial greedy decoding).
+ *
+ * Greedy verification: target_next[b,0] is the target's next token after the accepted prefix (the root), and
+ * target_next[b,1+i] its next token after tree node i. From the root, the walk steps into the child whose token is
+ * the target's next token at the current node (the earlier pop if two children carry it) until none does.
+ *   tokens, parents     [B,n] int32, a tree as dt_build_trees emits it (every parent precedes its children; for
+ *                       other input the result is unspecified but the call terminates and stays in bounds).
+ *   target_next         [B,n+1] int32.
+ *   out_accept_len      [B] int32: accepted draft tokens (0..max depth); the round emits out_accept_len + 1 tokens.
+ *   out_path            [B,n] int32: the accepted nodes in path order, then -1. These are also the KV-compaction
+ *                       indices: the verify pass's cache entry of tree position out_path[b,j] moves to prefix + j.
+ *   out_bonus           [B] int32: the target's next token after the last accepted node.
+ * Pointers must be 4-byte aligned device pointers. n <= DT_MAX_N.
+ * ------------------------------------------------------------------------------------------------------------- */
+dt_status dt_accept_paths(int B, int n, const int32_t* tokens, const int32_t* parents, const int32_t* target_next,
+                          int32_t* out_accept_len, int32_t* out_path, int32_t* out_bonus, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------------------------------------
  * dt_topm_static — dt_topm for callers that cannot allocate device memory.
  * No counterpart in the paper: this is a deployment variant of dt_topm, with the same arguments minus the
  * workspace and bit-identical results.

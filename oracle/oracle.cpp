@@ -22,6 +22,8 @@
 //                     W_c = 0 factorised closed form; the M = 1 / max_depth = 1 / n = 1 special cases.
 //   orc_rescore     - pinned: must reproduce orc_build_trees' own scores on its own trees, and the brute-force
 //                     path scores.
+//   orc_accept_paths - pinned: the longest path, among all root-to-node paths enumerated, whose tokens agree with
+//                     the target's next tokens along it; special cases (all rejected, a whole chain accepted).
 //   orc_build_trees_marginal - pinned: brute-force enumeration of the depth-limited tree under the product of the
 //                     marginals (log-softmax by torch), and equality with orc_build_trees at W_c = 0.
 //   The GRU gate layout (rows r|z|n, PyTorch convention) and the order "add correction, then divide by T" are
@@ -309,6 +311,37 @@ int build_one_marginal(const int32_t* ids, const double* vals, int M, int n, int
   return ORC_OK;
 }
 
+// ---------------------------------------------------------------------------------------------------------------
+// Acceptance of a verified tree. [S] "Methodology — deep read": one target forward pass over the tree (ancestor-only
+// mask) verifies it and the longest accepted root-to-leaf path is kept; [S] "Threat model" and [G] "Résultats
+// Expérimentaux": lossless, the output equals serial greedy decoding. Reading (greedy verification): target_next[0]
+// is the target's next token after the accepted prefix, target_next[1 + i] its next token after node i; a path
+// v1 .. vk is accepted when token(v1) = target_next[0] and token(v_{j+1}) = target_next[1 + v_j]; the bonus token is
+// the target's next token after the last accepted node. If two children of a node carry the same token, the earlier
+// pop is taken. Returns ORC_ERR_TREE unless every parent precedes its child.
+int accept_one(int n, const int32_t* tokens, const int32_t* parents, const int32_t* target_next, int32_t* accept_len,
+               int32_t* path, int32_t* bonus) {
+  for (int i = 0; i < n; ++i)
+    if (parents[i] < -1 || parents[i] >= i) return ORC_ERR_TREE;
+  int cur = -1, len = 0, want = target_next[0];
+  while (true) {
+    int next = -1;
+    for (int i = 0; i < n; ++i)
+      if (parents[i] == cur && tokens[i] == want) {
+        next = i;
+        break;
+      }
+    if (next < 0) break;
+    path[len++] = next;
+    cur = next;
+    want = target_next[1 + next];
+  }
+  for (int i = len; i < n; ++i) path[i] = -1;
+  *accept_len = len;
+  *bonus = want;
+  return ORC_OK;
+}
+
 int threads_or_default(int threads) {
 #ifdef _OPENMP
   return threads > 0 ? threads : omp_get_max_threads();
@@ -400,6 +433,20 @@ int orc_build_trees_marginal(int B, int K, int M, int n, int max_depth, double T
     }
   }
   return status;
+}
+
+// Accepted paths of B verified trees: tokens/parents [B,n], target_next [B,n+1] -> accept_len [B], path [B,n]
+// (node indices in path order, then -1), bonus [B].
+int orc_accept_paths(int B, int n, const int32_t* tokens, const int32_t* parents, const int32_t* target_next,
+                     int32_t* accept_len, int32_t* path, int32_t* bonus) {
+  if (!tokens || !parents || !target_next || !accept_len || !path || !bonus || B < 0 || n < 1) return ORC_ERR_ARG;
+  for (int b = 0; b < B; ++b) {
+    const size_t nb = static_cast<size_t>(b) * n;
+    const int s = accept_one(n, tokens + nb, parents + nb, target_next + static_cast<size_t>(b) * (n + 1),
+                             accept_len + b, path + nb, bonus + b);
+    if (s != ORC_OK) return s;
+  }
+  return ORC_OK;
 }
 
 // Scores of given trees (tokens/parents/depth [B,n], in any valid prefix order), recomputed in fp64.

@@ -59,6 +59,8 @@ def load(path=None) -> ctypes.CDLL:
                                 _P, _P, _P, _P, _I]
     lib.orc_build_trees_marginal.argtypes = [_I, _I, _I, _I, _I, _D, _P, _P, _P, _P, _P, _P, _P, _P, _I]
     lib.orc_build_trees_marginal.restype = _I
+    lib.orc_accept_paths.argtypes = [_I, _I, _P, _P, _P, _P, _P, _P]
+    lib.orc_accept_paths.restype = _I
     lib.orc_tree_size.argtypes = [_I, _I, ctypes.c_longlong]
     lib.orc_tree_size.restype = ctypes.c_longlong
     for f in (lib.orc_topm, lib.orc_gru_step, lib.orc_child_logp, lib.orc_build_trees, lib.orc_rescore):
@@ -164,6 +166,20 @@ def build_trees_marginal(ids, vals, n: int, max_depth: int, T: float, threads: i
     _check(L.orc_build_trees_marginal(B, K, M, n, max_depth, float(T), _ptr(ids), _ptr(vals), _ptr(out["tokens"]),
                                       _ptr(out["parents"]), _ptr(out["depth"]), _ptr(out["scores"]),
                                       _ptr(out["mask"]), _ptr(out["gaps"]), threads))
+    return out
+
+
+def accept_paths(tokens, parents, target_next, L=None) -> dict:
+    """Accepted path of each verified tree: accept_len [B], path [B,n] (node indices, then -1), bonus [B]."""
+    L = L or lib()
+    B, n = tokens.shape
+    tokens = np.ascontiguousarray(tokens, np.int32)
+    parents = np.ascontiguousarray(parents, np.int32)
+    target_next = np.ascontiguousarray(target_next, np.int32)
+    assert target_next.shape == (B, n + 1)
+    out = dict(accept_len=np.empty(B, np.int32), path=np.empty((B, n), np.int32), bonus=np.empty(B, np.int32))
+    _check(L.orc_accept_paths(B, n, _ptr(tokens), _ptr(parents), _ptr(target_next), _ptr(out["accept_len"]),
+                              _ptr(out["path"]), _ptr(out["bonus"])))
     return out
 
 

@@ -53,6 +53,7 @@ SIGNATURES = {
     "dt_build_trees": (_I, [_I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _P, ctypes.POINTER(_Weights), _P, _P,
                             _P, _P, _P, _P, _SZ, _P]),
     "dt_topm_static": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "dt_accept_paths": (_I, [_I, _I, _P, _P, _P, _P, _P, _P, _P]),
     "dt_build_trees_marginal": (_I, [_I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
                                      _P]),
     "dt_get_error": (_I, [_P, _P]),
@@ -248,6 +249,25 @@ def dt_build_trees_marginal(topm_ids: torch.Tensor, topm_vals: torch.Tensor, V: 
         _dev(out["scores"], "out_scores", torch.float32, (B, n)),
         _dev(out["mask"], "out_mask", torch.uint8, (B, n, n)), _dev(workspace, "workspace", torch.uint8),
         workspace.numel(), _stream(stream)), "dt_build_trees_marginal")
+    return out
+
+
+def dt_accept_paths(tokens: torch.Tensor, parents: torch.Tensor, target_next: torch.Tensor, out: Optional[dict] = None,
+                    stream=None) -> dict:
+    """Accepted path of each verified tree -> accept_len [B], path [B,n] (node indices, then -1), bonus [B]."""
+    B, n = tokens.shape
+    dev = tokens.device
+    if out is None:
+        out = dict(accept_len=torch.empty(B, dtype=torch.int32, device=dev),
+                   path=torch.empty((B, n), dtype=torch.int32, device=dev),
+                   bonus=torch.empty(B, dtype=torch.int32, device=dev))
+    _check(lib().dt_accept_paths(B, n, _dev(tokens, "tokens", torch.int32, (B, n)),
+                                 _dev(parents, "parents", torch.int32, (B, n)),
+                                 _dev(target_next, "target_next", torch.int32, (B, n + 1)),
+                                 _dev(out["accept_len"], "out_accept_len", torch.int32, (B,)),
+                                 _dev(out["path"], "out_path", torch.int32, (B, n)),
+                                 _dev(out["bonus"], "out_bonus", torch.int32, (B,)), _stream(stream)),
+           "dt_accept_paths")
     return out
 
 

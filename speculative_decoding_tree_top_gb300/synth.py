@@ -198,3 +198,23 @@ def host_array(t: Optional[torch.Tensor]):
     if t.dtype == torch.bfloat16:
         return bits_u16(t)
     return t.detach().to("cpu").contiguous().numpy()
+
+
+def make_target_next(tokens, parents, V: int, p_agree: float, seed: int = 99):
+    """Synthetic greedy next tokens of a target model for verified trees (input data for the acceptance walk).
+
+    tokens/parents [B,n] (numpy); returns [B,n+1] int32: entry 0 stands for the root, entry 1 + i for node i. With
+    probability ``p_agree`` the entry is the token of one of that node's children in the tree (drawn uniformly),
+    otherwise a uniform vocabulary id (a node without children always gets a uniform id)."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    B, n = tokens.shape
+    out = rng.integers(0, V, size=(B, n + 1), dtype=np.int64)
+    for b in range(B):
+        kids = [[] for _ in range(n + 1)]
+        for i in range(n):
+            kids[int(parents[b, i]) + 1].append(int(tokens[b, i]))
+        for j in range(n + 1):
+            if kids[j] and rng.random() < p_agree:
+                out[b, j] = kids[j][int(rng.integers(0, len(kids[j])))]
+    return out.astype(np.int32)

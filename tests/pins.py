@@ -241,6 +241,44 @@ def pin_marginal_builder(L):
         assert np.max(np.abs(cond["scores"] - tree["scores"])) < 1e-12
 
 
+def pin_accept_paths(L):
+    """The acceptance walk equals the longest root-to-node path, among all paths of the tree enumerated, whose tokens
+    agree with the target's next tokens along it (greedy verification); plus the all-rejected and whole-chain cases."""
+    from oracle import oracle as orc
+    for trial in range(40):
+        inp = tiny_inputs(70 + trial % 4, M=3, n=20, max_depth=4, T=0.5)
+        logits, h0, w = host(inp)
+        ids, vals = orc.topm(logits, 3, L=L)
+        tree = orc.build_trees(ids, vals, h0, w, 20, 4, 0.5, L=L)
+        tok, par = tree["tokens"], tree["parents"]
+        tn = synth.make_target_next(tok, par, 600, p_agree=[0.0, 0.5, 0.9, 1.0][trial % 4], seed=trial)
+        got = orc.accept_paths(tok, par, tn, L=L)
+        best = ()
+        for i in range(tok.shape[1]):   # node i's path as node indices
+            nodes_on = []
+            j = i
+            while j >= 0:
+                nodes_on.append(j)
+                j = int(par[0, j])
+            nodes_on.reverse()
+            ok = all(int(tok[0, v]) == int(tn[0, 0 if k == 0 else 1 + nodes_on[k - 1]]) for k, v in enumerate(nodes_on))
+            if ok and len(nodes_on) > len(best):
+                best = tuple(nodes_on)
+        assert got["accept_len"][0] == len(best), (trial, got["accept_len"][0], best)
+        assert tuple(got["path"][0, :len(best)]) == best
+        assert np.all(got["path"][0, len(best):] == -1)
+        last = best[-1] if best else -1
+        assert got["bonus"][0] == tn[0, 1 + last if best else 0]
+    # nothing agrees: nothing accepted, the bonus is the target's token after the prefix
+    tok = np.array([[5, 6, 7]], np.int32)
+    par = np.array([[-1, 0, 1]], np.int32)
+    got = orc.accept_paths(tok, par, np.array([[9, 6, 7, 8]], np.int32), L=L)
+    assert got["accept_len"][0] == 0 and got["bonus"][0] == 9 and np.all(got["path"] == -1)
+    # a chain the target agrees with all the way: everything accepted, the bonus comes from the leaf
+    got = orc.accept_paths(tok, par, np.array([[5, 6, 7, 4]], np.int32), L=L)
+    assert got["accept_len"][0] == 3 and list(got["path"][0]) == [0, 1, 2] and got["bonus"][0] == 4
+
+
 def _all_paths(ids, max_depth):
     out, level = [], [()]
     for d in range(max_depth):
@@ -375,4 +413,5 @@ def pin_rescore(L):
 
 
 ALL_PINS = [pin_topm_bruteforce, pin_gru_vs_grucell, pin_full_vocab_softmax, pin_golden, pin_special_cases,
-            pin_factorised_closed_form, pin_bruteforce_tree, pin_invariants, pin_rescore, pin_marginal_builder]
+            pin_factorised_closed_form, pin_bruteforce_tree, pin_invariants, pin_rescore, pin_marginal_builder,
+            pin_accept_paths]

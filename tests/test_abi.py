@@ -142,3 +142,13 @@ def test_marginal_rejects_bad_arguments(dtlib):
     assert call(M=2000, V=5000) == UNSUPPORTED
     assert f(1, 4, 100, 5, 8, 4, 0.0, A, A, A, A, A, A, A + 8, A, 1 << 20, None) == INVALID  # misaligned
     assert call(B=0) == OK
+
+
+def test_accept_rejects_bad_arguments(dtlib):
+    f = dtlib.lib().dt_accept_paths
+    assert f(1, 0, A, A, A, A, A, A, None) == INVALID
+    assert f(-1, 4, A, A, A, A, A, A, None) == INVALID
+    assert f(1, 4, A + 2, A, A, A, A, A, None) == INVALID
+    assert f(1, 4, None, A, A, A, A, A, None) == INVALID
+    assert f(1, 2000, A, A, A, A, A, A, None) == UNSUPPORTED
+    assert f(0, 4, A, A, A, A, A, A, None) == OK

@@ -32,6 +32,12 @@ MUTANTS = {
                                  "const double* hp = h0;"),
     "score-not-cumulative": ("frontier.push(Cand{score + logp[m],", "frontier.push(Cand{logp[m],"),
     "mask-self-only": ("for (int j = i; j >= 0; j = parents[j]) mask", "for (int j = i; j == i; j = parents[j]) mask"),
+    "marginal-drops-temperature": ("marg[static_cast<size_t>(d) * M + m] = (v[m] / T_eff - mx) - lse;",
+                                   "marg[static_cast<size_t>(d) * M + m] = (v[m] - mx) - lse;"),
+    "marginal-position-off-by-one": ("expand(i, u.depth, u.score);", "expand(i, u.depth > 1 ? u.depth - 1 : 0, u.score);"),
+    "accept-target-index-off-by-one": ("want = target_next[1 + next];", "want = target_next[next];"),
+    "accept-root-token-skipped": ("int cur = -1, len = 0, want = target_next[0];",
+                                  "int cur = -1, len = 0, want = target_next[1];"),
     "embedding-of-parent": ("load(w.emb, w.dtype, static_cast<size_t>(u.token) * E + e)",
                             "load(w.emb, w.dtype, static_cast<size_t>(u.parent < 0 ? u.token : tokens[u.parent]) * E + e)"),
 }
