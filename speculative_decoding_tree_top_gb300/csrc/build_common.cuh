@@ -44,23 +44,31 @@ struct Job {
 };
 
 // Warp-wide best of one candidate per lane (`has` false: none), in pop order: higher score (-0.0 equal to +0.0),
-// then lower token, then lower insertion index, then lower lane. Three warp reductions and one ballot pick the lane;
-// returns it (-1 if no lane has a candidate) and leaves its node in `e` in every lane.
-__device__ __forceinline__ int warp_best(bool has, Node& e) {
+// then lower token, then lower insertion index, then lower lane. One warp reduction picks the lane when the best
+// score is held by one lane only (the common case); ties take two more reductions. Returns the lane (-1 if no lane
+// has a candidate) and leaves its node in `e` and its `dep` value in every lane.
+__device__ __forceinline__ int warp_best(bool has, Node& e, int& dep) {
   const uint32_t sk = has ? key_of_f32(__float_as_uint(e.score)) : 0u;  // keys of real scores are >= 1
   const uint32_t ms = __reduce_max_sync(0xFFFFFFFFu, sk);
   if (ms == 0u) return -1;
   const bool c1 = sk == ms;
-  const uint32_t mt = __reduce_min_sync(0xFFFFFFFFu, c1 ? static_cast<uint32_t>(e.token) : 0xFFFFFFFFu);
-  const bool c2 = c1 && static_cast<uint32_t>(e.token) == mt;
-  const uint32_t mq = __reduce_min_sync(0xFFFFFFFFu, c2 ? static_cast<uint32_t>(e.seq) : 0xFFFFFFFFu);
-  const bool c3 = c2 && static_cast<uint32_t>(e.seq) == mq;
-  const int wl = __ffs(__ballot_sync(0xFFFFFFFFu, c3)) - 1;
+  const unsigned top = __ballot_sync(0xFFFFFFFFu, c1);
+  int wl;
+  if ((top & (top - 1u)) == 0u) {
+    wl = __ffs(top) - 1;
+  } else {
+    const uint32_t mt = __reduce_min_sync(0xFFFFFFFFu, c1 ? static_cast<uint32_t>(e.token) : 0xFFFFFFFFu);
+    const bool c2 = c1 && static_cast<uint32_t>(e.token) == mt;
+    const uint32_t mq = __reduce_min_sync(0xFFFFFFFFu, c2 ? static_cast<uint32_t>(e.seq) : 0xFFFFFFFFu);
+    const bool c3 = c2 && static_cast<uint32_t>(e.seq) == mq;
+    wl = __ffs(__ballot_sync(0xFFFFFFFFu, c3)) - 1;
+  }
   e.score = __shfl_sync(0xFFFFFFFFu, e.score, wl);
   e.token = __shfl_sync(0xFFFFFFFFu, e.token, wl);
   e.seq = __shfl_sync(0xFFFFFFFFu, e.seq, wl);
   e.pslot = static_cast<short>(__shfl_sync(0xFFFFFFFFu, static_cast<int>(e.pslot), wl));
   e.xslot = static_cast<short>(__shfl_sync(0xFFFFFFFFu, static_cast<int>(e.xslot), wl));
+  dep = __shfl_sync(0xFFFFFFFFu, dep, wl);
   return wl;
 }
 
@@ -76,17 +84,19 @@ struct ReqCtl {
 
 // The frontier of a request is the union of up to 32 sorted sources, one per lane of the warp that works on it:
 // lane 0 walks the merged list, lane l > 0 the ranked children list of a popped node (slot `src`), whose entry m
-// has insertion index base + m. An idle lane has src = -1.
+// has insertion index base + m and depth `dep`. An idle lane has src = -1.
 struct LaneSrc {
   int src;   // -2: the merged list, -1: none, >= 0: the children list of that slot
   int idx;   // next entry
   int cnt;   // entries
   int base;  // insertion index of the list's candidate 0
+  int dep;   // depth of the list's entries (-1 for the merged list: read from the parent's slot)
+  int pad[3];
 };
 
 struct PopRec {  // a popped node, as the outputs need it
   int token;
-  int parent;
+  int parent;  // while building: the expansion slot of the parent; resolve_parents turns it into its pop index
   int depth;
   float score;
 };
@@ -103,15 +113,33 @@ struct ReqView {
   PopRec* pops;    // [n]
 };
 
-__device__ __forceinline__ bool lane_head(const ReqView& R, const LaneSrc& q, const Node* mg, int KM, Node& h) {
-  if (q.src == -1 || q.idx >= q.cnt) return false;
+// A lane's view of its source: the head entry, in registers.
+struct Cursor {
+  Node hd;
+  bool has;
+};
+__device__ __forceinline__ bool lane_entry(const ReqView& R, const LaneSrc& q, const Node* mg, int KM, int i, Node& h) {
+  if (q.src == -1 || i >= q.cnt) return false;
   if (q.src == -2) {
-    h = mg[q.idx];
+    h = mg[i];
   } else {
-    h = R.kids[static_cast<size_t>(q.src) * KM + q.idx];
+    h = R.kids[static_cast<size_t>(q.src) * KM + i];
     h.seq += q.base;
   }
   return true;
+}
+__device__ __forceinline__ void cursor_load(const ReqView& R, const LaneSrc& q, const Node* mg, int KM, Cursor& c) {
+  c.has = lane_entry(R, q, mg, KM, q.idx, c.hd);
+}
+__device__ __forceinline__ void cursor_advance(const ReqView& R, LaneSrc& q, const Node* mg, int KM, Cursor& c) {
+  ++q.idx;
+  c.has = lane_entry(R, q, mg, KM, q.idx, c.hd);
+}
+
+// Pop records hold the parent's expansion slot while a request is being built; once every pop is known this turns
+// them into pop indices (-1 for children of the root). Called by the threads of one block, followed by a barrier.
+__device__ __forceinline__ void resolve_parents(PopRec* pops, const int* popidx, int n, int t, int nthreads) {
+  for (int i = t; i < n; i += nthreads) pops[i].parent = popidx[pops[i].parent];
 }
 
 // Called by one whole warp for request b once its wave's expansions are known. Pops best-first while the best node
@@ -127,29 +155,29 @@ __device__ inline void request_step(const ReqView& R, int b, int n, int M, int m
   LaneSrc ls = R.lanes[lane];
   if (ls.src >= 0 && ls.cnt < 0) ls.cnt = R.kcount[ls.src];  // the root's list, attached at launch, filled in wave 0
   Node* mg = R.merged + static_cast<size_t>(st.fb) * n;
-  Node hd{};
-  bool has = lane_head(R, ls, mg, KM, hd);
+  Cursor cu;
+  cursor_load(R, ls, mg, KM, cu);
+  // the depth of a candidate: its list's, or (merged list) one more than its parent's
+  auto depth_of = [&](const Node& e, int dep) { return dep >= 0 ? dep : R.sdepth[e.pslot] + 1; };
   while (st.s < n) {
-    Node e = hd;
-    const int wl = warp_best(has, e);
+    Node e = cu.hd;
+    int dep = ls.dep;
+    const int wl = warp_best(cu.has, e, dep);
     if (wl < 0) {  // unreachable when n <= the size of the depth-limited tree (checked on the host)
       if (lane == 0) record_error(hdr, DT_ERR_INVALID_ARG);
       break;
     }
-    const int depth = R.sdepth[e.pslot] + 1;
+    const int depth = depth_of(e, dep);
     const bool need = (st.s + 1 < n) && (depth < maxd);
     if (need && e.xslot < 0) break;  // its children are not known yet: the next wave expands it
-    if (lane == 0) R.pops[st.s] = PopRec{e.token, R.popidx[e.pslot], depth, e.score};
-    if (lane == wl) {
-      ++ls.idx;
-      has = lane_head(R, ls, mg, KM, hd);
-    }
+    if (lane == 0) R.pops[st.s] = PopRec{e.token, e.pslot, depth, e.score};
+    if (lane == wl) cursor_advance(R, ls, mg, KM, cu);
     if (need) {
       const int x = e.xslot;
       if (lane == 0) R.popidx[x] = st.s;
       const int kc = R.kcount[x];
       if (kc > 0) {
-        unsigned idle = __ballot_sync(0xFFFFFFFFu, lane > 0 && !has);
+        unsigned idle = __ballot_sync(0xFFFFFFFFu, lane > 0 && !cu.has);
         if (idle == 0u) {
           // Every lane walks a live list: fold the shortest into the merged list, keeping what can still be popped.
           const unsigned rem = lane > 0 ? static_cast<unsigned>(ls.cnt - ls.idx) : 0xFFFFFFFFu;
@@ -192,15 +220,15 @@ __device__ inline void request_step(const ReqView& R, int b, int n, int M, int m
           __syncwarp();
           st.fb ^= 1;
           mg = out;
-          if (lane == 0) ls = LaneSrc{-2, 0, min(na + nb, limit), 0};
+          if (lane == 0) ls = LaneSrc{-2, 0, min(na + nb, limit), 0, -1, {0, 0, 0}};
           if (lane == L) ls.src = -1;
-          if (lane == 0 || lane == L) has = lane_head(R, ls, mg, KM, hd);
-          idle = __ballot_sync(0xFFFFFFFFu, lane > 0 && !has);
+          if (lane == 0 || lane == L) cursor_load(R, ls, mg, KM, cu);
+          idle = __ballot_sync(0xFFFFFFFFu, lane > 0 && !cu.has);
         }
         const int nl = __ffs(idle) - 1;
         if (lane == nl) {
-          ls = LaneSrc{x, 0, kc, st.seq_next};
-          has = lane_head(R, ls, mg, KM, hd);
+          ls = LaneSrc{x, 0, kc, st.seq_next, depth + 1, {0, 0, 0}};
+          cursor_load(R, ls, mg, KM, cu);
         }
       }
       st.seq_next += M;
@@ -212,14 +240,14 @@ __device__ inline void request_step(const ReqView& R, int b, int n, int M, int m
   int njobs = 0;
   if (st.s < n) {
     LaneSrc ss = ls;
-    Node sh = hd;
-    bool shas = has;
+    Cursor sc = cu;
     int sseq = st.seq_next;
     for (int sim = st.s; sim < n - 1 && njobs < kla; ++sim) {
-      Node e = sh;
-      const int wl = warp_best(shas, e);
+      Node e = sc.hd;
+      int dep = ss.dep;
+      const int wl = warp_best(sc.has, e, dep);
       if (wl < 0) break;
-      const int depth = R.sdepth[e.pslot] + 1;
+      const int depth = depth_of(e, dep);
       if (depth < maxd && e.xslot < 0) {
         const bool allowed = njobs == 0 || st.next_slot + 1 + (n - 1 - st.s) <= X;
         if (!allowed || st.next_slot >= X) break;
@@ -236,19 +264,16 @@ __device__ inline void request_step(const ReqView& R, int b, int n, int M, int m
         }
         ++njobs;
       }
-      if (lane == wl) {
-        ++ss.idx;
-        shas = lane_head(R, ss, mg, KM, sh);
-      }
+      if (lane == wl) cursor_advance(R, ss, mg, KM, sc);
       if (depth < maxd && e.xslot >= 0) {  // expanded but not popped: its children join the walk
         const int kc = R.kcount[e.xslot];
         if (kc > 0) {
-          const unsigned idle = __ballot_sync(0xFFFFFFFFu, lane > 0 && !shas);
+          const unsigned idle = __ballot_sync(0xFFFFFFFFu, lane > 0 && !sc.has);
           if (idle == 0u) break;
           const int nl = __ffs(idle) - 1;
           if (lane == nl) {
-            ss = LaneSrc{e.xslot, 0, kc, sseq};
-            shas = lane_head(R, ss, mg, KM, sh);
+            ss = LaneSrc{e.xslot, 0, kc, sseq, depth + 1, {0, 0, 0}};
+            cursor_load(R, ss, mg, KM, sc);
           }
         }
         sseq += M;

@@ -58,13 +58,13 @@ __global__ void __launch_bounds__(kThreads, 1) marginal_builder(Params p, MargSm
     *R.ctl = ReqCtl{0, 0, M, 1, 1, {0, 0, 0}};
     jobs[0] = Job{b, 0, -1, 0, 0, 0.f, {0, 0}};
   }
-  if (t < 32) R.lanes[t] = t == 0 ? LaneSrc{-2, 0, 0, 0} : t == 1 ? LaneSrc{0, 0, -1, 0} : LaneSrc{-1, 0, 0, 0};
+  if (t < 32) R.lanes[t] = t == 0 ? LaneSrc{-2, 0, 0, 0, -1, {0, 0, 0}} : t == 1 ? LaneSrc{0, 0, -1, 0, 1, {0, 0, 0}} : LaneSrc{-1, 0, 0, 0, -1, {0, 0, 0}};
   for (int i = t; i < X; i += kThreads) {
     R.kcount[i] = 0;
     R.popidx[i] = i == 0 ? -1 : -2;
     R.sdepth[i] = 0;
   }
-  for (int i = t; i < n; i += kThreads) R.pops[i] = PopRec{0, -1, 0, -INFINITY};
+  for (int i = t; i < n; i += kThreads) R.pops[i] = PopRec{0, 0, 0, -INFINITY};
   __syncthreads();
 
   for (int w = 0; w < X; ++w) {
@@ -122,6 +122,8 @@ __global__ void __launch_bounds__(kThreads, 1) marginal_builder(Params p, MargSm
   }
 
   // outputs, and each node's ancestor-mask row by walking its parent chain
+  resolve_parents(R.pops, R.popidx, n, t, kThreads);
+  __syncthreads();
   const size_t o = static_cast<size_t>(b) * n;
   for (int i = t; i < n; i += kThreads) {
     const PopRec r = R.pops[i];

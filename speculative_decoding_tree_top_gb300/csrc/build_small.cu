@@ -45,6 +45,7 @@ constexpr int kMaxRows = 16;  // gate rows per CTA, one warp each (3 * units <= 
 constexpr int kRowPad = 8;    // elements of padding per shared-memory weight row (16 bytes)
 constexpr int kJ = kWaveJobs;
 static_assert(kJ == 8, "a wave's jobs are the n8 tile of the GRU MMA");
+constexpr int kPrefetchPositions = 4;  // block positions whose candidates' embedding rows are prefetched at launch
 
 // Shared-memory plan of one CTA (identical on host and device).
 struct Plan {
@@ -148,7 +149,7 @@ __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, u
   lo = static_cast<uint32_t>(__bfloat16_as_ushort(l0)) | (static_cast<uint32_t>(__bfloat16_as_ushort(l1)) << 16);
 }
 
-template <bool kBf16>
+template <bool kBf16, bool kMma>  // kMma: bf16 weights with E and H multiples of 16 (tensor-core GRU)
 __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
   using T = typename WT<kBf16>::T;
   extern __shared__ __align__(16) unsigned char smem[];
@@ -198,6 +199,46 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
     mbar_fence_init();
   }
   __syncthreads();
+  // The launch's loads in the order they are needed: the candidate ids and base logits (and the biases), then the
+  // owned units' W_c columns of every candidate (they depend on the ids), then the GRU weight rows, which the first
+  // GRU step (wave 1) only needs: the dependent chain is not queued behind 9.4 MB of weights.
+  for (int i = t; i < 3 * umax; i += kThreads) {
+    const int g = i / umax, u = i % umax;
+    const size_t row = static_cast<size_t>(g) * H + u0 + u;
+    bias[2 * i] = (u < nu && p.b_ih) ? ldw(p.b_ih, kBf16, row) : 0.f;
+    bias[2 * i + 1] = (u < nu && p.b_hh) ? ldw(p.b_hh, kBf16, row) : 0.f;
+  }
+  for (int i = t; i < B * maxd * M; i += kThreads) {
+    const int b = i / (maxd * M), pos = (i / M) % maxd, m = i % M;
+    const size_t gi = (static_cast<size_t>(b) * K + pos) * M + m;
+    ids_s[i] = valid_id(p, __ldg(p.ids + gi));
+    vals_s[i] = __ldg(p.vals + gi);
+  }
+  __syncthreads();
+  // The owned units' W_c columns of the candidates of block positions [p0, p1): each needed row comes into L2 once
+  // (one bulk prefetch per row, spread over the CTAs, so HBM serves whole rows), then every CTA takes its columns.
+  auto gather_wc = [&](int p0, int p1) {
+    const int np = p1 - p0;
+    const unsigned rb = static_cast<unsigned>(H * esize);
+    for (int i = j * kThreads + t; i < B * np * M; i += G * kThreads) {
+      const int b = i / (np * M), pos = p0 + (i / M) % np, m = i % M;
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                   ::"l"(static_cast<const char*>(p.w_c) + static_cast<size_t>(ids_s[(b * maxd + pos) * M + m]) * rb),
+                   "r"(rb)
+                   : "memory");
+    }
+#pragma unroll 8
+    for (int q = t; q < B * np * M * umax; q += kThreads) {
+      const int i = q / umax, u = q % umax;
+      const int b = i / (np * M), pos = p0 + (i / M) % np, m = i % M;
+      const int c = (b * maxd + pos) * M + m;
+      wc[c * umax + u] = u < nu ? static_cast<const T*>(p.w_c)[static_cast<size_t>(ids_s[c]) * H + u0 + u] : T(0);
+    }
+  };
+  int wc_pos = maxd < kPrefetchPositions ? maxd : kPrefetchPositions;  // positions gathered so far
+  gather_wc(0, wc_pos);
+  // the 3 * nu rows of W_ih and of W_hh as bulk copies (1 to 8 KB each) completing on one mbarrier, issued by warp 0;
+  // waited for before the first GRU step
   if (warp == 0) {
     if (lane == 0) mbar_expect_tx(&wbar, static_cast<unsigned>(3 * nu * (E + H) * esize));
     __syncwarp();
@@ -215,39 +256,21 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
   }
   // A return before the first GRU step leaves no copy in flight: this waits (bounded) for the weights.
   auto drain = [&]() { mbar_wait(&wbar, 0, kCopyBudgetNs); };
-  for (int i = t; i < 3 * umax; i += kThreads) {
-    const int g = i / umax, u = i % umax;
-    const size_t row = static_cast<size_t>(g) * H + u0 + u;
-    bias[2 * i] = (u < nu && p.b_ih) ? ldw(p.b_ih, kBf16, row) : 0.f;
-    bias[2 * i + 1] = (u < nu && p.b_hh) ? ldw(p.b_hh, kBf16, row) : 0.f;
-  }
-  // candidate ids and base logits of every (request, position) first, then the owned units' W_c columns of every
-  // candidate, all independent loads
-  for (int i = t; i < B * maxd * M; i += kThreads) {
-    const int b = i / (maxd * M), pos = (i / M) % maxd, m = i % M;
-    const size_t gi = (static_cast<size_t>(b) * K + pos) * M + m;
-    ids_s[i] = valid_id(p, __ldg(p.ids + gi));
-    vals_s[i] = __ldg(p.vals + gi);
-  }
-  __syncthreads();
-#pragma unroll 8
-  for (int q = t; q < B * maxd * M * umax; q += kThreads) {
-    const int i = q / umax, u = q % umax;
-    wc[q] = u < nu ? static_cast<const T*>(p.w_c)[static_cast<size_t>(ids_s[i]) * H + u0 + u] : T(0);
-  }
+  bool weights_in = false;
+  // the embedding rows of the candidates of the first block positions (where the waves' jobs come from in the
+  // shallow trees of drafting) into L2, spread over the CTAs: the wave transitions then read them from L2
   {
     const size_t row_bytes = static_cast<size_t>(E) * esize;
     const size_t lines = (row_bytes + 127) / 128;
-    const size_t total = static_cast<size_t>(B) * maxd * M * lines;
+    const int npos = maxd < kPrefetchPositions ? maxd : kPrefetchPositions;
+    const size_t total = static_cast<size_t>(B) * npos * M * lines;
     for (size_t i = static_cast<size_t>(j) * kThreads + t; i < total; i += static_cast<size_t>(G) * kThreads) {
       const size_t c = i / lines, line = i % lines;
-      const int b = static_cast<int>(c / (maxd * M)), pos = static_cast<int>((c / M) % maxd);
+      const int b = static_cast<int>(c / (npos * M)), pos = static_cast<int>((c / M) % npos);
       const int m = static_cast<int>(c % M);
-      const int id = __ldg(p.ids + (static_cast<size_t>(b) * K + pos) * M + m);
-      if (static_cast<unsigned>(id) < static_cast<unsigned>(p.V)) {
-        const char* a = static_cast<const char*>(p.emb) + static_cast<size_t>(id) * row_bytes + line * 128;
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
-      }
+      const int id = ids_s[(static_cast<size_t>(b) * maxd + pos) * M + m];  // range-checked
+      const char* a = static_cast<const char*>(p.emb) + static_cast<size_t>(id) * row_bytes + line * 128;
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
     }
   }
   // every wave's accumulators and the slots' publication counters start at zero; one grid barrier orders that
@@ -264,10 +287,10 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
     ctl[b] = ReqCtl{0, 0, M, 1, 0, {0, 0, 0}};  // the root's children take insertion indices 0 .. M - 1
     jobs[b] = Job{b, 0, -1, 0, 0, 0.f, {0, 0}};
   }
-  for (int i = t; i < B * n; i += kThreads) pops[i] = PopRec{0, -1, 0, -INFINITY};
+  for (int i = t; i < B * n; i += kThreads) pops[i] = PopRec{0, 0, 0, -INFINITY};
   for (int i = t; i < B * 32; i += kThreads) {  // lane 0: the merged list (empty), lane 1: the root's children
     const int l = i % 32;
-    lanes[i] = l == 0 ? LaneSrc{-2, 0, 0, 0} : l == 1 ? LaneSrc{0, 0, -1, 0} : LaneSrc{-1, 0, 0, 0};
+    lanes[i] = l == 0 ? LaneSrc{-2, 0, 0, 0, -1, {0, 0, 0}} : l == 1 ? LaneSrc{0, 0, -1, 0, 1, {0, 0, 0}} : LaneSrc{-1, 0, 0, 0, -1, {0, 0, 0}};
   }
   for (int i = t; i < B * X; i += kThreads) {
     kcount[i] = 0;
@@ -279,7 +302,6 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
     drain();
     return;
   }
-  if (!mbar_wait(&wbar, 0, kCopyBudgetNs)) record_error(p.hdr, DT_ERR_TIMEOUT);  // the weight rows (bounded)
 
   for (int w = 0;; ++w) {
     __syncthreads();
@@ -289,13 +311,28 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
     if (w > 0 && !mbar_wait(&jbar, (w - 1) & 1, kCopyBudgetNs)) {
       record_error(p.hdr, DT_ERR_TIMEOUT);
       atomicExch(&p.hdr->abort, 1u);
+      if (!weights_in) drain();
       return;
     }
     long long* acc_w = p.acc + static_cast<size_t>(w) * kJ * M * AS;
     const bool roots = w == 0;  // wave 0 expands the roots (h = h0, no GRU step); later waves never do
+    if (!roots && !weights_in) {  // the weight rows, before the first GRU step (bounded)
+      if (!mbar_wait(&wbar, 0, kCopyBudgetNs)) record_error(p.hdr, DT_ERR_TIMEOUT);
+      weights_in = true;
+    }
+    {  // a job deeper than the positions gathered so far: gather up to it and a few beyond (same in every CTA)
+      int deepest = 0;
+      for (int q = 0; q < J; ++q) deepest = max(deepest, jobs[q].depth);
+      if (deepest >= wc_pos) {
+        const int upto = min(maxd, deepest + kPrefetchPositions);
+        gather_wc(wc_pos, upto);
+        wc_pos = upto;
+        __syncthreads();
+      }
+    }
 
     // ---- phase A: this CTA's units of every job's GRU step, then its share of every job's correction ----
-    const bool mma = kBf16 && E % 16 == 0 && H % 16 == 0;  // the tensor-core GRU (else the CUDA-core one below)
+    constexpr bool mma = kBf16 && kMma;  // the tensor-core GRU (else the CUDA-core one below)
     if (!roots && mma) {
       // Tensor cores, mma.sync m16n8k16 (bf16 in, fp32 accumulate): D[16 gate rows][8 jobs] = W[rows][K] X[K][jobs],
       // the warps splitting the k16 steps. A = this CTA's gate rows (rows past R repeat row R - 1: their outputs are
@@ -547,7 +584,10 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
         kkey[q * M + m] = sibling_key(e);
       }
     }
-    if (!__syncthreads_and(ok)) return;  // a wait ran out (recorded); no copy is in flight
+    if (!__syncthreads_and(ok)) {  // a wait ran out (recorded): leave with no copy in flight
+      if (!weights_in) drain();
+      return;
+    }
     // (2) every job's children ranked among themselves by their sibling keys (tpe threads per child), the first kc
     //     kept: at most n - s - 1 of them can still be popped after the job's node itself (n for the root's)
     {
@@ -613,8 +653,11 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
     }
   }
 
+  if (!weights_in) drain();  // a round without GRU steps (n = 1, or max depth 1) never waited for them
   // ---- outputs (CTA 0): nodes in pop order, and the ancestor mask by walking each node's parent chain ----
   if (j == 0) {
+    for (int b = 0; b < B; ++b) resolve_parents(pops + b * n, popidx + b * X, n, t, kThreads);
+    __syncthreads();
     for (int i = t; i < B * n; i += kThreads) {
       const PopRec r = pops[i];
       p.tokens[i] = r.token;
@@ -652,8 +695,10 @@ bool small_builder_fits(const Params& p, const DeviceInfo& di) {
 // G CTAs are co-resident; the cooperative launch checks it again.
 cudaError_t launch_small_builder(const Params& p, const DeviceInfo& di, cudaStream_t stream) {
   const Plan P = plan_for(p, di.sms);
-  const void* fn = p.bf16 ? reinterpret_cast<const void*>(small_builder<true>)
-                          : reinterpret_cast<const void*>(small_builder<false>);
+  const bool mma = p.bf16 && p.E % 16 == 0 && p.H % 16 == 0;
+  const void* fn = !p.bf16 ? reinterpret_cast<const void*>(small_builder<false, false>)
+                   : mma   ? reinterpret_cast<const void*>(small_builder<true, true>)
+                           : reinterpret_cast<const void*>(small_builder<true, false>);
   cudaError_t e = ensure_dynamic_smem(fn, P.bytes);
   if (e != cudaSuccess) return e;
   Params pp = p;

@@ -516,6 +516,8 @@ __device__ bool frontier_phase(const Params& p, int w, unsigned char* smem, uint
     __syncthreads();
     for (int q = t; q < st.njobs; q += kThreads) next[s_off + q] = jobs[q];
     if (st.s >= n) {  // finished: the outputs, and each node's ancestor-mask row by walking its parent chain
+      resolve_parents(R.pops, R.popidx, n, t, kThreads);
+      __syncthreads();
       const size_t o = static_cast<size_t>(b) * n;
       for (int i = t; i < n; i += kThreads) {
         const PopRec r = R.pops[i];
@@ -557,13 +559,13 @@ __device__ void init_requests(const Params& p, unsigned char* smem) {
       *R.ctl = ReqCtl{0, 0, M, 1, 1, {0, 0, 0}};  // the root's children take insertion indices 0 .. M - 1
       jobs[0] = Job{b, 0, -1, 0, 0, 0.f, {0, 0}};
     }
-    if (t < 32) R.lanes[t] = t == 0 ? LaneSrc{-2, 0, 0, 0} : t == 1 ? LaneSrc{0, 0, -1, 0} : LaneSrc{-1, 0, 0, 0};
+    if (t < 32) R.lanes[t] = t == 0 ? LaneSrc{-2, 0, 0, 0, -1, {0, 0, 0}} : t == 1 ? LaneSrc{0, 0, -1, 0, 1, {0, 0, 0}} : LaneSrc{-1, 0, 0, 0, -1, {0, 0, 0}};
     for (int i = t; i < X; i += kThreads) {
       R.kcount[i] = 0;
       R.popidx[i] = i == 0 ? -1 : -2;
       R.sdepth[i] = 0;
     }
-    for (int i = t; i < n; i += kThreads) R.pops[i] = PopRec{0, -1, 0, -INFINITY};
+    for (int i = t; i < n; i += kThreads) R.pops[i] = PopRec{0, 0, 0, -INFINITY};
     for (int i = t; i < H; i += kThreads)
       p.hs[static_cast<size_t>(b) * X * H + i] = __ldg(p.h0 + static_cast<size_t>(b) * H + i);
   }
