@@ -430,7 +430,7 @@ __host__ __device__ inline ReqView req_view(unsigned char* base, const ReqLayout
                  reinterpret_cast<int*>(base + L.sdepth), reinterpret_cast<PopRec*>(base + L.pops)};
 }
 constexpr int kLargeLookahead = 8;  // the large-batch builder's most expansions per request and wave
-constexpr int kLargeDefault = 4;    // ... and its default
+constexpr int kLargeDefault = 4;    // ... and its default (kLargeLookahead once a wave holds 128 requests or more)
 
 // Builder region of the workspace, after the top-M region (one workspace serves the whole round): the hidden states
 // of every expansion slot [B][X][H] fp32; for small batches the per-wave fixed-point correction accumulators and the

@@ -153,10 +153,6 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   const unsigned d = static_cast<unsigned>(__cvta_generic_to_shared(dst));
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
 }
-__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
-  const unsigned d = static_cast<unsigned>(__cvta_generic_to_shared(dst));
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(src) : "memory");
-}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 // Asks L2 to fetch [src, src + bytes) (bytes a multiple of 16, src 16-byte aligned); completes on its own.
@@ -391,74 +387,91 @@ __device__ __forceinline__ void bulk_s2g(void* gdst, const void* ssrc, unsigned 
                : "memory");
 }
 
-// Returns false when a bulk-copy wait ran out (recorded); the caller leaves the kernel.
-__device__ bool frontier_phase(const Params& p, int w, unsigned char* smem, uint64_t* bar, unsigned& bar_uses) {
+// Waits (bounded) for the current phase of `bar`; false when the wait ran out (recorded, abort raised).
+__device__ __forceinline__ bool wait_copies(const Params& p, uint64_t* bar, unsigned& uses) {
+  const bool ok = mbar_wait(bar, uses & 1u, kCopyBudgetNs);  // bulk copies take microseconds: this stops a lost one
+  ++uses;
+  if (!ok) {
+    record_error(p.hdr, DT_ERR_TIMEOUT);
+    atomicExch(&p.hdr->abort, 1u);
+  }
+  return ok;
+}
+
+// ---- phase B1: the children of every expansion of the wave, spread over all CTAs ------------------------------
+// Expansion q of the packed list goes to CTA q mod G: the M correction rows of the node's block position gathered
+// and dotted with its new hidden state (bulk copies on an mbarrier; the next expansion's rows are asked of L2
+// meanwhile), the restricted log-softmax, the siblings ranked by 64-bit keys; the first min(M, n) children and their
+// count go into the request's state block in the workspace. Returns false when a copy wait ran out.
+__device__ bool children_phase(const Params& p, const Job* jl, int rows, unsigned char* smem, uint64_t* bar,
+                               unsigned& bar_uses) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int M = p.M, n = p.n, H = p.H, X = p.xslots, KM = M < n ? M : n, kla = p.lookahead;
+  const int M = p.M, n = p.n, H = p.H, X = p.xslots, KM = M < n ? M : n;
   const size_t esize = p.bf16 ? 2 : 4;
-  const ReqLayout RL = req_layout(n, X, KM, kla);
-  const FrontierSmem FS = frontier_smem(RL.bytes, M, H);
-  const ReqView R = req_view(smem, RL);
-  Job* jobs = reinterpret_cast<Job*>(smem + RL.jobs);
+  const ReqLayout RL = req_layout(n, X, KM, p.lookahead);
+  const FrontierSmem FS = frontier_smem(0, M, H);
   float* h = reinterpret_cast<float*>(smem + FS.h);
   float* z = reinterpret_cast<float*>(smem + FS.z);
   float* vals = reinterpret_cast<float*>(smem + FS.vals);
   int* ids = reinterpret_cast<int*>(smem + FS.ids);
   unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem + FS.keys);
   Node* kraw = reinterpret_cast<Node*>(smem + FS.kraw);
-  unsigned char* rows = smem + FS.rows;
+  unsigned char* rows_s = smem + FS.rows;
   const bool rows_in_smem = p.rows_smem;
-  Job* next = p.joblist + static_cast<size_t>((w + 1) & 1) * p.B * kla;
+  const unsigned rb = static_cast<unsigned>(H * esize);
   __shared__ float s_red[2];
-  __shared__ int s_off;
-  auto wait_bar = [&]() -> bool {  // bulk copies take microseconds: the budget only stops a lost one
-    const bool ok = mbar_wait(bar, bar_uses & 1u, kCopyBudgetNs);
-    ++bar_uses;
-    if (!ok) {
-      record_error(p.hdr, DT_ERR_TIMEOUT);
-      atomicExch(&p.hdr->abort, 1u);
+  // With at least one request per CTA every CTA takes its own requests' expansions (no CTA would idle, and the
+  // children lists need no grid barrier before the owner reads them); else expansion q goes to CTA q mod G.
+  const bool own = p.B >= static_cast<int>(gridDim.x);
+  __shared__ int s_mine[kThreads + 1];  // own mode: this CTA's expansions among the next kThreads of the list
+  for (int q0 = own ? 0 : blockIdx.x; q0 < rows; q0 += own ? kThreads : gridDim.x) {
+    int nmine = 1;
+    if (own) {  // the owned expansions of this batch, found by every thread at once (their order does not matter)
+      __syncthreads();
+      if (t == 0) s_mine[kThreads] = 0;
+      __syncthreads();
+      if (q0 + t < rows && jl[q0 + t].b % static_cast<int>(gridDim.x) == static_cast<int>(blockIdx.x))
+        s_mine[atomicAdd(&s_mine[kThreads], 1)] = q0 + t;
+      __syncthreads();
+      nmine = s_mine[kThreads];
     }
-    return ok;
-  };
-  for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
-    unsigned char* gstate = p.rstate + static_cast<size_t>(b) * RL.bytes;
-    __syncthreads();  // the previous request (or phase) is done with the shared buffers
-    if (t == 0) {
-      mbar_expect_tx(bar, static_cast<unsigned>(RL.bytes));
-      bulk_g2s(smem, gstate, static_cast<unsigned>(RL.bytes), bar);
-    }
-    if (!__syncthreads_and(wait_bar())) return false;
-    const ReqCtl st0 = *R.ctl;
-    if (st0.s >= n) continue;  // finished in an earlier wave
-    // each expansion of the wave: correction on the gathered slice, restricted log-softmax, children ranked
-    for (int q = 0; q < st0.njobs; ++q) {
-      const Job jb = jobs[q];
-      const size_t pos = (static_cast<size_t>(b) * p.K + jb.depth) * M;
-      const float* hsrc = p.hs + (static_cast<size_t>(b) * X + jb.xslot) * H;
-      if (t == 0) {  // the node's hidden state (written by the GRU phase through the generic proxy): a bulk copy
+    for (int k = 0; k < nmine; ++k) {
+      const int q = own ? s_mine[k] : q0;
+      const Job jb = jl[q];
+      const size_t pos = (static_cast<size_t>(jb.b) * p.K + jb.depth) * M;
+      __syncthreads();  // the previous expansion is done with the shared buffers
+      if (t == 0) {  // the node's hidden state (written through the generic proxy by the GRU phase): a bulk copy
         asm volatile("fence.proxy.async.global;" ::: "memory");
         mbar_expect_tx(bar, static_cast<unsigned>(H * 4));
-        bulk_g2s(h, hsrc, static_cast<unsigned>(H * 4), bar);
+        bulk_g2s(h, p.hs + (static_cast<size_t>(jb.b) * X + jb.xslot) * H, static_cast<unsigned>(H * 4), bar);
       }
       for (int m = t; m < M; m += kThreads) {  // ids and base logits of its block position (any M: plain loads)
         ids[m] = valid_id(p, __ldg(p.ids + pos + m));
         vals[m] = __ldg(p.vals + pos + m);
       }
-      if (!__syncthreads_and(wait_bar())) return false;
+      if (!own && q + static_cast<int>(gridDim.x) < rows && warp == 1) {  // the next expansion's rows, into L2
+        const Job nj = jl[q + gridDim.x];
+        const size_t npos = (static_cast<size_t>(nj.b) * p.K + nj.depth) * M;
+        for (int m = lane; m < M; m += 32) {
+          const int id = __ldg(p.ids + npos + m);
+          if (static_cast<unsigned>(id) < static_cast<unsigned>(p.V))
+            prefetch_l2(static_cast<const char*>(p.w_c) + static_cast<size_t>(id) * rb, rb);
+        }
+      }
+      if (!__syncthreads_and(wait_copies(p, bar, bar_uses))) return false;
       if (rows_in_smem) {  // the M correction rows, one bulk copy each (issued by warp 0's lanes)
-        const unsigned rb = static_cast<unsigned>(H * esize);
         if (warp == 0) {
           if (lane == 0) mbar_expect_tx(bar, rb * static_cast<unsigned>(M));
           __syncwarp();
           for (int m = lane; m < M; m += 32)
-            bulk_g2s(rows + static_cast<size_t>(m) * rb, static_cast<const char*>(p.w_c) + static_cast<size_t>(ids[m]) * rb,
+            bulk_g2s(rows_s + static_cast<size_t>(m) * rb, static_cast<const char*>(p.w_c) + static_cast<size_t>(ids[m]) * rb,
                      rb, bar);
         }
-        if (!__syncthreads_and(wait_bar())) return false;
+        if (!__syncthreads_and(wait_copies(p, bar, bar_uses))) return false;
       }
       for (int m0 = warp * 8; m0 < M; m0 += kWarps * 8) {  // each warp: 8 consecutive rows at a time
         float d[8];
-        warp_dot_rows8(rows_in_smem ? rows : nullptr, p.w_c, ids, p.bf16, m0, M, h, H, d);
+        warp_dot_rows8(rows_in_smem ? rows_s : nullptr, p.w_c, ids, p.bf16, m0, M, h, H, d);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
           if (lane == j && m0 + j < M) z[m0 + j] = (vals[m0 + j] + d[j]) / p.T_eff;
@@ -492,9 +505,11 @@ __device__ bool frontier_phase(const Params& p, int w, unsigned char* smem, uint
                   static_cast<unsigned long long>(~static_cast<uint32_t>(e.token));
       }
       __syncthreads();
-      // rank among siblings (score, then token, then candidate index); keep the first kc: at most n - s - 1 of them
-      // can still be popped after the node itself (n for the root's)
-      const int kc = min(KM, jb.pslot < 0 ? n : n - st0.s - 1);
+      // rank among siblings (score, then token, then candidate index); the first kc kept: at most n - s - 1 of them can
+      // still be popped after the node itself (n for the root's), s being the request's pops so far (its state block,
+      // written back by its owner before the last barrier)
+      const ReqView R = req_view(p.rstate + static_cast<size_t>(jb.b) * RL.bytes, RL);
+      const int kc = min(KM, jb.pslot < 0 ? n : n - __ldcg(&R.ctl->s) - 1);
       for (int i = t; i < M; i += kThreads) {
         const unsigned long long ki = keys[i];
         int r = 0;
@@ -506,9 +521,35 @@ __device__ bool frontier_phase(const Params& p, int w, unsigned char* smem, uint
         if (r < kc) R.kids[static_cast<size_t>(jb.xslot) * KM + r] = kraw[i];
       }
       if (t == 0) R.kcount[jb.xslot] = kc;
-      __syncthreads();
     }
-    // pops and the next wave's picks (one warp), then the picks join the next wave's packed list
+  }
+  // the children lists are read back through the async proxy (the owner's bulk copy of the state block)
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return true;
+}
+
+// ---- phase B2: pops and picks of every request (the CTA that owns it) -----------------------------------------
+// The request's state block comes into shared memory as one bulk copy; one warp pops and picks (request_step); the
+// picks join the next wave's packed list; the block goes back as one bulk copy; a finished request writes its
+// outputs and ancestor-mask rows. Returns false when a copy wait ran out.
+__device__ bool control_phase(const Params& p, int w, unsigned char* smem, uint64_t* bar, unsigned& bar_uses) {
+  const int t = threadIdx.x, warp = t >> 5;
+  const int M = p.M, n = p.n, X = p.xslots, KM = M < n ? M : n, kla = p.lookahead;
+  const ReqLayout RL = req_layout(n, X, KM, kla);
+  const ReqView R = req_view(smem, RL);
+  Job* jobs = reinterpret_cast<Job*>(smem + RL.jobs);
+  Job* next = p.joblist + static_cast<size_t>((w + 1) & 1) * p.B * kla;
+  __shared__ int s_off;
+  for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
+    unsigned char* gstate = p.rstate + static_cast<size_t>(b) * RL.bytes;
+    __syncthreads();  // the previous request (or phase) is done with the shared buffers
+    if (t == 0) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      mbar_expect_tx(bar, static_cast<unsigned>(RL.bytes));
+      bulk_g2s(smem, gstate, static_cast<unsigned>(RL.bytes), bar);
+    }
+    if (!__syncthreads_and(wait_copies(p, bar, bar_uses))) return false;
+    if (R.ctl->s >= n) continue;  // finished in an earlier wave
     if (warp == 0) request_step(R, b, n, M, p.max_depth, X, KM, kla, jobs, p.hdr);
     __syncthreads();
     const ReqCtl st = *R.ctl;
@@ -540,6 +581,7 @@ __device__ bool frontier_phase(const Params& p, int w, unsigned char* smem, uint
       bulk_s2g(gstate, smem, static_cast<unsigned>(RL.bytes));
       asm volatile("cp.async.bulk.commit_group;" ::: "memory");
       asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+      asm volatile("fence.proxy.async.global;" ::: "memory");  // other CTAs write new children lists into it next
     }
   }
   return true;
@@ -551,8 +593,10 @@ __device__ void init_requests(const Params& p, unsigned char* smem) {
   const int t = threadIdx.x;
   const int M = p.M, n = p.n, H = p.H, X = p.xslots, KM = M < n ? M : n;
   const ReqLayout RL = req_layout(n, X, KM, p.lookahead);
-  for (int i = blockIdx.x * kThreads + t; i < X + 2; i += gridDim.x * kThreads) p.jobcount[i] = 0;
+  // wave 0 expands the roots: its packed list holds one job per request
+  for (int i = blockIdx.x * kThreads + t; i < X + 2; i += gridDim.x * kThreads) p.jobcount[i] = i == 0 ? p.B : 0;
   for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
+    if (t == 0) p.joblist[b] = Job{b, 0, -1, 0, 0, 0.f, {0, 0}};
     const ReqView R = req_view(p.rstate + static_cast<size_t>(b) * RL.bytes, RL);
     Job* jobs = reinterpret_cast<Job*>(p.rstate + static_cast<size_t>(b) * RL.bytes + RL.jobs);
     if (t == 0) {
@@ -594,10 +638,10 @@ __global__ void __launch_bounds__(kThreads, 1) build_kernel(Params p) {
   if (!grid_barrier(p.hdr, G, p.timeout_ns, &s_flag)) return;
   unsigned long long target = s_base;
   for (int w = 0; w < p.xslots; ++w) {
-    if (w > 0) {
-      const int rows = __ldcg(p.jobcount + w);
-      if (rows == 0) break;  // every request is finished (the same count in every CTA)
-      const Job* jl = p.joblist + static_cast<size_t>(w & 1) * p.B * p.lookahead;
+    const int rows = __ldcg(p.jobcount + w);
+    if (rows == 0) break;  // every request is finished (the same count in every CTA)
+    const Job* jl = p.joblist + static_cast<size_t>(w & 1) * p.B * p.lookahead;
+    if (w > 0) {  // wave 0 expands the roots, whose hidden state is h0: no GRU step
       if (kGemm == 1) gemm_gru_phase<TileS, 32, 8>(p, jl, rows, smem);
       else if (kGemm == 2) gemm_gru_phase<TileL, 64, 16>(p, jl, rows, smem);
       else if (kGemm == 3) gemm_gru_phase<TileS128, 32, 8>(p, jl, rows, smem);
@@ -605,7 +649,14 @@ __global__ void __launch_bounds__(kThreads, 1) build_kernel(Params p) {
       target += G;
       if (!counter_barrier(p.hdr, target, p.timeout_ns, &s_flag)) return;
     }
-    if (!frontier_phase(p, w, smem, &bar, bar_uses)) return;
+    if (!children_phase(p, jl, rows, smem, &bar, bar_uses)) return;
+    if (p.B < static_cast<int>(G)) {  // children computed by other CTAs: wait for all of them
+      target += G;
+      if (!counter_barrier(p.hdr, target, p.timeout_ns, &s_flag)) return;
+    } else {
+      __syncthreads();  // this CTA's own children lists, stored before its fence, then read back in bulk
+    }
+    if (!control_phase(p, w, smem, &bar, bar_uses)) return;
     target += G;
     if (!counter_barrier(p.hdr, target, p.timeout_ns, &s_flag)) return;
   }
@@ -619,11 +670,13 @@ size_t smem_bytes(int gemm, int M, int n, int H, int kla, size_t esize, size_t o
   if (gemm == 2) a = TileL::kBytes;
   if (gemm == 3) a = TileS128::kBytes;
   const int X = expansion_slots(n), KM = M < n ? M : n;
-  const FrontierSmem F = frontier_smem(req_layout(n, X, KM, kla).bytes, M, H);
+  const size_t ctl = req_layout(n, X, KM, kla).bytes;                 // the control phase: one state block
+  const FrontierSmem F = frontier_smem(0, M, H);                       // the children phase
   const size_t rows = static_cast<size_t>(M) * H * esize;
   *rows_smem = rows <= kFrontierRowsCap && F.bytes + rows <= optin;
   const size_t b = F.bytes + (*rows_smem ? rows : 0);
-  return a > b ? a : b;
+  size_t m = a > b ? a : b;
+  return m > ctl ? m : ctl;
 }
 
 }  // namespace
@@ -694,7 +747,8 @@ extern "C" dt_status dt_build_trees(int B, int K, int V, int M, int n, int max_d
     p.lookahead = k_set > 0 ? (k_set < fit ? k_set : fit) : fit;
   }
   if (small_builder_fits(p, di)) return cuda_status(launch_small_builder(p, di, stream));
-  p.lookahead = k_set > 0 ? (k_set < kLargeLookahead ? k_set : kLargeLookahead) : kLargeDefault;
+  p.lookahead = k_set > 0 ? (k_set < kLargeLookahead ? k_set : kLargeLookahead)
+                          : (B >= 128 ? kLargeLookahead : kLargeDefault);
 
   // phase A: tensor cores for bf16 weights whose widths are multiples of the pipeline chunk; the larger tile once a
   // wave can hold 128 expansions or more
