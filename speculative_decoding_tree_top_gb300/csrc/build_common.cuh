@@ -311,6 +311,8 @@ struct Params {
   unsigned char* rstate;  // [B] per-request best-first state blocks of req_layout(...).bytes (large-batch builder)
   Job* joblist;     // [2][B * lookahead] the expansions of a wave, packed (large-batch builder)
   int* jobcount;    // [xslots + 2] expansions per wave (large-batch builder)
+  unsigned short* xact;  // [B * lookahead][E + 2H] bf16 GRU inputs of the next wave's expansions (tensor-core GRU)
+  bool xact_on;     // the control phase writes xact (the tensor-core GRU runs)
   uint64_t timeout_ns;
   bool rows_smem;   // large-batch builder: the M gathered correction rows of a node are staged in shared memory
   int lookahead;    // expansions a request may run per wave (1 = one pop at a time)
@@ -437,7 +439,7 @@ constexpr int kLargeDefault = 4;    // ... and its default (kLargeLookahead once
 // per-slot publication counters; for larger ones the per-request state blocks, the packed job lists of two waves and
 // the per-wave job counts.
 struct BuildLayout {
-  size_t hs, acc, hs_count, rstate, joblist, jobcount, bytes;
+  size_t hs, acc, hs_count, rstate, joblist, jobcount, xact, bytes;
 };
 
 // Words between two correction accumulators: one 128-byte line each, so that the shares of a wave (every SM adds
@@ -446,7 +448,7 @@ __host__ __device__ inline int acc_stride(int M, int n) {
   return static_cast<size_t>(expansion_slots(n)) * kWaveJobs * M * 128u <= (64u << 20) ? 16 : 1;
 }
 
-inline BuildLayout build_layout(int B, int K, int V, int M, int n, int H) {
+inline BuildLayout build_layout(int B, int K, int V, int M, int n, int H, int E) {
   BuildLayout L{};
   const size_t X = static_cast<size_t>(expansion_slots(n));
   const int KM = M < n ? M : n;
@@ -458,7 +460,9 @@ inline BuildLayout build_layout(int B, int K, int V, int M, int n, int H) {
   // both builders may run for small batches (the small one needs shared memory the device may not have)
   L.joblist = align_up(L.rstate + req_layout(n, static_cast<int>(X), KM, kLargeLookahead).bytes * B);
   L.jobcount = align_up(L.joblist + sizeof(Job) * 2 * static_cast<size_t>(B) * kLargeLookahead);
-  L.bytes = align_up(L.jobcount + sizeof(int) * (X + 2));
+  // the tensor-core GRU's A operand: one bf16 row [emb | hi(h_parent) | lo(h_parent)] per expansion of a wave
+  L.xact = align_up(L.jobcount + sizeof(int) * (X + 2));
+  L.bytes = align_up(L.xact + sizeof(unsigned short) * static_cast<size_t>(B) * kLargeLookahead * (E + 2 * H));
   return L;
 }
 

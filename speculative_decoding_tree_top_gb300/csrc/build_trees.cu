@@ -22,9 +22,13 @@
 //   * grid barrier; next wave (none when no request added an expansion).
 // Every reduction has a fixed order (no floating-point atomics), so the output is bit-identical run to run and
 // does not depend on the lookahead width or on where an expansion sits in the packed list.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
+
+#include <mutex>
 
 #include "build_common.cuh"
 
@@ -387,6 +391,161 @@ __device__ __forceinline__ void bulk_s2g(void* gdst, const void* ssrc, unsigned 
                : "memory");
 }
 
+// ---- phase A on the 5th-generation tensor cores (tcgen05, TMEM, 2-D TMA) ---------------------------------------
+// One tile = 128 expansions (rows) x 32 hidden units. The A operand is the packed activations [emb | hi(h) | lo(h)]
+// of the wave (bf16, written by the control phase that picked the expansions), the B operand the r, z, n gate rows of
+// the tile's units in W_ih / W_hh, both K-major, moved by TMA in 64-column blocks with 128-byte swizzle through a
+// 4-stage ring of full / empty mbarriers. One lane issues the TMA loads, one lane the MMAs (kind::f16, fp32 accumulate
+// in TMEM): embedding blocks into TMEM columns [0, 96) = r | z | n_in (N = 96), hidden blocks (hi, then lo: the fp32
+// parent state to 2^-16) into [0, 64) = r | z (N = 64) and [96, 128) = n_h (N = 32), which the GRU keeps apart. The
+// four warps of the second warpgroup read the tile back (tcgen05.ld, one row per thread) and finish the GRU step.
+struct TmaMaps {
+  CUtensorMap x;    // [rows cap][E + 2H] bf16, box 64 x 128
+  CUtensorMap wih;  // [3H][E] bf16, box 64 x 32
+  CUtensorMap whh;  // [3H][H] bf16, box 64 x 32
+};
+constexpr int kUmmaRows = 128, kUmmaUnits = 32, kUmmaBK = 64, kUmmaStages = 4;
+constexpr int kUmmaA = kUmmaRows * kUmmaBK * 2;            // 16 KB
+constexpr int kUmmaB = 3 * kUmmaUnits * kUmmaBK * 2;       // 12 KB
+constexpr int kUmmaStage = kUmmaA + kUmmaB;                // 28 KB (a multiple of 1024)
+constexpr size_t kUmmaSmem = static_cast<size_t>(kUmmaStages) * kUmmaStage + 1024;  // + alignment slack
+constexpr int kTmemCols = 128;
+
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {  // K-major tile, 128-byte rows, 8-row atoms
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) | (static_cast<uint64_t>(2) << 61);
+}
+__device__ __forceinline__ uint32_t umma_idesc(int n) {  // bf16 x bf16 -> fp32, both K-major, M = 128
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(kUmmaRows >> 4) << 24);
+}
+__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t idesc, uint32_t acc) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
+               ::"r"(tmem_d), "l"(da), "l"(db), "r"(idesc), "r"(acc) : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
+  asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+               ::"r"(smem_u32(dst)), "l"(map), "r"(c0), "r"(c1), "r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+// Per-launch state of the tensor-core phase: the ring's barriers and how far each has gone (the same in every thread).
+struct UmmaRing {
+  uint64_t* full;   // [kUmmaStages]
+  uint64_t* empty;  // [kUmmaStages]
+  uint64_t* done;   // accumulator complete
+  uint32_t tmem;
+  unsigned blocks;  // K blocks loaded so far (ring position)
+  unsigned tiles;   // tiles finished so far (done phase)
+};
+
+// Returns false when a wait ran out (recorded, abort raised); nothing is then in flight from this CTA.
+__device__ bool umma_gru_phase(const Params& p, const TmaMaps& maps, const Job* jl, int rows, unsigned char* smem,
+                               UmmaRing& ring) {
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int E = p.E, H = p.H, X = p.xslots;
+  const int nE = E / kUmmaBK, nH = H / kUmmaBK, nkb = nE + 2 * nH;
+  unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem) + 1023) & ~uintptr_t(1023));
+  const int rtiles = (rows + kUmmaRows - 1) / kUmmaRows, utiles = H / kUmmaUnits;
+  bool ok = true;
+  for (int tile = blockIdx.x; tile < rtiles * utiles; tile += gridDim.x) {
+    const int row0 = (tile / utiles) * kUmmaRows, u0 = (tile % utiles) * kUmmaUnits;
+    if (warp == 0 && lane == 0) {  // TMA producer
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the other phases' shared-memory use came first
+      for (int kb = 0; kb < nkb && ok; ++kb) {
+        const unsigned n = ring.blocks + kb, st = n % kUmmaStages, use = n / kUmmaStages;
+        if (use > 0) ok = mbar_wait(&ring.empty[st], (use - 1) & 1u, kCopyBudgetNs);
+        if (!ok) break;
+        unsigned char* a = base + st * kUmmaStage;
+        unsigned char* bsm = a + kUmmaA;
+        mbar_expect_tx(&ring.full[st], kUmmaStage);
+        const bool emb = kb < nE;
+        const int acol = emb ? kb * kUmmaBK : E + (kb - nE) * kUmmaBK;                   // hi blocks, then lo blocks
+        const int wcol = emb ? kb * kUmmaBK : ((kb - nE) % nH) * kUmmaBK;
+        tma_load_2d(a, &maps.x, acol, row0, &ring.full[st]);
+        for (int g = 0; g < 3; ++g)
+          tma_load_2d(bsm + g * kUmmaUnits * 128, emb ? &maps.wih : &maps.whh, wcol, g * H + u0, &ring.full[st]);
+      }
+    } else if (warp == 1 && lane == 0) {  // MMA issuer
+      for (int kb = 0; kb < nkb && ok; ++kb) {
+        const unsigned n = ring.blocks + kb, st = n % kUmmaStages, use = n / kUmmaStages;
+        ok = mbar_wait(&ring.full[st], use & 1u, kCopyBudgetNs);
+        if (!ok) break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t a = smem_u32(base + st * kUmmaStage), bsm = a + kUmmaA;
+        const bool emb = kb < nE;
+#pragma unroll
+        for (int k = 0; k < kUmmaBK / 16; ++k) {
+          const uint64_t da = umma_desc_sw128(a + 32 * k);
+          if (emb) {
+            umma_f16(ring.tmem, da, umma_desc_sw128(bsm + 32 * k), umma_idesc(3 * kUmmaUnits), (kb > 0 || k > 0) ? 1u : 0u);
+          } else {
+            umma_f16(ring.tmem, da, umma_desc_sw128(bsm + 32 * k), umma_idesc(2 * kUmmaUnits), 1u);
+            umma_f16(ring.tmem + 3 * kUmmaUnits, da, umma_desc_sw128(bsm + 2 * kUmmaUnits * 128 + 32 * k),
+                     umma_idesc(kUmmaUnits), (kb > nE || k > 0) ? 1u : 0u);
+          }
+        }
+        umma_commit(&ring.empty[st]);  // the stage is free once these MMAs have read it
+      }
+      if (ok) umma_commit(ring.done);  // and the accumulator is complete after the last block's MMAs
+    }
+    ring.blocks += nkb;
+    ok = __syncthreads_and(ok);
+    if (ok && warp >= 4) {  // epilogue: one row (expansion) per thread, the GRU pointwise of the tile's units
+      ok = mbar_wait(ring.done, ring.tiles & 1u, kCopyBudgetNs);
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const int r = 32 * (warp - 4) + lane, q = row0 + r;
+      const uint32_t trow = ring.tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+      Job jb{};
+      if (q < rows) jb = jl[q];
+      for (int c = 0; c < kUmmaUnits; c += 8) {
+        float dr[8], dz[8], dn[8], dh[8];
+        tmem_ld8(trow + c, dr);  // every lane takes part in the loads (.sync.aligned)
+        tmem_ld8(trow + kUmmaUnits + c, dz);
+        tmem_ld8(trow + 2 * kUmmaUnits + c, dn);
+        tmem_ld8(trow + 3 * kUmmaUnits + c, dh);
+        if (q < rows && ok) {
+          const float* hprev = p.hs + (static_cast<size_t>(jb.b) * X + jb.pslot) * H + u0 + c;
+          float* hout = p.hs + (static_cast<size_t>(jb.b) * X + jb.xslot) * H + u0 + c;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const size_t g0 = u0 + c + j, g1 = static_cast<size_t>(H) + g0, g2 = 2 * static_cast<size_t>(H) + g0;
+            const float bir = p.b_ih ? ldw(p.b_ih, true, g0) : 0.f, bhr = p.b_hh ? ldw(p.b_hh, true, g0) : 0.f;
+            const float biz = p.b_ih ? ldw(p.b_ih, true, g1) : 0.f, bhz = p.b_hh ? ldw(p.b_hh, true, g1) : 0.f;
+            const float bin = p.b_ih ? ldw(p.b_ih, true, g2) : 0.f, bhn = p.b_hh ? ldw(p.b_hh, true, g2) : 0.f;
+            const float rg = sigmoidf_(dr[j] + bir + bhr);
+            const float zg = sigmoidf_(dz[j] + biz + bhz);
+            const float ng = tanhf(dn[j] + bin + rg * (dh[j] + bhn));
+            hout[j] = (1.f - zg) * ng + zg * __ldcg(hprev + j);
+          }
+        }
+      }
+    }
+    ring.tiles += 1;
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    ok = __syncthreads_and(ok);  // the accumulator is read before the next tile's first MMA overwrites it
+    if (!ok) {
+      record_error(p.hdr, DT_ERR_TIMEOUT);
+      atomicExch(&p.hdr->abort, 1u);
+      return false;
+    }
+  }
+  return true;
+}
+
 // Waits (bounded) for the current phase of `bar`; false when the wait ran out (recorded, abort raised).
 __device__ __forceinline__ bool wait_copies(const Params& p, uint64_t* bar, unsigned& uses) {
   const bool ok = mbar_wait(bar, uses & 1u, kCopyBudgetNs);  // bulk copies take microseconds: this stops a lost one
@@ -556,6 +715,25 @@ __device__ bool control_phase(const Params& p, int w, unsigned char* smem, uint6
     if (t == 0) s_off = st.njobs > 0 ? atomicAdd(p.jobcount + w + 1, st.njobs) : 0;
     __syncthreads();
     for (int q = t; q < st.njobs; q += kThreads) next[s_off + q] = jobs[q];
+    if (p.xact_on) {  // the picks' GRU inputs as the tensor-core GRU reads them: [emb | hi(h_parent) | lo(h_parent)]
+      const int E = p.E, H = p.H, Kx = E + 2 * H;
+      for (int q = 0; q < st.njobs; ++q) {
+        const Job jb = jobs[q];
+        unsigned short* xr = p.xact + static_cast<size_t>(s_off + q) * Kx;
+        const uint4* er = reinterpret_cast<const uint4*>(static_cast<const unsigned short*>(p.emb) +
+                                                         static_cast<size_t>(jb.token) * E);
+        for (int i = t; i < E / 8; i += kThreads) reinterpret_cast<uint4*>(xr)[i] = __ldg(er + i);
+        const float2* hp = reinterpret_cast<const float2*>(p.hs + (static_cast<size_t>(b) * X + jb.pslot) * H);
+        for (int i = t; i < H / 2; i += kThreads) {
+          const float2 v = __ldcg(hp + i);
+          uint32_t hi, lo;
+          split_bf16x2(v.x, v.y, hi, lo);
+          reinterpret_cast<uint32_t*>(xr + E)[i] = hi;
+          reinterpret_cast<uint32_t*>(xr + E + H)[i] = lo;
+        }
+      }
+      asm volatile("fence.proxy.async.global;" ::: "memory");  // read by TMA (async proxy) after the next barrier
+    }
     if (st.s >= n) {  // finished: the outputs, and each node's ancestor-mask row by walking its parent chain
       resolve_parents(R.pops, R.popidx, n, t, kThreads);
       __syncthreads();
@@ -618,54 +796,140 @@ __device__ void init_requests(const Params& p, unsigned char* smem) {
   (void)smem;
 }
 
-// kGemm: 0 = CUDA-core GRU tiles (fp32 weights or widths not multiples of 128), tensor cores with 1 = TileS,
-// 2 = TileL, 3 = TileS128.
+// The waves of one launch; every way out (done, or a wait that ran out) returns here in every thread of the CTA.
 template <int kGemm>
-__global__ void __launch_bounds__(kThreads, 1) build_kernel(Params p) {
-  extern __shared__ float4 smem_f4[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>(smem_f4);
-  __shared__ int s_flag;
-  __shared__ unsigned long long s_base;
-  __shared__ uint64_t bar;  // completion of the frontier phase's bulk copies
+__device__ void run_waves(const Params& p, const TmaMaps& maps, unsigned char* smem, UmmaRing& ring,
+                          unsigned long long base_count, uint64_t* bar, int* s_flag) {
   unsigned bar_uses = 0;
   const unsigned G = gridDim.x;
-  if (threadIdx.x == 0) {
-    s_base = ld_relaxed_gpu_u64(&p.hdr->sync_count);  // before anyone can pass this barrier
-    mbar_init(&bar, 1);
-    mbar_fence_init();
-  }
   init_requests(p, smem);
-  if (!grid_barrier(p.hdr, G, p.timeout_ns, &s_flag)) return;
-  unsigned long long target = s_base;
+  if (!grid_barrier(p.hdr, G, p.timeout_ns, s_flag)) return;
+  unsigned long long target = base_count;
   for (int w = 0; w < p.xslots; ++w) {
     const int rows = __ldcg(p.jobcount + w);
     if (rows == 0) break;  // every request is finished (the same count in every CTA)
     const Job* jl = p.joblist + static_cast<size_t>(w & 1) * p.B * p.lookahead;
     if (w > 0) {  // wave 0 expands the roots, whose hidden state is h0: no GRU step
-      if (kGemm == 1) gemm_gru_phase<TileS, 32, 8>(p, jl, rows, smem);
-      else if (kGemm == 2) gemm_gru_phase<TileL, 64, 16>(p, jl, rows, smem);
-      else if (kGemm == 3) gemm_gru_phase<TileS128, 32, 8>(p, jl, rows, smem);
-      else gru_phase(p, jl, rows, reinterpret_cast<float*>(smem));
+      if (kGemm == 4) {
+        if (!umma_gru_phase(p, maps, jl, rows, smem, ring)) return;
+      } else if (kGemm == 1) {
+        gemm_gru_phase<TileS, 32, 8>(p, jl, rows, smem);
+      } else if (kGemm == 2) {
+        gemm_gru_phase<TileL, 64, 16>(p, jl, rows, smem);
+      } else if (kGemm == 3) {
+        gemm_gru_phase<TileS128, 32, 8>(p, jl, rows, smem);
+      } else {
+        gru_phase(p, jl, rows, reinterpret_cast<float*>(smem));
+      }
       target += G;
-      if (!counter_barrier(p.hdr, target, p.timeout_ns, &s_flag)) return;
+      if (!counter_barrier(p.hdr, target, p.timeout_ns, s_flag)) return;
     }
-    if (!children_phase(p, jl, rows, smem, &bar, bar_uses)) return;
+    if (!children_phase(p, jl, rows, smem, bar, bar_uses)) return;
     if (p.B < static_cast<int>(G)) {  // children computed by other CTAs: wait for all of them
       target += G;
-      if (!counter_barrier(p.hdr, target, p.timeout_ns, &s_flag)) return;
+      if (!counter_barrier(p.hdr, target, p.timeout_ns, s_flag)) return;
     } else {
       __syncthreads();  // this CTA's own children lists, stored before its fence, then read back in bulk
     }
-    if (!control_phase(p, w, smem, &bar, bar_uses)) return;
+    if (!control_phase(p, w, smem, bar, bar_uses)) return;
     target += G;
-    if (!counter_barrier(p.hdr, target, p.timeout_ns, &s_flag)) return;
+    if (!counter_barrier(p.hdr, target, p.timeout_ns, s_flag)) return;
   }
+}
+
+// kGemm: 0 = CUDA-core GRU tiles (fp32 weights or other widths), mma.sync tensor-core tiles with 1 = TileS,
+// 2 = TileL, 3 = TileS128; 4 = tcgen05 tiles (bf16, E and H multiples of 64). With kGemm = 4 the CTA holds 128 TMEM
+// columns for the whole launch and frees them on every way out.
+template <int kGemm>
+__global__ void __launch_bounds__(kThreads, 1) build_kernel(Params p, const __grid_constant__ TmaMaps maps) {
+  extern __shared__ float4 smem_f4[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(smem_f4);
+  __shared__ int s_flag;
+  __shared__ unsigned long long s_base;
+  __shared__ uint64_t bar;  // completion of the frontier phase's bulk copies
+  __shared__ uint64_t ufull[kUmmaStages], uempty[kUmmaStages], udone;
+  __shared__ uint32_t s_tmem;
+  if (threadIdx.x == 0) {
+    s_base = ld_relaxed_gpu_u64(&p.hdr->sync_count);  // before anyone can pass the first barrier
+    mbar_init(&bar, 1);
+    if (kGemm == 4) {
+      for (int i = 0; i < kUmmaStages; ++i) {
+        mbar_init(&ufull[i], 1);
+        mbar_init(&uempty[i], 1);
+      }
+      mbar_init(&udone, 1);
+    }
+    mbar_fence_init();
+  }
+  if (kGemm == 4 && threadIdx.x < 32) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                 "r"(kTmemCols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (kGemm == 4) asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (kGemm == 4) asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  UmmaRing ring{ufull, uempty, &udone, kGemm == 4 ? s_tmem : 0u, 0u, 0u};
+  run_waves<kGemm>(p, maps, smem, ring, s_base, &bar, &s_flag);
+  if (kGemm == 4) {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (threadIdx.x < 32)
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(ring.tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+// The tcgen05 GRU's tensor maps (2-D, bf16, 128-byte swizzle): the packed activations and the two weight matrices.
+// cuTensorMapEncodeTiled comes from the driver through the runtime's entry-point query (no link to the driver
+// library); the last maps built are kept and reused while the pointers and sizes stay the same.
+bool gru_tensor_maps(TmaMaps* out, const void* xact, uint64_t xrows, const void* w_ih, const void* w_hh, int E, int H) {
+  static std::mutex mu;
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  static bool looked = false;
+  static TmaMaps last{};
+  static const void* key[3] = {nullptr, nullptr, nullptr};
+  static uint64_t key_dims[3] = {0, 0, 0};
+  std::lock_guard<std::mutex> lock(mu);
+  if (!looked) {
+    looked = true;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  if (!encode) return false;
+  if (key[0] == xact && key[1] == w_ih && key[2] == w_hh && key_dims[0] == xrows && key_dims[1] == static_cast<uint64_t>(E) &&
+      key_dims[2] == static_cast<uint64_t>(H)) {
+    *out = last;
+    return true;
+  }
+  auto map2d = [&](CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+    const cuuint64_t gdim[2] = {cols, rows};
+    const cuuint64_t gstride[1] = {cols * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kUmmaBK), box_rows};
+    const cuuint32_t estride[2] = {1, 1};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), gdim, gstride, box, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  TmaMaps m{};
+  if (!map2d(&m.x, xact, static_cast<uint64_t>(E) + 2 * static_cast<uint64_t>(H), xrows, kUmmaRows) ||
+      !map2d(&m.wih, w_ih, static_cast<uint64_t>(E), 3 * static_cast<uint64_t>(H), kUmmaUnits) ||
+      !map2d(&m.whh, w_hh, static_cast<uint64_t>(H), 3 * static_cast<uint64_t>(H), kUmmaUnits))
+    return false;
+  last = m;
+  key[0] = xact; key[1] = w_ih; key[2] = w_hh;
+  key_dims[0] = xrows; key_dims[1] = static_cast<uint64_t>(E); key_dims[2] = static_cast<uint64_t>(H);
+  *out = m;
+  return true;
 }
 
 // Dynamic shared memory of the large-batch kernel; the gathered rows are staged only when they fit under both the
 // cap and the device's opt-in limit (`rows_smem` reports the choice).
 size_t smem_bytes(int gemm, int M, int n, int H, int kla, size_t esize, size_t optin, bool* rows_smem) {
   size_t a = sizeof(float) * (kTB * kPad + 3 * kTU * kPad);
+  if (gemm == 4) a = kUmmaSmem;
   if (gemm == 1) a = TileS::kBytes;
   if (gemm == 2) a = TileL::kBytes;
   if (gemm == 3) a = TileS128::kBytes;
@@ -683,9 +947,8 @@ size_t smem_bytes(int gemm, int M, int n, int H, int kla, size_t esize, size_t o
 }  // namespace dt
 
 extern "C" size_t dt_build_workspace_bytes(int B, int K, int V, int M, int n, int H, int E) {
-  (void)E;
-  if (B < 0 || K < 1 || V < 1 || M < 1 || n < 1 || H < 1) return 0;
-  return dt::build_layout(B, K, V, M, n, H).bytes;
+  if (B < 0 || K < 1 || V < 1 || M < 1 || n < 1 || H < 1 || E < 1) return 0;
+  return dt::build_layout(B, K, V, M, n, H, E).bytes;
 }
 
 extern "C" dt_status dt_build_trees(int B, int K, int V, int M, int n, int max_depth, float T,
@@ -715,7 +978,7 @@ extern "C" dt_status dt_build_trees(int B, int K, int V, int M, int n, int max_d
   for (const void* q : ptrs)
     if (!q || !aligned16(q)) return DT_ERR_INVALID_ARG;
   if ((w->b_ih && !aligned16(w->b_ih)) || (w->b_hh && !aligned16(w->b_hh))) return DT_ERR_INVALID_ARG;
-  const BuildLayout L = build_layout(B, K, V, M, n, H);
+  const BuildLayout L = build_layout(B, K, V, M, n, H, E);
   if (workspace_bytes < L.bytes) return DT_ERR_INVALID_ARG;
 
   char* ws = static_cast<char*>(workspace);
@@ -733,6 +996,7 @@ extern "C" dt_status dt_build_trees(int B, int K, int V, int M, int n, int max_d
   p.rstate = reinterpret_cast<unsigned char*>(ws + L.rstate);
   p.joblist = reinterpret_cast<Job*>(ws + L.joblist);
   p.jobcount = reinterpret_cast<int*>(ws + L.jobcount);
+  p.xact = reinterpret_cast<unsigned short*>(ws + L.xact);
   p.acc_stride = acc_stride(M, n);
   p.xslots = expansion_slots(n);
   p.timeout_ns = barrier_timeout_ns();
@@ -753,21 +1017,29 @@ extern "C" dt_status dt_build_trees(int B, int K, int V, int M, int n, int max_d
   // phase A: tensor cores for bf16 weights whose widths are multiples of the pipeline chunk; the larger tile once a
   // wave can hold 128 expansions or more
   const long long max_rows = static_cast<long long>(B) * p.lookahead;
+  // tcgen05 tiles (128 expansions x 32 units) once a wave can fill the SMs with them
+  const bool umma = p.bf16 && E % kUmmaBK == 0 && H % kUmmaBK == 0 && max_rows >= 512;
   const int gemm = !p.bf16 ? 0
+                   : umma ? 4
                    : max_rows >= 128 ? (E % TileL::kKc == 0 && H % TileL::kKc == 0 ? 2 : 0)
                    : E % TileS::kKc == 0 && H % TileS::kKc == 0 ? 1
                    : E % TileS128::kKc == 0 && H % TileS128::kKc == 0 ? 3 : 0;
   const void* fn = gemm == 0 ? reinterpret_cast<const void*>(build_kernel<0>)
-                             : gemm == 3 ? reinterpret_cast<const void*>(build_kernel<3>)
-                             : gemm == 1 ? reinterpret_cast<const void*>(build_kernel<1>)
-                                         : reinterpret_cast<const void*>(build_kernel<2>);
-  // static shared memory of the kernel (flags, reductions) is well under 1 KB; one CTA per SM (launch bounds), so
+                   : gemm == 4 ? reinterpret_cast<const void*>(build_kernel<4>)
+                   : gemm == 3 ? reinterpret_cast<const void*>(build_kernel<3>)
+                   : gemm == 1 ? reinterpret_cast<const void*>(build_kernel<1>)
+                               : reinterpret_cast<const void*>(build_kernel<2>);
+  TmaMaps maps{};
+  p.xact_on = gemm == 4;
+  if (gemm == 4 && !gru_tensor_maps(&maps, p.xact, static_cast<uint64_t>(B) * kLargeLookahead, w->w_ih, w->w_hh, E, H))
+    return DT_ERR_CUDA;
+  // static shared memory of the kernel (flags, barriers, reductions) is under 2 KB; one CTA per SM (launch bounds), so
   // the shared memory alone decides whether a CTA fits
-  const size_t smem = smem_bytes(gemm, M, n, H, p.lookahead, p.bf16 ? 2 : 4, static_cast<size_t>(di.optin) - 1024,
+  const size_t smem = smem_bytes(gemm, M, n, H, p.lookahead, p.bf16 ? 2 : 4, static_cast<size_t>(di.optin) - 2048,
                                  &p.rows_smem);
-  if (smem + 1024 > static_cast<size_t>(di.optin)) return DT_ERR_UNSUPPORTED;
+  if (smem + 2048 > static_cast<size_t>(di.optin)) return DT_ERR_UNSUPPORTED;
   if (ensure_dynamic_smem(fn, smem) != cudaSuccess) return DT_ERR_CUDA;
   const unsigned grid = static_cast<unsigned>(di.sms);  // one CTA per SM; co-resident under a cooperative launch
-  void* args[] = {&p};
+  void* args[] = {&p, &maps};
   return cuda_status(cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kThreads), args, smem, stream));
 }
