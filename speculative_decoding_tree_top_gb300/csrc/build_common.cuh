@@ -318,6 +318,9 @@ struct Params {
   int lookahead;    // expansions a request may run per wave (1 = one pop at a time)
   int xslots;       // expansion slots per request (expansion_slots(n))
   int* hs_count;    // [B][xslots] units of each slot's hidden state published (small-batch builder)
+  float* gru_part;  // [gru_tiles][kGruSplits][128][128] K-split partial gate sums of the tensor-core GRU
+  unsigned* gru_ticket;  // [gru_tiles] CTAs of a tile that stored their partials in the current wave (tensor-core GRU)
+  int gru_tiles;
 };
 
 __device__ __forceinline__ float ldw(const void* p, bool bf16, size_t i) {
@@ -439,8 +442,21 @@ constexpr int kLargeDefault = 4;    // ... and its default (kLargeLookahead once
 // per-slot publication counters; for larger ones the per-request state blocks, the packed job lists of two waves and
 // the per-wave job counts.
 struct BuildLayout {
-  size_t hs, acc, hs_count, rstate, joblist, jobcount, xact, bytes;
+  size_t hs, acc, hs_count, rstate, joblist, jobcount, xact, gru_part, gru_ticket, bytes;
+  int gru_tiles;
 };
+
+// The tensor-core GRU of the large-batch builder sums K as kGruSplits partials in a fixed order. A wave of at most
+// kGruSpreadTiles tiles (128 expansions x 32 units) spreads the partials over CTAs and adds them up from the
+// workspace; the tiles a wave of B * kLargeLookahead expansions can have, capped there, size that region.
+constexpr int kGruSplits = 4;
+constexpr int kGruSpreadTiles = 128;
+constexpr int kGruTileRows = 128, kGruTileUnits = 32;
+inline int gru_spread_tiles(int B, int H) {
+  const long long t = (static_cast<long long>(B) * kLargeLookahead + kGruTileRows - 1) / kGruTileRows *
+                      (H / kGruTileUnits);
+  return static_cast<int>(t < kGruSpreadTiles ? t : kGruSpreadTiles);
+}
 
 // Words between two correction accumulators: one 128-byte line each, so that the shares of a wave (every SM adds
 // one to every candidate's slot) spread over the L2 slices, unless that takes more than 64 MB.
@@ -462,7 +478,11 @@ inline BuildLayout build_layout(int B, int K, int V, int M, int n, int H, int E)
   L.jobcount = align_up(L.joblist + sizeof(Job) * 2 * static_cast<size_t>(B) * kLargeLookahead);
   // the tensor-core GRU's A operand: one bf16 row [emb | hi(h_parent) | lo(h_parent)] per expansion of a wave
   L.xact = align_up(L.jobcount + sizeof(int) * (X + 2));
-  L.bytes = align_up(L.xact + sizeof(unsigned short) * static_cast<size_t>(B) * kLargeLookahead * (E + 2 * H));
+  L.gru_part = align_up(L.xact + sizeof(unsigned short) * static_cast<size_t>(B) * kLargeLookahead * (E + 2 * H));
+  L.gru_tiles = gru_spread_tiles(B, H);
+  L.gru_ticket = align_up(L.gru_part + sizeof(float) * static_cast<size_t>(L.gru_tiles) * kGruSplits * kGruTileRows *
+                                           4 * kGruTileUnits);
+  L.bytes = align_up(L.gru_ticket + sizeof(unsigned) * static_cast<size_t>(L.gru_tiles));
   return L;
 }
 

@@ -404,12 +404,12 @@ struct TmaMaps {
   CUtensorMap wih;  // [3H][E] bf16, box 64 x 32
   CUtensorMap whh;  // [3H][H] bf16, box 64 x 32
 };
-constexpr int kUmmaRows = 128, kUmmaUnits = 32, kUmmaBK = 64, kUmmaStages = 4;
+constexpr int kUmmaRows = 128, kUmmaUnits = 32, kUmmaBK = 64, kUmmaStages = 8;
 constexpr int kUmmaA = kUmmaRows * kUmmaBK * 2;            // 16 KB
 constexpr int kUmmaB = 3 * kUmmaUnits * kUmmaBK * 2;       // 12 KB
 constexpr int kUmmaStage = kUmmaA + kUmmaB;                // 28 KB (a multiple of 1024)
 constexpr size_t kUmmaSmem = static_cast<size_t>(kUmmaStages) * kUmmaStage + 1024;  // + alignment slack
-constexpr int kTmemCols = 128;
+constexpr int kTmemCols = 512;  // kSplits partials of 128 columns
 
 __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {  // K-major tile, 128-byte rows, 8-row atoms
   return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
@@ -432,14 +432,26 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
   asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
                ::"r"(smem_u32(dst)), "l"(map), "r"(c0), "r"(c1), "r"(smem_u32(bar)) : "memory");
 }
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
-  uint32_t r[8];
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-               : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+// Four 32-lane x 8-column TMEM loads, `stride` columns apart, and the wait for them, in one statement (nothing can
+// read the registers before the wait).
+__device__ __forceinline__ void tmem_ld4x8(uint32_t taddr, uint32_t stride, float (&v)[4][8]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%32];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8,%9,%10,%11,%12,%13,%14,%15}, [%33];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%16,%17,%18,%19,%20,%21,%22,%23}, [%34];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%24,%25,%26,%27,%28,%29,%30,%31}, [%35];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr), "r"(taddr + stride), "r"(taddr + 2 * stride), "r"(taddr + 3 * stride)
+      : "memory");
 #pragma unroll
-  for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(r[j]);
+  for (int g = 0; g < 4; ++g)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[g][j] = __uint_as_float(r[8 * g + j]);
 }
 
 // Per-launch state of the tensor-core phase: the ring's barriers and how far each has gone (the same in every thread).
@@ -452,21 +464,85 @@ struct UmmaRing {
   unsigned tiles;   // tiles finished so far (done phase)
 };
 
-// Returns false when a wait ran out (recorded, abort raised); nothing is then in flight from this CTA.
+// The GRU pointwise of U consecutive units u .. u + U - 1 of one expansion from its gate sums d[r | z | n_in | n_h][U].
+template <int U>
+__device__ __forceinline__ void gru_pointwise(const Params& p, const Job& jb, int u, const float (&d)[4][U], int X, int H) {
+  const float* hprev = p.hs + (static_cast<size_t>(jb.b) * X + jb.pslot) * H + u;
+  float* hout = p.hs + (static_cast<size_t>(jb.b) * X + jb.xslot) * H + u;
+#pragma unroll
+  for (int j = 0; j < U; ++j) {
+    const size_t g0 = u + j, g1 = static_cast<size_t>(H) + g0, g2 = 2 * static_cast<size_t>(H) + g0;
+    const float bir = p.b_ih ? ldw(p.b_ih, true, g0) : 0.f, bhr = p.b_hh ? ldw(p.b_hh, true, g0) : 0.f;
+    const float biz = p.b_ih ? ldw(p.b_ih, true, g1) : 0.f, bhz = p.b_hh ? ldw(p.b_hh, true, g1) : 0.f;
+    const float bin = p.b_ih ? ldw(p.b_ih, true, g2) : 0.f, bhn = p.b_hh ? ldw(p.b_hh, true, g2) : 0.f;
+    const float rg = sigmoidf_(d[0][j] + bir + bhr);
+    const float zg = sigmoidf_(d[1][j] + biz + bhz);
+    const float ng = tanhf(d[2][j] + bin + rg * (d[3][j] + bhn));
+    hout[j] = (1.f - zg) * ng + zg * __ldcg(hprev + j);
+  }
+}
+
+// The K range of the step is summed as kSplits partials in a fixed order, whoever computes them. A wave with enough
+// tiles gives each tile to one CTA, which holds all the partials in separate TMEM regions. A smaller wave gives each
+// CTA `per` consecutive partials of a tile (per = 1 or 2, so that kSplits / per CTAs share it and every CTA of the
+// phase has at most one). Those CTAs store their partials in the workspace, wait (bounded) for one another, and each
+// then adds up all kSplits partials for its share of the tile's units. Both ways give the same bits, so the result
+// of an expansion does not depend on how many share its wave.
+constexpr int kSplits = kGruSplits;
+static_assert(kUmmaRows == kGruTileRows && kUmmaUnits == kGruTileUnits, "workspace tiles are the MMA tiles");
+__device__ __forceinline__ int split_begin(int s, int nkb) { return s * nkb / kSplits; }
+
+// Adds up the kSplits partials of rows [row0, row0 + 128) x units [u0 + uoff, + 2 * U) of a tile from the workspace and
+// runs the GRU pointwise; thread t takes row t % 128 and U units from uoff + U * (t / 128).
+template <int U>
+__device__ __forceinline__ void reduce_partials(const Params& p, const Job* jl, int rows, const float* part, int row0,
+                                                int u0, int uoff, int X, int H) {
+  const int r = threadIdx.x & (kUmmaRows - 1), q = row0 + r, c = uoff + U * (threadIdx.x / kUmmaRows);
+  if (q >= rows) return;
+  float dsum[4][U];
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+#pragma unroll
+    for (int j = 0; j < U; ++j) dsum[g][j] = 0.f;
+#pragma unroll
+  for (int sp = 0; sp < kSplits; ++sp) {  // in order 0 .. kSplits - 1
+    const float* pr = part + static_cast<size_t>(sp) * kUmmaRows * 128 + r;
+    float v[4][U];
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+#pragma unroll
+      for (int j = 0; j < U; ++j) v[g][j] = __ldcg(pr + static_cast<size_t>(g * kUmmaUnits + c + j) * kUmmaRows);
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+#pragma unroll
+      for (int j = 0; j < U; ++j) dsum[g][j] += v[g][j];
+  }
+  gru_pointwise<U>(p, jl[q], u0 + c, dsum, X, H);
+}
+
+// Returns false when a wait ran out (recorded, abort raised).
 __device__ bool umma_gru_phase(const Params& p, const TmaMaps& maps, const Job* jl, int rows, unsigned char* smem,
                                UmmaRing& ring) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int E = p.E, H = p.H, X = p.xslots;
   const int nE = E / kUmmaBK, nH = H / kUmmaBK, nkb = nE + 2 * nH;
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem) + 1023) & ~uintptr_t(1023));
-  const int rtiles = (rows + kUmmaRows - 1) / kUmmaRows, utiles = H / kUmmaUnits;
+  const int rtiles = (rows + kUmmaRows - 1) / kUmmaRows, utiles = H / kUmmaUnits, tiles = rtiles * utiles;
+  const int G = static_cast<int>(gridDim.x);
+  const int per = tiles > p.gru_tiles ? kSplits : tiles * kSplits <= G ? 1 : tiles * (kSplits / 2) <= G ? 2 : kSplits;
+  const int cpt = kSplits / per;  // CTAs per tile
+  const int units = tiles * cpt;
+  __shared__ int s_ok;
   bool ok = true;
-  for (int tile = blockIdx.x; tile < rtiles * utiles; tile += gridDim.x) {
+  for (int unit = blockIdx.x; unit < units; unit += G) {
+    const int tile = unit / cpt, part_idx = unit % cpt;
+    const int s_lo = part_idx * per, s_hi = s_lo + per;
     const int row0 = (tile / utiles) * kUmmaRows, u0 = (tile % utiles) * kUmmaUnits;
+    const int kb_lo = split_begin(s_lo, nkb), kb_hi = split_begin(s_hi, nkb);
     if (warp == 0 && lane == 0) {  // TMA producer
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the other phases' shared-memory use came first
-      for (int kb = 0; kb < nkb && ok; ++kb) {
-        const unsigned n = ring.blocks + kb, st = n % kUmmaStages, use = n / kUmmaStages;
+      for (int kb = kb_lo; kb < kb_hi && ok; ++kb) {
+        const unsigned n = ring.blocks + (kb - kb_lo), st = n % kUmmaStages, use = n / kUmmaStages;
         if (use > 0) ok = mbar_wait(&ring.empty[st], (use - 1) & 1u, kCopyBudgetNs);
         if (!ok) break;
         unsigned char* a = base + st * kUmmaStage;
@@ -479,64 +555,112 @@ __device__ bool umma_gru_phase(const Params& p, const TmaMaps& maps, const Job* 
         for (int g = 0; g < 3; ++g)
           tma_load_2d(bsm + g * kUmmaUnits * 128, emb ? &maps.wih : &maps.whh, wcol, g * H + u0, &ring.full[st]);
       }
-    } else if (warp == 1 && lane == 0) {  // MMA issuer
-      for (int kb = 0; kb < nkb && ok; ++kb) {
-        const unsigned n = ring.blocks + kb, st = n % kUmmaStages, use = n / kUmmaStages;
+    } else if (warp == 1 && lane == 0) {  // MMA issuer: partial s into TMEM columns [128 (s - s_lo), +128)
+      for (int kb = kb_lo; kb < kb_hi && ok; ++kb) {
+        const unsigned n = ring.blocks + (kb - kb_lo), st = n % kUmmaStages, use = n / kUmmaStages;
         ok = mbar_wait(&ring.full[st], use & 1u, kCopyBudgetNs);
         if (!ok) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        int sp = s_lo;  // the partial this block belongs to
+        while (sp + 1 < s_hi && kb >= split_begin(sp + 1, nkb)) ++sp;
+        const int sb = split_begin(sp, nkb), hb = sb > nE ? sb : nE;  // its first block, its first hidden block
+        const uint32_t d = ring.tmem + 128u * static_cast<uint32_t>(sp - s_lo);
         const uint32_t a = smem_u32(base + st * kUmmaStage), bsm = a + kUmmaA;
         const bool emb = kb < nE;
 #pragma unroll
         for (int k = 0; k < kUmmaBK / 16; ++k) {
           const uint64_t da = umma_desc_sw128(a + 32 * k);
           if (emb) {
-            umma_f16(ring.tmem, da, umma_desc_sw128(bsm + 32 * k), umma_idesc(3 * kUmmaUnits), (kb > 0 || k > 0) ? 1u : 0u);
+            umma_f16(d, da, umma_desc_sw128(bsm + 32 * k), umma_idesc(3 * kUmmaUnits), (kb > sb || k > 0) ? 1u : 0u);
           } else {
-            umma_f16(ring.tmem, da, umma_desc_sw128(bsm + 32 * k), umma_idesc(2 * kUmmaUnits), 1u);
-            umma_f16(ring.tmem + 3 * kUmmaUnits, da, umma_desc_sw128(bsm + 2 * kUmmaUnits * 128 + 32 * k),
-                     umma_idesc(kUmmaUnits), (kb > nE || k > 0) ? 1u : 0u);
+            umma_f16(d, da, umma_desc_sw128(bsm + 32 * k), umma_idesc(2 * kUmmaUnits), (kb > sb || k > 0) ? 1u : 0u);
+            umma_f16(d + 3 * kUmmaUnits, da, umma_desc_sw128(bsm + 2 * kUmmaUnits * 128 + 32 * k),
+                     umma_idesc(kUmmaUnits), (kb > hb || k > 0) ? 1u : 0u);
           }
         }
         umma_commit(&ring.empty[st]);  // the stage is free once these MMAs have read it
       }
-      if (ok) umma_commit(ring.done);  // and the accumulator is complete after the last block's MMAs
+      if (ok) umma_commit(ring.done);  // and the partials are complete after the last block's MMAs
     }
-    ring.blocks += nkb;
+    ring.blocks += kb_hi - kb_lo;
     ok = __syncthreads_and(ok);
-    if (ok && warp >= 4) {  // epilogue: one row (expansion) per thread, the GRU pointwise of the tile's units
+    const int r = 32 * (warp & 3) + lane, q = row0 + r;  // the epilogue warps' row (expansion)
+    // a tile's partials in the workspace: [split][gate column][row], so that a warp's rows are adjacent words
+    float* part = p.gru_part + static_cast<size_t>(tile) * kSplits * kUmmaRows * 128;
+    if (ok) {  // epilogue: one row per thread, warps w and w + 4 (the same TMEM lanes) half of the units each
       ok = mbar_wait(ring.done, ring.tiles & 1u, kCopyBudgetNs);
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const int r = 32 * (warp - 4) + lane, q = row0 + r;
       const uint32_t trow = ring.tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
       Job jb{};
       if (q < rows) jb = jl[q];
-      for (int c = 0; c < kUmmaUnits; c += 8) {
-        float dr[8], dz[8], dn[8], dh[8];
-        tmem_ld8(trow + c, dr);  // every lane takes part in the loads (.sync.aligned)
-        tmem_ld8(trow + kUmmaUnits + c, dz);
-        tmem_ld8(trow + 2 * kUmmaUnits + c, dn);
-        tmem_ld8(trow + 3 * kUmmaUnits + c, dh);
-        if (q < rows && ok) {
-          const float* hprev = p.hs + (static_cast<size_t>(jb.b) * X + jb.pslot) * H + u0 + c;
-          float* hout = p.hs + (static_cast<size_t>(jb.b) * X + jb.xslot) * H + u0 + c;
+      const int c0 = (warp >> 2) * (kUmmaUnits / 2);
+      for (int c = c0; c < c0 + kUmmaUnits / 2; c += 8) {
+        float dsum[4][8];
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) dsum[g][j] = 0.f;
+        for (int sp = s_lo; sp < s_hi; ++sp) {
+          const int sb = split_begin(sp, nkb), se = split_begin(sp + 1, nkb);
+          // n_in is written only by embedding blocks, n_h only by hidden ones, nothing by an empty split (K shorter
+          // than kSplits blocks): what a partial did not write contributes 0
+          const bool has_any = se > sb, has_emb = has_any && sb < nE, has_hid = has_any && se > nE;
+          float dv[4][8];
+          tmem_ld4x8(trow + 128u * static_cast<uint32_t>(sp - s_lo) + c, kUmmaUnits, dv);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const size_t g0 = u0 + c + j, g1 = static_cast<size_t>(H) + g0, g2 = 2 * static_cast<size_t>(H) + g0;
-            const float bir = p.b_ih ? ldw(p.b_ih, true, g0) : 0.f, bhr = p.b_hh ? ldw(p.b_hh, true, g0) : 0.f;
-            const float biz = p.b_ih ? ldw(p.b_ih, true, g1) : 0.f, bhz = p.b_hh ? ldw(p.b_hh, true, g1) : 0.f;
-            const float bin = p.b_ih ? ldw(p.b_ih, true, g2) : 0.f, bhn = p.b_hh ? ldw(p.b_hh, true, g2) : 0.f;
-            const float rg = sigmoidf_(dr[j] + bir + bhr);
-            const float zg = sigmoidf_(dz[j] + biz + bhz);
-            const float ng = tanhf(dn[j] + bin + rg * (dh[j] + bhn));
-            hout[j] = (1.f - zg) * ng + zg * __ldcg(hprev + j);
+            if (!has_any) dv[0][j] = dv[1][j] = 0.f;
+            if (!has_emb) dv[2][j] = 0.f;
+            if (!has_hid) dv[3][j] = 0.f;
+          }
+          if (per < kSplits) {  // this CTA's partials, for the tile's CTAs to add up
+            if (ok && q < rows) {
+              float* pr = part + static_cast<size_t>(sp) * kUmmaRows * 128 + r;
+#pragma unroll
+              for (int g = 0; g < 4; ++g)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) pr[static_cast<size_t>(g * kUmmaUnits + c + j) * kUmmaRows] = dv[g][j];
+            }
+          } else {  // partials in order 0 .. kSplits - 1
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+#pragma unroll
+              for (int j = 0; j < 8; ++j) dsum[g][j] += dv[g][j];
           }
         }
+        if (per == kSplits && q < rows && ok) gru_pointwise<8>(p, jb, u0 + c, dsum, X, H);
+      }
+    }
+    if (per < kSplits) {  // the tile's CTAs meet, then each adds up all partials for its share of the units
+      __threadfence();
+      ok = __syncthreads_and(ok);
+      if (t == 0) {
+        bool met = ok;
+        if (met) {
+          unsigned* tk = p.gru_ticket + tile;
+          atom_add_acq_rel_gpu(tk, 1u);
+          const uint64_t t0 = global_timer_ns();
+          while (ld_acquire_gpu(tk) < static_cast<unsigned>(cpt)) {  // the others run now: one unit per CTA
+            if (global_timer_ns() - t0 > kCopyBudgetNs || ld_acquire_gpu(&p.hdr->abort) != 0u) {
+              met = false;
+              break;
+            }
+          }
+        }
+        s_ok = met;
+      }
+      __syncthreads();
+      ok = s_ok != 0;
+      if (ok) {
+        __threadfence();
+        const int share = kUmmaUnits / cpt;  // 8 or 16 units of this CTA, over two groups of 128 threads
+        if (share == 8) reduce_partials<4>(p, jl, rows, part, row0, u0, part_idx * share, X, H);
+        else reduce_partials<8>(p, jl, rows, part, row0, u0, part_idx * share, X, H);
       }
     }
     ring.tiles += 1;
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    ok = __syncthreads_and(ok);  // the accumulator is read before the next tile's first MMA overwrites it
+    ok = __syncthreads_and(ok);  // the accumulators are read before the next unit's first MMA overwrites them
     if (!ok) {
       record_error(p.hdr, DT_ERR_TIMEOUT);
       atomicExch(&p.hdr->abort, 1u);
@@ -773,6 +897,7 @@ __device__ void init_requests(const Params& p, unsigned char* smem) {
   const ReqLayout RL = req_layout(n, X, KM, p.lookahead);
   // wave 0 expands the roots: its packed list holds one job per request
   for (int i = blockIdx.x * kThreads + t; i < X + 2; i += gridDim.x * kThreads) p.jobcount[i] = i == 0 ? p.B : 0;
+  for (int i = blockIdx.x * kThreads + t; i < p.gru_tiles; i += gridDim.x * kThreads) p.gru_ticket[i] = 0u;
   for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
     if (t == 0) p.joblist[b] = Job{b, 0, -1, 0, 0, 0.f, {0, 0}};
     const ReqView R = req_view(p.rstate + static_cast<size_t>(b) * RL.bytes, RL);
@@ -823,6 +948,9 @@ __device__ void run_waves(const Params& p, const TmaMaps& maps, unsigned char* s
       }
       target += G;
       if (!counter_barrier(p.hdr, target, p.timeout_ns, s_flag)) return;
+      // every CTA has left the GRU phase: its meeting counters start again from zero for the next wave
+      if (kGemm == 4 && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < p.gru_tiles; i += kThreads) p.gru_ticket[i] = 0u;
     }
     if (!children_phase(p, jl, rows, smem, bar, bar_uses)) return;
     if (p.B < static_cast<int>(G)) {  // children computed by other CTAs: wait for all of them
@@ -838,7 +966,7 @@ __device__ void run_waves(const Params& p, const TmaMaps& maps, unsigned char* s
 }
 
 // kGemm: 0 = CUDA-core GRU tiles (fp32 weights or other widths), mma.sync tensor-core tiles with 1 = TileS,
-// 2 = TileL, 3 = TileS128; 4 = tcgen05 tiles (bf16, E and H multiples of 64). With kGemm = 4 the CTA holds 128 TMEM
+// 2 = TileL, 3 = TileS128; 4 = tcgen05 tiles (bf16, E and H multiples of 64). With kGemm = 4 the CTA holds 512 TMEM
 // columns for the whole launch and frees them on every way out.
 template <int kGemm>
 __global__ void __launch_bounds__(kThreads, 1) build_kernel(Params p, const __grid_constant__ TmaMaps maps) {
@@ -997,6 +1125,9 @@ extern "C" dt_status dt_build_trees(int B, int K, int V, int M, int n, int max_d
   p.joblist = reinterpret_cast<Job*>(ws + L.joblist);
   p.jobcount = reinterpret_cast<int*>(ws + L.jobcount);
   p.xact = reinterpret_cast<unsigned short*>(ws + L.xact);
+  p.gru_part = reinterpret_cast<float*>(ws + L.gru_part);
+  p.gru_ticket = reinterpret_cast<unsigned*>(ws + L.gru_ticket);
+  p.gru_tiles = L.gru_tiles;
   p.acc_stride = acc_stride(M, n);
   p.xslots = expansion_slots(n);
   p.timeout_ns = barrier_timeout_ns();
@@ -1017,8 +1148,9 @@ extern "C" dt_status dt_build_trees(int B, int K, int V, int M, int n, int max_d
   // phase A: tensor cores for bf16 weights whose widths are multiples of the pipeline chunk; the larger tile once a
   // wave can hold 128 expansions or more
   const long long max_rows = static_cast<long long>(B) * p.lookahead;
-  // tcgen05 tiles (128 expansions x 32 units) once a wave can fill the SMs with them
-  const bool umma = p.bf16 && E % kUmmaBK == 0 && H % kUmmaBK == 0 && max_rows >= 512;
+  // tcgen05 tiles (128 expansions x 32 units) for every bf16 wave whose widths fit them: the K split makes the sums
+  // independent of the wave's size, so the tree does not depend on the lookahead width
+  const bool umma = p.bf16 && E % kUmmaBK == 0 && H % kUmmaBK == 0 && kUmmaSmem + 2048 <= static_cast<size_t>(di.optin);
   const int gemm = !p.bf16 ? 0
                    : umma ? 4
                    : max_rows >= 128 ? (E % TileL::kKc == 0 && H % TileL::kKc == 0 ? 2 : 0)

@@ -62,6 +62,7 @@ def tiny(seed, **kw):
     dict(dtype="bf16", n=25, T=2.0),
     dict(dtype="bf16", M=40, n=64, max_depth=5, K=5),    # a wide, deep frontier
     dict(B=3, V=9000, M=100, n=40, T=1.0, logit_scale=0.5),
+    dict(dtype="bf16", B=20, E=64, H=64, n=20),          # tensor-core GRU with fewer K blocks than K splits
 ])
 def test_build_edge_cases(dtlib, orc, kw):
     inp = tiny(abs(hash(str(sorted(kw.items())))) % 10000, **kw)
@@ -149,6 +150,8 @@ def test_out_of_range_ids_are_reported_not_gathered(dtlib):
     dict(config=2, B=16),                                              # the large-batch builder
     dict(config=3, B=12),                                              # ... deeper trees, H = 1024
     dict(config=4, B=12),                                              # ... M = 128, n = 64
+    dict(config=2, B=160),                                             # ... GRU tiles on one CTA each at k = 8,
+                                                                       #     K split over CTAs at k = 1
     dict(tiny=dict(B=20, M=6, n=30, max_depth=4)),                     # ... fp32, CUDA-core GRU tiles
 ])
 def test_lookahead_width_does_not_change_the_tree(dtlib, case):
