@@ -36,6 +36,8 @@ template <bool kBf16, int kThreads>
 struct Topm {
   static constexpr int kPer16 = kBf16 ? 8 : 4;  // logits per 16-byte load
   static constexpr int kGroups = 16;            // 16-byte groups per thread: 64 KB of shared memory per CTA
+  static constexpr int kParts = 4;              // copy groups committed per thread, waited for one by one
+  static constexpr int kPartGroups = kGroups / kParts;
   static constexpr int kPer = kGroups * kPer16;  // logits per thread
   static constexpr int kChunk = kThreads * kPer;
   static constexpr int kKeyBits = kBf16 ? 16 : 32;
@@ -62,8 +64,8 @@ struct Topm {
   // Stages this thread's logits into the shared chunk (16-byte groups t, t + kThreads, ...): whole groups inside
   // the row by cp.async (no registers held while the bytes are in flight), the rest element by element. Past the
   // end of the row the slots hold -inf, which never changes a maximum and is kept out of the candidates by its
-  // index. The caller waits (cp.async.wait_group 0) and synchronises before reading. Reports NaNs (fp32 here,
-  // after the wait; bf16 in max_key).
+  // index. The copies are committed in kParts groups of kPartGroups; a thread waits for its parts (wait_part) and
+  // reads only the groups it staged itself, so no barrier is needed before it computes on them.
   __device__ __forceinline__ void stage(const void* logits, long long row_off, int c0, int len, bool vec_ok) const {
     const int t = threadIdx.x;
     constexpr uint32_t kPad = kBf16 ? 0xFF80FF80u : 0xFF800000u;
@@ -72,10 +74,12 @@ struct Topm {
     const unsigned dst0 = static_cast<unsigned>(__cvta_generic_to_shared(s_ + t));
     if (vec_ok && len == kChunk) {  // a whole chunk: constant offsets, no tests
 #pragma unroll
-      for (int k = 0; k < kGroups; ++k)
+      for (int k = 0; k < kGroups; ++k) {
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
                      ::"r"(dst0 + 16u * kThreads * k), "l"(src0 + 16ll * kThreads * k)
                      : "memory");
+        if (k % kPartGroups == kPartGroups - 1) asm volatile("cp.async.commit_group;" ::: "memory");
+      }
     } else {
 #pragma unroll
       for (int k = 0; k < kGroups; ++k) {
@@ -96,9 +100,14 @@ struct Topm {
           }
           s_[t + kThreads * k] = make_uint4(w[0], w[1], w[2], w[3]);
         }
+        if (k % kPartGroups == kPartGroups - 1) asm volatile("cp.async.commit_group;" ::: "memory");
       }
     }
-    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  // Waits until the copies of this thread's parts 0 .. p have landed (a thread reads only its own staged groups).
+  template <int p>
+  __device__ static __forceinline__ void wait_part() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(kParts - 1 - p) : "memory");
   }
   __device__ __forceinline__ bool any_nan_f32() const {
     bool nan = false;
@@ -157,14 +166,14 @@ struct Topm {
   // packed compare covers two logits and the common "nothing here" group costs five instructions.
   // With kNan (bf16), the same pass also folds the groups into a NaN-propagating maximum and sets `nan` when a NaN
   // is present: one pass over the chunk when the bound is known in advance.
-  template <bool kNan = false>
+  template <bool kNan = false, int kFrom = 0, int kTo = kGroups>
   __device__ __forceinline__ unsigned group_mask(uint32_t thr_bits, bool* nan = nullptr) const {
     unsigned sel = 0;
     if (kBf16) {
       const __nv_bfloat162 th = as_bf2(thr_bits | (thr_bits << 16));
       __nv_bfloat162 mx = as_bf2(0xFF80FF80u);
 #pragma unroll
-      for (int k = 0; k < kGroups; ++k) {
+      for (int k = kFrom; k < kTo; ++k) {
         const uint4 v = g_(k);
         const unsigned any = __hge2_mask(as_bf2(v.x), th) | __hge2_mask(as_bf2(v.y), th) |
                              __hge2_mask(as_bf2(v.z), th) | __hge2_mask(as_bf2(v.w), th);
@@ -179,7 +188,7 @@ struct Topm {
     } else {
       const float th = __uint_as_float(thr_bits);
 #pragma unroll
-      for (int k = 0; k < kGroups; ++k) {
+      for (int k = kFrom; k < kTo; ++k) {
         const uint4 v = g_(k);
         const bool any = __uint_as_float(v.x) >= th || __uint_as_float(v.y) >= th || __uint_as_float(v.z) >= th ||
                          __uint_as_float(v.w) >= th;
@@ -236,23 +245,71 @@ struct Topm {
   }
 };
 
-// The M-th largest of kN keys in shared memory (kN a multiple of 32), by one warp: bisection on the key bits,
-// counting with ballots.
-template <int kKeyBits, int kN>
-__device__ __forceinline__ uint32_t warp_kth_key(const uint32_t* keys, int M) {
-  const int lane = threadIdx.x & 31;
-  uint32_t v[kN / 32];
+// Lane L of warp 0 holds the counts cb[0..7] of bins 255 - 8L down to 248 - 8L, and `excl` words in the bins above
+// them. Returns the first j with excl + cb[0] + ... + cb[j] >= need (7 if none before the last), and sets `acc` to
+// the words above bin j and `at` to cb[j] (no run-time indexing of cb: it stays in registers).
+__device__ __forceinline__ int pick_bin(const unsigned (&cb)[8], unsigned excl, unsigned need, unsigned& acc,
+                                        unsigned& at) {
+  acc = excl;
+  int j = 0;
+  bool stop = false;
 #pragma unroll
-  for (int i = 0; i < kN / 32; ++i) v[i] = keys[lane + 32 * i];
-  uint32_t th = 0;
-  for (int bit = kKeyBits - 1; bit >= 0; --bit) {
-    const uint32_t c = th | (1u << bit);
-    int cnt = 0;
-#pragma unroll
-    for (int i = 0; i < kN / 32; ++i) cnt += __popc(__ballot_sync(0xFFFFFFFFu, v[i] >= c));
-    if (cnt >= M) th = c;
+  for (int i = 0; i < 7; ++i) {
+    stop = stop || acc + cb[i] >= need;
+    if (!stop) {
+      acc += cb[i];
+      j = i + 1;
+    }
   }
-  return th;
+  at = cb[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i)
+    if (i == j) at = cb[i];
+  return j;
+}
+
+// The M-th largest of the block's keys, one per thread (1 <= M <= kThreads), in every thread: radix select with
+// 8-bit digits from the top, one 256-bin shared histogram per digit over the keys that share the digits found so far.
+template <int kKeyBits, int kThreads>
+__device__ __forceinline__ uint32_t block_kth_key(uint32_t key, int M, unsigned* hist, unsigned* s_sel) {
+  static_assert(kThreads >= 256, "one histogram bin per thread");
+  const int t = threadIdx.x, lane = t & 31;
+  uint32_t prefix = 0;
+  int need = M;
+#pragma unroll
+  for (int d = kKeyBits / 8 - 1; d >= 0; --d) {
+    if (t < 256) hist[t] = 0u;
+    __syncthreads();
+    const bool match = d == kKeyBits / 8 - 1 || (key >> (8 * (d + 1))) == prefix;
+    if (match) atomicAdd(&hist[(key >> (8 * d)) & 255u], 1u);
+    __syncthreads();
+    if (t < 32) {  // lane L holds bins 255 - 8L down to 248 - 8L: counts from the top
+      unsigned cb[8], sum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        cb[j] = hist[255 - 8 * lane - j];
+        sum += cb[j];
+      }
+      unsigned incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned excl = incl - sum;
+      if (excl < static_cast<unsigned>(need) && incl >= static_cast<unsigned>(need)) {
+        unsigned acc, at;
+        const int j = pick_bin(cb, excl, static_cast<unsigned>(need), acc, at);
+        s_sel[0] = static_cast<unsigned>(255 - 8 * lane - j);
+        s_sel[1] = acc;
+      }
+    }
+    __syncthreads();
+    prefix = (prefix << 8) | s_sel[0];
+    need -= static_cast<int>(s_sel[1]);
+    __syncthreads();  // s_sel and hist are rewritten by the next digit
+  }
+  return prefix;
 }
 
 // Ranks the `total` distinct words of cand; the M largest, in descending order, go to out[0..M). Slots past `total`
@@ -291,19 +348,23 @@ constexpr int kCandMax = 1024;  // >= topm_cap(M) for every supported M
 constexpr size_t kChunkSmem = static_cast<size_t>(kFThreads) * 16 * 16;  // 64 KB: the staged chunk
 
 // ---- the row's final selection (run by the row's last filter CTA) -----------------------------------------------
-// The row's candidates (a few hundred words) as 64-bit words (value key, inverted row index), the exact M-th largest
-// word by radix select (8-bit digits from the top, 256-bin shared histograms; stops once a digit's bin is taken
-// whole, or once the key digits are fixed and the ties fit the ranking buffer), then the words at or above it
-// ranked by counting and the first M written out in order. Candidates written by other CTAs are read through L2.
+// The row's candidates (a few hundred words) as 64-bit words (value key, inverted row index), gathered into shared
+// memory (the chunks' counts, their offsets by a scan, then the words). The M-th largest word is then bracketed by one histogram of the keys relative to the smallest candidate key (256 bins,
+// as fine as the key range allows): the words of the bins at and above the bin holding the M-th largest are ranked
+// by counting, and the first M are written out in order. When that bin holds too many words, the M-th largest word
+// is found by radix select instead (8-bit digits from the top; stops once a digit's bin is taken whole, or once the
+// key digits are fixed and the ties fit the ranking buffer). Candidates written by other CTAs are read through L2.
 constexpr int kSelThreads = kFThreads;
-constexpr int kSelCap = 4096;                 // candidate words of a row kept in shared memory (more: re-read)
-constexpr int kMaxChunks = 4 * kSelThreads;   // chunk offsets kept in shared memory up to this many chunks
+constexpr int kSelCap = 2048;                 // candidate words of a row kept in shared memory (more: re-read)
+constexpr int kChunksPerThread = 1;
+constexpr int kMaxChunks = kChunksPerThread * kSelThreads;  // chunk offsets kept in shared memory up to this many
 struct SelectSmem {                           // lives in the filter's 64 KB chunk buffer
   uint64_t w[kSelCap];
-  uint64_t top[DT_MAX_M];
+  uint64_t top[DT_MAX_M];                     // the words ranked by counting
   int off[kMaxChunks + 1];
   unsigned hist[256];
   unsigned sel[2];
+  unsigned red[2][kSelThreads / 32];          // per-warp key minima and maxima
 };
 static_assert(sizeof(SelectSmem) <= kChunkSmem, "the selection fits the chunk buffer");
 
@@ -321,25 +382,25 @@ __device__ void select_row(int row, const void* __restrict__ words, const int* _
   unsigned* hist = S.hist;
   unsigned* sel = S.sel;
   int& s_n = *s_n_ptr;
-  const int t = threadIdx.x, lane = t & 31;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const CWord* base = static_cast<const CWord*>(words) + static_cast<size_t>(row) * chunks * cap;
   const int* cnt = counts + static_cast<size_t>(row) * chunks;
-  const bool few = chunks <= kMaxChunks;
   int total = 0;
+  const bool few = chunks <= kMaxChunks;
   if (few) {  // per-chunk offsets of the row's candidates, one parallel load and a scan
-    int c4[4], mine = 0;
+    int mine = 0, c_of[kChunksPerThread];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int c = 4 * t + j;
-      c4[j] = c < chunks ? __ldcg(cnt + c) : 0;
-      mine += c4[j];
+    for (int j = 0; j < kChunksPerThread; ++j) {
+      const int c = kChunksPerThread * t + j;
+      c_of[j] = c < chunks ? __ldcg(cnt + c) : 0;
+      mine += c_of[j];
     }
     int off = block_exclusive_scan<kWarps>(mine, &total, s_warp);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int c = 4 * t + j;
+    for (int j = 0; j < kChunksPerThread; ++j) {
+      const int c = kChunksPerThread * t + j;
       if (c <= chunks) s_off[c] = off;
-      off += c4[j];
+      off += c_of[j];
     }
   } else {
     int mine = 0;
@@ -373,7 +434,60 @@ __device__ void select_row(int row, const void* __restrict__ words, const int* _
     }
   };
   uint64_t thresh = 0;  // take every word >= thresh
-  if (total > M) {
+  bool bracketed = false;
+  if (total > M && in_smem) {
+    // the candidates' key range, then one histogram relative to its minimum
+    uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+    for (int i = t; i < total; i += kSelThreads) {
+      const uint32_t k = candidate_key(w[i]);
+      kmin = min(kmin, k);
+      kmax = max(kmax, k);
+    }
+    kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
+    kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
+    if (lane == 0) {
+      S.red[0][warp] = kmin;
+      S.red[1][warp] = kmax;
+    }
+    hist[t] = 0u;  // kSelThreads == 256 bins
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i) {
+      kmin = min(kmin, S.red[0][i]);
+      kmax = max(kmax, S.red[1][i]);
+    }
+    int shift = 0;
+    while (((kmax - kmin) >> shift) > 255u) ++shift;
+    for (int i = t; i < total; i += kSelThreads) atomicAdd(&hist[(candidate_key(w[i]) - kmin) >> shift], 1u);
+    __syncthreads();
+    if (t < 32) {  // lane L holds bins 255 - 8L down to 248 - 8L: counts from the top
+      unsigned cb[8], sum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        cb[j] = hist[255 - 8 * lane - j];
+        sum += cb[j];
+      }
+      unsigned incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned excl = incl - sum;
+      if (excl < static_cast<unsigned>(M) && incl >= static_cast<unsigned>(M)) {
+        unsigned acc, at;
+        const int j = pick_bin(cb, excl, static_cast<unsigned>(M), acc, at);
+        sel[0] = static_cast<unsigned>(255 - 8 * lane - j);  // the bin holding the M-th largest
+        sel[1] = acc + at;                                    // words at or above it
+      }
+    }
+    __syncthreads();
+    if (sel[1] <= static_cast<unsigned>(DT_MAX_M)) {
+      thresh = static_cast<uint64_t>(kmin + (sel[0] << shift)) << 32;  // the bin's smallest key, any index
+      bracketed = true;
+    }
+  }
+  if (total > M && !bracketed) {
     uint64_t prefix = 0, pmask = 0;
     int need = M;
     for (int d = kTopDigit; d >= 0; --d) {
@@ -398,9 +512,8 @@ __device__ void select_row(int row, const void* __restrict__ words, const int* _
         }
         const unsigned excl = incl - sum;
         if (excl < static_cast<unsigned>(need) && incl >= static_cast<unsigned>(need)) {
-          unsigned acc = excl;
-          int j = 0;
-          while (j < 7 && acc + cb[j] < static_cast<unsigned>(need)) acc += cb[j++];
+          unsigned acc, at;
+          const int j = pick_bin(cb, excl, static_cast<unsigned>(need), acc, at);
           sel[0] = static_cast<unsigned>(255 - 8 * lane - j);
           sel[1] = acc;
         }
@@ -423,7 +536,7 @@ __device__ void select_row(int row, const void* __restrict__ words, const int* _
     if (wd >= thresh) top[atomicAdd(&s_n, 1)] = wd;
   });
   __syncthreads();
-  const int m = s_n;  // min(M, total)
+  const int m = s_n;  // the words ranked: min(M, total) up to the ranking buffer
   uint64_t* sorted = w;  // the row's words are no longer needed
   __syncthreads();
   rank_and_emit<kSelThreads>(top, m, M, sorted);
@@ -448,7 +561,8 @@ __global__ void __launch_bounds__(kFThreads, 3)
   constexpr uint32_t kMinKey = kBf16 ? 0x7Fu : 0x7FFFFFu;  // key of -inf: every real logit has a key >= it
   extern __shared__ uint4 chunk_s[];
   __shared__ CWord cand[kCandMax];
-  __shared__ uint32_t tmax[kFThreads];
+  __shared__ unsigned tmax[kFThreads];  // the bound's digit histogram
+  __shared__ unsigned s_sel[2];
   __shared__ int s_warp[kWarps];
   __shared__ uint32_t s_theta;
   __shared__ int s_n;
@@ -458,36 +572,55 @@ __global__ void __launch_bounds__(kFThreads, 3)
   const int c0 = chunk * T::kChunk;
   const int len = min(T::kChunk, V - c0);
 
-  T x{chunk_s};
-  x.stage(logits, row_off, c0, len, vec_ok);
+  // every CTA of the grid has started once all have passed here: the selection launch may then take the SMs that
+  // the filter's last wave leaves free (it waits for the filter's completion before reading anything)
+  if (!kFuse) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // Any chunk's lane-maximum bound is a lower bound of the whole row's M-th largest: a later chunk of the row takes
-  // the largest one published so far instead of computing its own. Read while the chunk is in flight.
+  // the largest one published so far instead of computing its own. Read before the chunk's copies are issued (the
+  // load would otherwise queue behind them).
   if (t == 0) {
     s_n = 0;
     s_theta = M <= kFThreads ? *reinterpret_cast<volatile uint32_t*>(bounds + row) : 0u;
   }
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
-  __syncthreads();
-  bool nan = kBf16 ? false : x.any_nan_f32();
-  const bool known = s_theta != 0u;  // uniform: written by thread 0 before the barrier
-  if (!known) {  // this chunk computes (and publishes) the bound
-    tmax[t] = x.max_key(nan);
-    __syncthreads();  // every thread has read s_theta, tmax is complete
-    if (warp == 0) {
-      const uint32_t th = M <= kFThreads ? warp_kth_key<T::kKeyBits, kFThreads>(tmax, M) : 0u;
-      if (lane == 0) {
-        s_theta = th;
-        if (th) atomicMax(bounds + row, th);
-      }
-    }
-    __syncthreads();
-  }
+  T x{chunk_s};
+  x.stage(logits, row_off, c0, len, vec_ok);
   // bit pattern of the smallest value whose key is >= key
   auto thr_of = [&](uint32_t key) -> uint32_t {
     if (key <= kMinKey) return kNegInf;
     return kBf16 ? ((key & 0x8000u) ? (key & 0x7FFFu) : (~key & 0xFFFFu))
                  : ((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
   };
+  __syncthreads();
+  const bool known = s_theta != 0u;  // uniform: written by thread 0 before the barrier
+  bool nan = false;
+  unsigned sel_known = 0;  // with a known bound (bf16): the groups holding candidates, found part by part
+  if (kBf16 && known) {
+    // each part is scanned as soon as this thread's copies of it have landed, while the later parts are in flight
+    const uint32_t thr = thr_of(s_theta);
+    T::template wait_part<0>();
+    sel_known |= x.template group_mask<true, 0, T::kPartGroups>(thr, &nan);
+    T::template wait_part<1>();
+    sel_known |= x.template group_mask<true, T::kPartGroups, 2 * T::kPartGroups>(thr, &nan);
+    T::template wait_part<2>();
+    sel_known |= x.template group_mask<true, 2 * T::kPartGroups, 3 * T::kPartGroups>(thr, &nan);
+    T::template wait_part<3>();
+    sel_known |= x.template group_mask<true, 3 * T::kPartGroups, T::kGroups>(thr, &nan);
+  } else {
+    T::template wait_part<T::kParts - 1>();
+    if (!kBf16) nan = x.any_nan_f32();
+  }
+  if (!known) {  // this chunk computes (and publishes) the bound
+    const uint32_t mk = x.max_key(nan);
+    if (M <= kFThreads) {
+      __syncthreads();  // every thread has read s_theta
+      const uint32_t th = block_kth_key<T::kKeyBits, kFThreads>(mk, M, tmax, s_sel);
+      if (t == 0) {
+        s_theta = th;
+        if (th) atomicMax(bounds + row, th);
+      }
+      __syncthreads();
+    }
+  }
   // Appends the elements whose bits are set in e0 (groups 0..7) and e1 (groups 8..15), kPer16 bits per group. One
   // shared atomic per warp reserves the warp's slots; slots past cap are dropped (and show up as s_n > cap). The
   // chunk is in shared memory, so groups are visited by run-time index (no unrolling, few registers).
@@ -537,7 +670,7 @@ __global__ void __launch_bounds__(kFThreads, 3)
     const uint32_t thr = thr_of(s_theta);
     uint64_t e0, e1;
     // cheap "anything here" test first; with a known bound it is the only pass and also looks for NaNs
-    const unsigned sel = known && kBf16 ? x.template group_mask<true>(thr, &nan) : x.group_mask(thr);
+    const unsigned sel = known && kBf16 ? sel_known : x.group_mask(thr);
     masks(sel, thr, false, e0, e1);
     append(e0, e1);
   }
@@ -606,7 +739,7 @@ __global__ void __launch_bounds__(kFThreads, 3)
 }
 
 template <bool kBf16>
-__global__ void __launch_bounds__(kSelThreads) topm_select_kernel(const void* __restrict__ words,
+__global__ void __launch_bounds__(kSelThreads, 7) topm_select_kernel(const void* __restrict__ words,
                                                                   const int* __restrict__ counts, int chunks, int cap,
                                                                   int M, uint32_t* __restrict__ bounds,
                                                                   int32_t* __restrict__ out_ids,
@@ -614,6 +747,9 @@ __global__ void __launch_bounds__(kSelThreads) topm_select_kernel(const void* __
   extern __shared__ uint4 smem_u4[];
   __shared__ int s_warp[kSelThreads / 32];
   __shared__ int s_n;
+  // Launched as a programmatic dependent of the filter: the CTAs may start while its last CTAs still run, and wait
+  // here until that launch has completed and its writes are visible (a no-op after an ordinary launch).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (threadIdx.x == 0) bounds[blockIdx.x] = 0u;  // the filter launch has finished with it: zero for the next call
   select_row<kBf16>(blockIdx.x, words, counts, chunks, cap, M, out_ids, out_vals,
                     *reinterpret_cast<SelectSmem*>(smem_u4), s_warp, &s_n);
@@ -650,8 +786,20 @@ dt_status launch_topm(const void* logits, dt_dtype dtype, int B, int K, int V, i
     } else {
       topm_filter_kernel<kB, false><<<grid, kFThreads, kChunkSmem, stream>>>(
           logits, V, M, chunks, L.cap, vec_ok, bounds, tickets, words, counts, out_ids, out_vals, hdr);
-      topm_select_kernel<kB><<<static_cast<unsigned>(rows), kSelThreads, sizeof(SelectSmem), stream>>>(
-          words, counts, chunks, L.cap, M, bounds, out_ids, out_vals);
+      cudaLaunchConfig_t cfg{};
+      cfg.gridDim = dim3(static_cast<unsigned>(rows));
+      cfg.blockDim = dim3(kSelThreads);
+      cfg.dynamicSmemBytes = sizeof(SelectSmem);
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaLaunchKernelEx(&cfg, topm_select_kernel<kB>, static_cast<const void*>(words),
+                             static_cast<const int*>(counts), chunks, L.cap, M, bounds, out_ids, out_vals) !=
+          cudaSuccess)
+        return false;
     }
     return true;
   };
