@@ -12,13 +12,15 @@
 //     the next unexpanded nodes in the order best-first would reach them; the pops themselves stay exact, see
 //     request_step), so a round takes a few waves rather than n steps;
 //   * phase A (all CTAs): the GRU step of every expansion of the wave as one GEMM, rows = the packed expansions,
-//     columns = the r, z, n_in, n_h gate sets of the hidden units, tensor cores (mma.sync) for bf16 weights;
+//     columns = the r, z, n_in, n_h gate sets of the hidden units: tcgen05 tiles for bf16 weights whose widths are
+//     multiples of 64, else mma.sync or CUDA-core tiles;
 //   * grid barrier;
-//   * phase B (the CTA that owns the request): its best-first state comes into shared memory as one bulk copy; for
-//     each expansion, the M correction rows of the node's block position dotted with its new hidden state, the
-//     restricted log-softmax, the children ranked; then one warp pops and picks the next wave's expansions, which
-//     join the packed list of the next wave; the state goes back as one bulk copy; a finished request writes its
-//     outputs and ancestor mask;
+//   * phase B1 (spread over all CTAs): for each expansion, the M correction rows of the node's block position dotted
+//     with its new hidden state, the restricted log-softmax, the children ranked into the request's state block;
+//   * grid barrier (unless every CTA took its own requests' expansions);
+//   * phase B2 (the CTA that owns the request): its best-first state comes into shared memory as one bulk copy; one
+//     warp pops and picks the next wave's expansions, which join the packed list of the next wave; the state goes
+//     back as one bulk copy; a finished request writes its outputs and ancestor mask;
 //   * grid barrier; next wave (none when no request added an expansion).
 // Every reduction has a fixed order (no floating-point atomics), so the output is bit-identical run to run and
 // does not depend on the lookahead width or on where an expansion sits in the packed list.
@@ -359,9 +361,9 @@ __device__ void gemm_gru_phase(const Params& p, const Job* jl, int rows, unsigne
   }
 }
 
-// ---- phase B: the expansions' children, then pops and picks (the CTA that owns the request) ---------------------
-// Shared memory of the phase: the request's state block, then per expansion [H] hidden state, [M4] logits,
-// [M4] base logits, [M4] ids, [M] sibling keys, [M] children, then (when it fits) the M gathered W_c rows.
+// ---- phases B1 / B2: shared memory --------------------------------------------------------------------------------
+// The children phase holds, per expansion, [H] hidden state, [M4] logits, [M4] base logits, [M4] ids, [M] sibling
+// keys, [M] children, then (when it fits) the M gathered W_c rows; the control phase holds one request's state block.
 __host__ __device__ inline int round4(int x) { return (x + 3) & ~3; }
 struct FrontierSmem {
   size_t h, z, vals, ids, keys, kraw, rows, bytes;
@@ -394,11 +396,12 @@ __device__ __forceinline__ void bulk_s2g(void* gdst, const void* ssrc, unsigned 
 // ---- phase A on the 5th-generation tensor cores (tcgen05, TMEM, 2-D TMA) ---------------------------------------
 // One tile = 128 expansions (rows) x 32 hidden units. The A operand is the packed activations [emb | hi(h) | lo(h)]
 // of the wave (bf16, written by the control phase that picked the expansions), the B operand the r, z, n gate rows of
-// the tile's units in W_ih / W_hh, both K-major, moved by TMA in 64-column blocks with 128-byte swizzle through a
-// 4-stage ring of full / empty mbarriers. One lane issues the TMA loads, one lane the MMAs (kind::f16, fp32 accumulate
+// the tile's units in W_ih / W_hh, both K-major, moved by TMA in 64-column blocks with 128-byte swizzle through an
+// 8-stage ring of full / empty mbarriers. One lane issues the TMA loads, one lane the MMAs (kind::f16, fp32 accumulate
 // in TMEM): embedding blocks into TMEM columns [0, 96) = r | z | n_in (N = 96), hidden blocks (hi, then lo: the fp32
-// parent state to 2^-16) into [0, 64) = r | z (N = 64) and [96, 128) = n_h (N = 32), which the GRU keeps apart. The
-// four warps of the second warpgroup read the tile back (tcgen05.ld, one row per thread) and finish the GRU step.
+// parent state to 2^-16) into [0, 64) = r | z (N = 64) and [96, 128) = n_h (N = 32), which the GRU keeps apart; each
+// K partial (below) has its own 128 columns. All eight warps read the tile back (tcgen05.ld, one row per thread,
+// warps w and w + 4 on the same TMEM lanes with half of the units each) and finish the GRU step.
 struct TmaMaps {
   CUtensorMap x;    // [rows cap][E + 2H] bf16, box 64 x 128
   CUtensorMap wih;  // [3H][E] bf16, box 64 x 32
@@ -1145,8 +1148,8 @@ extern "C" dt_status dt_build_trees(int B, int K, int V, int M, int n, int max_d
   p.lookahead = k_set > 0 ? (k_set < kLargeLookahead ? k_set : kLargeLookahead)
                           : (B >= 128 ? kLargeLookahead : kLargeDefault);
 
-  // phase A: tensor cores for bf16 weights whose widths are multiples of the pipeline chunk; the larger tile once a
-  // wave can hold 128 expansions or more
+  // phase A: tcgen05 tiles when they fit (below); else mma.sync tiles for bf16 weights whose widths are multiples of
+  // the pipeline chunk (the larger tile once a wave can hold 128 expansions or more); else CUDA cores
   const long long max_rows = static_cast<long long>(B) * p.lookahead;
   // tcgen05 tiles (128 expansions x 32 units) for every bf16 wave whose widths fit them: the K split makes the sums
   // independent of the wave's size, so the tree does not depend on the lookahead width
