@@ -24,6 +24,9 @@
 //                     path scores.
 //   orc_accept_paths - pinned: the longest path, among all root-to-node paths enumerated, whose tokens agree with
 //                     the target's next tokens along it; special cases (all rejected, a whole chain accepted).
+//   orc_lmhead_topm - pinned: numpy's fp64 matmul of the widened inputs followed by a full lexicographic sort; a
+//                     one-hot head whose logits are the hidden values themselves; duplicated head rows (ties go
+//                     to the lower id).
 //   orc_build_trees_marginal - pinned: brute-force enumeration of the depth-limited tree under the product of the
 //                     marginals (log-softmax by torch), and equality with orc_build_trees at W_c = 0.
 //   The GRU gate layout (rows r|z|n, PyTorch convention) and the order "add correction, then divide by T" are
@@ -44,7 +47,7 @@
 
 namespace {
 
-enum { ORC_F32 = 0, ORC_BF16 = 1 };
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_F64 = 2 };  // ORC_F64: the oracle's own fp64 intermediates
 
 enum {
   ORC_OK = 0,
@@ -56,6 +59,7 @@ enum {
 
 // Exact widening of one stored element to double.
 double load(const void* base, int dtype, size_t i) {
+  if (dtype == ORC_F64) return static_cast<const double*>(base)[i];
   if (dtype == ORC_F32) return static_cast<double>(static_cast<const float*>(base)[i]);
   const uint32_t bits = static_cast<uint32_t>(static_cast<const uint16_t*>(base)[i]) << 16;
   float f;
@@ -363,6 +367,35 @@ int orc_topm(const void* logits, int dtype, int B, int K, int V, int M, int32_t*
 #pragma omp parallel for schedule(dynamic) num_threads(threads_or_default(threads))
   for (long long r = 0; r < rows; ++r) {
     const int s = topm_row(logits, dtype, static_cast<size_t>(r) * V, V, M, ids + r * M, vals + r * M);
+    if (s != ORC_OK) {
+#pragma omp critical
+      status = s;
+    }
+  }
+  return status;
+}
+
+// Top-M of the full-vocabulary projection: logits[r][v] = sum_k hidden[r][k] * w_head[v][k] (fp64 from the exactly
+// widened inputs, the plain dot product, no bias), then the M largest of every row with ties to the lower id, as in
+// orc_topm. [S] "Methodology — deep read" and [G] "Composants Clés — Restriction de Candidats": the drafter's base
+// logits come from the costly projection over the whole vocabulary (W2), of which only the top-M are kept.
+// hidden [R,D], w_head [V,D], each fp32 or bf16 (dtype code as for the weights); ids [R,M], vals [R,M].
+int orc_lmhead_topm(int R, int D, int V, int M, const void* hidden, int hdtype, const void* w_head, int wdtype,
+                    int32_t* ids, double* vals, int threads) {
+  if (!hidden || !w_head || !ids || !vals || R < 0 || D < 1 || V < 1 || M < 1 || M > V) return ORC_ERR_ARG;
+  int status = ORC_OK;
+#pragma omp parallel for schedule(dynamic) num_threads(threads_or_default(threads))
+  for (int r = 0; r < R; ++r) {
+    std::vector<double> h(static_cast<size_t>(D));
+    for (int k = 0; k < D; ++k) h[k] = load(hidden, hdtype, static_cast<size_t>(r) * D + k);
+    std::vector<double> logits(static_cast<size_t>(V));
+    for (int v = 0; v < V; ++v) {
+      double acc = 0.0;
+      for (int k = 0; k < D; ++k) acc += h[k] * load(w_head, wdtype, static_cast<size_t>(v) * D + k);
+      logits[v] = acc;
+    }
+    const int s = topm_row(logits.data(), ORC_F64, 0, V, M, ids + static_cast<size_t>(r) * M,
+                           vals + static_cast<size_t>(r) * M);
     if (s != ORC_OK) {
 #pragma omp critical
       status = s;

@@ -51,6 +51,7 @@ _D = ctypes.c_double
 def load(path=None) -> ctypes.CDLL:
     lib = ctypes.CDLL(str(path or build()))
     lib.orc_topm.argtypes = [_P, _I, _I, _I, _I, _I, _P, _P, _I]
+    lib.orc_lmhead_topm.argtypes = [_I, _I, _I, _I, _P, _I, _P, _I, _P, _P, _I]
     lib.orc_gru_step.argtypes = [_I, _I, _I, _P, _P, _P, _P, _P, _P, _P]
     lib.orc_child_logp.argtypes = [_I, _I, _P, _P, _P, _I, _D, _P, _P]
     lib.orc_build_trees.argtypes = [_I, _I, _I, _I, _I, _D, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P,
@@ -106,6 +107,21 @@ def topm(logits: np.ndarray, M: int, threads: int = 0, L=None):
     ids = np.empty((B, K, M), np.int32)
     vals = np.empty((B, K, M), np.float64)
     _check(L.orc_topm(_ptr(logits), _dtype_code(logits), B, K, V, M, _ptr(ids), _ptr(vals), threads))
+    return ids, vals
+
+
+def lmhead_topm(hidden: np.ndarray, w_head: np.ndarray, M: int, threads: int = 0, L=None):
+    """hidden [R,D], w_head [V,D] (fp32, or bf16 bit patterns as uint16) -> ids [R,M] int32, vals [R,M] float64:
+    the top-M of the full-vocabulary projection hidden @ w_head.T."""
+    L = L or lib()
+    R, D = hidden.shape
+    V = w_head.shape[0]
+    hidden = np.ascontiguousarray(hidden)
+    w_head = np.ascontiguousarray(w_head)
+    ids = np.empty((R, M), np.int32)
+    vals = np.empty((R, M), np.float64)
+    _check(L.orc_lmhead_topm(R, D, V, M, _ptr(hidden), _dtype_code(hidden), _ptr(w_head), _dtype_code(w_head),
+                             _ptr(ids), _ptr(vals), threads))
     return ids, vals
 
 

@@ -5,6 +5,8 @@ copies of the oracle) and raises AssertionError (or the oracle's own error) when
 
 What each pin leans on, outside the oracle:
   * top-M             - a full lexicographic sort of every row (numpy lexsort), i.e. brute force;
+  * projection top-M  - numpy's fp64 matmul on exactly representable inputs, then the same full sort; a one-hot
+                        head (closed form);
   * GRU step          - torch.nn.GRUCell in fp64 (library routine);
   * restricted softmax- with M = V it must equal torch.log_softmax over the full-vocabulary corrected row
                         computed with a dense matmul (no gather);
@@ -412,6 +414,41 @@ def pin_rescore(L):
     assert np.max(np.abs(sc[0] - [nodes[p] for p in chosen])) < 1e-12
 
 
+def pin_lmhead_topm(L):
+    """The top-M of the full-vocabulary projection against numpy's fp64 matmul of the widened inputs and a full
+    lexicographic sort. Small-integer inputs make every dot product exact in any summation order, so the ties that
+    the integers produce (and the duplicated head rows) must go to the lower id exactly. Then a one-hot head whose
+    logits are the hidden values themselves, scaled per block of D vocabulary rows (a closed form)."""
+    from oracle import oracle as orc
+    rng = np.random.default_rng(11)
+    R, D, V = 5, 96, 301
+    for dtype in ("f32", "bf16"):
+        h = rng.integers(-8, 9, size=(R, D)).astype(np.float32)
+        w = rng.integers(-8, 9, size=(V, D)).astype(np.float32)
+        w[101] = w[100]                                  # duplicated head rows: equal logits in every row
+        w[250] = w[7]
+        cast = (lambda a: a) if dtype == "f32" else (lambda a: synth.bits_u16(torch.from_numpy(a).to(torch.bfloat16)))
+        hh, ww = cast(h), cast(w)
+        full = widen(hh) @ widen(ww).T
+        for M in (1, 40, V):
+            ids, vals = orc.lmhead_topm(hh, ww, M, L=L)
+            for r in range(R):
+                order = np.lexsort((np.arange(V), -full[r]))[:M]
+                assert np.array_equal(ids[r], order), (dtype, M, r)
+                assert np.array_equal(vals[r], full[r][order]), (dtype, M, r)
+    # one-hot head: row v of the head is 2^(v // D) e_(v mod D), so logit[r][v] = 2^(v // D) h[r][v mod D]
+    D, V = 8, 40
+    h = rng.standard_normal((3, D)).astype(np.float32)
+    w = np.zeros((V, D), np.float32)
+    for v in range(V):
+        w[v, v % D] = 2.0 ** (v // D)
+    ids, vals = orc.lmhead_topm(h, w, V, L=L)
+    expect = np.array([[2.0 ** (v // D) * float(h[r, v % D]) for v in range(V)] for r in range(3)])
+    for r in range(3):
+        order = np.lexsort((np.arange(V), -expect[r]))
+        assert np.array_equal(ids[r], order) and np.array_equal(vals[r], expect[r][order]), r
+
+
 ALL_PINS = [pin_topm_bruteforce, pin_gru_vs_grucell, pin_full_vocab_softmax, pin_golden, pin_special_cases,
             pin_factorised_closed_form, pin_bruteforce_tree, pin_invariants, pin_rescore, pin_marginal_builder,
-            pin_accept_paths]
+            pin_accept_paths, pin_lmhead_topm]

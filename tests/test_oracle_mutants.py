@@ -38,6 +38,12 @@ MUTANTS = {
     "accept-target-index-off-by-one": ("want = target_next[1 + next];", "want = target_next[next];"),
     "accept-root-token-skipped": ("int cur = -1, len = 0, want = target_next[0];",
                                   "int cur = -1, len = 0, want = target_next[1];"),
+    "lmhead-drops-last-term": ("for (int k = 0; k < D; ++k) acc += h[k] * load(w_head,",
+                               "for (int k = 0; k + 1 < D; ++k) acc += h[k] * load(w_head,"),
+    "lmhead-head-transposed": ("load(w_head, wdtype, static_cast<size_t>(v) * D + k)",
+                               "load(w_head, wdtype, (static_cast<size_t>(k) * V + v) % (static_cast<size_t>(V) * D))"),
+    "lmhead-hidden-row-0": ("h[k] = load(hidden, hdtype, static_cast<size_t>(r) * D + k);",
+                            "h[k] = load(hidden, hdtype, static_cast<size_t>(k));"),
     "embedding-of-parent": ("load(w.emb, w.dtype, static_cast<size_t>(u.token) * E + e)",
                             "load(w.emb, w.dtype, static_cast<size_t>(u.parent < 0 ? u.token : tokens[u.parent]) * E + e)"),
 }
