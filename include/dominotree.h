@@ -170,6 +170,31 @@ dt_status dt_accept_paths(int B, int n, const int32_t* tokens, const int32_t* pa
                           int32_t* out_accept_len, int32_t* out_path, int32_t* out_bonus, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------------------------------------------
+ * dt_lmhead_topm — the drafter's full-vocabulary projection fused with its top-M: the logits are never written.
+ * Source: blog.captcha.la, "Methodology — deep read" (the costly full-vocabulary projection, of which the per-node
+ * work keeps only the M highest-marginal tokens); gist.science, "Composants Clés — Restriction de Candidats"
+ * (re-running the projection W2 over the whole vocabulary is the cost that the top-M restriction avoids).
+ *
+ * Semantics: for every row r < R, logits[r][v] = sum_k hidden[r][k] * w_head[v][k] (no bias), computed on the tensor
+ * cores as bf16 products accumulated in fp32; out_ids[r] / out_vals[r] are the M largest of those fp32 logits in
+ * descending order, ties to the lower id (as dt_topm over the logits, exactly those the kernel computed).
+ *   hidden       [R,D] bf16, row-major (the backbone's hidden state of each (request, block position) row).
+ *   w_head       [V,D] bf16, row-major (the LM head W2, one row per vocabulary entry).
+ *   out_ids      [R,M] int32; out_vals [R,M] fp32.
+ *   workspace    dt_lmhead_workspace_bytes(R,D,V,M) bytes (on the current device), header initialised by
+ *                dt_workspace_init; the status word reports DT_ERR_NUMERIC for a NaN logit and DT_ERR_TIMEOUT if a
+ *                grid-barrier or copy wait ran out (dt_get_error).
+ * One persistent cooperative launch, one CTA per SM, each CTA's slice of the logits held in tensor memory; the
+ * supported envelope: dtype DT_BF16, D a multiple of 64, R <= 64, M <= DT_MAX_M, and ceil(ceil(V/128)/SMs) * R
+ * (R rounded up to 16) <= 512 (V = 151936 on 152 SMs: R <= 64). Outside it: DT_ERR_UNSUPPORTED, before any launch.
+ * Pointers must be 16-byte aligned device pointers; argument errors return DT_ERR_INVALID_ARG before any launch.
+ * ------------------------------------------------------------------------------------------------------------- */
+size_t dt_lmhead_workspace_bytes(int R, int D, int V, int M);
+dt_status dt_lmhead_topm(int R, int D, int V, int M, const void* hidden, const void* w_head, dt_dtype dtype,
+                         int32_t* out_ids, float* out_vals, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------------------------------------
  * dt_topm_static — dt_topm for callers that cannot allocate device memory.
  * No counterpart in the paper: this is a deployment variant of dt_topm, with the same arguments minus the
  * workspace and bit-identical results.

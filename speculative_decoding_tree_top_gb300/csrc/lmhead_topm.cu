@@ -1,0 +1,334 @@
+// dt_lmhead_topm — the drafter's full-vocabulary projection and its top-M in one launch, the logits never written.
+//
+// Method: blog.captcha.la, "Methodology — deep read" (the costly full-vocabulary projection; the per-node work only
+// sees the M highest-marginal tokens of each depth); gist.science, "Composants Clés — Restriction de Candidats"
+// (re-running the projection W2 over the whole vocabulary is what the top-M restriction avoids). The marginal
+// logits of a row are hidden_r . W2^T (no bias), of which the M largest are kept, ties to the lower id.
+//
+// GB300 design: one persistent cooperative launch, one CTA per SM, logits kept in tensor memory.
+//   * GEMM on tcgen05: CTA c owns vocabulary tiles c, c + G, ... (128 head rows each, at most 512 / Rp of them);
+//     the head rows are the MMA's M side, the R hidden rows (padded to Rp, a multiple of 16) its N side. Both
+//     operands arrive by 2-D TMA (128-byte swizzle, 64-column K blocks) through an 8-stage mbarrier ring; one lane
+//     issues TMA, one lane the MMAs; tile i accumulates in TMEM columns [i Rp, (i + 1) Rp), so the CTA's whole slice
+//     of logits stays on chip. The head is read once from HBM: at small R the launch is an HBM stream of V x D bf16.
+//   * Bound: per row, every warp quarter (32 TMEM lanes: 32 head rows of every tile) offers its two largest logits
+//     to a pool in the workspace; after a grid barrier every CTA takes the M-th largest of the row's pool (G x 8
+//     values, a subset of the row's logits, so a lower bound of its M-th largest logit, and tight because the row's
+//     top M are spread over many quarters).
+//   * Filter: every logit at or above its row's bound is appended, as a 64-bit row word (value key, inverted id),
+//     to the CTA's list for the row (room for all of the CTA's values: exact whatever the data).
+//   * Grid barrier; then CTA r selects row r from the G lists (the selection shared with dt_topm).
+// Every comparison is on integer words, so the result is deterministic and exact for the logits as computed (fp32
+// accumulation of bf16 products in the tensor cores).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+
+#include "dt_internal.cuh"
+#include "topm_select.cuh"
+#include "umma.cuh"
+
+namespace dt {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kTileV = 128;           // head rows per tile (the MMA's M)
+constexpr int kBK = 64;               // K block: 64 bf16 = one 128-byte swizzle row
+constexpr int kStages = 8;
+constexpr int kMaxRp = 64;            // padded hidden rows (the MMA's N): a multiple of 16
+constexpr int kTmemMax = 512;
+constexpr int kPoolPerQuarter = 2;    // logits a warp quarter offers per row
+constexpr int kPoolPerCta = 4 * kPoolPerQuarter;
+constexpr uint64_t kBudgetNs = 4000000000ull;  // copies and MMAs take microseconds: this stops a lost one
+
+struct LhParams {
+  int R, Rp, D, V, M, tiles, tpc, G, cap;
+  uint32_t* pool;   // [Rp][G * kPoolPerCta] value keys (0: none)
+  uint64_t* cand;   // [R][G][cap] row words
+  int* counts;      // [R][G]
+  int32_t* ids;     // [R][M]
+  float* vals;      // [R][M]
+  WsHeader* hdr;
+  uint64_t timeout_ns;
+};
+struct LhMaps {
+  CUtensorMap w;    // head [V][D] bf16, box 64 x 128
+  CUtensorMap h;    // hidden [R][D] bf16, box 64 x Rp
+};
+
+__host__ __device__ inline size_t lh_stage_bytes(int Rp) {
+  return static_cast<size_t>(kTileV) * kBK * 2 + static_cast<size_t>(Rp) * kBK * 2;
+}
+__host__ __device__ inline size_t lh_smem_bytes(int Rp) {
+  const size_t ring = kStages * lh_stage_bytes(Rp);
+  return 1024 + (ring > sizeof(SelectSmem) ? ring : sizeof(SelectSmem));
+}
+
+// Sixteen consecutive TMEM columns of this warp's 32 lanes, and the wait for them, in one statement.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1) lmhead_topm_kernel(LhParams p, const __grid_constant__ LhMaps maps) {
+  extern __shared__ float4 smem_f4[];
+  unsigned char* base =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_f4) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t full[kStages], empty[kStages], done;
+  __shared__ uint32_t s_tmem;
+  __shared__ uint32_t s_bound[kMaxRp];
+  __shared__ int s_cnt[kMaxRp];
+  __shared__ int s_flag, s_warp[kThreads / 32], s_n;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int G = static_cast<int>(gridDim.x), bid = static_cast<int>(blockIdx.x);
+  const int R = p.R, Rp = p.Rp, nkb = p.D / kBK;
+  const int my_tiles = bid < p.tiles ? (p.tiles - 1 - bid) / G + 1 : 0;
+  const uint32_t cols = static_cast<uint32_t>(p.tpc * Rp) <= 32u ? 32u
+                        : static_cast<uint32_t>(p.tpc * Rp) <= 64u ? 64u
+                        : static_cast<uint32_t>(p.tpc * Rp) <= 128u ? 128u
+                        : static_cast<uint32_t>(p.tpc * Rp) <= 256u ? 256u : 512u;
+  if (t == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(&done, 1);
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                 "r"(cols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = s_tmem;
+  const size_t stage = lh_stage_bytes(Rp);
+  const uint32_t tx = static_cast<uint32_t>(stage);
+  bool ok = true;
+
+  // ---- GEMM: tile i of this CTA (vocabulary rows (bid + i G) * 128 ...) into TMEM columns [i Rp, (i + 1) Rp) ----
+  if (warp == 0 && lane == 0) {  // TMA producer
+    for (int i = 0; i < my_tiles && ok; ++i) {
+      const int tile = bid + i * G;
+      for (int kb = 0; kb < nkb; ++kb) {
+        const unsigned n = static_cast<unsigned>(i * nkb + kb), st = n % kStages, use = n / kStages;
+        if (use > 0) ok = mbar_wait(&empty[st], (use - 1) & 1u, kBudgetNs);
+        if (!ok) break;
+        unsigned char* a = base + st * stage;
+        mbar_expect_tx(&full[st], tx);
+        tma_load_2d(a, &maps.w, kb * kBK, tile * kTileV, &full[st]);
+        tma_load_2d(a + kTileV * kBK * 2, &maps.h, kb * kBK, 0, &full[st]);
+      }
+    }
+  } else if (warp == 1 && lane == 0) {  // MMA issuer
+    const uint32_t idesc = umma_idesc(Rp, kTileV);
+    for (int i = 0; i < my_tiles && ok; ++i) {
+      for (int kb = 0; kb < nkb; ++kb) {
+        const unsigned n = static_cast<unsigned>(i * nkb + kb), st = n % kStages, use = n / kStages;
+        ok = mbar_wait(&full[st], use & 1u, kBudgetNs);
+        if (!ok) break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t a = smem_u32(base + st * stage), b = a + kTileV * kBK * 2;
+#pragma unroll
+        for (int k = 0; k < kBK / 16; ++k)
+          umma_f16(tmem + static_cast<uint32_t>(i * Rp), umma_desc_sw128(a + 32 * k), umma_desc_sw128(b + 32 * k),
+                   idesc, (kb > 0 || k > 0) ? 1u : 0u);
+        umma_commit(&empty[st]);  // the stage is free once these MMAs have read it
+      }
+    }
+    if (ok && my_tiles > 0) umma_commit(&done);  // every accumulator is complete after the last MMAs
+  }
+  ok = __syncthreads_and(ok);
+  if (ok && my_tiles > 0) ok = mbar_wait(&done, 0u, kBudgetNs);
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  ok = __syncthreads_and(ok);
+
+  // Warps w and w + 4 read TMEM lanes 32 (w % 4) .. + 31 (head row 32 (w % 4) + lane of every tile) and split the
+  // row groups of 16 columns between them.
+  const int q = warp & 3, half = warp >> 2;
+  const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16);
+  const int np = G * kPoolPerCta;
+  bool nan = false;
+  if (ok) {
+    // ---- pool: every quarter's two largest logits of each row ----
+    for (int g = half; g < Rp / 16; g += 2) {
+      uint32_t b1[16], b2[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) b1[j] = b2[j] = 0u;
+      for (int i = 0; i < my_tiles; ++i) {
+        uint32_t v[16];
+        tmem_ld16(tq + static_cast<uint32_t>(i * Rp + 16 * g), v);
+        const bool valid = (bid + i * G) * kTileV + 32 * q + lane < p.V;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const bool isnan = (v[j] & 0x7FFFFFFFu) > 0x7F800000u;
+          nan |= valid && isnan && 16 * g + j < R;
+          const uint32_t k = valid && !isnan ? key_of_f32(v[j]) : 0u;
+          if (k > b1[j]) {
+            b2[j] = b1[j];
+            b1[j] = k;
+          } else if (k > b2[j]) {
+            b2[j] = k;
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t m1 = __reduce_max_sync(0xFFFFFFFFu, b1[j]);
+        const int win = __ffs(__ballot_sync(0xFFFFFFFFu, b1[j] == m1)) - 1;
+        const uint32_t m2 = __reduce_max_sync(0xFFFFFFFFu, lane == win ? b2[j] : b1[j]);
+        if (lane == 0) {
+          uint32_t* pr = p.pool + static_cast<size_t>(16 * g + j) * np + bid * kPoolPerCta + q * kPoolPerQuarter;
+          pr[0] = m1;
+          pr[1] = m2;
+        }
+      }
+    }
+  }
+  if (__syncthreads_or(nan) && t == 0) record_error(p.hdr, DT_ERR_NUMERIC);
+  if (ok) ok = grid_barrier(p.hdr, static_cast<unsigned>(G), p.timeout_ns, &s_flag);
+
+  if (ok) {
+    // ---- bound: the M-th largest key of each row's pool (0: fewer than M values, take every logit) ----
+    uint32_t* pk = reinterpret_cast<uint32_t*>(base) + static_cast<size_t>(warp) * np;  // this warp's copy
+    for (int r = warp; r < R; r += kThreads / 32) {
+      const uint32_t* pr = p.pool + static_cast<size_t>(r) * np;
+      for (int i = lane; i < np; i += 32) pk[i] = __ldcg(pr + i);
+      __syncwarp();
+      uint32_t th = 0;
+      if (np >= p.M) {
+        for (int bit = 31; bit >= 0; --bit) {
+          const uint32_t c = th | (1u << bit);
+          int cnt = 0;
+          for (int i = lane; i < np; i += 32) cnt += pk[i] >= c;
+          if (__reduce_add_sync(0xFFFFFFFFu, cnt) >= p.M) th = c;
+        }
+      }
+      if (lane == 0) s_bound[r] = th;
+      __syncwarp();
+    }
+    for (int r = t; r < R; r += kThreads) s_cnt[r] = 0;
+    __syncthreads();
+    // ---- filter: the logits at or above their row's bound, as row words, into this CTA's list of the row ----
+    for (int g = half; g < Rp / 16; g += 2) {
+      for (int i = 0; i < my_tiles; ++i) {
+        uint32_t v[16];
+        tmem_ld16(tq + static_cast<uint32_t>(i * Rp + 16 * g), v);
+        const int vid = (bid + i * G) * kTileV + 32 * q + lane;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int r = 16 * g + j;
+          const bool isnan = (v[j] & 0x7FFFFFFFu) > 0x7F800000u;
+          if (vid < p.V && r < R && !isnan) {
+            const uint32_t k = key_of_f32(v[j]);
+            if (k >= s_bound[r]) {
+              const int pos = atomicAdd(&s_cnt[r], 1);  // < cap: the CTA holds at most cap logits of a row
+              p.cand[(static_cast<size_t>(r) * G + bid) * p.cap + pos] = pack_candidate(k, static_cast<uint32_t>(vid));
+            }
+          }
+        }
+      }
+    }
+    __syncthreads();
+    for (int r = t; r < R; r += kThreads) p.counts[static_cast<size_t>(r) * G + bid] = s_cnt[r];
+    ok = grid_barrier(p.hdr, static_cast<unsigned>(G), p.timeout_ns, &s_flag);
+  }
+
+  if (ok) {
+    // ---- selection: CTA r takes row r from the G lists ----
+    SelectSmem& S = *reinterpret_cast<SelectSmem*>(base);
+    for (int r = bid; r < R; r += G) {
+      const uint64_t* rc = p.cand + static_cast<size_t>(r) * G * p.cap;
+      const int cap = p.cap;
+      select_words<false>(
+          p.counts + static_cast<size_t>(r) * G, G, p.M,
+          [&](int c, int i) { return __ldcg(rc + static_cast<size_t>(c) * cap + i); },
+          p.ids + static_cast<size_t>(r) * p.M, p.vals + static_cast<size_t>(r) * p.M, S, s_warp, &s_n);
+      __syncthreads();
+    }
+  } else if (t == 0) {
+    record_error(p.hdr, DT_ERR_TIMEOUT);
+    atomicExch(&p.hdr->abort, 1u);
+  }
+
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(cols) : "memory");
+}
+
+struct LhLayout {
+  size_t pool, counts, cand, bytes;
+  int Rp, tiles, tpc, cap;
+};
+inline LhLayout lh_layout(int R, int V, int G) {
+  LhLayout L{};
+  L.Rp = (R + 15) / 16 * 16;
+  L.tiles = (V + kTileV - 1) / kTileV;
+  L.tpc = (L.tiles + G - 1) / G;
+  L.cap = L.tpc * kTileV;
+  L.pool = align_up(sizeof(WsHeader));
+  L.counts = align_up(L.pool + sizeof(uint32_t) * static_cast<size_t>(L.Rp) * G * kPoolPerCta);
+  L.cand = align_up(L.counts + sizeof(int) * static_cast<size_t>(R) * G);
+  L.bytes = align_up(L.cand + sizeof(uint64_t) * static_cast<size_t>(R) * G * L.cap);
+  return L;
+}
+
+}  // namespace
+}  // namespace dt
+
+extern "C" size_t dt_lmhead_workspace_bytes(int R, int D, int V, int M) {
+  if (R < 1 || D < 1 || V < 1 || M < 1) return 0;
+  dt::DeviceInfo di{};
+  if (dt::current_device_info(&di) != cudaSuccess) return 0;
+  return dt::lh_layout(R, V, di.sms).bytes;
+}
+
+extern "C" dt_status dt_lmhead_topm(int R, int D, int V, int M, const void* hidden, const void* w_head, dt_dtype dtype,
+                                    int32_t* out_ids, float* out_vals, void* workspace, size_t workspace_bytes,
+                                    cudaStream_t stream) {
+  using namespace dt;
+  if (R < 0 || D < 1 || V < 1 || M < 1 || M > V) return DT_ERR_INVALID_ARG;
+  if (dtype != DT_F32 && dtype != DT_BF16) return DT_ERR_INVALID_ARG;
+  if (R == 0) return DT_OK;
+  const void* ptrs[] = {hidden, w_head, out_ids, out_vals, workspace};
+  for (const void* q : ptrs)
+    if (!q || !aligned16(q)) return DT_ERR_INVALID_ARG;
+  if (dtype != DT_BF16 || D % kBK != 0 || M > DT_MAX_M || R > kMaxRp) return DT_ERR_UNSUPPORTED;
+  if (static_cast<long long>(V) + kTileV > INT_MAX) return DT_ERR_UNSUPPORTED;
+  DeviceInfo di{};
+  if (current_device_info(&di) != cudaSuccess) return DT_ERR_CUDA;
+  const LhLayout L = lh_layout(R, V, di.sms);
+  if (workspace_bytes < L.bytes) return DT_ERR_INVALID_ARG;
+  if (L.tpc * L.Rp > kTmemMax) return DT_ERR_UNSUPPORTED;  // the CTA's slice of logits must fit its tensor memory
+  const size_t smem = lh_smem_bytes(L.Rp);
+  if (smem + 2048 > static_cast<size_t>(di.optin)) return DT_ERR_UNSUPPORTED;
+  LhMaps maps{};
+  if (!encode_bf16_2d(&maps.w, w_head, static_cast<uint64_t>(D), static_cast<uint64_t>(V), static_cast<uint64_t>(D),
+                      kBK, kTileV) ||
+      !encode_bf16_2d(&maps.h, hidden, static_cast<uint64_t>(D), static_cast<uint64_t>(R), static_cast<uint64_t>(D),
+                      kBK, static_cast<uint32_t>(L.Rp)))
+    return DT_ERR_CUDA;
+  char* ws = static_cast<char*>(workspace);
+  LhParams p{};
+  p.R = R; p.Rp = L.Rp; p.D = D; p.V = V; p.M = M; p.tiles = L.tiles; p.tpc = L.tpc; p.G = di.sms; p.cap = L.cap;
+  p.pool = reinterpret_cast<uint32_t*>(ws + L.pool);
+  p.counts = reinterpret_cast<int*>(ws + L.counts);
+  p.cand = reinterpret_cast<uint64_t*>(ws + L.cand);
+  p.ids = out_ids;
+  p.vals = out_vals;
+  p.hdr = reinterpret_cast<WsHeader*>(ws);
+  p.timeout_ns = barrier_timeout_ns();
+  const void* fn = reinterpret_cast<const void*>(lmhead_topm_kernel);
+  if (ensure_dynamic_smem(fn, smem) != cudaSuccess) return DT_ERR_CUDA;
+  void* args[] = {&p, &maps};
+  return cuda_status(cudaLaunchCooperativeKernel(fn, dim3(static_cast<unsigned>(di.sms)), dim3(kThreads), args, smem,
+                                                 stream));
+}

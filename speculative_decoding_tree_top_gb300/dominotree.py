@@ -56,6 +56,8 @@ SIGNATURES = {
     "dt_accept_paths": (_I, [_I, _I, _P, _P, _P, _P, _P, _P, _P]),
     "dt_build_trees_marginal": (_I, [_I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
                                      _P]),
+    "dt_lmhead_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
+    "dt_lmhead_topm": (_I, [_I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _SZ, _P]),
     "dt_get_error": (_I, [_P, _P]),
     "dt_set_barrier_timeout_ns": (None, [ctypes.c_uint64]),
     "dt_set_lookahead": (_I, [_I]),
@@ -159,6 +161,31 @@ def dt_topm(logits: torch.Tensor, M: int, out_ids: Optional[torch.Tensor] = None
                          _dev(out_ids, "out_ids", torch.int32, (B, K, M)),
                          _dev(out_vals, "out_vals", torch.float32, (B, K, M)),
                          _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream)), "dt_topm")
+    return out_ids, out_vals
+
+
+def dt_lmhead_workspace_bytes(R: int, D: int, V: int, M: int) -> int:
+    return int(lib().dt_lmhead_workspace_bytes(R, D, V, M))
+
+
+def dt_lmhead_topm(hidden: torch.Tensor, w_head: torch.Tensor, M: int, out_ids: Optional[torch.Tensor] = None,
+                   out_vals: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None, stream=None):
+    """Top-M of the full-vocabulary projection hidden [R,D] . w_head [V,D]^T, fused (the logits are never written)
+    -> (ids [R,M] int32, vals [R,M] fp32)."""
+    R, D = hidden.shape
+    V = w_head.shape[0]
+    if out_ids is None:
+        out_ids = torch.empty((R, M), dtype=torch.int32, device=hidden.device)
+    if out_vals is None:
+        out_vals = torch.empty((R, M), dtype=torch.float32, device=hidden.device)
+    if workspace is None:
+        workspace = new_workspace(dt_lmhead_workspace_bytes(R, D, V, M), hidden.device)
+    _check(lib().dt_lmhead_topm(R, D, V, M, _dev(hidden, "hidden", hidden.dtype, (R, D)),
+                                _dev(w_head, "w_head", hidden.dtype, (V, D)), _code(hidden.dtype),
+                                _dev(out_ids, "out_ids", torch.int32, (R, M)),
+                                _dev(out_vals, "out_vals", torch.float32, (R, M)),
+                                _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream)),
+           "dt_lmhead_topm")
     return out_ids, out_vals
 
 

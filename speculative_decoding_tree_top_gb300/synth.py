@@ -43,7 +43,7 @@ CONFIGS: Dict[int, dict] = {
 }
 
 STREAM = {"logits": 1, "boost_ids": 2, "boost_vals": 3, "h0": 4, "w_ih": 5, "w_hh": 6, "b_ih": 7, "b_hh": 8,
-          "emb": 9, "w_c": 10}
+          "emb": 9, "w_c": 10, "lmhead_hidden": 11, "lmhead_w": 12}
 
 
 @dataclass
@@ -218,3 +218,12 @@ def make_target_next(tokens, parents, V: int, p_agree: float, seed: int = 99):
             if kids[j] and rng.random() < p_agree:
                 out[b, j] = kids[j][int(rng.integers(0, len(kids[j])))]
     return out.astype(np.int32)
+
+
+def make_lmhead_inputs(R: int, D: int, V: int, device="cpu", seed: int = 4321):
+    """The fused projection's inputs: the backbone hidden states of R (request, block position) rows, N(0, 1), and
+    an LM head of V rows, N(0, 1/sqrt(D)) (so the logits are about N(0, 1)); both drawn in fp32 from one seeded
+    CPU generator, then rounded to bf16, which is the input of both the GPU path and the oracle."""
+    hidden = _normal((R, D), 1.0, "cpu", seed, "lmhead_hidden").to(torch.bfloat16)
+    w_head = _normal((V, D), 1.0 / math.sqrt(D), "cpu", seed, "lmhead_w").to(torch.bfloat16)
+    return hidden.to(device), w_head.to(device)

@@ -152,3 +152,23 @@ def test_accept_rejects_bad_arguments(dtlib):
     assert f(1, 4, None, A, A, A, A, A, None) == INVALID
     assert f(1, 2000, A, A, A, A, A, A, None) == UNSUPPORTED
     assert f(0, 4, A, A, A, A, A, A, None) == OK
+
+
+def test_lmhead_rejects_bad_arguments(dtlib):
+    f = dtlib.lib().dt_lmhead_topm
+    BF16, F32 = 1, 0
+
+    def call(R=16, D=128, V=1000, M=8, dtype=BF16, h=A, w=A, ids=A, vals=A, ws=A):
+        return f(R, D, V, M, h, w, dtype, ids, vals, ws, 1 << 30, None)
+    assert call(M=0) == INVALID
+    assert call(M=1001) == INVALID                    # more candidates than vocabulary
+    assert call(R=-1) == INVALID
+    assert call(D=0) == INVALID
+    assert call(dtype=7) == INVALID
+    assert call(h=None) == INVALID
+    assert call(w=A + 8) == INVALID                   # misaligned
+    assert call(dtype=F32) == UNSUPPORTED             # the tensor-core path takes bf16
+    assert call(D=96) == UNSUPPORTED                  # K blocks of 64
+    assert call(R=65) == UNSUPPORTED                  # the rows must fit the tensor-memory slice
+    assert call(M=2000, V=5000) == UNSUPPORTED
+    assert call(R=0) == OK
