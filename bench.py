@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--with-accept", action="store_true",
                     help="also time dt_accept_paths on the round's trees (synthetic target tokens), reported apart")
+    ap.add_argument("--with-lmhead", action="store_true",
+                    help="also time dt_lmhead_topm (the projection fused with the top-M) against cuBLAS + dt_topm")
     ap.add_argument("--builder", choices=["conditional", "marginal"], default="conditional",
                     help="conditional: dt_build_trees (the method); marginal: dt_build_trees_marginal (DDTree scoring)")
     ap.add_argument("--reference-budget", type=float, default=150.0, help="seconds for the whole reference arm")
@@ -306,6 +308,59 @@ def run_ours(args, world, rank, local):
         kernels["dt_accept_paths"] = dict(us=float(acc_ms.mean() * 1e3), bytes=s.B * s.n * 8 + s.B * (s.n + 1) * 4,
                                           mean_accept_len=float(acc_out["accept_len"].float().mean().item()),
                                           sources=["accept.cu"])
+
+    if args.with_lmhead and s.B * s.K <= 64 and s.dtype == "bf16":
+        # The drafter's projection of the R = B*K backbone hidden states (width E) onto the vocabulary, fused with
+        # its top-M, against the unfused path: the cuBLAS GEMM writes the logits, dt_topm reads them back.
+        R = s.B * s.K
+        hid, head = (t.to(dev) for t in synth.make_lmhead_inputs(R, s.E, s.V, seed=777 + rank))
+        lws = dt.new_workspace(dt.dt_lmhead_workspace_bytes(R, s.E, s.V, s.M), dev)
+        l_ids = torch.empty((R, s.M), dtype=torch.int32, device=dev)
+        l_vals = torch.empty((R, s.M), dtype=torch.float32, device=dev)
+        u_logits = torch.empty((1, R, s.V), dtype=torch.bfloat16, device=dev)
+        u_ids = torch.empty((1, R, s.M), dtype=torch.int32, device=dev)
+        u_vals = torch.empty((1, R, s.M), dtype=torch.float32, device=dev)
+        tws = dt.new_workspace(dt.dt_topm_workspace_bytes(1, R, s.V, s.M), dev)
+
+        def fused():
+            dt.dt_lmhead_topm(hid, head, s.M, l_ids, l_vals, lws, stream)
+
+        def unfused(ev=None):
+            torch.matmul(hid, head.t(), out=u_logits[0])
+            if ev is not None:
+                ev.record(stream)
+            dt.dt_topm(u_logits, s.M, u_ids, u_vals, tws, stream)
+
+        for _ in range(args.warmup):
+            fused()
+            unfused()
+        steps = max(20, min(args.steps, 200))
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+        torch.cuda.synchronize()
+        for e in ev:
+            flush_l2()
+            e[0].record(stream)
+            fused()
+            e[1].record(stream)
+            flush_l2()
+            e[2].record(stream)
+            unfused(e[3])
+            e[4].record(stream)
+        torch.cuda.synchronize()
+        f_us = np.array([e[0].elapsed_time(e[1]) for e in ev]) * 1e3
+        g_us = np.array([e[2].elapsed_time(e[3]) for e in ev]) * 1e3
+        t_us = np.array([e[3].elapsed_time(e[4]) for e in ev]) * 1e3
+        lbytes = s.V * s.E * 2 + R * s.E * 2 + R * s.M * 8
+        # the unfused logits are rounded to bf16 by the GEMM, the fused ones stay fp32: near-ties may differ
+        a, b = l_ids.cpu().numpy(), u_ids[0].cpu().numpy()
+        common = float(np.mean([len(set(a[r]) & set(b[r])) / s.M for r in range(R)]))
+        kernels["dt_lmhead_topm"] = dict(
+            us=float(f_us.mean()), bytes=lbytes, gbps=lbytes / (f_us.mean() * 1e3),
+            frac_of_hbm_peak=round(lbytes / (f_us.mean() * 1e3) / peak, 4),
+            tflops=2.0 * R * s.E * s.V / (f_us.mean() * 1e6), rows=R, width=s.E,
+            unfused_us=dict(cublas_projection=float(g_us.mean()), dt_topm=float(t_us.mean()),
+                            total=float((g_us + t_us).mean())),
+            ids_shared_with_unfused=round(common, 4), sources=["lmhead_topm.cu", "topm_select.cuh", "umma.cuh"])
 
     e2e = None
     if not args.no_e2e and not marginal:

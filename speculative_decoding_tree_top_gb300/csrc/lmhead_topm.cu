@@ -35,7 +35,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kTileV = 128;           // head rows per tile (the MMA's M)
 constexpr int kBK = 64;               // K block: 64 bf16 = one 128-byte swizzle row
-constexpr int kStages = 8;
+constexpr int kMaxStages = 12;
 constexpr int kMaxRp = 64;            // padded hidden rows (the MMA's N): a multiple of 16
 constexpr int kTmemMax = 512;
 constexpr int kPoolPerQuarter = 2;    // logits a warp quarter offers per row
@@ -44,6 +44,7 @@ constexpr uint64_t kBudgetNs = 4000000000ull;  // copies and MMAs take microseco
 
 struct LhParams {
   int R, Rp, D, V, M, tiles, tpc, G, cap;
+  int stages, kbps;  // ring stages, and K blocks per stage (a divisor of D / 64)
   uint32_t* pool;   // [Rp][G * kPoolPerCta] value keys (0: none)
   uint64_t* cand;   // [R][G][cap] row words
   int* counts;      // [R][G]
@@ -57,11 +58,12 @@ struct LhMaps {
   CUtensorMap h;    // hidden [R][D] bf16, box 64 x Rp
 };
 
-__host__ __device__ inline size_t lh_stage_bytes(int Rp) {
+// One K block of a stage: the head tile's 128 rows x 64 columns, then the hidden rows' Rp x 64 (both 1 KB-aligned).
+__host__ __device__ inline size_t lh_block_bytes(int Rp) {
   return static_cast<size_t>(kTileV) * kBK * 2 + static_cast<size_t>(Rp) * kBK * 2;
 }
-__host__ __device__ inline size_t lh_smem_bytes(int Rp) {
-  const size_t ring = kStages * lh_stage_bytes(Rp);
+__host__ __device__ inline size_t lh_smem_bytes(int Rp, int stages, int kbps) {
+  const size_t ring = static_cast<size_t>(stages) * kbps * lh_block_bytes(Rp);
   return 1024 + (ring > sizeof(SelectSmem) ? ring : sizeof(SelectSmem));
 }
 
@@ -80,21 +82,21 @@ __global__ void __launch_bounds__(kThreads, 1) lmhead_topm_kernel(LhParams p, co
   extern __shared__ float4 smem_f4[];
   unsigned char* base =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_f4) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t full[kStages], empty[kStages], done;
+  __shared__ uint64_t full[kMaxStages], empty[kMaxStages], done;
   __shared__ uint32_t s_tmem;
   __shared__ uint32_t s_bound[kMaxRp];
   __shared__ int s_cnt[kMaxRp];
   __shared__ int s_flag, s_warp[kThreads / 32], s_n;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int G = static_cast<int>(gridDim.x), bid = static_cast<int>(blockIdx.x);
-  const int R = p.R, Rp = p.Rp, nkb = p.D / kBK;
+  const int R = p.R, Rp = p.Rp, nst = p.D / kBK / p.kbps, S = p.stages, kbps = p.kbps;
   const int my_tiles = bid < p.tiles ? (p.tiles - 1 - bid) / G + 1 : 0;
   const uint32_t cols = static_cast<uint32_t>(p.tpc * Rp) <= 32u ? 32u
                         : static_cast<uint32_t>(p.tpc * Rp) <= 64u ? 64u
                         : static_cast<uint32_t>(p.tpc * Rp) <= 128u ? 128u
                         : static_cast<uint32_t>(p.tpc * Rp) <= 256u ? 256u : 512u;
   if (t == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kMaxStages; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
@@ -110,37 +112,42 @@ __global__ void __launch_bounds__(kThreads, 1) lmhead_topm_kernel(LhParams p, co
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = s_tmem;
-  const size_t stage = lh_stage_bytes(Rp);
+  const size_t blk = lh_block_bytes(Rp), stage = blk * kbps;
   const uint32_t tx = static_cast<uint32_t>(stage);
   bool ok = true;
 
   // ---- GEMM: tile i of this CTA (vocabulary rows (bid + i G) * 128 ...) into TMEM columns [i Rp, (i + 1) Rp) ----
-  if (warp == 0 && lane == 0) {  // TMA producer
+  if (warp == 0 && lane == 0) {  // TMA producer: stage s of tile i holds K blocks [s kbps, (s + 1) kbps)
     for (int i = 0; i < my_tiles && ok; ++i) {
       const int tile = bid + i * G;
-      for (int kb = 0; kb < nkb; ++kb) {
-        const unsigned n = static_cast<unsigned>(i * nkb + kb), st = n % kStages, use = n / kStages;
+      for (int sk = 0; sk < nst; ++sk) {
+        const unsigned n = static_cast<unsigned>(i * nst + sk), st = n % S, use = n / S;
         if (use > 0) ok = mbar_wait(&empty[st], (use - 1) & 1u, kBudgetNs);
         if (!ok) break;
         unsigned char* a = base + st * stage;
         mbar_expect_tx(&full[st], tx);
-        tma_load_2d(a, &maps.w, kb * kBK, tile * kTileV, &full[st]);
-        tma_load_2d(a + kTileV * kBK * 2, &maps.h, kb * kBK, 0, &full[st]);
+        for (int j = 0; j < kbps; ++j) {
+          const int kb = sk * kbps + j;
+          tma_load_2d(a + j * blk, &maps.w, kb * kBK, tile * kTileV, &full[st]);
+          tma_load_2d(a + j * blk + kTileV * kBK * 2, &maps.h, kb * kBK, 0, &full[st]);
+        }
       }
     }
   } else if (warp == 1 && lane == 0) {  // MMA issuer
     const uint32_t idesc = umma_idesc(Rp, kTileV);
     for (int i = 0; i < my_tiles && ok; ++i) {
-      for (int kb = 0; kb < nkb; ++kb) {
-        const unsigned n = static_cast<unsigned>(i * nkb + kb), st = n % kStages, use = n / kStages;
+      for (int sk = 0; sk < nst; ++sk) {
+        const unsigned n = static_cast<unsigned>(i * nst + sk), st = n % S, use = n / S;
         ok = mbar_wait(&full[st], use & 1u, kBudgetNs);
         if (!ok) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t a = smem_u32(base + st * stage), b = a + kTileV * kBK * 2;
+        for (int j = 0; j < kbps; ++j) {
+          const uint32_t a = smem_u32(base + st * stage + j * blk), b = a + kTileV * kBK * 2;
 #pragma unroll
-        for (int k = 0; k < kBK / 16; ++k)
-          umma_f16(tmem + static_cast<uint32_t>(i * Rp), umma_desc_sw128(a + 32 * k), umma_desc_sw128(b + 32 * k),
-                   idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < kBK / 16; ++k)
+            umma_f16(tmem + static_cast<uint32_t>(i * Rp), umma_desc_sw128(a + 32 * k), umma_desc_sw128(b + 32 * k),
+                     idesc, (sk > 0 || j > 0 || k > 0) ? 1u : 0u);
+        }
         umma_commit(&empty[st]);  // the stage is free once these MMAs have read it
       }
     }
@@ -264,6 +271,13 @@ __global__ void __launch_bounds__(kThreads, 1) lmhead_topm_kernel(LhParams p, co
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(cols) : "memory");
 }
 
+constexpr int kLhKbps = 4;  // K blocks per stage (the largest divisor of D / 64 up to this): 512 bytes of a head row
+inline int lh_kbps_setting(int nkb) {
+  int k = kLhKbps < nkb ? kLhKbps : nkb;
+  while (nkb % k) --k;
+  return k;
+}
+
 struct LhLayout {
   size_t pool, counts, cand, bytes;
   int Rp, tiles, tpc, cap;
@@ -308,7 +322,15 @@ extern "C" dt_status dt_lmhead_topm(int R, int D, int V, int M, const void* hidd
   const LhLayout L = lh_layout(R, V, di.sms);
   if (workspace_bytes < L.bytes) return DT_ERR_INVALID_ARG;
   if (L.tpc * L.Rp > kTmemMax) return DT_ERR_UNSUPPORTED;  // the CTA's slice of logits must fit its tensor memory
-  const size_t smem = lh_smem_bytes(L.Rp);
+  // the ring: K blocks per stage and as many stages as the shared memory takes (a 2 KB reserve for the kernel's
+  // static shared memory)
+  const int nkb = D / kBK;
+  const int kbps = lh_kbps_setting(nkb);
+  const size_t room = static_cast<size_t>(di.optin) - 2048 - 1024;
+  int stages = static_cast<int>(room / (kbps * lh_block_bytes(L.Rp)));
+  stages = stages < kMaxStages ? stages : kMaxStages;
+  if (stages < 2) return DT_ERR_UNSUPPORTED;
+  const size_t smem = lh_smem_bytes(L.Rp, stages, kbps);
   if (smem + 2048 > static_cast<size_t>(di.optin)) return DT_ERR_UNSUPPORTED;
   LhMaps maps{};
   if (!encode_bf16_2d(&maps.w, w_head, static_cast<uint64_t>(D), static_cast<uint64_t>(V), static_cast<uint64_t>(D),
@@ -319,6 +341,7 @@ extern "C" dt_status dt_lmhead_topm(int R, int D, int V, int M, const void* hidd
   char* ws = static_cast<char*>(workspace);
   LhParams p{};
   p.R = R; p.Rp = L.Rp; p.D = D; p.V = V; p.M = M; p.tiles = L.tiles; p.tpc = L.tpc; p.G = di.sms; p.cap = L.cap;
+  p.stages = stages; p.kbps = kbps;
   p.pool = reinterpret_cast<uint32_t*>(ws + L.pool);
   p.counts = reinterpret_cast<int*>(ws + L.counts);
   p.cand = reinterpret_cast<uint64_t*>(ws + L.cand);
