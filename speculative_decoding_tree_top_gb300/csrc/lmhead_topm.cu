@@ -38,15 +38,19 @@ constexpr int kBK = 64;               // K block: 64 bf16 = one 128-byte swizzle
 constexpr int kMaxStages = 12;
 constexpr int kMaxRp = 64;            // padded hidden rows (the MMA's N): a multiple of 16
 constexpr int kTmemMax = 512;
+constexpr int kMaxTiles = kTmemMax / 16;  // tiles per CTA at most (each takes Rp >= 16 TMEM columns)
 constexpr int kPoolPerQuarter = 2;    // logits a warp quarter offers per row
 constexpr int kPoolPerCta = 4 * kPoolPerQuarter;
+constexpr int kPoolPerThread = 8;     // pool values per thread in the bound's selection: G x kPoolPerCta <= 2048
 constexpr uint64_t kBudgetNs = 4000000000ull;  // copies and MMAs take microseconds: this stops a lost one
+constexpr size_t kStaticReserve = 3072;        // shared memory kept for the kernel's static variables
 
 struct LhParams {
-  int R, Rp, D, V, M, tiles, tpc, G, cap;
+  int R, Rp, D, V, M, rpc, tpc, last, G;  // head rows per CTA, tiles per CTA, rows of a CTA's last tile
   int stages, kbps;  // ring stages, and K blocks per stage (a divisor of D / 64)
   uint32_t* pool;   // [Rp][G * kPoolPerCta] value keys (0: none)
-  uint64_t* cand;   // [R][G][cap] row words
+  uint32_t* bounds; // [R] each row's bound (a key)
+  uint64_t* cand;   // [R][G][rpc] each CTA's candidates of each row as row words
   int* counts;      // [R][G]
   int32_t* ids;     // [R][M]
   float* vals;      // [R][M]
@@ -55,6 +59,7 @@ struct LhParams {
 };
 struct LhMaps {
   CUtensorMap w;    // head [V][D] bf16, box 64 x 128
+  CUtensorMap wl;   // the same, box 64 x last (a CTA's last tile)
   CUtensorMap h;    // hidden [R][D] bf16, box 64 x Rp
 };
 
@@ -78,19 +83,87 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "memory");
 }
 
+// Two groups of sixteen TMEM columns of this warp's 32 lanes, and one wait for both.
+__device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, uint32_t (&a)[16], uint32_t (&b)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]),
+        "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]),
+        "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]),
+        "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15])
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
+
+// The M-th largest of n keys (np values of a row's pool, kPer per thread at most, read from global memory) in
+// every thread of the block, 0 when n < M: radix select with 8-bit digits from the top, one 256-bin shared
+// histogram per digit over the keys that share the digits found so far.
+template <int kPer>
+__device__ uint32_t block_kth_of(const uint32_t* __restrict__ keys, int n, int M, unsigned* hist, unsigned* s_sel) {
+  const int t = threadIdx.x, lane = t & 31;
+  if (n < M) return 0u;
+  uint32_t v[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) v[k] = t + kThreads * k < n ? __ldcg(keys + t + kThreads * k) : 0u;
+  uint32_t prefix = 0;
+  int need = M;
+#pragma unroll 1
+  for (int d = 3; d >= 0; --d) {
+    hist[t] = 0u;  // kThreads == 256 bins
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const bool in = t + kThreads * k < n && (d == 3 || (v[k] >> (8 * (d + 1))) == prefix);
+      if (in) atomicAdd(&hist[(v[k] >> (8 * d)) & 255u], 1u);
+    }
+    __syncthreads();
+    if (t < 32) {  // lane L holds bins 255 - 8L down to 248 - 8L: counts from the top
+      unsigned cb[8], sum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        cb[j] = hist[255 - 8 * lane - j];
+        sum += cb[j];
+      }
+      unsigned incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned excl = incl - sum;
+      if (excl < static_cast<unsigned>(need) && incl >= static_cast<unsigned>(need)) {
+        unsigned acc, at;
+        const int j = pick_bin(cb, excl, static_cast<unsigned>(need), acc, at);
+        s_sel[0] = static_cast<unsigned>(255 - 8 * lane - j);
+        s_sel[1] = acc;
+      }
+    }
+    __syncthreads();
+    prefix = (prefix << 8) | s_sel[0];
+    need -= static_cast<int>(s_sel[1]);
+    __syncthreads();  // s_sel and hist are rewritten by the next digit
+  }
+  return prefix;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) lmhead_topm_kernel(LhParams p, const __grid_constant__ LhMaps maps) {
   extern __shared__ float4 smem_f4[];
   unsigned char* base =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_f4) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t full[kMaxStages], empty[kMaxStages], done;
+  __shared__ uint64_t full[kMaxStages], empty[kMaxStages], done, tdone[kMaxTiles];
   __shared__ uint32_t s_tmem;
   __shared__ uint32_t s_bound[kMaxRp];
   __shared__ int s_cnt[kMaxRp];
   __shared__ int s_flag, s_warp[kThreads / 32], s_n;
+  __shared__ unsigned s_hist[256], s_sel[2];
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int G = static_cast<int>(gridDim.x), bid = static_cast<int>(blockIdx.x);
   const int R = p.R, Rp = p.Rp, nst = p.D / kBK / p.kbps, S = p.stages, kbps = p.kbps;
-  const int my_tiles = bid < p.tiles ? (p.tiles - 1 - bid) / G + 1 : 0;
+  // this CTA's head rows: [row0, row0 + nrows), in tiles of 128 (the last one of `last` rows)
+  const int row0 = bid * p.rpc, nrows = min(p.rpc, p.V - row0);
+  const int my_tiles = nrows > 0 ? (nrows + kTileV - 1) / kTileV : 0;
   const uint32_t cols = static_cast<uint32_t>(p.tpc * Rp) <= 32u ? 32u
                         : static_cast<uint32_t>(p.tpc * Rp) <= 64u ? 64u
                         : static_cast<uint32_t>(p.tpc * Rp) <= 128u ? 128u
@@ -101,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1) lmhead_topm_kernel(LhParams p, co
       mbar_init(&empty[i], 1);
     }
     mbar_init(&done, 1);
+    for (int i = 0; i < kMaxTiles; ++i) mbar_init(&tdone[i], 1);
     mbar_fence_init();
   }
   if (warp == 0) {
@@ -113,13 +187,14 @@ __global__ void __launch_bounds__(kThreads, 1) lmhead_topm_kernel(LhParams p, co
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = s_tmem;
   const size_t blk = lh_block_bytes(Rp), stage = blk * kbps;
-  const uint32_t tx = static_cast<uint32_t>(stage);
   bool ok = true;
 
   // ---- GEMM: tile i of this CTA (vocabulary rows (bid + i G) * 128 ...) into TMEM columns [i Rp, (i + 1) Rp) ----
   if (warp == 0 && lane == 0) {  // TMA producer: stage s of tile i holds K blocks [s kbps, (s + 1) kbps)
     for (int i = 0; i < my_tiles && ok; ++i) {
-      const int tile = bid + i * G;
+      const bool lastt = i == p.tpc - 1;  // the CTA's last tile reads `last` head rows
+      const CUtensorMap* wm = lastt ? &maps.wl : &maps.w;
+      const uint32_t tx = static_cast<uint32_t>(kbps * ((lastt ? p.last : kTileV) + Rp) * kBK * 2);
       for (int sk = 0; sk < nst; ++sk) {
         const unsigned n = static_cast<unsigned>(i * nst + sk), st = n % S, use = n / S;
         if (use > 0) ok = mbar_wait(&empty[st], (use - 1) & 1u, kBudgetNs);
@@ -128,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1) lmhead_topm_kernel(LhParams p, co
         mbar_expect_tx(&full[st], tx);
         for (int j = 0; j < kbps; ++j) {
           const int kb = sk * kbps + j;
-          tma_load_2d(a + j * blk, &maps.w, kb * kBK, tile * kTileV, &full[st]);
+          tma_load_2d(a + j * blk, wm, kb * kBK, row0 + i * kTileV, &full[st]);
           tma_load_2d(a + j * blk + kTileV * kBK * 2, &maps.h, kb * kBK, 0, &full[st]);
         }
       }
@@ -150,30 +225,58 @@ __global__ void __launch_bounds__(kThreads, 1) lmhead_topm_kernel(LhParams p, co
         }
         umma_commit(&empty[st]);  // the stage is free once these MMAs have read it
       }
+      if (ok) umma_commit(&tdone[i]);  // tile i's accumulator is complete after these MMAs
     }
     if (ok && my_tiles > 0) umma_commit(&done);  // every accumulator is complete after the last MMAs
+  }
+  // Warps 4..7 (TMEM lanes 32 (w % 4) .. + 31: head row 32 (w % 4) + lane of every tile) fold each tile into the
+  // running two largest logits of rows 0..15 as soon as its accumulator is complete, while the GEMM goes on.
+  const int q = warp & 3, half = warp >> 2;
+  const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16);
+  const int np = G * kPoolPerCta;
+  bool nan = false;
+  uint32_t b1[16], b2[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) b1[j] = b2[j] = 0u;
+  if (warp >= 4) {
+    for (int i = 0; i < my_tiles && ok; ++i) {
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(&tdone[i], 0u, kBudgetNs));  // the TMEM load below is warp-wide
+      if (!ok) break;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      uint32_t v[16];
+      tmem_ld16(tq + static_cast<uint32_t>(i * Rp), v);
+      const bool valid = i * kTileV + 32 * q + lane < nrows;  // rows past the range hold stale shared memory
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const bool isnan = (v[j] & 0x7FFFFFFFu) > 0x7F800000u;
+        nan |= valid && isnan && j < R;
+        const uint32_t k = valid && !isnan ? key_of_f32(v[j]) : 0u;
+        if (k > b1[j]) {
+          b2[j] = b1[j];
+          b1[j] = k;
+        } else if (k > b2[j]) {
+          b2[j] = k;
+        }
+      }
+    }
   }
   ok = __syncthreads_and(ok);
   if (ok && my_tiles > 0) ok = mbar_wait(&done, 0u, kBudgetNs);
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   ok = __syncthreads_and(ok);
 
-  // Warps w and w + 4 read TMEM lanes 32 (w % 4) .. + 31 (head row 32 (w % 4) + lane of every tile) and split the
-  // row groups of 16 columns between them.
-  const int q = warp & 3, half = warp >> 2;
-  const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16);
-  const int np = G * kPoolPerCta;
-  bool nan = false;
   if (ok) {
-    // ---- pool: every quarter's two largest logits of each row ----
-    for (int g = half; g < Rp / 16; g += 2) {
-      uint32_t b1[16], b2[16];
+    // ---- pool: every quarter's two largest logits of each row (rows 0..15 already folded by warps 4..7; the other
+    // row groups now, warps w and w + 4 taking alternate groups) ----
+    for (int g = half ? 0 : 1; g < Rp / 16; g += 2) {
+      if (g > 0) {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) b1[j] = b2[j] = 0u;
-      for (int i = 0; i < my_tiles; ++i) {
+        for (int j = 0; j < 16; ++j) b1[j] = b2[j] = 0u;
+      }
+      for (int i = 0; i < (g > 0 ? my_tiles : 0); ++i) {
         uint32_t v[16];
         tmem_ld16(tq + static_cast<uint32_t>(i * Rp + 16 * g), v);
-        const bool valid = (bid + i * G) * kTileV + 32 * q + lane < p.V;
+        const bool valid = i * kTileV + 32 * q + lane < nrows;  // rows past the range hold stale shared memory
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const bool isnan = (v[j] & 0x7FFFFFFFu) > 0x7F800000u;
@@ -204,44 +307,43 @@ __global__ void __launch_bounds__(kThreads, 1) lmhead_topm_kernel(LhParams p, co
   if (ok) ok = grid_barrier(p.hdr, static_cast<unsigned>(G), p.timeout_ns, &s_flag);
 
   if (ok) {
-    // ---- bound: the M-th largest key of each row's pool (0: fewer than M values, take every logit) ----
-    uint32_t* pk = reinterpret_cast<uint32_t*>(base) + static_cast<size_t>(warp) * np;  // this warp's copy
-    for (int r = warp; r < R; r += kThreads / 32) {
-      const uint32_t* pr = p.pool + static_cast<size_t>(r) * np;
-      for (int i = lane; i < np; i += 32) pk[i] = __ldcg(pr + i);
-      __syncwarp();
-      uint32_t th = 0;
-      if (np >= p.M) {
-        for (int bit = 31; bit >= 0; --bit) {
-          const uint32_t c = th | (1u << bit);
-          int cnt = 0;
-          for (int i = lane; i < np; i += 32) cnt += pk[i] >= c;
-          if (__reduce_add_sync(0xFFFFFFFFu, cnt) >= p.M) th = c;
-        }
-      }
-      if (lane == 0) s_bound[r] = th;
-      __syncwarp();
+    // ---- bound: CTA r takes row r's pool and publishes its M-th largest key (0: fewer than M values in the pool,
+    // take every logit); after a grid barrier every CTA reads all the rows' bounds ----
+    for (int r = bid; r < R; r += G) {
+      const uint32_t th = block_kth_of<kPoolPerThread>(p.pool + static_cast<size_t>(r) * np, np, p.M, s_hist, s_sel);
+      if (t == 0) p.bounds[r] = th;
     }
+    ok = grid_barrier(p.hdr, static_cast<unsigned>(G), p.timeout_ns, &s_flag);
+  }
+  if (ok) {
+    for (int r = t; r < R; r += kThreads) s_bound[r] = __ldcg(p.bounds + r);
     for (int r = t; r < R; r += kThreads) s_cnt[r] = 0;
     __syncthreads();
-    // ---- filter: the logits at or above their row's bound, as row words, into this CTA's list of the row ----
-    for (int g = half; g < Rp / 16; g += 2) {
-      for (int i = 0; i < my_tiles; ++i) {
-        uint32_t v[16];
-        tmem_ld16(tq + static_cast<uint32_t>(i * Rp + 16 * g), v);
-        const int vid = (bid + i * G) * kTileV + 32 * q + lane;
+    // ---- filter: the logits at or above their row's bound, as row words, into this CTA's list of the row; warps w
+    // and w + 4 take alternate tiles, two tiles per TMEM wait ----
+    auto keep = [&](const uint32_t (&v)[16], int i, int g) {
+      const int loc = i * kTileV + 32 * q + lane;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int r = 16 * g + j;
-          const bool isnan = (v[j] & 0x7FFFFFFFu) > 0x7F800000u;
-          if (vid < p.V && r < R && !isnan) {
-            const uint32_t k = key_of_f32(v[j]);
-            if (k >= s_bound[r]) {
-              const int pos = atomicAdd(&s_cnt[r], 1);  // < cap: the CTA holds at most cap logits of a row
-              p.cand[(static_cast<size_t>(r) * G + bid) * p.cap + pos] = pack_candidate(k, static_cast<uint32_t>(vid));
-            }
+      for (int j = 0; j < 16; ++j) {
+        const int r = 16 * g + j;
+        const bool isnan = (v[j] & 0x7FFFFFFFu) > 0x7F800000u;
+        if (loc < nrows && r < R && !isnan) {
+          const uint32_t k = key_of_f32(v[j]);
+          if (k >= s_bound[r]) {
+            const int pos = atomicAdd(&s_cnt[r], 1);  // < rpc: the CTA holds at most rpc logits of a row
+            p.cand[(static_cast<size_t>(r) * G + bid) * p.rpc + pos] = pack_candidate(k, static_cast<uint32_t>(row0 + loc));
           }
         }
+      }
+    };
+    for (int g = 0; g < Rp / 16; ++g) {
+      for (int i = half; i < my_tiles; i += 4) {
+        uint32_t v0[16], v1[16];
+        const bool two = i + 2 < my_tiles;
+        tmem_ld16x2(tq + static_cast<uint32_t>(i * Rp + 16 * g), tq + static_cast<uint32_t>((two ? i + 2 : i) * Rp + 16 * g),
+                    v0, v1);
+        keep(v0, i, g);
+        if (two) keep(v1, i + 2, g);
       }
     }
     __syncthreads();
@@ -253,8 +355,8 @@ __global__ void __launch_bounds__(kThreads, 1) lmhead_topm_kernel(LhParams p, co
     // ---- selection: CTA r takes row r from the G lists ----
     SelectSmem& S = *reinterpret_cast<SelectSmem*>(base);
     for (int r = bid; r < R; r += G) {
-      const uint64_t* rc = p.cand + static_cast<size_t>(r) * G * p.cap;
-      const int cap = p.cap;
+      const uint64_t* rc = p.cand + static_cast<size_t>(r) * G * p.rpc;
+      const int cap = p.rpc;
       select_words<false>(
           p.counts + static_cast<size_t>(r) * G, G, p.M,
           [&](int c, int i) { return __ldcg(rc + static_cast<size_t>(c) * cap + i); },
@@ -279,19 +381,20 @@ inline int lh_kbps_setting(int nkb) {
 }
 
 struct LhLayout {
-  size_t pool, counts, cand, bytes;
-  int Rp, tiles, tpc, cap;
+  size_t pool, bounds, counts, cand, bytes;
+  int Rp, rpc, tpc, last;
 };
 inline LhLayout lh_layout(int R, int V, int G) {
   LhLayout L{};
   L.Rp = (R + 15) / 16 * 16;
-  L.tiles = (V + kTileV - 1) / kTileV;
-  L.tpc = (L.tiles + G - 1) / G;
-  L.cap = L.tpc * kTileV;
+  L.rpc = (V + G - 1) / G;                       // head rows per CTA, contiguous
+  L.tpc = (L.rpc + kTileV - 1) / kTileV;         // tiles per CTA
+  L.last = L.rpc - kTileV * (L.tpc - 1);         // rows of a CTA's last tile
   L.pool = align_up(sizeof(WsHeader));
-  L.counts = align_up(L.pool + sizeof(uint32_t) * static_cast<size_t>(L.Rp) * G * kPoolPerCta);
+  L.bounds = align_up(L.pool + sizeof(uint32_t) * static_cast<size_t>(L.Rp) * G * kPoolPerCta);
+  L.counts = align_up(L.bounds + sizeof(uint32_t) * static_cast<size_t>(R));
   L.cand = align_up(L.counts + sizeof(int) * static_cast<size_t>(R) * G);
-  L.bytes = align_up(L.cand + sizeof(uint64_t) * static_cast<size_t>(R) * G * L.cap);
+  L.bytes = align_up(L.cand + sizeof(uint64_t) * static_cast<size_t>(R) * G * L.rpc);
   return L;
 }
 
@@ -322,27 +425,31 @@ extern "C" dt_status dt_lmhead_topm(int R, int D, int V, int M, const void* hidd
   const LhLayout L = lh_layout(R, V, di.sms);
   if (workspace_bytes < L.bytes) return DT_ERR_INVALID_ARG;
   if (L.tpc * L.Rp > kTmemMax) return DT_ERR_UNSUPPORTED;  // the CTA's slice of logits must fit its tensor memory
-  // the ring: K blocks per stage and as many stages as the shared memory takes (a 2 KB reserve for the kernel's
-  // static shared memory)
+  if (di.sms * kPoolPerCta > kThreads * kPoolPerThread) return DT_ERR_UNSUPPORTED;  // the pool of a row in registers
+  // the ring: K blocks per stage and as many stages as the shared memory takes (a reserve for the kernel's static
+  // shared memory, about 2 KB)
   const int nkb = D / kBK;
   const int kbps = lh_kbps_setting(nkb);
-  const size_t room = static_cast<size_t>(di.optin) - 2048 - 1024;
+  const size_t room = static_cast<size_t>(di.optin) - kStaticReserve - 1024;
   int stages = static_cast<int>(room / (kbps * lh_block_bytes(L.Rp)));
   stages = stages < kMaxStages ? stages : kMaxStages;
   if (stages < 2) return DT_ERR_UNSUPPORTED;
   const size_t smem = lh_smem_bytes(L.Rp, stages, kbps);
-  if (smem + 2048 > static_cast<size_t>(di.optin)) return DT_ERR_UNSUPPORTED;
+  if (smem + kStaticReserve > static_cast<size_t>(di.optin)) return DT_ERR_UNSUPPORTED;
   LhMaps maps{};
   if (!encode_bf16_2d(&maps.w, w_head, static_cast<uint64_t>(D), static_cast<uint64_t>(V), static_cast<uint64_t>(D),
                       kBK, kTileV) ||
+      !encode_bf16_2d(&maps.wl, w_head, static_cast<uint64_t>(D), static_cast<uint64_t>(V), static_cast<uint64_t>(D),
+                      kBK, static_cast<uint32_t>(L.last)) ||
       !encode_bf16_2d(&maps.h, hidden, static_cast<uint64_t>(D), static_cast<uint64_t>(R), static_cast<uint64_t>(D),
                       kBK, static_cast<uint32_t>(L.Rp)))
     return DT_ERR_CUDA;
   char* ws = static_cast<char*>(workspace);
   LhParams p{};
-  p.R = R; p.Rp = L.Rp; p.D = D; p.V = V; p.M = M; p.tiles = L.tiles; p.tpc = L.tpc; p.G = di.sms; p.cap = L.cap;
+  p.R = R; p.Rp = L.Rp; p.D = D; p.V = V; p.M = M; p.rpc = L.rpc; p.tpc = L.tpc; p.last = L.last; p.G = di.sms;
   p.stages = stages; p.kbps = kbps;
   p.pool = reinterpret_cast<uint32_t*>(ws + L.pool);
+  p.bounds = reinterpret_cast<uint32_t*>(ws + L.bounds);
   p.counts = reinterpret_cast<int*>(ws + L.counts);
   p.cand = reinterpret_cast<uint64_t*>(ws + L.cand);
   p.ids = out_ids;
