@@ -27,6 +27,9 @@
 //   orc_lmhead_topm - pinned: numpy's fp64 matmul of the widened inputs followed by a full lexicographic sort; a
 //                     one-hot head whose logits are the hidden values themselves; duplicated head rows (ties go
 //                     to the lower id).
+//   orc_tree_attention - pinned: torch's scaled_dot_product_attention in fp64 with the same boolean mask and the
+//                     key/value heads repeated for the grouped query heads; a diagonal mask with no prefix (every
+//                     node sees only itself: out = its own v); equal scores (out = the mean of the visible v).
 //   orc_build_trees_marginal - pinned: brute-force enumeration of the depth-limited tree under the product of the
 //                     marginals (log-softmax by torch), and equality with orc_build_trees at W_c = 0.
 //   The GRU gate layout (rows r|z|n, PyTorch convention) and the order "add correction, then divide by T" are
@@ -402,6 +405,51 @@ int orc_lmhead_topm(int R, int D, int V, int M, const void* hidden, int hdtype, 
     }
   }
   return status;
+}
+
+// Tree attention of the verify pass. [S] "Methodology — deep read": the tree is verified in one target forward pass
+// with an ancestor-only causal mask; [G] "Composants Clés — Vérification": standard tree attention, unchanged.
+// Reading: for request b, query head h and tree node i, the keys are the L prefix positions (all visible) and the n
+// tree positions L + t with mask[b][i][t] = 1 (its ancestors and itself); grouped-query heads: query head h reads
+// key/value head h / (Hq / Hkv). out = softmax_j(scale * q . k_j) v_j over the visible keys, in fp64.
+// q [B][n][Hq][d], k and v [B][Hkv][L + n][d] (fp32 or bf16), mask [B][n][n] uint8, out [B][n][Hq][d] fp64.
+int orc_tree_attention(int B, int n, int L, int Hq, int Hkv, int d, const void* q, const void* k, const void* v,
+                       int dtype, const uint8_t* mask, double scale, double* out, int threads) {
+  if (!q || !k || !v || !mask || !out || B < 0 || n < 1 || L < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv || d < 1)
+    return ORC_ERR_ARG;
+  const int G = Hq / Hkv, T = L + n;
+#pragma omp parallel for collapse(2) schedule(dynamic) num_threads(threads_or_default(threads))
+  for (int b = 0; b < B; ++b)
+    for (int h = 0; h < Hq; ++h) {
+      const int kvh = h / G;
+      const size_t kv0 = (static_cast<size_t>(b) * Hkv + kvh) * T;
+      std::vector<double> sc(static_cast<size_t>(T));
+      for (int i = 0; i < n; ++i) {
+        const size_t q0 = ((static_cast<size_t>(b) * n + i) * Hq + h) * d;
+        double mx = -std::numeric_limits<double>::infinity();
+        for (int j = 0; j < T; ++j) {
+          const bool visible = j < L || mask[(static_cast<size_t>(b) * n + i) * n + (j - L)] != 0;
+          if (!visible) {
+            sc[j] = -std::numeric_limits<double>::infinity();
+            continue;
+          }
+          double dot = 0.0;
+          for (int e = 0; e < d; ++e) dot += load(q, dtype, q0 + e) * load(k, dtype, (kv0 + j) * d + e);
+          sc[j] = scale * dot;
+          mx = std::max(mx, sc[j]);
+        }
+        double den = 0.0;
+        for (int j = 0; j < T; ++j) den += std::isinf(sc[j]) && sc[j] < 0 ? 0.0 : std::exp(sc[j] - mx);
+        double* o = out + q0;
+        for (int e = 0; e < d; ++e) o[e] = 0.0;
+        for (int j = 0; j < T; ++j) {
+          if (std::isinf(sc[j]) && sc[j] < 0) continue;
+          const double w = std::exp(sc[j] - mx) / den;
+          for (int e = 0; e < d; ++e) o[e] += w * load(v, dtype, (kv0 + j) * d + e);
+        }
+      }
+    }
+  return ORC_OK;
 }
 
 int orc_gru_step(int H, int E, int wdtype, const void* w_ih, const void* w_hh, const void* b_ih, const void* b_hh,

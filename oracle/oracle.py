@@ -52,6 +52,7 @@ def load(path=None) -> ctypes.CDLL:
     lib = ctypes.CDLL(str(path or build()))
     lib.orc_topm.argtypes = [_P, _I, _I, _I, _I, _I, _P, _P, _I]
     lib.orc_lmhead_topm.argtypes = [_I, _I, _I, _I, _P, _I, _P, _I, _P, _P, _I]
+    lib.orc_tree_attention.argtypes = [_I, _I, _I, _I, _I, _I, _P, _P, _P, _I, _P, _D, _P, _I]
     lib.orc_gru_step.argtypes = [_I, _I, _I, _P, _P, _P, _P, _P, _P, _P]
     lib.orc_child_logp.argtypes = [_I, _I, _P, _P, _P, _I, _D, _P, _P]
     lib.orc_build_trees.argtypes = [_I, _I, _I, _I, _I, _D, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P,
@@ -123,6 +124,21 @@ def lmhead_topm(hidden: np.ndarray, w_head: np.ndarray, M: int, threads: int = 0
     _check(L.orc_lmhead_topm(R, D, V, M, _ptr(hidden), _dtype_code(hidden), _ptr(w_head), _dtype_code(w_head),
                              _ptr(ids), _ptr(vals), threads))
     return ids, vals
+
+
+def tree_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, mask: np.ndarray, scale: float, threads: int = 0,
+                   L=None) -> np.ndarray:
+    """q [B,n,Hq,d], k/v [B,Hkv,L+n,d] (fp32, or bf16 bit patterns as uint16), mask [B,n,n] uint8 -> out [B,n,Hq,d]
+    float64: the verify pass's attention of each tree node over the prefix and its visible tree positions."""
+    Lib = L or lib()
+    B, n, Hq, d = q.shape
+    Hkv, T = k.shape[1], k.shape[2]
+    assert q.dtype == k.dtype == v.dtype
+    out = np.empty((B, n, Hq, d), np.float64)
+    _check(Lib.orc_tree_attention(B, n, T - n, Hq, Hkv, d, _ptr(np.ascontiguousarray(q)), _ptr(np.ascontiguousarray(k)),
+                                  _ptr(np.ascontiguousarray(v)), _dtype_code(q),
+                                  _ptr(np.ascontiguousarray(mask, np.uint8)), float(scale), _ptr(out), threads))
+    return out
 
 
 def gru_step(w_ih, w_hh, b_ih, b_hh, x: np.ndarray, h: np.ndarray, L=None) -> np.ndarray:

@@ -7,6 +7,7 @@ What each pin leans on, outside the oracle:
   * top-M             - a full lexicographic sort of every row (numpy lexsort), i.e. brute force;
   * projection top-M  - numpy's fp64 matmul on exactly representable inputs, then the same full sort; a one-hot
                         head (closed form);
+  * tree attention    - torch's scaled_dot_product_attention in fp64 with the same mask; two closed forms;
   * GRU step          - torch.nn.GRUCell in fp64 (library routine);
   * restricted softmax- with M = V it must equal torch.log_softmax over the full-vocabulary corrected row
                         computed with a dense matmul (no gather);
@@ -449,6 +450,62 @@ def pin_lmhead_topm(L):
         assert np.array_equal(ids[r], order) and np.array_equal(vals[r], expect[r][order]), r
 
 
+def _random_tree_mask(rng, B, n):
+    """Ancestor masks of random prefix-closed trees (each node's parent precedes it; -1 = a child of the root)."""
+    mask = np.zeros((B, n, n), np.uint8)
+    for b in range(B):
+        par = [-1] + [int(rng.integers(-1, i)) for i in range(1, n)]
+        for i in range(n):
+            j = i
+            while j >= 0:
+                mask[b, i, j] = 1
+                j = par[j]
+    return mask
+
+
+def pin_tree_attention(L):
+    """The verify pass's tree attention against torch's scaled_dot_product_attention in fp64 (the same boolean mask:
+    every prefix key, and the tree keys of the node's ancestors and itself; the key/value heads repeated for the
+    grouped query heads); then two closed forms: with no prefix and a diagonal mask every node sees only itself (out
+    = its own value row), and with q = 0 all visible keys weigh the same (out = the mean of their value rows)."""
+    from oracle import oracle as orc
+    rng = np.random.default_rng(5)
+    B, n, Lp, Hq, Hkv, d = 2, 7, 19, 4, 2, 16
+    G, T = Hq // Hkv, Lp + n
+    for dtype in ("f32", "bf16"):
+        q = rng.standard_normal((B, n, Hq, d)).astype(np.float32)
+        k = rng.standard_normal((B, Hkv, T, d)).astype(np.float32)
+        v = rng.standard_normal((B, Hkv, T, d)).astype(np.float32)
+        mask = _random_tree_mask(rng, B, n)
+        cast = (lambda a: a) if dtype == "f32" else (lambda a: synth.bits_u16(torch.from_numpy(a).to(torch.bfloat16)))
+        qq, kk, vv = cast(q), cast(k), cast(v)
+        scale = 0.37
+        out = orc.tree_attention(qq, kk, vv, mask, scale, L=L)
+        qt = torch.from_numpy(widen(qq)).permute(0, 2, 1, 3)                       # [B,Hq,n,d]
+        kt = torch.from_numpy(widen(kk)).repeat_interleave(G, dim=1)               # [B,Hq,T,d]
+        vt = torch.from_numpy(widen(vv)).repeat_interleave(G, dim=1)
+        am = torch.ones((B, 1, n, T), dtype=torch.bool)
+        am[:, 0, :, Lp:] = torch.from_numpy(mask.astype(bool))
+        ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=am, scale=scale)
+        assert np.max(np.abs(out - ref.permute(0, 2, 1, 3).numpy())) < 1e-12, dtype
+    # no prefix, diagonal mask: each node's output is its own value row
+    q = rng.standard_normal((1, n, Hq, d)).astype(np.float32)
+    k = rng.standard_normal((1, Hkv, n, d)).astype(np.float32)
+    v = rng.standard_normal((1, Hkv, n, d)).astype(np.float32)
+    out = orc.tree_attention(q, k, v, np.eye(n, dtype=np.uint8)[None], 1.0, L=L)
+    for h in range(Hq):
+        assert np.array_equal(out[0, :, h], v[0, h // G].astype(np.float64)), h
+    # q = 0: every visible key weighs the same
+    mask = _random_tree_mask(rng, 1, n)
+    k = rng.standard_normal((1, Hkv, Lp + n, d)).astype(np.float32)
+    v = rng.standard_normal((1, Hkv, Lp + n, d)).astype(np.float32)
+    out = orc.tree_attention(np.zeros((1, n, Hq, d), np.float32), k, v, mask, 0.5, L=L)
+    for i in range(n):
+        vis = list(range(Lp)) + [Lp + t for t in range(n) if mask[0, i, t]]
+        for h in range(Hq):
+            assert np.max(np.abs(out[0, i, h] - v[0, h // G, vis].astype(np.float64).mean(0))) < 1e-12, (i, h)
+
+
 ALL_PINS = [pin_topm_bruteforce, pin_gru_vs_grucell, pin_full_vocab_softmax, pin_golden, pin_special_cases,
             pin_factorised_closed_form, pin_bruteforce_tree, pin_invariants, pin_rescore, pin_marginal_builder,
-            pin_accept_paths, pin_lmhead_topm]
+            pin_accept_paths, pin_lmhead_topm, pin_tree_attention]

@@ -44,6 +44,10 @@ MUTANTS = {
                                "load(w_head, wdtype, (static_cast<size_t>(k) * V + v) % (static_cast<size_t>(V) * D))"),
     "lmhead-hidden-row-0": ("h[k] = load(hidden, hdtype, static_cast<size_t>(r) * D + k);",
                             "h[k] = load(hidden, hdtype, static_cast<size_t>(k));"),
+    "attention-mask-transposed": ("mask[(static_cast<size_t>(b) * n + i) * n + (j - L)]",
+                                  "mask[(static_cast<size_t>(b) * n + (j - L)) * n + i]"),
+    "attention-kv-head-interleaved": ("const int kvh = h / G;", "const int kvh = h % Hkv;"),
+    "attention-drops-scale": ("sc[j] = scale * dot;", "sc[j] = dot;"),
     "embedding-of-parent": ("load(w.emb, w.dtype, static_cast<size_t>(u.token) * E + e)",
                             "load(w.emb, w.dtype, static_cast<size_t>(u.parent < 0 ? u.token : tokens[u.parent]) * E + e)"),
 }
