@@ -195,6 +195,29 @@ dt_status dt_lmhead_topm(int R, int D, int V, int M, const void* hidden, const v
                          cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------------------------------------------
+ * dt_tree_attention — the verify pass's attention over the accepted prefix and the draft tree.
+ * Source: blog.captcha.la, "Methodology — deep read" (the prefix-closed tree is verified in one target forward pass
+ * with an unmodified ancestor-only causal mask, borrowed from DDTree/SpecInfer); gist.science, "Composants Clés —
+ * Vérification" (standard tree attention, unchanged and lossless).
+ *
+ * Semantics: for request b, query head h and tree node i, the visible keys are the L prefix positions and the tree
+ * positions L + t with mask[b][i][t] = 1 (as dt_build_trees emits it: the node's ancestors and itself); query head h
+ * reads key/value head h / (Hq / Hkv);  out[b][i][h] = sum_j softmax_j(scale * q[b][i][h] . k_j) v_j  over them.
+ * Arithmetic: bf16 products on the tensor cores, fp32 accumulation; the softmax weights are rounded to bf16 before
+ * they multiply the value rows.
+ *   q          [B,n,Hq,d] bf16;  k, v [B,Hkv,L+n,d] bf16 (the prefix's cache rows, then the tree's);
+ *   mask       [B,n,n] uint8 (device);  out [B,n,Hq,d] fp32;
+ *   workspace  dt_tree_attention_workspace_bytes(B,n,L,Hq,Hkv,d) bytes (partials of the key chunks).
+ * Supported: dtype DT_BF16, d = 128, (Hq / Hkv) * n <= 64. Outside it DT_ERR_UNSUPPORTED; argument errors (Hq not a
+ * multiple of Hkv, scale not finite and positive, null or misaligned pointers) DT_ERR_INVALID_ARG; both before any
+ * launch. Pointers are 16-byte aligned device pointers (mask: any alignment).
+ * ------------------------------------------------------------------------------------------------------------- */
+size_t dt_tree_attention_workspace_bytes(int B, int n, int L, int Hq, int Hkv, int d);
+dt_status dt_tree_attention(int B, int n, int L, int Hq, int Hkv, int d, const void* q, const void* k, const void* v,
+                            dt_dtype dtype, const uint8_t* mask, float scale, float* out, void* workspace,
+                            size_t workspace_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------------------------------------
  * dt_topm_static — dt_topm for callers that cannot allocate device memory.
  * No counterpart in the paper: this is a deployment variant of dt_topm, with the same arguments minus the
  * workspace and bit-identical results.

@@ -12,7 +12,7 @@ CSRC = PKG / "csrc"
 INCLUDE = ROOT / "include"
 BUILD = PKG / "_build"
 LIB = PKG / "libdominotree.so"
-SOURCES = ["topm.cu", "build_trees.cu", "build_small.cu", "build_marginal.cu", "accept.cu", "lmhead_topm.cu", "api.cu"]
+SOURCES = ["topm.cu", "build_trees.cu", "build_small.cu", "build_marginal.cu", "accept.cu", "lmhead_topm.cu", "tree_attn.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

@@ -1,0 +1,316 @@
+// dt_tree_attention — the verify pass's attention over the prefix and the draft tree with the ancestor-only mask.
+//
+// Method: blog.captcha.la, "Methodology — deep read" (the prefix-closed tree is verified in a single target forward
+// pass with an unmodified ancestor-only causal mask, borrowed from DDTree/SpecInfer); gist.science, "Composants
+// Clés — Vérification" (standard tree attention, unchanged and lossless). For request b, query head h and tree node
+// i the visible keys are the L prefix positions and the tree positions L + t with mask[b][i][t] = 1;
+// out = softmax(scale q.k) v over them; query head h reads key/value head h / (Hq / Hkv).
+//
+// GB300 design (flash decoding): the n tree nodes of the G = Hq / Hkv query heads that share a key/value head are
+// one block of G n <= 64 query rows, so each key and value row is read once per (request, key/value head) and feeds
+// 64 rows of dot products: a dense contraction on the tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate).
+// The keys of a (request, key/value head) are split into chunks so that the grid covers the SMs; a CTA streams its
+// chunk's key and value rows through a double-buffered cp.async ring in blocks of 64, keeps the running max and sum
+// of every row (online softmax, base 2) and its unnormalised output in registers, and writes them as a partial; a
+// second launch combines the chunks of each row. Memory bound: the key and value rows of the prefix are the bytes.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+
+#include "dt_internal.cuh"
+
+namespace dt {
+namespace {
+
+constexpr int kD = 128;           // head dimension
+constexpr int kRows = 64;         // query rows per CTA: G x n, padded
+constexpr int kBlockKeys = 64;    // keys per ring stage
+constexpr int kThreadsA = 128;    // four warps, 16 query rows each
+constexpr int kPitch = kD + 8;    // shared-memory row pitch in bf16 (272 bytes: conflict-free ldmatrix)
+constexpr int kMaxNodes = 64;
+
+struct TaParams {
+  int B, n, L, T, Hq, Hkv, G, R, nch, chunk;
+  const unsigned short* q;   // [B][n][Hq][kD] bf16
+  const unsigned short* k;   // [B][Hkv][T][kD] bf16
+  const unsigned short* v;   // [B][Hkv][T][kD] bf16
+  const uint8_t* mask;       // [B][n][n]
+  float scale_log2;          // scale * log2(e)
+  float* part;               // [units][kRows][kD] unnormalised outputs
+  float* ml;                 // [units][kRows][2] running max (base 2) and sum
+  float* out;                // [B][n][Hq][kD]
+};
+
+struct TaSmem {
+  __nv_bfloat16 q[kRows * kPitch];
+  __nv_bfloat16 k[2][kBlockKeys * kPitch];
+  __nv_bfloat16 v[2][kBlockKeys * kPitch];
+  uint8_t mask[kMaxNodes * kMaxNodes];
+};
+
+__device__ __forceinline__ void cp16(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(const void* p, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x4_t(const void* p, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Key and value rows [k0, k0 + 64) of one (request, key/value head) into ring stage s; rows past T read as zero.
+__device__ __forceinline__ void load_kv(const TaParams& p, TaSmem& S, int s, size_t kvbase, int k0) {
+  for (int c = threadIdx.x; c < kBlockKeys * (kD / 8); c += kThreadsA) {
+    const int r = c >> 4, col = (c & 15) * 8, key = k0 + r;
+    const bool ok = key < p.T;
+    const size_t off = (kvbase + (ok ? key : 0)) * kD + col;
+    cp16(&S.k[s][r * kPitch + col], p.k + off, ok);
+    cp16(&S.v[s][r * kPitch + col], p.v + off, ok);
+  }
+}
+
+// One CTA per (request b, key/value head, key chunk): the partial attention of the chunk for the 64 query rows.
+__global__ void __launch_bounds__(kThreadsA) tree_attn_partial(TaParams p) {
+  extern __shared__ float4 smem_f4[];
+  TaSmem& S = *reinterpret_cast<TaSmem*>(smem_f4);
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31, g = lane >> 2, tq = lane & 3;
+  const int unit = blockIdx.x, chunk = unit % p.nch, pair = unit / p.nch, b = pair / p.Hkv, kvh = pair % p.Hkv;
+  const int k0 = chunk * p.chunk, k1 = min(k0 + p.chunk, p.T);
+  const size_t kvbase = (static_cast<size_t>(b) * p.Hkv + kvh) * p.T;
+  // query row r = gi n + i: query head kvh G + gi, tree node i (rows >= R read as zero)
+  for (int c = t; c < kRows * (kD / 8); c += kThreadsA) {
+    const int r = c >> 4, col = (c & 15) * 8;
+    const bool ok = r < p.R;
+    const int gi = ok ? r / p.n : 0, i = ok ? r % p.n : 0;
+    cp16(&S.q[r * kPitch + col], p.q + ((static_cast<size_t>(b) * p.n + i) * p.Hq + kvh * p.G + gi) * kD + col, ok);
+  }
+  for (int c = t; c < p.n * p.n; c += kThreadsA) S.mask[c] = p.mask[static_cast<size_t>(b) * p.n * p.n + c];
+  const int nblk = (k1 - k0 + kBlockKeys - 1) / kBlockKeys;
+  load_kv(p, S, 0, kvbase, k0);
+  asm volatile("cp.async.commit_group;" ::: "memory");
+
+  const int rw0 = 16 * warp + g, rw1 = rw0 + 8;  // this thread's two query rows
+  const int node0 = rw0 < p.R ? rw0 % p.n : -1, node1 = rw1 < p.R ? rw1 % p.n : -1;
+  float o[16][4];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  uint32_t qa[kD / 16][4];
+  for (int blk = 0; blk < nblk; ++blk) {
+    if (blk + 1 < nblk) load_kv(p, S, (blk + 1) & 1, kvbase, k0 + (blk + 1) * kBlockKeys);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+    __syncthreads();
+    if (blk == 0) {  // the warp's 16 query rows as A fragments, for the whole chunk
+#pragma unroll
+      for (int ks = 0; ks < kD / 16; ++ks)
+        ldsm_x4(&S.q[(16 * warp + (lane & 15)) * kPitch + ks * 16 + (lane >> 4) * 8], qa[ks][0], qa[ks][1],
+                qa[ks][2], qa[ks][3]);
+    }
+    const __nv_bfloat16* Ks = S.k[blk & 1];
+    const __nv_bfloat16* Vs = S.v[blk & 1];
+    // S = Q K^T for the block's 64 keys: 8 tiles of 8 keys
+    float s[8][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < kD / 16; ++ks) {
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(&Ks[(np * 16 + (lane & 7) + ((lane >> 4) << 3)) * kPitch + ks * 16 + ((lane >> 3) & 1) * 8], b0, b1,
+                b2, b3);
+        mma_bf16(s[2 * np], qa[ks], b0, b1);
+        mma_bf16(s[2 * np + 1], qa[ks], b2, b3);
+      }
+    }
+    // mask and scale (base 2), the rows' running maxima
+    const int kb = k0 + blk * kBlockKeys;
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int key = kb + nt * 8 + tq * 2 + e;
+        const bool in = key < k1;
+        const bool v0 = in && node0 >= 0 && (key < p.L || S.mask[node0 * p.n + (key - p.L)] != 0);
+        const bool v1 = in && node1 >= 0 && (key < p.L || S.mask[node1 * p.n + (key - p.L)] != 0);
+        s[nt][e] = v0 ? s[nt][e] * p.scale_log2 : -INFINITY;
+        s[nt][2 + e] = v1 ? s[nt][2 + e] * p.scale_log2 : -INFINITY;
+        mx0 = fmaxf(mx0, s[nt][e]);
+        mx1 = fmaxf(mx1, s[nt][2 + e]);
+      }
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 2));
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float a0 = mn0 == -INFINITY ? 1.f : exp2f(m0 - mn0), a1 = mn1 == -INFINITY ? 1.f : exp2f(m1 - mn1);
+    float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        s[nt][e] = mn0 == -INFINITY ? 0.f : exp2f(s[nt][e] - mn0);
+        s[nt][2 + e] = mn1 == -INFINITY ? 0.f : exp2f(s[nt][2 + e] - mn1);
+        ls0 += s[nt][e];
+        ls1 += s[nt][2 + e];
+      }
+    }
+    l0 = l0 * a0 + ls0;  // this thread's share of the row sums (the quad adds them up at the end)
+    l1 = l1 * a1 + ls1;
+    m0 = mn0;
+    m1 = mn1;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      o[j][0] *= a0;
+      o[j][1] *= a0;
+      o[j][2] *= a1;
+      o[j][3] *= a1;
+    }
+    // O += P V: P from the score registers (bf16), V by transposed ldmatrix
+#pragma unroll
+    for (int kp = 0; kp < 4; ++kp) {
+      const uint32_t pa[4] = {pack_bf16(s[2 * kp][0], s[2 * kp][1]), pack_bf16(s[2 * kp][2], s[2 * kp][3]),
+                              pack_bf16(s[2 * kp + 1][0], s[2 * kp + 1][1]),
+                              pack_bf16(s[2 * kp + 1][2], s[2 * kp + 1][3])};
+#pragma unroll
+      for (int dp = 0; dp < kD / 16; ++dp) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(&Vs[(kp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * kPitch + dp * 16 + (lane >> 4) * 8], b0, b1,
+                  b2, b3);
+        mma_bf16(o[2 * dp], pa, b0, b1);
+        mma_bf16(o[2 * dp + 1], pa, b2, b3);
+      }
+    }
+    __syncthreads();  // the stage is refilled by the load two blocks on
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 1);
+  l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 2);
+  l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 1);
+  l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 2);
+  float* po = p.part + static_cast<size_t>(unit) * kRows * kD;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int col = j * 8 + tq * 2;
+    *reinterpret_cast<float2*>(po + rw0 * kD + col) = make_float2(o[j][0], o[j][1]);
+    *reinterpret_cast<float2*>(po + rw1 * kD + col) = make_float2(o[j][2], o[j][3]);
+  }
+  if (tq == 0) {
+    float* pm = p.ml + static_cast<size_t>(unit) * kRows * 2;
+    pm[rw0 * 2] = m0;
+    pm[rw0 * 2 + 1] = l0;
+    pm[rw1 * 2] = m1;
+    pm[rw1 * 2 + 1] = l1;
+  }
+}
+
+// One CTA per (request, key/value head), one thread per output column: the chunks' partials of every query row,
+// rescaled to the row's overall maximum and normalised by its overall sum.
+__global__ void __launch_bounds__(kD) tree_attn_combine(TaParams p) {
+  const int pair = blockIdx.x, b = pair / p.Hkv, kvh = pair % p.Hkv, dcol = threadIdx.x;
+  const size_t u0 = static_cast<size_t>(pair) * p.nch;
+  for (int r = 0; r < p.R; ++r) {
+    float mx = -INFINITY;
+    for (int c = 0; c < p.nch; ++c) mx = fmaxf(mx, p.ml[((u0 + c) * kRows + r) * 2]);
+    float num = 0.f, den = 0.f;
+    if (mx != -INFINITY) {
+      for (int c = 0; c < p.nch; ++c) {
+        const float* pm = p.ml + ((u0 + c) * kRows + r) * 2;
+        if (pm[0] == -INFINITY) continue;
+        const float w = exp2f(pm[0] - mx);
+        den += w * pm[1];
+        num += w * p.part[((u0 + c) * kRows + r) * kD + dcol];
+      }
+    }
+    const int gi = r / p.n, i = r % p.n;
+    p.out[((static_cast<size_t>(b) * p.n + i) * p.Hq + kvh * p.G + gi) * kD + dcol] = den > 0.f ? num / den : 0.f;
+  }
+}
+
+struct TaPlan {
+  int nch, chunk;
+  size_t part, ml, bytes;
+};
+inline TaPlan ta_plan(int B, int T, int Hkv, int sms) {
+  TaPlan P{};
+  const long long pairs = static_cast<long long>(B) * Hkv;
+  const int blocks = (T + kBlockKeys - 1) / kBlockKeys;
+  long long want = (2LL * sms + pairs - 1) / pairs;  // chunks per (request, key/value head): about two CTAs per SM
+  want = want < 1 ? 1 : (want > blocks ? blocks : want);
+  const int per = (blocks + static_cast<int>(want) - 1) / static_cast<int>(want);
+  P.chunk = per * kBlockKeys;
+  P.nch = (T + P.chunk - 1) / P.chunk;
+  const size_t units = static_cast<size_t>(pairs) * P.nch;
+  P.part = 0;
+  P.ml = align_up(sizeof(float) * units * kRows * kD);
+  P.bytes = align_up(P.ml + sizeof(float) * units * kRows * 2);
+  return P;
+}
+
+}  // namespace
+}  // namespace dt
+
+extern "C" size_t dt_tree_attention_workspace_bytes(int B, int n, int L, int Hq, int Hkv, int d) {
+  if (B < 1 || n < 1 || L < 0 || Hq < 1 || Hkv < 1 || d < 1) return 0;
+  dt::DeviceInfo di{};
+  if (dt::current_device_info(&di) != cudaSuccess) return 0;
+  return dt::ta_plan(B, L + n, Hkv, di.sms).bytes;
+}
+
+extern "C" dt_status dt_tree_attention(int B, int n, int L, int Hq, int Hkv, int d, const void* q, const void* k,
+                                       const void* v, dt_dtype dtype, const uint8_t* mask, float scale, float* out,
+                                       void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  using namespace dt;
+  if (B < 0 || n < 1 || L < 0 || Hq < 1 || Hkv < 1 || d < 1 || Hq % Hkv != 0) return DT_ERR_INVALID_ARG;
+  if (dtype != DT_F32 && dtype != DT_BF16) return DT_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return DT_ERR_INVALID_ARG;
+  if (B == 0) return DT_OK;
+  const void* ptrs[] = {q, k, v, out, workspace};
+  for (const void* x : ptrs)
+    if (!x || !aligned16(x)) return DT_ERR_INVALID_ARG;
+  if (!mask) return DT_ERR_INVALID_ARG;
+  const int G = Hq / Hkv;
+  if (dtype != DT_BF16 || d != kD || G * n > kRows || n > kMaxNodes) return DT_ERR_UNSUPPORTED;
+  if (static_cast<long long>(L) + n > INT_MAX / 2) return DT_ERR_UNSUPPORTED;
+  DeviceInfo di{};
+  if (current_device_info(&di) != cudaSuccess) return DT_ERR_CUDA;
+  const int T = L + n;
+  const TaPlan P = ta_plan(B, T, Hkv, di.sms);
+  if (workspace_bytes < P.bytes) return DT_ERR_INVALID_ARG;
+  const long long units = static_cast<long long>(B) * Hkv * P.nch;
+  if (units > INT_MAX || static_cast<long long>(B) * Hkv > INT_MAX) return DT_ERR_UNSUPPORTED;
+  TaParams p{};
+  p.B = B; p.n = n; p.L = L; p.T = T; p.Hq = Hq; p.Hkv = Hkv; p.G = G; p.R = G * n; p.nch = P.nch; p.chunk = P.chunk;
+  p.q = static_cast<const unsigned short*>(q);
+  p.k = static_cast<const unsigned short*>(k);
+  p.v = static_cast<const unsigned short*>(v);
+  p.mask = mask;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  char* ws = static_cast<char*>(workspace);
+  p.part = reinterpret_cast<float*>(ws + P.part);
+  p.ml = reinterpret_cast<float*>(ws + P.ml);
+  p.out = out;
+  const void* fa = reinterpret_cast<const void*>(tree_attn_partial);
+  if (ensure_dynamic_smem(fa, sizeof(TaSmem)) != cudaSuccess) return DT_ERR_CUDA;
+  tree_attn_partial<<<static_cast<unsigned>(units), kThreadsA, sizeof(TaSmem), stream>>>(p);
+  tree_attn_combine<<<static_cast<unsigned>(B * Hkv), kD, 0, stream>>>(p);
+  return cuda_status(cudaGetLastError());
+}

@@ -58,6 +58,8 @@ SIGNATURES = {
                                      _P]),
     "dt_lmhead_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "dt_lmhead_topm": (_I, [_I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _SZ, _P]),
+    "dt_tree_attention_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "dt_tree_attention": (_I, [_I, _I, _I, _I, _I, _I, _P, _P, _P, _I, _P, ctypes.c_float, _P, _P, _SZ, _P]),
     "dt_get_error": (_I, [_P, _P]),
     "dt_set_barrier_timeout_ns": (None, [ctypes.c_uint64]),
     "dt_set_lookahead": (_I, [_I]),
@@ -187,6 +189,31 @@ def dt_lmhead_topm(hidden: torch.Tensor, w_head: torch.Tensor, M: int, out_ids: 
                                 _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream)),
            "dt_lmhead_topm")
     return out_ids, out_vals
+
+
+def dt_tree_attention_workspace_bytes(B: int, n: int, L: int, Hq: int, Hkv: int, d: int) -> int:
+    return int(lib().dt_tree_attention_workspace_bytes(B, n, L, Hq, Hkv, d))
+
+
+def dt_tree_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: torch.Tensor, scale: float,
+                      out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None, stream=None):
+    """The verify pass's tree attention: q [B,n,Hq,d], k/v [B,Hkv,L+n,d] (bf16), mask [B,n,n] uint8
+    -> out [B,n,Hq,d] fp32."""
+    B, n, Hq, d = q.shape
+    Hkv, T = k.shape[1], k.shape[2]
+    L = T - n
+    if out is None:
+        out = torch.empty((B, n, Hq, d), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(max(dt_tree_attention_workspace_bytes(B, n, L, Hq, Hkv, d), 256), dtype=torch.uint8,
+                                device=q.device)
+    _check(lib().dt_tree_attention(B, n, L, Hq, Hkv, d, _dev(q, "q", q.dtype, (B, n, Hq, d)),
+                                   _dev(k, "k", q.dtype, (B, Hkv, T, d)), _dev(v, "v", q.dtype, (B, Hkv, T, d)),
+                                   _code(q.dtype), _dev(mask, "mask", torch.uint8, (B, n, n)), float(scale),
+                                   _dev(out, "out", torch.float32, (B, n, Hq, d)),
+                                   _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream)),
+           "dt_tree_attention")
+    return out
 
 
 def dt_topm_static(logits: torch.Tensor, M: int, out_ids: Optional[torch.Tensor] = None,

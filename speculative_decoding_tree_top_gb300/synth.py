@@ -43,7 +43,8 @@ CONFIGS: Dict[int, dict] = {
 }
 
 STREAM = {"logits": 1, "boost_ids": 2, "boost_vals": 3, "h0": 4, "w_ih": 5, "w_hh": 6, "b_ih": 7, "b_hh": 8,
-          "emb": 9, "w_c": 10, "lmhead_hidden": 11, "lmhead_w": 12}
+          "emb": 9, "w_c": 10, "lmhead_hidden": 11, "lmhead_w": 12, "attn_q": 13, "attn_k": 14, "attn_v": 15,
+          "attn_tree": 16}
 
 
 @dataclass
@@ -227,3 +228,25 @@ def make_lmhead_inputs(R: int, D: int, V: int, device="cpu", seed: int = 4321):
     hidden = _normal((R, D), 1.0, "cpu", seed, "lmhead_hidden").to(torch.bfloat16)
     w_head = _normal((V, D), 1.0 / math.sqrt(D), "cpu", seed, "lmhead_w").to(torch.bfloat16)
     return hidden.to(device), w_head.to(device)
+
+
+def make_attention_inputs(B: int, n: int, L: int, Hq: int, Hkv: int, d: int, device="cpu", seed: int = 2468):
+    """The verify pass's attention inputs: queries of the n tree nodes [B,n,Hq,d], the key and value cache rows of
+    the L prefix positions and the n tree positions [B,Hkv,L+n,d] (all N(0,1) in fp32, cast to bf16), and the
+    ancestor masks [B,n,n] of random prefix-closed trees (node i's parent drawn uniformly among the root and the
+    nodes before it), the structure dt_build_trees emits."""
+    q = _normal((B, n, Hq, d), 1.0, "cpu", seed, "attn_q").to(torch.bfloat16)
+    k = _normal((B, Hkv, L + n, d), 1.0, "cpu", seed, "attn_k").to(torch.bfloat16)
+    v = _normal((B, Hkv, L + n, d), 1.0, "cpu", seed, "attn_v").to(torch.bfloat16)
+    g = _gen("cpu", seed, "attn_tree")
+    mask = torch.zeros((B, n, n), dtype=torch.uint8)
+    for b in range(B):
+        par = [-1]
+        for i in range(1, n):
+            par.append(int(torch.randint(-1, i, (1,), generator=g).item()))
+        for i in range(n):
+            j = i
+            while j >= 0:
+                mask[b, i, j] = 1
+                j = par[j]
+    return q.to(device), k.to(device), v.to(device), mask.to(device)

@@ -172,3 +172,24 @@ def test_lmhead_rejects_bad_arguments(dtlib):
     assert call(R=65) == UNSUPPORTED                  # the rows must fit the tensor-memory slice
     assert call(M=2000, V=5000) == UNSUPPORTED
     assert call(R=0) == OK
+
+
+def test_tree_attention_rejects_bad_arguments(dtlib):
+    f = dtlib.lib().dt_tree_attention
+    BF16, F32 = 1, 0
+
+    def call(B=1, n=16, L=100, Hq=32, Hkv=8, d=128, dtype=BF16, q=A, mask=A, scale=0.088, ws=A):
+        return f(B, n, L, Hq, Hkv, d, q, A, A, dtype, mask, scale, A, ws, 1 << 30, None)
+    assert call(Hq=30) == INVALID                     # not a multiple of the key/value heads
+    assert call(n=0) == INVALID
+    assert call(L=-1) == INVALID
+    assert call(scale=0.0) == INVALID
+    assert call(scale=float("nan")) == INVALID
+    assert call(q=None) == INVALID
+    assert call(q=A + 4) == INVALID                   # misaligned
+    assert call(mask=None) == INVALID
+    assert call(dtype=7) == INVALID
+    assert call(dtype=F32) == UNSUPPORTED             # the tensor-core path takes bf16
+    assert call(d=64) == UNSUPPORTED
+    assert call(n=17) == UNSUPPORTED                  # 4 query heads per key/value head x 17 nodes > 64 rows
+    assert call(B=0) == OK
