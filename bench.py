@@ -46,6 +46,9 @@ def parse():
                     help="also time dt_accept_paths on the round's trees (synthetic target tokens), reported apart")
     ap.add_argument("--with-lmhead", action="store_true",
                     help="also time dt_lmhead_topm (the projection fused with the top-M) against cuBLAS + dt_topm")
+    ap.add_argument("--with-attention", action="store_true",
+                    help="also time dt_tree_attention (the verify pass over a prefix and the tree) on the workload's batch")
+    ap.add_argument("--prefix", type=int, default=2048, help="prefix length of --with-attention")
     ap.add_argument("--builder", choices=["conditional", "marginal"], default="conditional",
                     help="conditional: dt_build_trees (the method); marginal: dt_build_trees_marginal (DDTree scoring)")
     ap.add_argument("--reference-budget", type=float, default=150.0, help="seconds for the whole reference arm")
@@ -361,6 +364,50 @@ def run_ours(args, world, rank, local):
             unfused_us=dict(cublas_projection=float(g_us.mean()), dt_topm=float(t_us.mean()),
                             total=float((g_us + t_us).mean())),
             ids_shared_with_unfused=round(common, 4), sources=["lmhead_topm.cu", "topm_select.cuh", "umma.cuh"])
+
+    if args.with_attention:
+        # The target's verify pass over the accepted prefix and the n tree nodes, Qwen3-4B's attention shape (32
+        # query heads over 8 key/value heads, d = 128), with the ancestor masks of this step's own trees; against
+        # torch's scaled_dot_product_attention with the same boolean mask (context).
+        Hq, Hkv, d, Lp = 32, 8, 128, args.prefix
+        aq, ak, av, _ = (t.to(dev) for t in synth.make_attention_inputs(s.B, s.n, Lp, Hq, Hkv, d, seed=99 + rank))
+        amask = rnd.out["mask"]
+        aws = torch.empty(dt.dt_tree_attention_workspace_bytes(s.B, s.n, Lp, Hq, Hkv, d), dtype=torch.uint8, device=dev)
+        aout = torch.empty((s.B, s.n, Hq, d), dtype=torch.float32, device=dev)
+        scale = 1.0 / math.sqrt(d)
+        bm = torch.ones((s.B, 1, s.n, Lp + s.n), dtype=torch.bool, device=dev)
+        bm[:, 0, :, Lp:] = amask.bool()
+        qt = aq.permute(0, 2, 1, 3)
+
+        def sdpa():
+            return torch.nn.functional.scaled_dot_product_attention(qt, ak, av, attn_mask=bm, scale=scale,
+                                                                    enable_gqa=True)
+
+        for _ in range(args.warmup):
+            dt.dt_tree_attention(aq, ak, av, amask, scale, aout, aws, stream)
+            sdpa()
+        steps = max(20, min(args.steps, 200))
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        torch.cuda.synchronize()
+        for e in ev:
+            flush_l2()
+            e[0].record(stream)
+            dt.dt_tree_attention(aq, ak, av, amask, scale, aout, aws, stream)
+            e[1].record(stream)
+            flush_l2()
+            e[2].record(stream)
+            sdpa()
+            e[3].record(stream)
+        torch.cuda.synchronize()
+        a_us = np.array([e[0].elapsed_time(e[1]) for e in ev]) * 1e3
+        s_us = np.array([e[2].elapsed_time(e[3]) for e in ev]) * 1e3
+        abytes = 2 * s.B * Hkv * (Lp + s.n) * d * 2 + s.B * s.n * Hq * d * (2 + 4) + s.B * s.n * s.n
+        diff = float((sdpa().permute(0, 2, 1, 3).float() - aout).abs().max().item())
+        kernels["dt_tree_attention"] = dict(
+            us=float(a_us.mean()), bytes=abytes, gbps=abytes / (a_us.mean() * 1e3),
+            frac_of_hbm_peak=round(abytes / (a_us.mean() * 1e3) / peak, 4), prefix=Lp, heads=[Hq, Hkv, d],
+            torch_sdpa_us=float(s_us.mean()), max_abs_diff_vs_sdpa=round(diff, 5),
+            sources=["tree_attn.cu"])
 
     e2e = None
     if not args.no_e2e and not marginal:

@@ -10,7 +10,8 @@
 // one block of G n <= 64 query rows, so each key and value row is read once per (request, key/value head) and feeds
 // 64 rows of dot products: a dense contraction on the tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate).
 // The keys of a (request, key/value head) are split into chunks so that the grid covers the SMs; a CTA streams its
-// chunk's key and value rows through a double-buffered cp.async ring in blocks of 64, keeps the running max and sum
+// chunk's key and value rows through a double-buffered cp.async ring in blocks of 32 (55 KB and 128 registers:
+// four CTAs per SM), keeps the running max and sum
 // of every row (online softmax, base 2) and its unnormalised output in registers, and writes them as a partial; a
 // second launch combines the chunks of each row. Memory bound: the key and value rows of the prefix are the bytes.
 #include <cuda_bf16.h>
@@ -26,7 +27,7 @@ namespace {
 
 constexpr int kD = 128;           // head dimension
 constexpr int kRows = 64;         // query rows per CTA: G x n, padded
-constexpr int kBlockKeys = 64;    // keys per ring stage
+constexpr int kBlockKeys = 32;    // keys per ring stage (small: four CTAs fit an SM)
 constexpr int kThreadsA = 128;    // four warps, 16 query rows each
 constexpr int kPitch = kD + 8;    // shared-memory row pitch in bf16 (272 bytes: conflict-free ldmatrix)
 constexpr int kMaxNodes = 64;
@@ -76,7 +77,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // Key and value rows [k0, k0 + 64) of one (request, key/value head) into ring stage s; rows past T read as zero.
 __device__ __forceinline__ void load_kv(const TaParams& p, TaSmem& S, int s, size_t kvbase, int k0) {
   for (int c = threadIdx.x; c < kBlockKeys * (kD / 8); c += kThreadsA) {
-    const int r = c >> 4, col = (c & 15) * 8, key = k0 + r;
+    const int r = c >> 4, col = (c & 15) * 8, key = k0 + r;  // 16 chunks of 16 bytes per row
     const bool ok = key < p.T;
     const size_t off = (kvbase + (ok ? key : 0)) * kD + col;
     cp16(&S.k[s][r * kPitch + col], p.k + off, ok);
@@ -85,7 +86,7 @@ __device__ __forceinline__ void load_kv(const TaParams& p, TaSmem& S, int s, siz
 }
 
 // One CTA per (request b, key/value head, key chunk): the partial attention of the chunk for the 64 query rows.
-__global__ void __launch_bounds__(kThreadsA) tree_attn_partial(TaParams p) {
+__global__ void __launch_bounds__(kThreadsA, 4) tree_attn_partial(TaParams p) {
   extern __shared__ float4 smem_f4[];
   TaSmem& S = *reinterpret_cast<TaSmem*>(smem_f4);
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31, g = lane >> 2, tq = lane & 3;
@@ -110,40 +111,36 @@ __global__ void __launch_bounds__(kThreadsA) tree_attn_partial(TaParams p) {
 #pragma unroll
   for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  uint32_t qa[kD / 16][4];
   for (int blk = 0; blk < nblk; ++blk) {
     if (blk + 1 < nblk) load_kv(p, S, (blk + 1) & 1, kvbase, k0 + (blk + 1) * kBlockKeys);
     asm volatile("cp.async.commit_group;" ::: "memory");
     asm volatile("cp.async.wait_group 1;" ::: "memory");
     __syncthreads();
-    if (blk == 0) {  // the warp's 16 query rows as A fragments, for the whole chunk
-#pragma unroll
-      for (int ks = 0; ks < kD / 16; ++ks)
-        ldsm_x4(&S.q[(16 * warp + (lane & 15)) * kPitch + ks * 16 + (lane >> 4) * 8], qa[ks][0], qa[ks][1],
-                qa[ks][2], qa[ks][3]);
-    }
     const __nv_bfloat16* Ks = S.k[blk & 1];
     const __nv_bfloat16* Vs = S.v[blk & 1];
-    // S = Q K^T for the block's 64 keys: 8 tiles of 8 keys
-    float s[8][4];
+    // S = Q K^T for the block's keys: tiles of 8 keys; the warp's 16 query rows re-read as A fragments per K step
+    constexpr int kNT = kBlockKeys / 8;
+    float s[kNT][4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+    for (int j = 0; j < kNT; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < kD / 16; ++ks) {
+      uint32_t qa[4];
+      ldsm_x4(&S.q[(16 * warp + (lane & 15)) * kPitch + ks * 16 + (lane >> 4) * 8], qa[0], qa[1], qa[2], qa[3]);
 #pragma unroll
-      for (int np = 0; np < 4; ++np) {
+      for (int np = 0; np < kNT / 2; ++np) {
         uint32_t b0, b1, b2, b3;
         ldsm_x4(&Ks[(np * 16 + (lane & 7) + ((lane >> 4) << 3)) * kPitch + ks * 16 + ((lane >> 3) & 1) * 8], b0, b1,
                 b2, b3);
-        mma_bf16(s[2 * np], qa[ks], b0, b1);
-        mma_bf16(s[2 * np + 1], qa[ks], b2, b3);
+        mma_bf16(s[2 * np], qa, b0, b1);
+        mma_bf16(s[2 * np + 1], qa, b2, b3);
       }
     }
     // mask and scale (base 2), the rows' running maxima
     const int kb = k0 + blk * kBlockKeys;
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
+    for (int nt = 0; nt < kNT; ++nt) {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int key = kb + nt * 8 + tq * 2 + e;
@@ -164,7 +161,7 @@ __global__ void __launch_bounds__(kThreadsA) tree_attn_partial(TaParams p) {
     const float a0 = mn0 == -INFINITY ? 1.f : exp2f(m0 - mn0), a1 = mn1 == -INFINITY ? 1.f : exp2f(m1 - mn1);
     float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
+    for (int nt = 0; nt < kNT; ++nt) {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         s[nt][e] = mn0 == -INFINITY ? 0.f : exp2f(s[nt][e] - mn0);
@@ -186,7 +183,7 @@ __global__ void __launch_bounds__(kThreadsA) tree_attn_partial(TaParams p) {
     }
     // O += P V: P from the score registers (bf16), V by transposed ldmatrix
 #pragma unroll
-    for (int kp = 0; kp < 4; ++kp) {
+    for (int kp = 0; kp < kBlockKeys / 16; ++kp) {
       const uint32_t pa[4] = {pack_bf16(s[2 * kp][0], s[2 * kp][1]), pack_bf16(s[2 * kp][2], s[2 * kp][3]),
                               pack_bf16(s[2 * kp + 1][0], s[2 * kp + 1][1]),
                               pack_bf16(s[2 * kp + 1][2], s[2 * kp + 1][3])};
@@ -222,27 +219,48 @@ __global__ void __launch_bounds__(kThreadsA) tree_attn_partial(TaParams p) {
   }
 }
 
-// One CTA per (request, key/value head), one thread per output column: the chunks' partials of every query row,
-// rescaled to the row's overall maximum and normalised by its overall sum.
+// One CTA per (request, key/value head, query row), one thread per output column: the chunks' partials of the row,
+// rescaled to its overall maximum and normalised by its overall sum. The chunks' weights are found once per CTA.
+constexpr int kMaxChunks = 1024;
 __global__ void __launch_bounds__(kD) tree_attn_combine(TaParams p) {
-  const int pair = blockIdx.x, b = pair / p.Hkv, kvh = pair % p.Hkv, dcol = threadIdx.x;
+  __shared__ float s_w[kMaxChunks];
+  __shared__ float s_red[kD / 32];
+  __shared__ float s_den;
+  const int r = blockIdx.x % p.R, pair = blockIdx.x / p.R, b = pair / p.Hkv, kvh = pair % p.Hkv;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const size_t u0 = static_cast<size_t>(pair) * p.nch;
-  for (int r = 0; r < p.R; ++r) {
-    float mx = -INFINITY;
-    for (int c = 0; c < p.nch; ++c) mx = fmaxf(mx, p.ml[((u0 + c) * kRows + r) * 2]);
-    float num = 0.f, den = 0.f;
-    if (mx != -INFINITY) {
-      for (int c = 0; c < p.nch; ++c) {
-        const float* pm = p.ml + ((u0 + c) * kRows + r) * 2;
-        if (pm[0] == -INFINITY) continue;
-        const float w = exp2f(pm[0] - mx);
-        den += w * pm[1];
-        num += w * p.part[((u0 + c) * kRows + r) * kD + dcol];
-      }
-    }
-    const int gi = r / p.n, i = r % p.n;
-    p.out[((static_cast<size_t>(b) * p.n + i) * p.Hq + kvh * p.G + gi) * kD + dcol] = den > 0.f ? num / den : 0.f;
+  float mx = -INFINITY;
+  for (int c = t; c < p.nch; c += kD) mx = fmaxf(mx, p.ml[((u0 + c) * kRows + r) * 2]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+  if (lane == 0) s_red[warp] = mx;
+  __syncthreads();
+  mx = s_red[0];
+#pragma unroll
+  for (int w = 1; w < kD / 32; ++w) mx = fmaxf(mx, s_red[w]);
+  __syncthreads();
+  float den = 0.f;
+  for (int c = t; c < p.nch; c += kD) {
+    const float* pm = p.ml + ((u0 + c) * kRows + r) * 2;
+    const float w = (mx == -INFINITY || pm[0] == -INFINITY) ? 0.f : exp2f(pm[0] - mx);
+    s_w[c] = w;
+    den += w * pm[1];
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xFFFFFFFFu, den, o);
+  if (lane == 0) s_red[warp] = den;
+  __syncthreads();
+  if (t == 0) {
+    float d0 = 0.f;
+#pragma unroll
+    for (int w = 0; w < kD / 32; ++w) d0 += s_red[w];
+    s_den = d0;
+  }
+  __syncthreads();
+  float num = 0.f;
+  for (int c = 0; c < p.nch; ++c) num += s_w[c] * p.part[((u0 + c) * kRows + r) * kD + t];
+  const int gi = r / p.n, i = r % p.n;
+  p.out[((static_cast<size_t>(b) * p.n + i) * p.Hq + kvh * p.G + gi) * kD + t] = s_den > 0.f ? num / s_den : 0.f;
 }
 
 struct TaPlan {
@@ -253,7 +271,7 @@ inline TaPlan ta_plan(int B, int T, int Hkv, int sms) {
   TaPlan P{};
   const long long pairs = static_cast<long long>(B) * Hkv;
   const int blocks = (T + kBlockKeys - 1) / kBlockKeys;
-  long long want = (2LL * sms + pairs - 1) / pairs;  // chunks per (request, key/value head): about two CTAs per SM
+  long long want = (4LL * sms + pairs - 1) / pairs;  // chunks per (request, key/value head): four CTAs per SM
   want = want < 1 ? 1 : (want > blocks ? blocks : want);
   const int per = (blocks + static_cast<int>(want) - 1) / static_cast<int>(want);
   P.chunk = per * kBlockKeys;
@@ -296,7 +314,8 @@ extern "C" dt_status dt_tree_attention(int B, int n, int L, int Hq, int Hkv, int
   const TaPlan P = ta_plan(B, T, Hkv, di.sms);
   if (workspace_bytes < P.bytes) return DT_ERR_INVALID_ARG;
   const long long units = static_cast<long long>(B) * Hkv * P.nch;
-  if (units > INT_MAX || static_cast<long long>(B) * Hkv > INT_MAX) return DT_ERR_UNSUPPORTED;
+  if (units > INT_MAX || static_cast<long long>(B) * Hkv * G * n > INT_MAX || P.nch > kMaxChunks)
+    return DT_ERR_UNSUPPORTED;
   TaParams p{};
   p.B = B; p.n = n; p.L = L; p.T = T; p.Hq = Hq; p.Hkv = Hkv; p.G = G; p.R = G * n; p.nch = P.nch; p.chunk = P.chunk;
   p.q = static_cast<const unsigned short*>(q);
@@ -311,6 +330,6 @@ extern "C" dt_status dt_tree_attention(int B, int n, int L, int Hq, int Hkv, int
   const void* fa = reinterpret_cast<const void*>(tree_attn_partial);
   if (ensure_dynamic_smem(fa, sizeof(TaSmem)) != cudaSuccess) return DT_ERR_CUDA;
   tree_attn_partial<<<static_cast<unsigned>(units), kThreadsA, sizeof(TaSmem), stream>>>(p);
-  tree_attn_combine<<<static_cast<unsigned>(B * Hkv), kD, 0, stream>>>(p);
+  tree_attn_combine<<<static_cast<unsigned>(static_cast<long long>(B) * Hkv * p.R), kD, 0, stream>>>(p);
   return cuda_status(cudaGetLastError());
 }
