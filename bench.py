@@ -131,8 +131,8 @@ def measured_peaks():
 
 # The sources each C-ABI call is built from: a committed ncu figure counts only while they are unchanged.
 CALL_SOURCES = {
-    "dt_topm": ["topm.cu", "dt_internal.cuh"],
-    "dt_build_trees": ["build_trees.cu", "build_small.cu", "build_common.cuh", "dt_internal.cuh"],
+    "dt_topm": ["topm.cu", "topm_select.cuh", "dt_internal.cuh"],
+    "dt_build_trees": ["build_trees.cu", "build_small.cu", "build_common.cuh", "umma.cuh", "dt_internal.cuh"],
 }
 
 
