@@ -46,8 +46,9 @@ struct Job {
 // Warp-wide best of one candidate per lane (`has` false: none), in pop order: higher score (-0.0 equal to +0.0),
 // then lower token, then lower insertion index, then lower lane. One warp reduction picks the lane when the best
 // score is held by one lane only (the common case); ties take two more reductions. Returns the lane (-1 if no lane
-// has a candidate) and leaves its node in `e` and its `dep` value in every lane.
-__device__ __forceinline__ int warp_best(bool has, Node& e, int& dep) {
+// has a candidate) and gives every lane the winner's `word` in `won` (one shuffle: the walk needs only a packed
+// summary of the winner in every lane; the winning lane still holds its whole node).
+__device__ __forceinline__ int warp_pick(bool has, const Node& e, uint32_t word, uint32_t& won) {
   const uint32_t sk = has ? key_of_f32(__float_as_uint(e.score)) : 0u;  // keys of real scores are >= 1
   const uint32_t ms = __reduce_max_sync(0xFFFFFFFFu, sk);
   if (ms == 0u) return -1;
@@ -63,14 +64,15 @@ __device__ __forceinline__ int warp_best(bool has, Node& e, int& dep) {
     const bool c3 = c2 && static_cast<uint32_t>(e.seq) == mq;
     wl = __ffs(__ballot_sync(0xFFFFFFFFu, c3)) - 1;
   }
-  e.score = __shfl_sync(0xFFFFFFFFu, e.score, wl);
-  e.token = __shfl_sync(0xFFFFFFFFu, e.token, wl);
-  e.seq = __shfl_sync(0xFFFFFFFFu, e.seq, wl);
-  e.pslot = static_cast<short>(__shfl_sync(0xFFFFFFFFu, static_cast<int>(e.pslot), wl));
-  e.xslot = static_cast<short>(__shfl_sync(0xFFFFFFFFu, static_cast<int>(e.xslot), wl));
-  dep = __shfl_sync(0xFFFFFFFFu, dep, wl);
+  won = __shfl_sync(0xFFFFFFFFu, word, wl);
   return wl;
 }
+// The winner's summary: its expansion slot (-1: not expanded) in the low half, its depth in the high half.
+__device__ __forceinline__ uint32_t pick_word(int xslot, int depth) {
+  return (static_cast<uint32_t>(xslot) & 0xFFFFu) | (static_cast<uint32_t>(depth) << 16);
+}
+__device__ __forceinline__ int word_xslot(uint32_t w) { return static_cast<int>(static_cast<short>(w & 0xFFFFu)); }
+__device__ __forceinline__ int word_depth(uint32_t w) { return static_cast<int>(w >> 16); }
 
 // A request's best-first bookkeeping.
 struct ReqCtl {
@@ -157,24 +159,28 @@ __device__ inline void request_step(const ReqView& R, int b, int n, int M, int m
   Node* mg = R.merged + static_cast<size_t>(st.fb) * n;
   Cursor cu;
   cursor_load(R, ls, mg, KM, cu);
-  // the depth of a candidate: its list's, or (merged list) one more than its parent's
-  auto depth_of = [&](const Node& e, int dep) { return dep >= 0 ? dep : R.sdepth[e.pslot] + 1; };
+  // the depth of a lane's head: its list's, or (merged list) one more than its parent's; found by every lane at once,
+  // so that only the winner's (with its expansion slot) travels in the pick's one shuffle
+  auto head_depth = [&](const Cursor& c, const LaneSrc& q) {
+    return c.has ? (q.dep >= 0 ? q.dep : R.sdepth[c.hd.pslot] + 1) : 0;
+  };
   while (st.s < n) {
-    Node e = cu.hd;
-    int dep = ls.dep;
-    const int wl = warp_best(cu.has, e, dep);
+    uint32_t won;
+    const int wl = warp_pick(cu.has, cu.hd, pick_word(cu.hd.xslot, head_depth(cu, ls)), won);
     if (wl < 0) {  // unreachable when n <= the size of the depth-limited tree (checked on the host)
       if (lane == 0) record_error(hdr, DT_ERR_INVALID_ARG);
       break;
     }
-    const int depth = depth_of(e, dep);
+    const int depth = word_depth(won), xs = word_xslot(won);
     const bool need = (st.s + 1 < n) && (depth < maxd);
-    if (need && e.xslot < 0) break;  // its children are not known yet: the next wave expands it
-    if (lane == 0) R.pops[st.s] = PopRec{e.token, e.pslot, depth, e.score};
-    if (lane == wl) cursor_advance(R, ls, mg, KM, cu);
+    if (need && xs < 0) break;  // its children are not known yet: the next wave expands it
+    if (lane == wl) {  // the winning lane records the pop and moves on in its list
+      R.pops[st.s] = PopRec{cu.hd.token, cu.hd.pslot, depth, cu.hd.score};
+      if (need) R.popidx[xs] = st.s;
+      cursor_advance(R, ls, mg, KM, cu);
+    }
     if (need) {
-      const int x = e.xslot;
-      if (lane == 0) R.popidx[x] = st.s;
+      const int x = xs;
       const int kc = R.kcount[x];
       if (kc > 0) {
         unsigned idle = __ballot_sync(0xFFFFFFFFu, lane > 0 && !cu.has);
@@ -243,36 +249,39 @@ __device__ inline void request_step(const ReqView& R, int b, int n, int M, int m
     Cursor sc = cu;
     int sseq = st.seq_next;
     for (int sim = st.s; sim < n - 1 && njobs < kla; ++sim) {
-      Node e = sc.hd;
-      int dep = ss.dep;
-      const int wl = warp_best(sc.has, e, dep);
+      uint32_t won;
+      const int wl = warp_pick(sc.has, sc.hd, pick_word(sc.hd.xslot, head_depth(sc, ss)), won);
       if (wl < 0) break;
-      const int depth = depth_of(e, dep);
-      if (depth < maxd && e.xslot < 0) {
+      const int depth = word_depth(won), xs = word_xslot(won);
+      const bool pick = depth < maxd && xs < 0;
+      if (pick) {
         const bool allowed = njobs == 0 || st.next_slot + 1 + (n - 1 - st.s) <= X;
         if (!allowed || st.next_slot >= X) break;
-        const int x = st.next_slot++;
-        if (lane == wl) {  // mark the node as expanded in the list it lives in
+      }
+      if (lane == wl) {  // the winning lane takes the pick (if any) and moves on in its list
+        if (pick) {
+          const int x = st.next_slot;
           Node* at = ss.src == -2 ? mg + ss.idx : R.kids + static_cast<size_t>(ss.src) * KM + ss.idx;
-          at->xslot = static_cast<short>(x);
-        }
-        if (lane == 0) {
+          at->xslot = static_cast<short>(x);  // marked as expanded in the list it lives in
           R.sdepth[x] = depth;
           R.popidx[x] = -2;
           R.kcount[x] = 0;
-          jobs_out[njobs] = Job{b, x, e.pslot, e.token, depth, e.score, {0, 0}};
+          jobs_out[njobs] = Job{b, x, sc.hd.pslot, sc.hd.token, depth, sc.hd.score, {0, 0}};
         }
+        cursor_advance(R, ss, mg, KM, sc);
+      }
+      if (pick) {
+        ++st.next_slot;
         ++njobs;
       }
-      if (lane == wl) cursor_advance(R, ss, mg, KM, sc);
-      if (depth < maxd && e.xslot >= 0) {  // expanded but not popped: its children join the walk
-        const int kc = R.kcount[e.xslot];
+      if (depth < maxd && xs >= 0) {  // expanded but not popped: its children join the walk
+        const int kc = R.kcount[xs];
         if (kc > 0) {
           const unsigned idle = __ballot_sync(0xFFFFFFFFu, lane > 0 && !sc.has);
           if (idle == 0u) break;
           const int nl = __ffs(idle) - 1;
           if (lane == nl) {
-            ss = LaneSrc{e.xslot, 0, kc, sseq, depth + 1, {0, 0, 0}};
+            ss = LaneSrc{xs, 0, kc, sseq, depth + 1, {0, 0, 0}};
             cursor_load(R, ss, mg, KM, sc);
           }
         }
