@@ -9,11 +9,11 @@
 // GB300 design (flash decoding): the n tree nodes of the G = Hq / Hkv query heads that share a key/value head are
 // one block of G n <= 64 query rows, so each key and value row is read once per (request, key/value head) and feeds
 // 64 rows of dot products: a dense contraction on the tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate).
-// The keys of a (request, key/value head) are split into chunks so that the grid covers the SMs; a CTA streams its
-// chunk's key and value rows through a double-buffered cp.async ring in blocks of 32 (55 KB and 128 registers:
-// four CTAs per SM), keeps the running max and sum
-// of every row (online softmax, base 2) and its unnormalised output in registers, and writes them as a partial; a
-// second launch combines the chunks of each row. Memory bound: the key and value rows of the prefix are the bytes.
+// The key blocks of all (request, key/value head) pairs, flattened, are split evenly over four CTAs per SM (a CTA's
+// share may span two pairs: one segment each); a CTA streams a segment's key and value rows through a two-stage
+// cp.async ring in blocks of 32 (55 KB, 128 registers), keeps the running max and sum of every query row
+// (online softmax, base 2) and its unnormalised output in registers, and writes them as the segment's partial; a
+// second launch combines the segments of each row. Memory bound: the key and value rows are the bytes.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -31,23 +31,27 @@ constexpr int kBlockKeys = 32;    // keys per ring stage (small: four CTAs fit a
 constexpr int kThreadsA = 128;    // four warps, 16 query rows each
 constexpr int kPitch = kD + 8;    // shared-memory row pitch in bf16 (272 bytes: conflict-free ldmatrix)
 constexpr int kMaxNodes = 64;
+constexpr int kStagesA = 2;      // key/value ring stages: one block in flight while one is consumed
 
 struct TaParams {
-  int B, n, L, T, Hq, Hkv, G, R, nch, chunk;
+  int B, n, L, T, Hq, Hkv, G, R;
+  int nb;              // key blocks of 32 per (request, key/value head)
+  int grid, maxseg;    // CTAs of the partial launch; partial slots per (request, key/value head)
+  long long work;      // all key blocks: (B Hkv) nb, split evenly over the CTAs
   const unsigned short* q;   // [B][n][Hq][kD] bf16
   const unsigned short* k;   // [B][Hkv][T][kD] bf16
   const unsigned short* v;   // [B][Hkv][T][kD] bf16
   const uint8_t* mask;       // [B][n][n]
   float scale_log2;          // scale * log2(e)
-  float* part;               // [units][kRows][kD] unnormalised outputs
-  float* ml;                 // [units][kRows][2] running max (base 2) and sum
+  float* part;               // [B Hkv][maxseg][kRows][kD] unnormalised outputs of each segment
+  float* ml;                 // [B Hkv][maxseg][kRows][2] running max (base 2) and sum
   float* out;                // [B][n][Hq][kD]
 };
 
 struct TaSmem {
   __nv_bfloat16 q[kRows * kPitch];
-  __nv_bfloat16 k[2][kBlockKeys * kPitch];
-  __nv_bfloat16 v[2][kBlockKeys * kPitch];
+  __nv_bfloat16 k[kStagesA][kBlockKeys * kPitch];
+  __nv_bfloat16 v[kStagesA][kBlockKeys * kPitch];
   uint8_t mask[kMaxNodes * kMaxNodes];
 };
 
@@ -74,7 +78,12 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Key and value rows [k0, k0 + 64) of one (request, key/value head) into ring stage s; rows past T read as zero.
+// The CTA whose even share of the flattened key blocks holds block x: CTA c takes [c W / G, (c + 1) W / G).
+__host__ __device__ __forceinline__ int block_owner(long long x, long long W, int G) {
+  return static_cast<int>(((x + 1) * G - 1) / W);
+}
+
+// Key and value rows [k0, k0 + 32) of one (request, key/value head) into ring stage s; rows past T read as zero.
 __device__ __forceinline__ void load_kv(const TaParams& p, TaSmem& S, int s, size_t kvbase, int k0) {
   for (int c = threadIdx.x; c < kBlockKeys * (kD / 8); c += kThreadsA) {
     const int r = c >> 4, col = (c & 15) * 8, key = k0 + r;  // 16 chunks of 16 bytes per row
@@ -85,13 +94,21 @@ __device__ __forceinline__ void load_kv(const TaParams& p, TaSmem& S, int s, siz
   }
 }
 
-// One CTA per (request b, key/value head, key chunk): the partial attention of the chunk for the 64 query rows.
+// CTA c takes an even share of the flattened (request, key/value head, key block) space; each run of its share
+// within one (request, key/value head) is a segment, whose partial attention for the 64 query rows goes to that
+// pair's slot (c - the owner of the pair's first block).
 __global__ void __launch_bounds__(kThreadsA, 4) tree_attn_partial(TaParams p) {
   extern __shared__ float4 smem_f4[];
   TaSmem& S = *reinterpret_cast<TaSmem*>(smem_f4);
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31, g = lane >> 2, tq = lane & 3;
-  const int unit = blockIdx.x, chunk = unit % p.nch, pair = unit / p.nch, b = pair / p.Hkv, kvh = pair % p.Hkv;
-  const int k0 = chunk * p.chunk, k1 = min(k0 + p.chunk, p.T);
+  const long long x1 = (static_cast<long long>(blockIdx.x) + 1) * p.work / p.grid;
+  for (long long x = static_cast<long long>(blockIdx.x) * p.work / p.grid; x < x1;) {
+  const int pair = static_cast<int>(x / p.nb), b = pair / p.Hkv, kvh = pair % p.Hkv;
+  const long long pfirst = static_cast<long long>(pair) * p.nb;
+  const int bend = static_cast<int>(min(x1, pfirst + p.nb) - pfirst);
+  const int k0 = static_cast<int>(x - pfirst) * kBlockKeys, k1 = min(bend * kBlockKeys, p.T);
+  const int slot = static_cast<int>(blockIdx.x) - block_owner(pfirst, p.work, p.grid);
+  x = pfirst + bend;
   const size_t kvbase = (static_cast<size_t>(b) * p.Hkv + kvh) * p.T;
   // query row r = gi n + i: query head kvh G + gi, tree node i (rows >= R read as zero)
   for (int c = t; c < kRows * (kD / 8); c += kThreadsA) {
@@ -102,8 +119,10 @@ __global__ void __launch_bounds__(kThreadsA, 4) tree_attn_partial(TaParams p) {
   }
   for (int c = t; c < p.n * p.n; c += kThreadsA) S.mask[c] = p.mask[static_cast<size_t>(b) * p.n * p.n + c];
   const int nblk = (k1 - k0 + kBlockKeys - 1) / kBlockKeys;
-  load_kv(p, S, 0, kvbase, k0);
-  asm volatile("cp.async.commit_group;" ::: "memory");
+  for (int j = 0; j < kStagesA - 1; ++j) {  // the first blocks (the queries' copies join the first group)
+    if (j < nblk) load_kv(p, S, j, kvbase, k0 + j * kBlockKeys);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
 
   const int rw0 = 16 * warp + g, rw1 = rw0 + 8;  // this thread's two query rows
   const int node0 = rw0 < p.R ? rw0 % p.n : -1, node1 = rw1 < p.R ? rw1 % p.n : -1;
@@ -112,12 +131,13 @@ __global__ void __launch_bounds__(kThreadsA, 4) tree_attn_partial(TaParams p) {
   for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   for (int blk = 0; blk < nblk; ++blk) {
-    if (blk + 1 < nblk) load_kv(p, S, (blk + 1) & 1, kvbase, k0 + (blk + 1) * kBlockKeys);
+    if (blk + kStagesA - 1 < nblk)
+      load_kv(p, S, (blk + kStagesA - 1) % kStagesA, kvbase, k0 + (blk + kStagesA - 1) * kBlockKeys);
     asm volatile("cp.async.commit_group;" ::: "memory");
-    asm volatile("cp.async.wait_group 1;" ::: "memory");
+    asm volatile("cp.async.wait_group %0;" ::"n"(kStagesA - 1) : "memory");  // block blk has landed
     __syncthreads();
-    const __nv_bfloat16* Ks = S.k[blk & 1];
-    const __nv_bfloat16* Vs = S.v[blk & 1];
+    const __nv_bfloat16* Ks = S.k[blk % kStagesA];
+    const __nv_bfloat16* Vs = S.v[blk % kStagesA];
     // S = Q K^T for the block's keys: tiles of 8 keys; the warp's 16 query rows re-read as A fragments per K step
     constexpr int kNT = kBlockKeys / 8;
     float s[kNT][4];
@@ -196,14 +216,15 @@ __global__ void __launch_bounds__(kThreadsA, 4) tree_attn_partial(TaParams p) {
         mma_bf16(o[2 * dp + 1], pa, b2, b3);
       }
     }
-    __syncthreads();  // the stage is refilled by the load two blocks on
+    __syncthreads();  // the stage is refilled by a later load
   }
   asm volatile("cp.async.wait_group 0;" ::: "memory");
   l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 1);
   l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 2);
   l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 1);
   l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 2);
-  float* po = p.part + static_cast<size_t>(unit) * kRows * kD;
+  const size_t unit = static_cast<size_t>(pair) * p.maxseg + slot;
+  float* po = p.part + unit * kRows * kD;
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const int col = j * 8 + tq * 2;
@@ -211,11 +232,13 @@ __global__ void __launch_bounds__(kThreadsA, 4) tree_attn_partial(TaParams p) {
     *reinterpret_cast<float2*>(po + rw1 * kD + col) = make_float2(o[j][2], o[j][3]);
   }
   if (tq == 0) {
-    float* pm = p.ml + static_cast<size_t>(unit) * kRows * 2;
+    float* pm = p.ml + unit * kRows * 2;
     pm[rw0 * 2] = m0;
     pm[rw0 * 2 + 1] = l0;
     pm[rw1 * 2] = m1;
     pm[rw1 * 2 + 1] = l1;
+  }
+  __syncthreads();  // the queries, mask and ring are reloaded for the next segment
   }
 }
 
@@ -228,9 +251,11 @@ __global__ void __launch_bounds__(kD) tree_attn_combine(TaParams p) {
   __shared__ float s_den;
   const int r = blockIdx.x % p.R, pair = blockIdx.x / p.R, b = pair / p.Hkv, kvh = pair % p.Hkv;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const size_t u0 = static_cast<size_t>(pair) * p.nch;
+  const size_t u0 = static_cast<size_t>(pair) * p.maxseg;
+  const long long pfirst = static_cast<long long>(pair) * p.nb;
+  const int nseg = block_owner(pfirst + p.nb - 1, p.work, p.grid) - block_owner(pfirst, p.work, p.grid) + 1;
   float mx = -INFINITY;
-  for (int c = t; c < p.nch; c += kD) mx = fmaxf(mx, p.ml[((u0 + c) * kRows + r) * 2]);
+  for (int c = t; c < nseg; c += kD) mx = fmaxf(mx, p.ml[((u0 + c) * kRows + r) * 2]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
   if (lane == 0) s_red[warp] = mx;
@@ -240,7 +265,7 @@ __global__ void __launch_bounds__(kD) tree_attn_combine(TaParams p) {
   for (int w = 1; w < kD / 32; ++w) mx = fmaxf(mx, s_red[w]);
   __syncthreads();
   float den = 0.f;
-  for (int c = t; c < p.nch; c += kD) {
+  for (int c = t; c < nseg; c += kD) {
     const float* pm = p.ml + ((u0 + c) * kRows + r) * 2;
     const float w = (mx == -INFINITY || pm[0] == -INFINITY) ? 0.f : exp2f(pm[0] - mx);
     s_w[c] = w;
@@ -258,28 +283,34 @@ __global__ void __launch_bounds__(kD) tree_attn_combine(TaParams p) {
   }
   __syncthreads();
   float num = 0.f;
-  for (int c = 0; c < p.nch; ++c) num += s_w[c] * p.part[((u0 + c) * kRows + r) * kD + t];
+  for (int c = 0; c < nseg; ++c) num += s_w[c] * p.part[((u0 + c) * kRows + r) * kD + t];
   const int gi = r / p.n, i = r % p.n;
   p.out[((static_cast<size_t>(b) * p.n + i) * p.Hq + kvh * p.G + gi) * kD + t] = s_den > 0.f ? num / s_den : 0.f;
 }
 
 struct TaPlan {
-  int nch, chunk;
+  int nb, grid, maxseg;
+  long long work;
   size_t part, ml, bytes;
 };
+// Four CTAs per SM share all key blocks evenly (a CTA takes at least one block); maxseg is the most CTAs any
+// (request, key/value head) is spread over, found pair by pair.
 inline TaPlan ta_plan(int B, int T, int Hkv, int sms) {
   TaPlan P{};
   const long long pairs = static_cast<long long>(B) * Hkv;
-  const int blocks = (T + kBlockKeys - 1) / kBlockKeys;
-  long long want = (4LL * sms + pairs - 1) / pairs;  // chunks per (request, key/value head): four CTAs per SM
-  want = want < 1 ? 1 : (want > blocks ? blocks : want);
-  const int per = (blocks + static_cast<int>(want) - 1) / static_cast<int>(want);
-  P.chunk = per * kBlockKeys;
-  P.nch = (T + P.chunk - 1) / P.chunk;
-  const size_t units = static_cast<size_t>(pairs) * P.nch;
+  P.nb = (T + kBlockKeys - 1) / kBlockKeys;
+  P.work = pairs * P.nb;
+  const long long g = 4LL * sms;
+  P.grid = static_cast<int>(g < P.work ? g : P.work);
+  P.maxseg = 1;
+  for (long long pr = 0; pr < pairs; ++pr) {
+    const int segs = block_owner((pr + 1) * P.nb - 1, P.work, P.grid) - block_owner(pr * P.nb, P.work, P.grid) + 1;
+    P.maxseg = segs > P.maxseg ? segs : P.maxseg;
+  }
+  const size_t slots = static_cast<size_t>(pairs) * P.maxseg;
   P.part = 0;
-  P.ml = align_up(sizeof(float) * units * kRows * kD);
-  P.bytes = align_up(P.ml + sizeof(float) * units * kRows * 2);
+  P.ml = align_up(sizeof(float) * slots * kRows * kD);
+  P.bytes = align_up(P.ml + sizeof(float) * slots * kRows * 2);
   return P;
 }
 
@@ -313,11 +344,10 @@ extern "C" dt_status dt_tree_attention(int B, int n, int L, int Hq, int Hkv, int
   const int T = L + n;
   const TaPlan P = ta_plan(B, T, Hkv, di.sms);
   if (workspace_bytes < P.bytes) return DT_ERR_INVALID_ARG;
-  const long long units = static_cast<long long>(B) * Hkv * P.nch;
-  if (units > INT_MAX || static_cast<long long>(B) * Hkv * G * n > INT_MAX || P.nch > kMaxChunks)
-    return DT_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Hkv * G * n > INT_MAX || P.maxseg > kMaxChunks) return DT_ERR_UNSUPPORTED;
   TaParams p{};
-  p.B = B; p.n = n; p.L = L; p.T = T; p.Hq = Hq; p.Hkv = Hkv; p.G = G; p.R = G * n; p.nch = P.nch; p.chunk = P.chunk;
+  p.B = B; p.n = n; p.L = L; p.T = T; p.Hq = Hq; p.Hkv = Hkv; p.G = G; p.R = G * n;
+  p.nb = P.nb; p.grid = P.grid; p.maxseg = P.maxseg; p.work = P.work;
   p.q = static_cast<const unsigned short*>(q);
   p.k = static_cast<const unsigned short*>(k);
   p.v = static_cast<const unsigned short*>(v);
@@ -329,7 +359,7 @@ extern "C" dt_status dt_tree_attention(int B, int n, int L, int Hq, int Hkv, int
   p.out = out;
   const void* fa = reinterpret_cast<const void*>(tree_attn_partial);
   if (ensure_dynamic_smem(fa, sizeof(TaSmem)) != cudaSuccess) return DT_ERR_CUDA;
-  tree_attn_partial<<<static_cast<unsigned>(units), kThreadsA, sizeof(TaSmem), stream>>>(p);
+  tree_attn_partial<<<static_cast<unsigned>(P.grid), kThreadsA, sizeof(TaSmem), stream>>>(p);
   tree_attn_combine<<<static_cast<unsigned>(static_cast<long long>(B) * Hkv * p.R), kD, 0, stream>>>(p);
   return cuda_status(cudaGetLastError());
 }
