@@ -130,6 +130,26 @@ dt_status dt_build_trees(int B, int K, int V, int M, int n, int max_depth, float
                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------------------------------------------
+ * dt_round — one drafting round: dt_topm into topm_ids / topm_vals, then dt_build_trees from them, on one stream.
+ * Source: blog.captcha.la, "Methodology — deep read" (the round restricts each block position to its top-M marginal
+ * candidates, then grows the best-first conditional tree over them); gist.science, "Composants Clés".
+ *
+ * Results are bit-identical to the two calls made one after the other with the same arguments; the difference is
+ * that every argument of both is checked before either is launched, so an invalid round launches nothing.
+ *
+ *   logits, dtype        as dt_topm (marginal logits [B,K,V]).
+ *   topm_ids, topm_vals  [B,K,M], written by the top-M and read by the builder (device memory the caller owns).
+ *   h0, w, out_*         as dt_build_trees.
+ *   workspace            one workspace of at least dt_build_workspace_bytes(B, K, V, M, n, w->H, w->E) bytes
+ *                        (which covers the top-M's part), initialised once by dt_workspace_init.
+ * Errors are those of dt_topm and dt_build_trees.
+ * ------------------------------------------------------------------------------------------------------------- */
+dt_status dt_round(const void* logits, dt_dtype dtype, int B, int K, int V, int M, int n, int max_depth, float T,
+                   const float* h0, const dt_weights* w, int32_t* topm_ids, float* topm_vals, int32_t* out_tokens,
+                   int32_t* out_parents, int32_t* out_depth, float* out_scores, uint8_t* out_mask, void* workspace,
+                   size_t workspace_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------------------------------------
  * dt_build_trees_marginal — the same best-first draft trees scored by DDTree's factorised marginals.
  * Source: blog.captcha.la, "Methodology — deep read" (DDTree scores tree nodes by factorised marginal
  * log-probabilities) and "Key findings" (the ablation that changes only the scoring function: conditional scoring

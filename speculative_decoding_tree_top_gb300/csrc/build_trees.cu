@@ -1022,12 +1022,18 @@ extern "C" size_t dt_build_workspace_bytes(int B, int K, int V, int M, int n, in
   return dt::build_layout(B, K, V, M, n, H, E).bytes;
 }
 
-extern "C" dt_status dt_build_trees(int B, int K, int V, int M, int n, int max_depth, float T,
-                                    const int32_t* topm_ids, const float* topm_vals, const float* h0,
-                                    const dt_weights* w, int32_t* out_tokens, int32_t* out_parents,
-                                    int32_t* out_depth, float* out_scores, uint8_t* out_mask, void* workspace,
-                                    size_t workspace_bytes, cudaStream_t stream) {
-  using namespace dt;
+namespace dt {
+namespace {
+
+enum class BuildMode {
+  kLaunch,  // validate and launch
+  kCheck,   // validate only, launch nothing (dt_round checks the whole round before its first launch)
+};
+
+dt_status build_trees(int B, int K, int V, int M, int n, int max_depth, float T, const int32_t* topm_ids,
+                      const float* topm_vals, const float* h0, const dt_weights* w, int32_t* out_tokens,
+                      int32_t* out_parents, int32_t* out_depth, float* out_scores, uint8_t* out_mask, void* workspace,
+                      size_t workspace_bytes, cudaStream_t stream, BuildMode mode) {
   if (!w) return DT_ERR_INVALID_ARG;
   const int H = w->H, E = w->E;
   if (B < 0 || K < 1 || V < 1 || M < 1 || M > V || n < 1 || max_depth < 1 || max_depth > K) return DT_ERR_INVALID_ARG;
@@ -1084,7 +1090,8 @@ extern "C" dt_status dt_build_trees(int B, int K, int V, int M, int n, int max_d
     const int fit = kWaveJobs / (B < kWaveJobs ? B : kWaveJobs);
     p.lookahead = k_set > 0 ? (k_set < fit ? k_set : fit) : fit;
   }
-  if (small_builder_fits(p, di)) return cuda_status(launch_small_builder(p, di, stream));
+  if (small_builder_fits(p, di))
+    return mode == BuildMode::kCheck ? DT_OK : cuda_status(launch_small_builder(p, di, stream));
   p.lookahead = k_set > 0 ? (k_set < kLargeLookahead ? k_set : kLargeLookahead)
                           : (B >= 128 ? kLargeLookahead : kLargeDefault);
 
@@ -1113,8 +1120,38 @@ extern "C" dt_status dt_build_trees(int B, int K, int V, int M, int n, int max_d
   const size_t smem = smem_bytes(gemm, M, n, H, p.lookahead, p.bf16 ? 2 : 4, static_cast<size_t>(di.optin) - 2048,
                                  &p.rows_smem);
   if (smem + 2048 > static_cast<size_t>(di.optin)) return DT_ERR_UNSUPPORTED;
+  if (mode == BuildMode::kCheck) return DT_OK;
   if (ensure_dynamic_smem(fn, smem) != cudaSuccess) return DT_ERR_CUDA;
   const unsigned grid = static_cast<unsigned>(di.sms);  // one CTA per SM; co-resident under a cooperative launch
   void* args[] = {&p, &maps};
   return cuda_status(cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kThreads), args, smem, stream));
+}
+
+}  // namespace
+}  // namespace dt
+
+extern "C" dt_status dt_build_trees(int B, int K, int V, int M, int n, int max_depth, float T,
+                                    const int32_t* topm_ids, const float* topm_vals, const float* h0,
+                                    const dt_weights* w, int32_t* out_tokens, int32_t* out_parents,
+                                    int32_t* out_depth, float* out_scores, uint8_t* out_mask, void* workspace,
+                                    size_t workspace_bytes, cudaStream_t stream) {
+  return dt::build_trees(B, K, V, M, n, max_depth, T, topm_ids, topm_vals, h0, w, out_tokens, out_parents, out_depth,
+                         out_scores, out_mask, workspace, workspace_bytes, stream, dt::BuildMode::kLaunch);
+}
+
+extern "C" dt_status dt_round(const void* logits, dt_dtype dtype, int B, int K, int V, int M, int n, int max_depth,
+                              float T, const float* h0, const dt_weights* w, int32_t* topm_ids, float* topm_vals,
+                              int32_t* out_tokens, int32_t* out_parents, int32_t* out_depth, float* out_scores,
+                              uint8_t* out_mask, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  using dt::BuildMode;
+  // every check of both calls first (they launch nothing), so that an invalid round launches nothing at all
+  dt_status st = dt::topm_check(logits, dtype, B, K, V, M, topm_ids, topm_vals, workspace, workspace_bytes);
+  if (st != DT_OK) return st;
+  st = dt::build_trees(B, K, V, M, n, max_depth, T, topm_ids, topm_vals, h0, w, out_tokens, out_parents,
+                                 out_depth, out_scores, out_mask, workspace, workspace_bytes, stream, BuildMode::kCheck);
+  if (st != DT_OK) return st;
+  st = dt_topm(logits, dtype, B, K, V, M, topm_ids, topm_vals, workspace, workspace_bytes, stream);
+  if (st != DT_OK) return st;
+  return dt::build_trees(B, K, V, M, n, max_depth, T, topm_ids, topm_vals, h0, w, out_tokens, out_parents, out_depth,
+                         out_scores, out_mask, workspace, workspace_bytes, stream, BuildMode::kLaunch);
 }

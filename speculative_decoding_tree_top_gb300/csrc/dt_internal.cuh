@@ -313,5 +313,8 @@ cudaError_t current_device_info(DeviceInfo* out);
 // Raises the dynamic shared-memory limit of kernel `fn` on the current device to at least `bytes`; the runtime is
 // called only when a larger size than any set before for this (device, kernel) is asked for.
 cudaError_t ensure_dynamic_smem(const void* fn, size_t bytes);
+// dt_topm's argument checks without the launch (dt_round checks a whole round before its first launch)
+dt_status topm_check(const void* logits, dt_dtype dtype, int B, int K, int V, int M, const int32_t* out_ids,
+                     const float* out_vals, const void* workspace, size_t workspace_bytes);
 
 }  // namespace dt

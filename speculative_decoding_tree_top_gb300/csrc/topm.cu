@@ -5,18 +5,19 @@
 //
 // GB300 design. The op is a pure HBM stream (every logit is read once, nothing is reused), so it is laid out for
 // bandwidth and for few instructions per logit, not for tensor cores. Two launches:
-//   * filter: grid = (chunks of 16384 logits) x (B*K rows), 256 threads; every thread issues its eight (bf16)
-//     16-byte loads up front (64 logits in registers), consecutive threads on consecutive 16 bytes. The CTAs are
-//     short-lived and many, so the loads of thousands of them are in flight at once (a persistent bulk-copy ring
-//     measured slower on this part). A chunk keeps the logits at or above the M-th largest of its 256 lane maxima
-//     (one warp, ballot bisection): maxima use the packed bf16x2 max, the test the packed bf16x2 compare-to-mask,
-//     one instruction per two logits in the common "nothing here" case. About M of the 16384 survive and are
-//     written, unsorted, with their count;
-//   * select: one CTA per row radix-selects the row's exact M-th largest among those few hundred candidates and
-//     ranks the M at or above it.
+//   * filter: grid = (B*K rows) x (chunks of 32768 bf16 / 16384 fp32 logits), 256 threads. Each thread stages its
+//     sixteen 16-byte groups into shared memory with cp.async, committed as four parts, so all of a chunk's bytes
+//     are in flight at once and no registers are held while they are. A row's first chunk computes the M-th
+//     largest of its 256 lane maxima (radix over the key's bytes, one shared histogram per digit) and publishes it
+//     as the row's bound; later chunks of the row read the published bound before their copies are issued and scan
+//     each part as soon as it lands (packed bf16x2 compare-to-mask, one instruction per two logits). A chunk
+//     appends its logits at or above the bound, unsorted, with their count (a few per chunk, M or more per row);
+//   * select: one CTA per row, launched as a programmatic dependent of the filter so it takes the SMs the filter's
+//     last wave leaves idle. A histogram of the candidates' keys brackets the row's exact M-th largest, and the M
+//     at or above it are ranked by counting (a radix pass when the bracket holds too many).
 // Every comparison is on distinct integer words (value key, then inverted index), so the result is exact and
-// deterministic, ties broken by the lower id. A chunk with more than 4M survivors (heavy ties, sorted runs) keeps
-// exactly its top M instead (bisection over its registers): slower, same result.
+// deterministic, ties broken by the lower id. A chunk with more survivors than its list holds (heavy ties, sorted
+// runs) keeps exactly its top M instead (bisection over the staged chunk): slower, same result.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -590,9 +591,10 @@ extern "C" size_t dt_topm_workspace_bytes(int B, int K, int V, int M) {
   return dt::topm_layout(B, K, V, M).bytes;
 }
 
-extern "C" dt_status dt_topm(const void* logits, dt_dtype dtype, int B, int K, int V, int M, int32_t* out_ids,
-                             float* out_vals, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-  using namespace dt;
+namespace dt {
+// Every check of dt_topm's arguments, host-side only: nothing is launched.
+dt_status topm_check(const void* logits, dt_dtype dtype, int B, int K, int V, int M, const int32_t* out_ids,
+                     const float* out_vals, const void* workspace, size_t workspace_bytes) {
   if (B < 0 || K < 1 || V < 1 || M < 1 || M > V) return DT_ERR_INVALID_ARG;
   if (dtype != DT_F32 && dtype != DT_BF16) return DT_ERR_INVALID_ARG;
   if (M > DT_MAX_M) return DT_ERR_UNSUPPORTED;
@@ -603,7 +605,17 @@ extern "C" dt_status dt_topm(const void* logits, dt_dtype dtype, int B, int K, i
   const TopmLayout L = topm_layout(B, K, V, M);
   if (workspace_bytes < L.bytes) return DT_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * K > INT_MAX || L.chunks > 65535) return DT_ERR_UNSUPPORTED;  // grid limits
-  return launch_topm(logits, dtype, B, K, V, M, out_ids, out_vals, static_cast<char*>(workspace), L, stream);
+  return DT_OK;
+}
+}  // namespace dt
+
+extern "C" dt_status dt_topm(const void* logits, dt_dtype dtype, int B, int K, int V, int M, int32_t* out_ids,
+                             float* out_vals, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  using namespace dt;
+  const dt_status st = topm_check(logits, dtype, B, K, V, M, out_ids, out_vals, workspace, workspace_bytes);
+  if (st != DT_OK || B == 0) return st;
+  return launch_topm(logits, dtype, B, K, V, M, out_ids, out_vals, static_cast<char*>(workspace),
+                     topm_layout(B, K, V, M), stream);
 }
 
 // ---- dt_topm_static: the same top-M with no caller workspace ----------------------------------------------------

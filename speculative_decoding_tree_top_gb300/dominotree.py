@@ -52,6 +52,8 @@ SIGNATURES = {
     "dt_build_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "dt_build_trees": (_I, [_I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _P, ctypes.POINTER(_Weights), _P, _P,
                             _P, _P, _P, _P, _SZ, _P]),
+    "dt_round": (_I, [_P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, ctypes.POINTER(_Weights), _P, _P, _P, _P,
+                      _P, _P, _P, _P, _SZ, _P]),
     "dt_topm_static": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "dt_accept_paths": (_I, [_I, _I, _P, _P, _P, _P, _P, _P, _P]),
     "dt_build_trees_marginal": (_I, [_I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
@@ -286,6 +288,33 @@ def dt_build_trees(topm_ids: torch.Tensor, topm_vals: torch.Tensor, h0: torch.Te
     return out
 
 
+def dt_round(logits: torch.Tensor, h0: torch.Tensor, weights: Weights, M: int, n: int, max_depth: int, T: float,
+             topm_ids: Optional[torch.Tensor] = None, topm_vals: Optional[torch.Tensor] = None,
+             out: Optional[dict] = None, workspace: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """dt_topm then dt_build_trees in one call, every argument checked before either launch -> the tree outputs of
+    dt_build_trees; the candidates land in ``topm_ids`` / ``topm_vals`` [B,K,M]."""
+    B, K, V = logits.shape
+    dev = logits.device
+    if topm_ids is None:
+        topm_ids = torch.empty((B, K, M), dtype=torch.int32, device=dev)
+    if topm_vals is None:
+        topm_vals = torch.empty((B, K, M), dtype=torch.float32, device=dev)
+    if out is None:
+        out = alloc_tree_outputs(B, n, dev)
+    if workspace is None:
+        workspace = new_workspace(dt_build_workspace_bytes(B, K, V, M, n, weights.H, weights.E), dev)
+    w = weights.struct()
+    _check(lib().dt_round(
+        _dev(logits, "logits"), _code(logits.dtype), B, K, V, M, n, max_depth, float(T),
+        _dev(h0, "h0", torch.float32, (B, weights.H)), ctypes.byref(w),
+        _dev(topm_ids, "topm_ids", torch.int32, (B, K, M)), _dev(topm_vals, "topm_vals", torch.float32, (B, K, M)),
+        _dev(out["tokens"], "out_tokens", torch.int32, (B, n)), _dev(out["parents"], "out_parents", torch.int32, (B, n)),
+        _dev(out["depth"], "out_depth", torch.int32, (B, n)), _dev(out["scores"], "out_scores", torch.float32, (B, n)),
+        _dev(out["mask"], "out_mask", torch.uint8, (B, n, n)), _dev(workspace, "workspace", torch.uint8),
+        workspace.numel(), _stream(stream)), "dt_round")
+    return out
+
+
 def dt_build_trees_marginal(topm_ids: torch.Tensor, topm_vals: torch.Tensor, V: int, n: int, max_depth: int,
                             T: float, out: Optional[dict] = None, workspace: Optional[torch.Tensor] = None,
                             stream=None) -> dict:
@@ -396,9 +425,31 @@ class Round:
         _check(lib().dt_build_trees_marginal(*self._marg_args), "dt_build_trees_marginal")
         return self.out
 
+    def round(self, logits: torch.Tensor, h0: torch.Tensor, stream=None) -> dict:
+        """dt_round: the top-M into this round's ids/vals and the tree into its outputs, in one call (arguments kept
+        like ``topm``'s)."""
+        st = _stream(stream)
+        w = self.weights
+        key = (logits.data_ptr(), tuple(logits.shape), logits.dtype, h0.data_ptr(), tuple(h0.shape), h0.dtype, st,
+               id(w), *(t.data_ptr() if t is not None else 0 for t in (w.emb, w.w_ih, w.w_hh, w.b_ih, w.b_hh, w.w_c)))
+        if key != getattr(self, "_round_key", None):
+            B, K, V = logits.shape
+            if (B, K, V) != (self.B, self.K, self.V):
+                raise ValueError(f"logits must have shape {(self.B, self.K, self.V)}, not {(B, K, V)}")
+            self._round_w = w.struct()
+            o = self.out
+            self._round_args = (
+                _dev(logits, "logits"), _code(logits.dtype), B, K, V, self.M, self.n, self.max_depth, float(self.T),
+                _dev(h0, "h0", torch.float32, (self.B, w.H)), ctypes.byref(self._round_w), _dev(self.ids, "topm_ids"),
+                _dev(self.vals, "topm_vals"), _dev(o["tokens"], "out_tokens"), _dev(o["parents"], "out_parents"),
+                _dev(o["depth"], "out_depth"), _dev(o["scores"], "out_scores"), _dev(o["mask"], "out_mask"),
+                _dev(self.workspace, "workspace", torch.uint8), self.workspace.numel(), st)
+            self._round_key = key
+        _check(lib().dt_round(*self._round_args), "dt_round")
+        return self.out
+
     def __call__(self, logits: torch.Tensor, h0: torch.Tensor, stream=None) -> dict:
-        self.topm(logits, stream)
-        return self.build(h0, stream)
+        return self.round(logits, h0, stream)
 
     def check(self, stream=None):
         _check(int(dt_get_error(self.workspace, stream)), "device status")
@@ -410,7 +461,7 @@ def pinned_like(t: torch.Tensor) -> torch.Tensor:
 
 class HostRound(Round):
     """A round whose inputs and outputs live in (pinned) host memory: each call copies the logits and h0 to the
-    device, runs dt_topm and dt_build_trees, and copies the tree back, all on one stream."""
+    device, runs dt_round (dt_topm and dt_build_trees), and copies the tree back, all on one stream."""
 
     def __init__(self, B, K, V, M, n, max_depth, T, weights: Weights, logits_dtype, device="cuda"):
         super().__init__(B, K, V, M, n, max_depth, T, weights, device)

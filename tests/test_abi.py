@@ -109,6 +109,24 @@ def test_build_rejects_bad_arguments(dtlib):
     assert _build(dtlib, B=0) == OK
 
 
+def test_round_rejects_bad_arguments(dtlib):
+    L = dtlib.lib()
+
+    def rnd(B=1, K=4, V=100, M=4, n=8, max_depth=3, T=0.0, w=None, dtype=1, logits=A, wsb=1 << 30):
+        w = w or _weights(dtlib)
+        return L.dt_round(logits, dtype, B, K, V, M, n, max_depth, T, A, ctypes.byref(w), A, A, A, A, A, A, A, A, wsb,
+                          None)
+
+    assert rnd(logits=None) == INVALID                      # the top-M's checks
+    assert rnd(dtype=7) == INVALID
+    assert rnd(M=2000, V=5000) == UNSUPPORTED
+    assert rnd(max_depth=5) == INVALID                      # the builder's
+    assert rnd(T=-1.0) == INVALID
+    assert rnd(w=_weights(dtlib, H=30)) == INVALID
+    assert rnd(wsb=64) == INVALID
+    assert rnd(B=0) == OK                                   # nothing to do, nothing launched
+
+
 def test_binding_refuses_host_tensors(dtlib):
     import torch
     with pytest.raises(TypeError):

@@ -177,3 +177,41 @@ def test_lookahead_width_does_not_change_the_tree(dtlib, case):
     for o in outs[1:]:
         for key in o:
             assert torch.equal(o[key], outs[0][key]), key
+
+
+@pytest.mark.parametrize("case", [
+    dict(config=1),           # one request
+    dict(config=0),           # tiny, fp32
+    dict(config=2, B=8),      # the largest small-batch round
+    dict(config=2, B=16),     # the large-batch builder: two ordinary launches
+])
+def test_round_matches_the_two_calls(dtlib, case):
+    """dt_round gives bit-identical ids, values and trees to dt_topm followed by dt_build_trees, also with several
+    rounds queued back to back on one workspace and no synchronisation between them."""
+    s = synth.shape(case["config"], **{k: v for k, v in case.items() if k != "config"})
+    inputs = [synth.make_inputs(s, device="cuda", seed=40 + i) for i in range(3)]
+    w = dtlib.Weights.of(inputs[0])
+    rnd = dtlib.Round(s.B, s.K, s.V, s.M, s.n, s.max_depth, s.T, w)
+    ref = []
+    for inp in inputs:
+        rnd.topm(inp.logits)
+        out = rnd.build(inp.h0)
+        torch.cuda.synchronize()
+        rnd.check()
+        ref.append(({k: v.clone() for k, v in out.items()}, rnd.ids.clone(), rnd.vals.clone()))
+    got = []
+    for inp in inputs:  # queued back to back: no synchronisation between the rounds
+        out = rnd.round(inp.logits, inp.h0)
+        got.append(({k: v.clone() for k, v in out.items()}, rnd.ids.clone(), rnd.vals.clone()))
+    torch.cuda.synchronize()
+    rnd.check()
+    for (ro, ri, rv), (go, gi, gv) in zip(ref, got):
+        assert torch.equal(ri, gi) and torch.equal(rv, gv)
+        for k in ro:
+            assert torch.equal(ro[k], go[k]), k
+    # the functional form, with its own buffers, agrees too
+    inp = inputs[-1]
+    out = dtlib.dt_round(inp.logits, inp.h0, w, s.M, s.n, s.max_depth, s.T)
+    torch.cuda.synchronize()
+    for k in ref[-1][0]:
+        assert torch.equal(ref[-1][0][k], out[k]), k
