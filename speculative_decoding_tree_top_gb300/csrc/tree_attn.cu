@@ -242,50 +242,107 @@ __global__ void __launch_bounds__(kThreadsA, 4) tree_attn_partial(TaParams p) {
   }
 }
 
-// One CTA per (request, key/value head, query row), one thread per output column: the chunks' partials of the row,
-// rescaled to its overall maximum and normalised by its overall sum. The chunks' weights are found once per CTA.
+// The segments' partials of each (request, key/value head, query row), rescaled to the row's overall maximum and
+// normalised by its overall sum; a lane works on four of the 128 output columns. With few segments per row (large
+// batches) one warp takes a row; with many (a request's keys spread over many CTAs) one CTA takes a row and its warps
+// split the segments, reducing through shared memory. CTAs stride over the rows with the grid sized to one resident
+// wave, and a row's loads (its segments' maxima and sums, then their partials) are independent of one another.
 constexpr int kMaxChunks = 1024;
-__global__ void __launch_bounds__(kD) tree_attn_combine(TaParams p) {
-  __shared__ float s_w[kMaxChunks];
-  __shared__ float s_red[kD / 32];
-  __shared__ float s_den;
-  const int r = blockIdx.x % p.R, pair = blockIdx.x / p.R, b = pair / p.Hkv, kvh = pair % p.Hkv;
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const size_t u0 = static_cast<size_t>(pair) * p.maxseg;
+constexpr int kCombineThreads = 256;
+constexpr int kCombineWarps = kCombineThreads / 32;
+constexpr int kCombinePerSm = 2048 / kCombineThreads;  // CTAs per SM: the SM's threads
+constexpr int kWarpRowSegs = 8;                        // at most this many segments per row: a warp per row
+struct RowRef {
+  size_t u0;  // first partial slot of the row's (request, key/value head)
+  int r, b, kvh, nseg;
+};
+__device__ __forceinline__ RowRef row_ref(const TaParams& p, long long u) {
+  RowRef q;
+  q.r = static_cast<int>(u % p.R);
+  const int pair = static_cast<int>(u / p.R);
+  q.b = pair / p.Hkv;
+  q.kvh = pair % p.Hkv;
+  q.u0 = static_cast<size_t>(pair) * p.maxseg;
   const long long pfirst = static_cast<long long>(pair) * p.nb;
-  const int nseg = block_owner(pfirst + p.nb - 1, p.work, p.grid) - block_owner(pfirst, p.work, p.grid) + 1;
-  float mx = -INFINITY;
-  for (int c = t; c < nseg; c += kD) mx = fmaxf(mx, p.ml[((u0 + c) * kRows + r) * 2]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-  if (lane == 0) s_red[warp] = mx;
-  __syncthreads();
-  mx = s_red[0];
-#pragma unroll
-  for (int w = 1; w < kD / 32; ++w) mx = fmaxf(mx, s_red[w]);
-  __syncthreads();
-  float den = 0.f;
-  for (int c = t; c < nseg; c += kD) {
-    const float* pm = p.ml + ((u0 + c) * kRows + r) * 2;
-    const float w = (mx == -INFINITY || pm[0] == -INFINITY) ? 0.f : exp2f(pm[0] - mx);
-    s_w[c] = w;
-    den += w * pm[1];
+  q.nseg = block_owner(pfirst + p.nb - 1, p.work, p.grid) - block_owner(pfirst, p.work, p.grid) + 1;
+  return q;
+}
+// Segments c0, c0 + step, ... of a row, weighted relative to the row's maximum `mx`: the weighted sum of the lane's
+// four partial columns and of the segments' sums.
+__device__ __forceinline__ void row_accumulate(const TaParams& p, const RowRef& q, float mx, int c0, int step,
+                                               int lane, float4& num, float& den) {
+#pragma unroll 4
+  for (int c = c0; c < q.nseg; c += step) {
+    const float2 ml = *reinterpret_cast<const float2*>(p.ml + ((q.u0 + c) * kRows + q.r) * 2);
+    const float4 pv = *reinterpret_cast<const float4*>(p.part + ((q.u0 + c) * kRows + q.r) * kD + lane * 4);
+    const float w = (mx == -INFINITY || ml.x == -INFINITY) ? 0.f : exp2f(ml.x - mx);
+    den += w * ml.y;
+    num.x += w * pv.x;
+    num.y += w * pv.y;
+    num.z += w * pv.z;
+    num.w += w * pv.w;
   }
+}
+__device__ __forceinline__ void row_store(const TaParams& p, const RowRef& q, int lane, float4 num, float den) {
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  const int gi = q.r / p.n, i = q.r % p.n;
+  *reinterpret_cast<float4*>(p.out + ((static_cast<size_t>(q.b) * p.n + i) * p.Hq + q.kvh * p.G + gi) * kD + lane * 4) =
+      make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
+}
+__device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xFFFFFFFFu, den, o);
-  if (lane == 0) s_red[warp] = den;
-  __syncthreads();
-  if (t == 0) {
-    float d0 = 0.f;
-#pragma unroll
-    for (int w = 0; w < kD / 32; ++w) d0 += s_red[w];
-    s_den = d0;
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+__global__ void __launch_bounds__(kCombineThreads) tree_attn_combine(TaParams p) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long long rows = static_cast<long long>(p.B) * p.Hkv * p.R;
+  if (p.maxseg <= kWarpRowSegs) {  // a warp per row
+    const long long stride = static_cast<long long>(gridDim.x) * kCombineWarps;
+    for (long long u = static_cast<long long>(blockIdx.x) * kCombineWarps + warp; u < rows; u += stride) {
+      const RowRef q = row_ref(p, u);
+      const float mx = warp_max(lane < q.nseg ? p.ml[((q.u0 + lane) * kRows + q.r) * 2] : -INFINITY);
+      float den = 0.f;
+      float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+      row_accumulate(p, q, mx, 0, 1, lane, num, den);
+      row_store(p, q, lane, num, den);
+    }
+    return;
   }
-  __syncthreads();
-  float num = 0.f;
-  for (int c = 0; c < nseg; ++c) num += s_w[c] * p.part[((u0 + c) * kRows + r) * kD + t];
-  const int gi = r / p.n, i = r % p.n;
-  p.out[((static_cast<size_t>(b) * p.n + i) * p.Hq + kvh * p.G + gi) * kD + t] = s_den > 0.f ? num / s_den : 0.f;
+  __shared__ float s_mx[kCombineWarps], s_den[kCombineWarps];
+  __shared__ float4 s_num[kCombineWarps][32];
+  for (long long u = blockIdx.x; u < rows; u += gridDim.x) {  // a CTA per row
+    const RowRef q = row_ref(p, u);
+    float mx = -INFINITY;
+    for (int c = threadIdx.x; c < q.nseg; c += kCombineThreads) mx = fmaxf(mx, p.ml[((q.u0 + c) * kRows + q.r) * 2]);
+    mx = warp_max(mx);
+    if (lane == 0) s_mx[warp] = mx;
+    __syncthreads();
+    mx = s_mx[0];
+#pragma unroll
+    for (int w = 1; w < kCombineWarps; ++w) mx = fmaxf(mx, s_mx[w]);
+    float den = 0.f;
+    float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+    row_accumulate(p, q, mx, warp, kCombineWarps, lane, num, den);
+    s_num[warp][lane] = num;
+    if (lane == 0) s_den[warp] = den;
+    __syncthreads();
+    if (warp == 0) {
+      float4 a = s_num[0][lane];
+      float d = s_den[0];
+#pragma unroll
+      for (int w = 1; w < kCombineWarps; ++w) {
+        const float4 b = s_num[w][lane];
+        a.x += b.x;
+        a.y += b.y;
+        a.z += b.z;
+        a.w += b.w;
+        d += s_den[w];
+      }
+      row_store(p, q, lane, a, d);
+    }
+    __syncthreads();  // s_mx, s_num and s_den are rewritten for the next row
+  }
 }
 
 struct TaPlan {
@@ -360,6 +417,8 @@ extern "C" dt_status dt_tree_attention(int B, int n, int L, int Hq, int Hkv, int
   const void* fa = reinterpret_cast<const void*>(tree_attn_partial);
   if (ensure_dynamic_smem(fa, sizeof(TaSmem)) != cudaSuccess) return DT_ERR_CUDA;
   tree_attn_partial<<<static_cast<unsigned>(P.grid), kThreadsA, sizeof(TaSmem), stream>>>(p);
-  tree_attn_combine<<<static_cast<unsigned>(static_cast<long long>(B) * Hkv * p.R), kD, 0, stream>>>(p);
+  const long long crows = static_cast<long long>(B) * Hkv * p.R, cper = P.maxseg <= kWarpRowSegs ? kCombineWarps : 1;
+  const long long cgrid = (crows + cper - 1) / cper, ccap = static_cast<long long>(kCombinePerSm) * di.sms;
+  tree_attn_combine<<<static_cast<unsigned>(cgrid < ccap ? cgrid : ccap), kCombineThreads, 0, stream>>>(p);
   return cuda_status(cudaGetLastError());
 }

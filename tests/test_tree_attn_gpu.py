@@ -51,3 +51,20 @@ def test_tree_attention_diagonal_mask_returns_own_values(dtlib):
     vf = v.float().numpy()
     for h in range(Hq):
         assert np.array_equal(out[:, :, h], vf[:, h // (Hq // Hkv)].astype(np.float64)), h
+
+
+def test_tree_attention_full_batch_sampled_requests(dtlib):
+    """The B = 64 configuration the bench times (its combine takes a warp per row): the whole batch on the GPU, two
+    sampled requests against the oracle one by one (requests are independent)."""
+    B, n, L, Hq, Hkv, d = 64, 16, 2048, 32, 8, 128
+    q, k, v, m = synth.make_attention_inputs(B, n, L, Hq, Hkv, d, seed=77)
+    scale = 1.0 / math.sqrt(d)
+    out = dtlib.dt_tree_attention(q.cuda(), k.cuda(), v.cuda(), m.cuda(), scale)
+    torch.cuda.synchronize()
+    out = out.cpu().numpy().astype(np.float64)
+    for b in (5, 63):
+        ref = orc.tree_attention(synth.bits_u16(q[b:b + 1]), synth.bits_u16(k[b:b + 1]), synth.bits_u16(v[b:b + 1]),
+                                 m[b:b + 1].numpy(), scale)
+        err = np.abs(out[b:b + 1] - ref)
+        assert err.max() <= TOL, (b, err.max())
+        assert err.mean() <= TOL / 10, (b, err.mean())
