@@ -436,12 +436,10 @@ def run_ours(args, world, rank, local):
     e2e = None
     if not args.no_e2e and not marginal:
         hr = dt.HostRound(s.B, s.K, s.V, s.M, s.n, s.max_depth, s.T, w, inp.logits.dtype, device=dev)
-        h_logits = dt.pinned_like(inp.logits)
-        h_logits.copy_(inp.logits)
-        h_h0 = dt.pinned_like(inp.h0)
-        h_h0.copy_(inp.h0)
+        hr.host_logits.copy_(inp.logits)  # the step's inputs, in the round's pinned input buffer
+        hr.host_h0.copy_(inp.h0)
         for _ in range(args.warmup):
-            hr.run(h_logits, h_h0)
+            hr.run()
         torch.cuda.synchronize()
         ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
@@ -449,7 +447,7 @@ def run_ours(args, world, rank, local):
         for i in range(args.steps):
             flush_l2()
             ev2[i][0].record(stream)
-            hr.run(h_logits, h_h0)
+            hr.run()
             ev2[i][1].record(stream)
         torch.cuda.synchronize()
         barrier()

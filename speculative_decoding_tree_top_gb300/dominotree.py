@@ -8,6 +8,7 @@ runs in the library's CUDA kernels; there is no fallback of any kind: without th
 from __future__ import annotations
 
 import ctypes
+import math
 import enum
 from dataclasses import dataclass
 from typing import Optional
@@ -455,30 +456,53 @@ class Round:
         _check(int(dt_get_error(self.workspace, stream)), "device status")
 
 
-def pinned_like(t: torch.Tensor) -> torch.Tensor:
-    return torch.empty(t.shape, dtype=t.dtype, device="cpu", pin_memory=True)
+def packed_buffers(specs, device, pin: bool = False):
+    """One byte buffer holding several tensors, each starting on a 16-byte boundary: ``specs`` is a list of (name,
+    shape, dtype). Returns the buffer and a dict of views into it. One copy of the buffer moves them all."""
+    offs, o = [], 0
+    for _, shape, dtype in specs:
+        nbytes = math.prod(shape) * torch.empty((), dtype=dtype).element_size()
+        offs.append((o, nbytes))
+        o += (nbytes + 15) // 16 * 16
+    if pin:
+        buf = torch.empty(o, dtype=torch.uint8, device="cpu", pin_memory=True)
+    else:
+        buf = torch.empty(o, dtype=torch.uint8, device=device)
+    views = {name: buf[off:off + nb].view(dtype).view(shape) for (name, shape, dtype), (off, nb) in zip(specs, offs)}
+    return buf, views
 
 
 class HostRound(Round):
-    """A round whose inputs and outputs live in (pinned) host memory: each call copies the logits and h0 to the
-    device, runs dt_round (dt_topm and dt_build_trees), and copies the tree back, all on one stream."""
+    """A round whose inputs and outputs live in pinned host memory: each call copies the logits and h0 to the device
+    (one copy: they sit in one buffer), runs dt_round (dt_topm and dt_build_trees), and copies the tree back (one
+    copy of one buffer), all on one stream. The caller writes a round's inputs into ``host_logits`` / ``host_h0``."""
 
     def __init__(self, B, K, V, M, n, max_depth, T, weights: Weights, logits_dtype, device="cuda"):
         super().__init__(B, K, V, M, n, max_depth, T, weights, device)
-        self.d_logits = torch.empty((B, K, V), dtype=logits_dtype, device=device)
-        self.d_h0 = torch.empty((B, weights.H), dtype=torch.float32, device=device)
-        self.host_out = {k: pinned_like(v) for k, v in self.out.items()}
+        ins = [("logits", (B, K, V), logits_dtype), ("h0", (B, weights.H), torch.float32)]
+        self._din, d = packed_buffers(ins, device)
+        self._hin, h = packed_buffers(ins, device, pin=True)
+        self.d_logits, self.d_h0 = d["logits"], d["h0"]
+        self.host_logits, self.host_h0 = h["logits"], h["h0"]
+        outs = [("tokens", (B, n), torch.int32), ("parents", (B, n), torch.int32), ("depth", (B, n), torch.int32),
+                ("scores", (B, n), torch.float32), ("mask", (B, n, n), torch.uint8)]
+        self._dout, self.out = packed_buffers(outs, device)
+        self._hout, self.host_out = packed_buffers(outs, device, pin=True)
 
     def h2d_bytes(self) -> int:
-        return self.d_logits.numel() * self.d_logits.element_size() + self.d_h0.numel() * 4
+        return self._hin.numel()
 
     def d2h_bytes(self) -> int:
-        return sum(v.numel() * v.element_size() for v in self.host_out.values())
+        return self._hout.numel()
 
-    def run(self, host_logits: torch.Tensor, host_h0: torch.Tensor, stream=None) -> dict:
-        self.d_logits.copy_(host_logits, non_blocking=True)
-        self.d_h0.copy_(host_h0, non_blocking=True)
-        out = self(self.d_logits, self.d_h0, stream)
-        for k, v in out.items():
-            self.host_out[k].copy_(v, non_blocking=True)
+    def run(self, host_logits: Optional[torch.Tensor] = None, host_h0: Optional[torch.Tensor] = None,
+            stream=None) -> dict:
+        """One round from the pinned inputs. Tensors passed here are first copied into them on the host."""
+        if host_logits is not None:
+            self.host_logits.copy_(host_logits)
+        if host_h0 is not None:
+            self.host_h0.copy_(host_h0)
+        self._din.copy_(self._hin, non_blocking=True)
+        self(self.d_logits, self.d_h0, stream)
+        self._hout.copy_(self._dout, non_blocking=True)
         return self.host_out

@@ -211,3 +211,21 @@ def test_tree_attention_rejects_bad_arguments(dtlib):
     assert call(d=64) == UNSUPPORTED
     assert call(n=17) == UNSUPPORTED                  # 4 query heads per key/value head x 17 nodes > 64 rows
     assert call(B=0) == OK
+
+
+def test_packed_buffers_align_every_view(dtlib):
+    """The host-round buffers: every view starts on a 16-byte boundary (the C ABI's rule) and they do not overlap."""
+    import torch
+    buf, v = dtlib.packed_buffers([("a", (3, 5), torch.int32), ("b", (7,), torch.uint8), ("c", (2, 3), torch.float32),
+                                   ("d", (1, 16, 16), torch.uint8)], "cpu")
+    base = buf.data_ptr()
+    spans = []
+    for name, t in v.items():
+        off = t.data_ptr() - base
+        assert off % 16 == 0, name
+        spans.append((off, off + t.numel() * t.element_size()))
+    spans.sort()
+    assert all(a[1] <= b[0] for a, b in zip(spans, spans[1:]))
+    assert spans[-1][1] <= buf.numel()
+    v["c"][1, 2] = 1.5
+    assert v["c"][1, 2].item() == 1.5 and v["a"].shape == (3, 5) and v["d"].dtype == torch.uint8

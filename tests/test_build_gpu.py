@@ -215,3 +215,21 @@ def test_round_matches_the_two_calls(dtlib, case):
     torch.cuda.synchronize()
     for k in ref[-1][0]:
         assert torch.equal(ref[-1][0][k], out[k]), k
+
+
+@pytest.mark.parametrize("config", [1, 0])
+def test_host_round_matches_the_device_round(dtlib, config):
+    """HostRound (inputs and outputs in one pinned buffer each, one copy each way) gives the device round's outputs
+    exactly, round after round."""
+    inp = synth.make_inputs(config, device="cuda")
+    s = inp.shape
+    w = dtlib.Weights.of(inp)
+    rnd = dtlib.Round(s.B, s.K, s.V, s.M, s.n, s.max_depth, s.T, w)
+    ref = {k: v.cpu() for k, v in rnd(inp.logits, inp.h0).items()}
+    hr = dtlib.HostRound(s.B, s.K, s.V, s.M, s.n, s.max_depth, s.T, w, inp.logits.dtype)
+    for _ in range(2):
+        out = hr.run(inp.logits.cpu(), inp.h0.cpu())
+        torch.cuda.synchronize()
+        hr.check()
+        for k in ref:
+            assert torch.equal(ref[k], out[k]), k
