@@ -248,14 +248,19 @@ dt_status dt_tree_attention(int B, int n, int L, int Hq, int Hkv, int d, const v
  * allocating library call): its scratch is one library-wide device array of DT_TOPM_STATIC_SCRATCH_BYTES bytes,
  * which every GPU that loads the library holds until the process exits. The caller still passes the logits and the
  * output arrays.
- *   - Sizes whose scratch (dt_topm_workspace_bytes(B,K,V,M)) exceeds the array return DT_ERR_UNSUPPORTED before
- *     any launch. For V = 151936 the array holds up to 817 rows (B·K) at M = 64 and 409 rows at M = 128; one
- *     request of 16 positions at M = 64 needs 321 KB of it.
- *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress, with that device
- *     current) and caches it; make that first call before any stream capture.
- *   - Every call shares the array and it keeps the previous call's contents; each call clears its header and
- *     per-row bounds (a cudaMemsetAsync on `stream`, 256 bytes plus 4 per row). Calls that may overlap on the GPU (other streams, other host
- *     threads) race on the array and must be serialised by the caller.
+ *   - Sizes whose scratch exceeds the array return DT_ERR_UNSUPPORTED before any launch. For V = 151936 the array
+ *     holds up to 3246 rows (B·K) of bf16 logits at M = 64 and 1630 at M = 128; fp32 logits need about four times
+ *     as much per row (817 rows at M = 64, 409 at M = 128). One request of 16 positions at M = 64 (bf16) uses 82 KB.
+ *   - The first call on a device (more precisely, in a device context) looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it with the context's unique id. That lookup
+ *     makes the device's primary context current if none is, and, under CUDA's lazy module loading, loads the
+ *     library's device code on that device, which is when the driver allocates the array and may synchronise the
+ *     device: make that first call during set-up, before any stream capture. A context created anew (for example
+ *     after cudaDeviceReset) gets a new id, so the next call looks the address up again.
+ *   - Every call shares the array and it keeps the previous call's contents; each call first clears the part that
+ *     must start at zero (a cudaMemsetAsync on `stream` of the 256-byte header and the per-row bounds and tickets,
+ *     4 + 4 bytes per row, each part rounded up to 256 bytes). Calls that may overlap on the GPU (other streams,
+ *     other host threads) race on the array and must be serialised by the caller.
  *   - A NaN among the logits is not reported (there is no caller-visible status word); use dt_topm to detect it.
  * ------------------------------------------------------------------------------------------------------------- */
 #define DT_TOPM_STATIC_SCRATCH_BYTES (16u << 20)

@@ -144,14 +144,22 @@ __device__ __forceinline__ void resolve_parents(PopRec* pops, const int* popidx,
   for (int i = t; i < n; i += nthreads) pops[i].parent = popidx[pops[i].parent];
 }
 
+// The default of request_step's pick hook: nothing happens when a pick is made.
+struct NoPickHook {
+  __device__ __forceinline__ void operator()(int, const Job&) const {}
+};
+
 // Called by one whole warp for request b once its wave's expansions are known. Pops best-first while the best node
 // of the frontier needs no expansion (a leaf of the depth limit, or the n-th pop) or is already expanded; then walks
 // on in the order best-first would follow on what is known (the frontier, plus the children of nodes expanded but
 // not popped yet, with the insertion indices they would get) and picks up to `kla` unexpanded nodes for the next
 // wave, the blocked best first. A pick takes an expansion slot; picks after the first keep enough slots free for
 // every pop still to come. The pops are exact whatever the picks: a pick only decides when children become known.
+// `on_pick(q, job)` runs in the lane that makes the q-th pick, as soon as it is made (the small-batch builder starts
+// the pick's input copies there, while the walk goes on).
+template <class OnPick = NoPickHook>
 __device__ inline void request_step(const ReqView& R, int b, int n, int M, int maxd, int X, int KM, int kla,
-                                    Job* jobs_out, WsHeader* hdr) {
+                                    Job* jobs_out, WsHeader* hdr, const OnPick& on_pick = OnPick()) {
   const int lane = threadIdx.x & 31;
   ReqCtl st = *R.ctl;
   LaneSrc ls = R.lanes[lane];
@@ -266,7 +274,9 @@ __device__ inline void request_step(const ReqView& R, int b, int n, int M, int m
           R.sdepth[x] = depth;
           R.popidx[x] = -2;
           R.kcount[x] = 0;
-          jobs_out[njobs] = Job{b, x, sc.hd.pslot, sc.hd.token, depth, sc.hd.score, {0, 0}};
+          const Job jb{b, x, sc.hd.pslot, sc.hd.token, depth, sc.hd.score, {0, 0}};
+          jobs_out[njobs] = jb;
+          on_pick(njobs, jb);
         }
         cursor_advance(R, ss, mg, KM, sc);
       }
@@ -326,7 +336,20 @@ struct Params {
   bool rows_smem;   // large-batch builder: the M gathered correction rows of a node are staged in shared memory
   int lookahead;    // expansions a request may run per wave (1 = one pop at a time)
   int xslots;       // expansion slots per request (expansion_slots(n))
-  int* hs_count;    // [B][xslots] units of each slot's hidden state published (small-batch builder)
+  int* hs_count;    // [xslots] per wave, the CTAs whose hidden-state units and correction shares are in (small batch)
+  // A whole round in one launch (dt_round, small batches): the top-M of `logits` [B,K,V] (the weights' dtype) runs
+  // first inside the builder's launch and writes the candidates to topm_ids / topm_vals (the arrays ids / vals
+  // point to), through the top-M region of the workspace (bounds, tickets, per-chunk counts and words). Null
+  // logits: the candidates are given (dt_build_trees).
+  const void* logits;
+  int32_t* topm_ids;
+  float* topm_vals;
+  uint32_t* t_bounds;
+  unsigned* t_tickets;
+  int* t_counts;
+  void* t_words;
+  int t_cap;
+  bool t_vec_ok;
   float* gru_part;  // [gru_tiles][kGruSplits][128][128] K-split partial gate sums of the tensor-core GRU
   unsigned* gru_ticket;  // [gru_tiles] CTAs of a tile that stored their partials in the current wave (tensor-core GRU)
   int gru_tiles;
@@ -499,6 +522,9 @@ inline BuildLayout build_layout(int B, int K, int V, int M, int n, int H, int E)
 // The small-batch builder (build_small.cu). Returns false when its shared-memory plan does not fit this device
 // (the caller then uses the general builder).
 bool small_builder_fits(const Params& p, const DeviceInfo& di);
+// Whether the small-batch builder can also run the round's top-M in its launch (p.logits set).
+bool small_round_fits(const Params& p, const DeviceInfo& di);
+// Launches the small-batch builder; with p.logits set, the whole round (top-M included) in that one launch.
 cudaError_t launch_small_builder(const Params& p, const DeviceInfo& di, cudaStream_t stream);
 
 }  // namespace dt

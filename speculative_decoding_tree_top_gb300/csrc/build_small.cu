@@ -132,6 +132,64 @@ __device__ __forceinline__ unsigned long long sibling_key(const Node& e) {
          static_cast<unsigned long long>(~static_cast<uint32_t>(e.token));
 }
 
+// A job's children ranked among themselves by one warp: a bitonic sort of their sibling keys (larger first; equal
+// keys, possible only when a row repeats an id, by the lower candidate index) over 32 * R elements, element i in
+// register i / 32 of lane i % 32; padding (index >= M) has key 0 and sorts last. The first kc go to out[0 .. kc).
+template <int R>
+__device__ __forceinline__ void rank_children_warp(const Node* kr, const unsigned long long* kk, int M, Node* out,
+                                                   int kc) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long k[R];
+  int m[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    m[r] = 32 * r + lane;
+    k[r] = m[r] < M ? kk[m[r]] : 0ull;
+  }
+  auto first = [](unsigned long long ka, int ma, unsigned long long kb, int mb) {
+    return (ka > kb) | ((ka == kb) & (ma < mb));
+  };
+#pragma unroll
+  for (int size = 2; size <= 32 * R; size <<= 1) {
+#pragma unroll
+    for (int j = size >> 1; j > 0; j >>= 1) {
+      if (j >= 32) {  // both elements of every pair sit in one lane: registers r and r + j / 32
+        const int jr = j >> 5;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          if (r & jr) continue;
+          const int r2 = r | jr;
+          const bool desc = ((32 * r + lane) & size) == 0;  // this block is sorted larger-first
+          if (first(k[r], m[r], k[r2], m[r2]) != desc) {
+            const unsigned long long tk = k[r];
+            k[r] = k[r2];
+            k[r2] = tk;
+            const int tm = m[r];
+            m[r] = m[r2];
+            m[r2] = tm;
+          }
+        }
+      } else {  // the pair spans lanes lane and lane ^ j, same register
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const unsigned long long ok = __shfl_xor_sync(0xFFFFFFFFu, k[r], j);
+          const int om = __shfl_xor_sync(0xFFFFFFFFu, m[r], j);
+          const bool desc = ((32 * r + lane) & size) == 0;
+          const bool lower = (lane & j) == 0;
+          const bool mine_first = first(k[r], m[r], ok, om);
+          if (mine_first != (lower == desc)) {
+            k[r] = ok;
+            m[r] = om;
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+    if (32 * r + lane < kc) out[32 * r + lane] = kr[m[r]];
+}
+
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                                uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -254,9 +312,14 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
                  static_cast<unsigned>(esize * E), &wbar);
     }
   }
-  // A return before the first GRU step leaves no copy in flight: this waits (bounded) for the weights.
-  auto drain = [&]() { mbar_wait(&wbar, 0, kCopyBudgetNs); };
+  // Before the CTA leaves, every bulk copy it issued must have landed (none may write shared memory after the exit):
+  // this waits (bounded) for the weight rows unless the GRU step already did, and for the next wave's inputs when
+  // `jobs_parity` >= 0 names the pending phase of their barrier.
   bool weights_in = false;
+  auto drain = [&](int jobs_parity) {
+    if (!weights_in) mbar_wait(&wbar, 0, kCopyBudgetNs);
+    if (jobs_parity >= 0) mbar_wait(&jbar, static_cast<unsigned>(jobs_parity), kCopyBudgetNs);
+  };
   // the embedding rows of the candidates of the first block positions (where the waves' jobs come from in the
   // shallow trees of drafting) into L2, spread over the CTAs: the wave transitions then read them from L2
   {
@@ -273,20 +336,20 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
       asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
     }
   }
-  // every wave's accumulators and the slots' publication counters start at zero; one grid barrier orders that
+  // every wave's accumulators and arrival counters start at zero; one grid barrier orders that
   {
     const size_t acc_words = static_cast<size_t>(X) * kJ * M * AS;
     for (size_t i = static_cast<size_t>(j) * kThreads + t; i < acc_words; i += static_cast<size_t>(G) * kThreads)
       p.acc[i] = 0;
-    for (size_t i = static_cast<size_t>(j) * kThreads + t; i < static_cast<size_t>(B) * X;
-         i += static_cast<size_t>(G) * kThreads)
-      p.hs_count[i] = 0;
+    for (int i = j * kThreads + t; i < X; i += G * kThreads) p.hs_count[i] = 0;
   }
-  // control state, identical in every CTA: the root of every request is expanded in wave 0
-  for (int b = t; b < B; b += kThreads) {
-    ctl[b] = ReqCtl{0, 0, M, 1, 0, {0, 0, 0}};  // the root's children take insertion indices 0 .. M - 1
-    jobs[b] = Job{b, 0, -1, 0, 0, 0.f, {0, 0}};
-  }
+  // control state, identical in every CTA: the root of every request is expanded in wave 0. A wave has S = B * kla job
+  // slots, slot b * kla + q holding request b's q-th expansion (b = -1: empty); the slot is the job's column of the
+  // GRU's MMA tile and its row of the staged inputs.
+  const int S = B * kla;
+  for (int b = t; b < B; b += kThreads) ctl[b] = ReqCtl{0, 0, M, 1, 0, {0, 0, 0}};  // root's children: 0 .. M - 1
+  for (int i = t; i < kJ; i += kThreads)
+    jobs[i] = (i < S && i % kla == 0) ? Job{i / kla, 0, -1, 0, 0, 0.f, {0, 0}} : Job{-1, 0, 0, 0, 0, 0.f, {0, 0}};
   for (int i = t; i < B * n; i += kThreads) pops[i] = PopRec{0, 0, 0, -INFINITY};
   for (int i = t; i < B * 32; i += kThreads) {  // lane 0: the merged list (empty), lane 1: the root's children
     const int l = i % 32;
@@ -299,30 +362,42 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
   }
   if (t == 0) s_J = B;
   if (!grid_barrier(p.hdr, G, p.timeout_ns, &s_flag)) {
-    drain();
+    drain(-1);
     return;
   }
+  const unsigned erow = static_cast<unsigned>(E * esize), hrow = static_cast<unsigned>(H * sizeof(float));
 
   for (int w = 0;; ++w) {
     __syncthreads();
-    const int J = s_J;
-    if (J == 0) break;
-    // the jobs' inputs, copied at the end of the previous wave (wave 0 expands the roots and reads none)
-    if (w > 0 && !mbar_wait(&jbar, (w - 1) & 1, kCopyBudgetNs)) {
+    const int J = s_J;  // expansions in this wave
+    if (J == 0) {
+      // the previous wave's barrier phase completes once its copies land (none were issued when nothing was picked)
+      if (w > 0) mbar_wait(&jbar, (w - 1) & 1, kCopyBudgetNs);
+      break;
+    }
+    // the jobs' inputs, copied while the previous wave picked them (wave 0 expands the roots and reads none); every
+    // thread waits, and the decision to leave is taken by the whole CTA at once
+    if (w > 0 && !__syncthreads_and(mbar_wait(&jbar, (w - 1) & 1, kCopyBudgetNs))) {
       record_error(p.hdr, DT_ERR_TIMEOUT);
       atomicExch(&p.hdr->abort, 1u);
-      if (!weights_in) drain();
+      drain((w - 1) & 1);  // the wave's input copies are still outstanding
       return;
     }
     long long* acc_w = p.acc + static_cast<size_t>(w) * kJ * M * AS;
     const bool roots = w == 0;  // wave 0 expands the roots (h = h0, no GRU step); later waves never do
     if (!roots && !weights_in) {  // the weight rows, before the first GRU step (bounded)
-      if (!mbar_wait(&wbar, 0, kCopyBudgetNs)) record_error(p.hdr, DT_ERR_TIMEOUT);
+      if (!__syncthreads_and(mbar_wait(&wbar, 0, kCopyBudgetNs))) {  // never compute on unstaged weights: leave
+        record_error(p.hdr, DT_ERR_TIMEOUT);
+        atomicExch(&p.hdr->abort, 1u);
+        drain(-1);
+        return;
+      }
       weights_in = true;
     }
     {  // a job deeper than the positions gathered so far: gather up to it and a few beyond (same in every CTA)
       int deepest = 0;
-      for (int q = 0; q < J; ++q) deepest = max(deepest, jobs[q].depth);
+      for (int q = 0; q < S; ++q)
+        if (jobs[q].b >= 0) deepest = max(deepest, jobs[q].depth);
       if (deepest >= wc_pos) {
         const int upto = min(maxd, deepest + kPrefetchPositions);
         gather_wc(wc_pos, upto);
@@ -338,7 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
       // the warps splitting the k16 steps. A = this CTA's gate rows (rows past R repeat row R - 1: their outputs are
       // not used), B = the jobs' embedding rows (input side) and the parents' fp32 states as bf16 hi + lo pairs
       // (hidden side); each side has its own accumulator, the n gate needs them apart. A job's column never mixes
-      // with another's, so its sums do not depend on which jobs share the wave.
+      // with another's, so its sums do not depend on which jobs share the wave (an empty slot's column is computed
+      // on whatever its rows hold, and never used).
       const int g = lane >> 2, tg = lane & 3, R = 3 * umax;
       float din[4] = {0.f, 0.f, 0.f, 0.f}, dh[4] = {0.f, 0.f, 0.f, 0.f};
       {
@@ -377,8 +453,8 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
       *reinterpret_cast<float2*>(rw + (kMaxRows + g + 8) * kJ + 2 * tg) = make_float2(dh[2], dh[3]);
     }
     if (!roots && !mma && warp < 3 * umax) {
-      // One warp per gate row (R <= 16 rows, 16 warps), every job against the row: the lanes stride over K, one
-      // accumulator per job and side, then one shuffle tree each. A job's sums do not depend on the other jobs.
+      // One warp per gate row (R <= 16 rows, 16 warps), every job slot against the row: the lanes stride over K, one
+      // accumulator per slot and side, then one shuffle tree each. A job's sums do not depend on the other jobs.
       // The row's input side (over E) and hidden side (over H) stay apart: the n gate needs them separately.
       const int r = warp;
       constexpr int kPer = kBf16 ? 8 : 4;
@@ -396,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
           const float w6 = __uint_as_float(wv.w << 16), w7 = __uint_as_float(wv.w & 0xFFFF0000u);
 #pragma unroll
           for (int q = 0; q < kJ; ++q) {
-            if (q >= J) break;
+            if (q >= S) break;
             const uint4 xv = *reinterpret_cast<const uint4*>(xe + static_cast<size_t>(q) * SE + c);
             float a = ai[q];
             a = fmaf(w0, __uint_as_float(xv.x << 16), a);
@@ -413,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
           const float4 wv = *reinterpret_cast<const float4*>(wr + c);
 #pragma unroll
           for (int q = 0; q < kJ; ++q) {
-            if (q >= J) break;
+            if (q >= S) break;
             const float4 xv = *reinterpret_cast<const float4*>(xe + static_cast<size_t>(q) * SE + c);
             float a = ai[q];
             a = fmaf(wv.x, xv.x, a);
@@ -435,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
           const float w6 = __uint_as_float(wv.w << 16), w7 = __uint_as_float(wv.w & 0xFFFF0000u);
 #pragma unroll
           for (int q = 0; q < kJ; ++q) {
-            if (q >= J) break;
+            if (q >= S) break;
             const float4 x0 = *reinterpret_cast<const float4*>(xh + static_cast<size_t>(q) * H + c);
             const float4 x1 = *reinterpret_cast<const float4*>(xh + static_cast<size_t>(q) * H + c + 4);
             float a = ah[q];
@@ -453,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
           const float4 wv = *reinterpret_cast<const float4*>(hr + c);
 #pragma unroll
           for (int q = 0; q < kJ; ++q) {
-            if (q >= J) break;
+            if (q >= S) break;
             const float4 xv = *reinterpret_cast<const float4*>(xh + static_cast<size_t>(q) * H + c);
             float a = ah[q];
             a = fmaf(wv.x, xv.x, a);
@@ -466,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
       }
 #pragma unroll
       for (int q = 0; q < kJ; ++q) {
-        if (q >= J) break;
+        if (q >= S) break;
         float si = ai[q], sh = ah[q];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
@@ -481,8 +557,8 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
     }
     __syncthreads();
     if (!roots && mma) {  // the partial tiles summed over the warps in a fixed order
-      for (int i = t; i < 2 * 3 * umax * J; i += kThreads) {
-        const int side = i / (3 * umax * J), r = (i / J) % (3 * umax), q = i % J;
+      for (int i = t; i < 2 * 3 * umax * S; i += kThreads) {
+        const int side = i / (3 * umax * S), r = (i / S) % (3 * umax), q = i % S;
         float v = 0.f;
 #pragma unroll
         for (int w2 = 0; w2 < kWarps; ++w2) v += red[(w2 * 2 + side) * kMaxRows * kJ + r * kJ + q];
@@ -490,12 +566,12 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
       }
     }
     __syncthreads();
-    // the GRU pointwise of the owned units (root jobs: h0), published unit by unit: a release reduction orders the
-    // store before the count (H units in all)
-    for (int i = t; i < J * umax; i += kThreads) {
+    // the GRU pointwise of the owned units (root jobs: h0), stored to the slot's hidden state; the CTA's arrival on
+    // the wave's counter below publishes them together with the correction shares
+    for (int i = t; i < S * umax; i += kThreads) {
       const int q = i / umax, u = i % umax;
-      if (u >= nu) continue;
       const Job jb = jobs[q];
+      if (u >= nu || jb.b < 0) continue;
       float hn;
       if (roots) {
         hn = __ldg(p.h0 + static_cast<size_t>(jb.b) * H + u0 + u);
@@ -508,53 +584,58 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
         hn = (1.f - zg) * g + zg * xh[static_cast<size_t>(q) * H + u0 + u];
       }
       hb[q * umax + u] = hn;
-      const size_t slot = static_cast<size_t>(jb.b) * X + jb.xslot;
-      p.hs[slot * H + u0 + u] = hn;
-      asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p.hs_count + slot) : "memory");
+      p.hs[(static_cast<size_t>(jb.b) * X + jb.xslot) * H + u0 + u] = hn;
     }
     __syncthreads();
     // this CTA's units' part of W_c[id]·h for the M candidates of each job's block position
-    for (int i = t; i < J * M; i += kThreads) {
+    for (int i = t; i < S * M; i += kThreads) {
       const int q = i / M, m = i % M;
       const Job jb = jobs[q];
+      if (jb.b < 0) continue;
       const T* wcp = wc + ((static_cast<size_t>(jb.b) * maxd + jb.depth) * M + m) * umax;
       float v = 0.f;
       for (int u = 0; u < nu; ++u) v = fmaf(WT<kBf16>::f(wcp[u]), hb[q * umax + u], v);
       add_share(p, acc_w + (static_cast<size_t>(q) * M + m) * AS, v);
     }
+    // One arrival per CTA and wave (release: the hidden-state units and the shares above come first). A CTA that
+    // sees G arrivals (acquire) sees every share of every candidate and every unit of the wave's hidden states.
+    __syncthreads();
+    if (t == 0) asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p.hs_count + w) : "memory");
+    if (t == 0) {
+      int ok = 1;
+      const unsigned* cnt = reinterpret_cast<const unsigned*>(p.hs_count + w);
+      const uint64_t t0 = global_timer_ns();
+      for (unsigned polls = 1; ld_acquire_gpu(cnt) < static_cast<unsigned>(G); ++polls)
+        if ((polls & 15u) == 0u && (ld_acquire_gpu(&p.hdr->abort) != 0u || global_timer_ns() - t0 > p.timeout_ns)) {
+          record_error(p.hdr, DT_ERR_TIMEOUT);
+          atomicExch(&p.hdr->abort, 1u);
+          ok = 0;
+          break;
+        }
+      s_flag = ok;
+    }
+    __syncthreads();
+    if (!s_flag) {  // a wait ran out (recorded): leave with no copy in flight
+      drain(-1);
+      return;
+    }
 
     // ---- phase C: every CTA finishes the wave (replicated) ----
-    // (1) one warp per job: all G shares of every candidate (each lane polls its slots, every read of a round in
-    //     flight together) and the job's published hidden state, then the restricted log-softmax and the children
-    int ok = 1;
-    if (warp < J) {
+    // (1) one warp per job: the corrected logits from the completed sums, the restricted log-softmax, the children;
+    //     for M <= 128 the same warp ranks them (a bitonic sort of 64-bit sibling keys across its lanes) and keeps the
+    //     first kc: at most n - s - 1 of them can still be popped after the job's node itself (n for the root's)
+    if (warp < S && jobs[warp].b >= 0) {
       const int q = warp;
       const Job jb = jobs[q];
       const size_t off = (static_cast<size_t>(jb.b) * maxd + jb.depth) * M;  // staged ids / base logits
-      auto complete = [&](long long v) { return (v & 0xFF) == (G & 0xFF); };
       const long long* slots = acc_w + static_cast<size_t>(q) * M * AS;
-      const unsigned* hcnt = reinterpret_cast<const unsigned*>(p.hs_count) + static_cast<size_t>(jb.b) * X + jb.xslot;
       float mx = -INFINITY;
       for (int m0 = lane; m0 < M; m0 += 128) {
         long long a[4];
-        bool done = false;
-        const uint64_t t0 = global_timer_ns();
-        for (unsigned polls = 0; !done; ++polls) {
-          done = true;
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            const int m = m0 + 32 * jj;
-            a[jj] = m < M ? ld_relaxed_s64(slots + static_cast<size_t>(m) * AS) : static_cast<long long>(G & 0xFF);
-            done &= complete(a[jj]);
-          }
-          if (lane == 0 && m0 == 0) done &= ld_acquire_gpu(hcnt) >= static_cast<unsigned>(H);
-          if (!done && (polls & 15u) == 15u &&
-              (ld_acquire_gpu(&p.hdr->abort) != 0u || global_timer_ns() - t0 > p.timeout_ns)) {
-            record_error(p.hdr, DT_ERR_TIMEOUT);
-            atomicExch(&p.hdr->abort, 1u);
-            ok = 0;
-            break;
-          }
+        for (int jj = 0; jj < 4; ++jj) {
+          const int m = m0 + 32 * jj;
+          a[jj] = m < M ? ld_relaxed_s64(slots + static_cast<size_t>(m) * AS) : 0ll;
         }
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
@@ -565,7 +646,6 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
           mx = fmaxf(mx, v);
         }
       }
-      ok = __all_sync(0xFFFFFFFFu, ok);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
       float sum = 0.f;
@@ -583,21 +663,28 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
         kraw[q * M + m] = e;
         kkey[q * M + m] = sibling_key(e);
       }
+      if (M <= 128) {
+        __syncwarp();
+        const int rem = roots ? n : n - ctl[jb.b].s - 1;
+        const int kc = min(min(M, KM), rem);
+        Node* out = kids + (static_cast<size_t>(jb.b) * X + jb.xslot) * KM;
+        if (M <= 32) rank_children_warp<1>(kraw + q * M, kkey + q * M, M, out, kc);
+        else if (M <= 64) rank_children_warp<2>(kraw + q * M, kkey + q * M, M, out, kc);
+        else rank_children_warp<4>(kraw + q * M, kkey + q * M, M, out, kc);
+        if (lane == 0) kcount[jb.b * X + jb.xslot] = kc;
+      }
     }
-    if (!__syncthreads_and(ok)) {  // a wait ran out (recorded): leave with no copy in flight
-      if (!weights_in) drain();
-      return;
-    }
-    // (2) every job's children ranked among themselves by their sibling keys (tpe threads per child), the first kc
-    //     kept: at most n - s - 1 of them can still be popped after the job's node itself (n for the root's)
-    {
+    __syncthreads();
+    // (2) M > 128: every job's children ranked among themselves by their sibling keys (tpe threads per child)
+    if (M > 128) {
       int tpe = 1;
-      while (tpe < 32 && tpe * 2 * J * M <= kThreads) tpe *= 2;
-      for (int base = 0; base < J * M * tpe; base += kThreads) {  // uniform bounds: every lane reaches the shuffles
+      while (tpe < 32 && tpe * 2 * S * M <= kThreads) tpe *= 2;
+      for (int base = 0; base < S * M * tpe; base += kThreads) {  // uniform bounds: every lane reaches the shuffles
         const int slot = base + t, i = slot / tpe, part = slot % tpe;
         const int q = i / M, mi = i % M;
+        const bool live = i < S * M && jobs[q < S ? q : 0].b >= 0;
         int r = 0;
-        if (i < J * M) {
+        if (live) {
           const unsigned long long ki = kkey[i];
           const unsigned long long* sib = kkey + q * M;
 #pragma unroll 8
@@ -607,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
           }
         }
         for (int o = 1; o < tpe; o <<= 1) r += __shfl_xor_sync(0xFFFFFFFFu, r, o);
-        if (i < J * M && part == 0) {
+        if (live && part == 0) {
           const Job jb = jobs[q];
           const int rem = roots ? n : n - ctl[jb.b].s - 1;
           const int kc = min(min(M, KM), rem);
@@ -615,45 +702,45 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
           if (r == 0) kcount[jb.b * X + jb.xslot] = kc;
         }
       }
+      __syncthreads();
     }
-    __syncthreads();
-    // (3) one warp per request: pops, then the next wave's picks
+    // (3) one warp per request: pops, then the next wave's picks. Each pick's inputs (its embedding row and its
+    //     parent's hidden state) are copied into the pick's job slot as soon as the pick is made, on jbar: the copies
+    //     overlap the rest of the walk. This wave's generic reads of those rows (phase A) and the other CTAs' stores
+    //     of the hidden states (acquired above) are ordered before the asynchronous copies by the proxy fences.
     if (warp < B) {
       const int b = warp;
       const ReqView R{ctl + b, lanes + b * 32, merged + static_cast<size_t>(b) * 2 * n,
                       kids + static_cast<size_t>(b) * X * KM, kcount + b * X, popidx + b * X, sdepth + b * X,
                       pops + static_cast<size_t>(b) * n};
-      request_step(R, b, n, M, maxd, X, KM, kla, jobs + b * kla, p.hdr);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      const auto start_copies = [&](int q, const Job& jb) {
+        const int slot = b * kla + q;
+        mbar_expect_tx_only(&jbar, erow + hrow);
+        bulk_g2s(xe + static_cast<size_t>(slot) * SE, static_cast<const char*>(p.emb) + static_cast<size_t>(jb.token) * erow,
+                 erow, &jbar);
+        bulk_g2s(xh + static_cast<size_t>(slot) * H, p.hs + (static_cast<size_t>(b) * X + jb.pslot) * H, hrow, &jbar);
+      };
+      request_step(R, b, n, M, maxd, X, KM, kla, jobs + b * kla, p.hdr, start_copies);
+      __syncwarp();
+      const int nj = ctl[b].njobs;
+      if (lane < kla && lane >= nj) jobs[b * kla + lane].b = -1;  // the request's slots left empty next wave
     }
     __syncthreads();
-    // the next wave's jobs, packed in request order; their inputs (embedding rows, parents' hidden states) in flight
-    // the next wave's jobs, packed in request order, and their inputs (embedding rows, parents' hidden states) as
-    // one bulk copy each, completing on jbar; every slot a wave can use was checked against X when it was taken
     if (t == 0) {
       int J2 = 0;
-      for (int b = 0; b < B; ++b)
-        for (int q = 0; q < ctl[b].njobs; ++q) jobs[J2++] = jobs[b * kla + q];
+      for (int b = 0; b < B; ++b) J2 += ctl[b].njobs;
       if (J2 > 0 && w + 1 >= X) {  // cannot happen: every wave expands at least one of a request's X slots
         record_error(p.hdr, DT_ERR_INVALID_ARG);
         J2 = 0;
       }
-      if (J2 > 0) {
-        const unsigned erow = static_cast<unsigned>(E * esize), hrow = static_cast<unsigned>(H * sizeof(float));
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // phase A's reads of xe / xh came first
-        asm volatile("fence.proxy.async.global;" ::: "memory");      // the states were stored by the generic proxy
-        mbar_expect_tx(&jbar, static_cast<unsigned>(J2) * (erow + hrow));
-        for (int q = 0; q < J2; ++q) {
-          const Job jb = jobs[q];
-          bulk_g2s(xe + static_cast<size_t>(q) * SE, static_cast<const char*>(p.emb) + static_cast<size_t>(jb.token) * erow,
-                   erow, &jbar);
-          bulk_g2s(xh + static_cast<size_t>(q) * H, p.hs + (static_cast<size_t>(jb.b) * X + jb.pslot) * H, hrow, &jbar);
-        }
-      }
+      mbar_arrive(&jbar);  // the phase completes once every copy the picks started has landed
       s_J = J2;
     }
   }
 
-  if (!weights_in) drain();  // a round without GRU steps (n = 1, or max depth 1) never waited for them
+  drain(-1);  // a round without GRU steps (n = 1, or max depth 1) never waited for the weights
   // ---- outputs (CTA 0): nodes in pop order, and the ancestor mask by walking each node's parent chain ----
   if (j == 0) {
     for (int b = 0; b < B; ++b) resolve_parents(pops + b * n, popidx + b * X, n, t, kThreads);

@@ -73,16 +73,18 @@ struct SelectSmem {                           // lives in the caller's shared me
   int off[kMaxChunks + 1];
   unsigned hist[256];
   unsigned sel[2];
-  unsigned red[2][kSelThreads / 32];          // per-warp key minima and maxima
+  unsigned red[2][16];                        // per-warp key minima and maxima (up to 512 threads)
 };
 
 // The row's selection over `chunks` lists of candidate words: cnt[c] words in list c, word i of list c given by
 // load(c, i) as a 64-bit row word (value key << 32 | ~id). kBf16: the keys are bf16 keys (16 bits), else fp32 keys.
-// Writes the row's M ids and values (in order) to ids[0..M), vals[0..M). Called by all kSelThreads threads.
-template <bool kBf16, class Load>
+// Writes the row's M ids and values (in order) to ids[0..M), vals[0..M). Called by all kThreads threads (256 or 512;
+// s_warp holds kThreads / 32 ints).
+template <bool kBf16, int kThreads, class Load>
 __device__ void select_words(const int* __restrict__ cnt, int chunks, int M, Load load, int32_t* __restrict__ ids,
                              float* __restrict__ vals, SelectSmem& S, int* s_warp, int* s_n_ptr) {
-  constexpr int kWarps = kSelThreads / 32;
+  static_assert(kThreads >= 256 && kThreads <= 512 && kThreads % 32 == 0, "one histogram bin per thread at most");
+  constexpr int kWarps = kThreads / 32;
   constexpr int kTopDigit = kBf16 ? 5 : 7;  // bf16 keys are 16 bits: word bits 48..63 are zero
   uint64_t* w = S.w;
   uint64_t* top = S.top;
@@ -110,14 +112,14 @@ __device__ void select_words(const int* __restrict__ cnt, int chunks, int M, Loa
     }
   } else {
     int mine = 0;
-    for (int c = t; c < chunks; c += kSelThreads) mine += __ldcg(cnt + c);
+    for (int c = t; c < chunks; c += kThreads) mine += __ldcg(cnt + c);
     total = block_sum<kWarps>(mine, s_warp);
   }
   if (t == 0) s_n = 0;
   __syncthreads();
   const bool in_smem = few && total <= kSelCap;
   if (in_smem) {
-    for (int i = t; i < total; i += kSelThreads) {
+    for (int i = t; i < total; i += kThreads) {
       int lo = 0, hi = chunks - 1;  // the chunk holding candidate i: the last offset <= i
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -130,11 +132,11 @@ __device__ void select_words(const int* __restrict__ cnt, int chunks, int M, Loa
   __syncthreads();
   auto for_each = [&](auto&& f) {
     if (in_smem) {
-      for (int i = t; i < total; i += kSelThreads) f(w[i]);
+      for (int i = t; i < total; i += kThreads) f(w[i]);
     } else {
       for (int c = 0; c < chunks; ++c) {
         const int nc = __ldcg(cnt + c);
-        for (int i = t; i < nc; i += kSelThreads) f(load(c, i));
+        for (int i = t; i < nc; i += kThreads) f(load(c, i));
       }
     }
   };
@@ -143,7 +145,7 @@ __device__ void select_words(const int* __restrict__ cnt, int chunks, int M, Loa
   if (total > M && in_smem) {
     // the candidates' key range, then one histogram relative to its minimum
     uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-    for (int i = t; i < total; i += kSelThreads) {
+    for (int i = t; i < total; i += kThreads) {
       const uint32_t k = candidate_key(w[i]);
       kmin = min(kmin, k);
       kmax = max(kmax, k);
@@ -154,7 +156,7 @@ __device__ void select_words(const int* __restrict__ cnt, int chunks, int M, Loa
       S.red[0][warp] = kmin;
       S.red[1][warp] = kmax;
     }
-    hist[t] = 0u;  // kSelThreads == 256 bins
+    if (t < 256) hist[t] = 0u;
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < kWarps; ++i) {
@@ -163,7 +165,7 @@ __device__ void select_words(const int* __restrict__ cnt, int chunks, int M, Loa
     }
     int shift = 0;
     while (((kmax - kmin) >> shift) > 255u) ++shift;
-    for (int i = t; i < total; i += kSelThreads) atomicAdd(&hist[(candidate_key(w[i]) - kmin) >> shift], 1u);
+    for (int i = t; i < total; i += kThreads) atomicAdd(&hist[(candidate_key(w[i]) - kmin) >> shift], 1u);
     __syncthreads();
     if (t < 32) {  // lane L holds bins 255 - 8L down to 248 - 8L: counts from the top
       unsigned cb[8], sum = 0;
@@ -196,7 +198,7 @@ __device__ void select_words(const int* __restrict__ cnt, int chunks, int M, Loa
     uint64_t prefix = 0, pmask = 0;
     int need = M;
     for (int d = kTopDigit; d >= 0; --d) {
-      for (int i = t; i < 256; i += kSelThreads) hist[i] = 0u;
+      for (int i = t; i < 256; i += kThreads) hist[i] = 0u;
       __syncthreads();
       for_each([&](uint64_t wd) {
         if ((wd & pmask) == prefix) atomicAdd(&hist[(wd >> (8 * d)) & 255u], 1u);
@@ -244,9 +246,9 @@ __device__ void select_words(const int* __restrict__ cnt, int chunks, int M, Loa
   const int m = s_n;  // the words ranked: min(M, total) up to the ranking buffer
   uint64_t* sorted = w;  // the row's words are no longer needed
   __syncthreads();
-  rank_and_emit<kSelThreads>(top, m, M, sorted);
+  rank_and_emit<kThreads>(top, m, M, sorted);
   __syncthreads();
-  emit_final<kBf16, kSelThreads>(sorted, M, ids, vals);
+  emit_final<kBf16, kThreads>(sorted, M, ids, vals);
 }
 
 }  // namespace

@@ -76,6 +76,31 @@ def test_topm_rejects_bad_arguments(dtlib):
     assert _topm(L, B=0) == OK                        # nothing to do, nothing launched
 
 
+def test_static_topm_rejects_bad_arguments(dtlib):
+    """dt_topm_static's own checks, all made on the host before any CUDA call (no GPU here)."""
+    L = dtlib.lib()
+
+    def call(logits=A, dtype=1, B=1, K=2, V=100, M=5, ids=A, vals=A):
+        return L.dt_topm_static(logits, dtype, B, K, V, M, ids, vals, None)
+    assert call(M=0) == INVALID
+    assert call(M=101) == INVALID                     # more candidates than vocabulary
+    assert call(K=0) == INVALID
+    assert call(B=-1) == INVALID
+    assert call(dtype=7) == INVALID
+    assert call(logits=None) == INVALID
+    assert call(ids=None) == INVALID
+    assert call(vals=None) == INVALID
+    assert call(logits=A + 8) == INVALID              # misaligned
+    assert call(ids=A + 4) == INVALID
+    assert call(vals=A + 2) == INVALID
+    assert call(V=5000, M=2000) == UNSUPPORTED        # M above DT_MAX_M
+    # beyond the fixed array: the limits are per dtype (fp32 words are twice as wide and its chunks half as long)
+    assert call(dtype=0, B=1, K=818, V=151936, M=64) == UNSUPPORTED
+    assert call(dtype=1, B=1, K=3247, V=151936, M=64) == UNSUPPORTED
+    assert call(dtype=1, B=1, K=1631, V=151936, M=128) == UNSUPPORTED
+    assert call(B=0) == OK                            # nothing to do, nothing launched
+
+
 def _weights(dtlib, H=32, E=32, dtype=1, b_ih=None, emb=A):
     return dtlib._Weights(H, E, dtype, emb, A, A, b_ih, None, A)
 
