@@ -40,7 +40,8 @@ struct Job {
   int token;    // its token: the GRU input
   int depth;    // its depth: the children take block position `depth`
   float score;  // its cumulative score
-  int pad[2];
+  int aux[2];   // aux[0], small-batch builder: 1 + the node's candidate index among the root's children when wave 0
+                // expands it speculatively (its score is known only once the root's children are scored), else 0
 };
 
 // Warp-wide best of one candidate per lane (`has` false: none), in pop order: higher score (-0.0 equal to +0.0),
@@ -337,6 +338,7 @@ struct Params {
   int lookahead;    // expansions a request may run per wave (1 = one pop at a time)
   int xslots;       // expansion slots per request (expansion_slots(n))
   int* hs_count;    // [xslots] per wave, the CTAs whose hidden-state units and correction shares are in (small batch)
+  unsigned* ready;  // [B*K] whole-round launch: 1 once the row's top-M is selected (cleared at launch)
   // A whole round in one launch (dt_round, small batches): the top-M of `logits` [B,K,V] (the weights' dtype) runs
   // first inside the builder's launch and writes the candidates to topm_ids / topm_vals (the arrays ids / vals
   // point to), through the top-M region of the workspace (bounds, tickets, per-chunk counts and words). Null
@@ -503,8 +505,8 @@ inline BuildLayout build_layout(int B, int K, int V, int M, int n, int H, int E)
   L.hs = topm_layout(B, K, V, M).bytes;
   const size_t acc_bytes = B <= kSmallMaxB ? sizeof(long long) * X * kWaveJobs * M * acc_stride(M, n) : 0;
   L.acc = align_up(L.hs + sizeof(float) * static_cast<size_t>(B) * X * H);
-  L.hs_count = align_up(L.acc + acc_bytes);
-  L.rstate = align_up(L.hs_count + (B <= kSmallMaxB ? sizeof(int) * static_cast<size_t>(B) * X : 0));
+  L.hs_count = align_up(L.acc + acc_bytes);  // the per-wave counters, then the top-M rows' ready flags
+  L.rstate = align_up(L.hs_count + (B <= kSmallMaxB ? sizeof(int) * (X + static_cast<size_t>(B) * K) : 0));
   // both builders may run for small batches (the small one needs shared memory the device may not have)
   L.joblist = align_up(L.rstate + req_layout(n, static_cast<int>(X), KM, kLargeLookahead).bytes * B);
   L.jobcount = align_up(L.joblist + sizeof(Job) * 2 * static_cast<size_t>(B) * kLargeLookahead);

@@ -34,6 +34,7 @@
 #include <type_traits>
 
 #include "build_common.cuh"
+#include "topm_filter.cuh"
 
 namespace dt {
 namespace {
@@ -46,6 +47,11 @@ constexpr int kRowPad = 8;    // elements of padding per shared-memory weight ro
 constexpr int kJ = kWaveJobs;
 static_assert(kJ == 8, "a wave's jobs are the n8 tile of the GRU MMA");
 constexpr int kPrefetchPositions = 4;  // block positions whose candidates' embedding rows are prefetched at launch
+// A whole round in one launch: the top-M's chunks are 512 threads x 8 groups of 16 bytes (32768 bf16 or 16384 fp32
+// logits, never more chunks per row than the workspace's top-M region holds), staged where the waves' state goes later.
+constexpr int kFuseGroups = 8;
+constexpr size_t kFuseStageBytes = static_cast<size_t>(kThreads) * kFuseGroups * 16;
+static_assert(sizeof(SelectSmem) <= kFuseStageBytes, "the row's selection fits the staged chunk's space");
 
 // Shared-memory plan of one CTA (identical on host and device).
 struct Plan {
@@ -207,7 +213,9 @@ __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, u
   lo = static_cast<uint32_t>(__bfloat16_as_ushort(l0)) | (static_cast<uint32_t>(__bfloat16_as_ushort(l1)) << 16);
 }
 
-template <bool kBf16, bool kMma>  // kMma: bf16 weights with E and H multiples of 16 (tensor-core GRU)
+// kMma: bf16 weights with E and H multiples of 16 (tensor-core GRU); kFused: the round's top-M runs in this launch
+// (logits of the weights' dtype)
+template <bool kBf16, bool kMma, bool kFused>
 __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
   using T = typename WT<kBf16>::T;
   extern __shared__ __align__(16) unsigned char smem[];
@@ -257,22 +265,48 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
     mbar_fence_init();
   }
   __syncthreads();
-  // The launch's loads in the order they are needed: the candidate ids and base logits (and the biases), then the
-  // owned units' W_c columns of every candidate (they depend on the ids), then the GRU weight rows, which the first
-  // GRU step (wave 1) only needs: the dependent chain is not queued behind 9.4 MB of weights.
   for (int i = t; i < 3 * umax; i += kThreads) {
     const int g = i / umax, u = i % umax;
     const size_t row = static_cast<size_t>(g) * H + u0 + u;
     bias[2 * i] = (u < nu && p.b_ih) ? ldw(p.b_ih, kBf16, row) : 0.f;
     bias[2 * i + 1] = (u < nu && p.b_hh) ? ldw(p.b_hh, kBf16, row) : 0.f;
   }
-  for (int i = t; i < B * maxd * M; i += kThreads) {
-    const int b = i / (maxd * M), pos = (i / M) % maxd, m = i % M;
-    const size_t gi = (static_cast<size_t>(b) * K + pos) * M + m;
-    ids_s[i] = valid_id(p, __ldg(p.ids + gi));
-    vals_s[i] = __ldg(p.vals + gi);
-  }
-  __syncthreads();
+  // the candidates' ids and base logits of every request and position the tree can reach, into shared memory (read
+  // through L2: in a whole-round launch they were written earlier in the same launch)
+  auto load_candidates = [&](int p0, int p1) {  // block positions [p0, p1)
+    const int np = p1 - p0;
+    for (int i = t; i < B * np * M; i += kThreads) {
+      const int b = i / (np * M), pos = p0 + (i / M) % np, m = i % M;
+      const size_t gi = (static_cast<size_t>(b) * K + pos) * M + m;
+      const int si = (b * maxd + pos) * M + m;
+      ids_s[si] = valid_id(p, __ldcg(p.ids + gi));
+      vals_s[si] = __ldcg(p.vals + gi);
+    }
+  };
+  // whole-round launch: waits (bounded, abort-aware) until the top-M rows of block positions [p0, p1) of every
+  // request are selected; false in every thread when a wait ran out (recorded)
+  auto wait_rows = [&](int p0, int p1) -> bool {
+    int ok = 1;
+    for (int i = t; i < B * (p1 - p0); i += kThreads) {
+      const unsigned* f = p.ready + static_cast<size_t>(i % B) * K + p0 + i / B;
+      if (p.timeout_ns == 0) {
+        ok = 0;
+      } else {
+        const uint64_t t0 = global_timer_ns();
+        for (unsigned polls = 1; ld_acquire_gpu(f) == 0u; ++polls)
+          if ((polls & 15u) == 0u && (ld_acquire_gpu(&p.hdr->abort) != 0u || global_timer_ns() - t0 > p.timeout_ns)) {
+            ok = 0;
+            break;
+          }
+      }
+      if (!ok) {
+        record_error(p.hdr, DT_ERR_TIMEOUT);
+        atomicExch(&p.hdr->abort, 1u);
+        break;
+      }
+    }
+    return __syncthreads_and(ok) != 0;
+  };
   // The owned units' W_c columns of the candidates of block positions [p0, p1): each needed row comes into L2 once
   // (one bulk prefetch per row, spread over the CTAs, so HBM serves whole rows), then every CTA takes its columns.
   auto gather_wc = [&](int p0, int p1) {
@@ -293,11 +327,10 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
       wc[c * umax + u] = u < nu ? static_cast<const T*>(p.w_c)[static_cast<size_t>(ids_s[c]) * H + u0 + u] : T(0);
     }
   };
-  int wc_pos = maxd < kPrefetchPositions ? maxd : kPrefetchPositions;  // positions gathered so far
-  gather_wc(0, wc_pos);
   // the 3 * nu rows of W_ih and of W_hh as bulk copies (1 to 8 KB each) completing on one mbarrier, issued by warp 0;
   // waited for before the first GRU step
-  if (warp == 0) {
+  auto issue_weights = [&]() {
+    if (warp != 0) return;
     if (lane == 0) mbar_expect_tx(&wbar, static_cast<unsigned>(3 * nu * (E + H) * esize));
     __syncwarp();
     for (int q = lane; q < 6 * nu; q += 32) {
@@ -311,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
         bulk_g2s(wih + static_cast<size_t>(r) * SE, static_cast<const char*>(p.w_ih) + row * E * esize,
                  static_cast<unsigned>(esize * E), &wbar);
     }
-  }
+  };
   // Before the CTA leaves, every bulk copy it issued must have landed (none may write shared memory after the exit):
   // this waits (bounded) for the weight rows unless the GRU step already did, and for the next wave's inputs when
   // `jobs_parity` >= 0 names the pending phase of their barrier.
@@ -320,9 +353,17 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
     if (!weights_in) mbar_wait(&wbar, 0, kCopyBudgetNs);
     if (jobs_parity >= 0) mbar_wait(&jbar, static_cast<unsigned>(jobs_parity), kCopyBudgetNs);
   };
-  // the embedding rows of the candidates of the first block positions (where the waves' jobs come from in the
-  // shallow trees of drafting) into L2, spread over the CTAs: the wave transitions then read them from L2
-  {
+  int wc_pos = maxd < kPrefetchPositions ? maxd : kPrefetchPositions;  // positions gathered so far
+  if (!kFused) {
+    // The launch's loads in the order they are needed: the candidates, then the owned units' W_c columns of every
+    // candidate (they depend on the ids), then the GRU weight rows, which the first GRU step (wave 1) only needs: the
+    // dependent chain is not queued behind 9.4 MB of weights.
+    load_candidates(0, maxd);
+    __syncthreads();
+    gather_wc(0, wc_pos);
+    issue_weights();
+    // the embedding rows of the candidates of the first block positions (where the waves' jobs come from in the
+    // shallow trees of drafting) into L2, spread over the CTAs: the wave transitions then read them from L2
     const size_t row_bytes = static_cast<size_t>(E) * esize;
     const size_t lines = (row_bytes + 127) / 128;
     const int npos = maxd < kPrefetchPositions ? maxd : kPrefetchPositions;
@@ -335,21 +376,108 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
       const char* a = static_cast<const char*>(p.emb) + static_cast<size_t>(id) * row_bytes + line * 128;
       asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
     }
+  } else {
+    // A whole round in this launch. The weight rows first (they depend on nothing), then the round's top-M: the
+    // (row, chunk) units of B*K rows in chunks of 512 x kFuseGroups 16-byte groups, spread over the CTAs, each
+    // filtered into the row's per-chunk candidate list in the workspace (the filter of dt_topm, in this launch's
+    // shared memory, which the waves use later). The last CTA of a row to finish (ticket) selects the row's M
+    // candidates, writes them to the round's top-M arrays, and asks L2 for the rows the waves will read first: the
+    // W_c rows and embedding rows of those candidates when the row's block position is one of the first few. The grid
+    // barrier below orders every selection before any CTA reads the candidates.
+    issue_weights();
+    using TF = Topm<kBf16, kThreads, kFuseGroups>;
+    uint4* chunk_s = reinterpret_cast<uint4*>(smem + P.wc);
+    auto& F = *reinterpret_cast<FilterShared<kBf16, kThreads>*>(smem + P.wc + kFuseStageBytes);
+    const int rows = B * K;
+    const int chunks = (p.V + TF::kChunk - 1) / TF::kChunk;
+    const int units = rows * chunks;
+    // units position-major (every request's position 0, then position 1, ...): when there are more units than CTAs,
+    // the rows the first wave waits for are selected first
+    auto unit_row = [&](int u) {
+      const int r = u % rows;
+      return (r % B) * K + r / B;
+    };
+    if (t == 0 && j < units && p.t_vec_ok) {  // this CTA's first chunk toward L2 while the grid barrier runs
+      const int c0 = (j / rows) * TF::kChunk;
+      const unsigned bytes = static_cast<unsigned>(static_cast<size_t>(min(TF::kChunk, p.V - c0)) * esize) & ~15u;
+      if (bytes)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                     ::"l"(static_cast<const char*>(p.logits) + (static_cast<size_t>(unit_row(j)) * p.V + c0) * esize),
+                     "r"(bytes)
+                     : "memory");
+    }
+    // the launch's accumulators, wave counters and rows' ready flags start at zero; the grid barrier orders that
+    // before any CTA uses them (it runs while the first chunks and the weight rows are in flight)
+    for (size_t i = static_cast<size_t>(j) * kThreads + t; i < static_cast<size_t>(X) * kJ * M;
+         i += static_cast<size_t>(G) * kThreads)
+      p.acc[i * AS] = 0;
+    for (int i = j * kThreads + t; i < X; i += G * kThreads) p.hs_count[i] = 0;
+    for (int i = j * kThreads + t; i < rows; i += G * kThreads) p.ready[i] = 0u;
+    if (!grid_barrier(p.hdr, G, p.timeout_ns, &s_flag)) {
+      drain(-1);
+      return;
+    }
+    for (int u = j; u < units; u += G) {
+      const int row = unit_row(u), chunk = u / rows;
+      filter_chunk<kBf16, kThreads, kFuseGroups>(p.logits, p.V, M, row, chunk, chunks, p.t_cap, p.t_vec_ok,
+                                                 p.t_bounds, p.t_words, p.t_counts, p.hdr, chunk_s, F);
+      __syncthreads();  // every thread's candidate words are written before thread 0's fence and ticket
+      if (t == 0) {
+        __threadfence();
+        F.s_theta = atomicAdd(p.t_tickets + row, 1u) == static_cast<unsigned>(chunks - 1) ? 1u : 0u;
+      }
+      __syncthreads();
+      if (F.s_theta == 0u) continue;  // uniform
+      if (t == 0) {
+        __threadfence();
+        p.t_tickets[row] = 0u;  // both zero for the next call
+        p.t_bounds[row] = 0u;
+      }
+      select_row<kBf16, kThreads, kFuseGroups>(row, p.t_words, p.t_counts, chunks, p.t_cap, M, p.topm_ids,
+                                               p.topm_vals, *reinterpret_cast<SelectSmem*>(chunk_s), F.s_warp, &F.s_n);
+      __syncthreads();  // the row's ids and values are written: the row is ready (release: the writes come first)
+      if (t == 0) st_release_gpu(p.ready + row, 1u);
+      const int pos = row % K;
+      if (pos < kPrefetchPositions && pos < maxd) {
+        const unsigned wrow = static_cast<unsigned>(H * esize), erow = static_cast<unsigned>(E * esize);
+        for (int q = t; q < 2 * M; q += kThreads) {
+          const int id = p.topm_ids[static_cast<size_t>(row) * M + (q % M)];
+          if (static_cast<unsigned>(id) >= static_cast<unsigned>(p.V)) continue;
+          if (q < M)
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                         ::"l"(static_cast<const char*>(p.w_c) + static_cast<size_t>(id) * wrow), "r"(wrow) : "memory");
+          else
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                         ::"l"(static_cast<const char*>(p.emb) + static_cast<size_t>(id) * erow), "r"(erow) : "memory");
+        }
+      }
+    }
+    __syncthreads();  // the staging area is reused by the state below
   }
-  // every wave's accumulators and arrival counters start at zero; one grid barrier orders that
-  {
-    const size_t acc_words = static_cast<size_t>(X) * kJ * M * AS;
+  // every wave's accumulators and arrival counters start at zero; one grid barrier orders that (in a whole-round
+  // launch this came before the top-M)
+  if (!kFused) {
+    const size_t acc_words = static_cast<size_t>(X) * kJ * M;  // one word per accumulator line
     for (size_t i = static_cast<size_t>(j) * kThreads + t; i < acc_words; i += static_cast<size_t>(G) * kThreads)
-      p.acc[i] = 0;
+      p.acc[i * AS] = 0;
     for (int i = j * kThreads + t; i < X; i += G * kThreads) p.hs_count[i] = 0;
   }
   // control state, identical in every CTA: the root of every request is expanded in wave 0. A wave has S = B * kla job
   // slots, slot b * kla + q holding request b's q-th expansion (b = -1: empty); the slot is the job's column of the
   // GRU's MMA tile and its row of the staged inputs.
+  // Wave 0 also expands, speculatively, the first nspec candidates of position 0 (the root's likeliest children by
+  // marginal logit) as depth-1 nodes in slots 1 .. nspec: their GRU inputs (embedding row, h0) are known before any
+  // score is. As with every pick, a wrong guess costs an unused expansion, never a different tree.
   const int S = B * kla;
-  for (int b = t; b < B; b += kThreads) ctl[b] = ReqCtl{0, 0, M, 1, 0, {0, 0, 0}};  // root's children: 0 .. M - 1
-  for (int i = t; i < kJ; i += kThreads)
-    jobs[i] = (i < S && i % kla == 0) ? Job{i / kla, 0, -1, 0, 0, 0.f, {0, 0}} : Job{-1, 0, 0, 0, 0, 0.f, {0, 0}};
+  const int nspec = (maxd >= 2 && n >= 2) ? min(kla - 1, M) : 0;
+  for (int b = t; b < B; b += kThreads) ctl[b] = ReqCtl{0, 0, M, 1 + nspec, 0, {0, 0, 0}};  // root's children: 0 .. M-1
+  for (int i = t; i < kJ; i += kThreads) {
+    const int b = i / kla, q = i % kla;
+    jobs[i] = i >= S ? Job{-1, 0, 0, 0, 0, 0.f, {0, 0}}
+              : q == 0 ? Job{b, 0, -1, 0, 0, 0.f, {0, 0}}       // the root
+              : q <= nspec ? Job{b, q, 0, 0, 1, 0.f, {q, 0}}    // candidate q - 1 of position 0 (token set below)
+                           : Job{-1, 0, 0, 0, 0, 0.f, {0, 0}};
+  }
   for (int i = t; i < B * n; i += kThreads) pops[i] = PopRec{0, 0, 0, -INFINITY};
   for (int i = t; i < B * 32; i += kThreads) {  // lane 0: the merged list (empty), lane 1: the root's children
     const int l = i % 32;
@@ -358,34 +486,69 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
   for (int i = t; i < B * X; i += kThreads) {
     kcount[i] = 0;
     popidx[i] = (i % X) == 0 ? -1 : -2;
-    sdepth[i] = 0;
+    sdepth[i] = (i % X) >= 1 && (i % X) <= nspec ? 1 : 0;
   }
   if (t == 0) s_J = B;
-  if (!grid_barrier(p.hdr, G, p.timeout_ns, &s_flag)) {
-    drain(-1);
-    return;
-  }
   const unsigned erow = static_cast<unsigned>(E * esize), hrow = static_cast<unsigned>(H * sizeof(float));
+  // wave 0's inputs: the speculative jobs' embedding rows and h0 as bulk copies on jbar (the candidates are staged);
+  // one arrival closes the barrier's phase 0, which wave 0 waits for (at once when nothing was copied)
+  auto issue_spec = [&]() {
+    __syncthreads();  // the jobs and the candidates are in place; the staging area's generic accesses are done
+    for (int i = t; i < S; i += kThreads) {
+      const int b = i / kla, q = i % kla;
+      if (q < 1 || q > nspec) continue;
+      const int tok = ids_s[static_cast<size_t>(b) * maxd * M + (q - 1)];
+      jobs[i].token = tok;
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_expect_tx_only(&jbar, erow + hrow);
+      bulk_g2s(xe + static_cast<size_t>(i) * SE, static_cast<const char*>(p.emb) + static_cast<size_t>(tok) * erow,
+               erow, &jbar);
+      bulk_g2s(xh + static_cast<size_t>(i) * H, p.h0 + static_cast<size_t>(b) * H, hrow, &jbar);
+    }
+    __syncthreads();
+    if (t == 0) mbar_arrive(&jbar);
+  };
+  if (!kFused) {
+    issue_spec();
+    if (!grid_barrier(p.hdr, G, p.timeout_ns, &s_flag)) {
+      drain(0);  // the speculative jobs' copies are in flight
+      return;
+    }
+  } else {
+    // the first wave needs the rows of position 0 (the roots' children) and, with speculative jobs, position 1; the
+    // other rows' selections may still be running (later waves wait for them when they first need them)
+    const int p_need = min(maxd, nspec > 0 ? 2 : 1);
+    if (!wait_rows(0, p_need)) {
+      drain(-1);
+      return;
+    }
+    load_candidates(0, p_need);
+    issue_spec();
+    gather_wc(0, p_need);
+    wc_pos = p_need;
+  }
 
   for (int w = 0;; ++w) {
     __syncthreads();
     const int J = s_J;  // expansions in this wave
     if (J == 0) {
-      // the previous wave's barrier phase completes once its copies land (none were issued when nothing was picked)
-      if (w > 0) mbar_wait(&jbar, (w - 1) & 1, kCopyBudgetNs);
+      // the barrier's pending phase completes once its copies land (none were issued when nothing was picked)
+      mbar_wait(&jbar, w & 1, kCopyBudgetNs);
       break;
     }
-    // the jobs' inputs, copied while the previous wave picked them (wave 0 expands the roots and reads none); every
-    // thread waits, and the decision to leave is taken by the whole CTA at once
-    if (w > 0 && !__syncthreads_and(mbar_wait(&jbar, (w - 1) & 1, kCopyBudgetNs))) {
+    // the jobs' inputs, copied while the previous wave picked them (wave 0: the speculative jobs' inputs, copied at
+    // launch); every thread waits, and the decision to leave is taken by the whole CTA at once
+    if (!__syncthreads_and(mbar_wait(&jbar, w & 1, kCopyBudgetNs))) {
       record_error(p.hdr, DT_ERR_TIMEOUT);
       atomicExch(&p.hdr->abort, 1u);
-      drain((w - 1) & 1);  // the wave's input copies are still outstanding
+      drain(w & 1);  // the wave's input copies are still outstanding
       return;
     }
     long long* acc_w = p.acc + static_cast<size_t>(w) * kJ * M * AS;
-    const bool roots = w == 0;  // wave 0 expands the roots (h = h0, no GRU step); later waves never do
-    if (!roots && !weights_in) {  // the weight rows, before the first GRU step (bounded)
+    // a GRU step runs unless the wave holds roots only (roots take h = h0); wave 0 also holds the speculative jobs
+    const bool gru = w > 0 || nspec > 0;
+    const bool spec_wave = w == 0 && nspec > 0;
+    if (gru && !weights_in) {  // the weight rows, before the first GRU step (bounded)
       if (!__syncthreads_and(mbar_wait(&wbar, 0, kCopyBudgetNs))) {  // never compute on unstaged weights: leave
         record_error(p.hdr, DT_ERR_TIMEOUT);
         atomicExch(&p.hdr->abort, 1u);
@@ -400,6 +563,14 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
         if (jobs[q].b >= 0) deepest = max(deepest, jobs[q].depth);
       if (deepest >= wc_pos) {
         const int upto = min(maxd, deepest + kPrefetchPositions);
+        if (kFused) {  // these positions' candidates come from selections made in this launch
+          if (!wait_rows(wc_pos, upto)) {
+            drain(-1);
+            return;
+          }
+          load_candidates(wc_pos, upto);
+          __syncthreads();
+        }
         gather_wc(wc_pos, upto);
         wc_pos = upto;
         __syncthreads();
@@ -408,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
 
     // ---- phase A: this CTA's units of every job's GRU step, then its share of every job's correction ----
     constexpr bool mma = kBf16 && kMma;  // the tensor-core GRU (else the CUDA-core one below)
-    if (!roots && mma) {
+    if (gru && mma) {
       // Tensor cores, mma.sync m16n8k16 (bf16 in, fp32 accumulate): D[16 gate rows][8 jobs] = W[rows][K] X[K][jobs],
       // the warps splitting the k16 steps. A = this CTA's gate rows (rows past R repeat row R - 1: their outputs are
       // not used), B = the jobs' embedding rows (input side) and the parents' fp32 states as bf16 hi + lo pairs
@@ -452,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
       *reinterpret_cast<float2*>(rw + (kMaxRows + g) * kJ + 2 * tg) = make_float2(dh[0], dh[1]);
       *reinterpret_cast<float2*>(rw + (kMaxRows + g + 8) * kJ + 2 * tg) = make_float2(dh[2], dh[3]);
     }
-    if (!roots && !mma && warp < 3 * umax) {
+    if (gru && !mma && warp < 3 * umax) {
       // One warp per gate row (R <= 16 rows, 16 warps), every job slot against the row: the lanes stride over K, one
       // accumulator per slot and side, then one shuffle tree each. A job's sums do not depend on the other jobs.
       // The row's input side (over E) and hidden side (over H) stay apart: the n gate needs them separately.
@@ -556,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
       }
     }
     __syncthreads();
-    if (!roots && mma) {  // the partial tiles summed over the warps in a fixed order
+    if (gru && mma) {  // the partial tiles summed over the warps in a fixed order
       for (int i = t; i < 2 * 3 * umax * S; i += kThreads) {
         const int side = i / (3 * umax * S), r = (i / S) % (3 * umax), q = i % S;
         float v = 0.f;
@@ -573,7 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
       const Job jb = jobs[q];
       if (u >= nu || jb.b < 0) continue;
       float hn;
-      if (roots) {
+      if (jb.pslot < 0) {  // a root
         hn = __ldg(p.h0 + static_cast<size_t>(jb.b) * H + u0 + u);
       } else {
         const float* gq = gates + q * 3 * umax * 2;
@@ -653,9 +824,20 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
       const float lse = logf(sum);
+      for (int m = lane; m < M; m += 32) z[q * M + m] = (z[q * M + m] - mx) - lse;  // the restricted log-softmax
+    }
+    // (1b) the children's scores: the node's score plus their log-probabilities. A speculative job of wave 0 takes its
+    //      own score from the root's children, scored by the root's warp in (1) (score 0 + logp, as a pop sees it).
+    if (spec_wave) __syncthreads();
+    if (warp < S && jobs[warp].b >= 0) {
+      const int q = warp;
+      const Job jb = jobs[q];
+      const size_t off = (static_cast<size_t>(jb.b) * maxd + jb.depth) * M;
+      const int rq = jb.b * kla;  // the request's root slot in wave 0
+      const float base = jb.aux[0] > 0 ? jobs[rq].score + z[rq * M + (jb.aux[0] - 1)] : jb.score;
       for (int m = lane; m < M; m += 32) {
         Node e;
-        e.score = jb.score + ((z[q * M + m] - mx) - lse);
+        e.score = base + z[q * M + m];
         e.token = ids_s[off + m];
         e.seq = m;  // the candidate index until the node is popped
         e.pslot = static_cast<short>(jb.xslot);
@@ -665,7 +847,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
       }
       if (M <= 128) {
         __syncwarp();
-        const int rem = roots ? n : n - ctl[jb.b].s - 1;
+        const int rem = jb.pslot < 0 ? n : n - ctl[jb.b].s - 1;
         const int kc = min(min(M, KM), rem);
         Node* out = kids + (static_cast<size_t>(jb.b) * X + jb.xslot) * KM;
         if (M <= 32) rank_children_warp<1>(kraw + q * M, kkey + q * M, M, out, kc);
@@ -696,7 +878,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
         for (int o = 1; o < tpe; o <<= 1) r += __shfl_xor_sync(0xFFFFFFFFu, r, o);
         if (live && part == 0) {
           const Job jb = jobs[q];
-          const int rem = roots ? n : n - ctl[jb.b].s - 1;
+          const int rem = jb.pslot < 0 ? n : n - ctl[jb.b].s - 1;
           const int kc = min(min(M, KM), rem);
           if (r < kc) kids[(static_cast<size_t>(jb.b) * X + jb.xslot) * KM + r] = kraw[i];
           if (r == 0) kcount[jb.b * X + jb.xslot] = kc;
@@ -713,6 +895,14 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
       const ReqView R{ctl + b, lanes + b * 32, merged + static_cast<size_t>(b) * 2 * n,
                       kids + static_cast<size_t>(b) * X * KM, kcount + b * X, popidx + b * X, sdepth + b * X,
                       pops + static_cast<size_t>(b) * n};
+      if (spec_wave) {  // the root's children that wave 0 expanded speculatively (candidate m: slot 1 + m) are known
+        const int kc0 = kcount[b * X];
+        for (int i = lane; i < kc0; i += 32) {
+          Node& e = kids[static_cast<size_t>(b) * X * KM + i];
+          if (e.seq < nspec) e.xslot = static_cast<short>(1 + e.seq);
+        }
+        __syncwarp();
+      }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       asm volatile("fence.proxy.async.global;" ::: "memory");
       const auto start_copies = [&](int q, const Job& jb) {
@@ -768,6 +958,23 @@ Plan plan_for(const Params& p, int sms) {
   return make_plan(p.B, p.M, p.n, p.max_depth, p.H, p.E, p.bf16 ? 2 : 4, grid_size(p, sms));
 }
 
+// Dynamic shared memory of a launch: the plan, and for a whole round also the top-M's staged chunk and filter state
+// (laid over the plan's regions from the W_c columns on).
+size_t launch_smem(const Params& p, const Plan& P) {
+  if (!p.logits) return P.bytes;
+  const size_t fs = p.bf16 ? sizeof(FilterShared<true, kThreads>) : sizeof(FilterShared<false, kThreads>);
+  const size_t need = P.wc + kFuseStageBytes + fs;
+  return need > P.bytes ? need : P.bytes;
+}
+
+template <bool kFused>
+const void* builder_fn(const Params& p) {
+  const bool mma = p.bf16 && p.E % 16 == 0 && p.H % 16 == 0;
+  return !p.bf16 ? reinterpret_cast<const void*>(small_builder<false, false, kFused>)
+         : mma   ? reinterpret_cast<const void*>(small_builder<true, true, kFused>)
+                 : reinterpret_cast<const void*>(small_builder<true, false, kFused>);
+}
+
 }  // namespace
 
 bool small_builder_fits(const Params& p, const DeviceInfo& di) {
@@ -778,20 +985,24 @@ bool small_builder_fits(const Params& p, const DeviceInfo& di) {
   return P.bytes <= static_cast<size_t>(di.optin);
 }
 
+bool small_round_fits(const Params& p, const DeviceInfo& di) {
+  if (!p.logits || !small_builder_fits(p, di)) return false;
+  const Plan P = plan_for(p, di.sms);
+  return launch_smem(p, P) <= static_cast<size_t>(di.optin);
+}
+
 // One CTA per SM at most (launch bounds of 512 threads, one block), so the shared-memory plan alone decides that the
 // G CTAs are co-resident; the cooperative launch checks it again.
 cudaError_t launch_small_builder(const Params& p, const DeviceInfo& di, cudaStream_t stream) {
   const Plan P = plan_for(p, di.sms);
-  const bool mma = p.bf16 && p.E % 16 == 0 && p.H % 16 == 0;
-  const void* fn = !p.bf16 ? reinterpret_cast<const void*>(small_builder<false, false>)
-                   : mma   ? reinterpret_cast<const void*>(small_builder<true, true>)
-                           : reinterpret_cast<const void*>(small_builder<true, false>);
-  cudaError_t e = ensure_dynamic_smem(fn, P.bytes);
+  const void* fn = p.logits ? builder_fn<true>(p) : builder_fn<false>(p);
+  const size_t smem = launch_smem(p, P);
+  cudaError_t e = ensure_dynamic_smem(fn, smem);
   if (e != cudaSuccess) return e;
   Params pp = p;
   Plan PP = P;
   void* args[] = {&pp, &PP};
-  return cudaLaunchCooperativeKernel(fn, dim3(static_cast<unsigned>(P.G)), dim3(kThreads), args, P.bytes, stream);
+  return cudaLaunchCooperativeKernel(fn, dim3(static_cast<unsigned>(P.G)), dim3(kThreads), args, smem, stream);
 }
 
 }  // namespace dt
