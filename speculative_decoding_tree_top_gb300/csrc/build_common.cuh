@@ -338,20 +338,6 @@ struct Params {
   int lookahead;    // expansions a request may run per wave (1 = one pop at a time)
   int xslots;       // expansion slots per request (expansion_slots(n))
   int* hs_count;    // [xslots] per wave, the CTAs whose hidden-state units and correction shares are in (small batch)
-  unsigned* ready;  // [B*K] whole-round launch: 1 once the row's top-M is selected (cleared at launch)
-  // A whole round in one launch (dt_round, small batches): the top-M of `logits` [B,K,V] (the weights' dtype) runs
-  // first inside the builder's launch and writes the candidates to topm_ids / topm_vals (the arrays ids / vals
-  // point to), through the top-M region of the workspace (bounds, tickets, per-chunk counts and words). Null
-  // logits: the candidates are given (dt_build_trees).
-  const void* logits;
-  int32_t* topm_ids;
-  float* topm_vals;
-  uint32_t* t_bounds;
-  unsigned* t_tickets;
-  int* t_counts;
-  void* t_words;
-  int t_cap;
-  bool t_vec_ok;
   float* gru_part;  // [gru_tiles][kGruSplits][128][128] K-split partial gate sums of the tensor-core GRU
   unsigned* gru_ticket;  // [gru_tiles] CTAs of a tile that stored their partials in the current wave (tensor-core GRU)
   int gru_tiles;
@@ -505,8 +491,8 @@ inline BuildLayout build_layout(int B, int K, int V, int M, int n, int H, int E)
   L.hs = topm_layout(B, K, V, M).bytes;
   const size_t acc_bytes = B <= kSmallMaxB ? sizeof(long long) * X * kWaveJobs * M * acc_stride(M, n) : 0;
   L.acc = align_up(L.hs + sizeof(float) * static_cast<size_t>(B) * X * H);
-  L.hs_count = align_up(L.acc + acc_bytes);  // the per-wave counters, then the top-M rows' ready flags
-  L.rstate = align_up(L.hs_count + (B <= kSmallMaxB ? sizeof(int) * (X + static_cast<size_t>(B) * K) : 0));
+  L.hs_count = align_up(L.acc + acc_bytes);  // the per-wave counters
+  L.rstate = align_up(L.hs_count + (B <= kSmallMaxB ? sizeof(int) * X : 0));
   // both builders may run for small batches (the small one needs shared memory the device may not have)
   L.joblist = align_up(L.rstate + req_layout(n, static_cast<int>(X), KM, kLargeLookahead).bytes * B);
   L.jobcount = align_up(L.joblist + sizeof(Job) * 2 * static_cast<size_t>(B) * kLargeLookahead);
@@ -524,9 +510,6 @@ inline BuildLayout build_layout(int B, int K, int V, int M, int n, int H, int E)
 // The small-batch builder (build_small.cu). Returns false when its shared-memory plan does not fit this device
 // (the caller then uses the general builder).
 bool small_builder_fits(const Params& p, const DeviceInfo& di);
-// Whether the small-batch builder can also run the round's top-M in its launch (p.logits set).
-bool small_round_fits(const Params& p, const DeviceInfo& di);
-// Launches the small-batch builder; with p.logits set, the whole round (top-M included) in that one launch.
 cudaError_t launch_small_builder(const Params& p, const DeviceInfo& di, cudaStream_t stream);
 
 }  // namespace dt

@@ -34,7 +34,6 @@
 #include <type_traits>
 
 #include "build_common.cuh"
-#include "topm_filter.cuh"
 
 namespace dt {
 namespace {
@@ -47,11 +46,6 @@ constexpr int kRowPad = 8;    // elements of padding per shared-memory weight ro
 constexpr int kJ = kWaveJobs;
 static_assert(kJ == 8, "a wave's jobs are the n8 tile of the GRU MMA");
 constexpr int kPrefetchPositions = 4;  // block positions whose candidates' embedding rows are prefetched at launch
-// A whole round in one launch: the top-M's chunks are 512 threads x 8 groups of 16 bytes (32768 bf16 or 16384 fp32
-// logits, never more chunks per row than the workspace's top-M region holds), staged where the waves' state goes later.
-constexpr int kFuseGroups = 8;
-constexpr size_t kFuseStageBytes = static_cast<size_t>(kThreads) * kFuseGroups * 16;
-static_assert(sizeof(SelectSmem) <= kFuseStageBytes, "the row's selection fits the staged chunk's space");
 
 // Shared-memory plan of one CTA (identical on host and device).
 struct Plan {
@@ -116,18 +110,26 @@ __device__ __forceinline__ long long ld_relaxed_s64(const long long* p) {
   return v;
 }
 
-// Correction accumulators: every CTA adds (round(v * 2^32) << 8) + 1 to the slot of each candidate. The upper 56
-// bits hold the exact fixed-point sum, the low byte the number of contributions (G < 256).
+// Correction accumulators: every CTA adds ((sum over its units of round(w * h * 2^32)) << 8) + 1 to the slot of each
+// candidate. The upper 56 bits hold the exact fixed-point sum, the low byte the number of contributions (G < 256).
 constexpr float kFix = 4294967296.0f;              // 2^32
 constexpr float kUnfix = 2.3283064365386963e-10f;  // 2^-32
-constexpr float kMaxShare = 32768.0f;              // |share| bound: 255 shares still fit in 56 bits
+constexpr float kMaxTerm = 4096.0f;                // |w * h| bound: H <= 2048 terms of < 2^44 sum below 2^55
 
-__device__ __forceinline__ void add_share(const Params& p, long long* slot, float v) {
-  if (!(fabsf(v) < kMaxShare)) {  // also catches NaN
+// One hidden unit's term of a correction, w * h, as a fixed-point integer: rounded on its own, so that a candidate's
+// sum is the same however the units are spread over the CTAs (and whatever the number of SMs).
+__device__ __forceinline__ long long fixed_term(const Params& p, float w, float h) {
+  float v = w * h;
+  if (!(fabsf(v) < kMaxTerm)) {  // also catches NaN
     record_error(p.hdr, DT_ERR_NUMERIC);
     v = 0.f;
   }
-  const unsigned long long c = (static_cast<unsigned long long>(__float2ll_rn(v * kFix)) << 8) + 1ull;
+  return __float2ll_rn(v * kFix);
+}
+// Adds a CTA's share (the sum of its units' fixed-point terms) to a candidate's accumulator, counting one
+// contribution in the low byte.
+__device__ __forceinline__ void add_share(long long* slot, long long share) {
+  const unsigned long long c = (static_cast<unsigned long long>(share) << 8) + 1ull;
   atomicAdd(reinterpret_cast<unsigned long long*>(slot), c);
 }
 
@@ -213,9 +215,7 @@ __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, u
   lo = static_cast<uint32_t>(__bfloat16_as_ushort(l0)) | (static_cast<uint32_t>(__bfloat16_as_ushort(l1)) << 16);
 }
 
-// kMma: bf16 weights with E and H multiples of 16 (tensor-core GRU); kFused: the round's top-M runs in this launch
-// (logits of the weights' dtype)
-template <bool kBf16, bool kMma, bool kFused>
+template <bool kBf16, bool kMma>  // kMma: bf16 weights with E and H multiples of 16 (tensor-core GRU)
 __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
   using T = typename WT<kBf16>::T;
   extern __shared__ __align__(16) unsigned char smem[];
@@ -271,8 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
     bias[2 * i] = (u < nu && p.b_ih) ? ldw(p.b_ih, kBf16, row) : 0.f;
     bias[2 * i + 1] = (u < nu && p.b_hh) ? ldw(p.b_hh, kBf16, row) : 0.f;
   }
-  // the candidates' ids and base logits of every request and position the tree can reach, into shared memory (read
-  // through L2: in a whole-round launch they were written earlier in the same launch)
+  // the candidates' ids and base logits of every request and position the tree can reach, into shared memory
   auto load_candidates = [&](int p0, int p1) {  // block positions [p0, p1)
     const int np = p1 - p0;
     for (int i = t; i < B * np * M; i += kThreads) {
@@ -282,30 +281,6 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
       ids_s[si] = valid_id(p, __ldcg(p.ids + gi));
       vals_s[si] = __ldcg(p.vals + gi);
     }
-  };
-  // whole-round launch: waits (bounded, abort-aware) until the top-M rows of block positions [p0, p1) of every
-  // request are selected; false in every thread when a wait ran out (recorded)
-  auto wait_rows = [&](int p0, int p1) -> bool {
-    int ok = 1;
-    for (int i = t; i < B * (p1 - p0); i += kThreads) {
-      const unsigned* f = p.ready + static_cast<size_t>(i % B) * K + p0 + i / B;
-      if (p.timeout_ns == 0) {
-        ok = 0;
-      } else {
-        const uint64_t t0 = global_timer_ns();
-        for (unsigned polls = 1; ld_acquire_gpu(f) == 0u; ++polls)
-          if ((polls & 15u) == 0u && (ld_acquire_gpu(&p.hdr->abort) != 0u || global_timer_ns() - t0 > p.timeout_ns)) {
-            ok = 0;
-            break;
-          }
-      }
-      if (!ok) {
-        record_error(p.hdr, DT_ERR_TIMEOUT);
-        atomicExch(&p.hdr->abort, 1u);
-        break;
-      }
-    }
-    return __syncthreads_and(ok) != 0;
   };
   // The owned units' W_c columns of the candidates of block positions [p0, p1): each needed row comes into L2 once
   // (one bulk prefetch per row, spread over the CTAs, so HBM serves whole rows), then every CTA takes its columns.
@@ -354,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
     if (jobs_parity >= 0) mbar_wait(&jbar, static_cast<unsigned>(jobs_parity), kCopyBudgetNs);
   };
   int wc_pos = maxd < kPrefetchPositions ? maxd : kPrefetchPositions;  // positions gathered so far
-  if (!kFused) {
+  {
     // The launch's loads in the order they are needed: the candidates, then the owned units' W_c columns of every
     // candidate (they depend on the ids), then the GRU weight rows, which the first GRU step (wave 1) only needs: the
     // dependent chain is not queued behind 9.4 MB of weights.
@@ -376,87 +351,9 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
       const char* a = static_cast<const char*>(p.emb) + static_cast<size_t>(id) * row_bytes + line * 128;
       asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
     }
-  } else {
-    // A whole round in this launch. The weight rows first (they depend on nothing), then the round's top-M: the
-    // (row, chunk) units of B*K rows in chunks of 512 x kFuseGroups 16-byte groups, spread over the CTAs, each
-    // filtered into the row's per-chunk candidate list in the workspace (the filter of dt_topm, in this launch's
-    // shared memory, which the waves use later). The last CTA of a row to finish (ticket) selects the row's M
-    // candidates, writes them to the round's top-M arrays, and asks L2 for the rows the waves will read first: the
-    // W_c rows and embedding rows of those candidates when the row's block position is one of the first few. The grid
-    // barrier below orders every selection before any CTA reads the candidates.
-    issue_weights();
-    using TF = Topm<kBf16, kThreads, kFuseGroups>;
-    uint4* chunk_s = reinterpret_cast<uint4*>(smem + P.wc);
-    auto& F = *reinterpret_cast<FilterShared<kBf16, kThreads>*>(smem + P.wc + kFuseStageBytes);
-    const int rows = B * K;
-    const int chunks = (p.V + TF::kChunk - 1) / TF::kChunk;
-    const int units = rows * chunks;
-    // units position-major (every request's position 0, then position 1, ...): when there are more units than CTAs,
-    // the rows the first wave waits for are selected first
-    auto unit_row = [&](int u) {
-      const int r = u % rows;
-      return (r % B) * K + r / B;
-    };
-    if (t == 0 && j < units && p.t_vec_ok) {  // this CTA's first chunk toward L2 while the grid barrier runs
-      const int c0 = (j / rows) * TF::kChunk;
-      const unsigned bytes = static_cast<unsigned>(static_cast<size_t>(min(TF::kChunk, p.V - c0)) * esize) & ~15u;
-      if (bytes)
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
-                     ::"l"(static_cast<const char*>(p.logits) + (static_cast<size_t>(unit_row(j)) * p.V + c0) * esize),
-                     "r"(bytes)
-                     : "memory");
-    }
-    // the launch's accumulators, wave counters and rows' ready flags start at zero; the grid barrier orders that
-    // before any CTA uses them (it runs while the first chunks and the weight rows are in flight)
-    for (size_t i = static_cast<size_t>(j) * kThreads + t; i < static_cast<size_t>(X) * kJ * M;
-         i += static_cast<size_t>(G) * kThreads)
-      p.acc[i * AS] = 0;
-    for (int i = j * kThreads + t; i < X; i += G * kThreads) p.hs_count[i] = 0;
-    for (int i = j * kThreads + t; i < rows; i += G * kThreads) p.ready[i] = 0u;
-    if (!grid_barrier(p.hdr, G, p.timeout_ns, &s_flag)) {
-      drain(-1);
-      return;
-    }
-    for (int u = j; u < units; u += G) {
-      const int row = unit_row(u), chunk = u / rows;
-      filter_chunk<kBf16, kThreads, kFuseGroups>(p.logits, p.V, M, row, chunk, chunks, p.t_cap, p.t_vec_ok,
-                                                 p.t_bounds, p.t_words, p.t_counts, p.hdr, chunk_s, F);
-      __syncthreads();  // every thread's candidate words are written before thread 0's fence and ticket
-      if (t == 0) {
-        __threadfence();
-        F.s_theta = atomicAdd(p.t_tickets + row, 1u) == static_cast<unsigned>(chunks - 1) ? 1u : 0u;
-      }
-      __syncthreads();
-      if (F.s_theta == 0u) continue;  // uniform
-      if (t == 0) {
-        __threadfence();
-        p.t_tickets[row] = 0u;  // both zero for the next call
-        p.t_bounds[row] = 0u;
-      }
-      select_row<kBf16, kThreads, kFuseGroups>(row, p.t_words, p.t_counts, chunks, p.t_cap, M, p.topm_ids,
-                                               p.topm_vals, *reinterpret_cast<SelectSmem*>(chunk_s), F.s_warp, &F.s_n);
-      __syncthreads();  // the row's ids and values are written: the row is ready (release: the writes come first)
-      if (t == 0) st_release_gpu(p.ready + row, 1u);
-      const int pos = row % K;
-      if (pos < kPrefetchPositions && pos < maxd) {
-        const unsigned wrow = static_cast<unsigned>(H * esize), erow = static_cast<unsigned>(E * esize);
-        for (int q = t; q < 2 * M; q += kThreads) {
-          const int id = p.topm_ids[static_cast<size_t>(row) * M + (q % M)];
-          if (static_cast<unsigned>(id) >= static_cast<unsigned>(p.V)) continue;
-          if (q < M)
-            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
-                         ::"l"(static_cast<const char*>(p.w_c) + static_cast<size_t>(id) * wrow), "r"(wrow) : "memory");
-          else
-            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
-                         ::"l"(static_cast<const char*>(p.emb) + static_cast<size_t>(id) * erow), "r"(erow) : "memory");
-        }
-      }
-    }
-    __syncthreads();  // the staging area is reused by the state below
   }
-  // every wave's accumulators and arrival counters start at zero; one grid barrier orders that (in a whole-round
-  // launch this came before the top-M)
-  if (!kFused) {
+  // every wave's accumulators and arrival counters start at zero; one grid barrier orders that
+  {
     const size_t acc_words = static_cast<size_t>(X) * kJ * M;  // one word per accumulator line
     for (size_t i = static_cast<size_t>(j) * kThreads + t; i < acc_words; i += static_cast<size_t>(G) * kThreads)
       p.acc[i * AS] = 0;
@@ -493,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
   // wave 0's inputs: the speculative jobs' embedding rows and h0 as bulk copies on jbar (the candidates are staged);
   // one arrival closes the barrier's phase 0, which wave 0 waits for (at once when nothing was copied)
   auto issue_spec = [&]() {
-    __syncthreads();  // the jobs and the candidates are in place; the staging area's generic accesses are done
+    __syncthreads();  // the jobs and the candidates are in place
     for (int i = t; i < S; i += kThreads) {
       const int b = i / kla, q = i % kla;
       if (q < 1 || q > nspec) continue;
@@ -508,24 +405,10 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
     __syncthreads();
     if (t == 0) mbar_arrive(&jbar);
   };
-  if (!kFused) {
-    issue_spec();
-    if (!grid_barrier(p.hdr, G, p.timeout_ns, &s_flag)) {
-      drain(0);  // the speculative jobs' copies are in flight
-      return;
-    }
-  } else {
-    // the first wave needs the rows of position 0 (the roots' children) and, with speculative jobs, position 1; the
-    // other rows' selections may still be running (later waves wait for them when they first need them)
-    const int p_need = min(maxd, nspec > 0 ? 2 : 1);
-    if (!wait_rows(0, p_need)) {
-      drain(-1);
-      return;
-    }
-    load_candidates(0, p_need);
-    issue_spec();
-    gather_wc(0, p_need);
-    wc_pos = p_need;
+  issue_spec();
+  if (!grid_barrier(p.hdr, G, p.timeout_ns, &s_flag)) {
+    drain(0);  // the speculative jobs' copies are in flight
+    return;
   }
 
   for (int w = 0;; ++w) {
@@ -563,14 +446,6 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
         if (jobs[q].b >= 0) deepest = max(deepest, jobs[q].depth);
       if (deepest >= wc_pos) {
         const int upto = min(maxd, deepest + kPrefetchPositions);
-        if (kFused) {  // these positions' candidates come from selections made in this launch
-          if (!wait_rows(wc_pos, upto)) {
-            drain(-1);
-            return;
-          }
-          load_candidates(wc_pos, upto);
-          __syncthreads();
-        }
         gather_wc(wc_pos, upto);
         wc_pos = upto;
         __syncthreads();
@@ -764,9 +639,9 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
       const Job jb = jobs[q];
       if (jb.b < 0) continue;
       const T* wcp = wc + ((static_cast<size_t>(jb.b) * maxd + jb.depth) * M + m) * umax;
-      float v = 0.f;
-      for (int u = 0; u < nu; ++u) v = fmaf(WT<kBf16>::f(wcp[u]), hb[q * umax + u], v);
-      add_share(p, acc_w + (static_cast<size_t>(q) * M + m) * AS, v);
+      long long v = 0;
+      for (int u = 0; u < nu; ++u) v += fixed_term(p, WT<kBf16>::f(wcp[u]), hb[q * umax + u]);
+      add_share(acc_w + (static_cast<size_t>(q) * M + m) * AS, v);
     }
     // One arrival per CTA and wave (release: the hidden-state units and the shares above come first). A CTA that
     // sees G arrivals (acquire) sees every share of every candidate and every unit of the wave's hidden states.
@@ -958,23 +833,6 @@ Plan plan_for(const Params& p, int sms) {
   return make_plan(p.B, p.M, p.n, p.max_depth, p.H, p.E, p.bf16 ? 2 : 4, grid_size(p, sms));
 }
 
-// Dynamic shared memory of a launch: the plan, and for a whole round also the top-M's staged chunk and filter state
-// (laid over the plan's regions from the W_c columns on).
-size_t launch_smem(const Params& p, const Plan& P) {
-  if (!p.logits) return P.bytes;
-  const size_t fs = p.bf16 ? sizeof(FilterShared<true, kThreads>) : sizeof(FilterShared<false, kThreads>);
-  const size_t need = P.wc + kFuseStageBytes + fs;
-  return need > P.bytes ? need : P.bytes;
-}
-
-template <bool kFused>
-const void* builder_fn(const Params& p) {
-  const bool mma = p.bf16 && p.E % 16 == 0 && p.H % 16 == 0;
-  return !p.bf16 ? reinterpret_cast<const void*>(small_builder<false, false, kFused>)
-         : mma   ? reinterpret_cast<const void*>(small_builder<true, true, kFused>)
-                 : reinterpret_cast<const void*>(small_builder<true, false, kFused>);
-}
-
 }  // namespace
 
 bool small_builder_fits(const Params& p, const DeviceInfo& di) {
@@ -985,24 +843,20 @@ bool small_builder_fits(const Params& p, const DeviceInfo& di) {
   return P.bytes <= static_cast<size_t>(di.optin);
 }
 
-bool small_round_fits(const Params& p, const DeviceInfo& di) {
-  if (!p.logits || !small_builder_fits(p, di)) return false;
-  const Plan P = plan_for(p, di.sms);
-  return launch_smem(p, P) <= static_cast<size_t>(di.optin);
-}
-
 // One CTA per SM at most (launch bounds of 512 threads, one block), so the shared-memory plan alone decides that the
 // G CTAs are co-resident; the cooperative launch checks it again.
 cudaError_t launch_small_builder(const Params& p, const DeviceInfo& di, cudaStream_t stream) {
   const Plan P = plan_for(p, di.sms);
-  const void* fn = p.logits ? builder_fn<true>(p) : builder_fn<false>(p);
-  const size_t smem = launch_smem(p, P);
-  cudaError_t e = ensure_dynamic_smem(fn, smem);
+  const bool mma = p.bf16 && p.E % 16 == 0 && p.H % 16 == 0;
+  const void* fn = !p.bf16 ? reinterpret_cast<const void*>(small_builder<false, false>)
+                   : mma   ? reinterpret_cast<const void*>(small_builder<true, true>)
+                           : reinterpret_cast<const void*>(small_builder<true, false>);
+  cudaError_t e = ensure_dynamic_smem(fn, P.bytes);
   if (e != cudaSuccess) return e;
   Params pp = p;
   Plan PP = P;
   void* args[] = {&pp, &PP};
-  return cudaLaunchCooperativeKernel(fn, dim3(static_cast<unsigned>(P.G)), dim3(kThreads), args, smem, stream);
+  return cudaLaunchCooperativeKernel(fn, dim3(static_cast<unsigned>(P.G)), dim3(kThreads), args, P.bytes, stream);
 }
 
 }  // namespace dt

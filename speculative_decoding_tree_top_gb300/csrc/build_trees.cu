@@ -1026,24 +1026,14 @@ namespace dt {
 namespace {
 
 enum class BuildMode {
-  kLaunch,      // validate and launch
-  kCheck,       // validate only, launch nothing (dt_round checks the whole round before its first launch)
-  kFusedRound,  // the whole round (top-M included) as one launch if the small-batch builder can take it; otherwise
-                // DT_ERR_UNSUPPORTED with nothing launched (dt_round then makes the two calls)
-};
-
-// The round's top-M when it runs inside the builder's launch.
-struct RoundTopm {
-  const void* logits;
-  dt_dtype dtype;
-  int32_t* ids;
-  float* vals;
+  kLaunch,  // validate and launch
+  kCheck,   // validate only, launch nothing (dt_round checks the whole round before its first launch)
 };
 
 dt_status build_trees(int B, int K, int V, int M, int n, int max_depth, float T, const int32_t* topm_ids,
                       const float* topm_vals, const float* h0, const dt_weights* w, int32_t* out_tokens,
                       int32_t* out_parents, int32_t* out_depth, float* out_scores, uint8_t* out_mask, void* workspace,
-                      size_t workspace_bytes, cudaStream_t stream, BuildMode mode, const RoundTopm* rt = nullptr) {
+                      size_t workspace_bytes, cudaStream_t stream, BuildMode mode) {
   if (!w) return DT_ERR_INVALID_ARG;
   const int H = w->H, E = w->E;
   if (B < 0 || K < 1 || V < 1 || M < 1 || M > V || n < 1 || max_depth < 1 || max_depth > K) return DT_ERR_INVALID_ARG;
@@ -1080,7 +1070,6 @@ dt_status build_trees(int B, int K, int V, int M, int n, int max_depth, float T,
   p.hs = reinterpret_cast<float*>(ws + L.hs);
   p.acc = B <= kSmallMaxB ? reinterpret_cast<long long*>(ws + L.acc) : nullptr;
   p.hs_count = B <= kSmallMaxB ? reinterpret_cast<int*>(ws + L.hs_count) : nullptr;
-  p.ready = B <= kSmallMaxB ? reinterpret_cast<unsigned*>(ws + L.hs_count) + expansion_slots(n) : nullptr;
   p.rstate = reinterpret_cast<unsigned char*>(ws + L.rstate);
   p.joblist = reinterpret_cast<Job*>(ws + L.joblist);
   p.jobcount = reinterpret_cast<int*>(ws + L.jobcount);
@@ -1100,21 +1089,6 @@ dt_status build_trees(int B, int K, int V, int M, int n, int max_depth, float T,
   {
     const int fit = kWaveJobs / (B < kWaveJobs ? B : kWaveJobs);
     p.lookahead = k_set > 0 ? (k_set < fit ? k_set : fit) : fit;
-  }
-  if (mode == BuildMode::kFusedRound) {
-    if (!rt || rt->dtype != w->dtype) return DT_ERR_UNSUPPORTED;
-    const TopmLayout TL = topm_layout(B, K, V, M);
-    p.logits = rt->logits;
-    p.topm_ids = rt->ids;
-    p.topm_vals = rt->vals;
-    p.t_bounds = reinterpret_cast<uint32_t*>(ws + TL.bounds);
-    p.t_tickets = reinterpret_cast<unsigned*>(ws + TL.tickets);
-    p.t_counts = reinterpret_cast<int*>(ws + TL.counts);
-    p.t_words = ws + TL.words;
-    p.t_cap = TL.cap;
-    p.t_vec_ok = (static_cast<size_t>(V) * (p.bf16 ? 2 : 4)) % 16 == 0;
-    if (!small_round_fits(p, di)) return DT_ERR_UNSUPPORTED;
-    return cuda_status(launch_small_builder(p, di, stream));
   }
   if (small_builder_fits(p, di))
     return mode == BuildMode::kCheck ? DT_OK : cuda_status(launch_small_builder(p, di, stream));
@@ -1176,11 +1150,6 @@ extern "C" dt_status dt_round(const void* logits, dt_dtype dtype, int B, int K, 
   st = dt::build_trees(B, K, V, M, n, max_depth, T, topm_ids, topm_vals, h0, w, out_tokens, out_parents,
                                  out_depth, out_scores, out_mask, workspace, workspace_bytes, stream, BuildMode::kCheck);
   if (st != DT_OK) return st;
-  // one launch for the whole round when the small-batch builder can run the top-M in it
-  const dt::RoundTopm rt{logits, dtype, topm_ids, topm_vals};
-  st = dt::build_trees(B, K, V, M, n, max_depth, T, topm_ids, topm_vals, h0, w, out_tokens, out_parents, out_depth,
-                       out_scores, out_mask, workspace, workspace_bytes, stream, BuildMode::kFusedRound, &rt);
-  if (st != DT_ERR_UNSUPPORTED) return st;
   st = dt_topm(logits, dtype, B, K, V, M, topm_ids, topm_vals, workspace, workspace_bytes, stream);
   if (st != DT_OK) return st;
   return dt::build_trees(B, K, V, M, n, max_depth, T, topm_ids, topm_vals, h0, w, out_tokens, out_parents, out_depth,

@@ -291,7 +291,7 @@ inline int topm_chunk(int B, int K) {
 }
 // Candidate words a chunk may keep: all of its logits at or above the chunk's bound when there are at most 4M of
 // them (M <= 256; at least 64), else exactly its top M.
-inline int topm_cap(int M) { return M <= 256 ? (4 * M < 64 ? 64 : 4 * M) : M; }
+__host__ __device__ inline int topm_cap(int M) { return M <= 256 ? (4 * M < 64 ? 64 : 4 * M) : M; }
 struct TopmLayout {
   size_t bounds, tickets, counts, words, bytes;
   int chunks, chunk, cap;

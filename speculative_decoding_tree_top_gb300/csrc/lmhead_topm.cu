@@ -357,8 +357,9 @@ __global__ void __launch_bounds__(kThreads, 1) lmhead_topm_kernel(LhParams p, co
     for (int r = bid; r < R; r += G) {
       const uint64_t* rc = p.cand + static_cast<size_t>(r) * G * p.rpc;
       const int cap = p.rpc;
+      const int* rn = p.counts + static_cast<size_t>(r) * G;
       select_words<false, kSelThreads>(
-          p.counts + static_cast<size_t>(r) * G, G, p.M,
+          [&](int c) { return __ldcg(rn + c); }, G, p.M,
           [&](int c, int i) { return __ldcg(rc + static_cast<size_t>(c) * cap + i); },
           p.ids + static_cast<size_t>(r) * p.M, p.vals + static_cast<size_t>(r) * p.M, S, s_warp, &s_n);
       __syncthreads();

@@ -1,5 +1,4 @@
-// The top-M filter of one chunk of a logits row, shared by dt_topm's filter kernel and the small-batch round kernel
-// (which runs the top-M inside its own persistent launch). Not part of the C ABI.
+// The top-M filter of one chunk of a logits row (dt_topm's filter kernel). Not part of the C ABI.
 //
 // A chunk is kThreads threads x kGroups 16-byte groups of logits, staged once into shared memory by cp.async (every
 // group in flight together, no registers held). It keeps every logit at or above a lower bound of its row's M-th
@@ -475,8 +474,9 @@ __device__ void select_row(int row, const void* __restrict__ words, const int* _
   using CWord = typename T::CWord;
   const CWord* base = static_cast<const CWord*>(words) + static_cast<size_t>(row) * chunks * cap;
   const long long row_out = static_cast<long long>(row) * M;
+  const int* cnt = counts + static_cast<size_t>(row) * chunks;
   select_words<kBf16, kThreads>(
-      counts + static_cast<size_t>(row) * chunks, chunks, M,
+      [&](int c) { return __ldcg(cnt + c); }, chunks, M,
       [&](int c, int i) { return T::global_word(__ldcg(base + static_cast<size_t>(c) * cap + i), c * T::kChunk); },
       out_ids + row_out, out_vals + row_out, S, s_warp, s_n_ptr);
 }

@@ -76,12 +76,12 @@ struct SelectSmem {                           // lives in the caller's shared me
   unsigned red[2][16];                        // per-warp key minima and maxima (up to 512 threads)
 };
 
-// The row's selection over `chunks` lists of candidate words: cnt[c] words in list c, word i of list c given by
+// The row's selection over `chunks` lists of candidate words: count(c) words in list c, word i of list c given by
 // load(c, i) as a 64-bit row word (value key << 32 | ~id). kBf16: the keys are bf16 keys (16 bits), else fp32 keys.
 // Writes the row's M ids and values (in order) to ids[0..M), vals[0..M). Called by all kThreads threads (256 or 512;
 // s_warp holds kThreads / 32 ints).
-template <bool kBf16, int kThreads, class Load>
-__device__ void select_words(const int* __restrict__ cnt, int chunks, int M, Load load, int32_t* __restrict__ ids,
+template <bool kBf16, int kThreads, class Count, class Load>
+__device__ void select_words(Count count, int chunks, int M, Load load, int32_t* __restrict__ ids,
                              float* __restrict__ vals, SelectSmem& S, int* s_warp, int* s_n_ptr) {
   static_assert(kThreads >= 256 && kThreads <= 512 && kThreads % 32 == 0, "one histogram bin per thread at most");
   constexpr int kWarps = kThreads / 32;
@@ -100,7 +100,7 @@ __device__ void select_words(const int* __restrict__ cnt, int chunks, int M, Loa
 #pragma unroll
     for (int j = 0; j < kChunksPerThread; ++j) {
       const int c = kChunksPerThread * t + j;
-      c_of[j] = c < chunks ? __ldcg(cnt + c) : 0;
+      c_of[j] = c < chunks ? count(c) : 0;
       mine += c_of[j];
     }
     int off = block_exclusive_scan<kWarps>(mine, &total, s_warp);
@@ -112,7 +112,7 @@ __device__ void select_words(const int* __restrict__ cnt, int chunks, int M, Loa
     }
   } else {
     int mine = 0;
-    for (int c = t; c < chunks; c += kThreads) mine += __ldcg(cnt + c);
+    for (int c = t; c < chunks; c += kThreads) mine += count(c);
     total = block_sum<kWarps>(mine, s_warp);
   }
   if (t == 0) s_n = 0;
@@ -135,7 +135,7 @@ __device__ void select_words(const int* __restrict__ cnt, int chunks, int M, Loa
       for (int i = t; i < total; i += kThreads) f(w[i]);
     } else {
       for (int c = 0; c < chunks; ++c) {
-        const int nc = __ldcg(cnt + c);
+        const int nc = count(c);
         for (int i = t; i < nc; i += kThreads) f(load(c, i));
       }
     }
