@@ -13,6 +13,11 @@ written lines are not written back inside the next timed call); barrier + synchr
 ranks. ``e2e`` runs the same rounds through the host-buffer API (pinned logits
 and h0 copied in, the tree copied out, every step). The SM clock is sampled through NVML during the timed region.
 
+``configs`` measures every workload (c0-c4) briefly in the same run: µs per round, trees/s, the top-M's and the gather
+stage's bandwidth (the builder's own statistics: correction-row bytes gathered over the longest time one CTA spent
+gathering them), the round-level roofline (logits read once plus gathered rows, over HBM bandwidth) and, for c0-c2,
+the oracle on one thread.
+
 ``--impl reference`` times the CPU oracle (fp64, the plain restatement of the method) on the same workload.
 Prints one JSON line (rank 0).
 """
@@ -54,6 +59,10 @@ def parse():
     ap.add_argument("--builder", choices=["conditional", "marginal"], default="conditional",
                     help="conditional: dt_build_trees (the method); marginal: dt_build_trees_marginal (DDTree scoring)")
     ap.add_argument("--reference-budget", type=float, default=150.0, help="seconds for the whole reference arm")
+    ap.add_argument("--configs", default="0,1,2,3,4",
+                    help="workloads also measured briefly in the same run (the 'configs' block; empty: none)")
+    ap.add_argument("--oracle-1t-budget", type=float, default=8.0,
+                    help="seconds of single-threaded oracle work per workload of the configs block (c0-c2)")
     return ap.parse_args()
 
 
@@ -133,7 +142,7 @@ def measured_peaks():
 
 # The sources each C-ABI call is built from: a committed ncu figure counts only while they are unchanged.
 CALL_SOURCES = {
-    "dt_topm": ["topm.cu", "topm_select.cuh", "dt_internal.cuh"],
+    "dt_topm": ["topm.cu", "topm_filter.cuh", "topm_select.cuh", "dt_internal.cuh"],
     "dt_build_trees": ["build_trees.cu", "build_small.cu", "build_common.cuh", "umma.cuh", "dt_internal.cuh"],
 }
 
@@ -191,6 +200,93 @@ def algorithmic_bytes(shape, tokens, parents, depth):
     gru_w = 3 * H * (E + H) * s + 6 * H * s
     build = wc + emb + gru_w + B * K * M * 8 + B * H * 4 + B * n * 16 + B * n * n
     return topm, build, dict(w_c_rows=wc, emb_rows=emb, gru_weights=gru_w)
+
+
+def round_bytes(shape, parts):
+    """The round-level roofline numerator: the logits read once plus the gathered rows (W_c rows of the expanded
+    block positions and the expansions' embedding rows), from the trees actually built."""
+    s = 4 if shape.dtype == "f32" else 2
+    return shape.B * shape.K * shape.V * s + parts["w_c_rows"] + parts["emb_rows"]
+
+
+def oracle_single_thread(inp, budget_s):
+    """The oracle on one thread: whole rounds of a bounded sample of the workload's requests, for about budget_s."""
+    import numpy as np
+    from oracle import oracle as orc
+    from speculative_decoding_tree_top_gb300.synth import host_array
+    s = inp.shape
+    logits = host_array(inp.logits)
+    h0 = host_array(inp.h0).astype(np.float64)
+    w = orc.weights_of(inp)
+    trees, t0 = 0, time.perf_counter()
+    b = 0
+    while True:
+        ids, vals = orc.topm(np.ascontiguousarray(logits[b:b + 1]), s.M, threads=1)
+        orc.build_trees(ids, vals, h0[b:b + 1], w, s.n, s.max_depth, s.T, threads=1)
+        trees += 1
+        b = (b + 1) % s.B
+        el = time.perf_counter() - t0
+        if el >= budget_s or (trees >= s.B and el >= 0.25 * budget_s):
+            break
+    return {"trees_per_sec": round(trees / el, 3), "s_per_tree": round(el / trees, 4), "cores": 1,
+            "sample": f"{trees} whole trees (top-M of the request's {s.K} rows, then its tree) in {el:.1f} s"}
+
+
+def measure_configs(args, dev, flush_l2, stream, peak):
+    """Every workload briefly, in the same process: round time, the per-call split, the stages' bandwidth, the
+    round-level roofline, and (c0-c2) the oracle on one thread."""
+    import numpy as np
+    import torch
+    from speculative_decoding_tree_top_gb300 import dominotree as dt, synth
+    out = {}
+    steps_of = {0: 50, 1: 50, 2: 30, 3: 30, 4: 15}
+    for c in [int(x) for x in args.configs.split(",") if x.strip() != ""]:
+        s = synth.shape(c)
+        inp = synth.make_inputs(c, device=dev, seed=1234 + 100 * c)
+        w = dt.Weights.of(inp)
+        rnd = dt.Round(s.B, s.K, s.V, s.M, s.n, s.max_depth, s.T, w, device=dev)
+        for _ in range(3):
+            rnd.round(inp.logits, inp.h0, stream)
+        steps = steps_of.get(c, 20)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+        torch.cuda.synchronize()
+        for e in ev:
+            flush_l2()
+            e[0].record(stream)
+            rnd.round(inp.logits, inp.h0, stream)
+            e[1].record(stream)
+            flush_l2()
+            e[2].record(stream)
+            rnd.topm(inp.logits, stream)
+            e[3].record(stream)
+            rnd.build(inp.h0, stream)
+            e[4].record(stream)
+        torch.cuda.synchronize()
+        rnd.check()
+        stats = dt.dt_build_stats_read(rnd.workspace, stream)
+        r_us = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]) * 1e3)
+        t_us = float(np.mean([e[2].elapsed_time(e[3]) for e in ev]) * 1e3)
+        b_us = float(np.mean([e[3].elapsed_time(e[4]) for e in ev]) * 1e3)
+        o = {k: v.cpu().numpy() for k, v in rnd.out.items()}
+        topm_b, build_b, parts = algorithmic_bytes(s, o["tokens"], o["parents"], o["depth"])
+        rb = round_bytes(s, parts)
+        gather_gbps = stats["gather_bytes"] / stats["gather_ns"] if stats["gather_ns"] else None
+        d = {"workload": s.describe(), "steps": steps, "us_per_round": round(r_us, 2),
+             "trees_per_sec": round(s.B / (r_us * 1e-6), 1),
+             "dt_topm": {"us": round(t_us, 2), "gbps": round(topm_b / (t_us * 1e3), 1),
+                         "frac_of_hbm_peak": round(topm_b / (t_us * 1e3) / peak, 4)},
+             "dt_build_trees": {"us": round(b_us, 2), "waves": stats["waves"], "expansions": stats["expansions"],
+                                "gather": {"bytes": stats["gather_bytes"], "ns": stats["gather_ns"],
+                                           "gbps": round(gather_gbps, 1) if gather_gbps else None,
+                                           "frac_of_hbm_peak": round(gather_gbps / peak, 4) if gather_gbps else None}},
+             "round_roofline": {"bytes": rb, "us_at_peak": round(rb / (peak * 1e3), 3),
+                                "frac": round(rb / (r_us * 1e3) / peak, 4)}}
+        if c <= 2 and args.oracle_1t_budget > 0:
+            d["oracle_1_thread"] = oracle_single_thread(inp, args.oracle_1t_budget)
+        out[f"c{c}"] = d
+        del rnd, inp, w
+        torch.cuda.empty_cache()
+    return out
 
 
 # ---------------------------------------------------------------------------------------------------------------
@@ -467,6 +563,15 @@ def run_ours(args, world, rank, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not marginal:
         cpu = cpu_baseline(inp, args.cpu_budget)
 
+    rbytes = round_bytes(s, parts) if not marginal else None
+    round_roofline = None if marginal else {
+        "bytes": rbytes, "achieved_gbps": round(rbytes / (total_s / args.steps * 1e9), 1), "peak": peak,
+        "frac": round(rbytes / (total_s / args.steps * 1e9) / peak, 4),
+        "definition": "logits read once plus the gathered W_c and embedding rows, over HBM bandwidth, per round"}
+    configs = None
+    if rank == 0 and world == 1 and not marginal and args.configs.strip():
+        configs = measure_configs(args, dev, flush_l2, stream, peak)
+
     if rank != 0:
         return None
     return {
@@ -481,7 +586,8 @@ def run_ours(args, world, rank, local):
                    "l2": "flushed between steps outside the timed events: a 256 MB memset, then a 256 MB read of another buffer"},
         "kernels": {k: {kk: (round(vv, 3) if isinstance(vv, float) else vv) for kk, vv in d.items()}
                     for k, d in kernels.items()},
-        "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": (topm_launches(s, torch.cuda.get_device_properties(dev).multi_processor_count) + 1) * args.steps,
+        "roofline": roofline, "round_roofline": round_roofline, "configs": configs, "e2e": e2e,
+        "cpu_baseline": cpu, "gpu_launches": (topm_launches(s, torch.cuda.get_device_properties(dev).multi_processor_count) + 1) * args.steps,
         "clocks": clocks.summary(), "wall_s_timed_loop": round(t_wall, 4),
     }
 

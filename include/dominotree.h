@@ -267,6 +267,27 @@ dt_status dt_tree_attention(int B, int n, int L, int Hq, int Hkv, int d, const v
 dt_status dt_topm_static(const void* logits, dt_dtype dtype, int B, int K, int V, int M, int32_t* out_ids,
                          float* out_vals, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------------------------------------------
+ * dt_build_stats_read — what the last dt_build_trees (or dt_round) launch on `workspace` did, for measurement.
+ * No counterpart in the paper (an observability hook). Synchronises `stream`, then reads the statistics the kernel
+ * recorded in the workspace's header (a few words, written on every launch at negligible cost):
+ *   launch_ns      time from CTA 0's start to its end (globaltimer), about the kernel's duration;
+ *   gather_ns      the longest time any one CTA spent gathering correction rows W_c[ids]: in the large-batch
+ *                  builder (B > 8) the children phases, where each group of expansions gathers its position's M rows
+ *                  and forms their corrections; in the small-batch builder the W_c column gathers;
+ *   gather_bytes   the correction rows those gathers read, counted once per gathered row (rows x H x element size);
+ *   waves          waves the launch ran; expansions: GRU steps and roots expanded.
+ * gather_bytes / gather_ns is the gather stage's achieved bandwidth. Argument errors: DT_ERR_INVALID_ARG.
+ * ------------------------------------------------------------------------------------------------------------- */
+typedef struct {
+  uint64_t launch_ns;
+  uint64_t gather_ns;
+  uint64_t gather_bytes;
+  int32_t waves;
+  int32_t expansions;
+} dt_build_stats;
+dt_status dt_build_stats_read(void* workspace, dt_build_stats* out, cudaStream_t stream);
+
 /* Synchronises `stream`, then reads and clears the status word the device wrote into `workspace`. Returns DT_OK
  * when no device-side problem was recorded. After DT_ERR_TIMEOUT the workspace must be re-initialised. */
 dt_status dt_get_error(void* workspace, cudaStream_t stream);

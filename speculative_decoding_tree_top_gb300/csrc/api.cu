@@ -109,3 +109,18 @@ extern "C" dt_status dt_get_error(void* workspace, cudaStream_t stream) {
   }
   return static_cast<dt_status>(status);
 }
+
+extern "C" dt_status dt_build_stats_read(void* workspace, dt_build_stats* out, cudaStream_t stream) {
+  if (!workspace || !out || !dt::aligned16(workspace)) return DT_ERR_INVALID_ARG;
+  dt::WsHeader h{};
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&h, workspace, sizeof h, cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return DT_ERR_CUDA;
+  out->launch_ns = h.stat_launch_ns;
+  out->gather_ns = h.stat_gather_ns;
+  out->gather_bytes = h.stat_gather_bytes;
+  out->waves = static_cast<int32_t>(h.stat_waves);
+  out->expansions = static_cast<int32_t>(h.stat_expansions);
+  return DT_OK;
+}

@@ -44,6 +44,15 @@ struct Job {
                 // expands it speculatively (its score is known only once the root's children are scored), else 0
 };
 
+// Expansions of one request at one block position, consecutive in a wave's packed list: they share the M correction
+// rows of that position (large-batch builder).
+struct JobGroup {
+  int start;  // first expansion in the packed list
+  int count;  // expansions (at most the lookahead width)
+  int b;      // request
+  int depth;  // depth of the expanded nodes: their children take block position `depth`
+};
+
 // Warp-wide best of one candidate per lane (`has` false: none), in pop order: higher score (-0.0 equal to +0.0),
 // then lower token, then lower insertion index, then lower lane. One warp reduction picks the lane when the best
 // score is held by one lane only (the common case); ties take two more reductions. Returns the lane (-1 if no lane
@@ -331,6 +340,10 @@ struct Params {
   unsigned char* rstate;  // [B] per-request best-first state blocks of req_layout(...).bytes (large-batch builder)
   Job* joblist;     // [2][B * lookahead] the expansions of a wave, packed (large-batch builder)
   int* jobcount;    // [xslots + 2] expansions per wave (large-batch builder)
+  JobGroup* grouplist;  // [2][B * lookahead] the wave's expansions of one request at one depth (large-batch builder)
+  int* groupcount;      // [xslots + 2] groups per wave (large-batch builder)
+  bool group_mma;   // large-batch builder: a group's corrections as one tensor-core product (bf16, H % 16 == 0,
+                    // M <= 128, the group's rows in shared memory)
   unsigned short* xact;  // [B * lookahead][E + 2H] bf16 GRU inputs of the next wave's expansions (tensor-core GRU)
   bool xact_on;     // the control phase writes xact (the tensor-core GRU runs)
   uint64_t timeout_ns;
@@ -423,6 +436,64 @@ __device__ __forceinline__ void warp_dot_rows8(const void* rows, const void* w, 
     for (int j = 0; j < 8; ++j) out[j] += __shfl_xor_sync(0xFFFFFFFFu, out[j], o);
 }
 
+// A job's children ranked among themselves by one warp: a bitonic sort of their sibling keys (larger first; equal
+// keys, possible only when a row repeats an id, by the lower candidate index) over 32 * R elements, element i in
+// register i / 32 of lane i % 32; padding (index >= M) has key 0 and sorts last. The first kc go to out[0 .. kc).
+template <int R>
+__device__ __forceinline__ void rank_children_warp(const Node* kr, const unsigned long long* kk, int M, Node* out,
+                                                   int kc) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long k[R];
+  int m[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    m[r] = 32 * r + lane;
+    k[r] = m[r] < M ? kk[m[r]] : 0ull;
+  }
+  auto first = [](unsigned long long ka, int ma, unsigned long long kb, int mb) {
+    return (ka > kb) | ((ka == kb) & (ma < mb));
+  };
+#pragma unroll
+  for (int size = 2; size <= 32 * R; size <<= 1) {
+#pragma unroll
+    for (int j = size >> 1; j > 0; j >>= 1) {
+      if (j >= 32) {  // both elements of every pair sit in one lane: registers r and r + j / 32
+        const int jr = j >> 5;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          if (r & jr) continue;
+          const int r2 = r | jr;
+          const bool desc = ((32 * r + lane) & size) == 0;  // this block is sorted larger-first
+          if (first(k[r], m[r], k[r2], m[r2]) != desc) {
+            const unsigned long long tk = k[r];
+            k[r] = k[r2];
+            k[r2] = tk;
+            const int tm = m[r];
+            m[r] = m[r2];
+            m[r2] = tm;
+          }
+        }
+      } else {  // the pair spans lanes lane and lane ^ j, same register
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const unsigned long long ok = __shfl_xor_sync(0xFFFFFFFFu, k[r], j);
+          const int om = __shfl_xor_sync(0xFFFFFFFFu, m[r], j);
+          const bool desc = ((32 * r + lane) & size) == 0;
+          const bool lower = (lane & j) == 0;
+          const bool mine_first = first(k[r], m[r], ok, om);
+          if (mine_first != (lower == desc)) {
+            k[r] = ok;
+            m[r] = om;
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+    if (32 * r + lane < kc) out[32 * r + lane] = kr[m[r]];
+}
+
 // A request's best-first state as one contiguous block (the large-batch builder keeps it in the workspace between
 // waves and works on it in shared memory; offsets are multiples of 16 so the block moves as one bulk copy).
 struct ReqLayout {
@@ -462,7 +533,7 @@ constexpr int kLargeDefault = 4;    // ... and its default (kLargeLookahead once
 // per-slot publication counters; for larger ones the per-request state blocks, the packed job lists of two waves and
 // the per-wave job counts.
 struct BuildLayout {
-  size_t hs, acc, hs_count, rstate, joblist, jobcount, xact, gru_part, gru_ticket, bytes;
+  size_t hs, acc, hs_count, rstate, joblist, jobcount, grouplist, groupcount, xact, gru_part, gru_ticket, bytes;
   int gru_tiles;
 };
 
@@ -496,8 +567,10 @@ inline BuildLayout build_layout(int B, int K, int V, int M, int n, int H, int E)
   // both builders may run for small batches (the small one needs shared memory the device may not have)
   L.joblist = align_up(L.rstate + req_layout(n, static_cast<int>(X), KM, kLargeLookahead).bytes * B);
   L.jobcount = align_up(L.joblist + sizeof(Job) * 2 * static_cast<size_t>(B) * kLargeLookahead);
+  L.grouplist = align_up(L.jobcount + sizeof(int) * (X + 2));
+  L.groupcount = align_up(L.grouplist + sizeof(JobGroup) * 2 * static_cast<size_t>(B) * kLargeLookahead);
   // the tensor-core GRU's A operand: one bf16 row [emb | hi(h_parent) | lo(h_parent)] per expansion of a wave
-  L.xact = align_up(L.jobcount + sizeof(int) * (X + 2));
+  L.xact = align_up(L.groupcount + sizeof(int) * (X + 2));
   L.gru_part = align_up(L.xact + sizeof(unsigned short) * static_cast<size_t>(B) * kLargeLookahead * (E + 2 * H));
   L.gru_tiles = gru_spread_tiles(B, H);
   L.gru_ticket = align_up(L.gru_part + sizeof(float) * static_cast<size_t>(L.gru_tiles) * kGruSplits * kGruTileRows *

@@ -140,64 +140,6 @@ __device__ __forceinline__ unsigned long long sibling_key(const Node& e) {
          static_cast<unsigned long long>(~static_cast<uint32_t>(e.token));
 }
 
-// A job's children ranked among themselves by one warp: a bitonic sort of their sibling keys (larger first; equal
-// keys, possible only when a row repeats an id, by the lower candidate index) over 32 * R elements, element i in
-// register i / 32 of lane i % 32; padding (index >= M) has key 0 and sorts last. The first kc go to out[0 .. kc).
-template <int R>
-__device__ __forceinline__ void rank_children_warp(const Node* kr, const unsigned long long* kk, int M, Node* out,
-                                                   int kc) {
-  const int lane = threadIdx.x & 31;
-  unsigned long long k[R];
-  int m[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    m[r] = 32 * r + lane;
-    k[r] = m[r] < M ? kk[m[r]] : 0ull;
-  }
-  auto first = [](unsigned long long ka, int ma, unsigned long long kb, int mb) {
-    return (ka > kb) | ((ka == kb) & (ma < mb));
-  };
-#pragma unroll
-  for (int size = 2; size <= 32 * R; size <<= 1) {
-#pragma unroll
-    for (int j = size >> 1; j > 0; j >>= 1) {
-      if (j >= 32) {  // both elements of every pair sit in one lane: registers r and r + j / 32
-        const int jr = j >> 5;
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          if (r & jr) continue;
-          const int r2 = r | jr;
-          const bool desc = ((32 * r + lane) & size) == 0;  // this block is sorted larger-first
-          if (first(k[r], m[r], k[r2], m[r2]) != desc) {
-            const unsigned long long tk = k[r];
-            k[r] = k[r2];
-            k[r2] = tk;
-            const int tm = m[r];
-            m[r] = m[r2];
-            m[r2] = tm;
-          }
-        }
-      } else {  // the pair spans lanes lane and lane ^ j, same register
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const unsigned long long ok = __shfl_xor_sync(0xFFFFFFFFu, k[r], j);
-          const int om = __shfl_xor_sync(0xFFFFFFFFu, m[r], j);
-          const bool desc = ((32 * r + lane) & size) == 0;
-          const bool lower = (lane & j) == 0;
-          const bool mine_first = first(k[r], m[r], ok, om);
-          if (mine_first != (lower == desc)) {
-            k[r] = ok;
-            m[r] = om;
-          }
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int r = 0; r < R; ++r)
-    if (32 * r + lane < kc) out[32 * r + lane] = kr[m[r]];
-}
-
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                                uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -259,12 +201,18 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
   // ---- launch: weights of the owned units, W_c columns / ids / base logits of the candidates, L2 prefetch ----
   // The 3 * nu rows of W_ih and of W_hh as bulk copies (1 to 8 KB each) completing on one mbarrier, issued by warp 0;
   // waited for before the first GRU step.
+  const uint64_t t_launch = global_timer_ns();
   if (t == 0) {
     mbar_init(&wbar, 1);
     mbar_init(&jbar, 1);
     mbar_fence_init();
+    if (j == 0) {  // the launch's statistics start from zero (before the grid barrier, after which they are raised)
+      p.hdr->stat_launch_ns = p.hdr->stat_gather_ns = p.hdr->stat_gather_bytes = 0ull;
+      p.hdr->stat_waves = p.hdr->stat_expansions = 0u;
+    }
   }
   __syncthreads();
+  uint64_t gather_ns = 0, gather_bytes = 0;  // this CTA's time in the W_c gathers; the rows they read (CTA 0)
   for (int i = t; i < 3 * umax; i += kThreads) {
     const int g = i / umax, u = i % umax;
     const size_t row = static_cast<size_t>(g) * H + u0 + u;
@@ -286,6 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
   // (one bulk prefetch per row, spread over the CTAs, so HBM serves whole rows), then every CTA takes its columns.
   auto gather_wc = [&](int p0, int p1) {
     const int np = p1 - p0;
+    const uint64_t g0 = global_timer_ns();
     const unsigned rb = static_cast<unsigned>(H * esize);
     for (int i = j * kThreads + t; i < B * np * M; i += G * kThreads) {
       const int b = i / (np * M), pos = p0 + (i / M) % np, m = i % M;
@@ -301,6 +250,9 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
       const int c = (b * maxd + pos) * M + m;
       wc[c * umax + u] = u < nu ? static_cast<const T*>(p.w_c)[static_cast<size_t>(ids_s[c]) * H + u0 + u] : T(0);
     }
+    __syncthreads();  // every thread's columns are in (and the statistics see the whole gather)
+    gather_ns += global_timer_ns() - g0;
+    gather_bytes += static_cast<uint64_t>(B) * np * M * H * esize;
   };
   // the 3 * nu rows of W_ih and of W_hh as bulk copies (1 to 8 KB each) completing on one mbarrier, issued by warp 0;
   // waited for before the first GRU step
@@ -428,6 +380,10 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
       return;
     }
     long long* acc_w = p.acc + static_cast<size_t>(w) * kJ * M * AS;
+    if (j == 0 && t == 0) {
+      p.hdr->stat_waves = w + 1;
+      p.hdr->stat_expansions += (w == 0 ? B * (1 + nspec) : J);
+    }
     // a GRU step runs unless the wave holds roots only (roots take h = h0); wave 0 also holds the speculative jobs
     const bool gru = w > 0 || nspec > 0;
     const bool spec_wave = w == 0 && nspec > 0;
@@ -806,6 +762,13 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
   }
 
   drain(-1);  // a round without GRU steps (n = 1, or max depth 1) never waited for the weights
+  if (t == 0) {
+    atomicMax(&p.hdr->stat_gather_ns, static_cast<unsigned long long>(gather_ns));
+    if (j == 0) {
+      p.hdr->stat_gather_bytes = gather_bytes;
+      p.hdr->stat_launch_ns = global_timer_ns() - t_launch;
+    }
+  }
   // ---- outputs (CTA 0): nodes in pop order, and the ancestor mask by walking each node's parent chain ----
   if (j == 0) {
     for (int b = 0; b < B; ++b) resolve_parents(pops + b * n, popidx + b * X, n, t, kThreads);

@@ -389,6 +389,34 @@ __host__ __device__ inline FrontierSmem frontier_smem(size_t state_bytes, int M,
 }
 constexpr size_t kFrontierRowsCap = 160 * 1024;  // gathered rows kept in shared memory up to this size
 
+// The children phase by groups (one request's expansions at one block position, group_mma): the J <= kLargeLookahead
+// hidden states [8][H] fp32, the position's ids and base logits, the M gathered correction rows [M][H + 8] bf16 (the
+// row stride padded by 16 bytes, so the MMA's row fragments fall in distinct banks), the corrected logits [8][M], and
+// per expansion its children [8][M] and their sibling keys [8][M].
+struct GroupSmem {
+  size_t h, ids, vals, rows, z, zpart, kraw, keys, mine, bytes;
+};
+__host__ __device__ inline GroupSmem group_smem(int M, int H) {
+  GroupSmem L{};
+  size_t o = 0;
+  auto take = [&o](size_t bytes) {
+    const size_t at = o;
+    o = (o + bytes + 15) / 16 * 16;
+    return at;
+  };
+  L.h = take(sizeof(float) * kLargeLookahead * H);
+  L.ids = take(sizeof(int) * round4(M));
+  L.vals = take(sizeof(float) * round4(M));
+  L.rows = take(sizeof(unsigned short) * static_cast<size_t>(M) * (H + 8));
+  L.z = take(sizeof(float) * kLargeLookahead * round4(M));
+  L.zpart = take(sizeof(float) * kWarps * kLargeLookahead * 16);  // one 16 x 8 partial tile per warp
+  L.kraw = take(sizeof(Node) * kLargeLookahead * M);
+  L.keys = take(sizeof(unsigned long long) * kLargeLookahead * M);
+  L.mine = take(sizeof(int) * (kThreads + 1));  // own mode: this CTA's groups among the next kThreads of the list
+  L.bytes = o;
+  return L;
+}
+
 __device__ __forceinline__ void bulk_s2g(void* gdst, const void* ssrc, unsigned bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(ssrc)), "r"(bytes)
                : "memory");
@@ -642,6 +670,169 @@ __device__ __forceinline__ bool wait_copies(const Params& p, uint64_t* bar, unsi
   return ok;
 }
 
+// ---- phase B1 by groups: one request's expansions at one block position share that position's correction rows --
+// The group's M rows W_c[ids] are gathered once (bulk copies on an mbarrier, with the group's hidden states) and the
+// corrections of all its J expansions come out of one tensor-core product Z[M][J] = W_c[ids] . [h_1 .. h_J]:
+// mma.sync m16n8k16, the rows as A (a warp per 16 rows), the hidden states as the n8 B tile, split into bf16 hi + lo
+// pairs (as the GRU's hidden side). Column j of Z depends on h_j alone, summed in a fixed order, so an expansion's
+// children do not depend on which expansions share its group. Then one warp per expansion: the restricted
+// log-softmax, and the children ranked by a warp sort (M <= 128) into the request's state block. Groups go to CTAs as
+// expansions do (own requests, or group g to CTA g mod G). Returns false when a copy wait ran out.
+__device__ bool children_groups(const Params& p, int w, const Job* jl, unsigned char* smem, uint64_t* bar,
+                                unsigned& bar_uses) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int M = p.M, n = p.n, H = p.H, X = p.xslots, KM = M < n ? M : n;
+  const ReqLayout RL = req_layout(n, X, KM, p.lookahead);
+  const GroupSmem GS = group_smem(M, H);
+  float* hbuf = reinterpret_cast<float*>(smem + GS.h);
+  int* ids = reinterpret_cast<int*>(smem + GS.ids);
+  float* vals = reinterpret_cast<float*>(smem + GS.vals);
+  unsigned short* rows_s = reinterpret_cast<unsigned short*>(smem + GS.rows);
+  float* z = reinterpret_cast<float*>(smem + GS.z);
+  Node* kraw = reinterpret_cast<Node*>(smem + GS.kraw);
+  unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem + GS.keys);
+  const int SW = H + 8;  // padded row stride of the gathered rows (elements)
+  const int M4 = round4(M);
+  const unsigned rb = static_cast<unsigned>(H * 2);
+  const int ngroups = __ldcg(p.groupcount + w);
+  const JobGroup* gl = p.grouplist + static_cast<size_t>(w & 1) * p.B * p.lookahead;
+  const bool own = p.B >= static_cast<int>(gridDim.x);
+  int* s_mine = reinterpret_cast<int*>(smem + GS.mine);
+  for (int g0 = own ? 0 : blockIdx.x; g0 < ngroups; g0 += own ? kThreads : gridDim.x) {
+    int nmine = 1;
+    if (own) {  // the groups of this CTA's requests in this batch, found by every thread at once
+      __syncthreads();
+      if (t == 0) s_mine[kThreads] = 0;
+      __syncthreads();
+      if (g0 + t < ngroups && gl[g0 + t].b % static_cast<int>(gridDim.x) == static_cast<int>(blockIdx.x))
+        s_mine[atomicAdd(&s_mine[kThreads], 1)] = g0 + t;
+      __syncthreads();
+      nmine = s_mine[kThreads];
+    }
+    for (int k = 0; k < nmine; ++k) {
+      const JobGroup gr = gl[own ? s_mine[k] : g0];
+      const int J = gr.count;
+      const size_t pos = (static_cast<size_t>(gr.b) * p.K + gr.depth) * M;
+      __syncthreads();  // the previous group is done with the shared buffers
+      for (int m = t; m < M; m += kThreads) {  // ids and base logits of the group's block position
+        ids[m] = valid_id(p, __ldg(p.ids + pos + m));
+        vals[m] = __ldg(p.vals + pos + m);
+      }
+      __syncthreads();
+      if (warp == 0) {  // the group's hidden states (written by the GRU phase through the generic proxy) and rows
+        if (lane == 0) {
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          mbar_expect_tx(bar, static_cast<unsigned>(J * H * 4) + rb * static_cast<unsigned>(M));
+        }
+        __syncwarp();
+        if (lane < J)
+          bulk_g2s(hbuf + static_cast<size_t>(lane) * H,
+                   p.hs + (static_cast<size_t>(gr.b) * X + jl[gr.start + lane].xslot) * H, static_cast<unsigned>(H * 4),
+                   bar);
+        for (int m = lane; m < M; m += 32)
+          bulk_g2s(rows_s + static_cast<size_t>(m) * SW, static_cast<const char*>(p.w_c) + static_cast<size_t>(ids[m]) * rb,
+                   rb, bar);
+      }
+      if (!own && g0 + static_cast<int>(gridDim.x) < ngroups && warp == 1) {  // the next group's rows, into L2
+        const JobGroup ng = gl[g0 + gridDim.x];
+        const size_t npos = (static_cast<size_t>(ng.b) * p.K + ng.depth) * M;
+        for (int m = lane; m < M; m += 32) {
+          const int id = __ldg(p.ids + npos + m);
+          if (static_cast<unsigned>(id) < static_cast<unsigned>(p.V))
+            prefetch_l2(static_cast<const char*>(p.w_c) + static_cast<size_t>(id) * rb, rb);
+        }
+      }
+      if (!__syncthreads_and(wait_copies(p, bar, bar_uses))) return false;
+      // Z[M][8] = rows . [h_0 .. h_7], columns j >= J unused. The 16-row tiles times `ks` K parts make the warps'
+      // work (ks = 8 / tiles, so every warp has a share when M < 128); each warp runs two accumulator chains (even
+      // and odd k16 steps) and stores its partial tile; the partials are then added in a fixed order (part 0 first,
+      // even chain before odd), the same for every group, so Z does not depend on how many columns are in use.
+      {
+        const int g = lane >> 2, tg = lane & 3;
+        const int tiles = (M + 15) / 16, ks = tiles >= kWarps ? 1 : kWarps / tiles, steps = H / 16;
+        const float* hb = hbuf + static_cast<size_t>(g < J ? g : 0) * H;
+        float* zp = reinterpret_cast<float*>(smem + GS.zpart);
+        for (int item = warp; item < tiles * ks; item += kWarps) {
+          const int mt = item / ks, part = item % ks;
+          const int s0 = steps * part / ks, s1 = steps * (part + 1) / ks;
+          const int r0 = min(mt * 16 + g, M - 1), r1 = min(mt * 16 + g + 8, M - 1);
+          const unsigned short* a_lo = rows_s + static_cast<size_t>(r0) * SW;
+          const unsigned short* a_hi = rows_s + static_cast<size_t>(r1) * SW;
+          float de[4] = {0.f, 0.f, 0.f, 0.f}, dodd[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int st = s0; st < s1; ++st) {
+            const int kk = st * 16 + tg * 2;
+            const uint32_t a0 = *reinterpret_cast<const uint32_t*>(a_lo + kk), a1 = *reinterpret_cast<const uint32_t*>(a_hi + kk);
+            const uint32_t a2 = *reinterpret_cast<const uint32_t*>(a_lo + kk + 8);
+            const uint32_t a3 = *reinterpret_cast<const uint32_t*>(a_hi + kk + 8);
+            const float2 x0 = *reinterpret_cast<const float2*>(hb + kk), x1 = *reinterpret_cast<const float2*>(hb + kk + 8);
+            uint32_t h0, l0, h1, l1;
+            split_bf16x2(x0.x, x0.y, h0, l0);
+            split_bf16x2(x1.x, x1.y, h1, l1);
+            float (&d)[4] = ((st - s0) & 1) ? dodd : de;
+            mma_bf16_16816(d, a0, a1, a2, a3, h0, h1);
+            mma_bf16_16816(d, a0, a1, a2, a3, l0, l1);
+          }
+          // this item's partial tile: rows g, g + 8 and columns 2 tg, 2 tg + 1 of tile mt
+          float* zt = zp + static_cast<size_t>(item) * 16 * kLargeLookahead;
+          zt[g * kLargeLookahead + 2 * tg] = de[0] + dodd[0];
+          zt[g * kLargeLookahead + 2 * tg + 1] = de[1] + dodd[1];
+          zt[(g + 8) * kLargeLookahead + 2 * tg] = de[2] + dodd[2];
+          zt[(g + 8) * kLargeLookahead + 2 * tg + 1] = de[3] + dodd[3];
+        }
+        __syncthreads();
+        for (int i = t; i < J * M; i += kThreads) {  // the corrected logits: the parts added in order
+          const int j = i / M, m = i % M, mt = m / 16, r = m % 16;
+          float v = 0.f;
+          for (int part = 0; part < ks; ++part)
+            v += zp[static_cast<size_t>(mt * ks + part) * 16 * kLargeLookahead + r * kLargeLookahead + j];
+          z[j * M4 + m] = (vals[m] + v) / p.T_eff;
+        }
+      }
+      __syncthreads();
+      // one warp per expansion: restricted log-softmax, children, their ranking into the request's state block (kc:
+      // at most n - s - 1 of them can still be popped after the node itself, n for the root's; s from the request's
+      // state block, written back by its owner before the last barrier)
+      if (warp < J) {
+        const Job jb = jl[gr.start + warp];
+        const float* zj = z + warp * M4;
+        Node* kr = kraw + warp * M;
+        unsigned long long* kk = keys + warp * M;
+        float mx = -INFINITY;
+        for (int m = lane; m < M; m += 32) mx = fmaxf(mx, zj[m]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+        float sum = 0.f;
+        for (int m = lane; m < M; m += 32) sum += expf(zj[m] - mx);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+        const float lse = logf(sum);
+        for (int m = lane; m < M; m += 32) {
+          Node e;
+          e.score = jb.score + ((zj[m] - mx) - lse);
+          e.token = ids[m];
+          e.seq = m;  // the candidate index until the node is popped
+          e.pslot = static_cast<short>(jb.xslot);
+          e.xslot = -1;
+          kr[m] = e;
+          kk[m] = (static_cast<unsigned long long>(key_of_f32(__float_as_uint(e.score))) << 32) |
+                  static_cast<unsigned long long>(~static_cast<uint32_t>(e.token));
+        }
+        __syncwarp();
+        const ReqView R = req_view(p.rstate + static_cast<size_t>(jb.b) * RL.bytes, RL);
+        const int kc = min(KM, jb.pslot < 0 ? n : n - __ldcg(&R.ctl->s) - 1);
+        Node* out = R.kids + static_cast<size_t>(jb.xslot) * KM;
+        if (M <= 32) rank_children_warp<1>(kr, kk, M, out, kc);
+        else if (M <= 64) rank_children_warp<2>(kr, kk, M, out, kc);
+        else rank_children_warp<4>(kr, kk, M, out, kc);
+        if (lane == 0) R.kcount[jb.xslot] = kc;
+      }
+    }
+  }
+  // the children lists are read back through the async proxy (the owner's bulk copy of the state block)
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return true;
+}
+
 // ---- phase B1: the children of every expansion of the wave, spread over all CTAs ------------------------------
 // Expansion q of the packed list goes to CTA q mod G: the M correction rows of the node's block position gathered
 // and dotted with its new hidden state (bulk copies on an mbarrier; the next expansion's rows are asked of L2
@@ -797,7 +988,27 @@ __device__ bool control_phase(const Params& p, int w, unsigned char* smem, uint6
     if (warp == 0) request_step(R, b, n, M, p.max_depth, X, KM, kla, jobs, p.hdr);
     __syncthreads();
     const ReqCtl st = *R.ctl;
-    if (t == 0) s_off = st.njobs > 0 ? atomicAdd(p.jobcount + w + 1, st.njobs) : 0;
+    if (t == 0 && st.njobs > 0) {
+      // the picks in order of depth (stable): a request's expansions at one block position sit together in the packed
+      // list, and each such run is a group of the children phase
+      for (int i = 1; i < st.njobs; ++i)
+        for (int k = i; k > 0 && jobs[k - 1].depth > jobs[k].depth; --k) {
+          const Job tmp = jobs[k];
+          jobs[k] = jobs[k - 1];
+          jobs[k - 1] = tmp;
+        }
+      int ng = 1;
+      for (int i = 1; i < st.njobs; ++i) ng += jobs[i].depth != jobs[i - 1].depth;
+      s_off = atomicAdd(p.jobcount + w + 1, st.njobs);
+      int gi = atomicAdd(p.groupcount + w + 1, ng);
+      JobGroup* gnext = p.grouplist + static_cast<size_t>((w + 1) & 1) * p.B * kla;
+      for (int i = 0; i < st.njobs;) {
+        int e = i + 1;
+        while (e < st.njobs && jobs[e].depth == jobs[i].depth) ++e;
+        gnext[gi++] = JobGroup{s_off + i, e - i, b, jobs[i].depth};
+        i = e;
+      }
+    }
     __syncthreads();
     for (int q = t; q < st.njobs; q += kThreads) next[s_off + q] = jobs[q];
     if (p.xact_on) {  // the picks' GRU inputs as the tensor-core GRU reads them: [emb | hi(h_parent) | lo(h_parent)]
@@ -857,10 +1068,16 @@ __device__ void init_requests(const Params& p, unsigned char* smem) {
   const int M = p.M, n = p.n, H = p.H, X = p.xslots, KM = M < n ? M : n;
   const ReqLayout RL = req_layout(n, X, KM, p.lookahead);
   // wave 0 expands the roots: its packed list holds one job per request
-  for (int i = blockIdx.x * kThreads + t; i < X + 2; i += gridDim.x * kThreads) p.jobcount[i] = i == 0 ? p.B : 0;
+  for (int i = blockIdx.x * kThreads + t; i < X + 2; i += gridDim.x * kThreads) {
+    p.jobcount[i] = i == 0 ? p.B : 0;
+    p.groupcount[i] = i == 0 ? p.B : 0;
+  }
   for (int i = blockIdx.x * kThreads + t; i < p.gru_tiles; i += gridDim.x * kThreads) p.gru_ticket[i] = 0u;
   for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
-    if (t == 0) p.joblist[b] = Job{b, 0, -1, 0, 0, 0.f, {0, 0}};
+    if (t == 0) {
+      p.joblist[b] = Job{b, 0, -1, 0, 0, 0.f, {0, 0}};
+      p.grouplist[b] = JobGroup{b, 1, b, 0};
+    }
     const ReqView R = req_view(p.rstate + static_cast<size_t>(b) * RL.bytes, RL);
     Job* jobs = reinterpret_cast<Job*>(p.rstate + static_cast<size_t>(b) * RL.bytes + RL.jobs);
     if (t == 0) {
@@ -888,6 +1105,13 @@ __device__ void run_waves(const Params& p, const TmaMaps& maps, unsigned char* s
                           unsigned long long base_count, uint64_t* bar, int* s_flag) {
   unsigned bar_uses = 0;
   const unsigned G = gridDim.x;
+  const uint64_t t_launch = global_timer_ns();
+  uint64_t gather_ns = 0, gather_bytes = 0;  // this CTA's time in the children phases; the rows read (CTA 0)
+  unsigned waves = 0, expansions = 0;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {  // the launch's statistics start from zero, raised after the barrier
+    p.hdr->stat_launch_ns = p.hdr->stat_gather_ns = p.hdr->stat_gather_bytes = 0ull;
+    p.hdr->stat_waves = p.hdr->stat_expansions = 0u;
+  }
   init_requests(p, smem);
   if (!grid_barrier(p.hdr, G, p.timeout_ns, s_flag)) return;
   unsigned long long target = base_count;
@@ -913,7 +1137,14 @@ __device__ void run_waves(const Params& p, const TmaMaps& maps, unsigned char* s
       if (kGemm == 4 && blockIdx.x == 0)
         for (int i = threadIdx.x; i < p.gru_tiles; i += kThreads) p.gru_ticket[i] = 0u;
     }
-    if (!children_phase(p, jl, rows, smem, bar, bar_uses)) return;
+    const uint64_t c0 = global_timer_ns();
+    if (!(p.group_mma ? children_groups(p, w, jl, smem, bar, bar_uses) : children_phase(p, jl, rows, smem, bar, bar_uses)))
+      return;
+    __syncthreads();
+    gather_ns += global_timer_ns() - c0;
+    ++waves;
+    expansions += static_cast<unsigned>(rows);
+    gather_bytes += static_cast<uint64_t>(p.group_mma ? __ldcg(p.groupcount + w) : rows) * p.M * p.H * (p.bf16 ? 2 : 4);
     if (p.B < static_cast<int>(G)) {  // children computed by other CTAs: wait for all of them
       target += G;
       if (!counter_barrier(p.hdr, target, p.timeout_ns, s_flag)) return;
@@ -923,6 +1154,15 @@ __device__ void run_waves(const Params& p, const TmaMaps& maps, unsigned char* s
     if (!control_phase(p, w, smem, bar, bar_uses)) return;
     target += G;
     if (!counter_barrier(p.hdr, target, p.timeout_ns, s_flag)) return;
+  }
+  if (threadIdx.x == 0) {
+    atomicMax(&p.hdr->stat_gather_ns, static_cast<unsigned long long>(gather_ns));
+    if (blockIdx.x == 0) {
+      p.hdr->stat_gather_bytes = gather_bytes;
+      p.hdr->stat_waves = waves;
+      p.hdr->stat_expansions = expansions;
+      p.hdr->stat_launch_ns = global_timer_ns() - t_launch;
+    }
   }
 }
 
@@ -1073,6 +1313,8 @@ dt_status build_trees(int B, int K, int V, int M, int n, int max_depth, float T,
   p.rstate = reinterpret_cast<unsigned char*>(ws + L.rstate);
   p.joblist = reinterpret_cast<Job*>(ws + L.joblist);
   p.jobcount = reinterpret_cast<int*>(ws + L.jobcount);
+  p.grouplist = reinterpret_cast<JobGroup*>(ws + L.grouplist);
+  p.groupcount = reinterpret_cast<int*>(ws + L.groupcount);
   p.xact = reinterpret_cast<unsigned short*>(ws + L.xact);
   p.gru_part = reinterpret_cast<float*>(ws + L.gru_part);
   p.gru_ticket = reinterpret_cast<unsigned*>(ws + L.gru_ticket);
@@ -1117,8 +1359,12 @@ dt_status build_trees(int B, int K, int V, int M, int n, int max_depth, float T,
     return DT_ERR_CUDA;
   // static shared memory of the kernel (flags, barriers, reductions) is under 2 KB; one CTA per SM (launch bounds), so
   // the shared memory alone decides whether a CTA fits
-  const size_t smem = smem_bytes(gemm, M, n, H, p.lookahead, p.bf16 ? 2 : 4, static_cast<size_t>(di.optin) - 2048,
-                                 &p.rows_smem);
+  size_t smem = smem_bytes(gemm, M, n, H, p.lookahead, p.bf16 ? 2 : 4, static_cast<size_t>(di.optin) - 2048,
+                           &p.rows_smem);
+  // the children phase by groups on the tensor cores when its buffers fit the same budget
+  p.group_mma = p.bf16 && H % 16 == 0 && M <= 128 &&
+                group_smem(M, H).bytes + 2048 <= static_cast<size_t>(di.optin);
+  if (p.group_mma && group_smem(M, H).bytes > smem) smem = group_smem(M, H).bytes;
   if (smem + 2048 > static_cast<size_t>(di.optin)) return DT_ERR_UNSUPPORTED;
   if (mode == BuildMode::kCheck) return DT_OK;
   if (ensure_dynamic_smem(fn, smem) != cudaSuccess) return DT_ERR_CUDA;

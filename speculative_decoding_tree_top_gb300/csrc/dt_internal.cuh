@@ -16,7 +16,14 @@ struct WsHeader {
   unsigned bar_count;  // grid barrier: CTAs arrived at the current barrier
   unsigned bar_gen;    // grid barrier: generation, bumped by the last CTA to arrive
   unsigned long long sync_count;  // step barrier: arrivals ever made (monotonic, never reset)
-  unsigned reserved[58];
+  // statistics of the last dt_build_trees launch (dt_build_stats): cleared by CTA 0 before the launch's first grid
+  // barrier, raised after it
+  unsigned long long stat_launch_ns;    // CTA 0: its start to its end
+  unsigned long long stat_gather_ns;    // the longest time one CTA spent gathering correction rows
+  unsigned long long stat_gather_bytes; // correction-row bytes the launch gathered (rows x H x element size)
+  unsigned stat_waves;                  // waves run
+  unsigned stat_expansions;             // expansions computed (the roots included)
+  unsigned reserved[50];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 

@@ -64,6 +64,7 @@ SIGNATURES = {
     "dt_tree_attention_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "dt_tree_attention": (_I, [_I, _I, _I, _I, _I, _I, _P, _P, _P, _I, _P, ctypes.c_float, _P, _P, _SZ, _P]),
     "dt_get_error": (_I, [_P, _P]),
+    "dt_build_stats_read": (_I, [_P, _P, _P]),
     "dt_set_barrier_timeout_ns": (None, [ctypes.c_uint64]),
     "dt_set_lookahead": (_I, [_I]),
     "dt_status_string": (ctypes.c_char_p, [_I]),
@@ -141,6 +142,19 @@ def new_workspace(nbytes: int, device="cuda") -> torch.Tensor:
 
 def dt_get_error(workspace: torch.Tensor, stream=None) -> Status:
     return Status(lib().dt_get_error(_dev(workspace, "workspace", torch.uint8), _stream(stream)))
+
+
+class _BuildStats(ctypes.Structure):
+    _fields_ = [("launch_ns", ctypes.c_uint64), ("gather_ns", ctypes.c_uint64), ("gather_bytes", ctypes.c_uint64),
+                ("waves", ctypes.c_int32), ("expansions", ctypes.c_int32)]
+
+
+def dt_build_stats_read(workspace: torch.Tensor, stream=None) -> dict:
+    """What the last dt_build_trees / dt_round launch on this workspace did (synchronises the stream)."""
+    st = _BuildStats()
+    _check(lib().dt_build_stats_read(_dev(workspace, "workspace", torch.uint8), ctypes.byref(st), _stream(stream)),
+           "dt_build_stats_read")
+    return {f: getattr(st, f) for f, _ in _BuildStats._fields_}
 
 
 def dt_set_barrier_timeout_ns(ns: int):

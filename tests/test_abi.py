@@ -159,6 +159,14 @@ def test_binding_refuses_host_tensors(dtlib):
                       out_vals=torch.zeros(1, 2, 4), workspace=torch.zeros(4096, dtype=torch.uint8))
 
 
+def test_build_stats_reject_bad_arguments(dtlib):
+    L = dtlib.lib()
+    st = dtlib._BuildStats()
+    assert L.dt_build_stats_read(None, ctypes.byref(st), None) == INVALID
+    assert L.dt_build_stats_read(A + 8, ctypes.byref(st), None) == INVALID   # misaligned
+    assert L.dt_build_stats_read(A, None, None) == INVALID
+
+
 def test_lookahead_setting_is_validated(dtlib):
     L = dtlib.lib()
     assert L.dt_set_lookahead(-1) == INVALID

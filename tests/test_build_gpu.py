@@ -233,3 +233,19 @@ def test_host_round_matches_the_device_round(dtlib, config):
         hr.check()
         for k in ref:
             assert torch.equal(ref[k], out[k]), k
+
+
+@pytest.mark.parametrize("config", [1, 2])
+def test_build_stats_describe_the_launch(dtlib, config):
+    """The statistics a builder launch records: its waves and expansions, and the correction rows it gathered."""
+    inp = synth.make_inputs(config, device="cuda")
+    s = inp.shape
+    rnd = dtlib.Round(s.B, s.K, s.V, s.M, s.n, s.max_depth, s.T, dtlib.Weights.of(inp))
+    out = rnd(inp.logits, inp.h0)
+    st = dtlib.dt_build_stats_read(rnd.workspace)
+    rnd.check()
+    depth = out["depth"].cpu().numpy()
+    assert 1 <= st["waves"] <= s.n + 16
+    assert st["expansions"] >= s.B * 1 + int((depth[:, :-1] < s.max_depth).sum())  # the roots and every needed step
+    assert st["gather_bytes"] > 0 and st["gather_bytes"] % (s.M * s.H * 2) == 0   # whole rows of H bf16
+    assert 0 < st["gather_ns"] < st["launch_ns"] < 10_000_000
