@@ -694,12 +694,17 @@ __device__ bool children_groups(const Params& p, int w, const Job* jl, unsigned 
   const int SW = H + 8;  // padded row stride of the gathered rows (elements)
   const int M4 = round4(M);
   const unsigned rb = static_cast<unsigned>(H * 2);
-  const int ngroups = __ldcg(p.groupcount + w);
   const JobGroup* gl = p.grouplist + static_cast<size_t>(w & 1) * p.B * p.lookahead;
   const bool own = p.B >= static_cast<int>(gridDim.x);
+  // the wave's group count and (spread mode) this CTA's first group, read together: the list's slot exists even when
+  // the group does not (then it holds an older wave's entry, unused)
+  JobGroup first_group{};
+  if (!own && static_cast<int>(blockIdx.x) < p.B * p.lookahead) first_group = gl[blockIdx.x];
+  const int ngroups = __ldcg(p.groupcount + w);
   int* s_mine = reinterpret_cast<int*>(smem + GS.mine);
   for (int g0 = own ? 0 : blockIdx.x; g0 < ngroups; g0 += own ? kThreads : gridDim.x) {
     int nmine = 1;
+    if (!own && g0 != static_cast<int>(blockIdx.x)) first_group = gl[g0];  // later rounds of the spread mode
     if (own) {  // the groups of this CTA's requests in this batch, found by every thread at once
       __syncthreads();
       if (t == 0) s_mine[kThreads] = 0;
@@ -710,7 +715,7 @@ __device__ bool children_groups(const Params& p, int w, const Job* jl, unsigned 
       nmine = s_mine[kThreads];
     }
     for (int k = 0; k < nmine; ++k) {
-      const JobGroup gr = gl[own ? s_mine[k] : g0];
+      const JobGroup gr = own ? gl[s_mine[k]] : first_group;
       const int J = gr.count;
       const size_t pos = (static_cast<size_t>(gr.b) * p.K + gr.depth) * M;
       __syncthreads();  // the previous group is done with the shared buffers
