@@ -130,23 +130,6 @@ struct Cursor {
   Node hd;
   bool has;
 };
-__device__ __forceinline__ bool lane_entry(const ReqView& R, const LaneSrc& q, const Node* mg, int KM, int i, Node& h) {
-  if (q.src == -1 || i >= q.cnt) return false;
-  if (q.src == -2) {
-    h = mg[i];
-  } else {
-    h = R.kids[static_cast<size_t>(q.src) * KM + i];
-    h.seq += q.base;
-  }
-  return true;
-}
-__device__ __forceinline__ void cursor_load(const ReqView& R, const LaneSrc& q, const Node* mg, int KM, Cursor& c) {
-  c.has = lane_entry(R, q, mg, KM, q.idx, c.hd);
-}
-__device__ __forceinline__ void cursor_advance(const ReqView& R, LaneSrc& q, const Node* mg, int KM, Cursor& c) {
-  ++q.idx;
-  c.has = lane_entry(R, q, mg, KM, q.idx, c.hd);
-}
 
 // Pop records hold the parent's expansion slot while a request is being built; once every pop is known this turns
 // them into pop indices (-1 for children of the root). Called by the threads of one block, followed by a barrier.
@@ -175,16 +158,32 @@ __device__ inline void request_step(const ReqView& R, int b, int n, int M, int m
   LaneSrc ls = R.lanes[lane];
   if (ls.src >= 0 && ls.cnt < 0) ls.cnt = R.kcount[ls.src];  // the root's list, attached at launch, filled in wave 0
   Node* mg = R.merged + static_cast<size_t>(st.fb) * n;
-  Cursor cu;
-  cursor_load(R, ls, mg, KM, cu);
-  // the depth of a lane's head: its list's, or (merged list) one more than its parent's; found by every lane at once,
-  // so that only the winner's (with its expansion slot) travels in the pick's one shuffle
-  auto head_depth = [&](const Cursor& c, const LaneSrc& q) {
-    return c.has ? (q.dep >= 0 ? q.dep : R.sdepth[c.hd.pslot] + 1) : 0;
+  // Every lane keeps its source's head entry and that entry's depth (its list's, or for the merged list one more
+  // than its parent's) in registers. A lane whose source moved (`go`) reloads them with predicated loads: there is no
+  // divergent branch in the walk's common steps, which run as one chain of warp-wide operations.
+  auto reload = [&](const LaneSrc& q, Cursor& c, int& dep, bool go) {
+    const bool has = q.src != -1 && q.idx < q.cnt;
+    const Node* base = q.src >= 0 ? R.kids + static_cast<size_t>(q.src) * KM : mg;
+    Node h = c.hd;
+    if (go && has) h = base[q.idx];
+    if (go && has && q.src >= 0) h.seq += q.base;
+    int d = dep;
+    if (go && has) d = q.dep >= 0 ? q.dep : R.sdepth[h.pslot] + 1;
+    if (go) {
+      c.hd = h;
+      c.has = has;
+      dep = d;
+    }
   };
+  auto live = [](const LaneSrc& q) { return q.src != -1 && q.idx < q.cnt; };
+  Cursor cu;
+  cu.hd = Node{0.f, 0, 0, 0, -1};
+  cu.has = false;
+  int hdep = 0;
+  reload(ls, cu, hdep, true);
   while (st.s < n) {
     uint32_t won;
-    const int wl = warp_pick(cu.has, cu.hd, pick_word(cu.hd.xslot, head_depth(cu, ls)), won);
+    const int wl = warp_pick(cu.has, cu.hd, pick_word(cu.hd.xslot, cu.has ? hdep : 0), won);
     if (wl < 0) {  // unreachable when n <= the size of the depth-limited tree (checked on the host)
       if (lane == 0) record_error(hdr, DT_ERR_INVALID_ARG);
       break;
@@ -192,16 +191,16 @@ __device__ inline void request_step(const ReqView& R, int b, int n, int M, int m
     const int depth = word_depth(won), xs = word_xslot(won);
     const bool need = (st.s + 1 < n) && (depth < maxd);
     if (need && xs < 0) break;  // its children are not known yet: the next wave expands it
-    if (lane == wl) {  // the winning lane records the pop and moves on in its list
-      R.pops[st.s] = PopRec{cu.hd.token, cu.hd.pslot, depth, cu.hd.score};
-      if (need) R.popidx[xs] = st.s;
-      cursor_advance(R, ls, mg, KM, cu);
-    }
+    const bool me = lane == wl;  // the winning lane records the pop and moves on in its list
+    if (me) R.pops[st.s] = PopRec{cu.hd.token, cu.hd.pslot, depth, cu.hd.score};
+    if (me && need) R.popidx[xs] = st.s;
+    ls.idx += me ? 1 : 0;
+    bool go = me;
     if (need) {
       const int x = xs;
       const int kc = R.kcount[x];
       if (kc > 0) {
-        unsigned idle = __ballot_sync(0xFFFFFFFFu, lane > 0 && !cu.has);
+        unsigned idle = __ballot_sync(0xFFFFFFFFu, lane > 0 && !live(ls));
         if (idle == 0u) {
           // Every lane walks a live list: fold the shortest into the merged list, keeping what can still be popped.
           const unsigned rem = lane > 0 ? static_cast<unsigned>(ls.cnt - ls.idx) : 0xFFFFFFFFu;
@@ -246,17 +245,16 @@ __device__ inline void request_step(const ReqView& R, int b, int n, int M, int m
           mg = out;
           if (lane == 0) ls = LaneSrc{-2, 0, min(na + nb, limit), 0, -1, {0, 0, 0}};
           if (lane == L) ls.src = -1;
-          if (lane == 0 || lane == L) cursor_load(R, ls, mg, KM, cu);
-          idle = __ballot_sync(0xFFFFFFFFu, lane > 0 && !cu.has);
+          go = go || lane == 0 || lane == L;
+          idle = __ballot_sync(0xFFFFFFFFu, lane > 0 && !live(ls));
         }
         const int nl = __ffs(idle) - 1;
-        if (lane == nl) {
-          ls = LaneSrc{x, 0, kc, st.seq_next, depth + 1, {0, 0, 0}};
-          cursor_load(R, ls, mg, KM, cu);
-        }
+        if (lane == nl) ls = LaneSrc{x, 0, kc, st.seq_next, depth + 1, {0, 0, 0}};
+        go = go || lane == nl;
       }
       st.seq_next += M;
     }
+    reload(ls, cu, hdep, go);
     ++st.s;
   }
   R.lanes[lane] = ls;
@@ -265,10 +263,11 @@ __device__ inline void request_step(const ReqView& R, int b, int n, int M, int m
   if (st.s < n) {
     LaneSrc ss = ls;
     Cursor sc = cu;
+    int sdep = hdep;
     int sseq = st.seq_next;
     for (int sim = st.s; sim < n - 1 && njobs < kla; ++sim) {
       uint32_t won;
-      const int wl = warp_pick(sc.has, sc.hd, pick_word(sc.hd.xslot, head_depth(sc, ss)), won);
+      const int wl = warp_pick(sc.has, sc.hd, pick_word(sc.hd.xslot, sc.has ? sdep : 0), won);
       if (wl < 0) break;
       const int depth = word_depth(won), xs = word_xslot(won);
       const bool pick = depth < maxd && xs < 0;
@@ -276,20 +275,20 @@ __device__ inline void request_step(const ReqView& R, int b, int n, int M, int m
         const bool allowed = njobs == 0 || st.next_slot + 1 + (n - 1 - st.s) <= X;
         if (!allowed || st.next_slot >= X) break;
       }
-      if (lane == wl) {  // the winning lane takes the pick (if any) and moves on in its list
-        if (pick) {
-          const int x = st.next_slot;
-          Node* at = ss.src == -2 ? mg + ss.idx : R.kids + static_cast<size_t>(ss.src) * KM + ss.idx;
-          at->xslot = static_cast<short>(x);  // marked as expanded in the list it lives in
-          R.sdepth[x] = depth;
-          R.popidx[x] = -2;
-          R.kcount[x] = 0;
-          const Job jb{b, x, sc.hd.pslot, sc.hd.token, depth, sc.hd.score, {0, 0}};
-          jobs_out[njobs] = jb;
-          on_pick(njobs, jb);
-        }
-        cursor_advance(R, ss, mg, KM, sc);
+      const bool me = lane == wl;
+      if (me && pick) {  // the winning lane takes the pick
+        const int x = st.next_slot;
+        Node* at = ss.src == -2 ? mg + ss.idx : R.kids + static_cast<size_t>(ss.src) * KM + ss.idx;
+        at->xslot = static_cast<short>(x);  // marked as expanded in the list it lives in
+        R.sdepth[x] = depth;
+        R.popidx[x] = -2;
+        R.kcount[x] = 0;
+        const Job jb{b, x, sc.hd.pslot, sc.hd.token, depth, sc.hd.score, {0, 0}};
+        jobs_out[njobs] = jb;
+        on_pick(njobs, jb);
       }
+      ss.idx += me ? 1 : 0;  // and moves on in its list
+      bool go = me;
       if (pick) {
         ++st.next_slot;
         ++njobs;
@@ -297,16 +296,15 @@ __device__ inline void request_step(const ReqView& R, int b, int n, int M, int m
       if (depth < maxd && xs >= 0) {  // expanded but not popped: its children join the walk
         const int kc = R.kcount[xs];
         if (kc > 0) {
-          const unsigned idle = __ballot_sync(0xFFFFFFFFu, lane > 0 && !sc.has);
+          const unsigned idle = __ballot_sync(0xFFFFFFFFu, lane > 0 && !live(ss));
           if (idle == 0u) break;
           const int nl = __ffs(idle) - 1;
-          if (lane == nl) {
-            ss = LaneSrc{xs, 0, kc, sseq, depth + 1, {0, 0, 0}};
-            cursor_load(R, ss, mg, KM, sc);
-          }
+          if (lane == nl) ss = LaneSrc{xs, 0, kc, sseq, depth + 1, {0, 0, 0}};
+          go = go || lane == nl;
         }
         sseq += M;
       }
+      reload(ss, sc, sdep, go);
     }
   }
   if (st.s < n && njobs == 0 && lane == 0) record_error(hdr, DT_ERR_INVALID_ARG);  // no slot left (unreachable)
