@@ -305,6 +305,14 @@ void dt_set_barrier_timeout_ns(uint64_t ns);
 #define DT_MAX_LOOKAHEAD 8
 dt_status dt_set_lookahead(int k);
 
+/* Which kernel dt_topm (and dt_topm_static, dt_round) runs for small grids, process-wide. With 1 (the default), when
+ * every row is a whole number of 16-byte groups, M <= 256, and the rows fit one wave of clusters of up to 8 CTAs on
+ * the device (a few rows: one request's block positions), each row is one thread-block cluster that bounds, filters
+ * and ranks its candidates in distributed shared memory; with 0, every launch takes the per-chunk candidate lists and
+ * the row selection. Both give bit-identical results; only the time changes. Returns DT_ERR_INVALID_ARG unless
+ * enable is 0 or 1. A tuning and test hook with no counterpart in the paper. */
+dt_status dt_set_topm_cluster(int enable);
+
 const char* dt_status_string(dt_status s);
 int dt_abi_version(void);
 

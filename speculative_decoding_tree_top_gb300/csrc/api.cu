@@ -11,9 +11,11 @@ namespace dt {
 namespace {
 std::atomic<uint64_t> g_barrier_timeout_ns{2000000000ull};
 std::atomic<int> g_lookahead{0};
+std::atomic<int> g_topm_cluster{1};
 }
 uint64_t barrier_timeout_ns() { return g_barrier_timeout_ns.load(std::memory_order_relaxed); }
 int lookahead_setting() { return g_lookahead.load(std::memory_order_relaxed); }
+bool topm_cluster_setting() { return g_topm_cluster.load(std::memory_order_relaxed) != 0; }
 
 namespace {
 std::mutex g_cache_mu;
@@ -38,9 +40,10 @@ cudaError_t current_device_info(DeviceInfo* out) {
         return cudaSuccess;
       }
   }
-  DeviceInfo d{dev, 0, 0, 0};
+  DeviceInfo d{dev, 0, 0, 0, 0};
   e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.coop, cudaDevAttrCooperativeLaunch, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.cluster, cudaDevAttrClusterLaunch, dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(g_cache_mu);
@@ -87,6 +90,12 @@ extern "C" void dt_set_barrier_timeout_ns(uint64_t ns) {
 extern "C" dt_status dt_set_lookahead(int k) {
   if (k < 0 || k > DT_MAX_LOOKAHEAD) return DT_ERR_INVALID_ARG;
   dt::g_lookahead.store(k, std::memory_order_relaxed);
+  return DT_OK;
+}
+
+extern "C" dt_status dt_set_topm_cluster(int enable) {
+  if (enable != 0 && enable != 1) return DT_ERR_INVALID_ARG;
+  dt::g_topm_cluster.store(enable, std::memory_order_relaxed);
   return DT_OK;
 }
 

@@ -188,6 +188,40 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
                : "memory");
 }
 
+// ---- thread-block clusters: distributed shared memory and the cluster barrier ------------------------------------
+__device__ __forceinline__ unsigned cluster_rank() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// The address, in the cluster's shared window, of the variable at `p` (this CTA's shared memory) in CTA `rank`.
+__device__ __forceinline__ uint32_t dsmem_addr(const void* p, unsigned rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ uint32_t ld_dsmem_u32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint64_t ld_dsmem_u64(uint32_t a) {
+  uint64_t v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_dsmem_u32(uint32_t a, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_dsmem_u64(uint32_t a, uint64_t v) {
+  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
+}
+// Every thread of every CTA of the cluster arrives (release), then waits for all (acquire): shared-memory writes
+// made before it, in any CTA of the cluster, are visible after it. Called by all threads, convergently.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ---- order-preserving unsigned keys of logits -------------------------------------------------------------------
 // Larger key <=> larger value. -0.0 is folded onto +0.0 so that both compare equal (the id then decides). Every
 // non-padding element gets a key >= 1, so key 0 marks "no element".
@@ -320,10 +354,11 @@ inline TopmLayout topm_layout(int B, int K, int V, int M) {
 // Host-side process-wide settings (dt_set_barrier_timeout_ns, dt_set_lookahead).
 uint64_t barrier_timeout_ns();
 int lookahead_setting();  // 0 = automatic
+bool topm_cluster_setting();  // dt_set_topm_cluster
 
 // Attributes of the current device, queried once per device and cached (a launch then costs one runtime call).
 struct DeviceInfo {
-  int dev, sms, coop, optin;
+  int dev, sms, coop, optin, cluster;
 };
 cudaError_t current_device_info(DeviceInfo* out);
 // Raises the dynamic shared-memory limit of kernel `fn` on the current device to at least `bytes`; the runtime is

@@ -4,7 +4,9 @@
 // the M highest-marginal tokens of each depth); gist.science, "Composants Clés — Restriction de Candidats".
 //
 // GB300 design. The op is a pure HBM stream (every logit is read once, nothing is reused), so it is laid out for
-// bandwidth and for few instructions per logit, not for tensor cores. Two launches:
+// bandwidth and for few instructions per logit, not for tensor cores. A few rows (one request's block positions)
+// are latency-bound instead: each row is then one thread-block cluster that keeps everything in distributed shared
+// memory (topm_cluster_kernel, below). Otherwise two launches:
 //   * filter: grid = (B*K rows) x (chunks of 32768 bf16 / 16384 fp32 logits), 256 threads. Each thread stages its
 //     sixteen 16-byte groups into shared memory with cp.async, committed as four parts, so all of a chunk's bytes
 //     are in flight at once and no registers are held while they are. A row's first chunk computes the M-th
@@ -95,6 +97,159 @@ __global__ void __launch_bounds__(kSelThreads, 7) topm_select_kernel(const void*
                                            *reinterpret_cast<SelectSmem*>(smem_u4), s_warp, &s_n);
 }
 
+// ---- one cluster per row: small grids ---------------------------------------------------------------------------
+// For few rows (a single request's block positions) the chunk-list path is a chain of global round trips: the
+// published bound, the candidate lists, the ticket, the last CTA's selection over words read back from L2. Here a
+// row is one thread-block cluster of C CTAs (C <= 8), CTA c holding the slice [c * slice, (c + 1) * slice) of the
+// row in shared memory, and the CTAs write into each other's shared memory (two cluster barriers in all):
+//   1. each CTA bulk-copies its slice in (TMA, one mbarrier) and pads the rest of its chunk buffer with -inf;
+//   2. each warp sorts its lanes' maxima (bitonic, in registers) and keeps its P largest; after a cluster barrier
+//      every CTA reads the row's C * 8 * P >= M keys (at most 256, one per thread) and finds the same bound, the
+//      M-th largest of those keys to 16 key bits (bisection, one block-wide count per bit). M
+//      distinct logits lie at or above it, so it is at most the row's M-th largest; and unless one warp holds more
+//      than P of the row's largest lane maxima it is the M-th largest lane maximum itself, which few other logits
+//      reach;
+//   3. each CTA keeps its logits at or above the bound (chunk_keep: its exact top M if it would keep too many) and
+//      writes them, as row words, to its region of every CTA's candidate buffer;
+//   4. each CTA ranks its own candidates among the row's by counting: the row's M largest are all candidates, so a
+//      candidate's rank among them is its rank in the row when below M, and it is written straight to out[rank].
+// No workspace and no global atomics; the row's CTAs compute the bound redundantly rather than wait for one another.
+constexpr uint64_t kTopmCopyBudgetNs = 4000000000ull;  // the slice copy takes a microsecond: this stops a lost one
+constexpr int kMaxClusterCtas = 8;
+
+// Dynamic shared memory of the cluster kernel: the slice, then the row's candidates.
+inline size_t cluster_smem_bytes(int C, int cap) { return kChunkSmem + sizeof(uint64_t) * static_cast<size_t>(C) * cap; }
+
+// The M-th largest of the keys held one per thread (0: none), to the top 16 key bits, in every thread: the largest
+// v with at least M keys whose top 16 bits are >= v, shifted back (exact for 16-bit keys, a lower bound otherwise).
+// Bisection over v, one block-wide count per bit. Called by all threads, convergently.
+template <int kKeyBits>
+__device__ __forceinline__ uint32_t block_kth_bound16(uint32_t key, int M) {
+  constexpr int kShift = kKeyBits - 16;
+  const uint32_t k16 = key >> kShift;
+  uint32_t v = 0;
+#pragma unroll
+  for (int bit = 15; bit >= 0; --bit) {
+    const uint32_t cand = v | (1u << bit);
+    if (__syncthreads_count(k16 >= cand) >= M) v = cand;
+  }
+  return v << kShift;
+}
+
+// Descending bitonic sort of one key per lane: lane i ends with the i-th largest of the warp's keys.
+__device__ __forceinline__ uint32_t warp_sort_desc(uint32_t v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const uint32_t o = __shfl_xor_sync(0xFFFFFFFFu, v, j);
+      const bool desc = (lane & k) == 0, lower = (lane & j) == 0;
+      v = (desc == lower) ? max(v, o) : min(v, o);
+    }
+  }
+  return v;
+}
+
+template <bool kBf16>
+__global__ void __launch_bounds__(kFThreads, 2)
+    topm_cluster_kernel(const void* __restrict__ logits, int V, int M, int slice, int cap,
+                        int32_t* __restrict__ out_ids, float* __restrict__ out_vals, WsHeader* hdr) {
+  using T = Topm<kBf16, kFThreads, kFGroups>;
+  constexpr int kWarps = kFThreads / 32;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int C = static_cast<int>(gridDim.x);  // the cluster spans the grid's x dimension: one row
+  const int c = static_cast<int>(cluster_rank());
+  const int row = blockIdx.y;
+  extern __shared__ uint4 chunk_s[];                                            // the slice
+  uint64_t* rw = reinterpret_cast<uint64_t*>(chunk_s + kFThreads * kFGroups);  // [C][cap] the row's candidates
+  __shared__ FilterShared<kBf16, kFThreads> F;
+  __shared__ uint32_t s_keys[kFThreads];  // [warps][P] this CTA's warps' largest lane maxima
+  __shared__ __align__(8) uint64_t s_bar;
+  __shared__ int s_cnt[kMaxClusterCtas];  // candidates of each CTA of the row
+  const int c0 = c * slice;
+  const int len = min(slice, V - c0);  // > 0 and whole 16-byte groups (host-checked)
+  const int ngroups = len / T::kPer16;
+  if (t == 0) {  // the copies go out first; the barrier below orders the barrier's initialisation before any wait
+    mbar_init(&s_bar, 1);
+    mbar_fence_init();
+    F.s_n = 0;
+    const char* src =
+        static_cast<const char*>(logits) + (static_cast<long long>(row) * V + c0) * static_cast<long long>(kBf16 ? 2 : 4);
+    const unsigned bytes = static_cast<unsigned>(ngroups) * 16u;
+    mbar_expect_tx(&s_bar, bytes);
+    constexpr unsigned kPiece = 8192;
+    for (unsigned o = 0; o < bytes; o += kPiece)
+      bulk_g2s(reinterpret_cast<char*>(chunk_s) + o, src + o, min(kPiece, bytes - o), &s_bar);
+  }
+  constexpr uint32_t kPad = kBf16 ? 0xFF80FF80u : 0xFF800000u;  // -inf: raises no maximum, dropped by index
+  for (int g = ngroups + t; g < kFThreads * kFGroups; g += kFThreads) chunk_s[g] = make_uint4(kPad, kPad, kPad, kPad);
+  __syncthreads();  // the barrier is initialised; the padding is in place
+  const bool ok = __syncthreads_and(mbar_wait(&s_bar, 0, kTopmCopyBudgetNs));
+  if (!ok && t == 0) record_error(hdr, DT_ERR_TIMEOUT);
+  T x{chunk_s};
+  bool nan = false;
+  if (!kBf16) nan = x.any_nan_f32();
+  const uint32_t mk = x.max_key(nan);
+  // keys per warp: at least 4, and enough that the row's warps send M or more (C * kWarps * P <= kFThreads)
+  const int P = min(32, max(4, (M + C * kWarps - 1) / (C * kWarps)));
+  const uint32_t sk = warp_sort_desc(mk);
+  if (lane < P) s_keys[warp * P + lane] = sk;
+  cluster_sync();  // 1: every CTA of the row runs and its keys are in place
+  uint32_t key = 0;  // thread t reads key t of the row's C * kWarps * P
+  if (t < C * kWarps * P)
+    key = ld_dsmem_u32(dsmem_addr(&s_keys[t % (kWarps * P)], static_cast<unsigned>(t / (kWarps * P))));
+  const uint32_t theta = block_kth_bound16<T::kKeyBits>(key, M);
+  if (t == 0) F.s_theta = theta;
+  __syncthreads();
+  const int n = chunk_keep(x, M, len, cap, false, 0u, nan, hdr, F);
+  for (int i = t; i < n; i += kFThreads) {
+    const uint64_t w = T::global_word(F.cand[i], c0);
+    for (int q = 0; q < C; ++q) st_dsmem_u64(dsmem_addr(&rw[static_cast<size_t>(c) * cap + i], static_cast<unsigned>(q)), w);
+  }
+  if (t < C) st_dsmem_u32(dsmem_addr(&s_cnt[c], static_cast<unsigned>(t)), static_cast<uint32_t>(n));
+  cluster_sync();  // 2: the row's candidates are in every CTA; no CTA touches another's memory after this
+  int total = 0;
+  for (int q = 0; q < C; ++q) total += s_cnt[q];
+  // Ranks: a warp takes four of this CTA's candidates at a time, its lanes splitting the row's words.
+  const long long row_out = static_cast<long long>(row) * M;
+  const uint64_t* mine = rw + static_cast<size_t>(c) * cap;
+  for (int i0 = 4 * warp; i0 < n; i0 += 4 * kWarps) {
+    uint64_t w[4];
+    int r[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      w[k] = i0 + k < n ? mine[i0 + k] : ~0ull;
+      r[k] = 0;
+    }
+    for (int q = 0; q < C; ++q) {
+      const uint64_t* src = rw + static_cast<size_t>(q) * cap;
+      const int nq = s_cnt[q];
+      for (int j = lane; j < nq; j += 32) {
+        const uint64_t v = src[j];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) r[k] += v > w[k];
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) r[k] = __reduce_add_sync(0xFFFFFFFFu, r[k]);
+    if (lane < 4 && i0 + lane < n) {
+      const int rank = lane == 0 ? r[0] : lane == 1 ? r[1] : lane == 2 ? r[2] : r[3];
+      const uint64_t wd = lane == 0 ? w[0] : lane == 1 ? w[1] : lane == 2 ? w[2] : w[3];
+      if (rank < M) {
+        out_ids[row_out + rank] = static_cast<int32_t>(candidate_id(wd));
+        out_vals[row_out + rank] = kBf16 ? value_of_key_bf16(candidate_key(wd)) : value_of_key_f32(candidate_key(wd));
+      }
+    }
+  }
+  if (c == 0)  // fewer candidates than M only for rows of NaNs: the missing slots as the chunk-list path fills them
+    for (int m = total + t; m < M; m += kFThreads) {
+      out_ids[row_out + m] = 0;
+      out_vals[row_out + m] = -INFINITY;
+    }
+  if (!ok) mbar_wait(&s_bar, 0, kTopmCopyBudgetNs);  // a late copy must not land after the CTA has left
+}
+
 dt_status launch_topm(const void* logits, dt_dtype dtype, int B, int K, int V, int M, int32_t* out_ids,
                       float* out_vals, char* ws, const TopmLayout& L, cudaStream_t stream) {
   const long long rows = static_cast<long long>(B) * K;
@@ -114,6 +269,34 @@ dt_status launch_topm(const void* logits, dt_dtype dtype, int B, int K, int V, i
     constexpr int kChunk = Topm<kB, kFThreads, kFGroups>::kChunk;
     const int chunks = (V + kChunk - 1) / kChunk;  // <= L.chunks: the layout is sized for the smaller fp32 chunk
     const dim3 grid(static_cast<unsigned>(rows), static_cast<unsigned>(chunks));
+    // one cluster per row: whole 16-byte groups in every row, M <= 256 (the candidate buffers stay small), a slice
+    // of at least 8192 bf16 / 4096 fp32 logits per CTA, the row in at most 8 slices, all in one wave
+    if (topm_cluster_setting() && vec_ok && M <= kFThreads && di.cluster) {
+      constexpr int kPer16 = kB ? 8 : 4;
+      constexpr int kMinSlice = kFThreads * kPer16 * 4;
+      int C = 1;
+      while (C < kMaxClusterCtas && static_cast<long long>(C) * kMinSlice < V) C *= 2;
+      const int slice = ((V + C - 1) / C + kPer16 - 1) / kPer16 * kPer16;
+      if (slice <= kChunk && static_cast<long long>(C - 1) * slice < V && rows * C <= 2LL * sms && rows <= 65535) {
+        const size_t smem = cluster_smem_bytes(C, L.cap);
+        if (ensure_dynamic_smem(reinterpret_cast<const void*>(topm_cluster_kernel<kB>), smem) != cudaSuccess)
+          return false;
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(static_cast<unsigned>(C), static_cast<unsigned>(rows));
+        cfg.blockDim = dim3(kFThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(C);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, topm_cluster_kernel<kB>, logits, V, M, slice, L.cap, out_ids, out_vals, hdr) ==
+               cudaSuccess;
+      }
+    }
     // about two waves of three CTAs per SM or fewer: fuse the selection into the launch
     const bool fuse = rows * chunks <= 6LL * sms;
     if (ensure_dynamic_smem(reinterpret_cast<const void*>(topm_filter_kernel<kB, true>), kChunkSmem) != cudaSuccess ||

@@ -40,6 +40,14 @@ struct Topm {
   uint4* s_;
   __device__ __forceinline__ uint4 g_(int k) const { return s_[threadIdx.x + kThreads * k]; }
 
+  // Bit pattern of the smallest value whose key is >= key (key 0: no bound, -inf).
+  __device__ static __forceinline__ uint32_t thr_of(uint32_t key) {
+    constexpr uint32_t kNegInf = kBf16 ? 0xFF80u : 0xFF800000u;
+    constexpr uint32_t kMinKey = kBf16 ? 0x7Fu : 0x7FFFFFu;  // key of -inf: every real logit has a key >= it
+    if (key <= kMinKey) return kNegInf;
+    return kBf16 ? ((key & 0x8000u) ? (key & 0x7FFFu) : (~key & 0xFFFFu))
+                 : ((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+  }
   __device__ static __forceinline__ CWord cword(uint32_t bits, int li) {
     const uint32_t key = kBf16 ? key_of_bf16(bits) : key_of_f32(bits);
     return (static_cast<CWord>(key) << kIdxBits) | static_cast<CWord>((kBf16 ? 0xFFFFu : 0xFFFFFFFFu) - li);
@@ -235,6 +243,31 @@ struct Topm {
   }
 };
 
+// Warp 0 (threads 0..31): the 256-bin histogram `hist`, read from the top, places the need-th largest key in bin
+// s_sel[0], with s_sel[1] keys in the bins above it. Requires at least `need` keys in the histogram.
+__device__ __forceinline__ void pick_from_top(const unsigned* hist, int need, unsigned* s_sel) {
+  const int lane = threadIdx.x & 31;
+  unsigned cb[8], sum = 0;  // lane L holds bins 255 - 8L down to 248 - 8L: counts from the top
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    cb[j] = hist[255 - 8 * lane - j];
+    sum += cb[j];
+  }
+  unsigned incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const unsigned excl = incl - sum;
+  if (excl < static_cast<unsigned>(need) && incl >= static_cast<unsigned>(need)) {
+    unsigned acc, at;
+    const int j = pick_bin(cb, excl, static_cast<unsigned>(need), acc, at);
+    s_sel[0] = static_cast<unsigned>(255 - 8 * lane - j);
+    s_sel[1] = acc;
+  }
+}
+
 // The M-th largest of the block's keys, one per thread (1 <= M <= kThreads), in every thread: radix select with
 // 8-bit digits from the top, one 256-bin shared histogram per digit over the keys that share the digits found so far.
 template <int kKeyBits, int kThreads>
@@ -256,27 +289,7 @@ __device__ __forceinline__ uint32_t block_kth_key(uint32_t key, int M, unsigned*
       if (lane == __ffs(peers) - 1) atomicAdd(&hist[digit], static_cast<unsigned>(__popc(peers)));
     }
     __syncthreads();
-    if (t < 32) {  // lane L holds bins 255 - 8L down to 248 - 8L: counts from the top
-      unsigned cb[8], sum = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        cb[j] = hist[255 - 8 * lane - j];
-        sum += cb[j];
-      }
-      unsigned incl = sum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const unsigned excl = incl - sum;
-      if (excl < static_cast<unsigned>(need) && incl >= static_cast<unsigned>(need)) {
-        unsigned acc, at;
-        const int j = pick_bin(cb, excl, static_cast<unsigned>(need), acc, at);
-        s_sel[0] = static_cast<unsigned>(255 - 8 * lane - j);
-        s_sel[1] = acc;
-      }
-    }
+    if (t < 32) pick_from_top(hist, need, s_sel);
     __syncthreads();
     prefix = (prefix << 8) | s_sel[0];
     need -= static_cast<int>(s_sel[1]);
@@ -299,73 +312,20 @@ struct FilterShared {
   int s_n;
 };
 
-// Filters chunk `chunk` of row `row` (logits [row][V]): the chunk keeps every logit at or above the M-th largest of
-// its kThreads lane maxima, or at or above the row's bound already published by another chunk (`bounds[row]`, the
-// largest such bound so far; read before the copies are issued, so the load does not queue behind them), and
-// publishes its own bound with atomicMax. More than `cap` survivors (ties, or sorted runs that put the large logits
-// in few lanes): exactly the chunk's top M instead, by bisection over the staged chunk and the lowest-index ties.
-// Writes the chunk's candidate words (chunk-local value key << bits | inverted local index) and their count to the
-// row's list `chunk` in `words` / `counts` (rows x chunks lists of `cap` words). A NaN among the logits sets
-// DT_ERR_NUMERIC. Called by all kThreads threads; `chunk_s` holds kThreads * kGroups 16-byte groups.
+// Keeps the chunk's candidates: every logit at or above the bound key F.s_theta (0: no bound), appended unsorted to
+// F.cand as chunk-local words (value key << bits | inverted local index), their count in F.s_n. `sel_known`, when
+// `have_sel` (bf16): the groups already found to hold a logit at or above the bound. More than `cap` survivors (ties,
+// or sorted runs that put the large logits in few lanes): exactly the chunk's top M instead, by bisection over the
+// staged chunk and the lowest-index ties. A NaN among the logits (`nan` in any thread) sets DT_ERR_NUMERIC. Called by
+// all kThreads threads after a barrier that follows the write of F.s_theta; returns the count in every thread.
 template <bool kBf16, int kThreads, int kGroups>
-__device__ void filter_chunk(const void* __restrict__ logits, int V, int M, int row, int chunk, int chunks, int cap,
-                             bool vec_ok, uint32_t* __restrict__ bounds, void* __restrict__ words,
-                             int* __restrict__ counts, WsHeader* hdr, uint4* chunk_s, FilterShared<kBf16, kThreads>& F) {
+__device__ int chunk_keep(const Topm<kBf16, kThreads, kGroups>& x, int M, int len, int cap, bool have_sel,
+                          unsigned sel_known, bool nan, WsHeader* hdr, FilterShared<kBf16, kThreads>& F) {
   using T = Topm<kBf16, kThreads, kGroups>;
-  using CWord = typename T::CWord;
   constexpr int kWarps = kThreads / 32;
   constexpr int kHalf = T::kGroups / 2;  // groups per 64-bit mask word
-  constexpr uint32_t kNegInf = kBf16 ? 0xFF80u : 0xFF800000u;
-  constexpr uint32_t kMinKey = kBf16 ? 0x7Fu : 0x7FFFFFu;  // key of -inf: every real logit has a key >= it
-  CWord* cand = F.cand;
+  auto* cand = F.cand;
   const int t = threadIdx.x, lane = t & 31;
-  const long long row_off = static_cast<long long>(row) * V;
-  const int c0 = chunk * T::kChunk;
-  const int len = min(T::kChunk, V - c0);
-  __syncthreads();  // the previous user of the shared state is done with it
-  if (t == 0) {
-    F.s_n = 0;
-    F.s_theta = M <= kThreads ? *reinterpret_cast<volatile uint32_t*>(bounds + row) : 0u;
-  }
-  T x{chunk_s};
-  x.stage(logits, row_off, c0, len, vec_ok);
-  // bit pattern of the smallest value whose key is >= key
-  auto thr_of = [&](uint32_t key) -> uint32_t {
-    if (key <= kMinKey) return kNegInf;
-    return kBf16 ? ((key & 0x8000u) ? (key & 0x7FFFu) : (~key & 0xFFFFu))
-                 : ((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
-  };
-  __syncthreads();
-  const bool known = F.s_theta != 0u;  // uniform: written by thread 0 before the barrier
-  bool nan = false;
-  unsigned sel_known = 0;  // with a known bound (bf16): the groups holding candidates, found part by part
-  if (kBf16 && known) {
-    // each part is scanned as soon as this thread's copies of it have landed, while the later parts are in flight
-    const uint32_t thr = thr_of(F.s_theta);
-    T::template wait_part<0>();
-    sel_known |= x.template group_mask<true, 0, T::kPartGroups>(thr, &nan);
-    T::template wait_part<1>();
-    sel_known |= x.template group_mask<true, T::kPartGroups, 2 * T::kPartGroups>(thr, &nan);
-    T::template wait_part<2>();
-    sel_known |= x.template group_mask<true, 2 * T::kPartGroups, 3 * T::kPartGroups>(thr, &nan);
-    T::template wait_part<3>();
-    sel_known |= x.template group_mask<true, 3 * T::kPartGroups, T::kGroups>(thr, &nan);
-  } else {
-    T::template wait_part<T::kParts - 1>();
-    if (!kBf16) nan = x.any_nan_f32();
-  }
-  if (!known) {  // this chunk computes (and publishes) the bound
-    const uint32_t mk = x.max_key(nan);
-    if (M <= kThreads) {
-      __syncthreads();  // every thread has read s_theta
-      const uint32_t th = block_kth_key<T::kKeyBits, kThreads>(mk, M, F.tmax, F.s_sel);
-      if (t == 0) {
-        F.s_theta = th;
-        if (th) atomicMax(bounds + row, th);
-      }
-      __syncthreads();
-    }
-  }
   // Appends the elements whose bits are set in e0 (groups 0..kHalf-1) and e1 (the rest), kPer16 bits per group. One
   // shared atomic per warp reserves the warp's slots; slots past cap are dropped (and show up as s_n > cap). The
   // chunk is in shared memory, so groups are visited by run-time index (no unrolling, few registers).
@@ -412,10 +372,10 @@ __device__ void filter_chunk(const void* __restrict__ logits, int V, int M, int 
   constexpr unsigned kAllGroups = (1u << T::kGroups) - 1u;
 
   {
-    const uint32_t thr = thr_of(F.s_theta);
+    const uint32_t thr = T::thr_of(F.s_theta);
     uint64_t e0, e1;
-    // cheap "anything here" test first; with a known bound it is the only pass and also looks for NaNs
-    const unsigned sel = known && kBf16 ? sel_known : x.group_mask(thr);
+    // cheap "anything here" test first, unless the caller's pass already found the groups
+    const unsigned sel = have_sel ? sel_known : x.group_mask(thr);
     masks(sel, thr, false, e0, e1);
     append(e0, e1);
   }
@@ -425,7 +385,7 @@ __device__ void filter_chunk(const void* __restrict__ logits, int V, int M, int 
     // Exactly the top M. kth: the largest key with at least M elements at or above it (bisection, counts from the
     // staged chunk); then all elements above kth and the lowest-index ties at kth, layer by layer in index order.
     auto count_ge = [&](uint32_t key) {
-      const uint32_t thr = thr_of(key);
+      const uint32_t thr = T::thr_of(key);
       int c = 0;
 #pragma unroll 1
       for (int k = 0; k < T::kGroups; ++k) c += __popc(x.template elem_mask<false>(k, thr, len));
@@ -441,10 +401,10 @@ __device__ void filter_chunk(const void* __restrict__ logits, int V, int M, int 
     __syncthreads();
     {
       uint64_t e0, e1;
-      masks(kAllGroups, thr_of(kth + 1u), false, e0, e1);
+      masks(kAllGroups, T::thr_of(kth + 1u), false, e0, e1);
       append(e0, e1);
     }
-    const uint32_t thr_eq = thr_of(kth);
+    const uint32_t thr_eq = T::thr_of(kth);
 #pragma unroll 1
     for (int k = 0; k < T::kGroups; ++k) {  // layer k holds indices [k * kThreads * kPer16, (k + 1) * ...)
       if (need <= 0) break;                  // uniform
@@ -460,8 +420,66 @@ __device__ void filter_chunk(const void* __restrict__ logits, int V, int M, int 
     __syncthreads();
     n = F.s_n;
   }
+  return n;
+}
+
+// Filters chunk `chunk` of row `row` (logits [row][V]): the chunk keeps every logit at or above the M-th largest of
+// its kThreads lane maxima, or at or above the row's bound already published by another chunk (`bounds[row]`, the
+// largest such bound so far; read before the copies are issued, so the load does not queue behind them), and
+// publishes its own bound with atomicMax (chunk_keep does the rest). Writes the chunk's candidate words and their
+// count to the row's list `chunk` in `words` / `counts` (rows x chunks lists of `cap` words). Called by all kThreads
+// threads; `chunk_s` holds kThreads * kGroups 16-byte groups.
+template <bool kBf16, int kThreads, int kGroups>
+__device__ void filter_chunk(const void* __restrict__ logits, int V, int M, int row, int chunk, int chunks, int cap,
+                             bool vec_ok, uint32_t* __restrict__ bounds, void* __restrict__ words,
+                             int* __restrict__ counts, WsHeader* hdr, uint4* chunk_s, FilterShared<kBf16, kThreads>& F) {
+  using T = Topm<kBf16, kThreads, kGroups>;
+  using CWord = typename T::CWord;
+  const int t = threadIdx.x;
+  const long long row_off = static_cast<long long>(row) * V;
+  const int c0 = chunk * T::kChunk;
+  const int len = min(T::kChunk, V - c0);
+  __syncthreads();  // the previous user of the shared state is done with it
+  if (t == 0) {
+    F.s_n = 0;
+    F.s_theta = M <= kThreads ? *reinterpret_cast<volatile uint32_t*>(bounds + row) : 0u;
+  }
+  T x{chunk_s};
+  x.stage(logits, row_off, c0, len, vec_ok);
+  __syncthreads();
+  const bool known = F.s_theta != 0u;  // uniform: written by thread 0 before the barrier
+  bool nan = false;
+  unsigned sel_known = 0;  // with a known bound (bf16): the groups holding candidates, found part by part
+  if (kBf16 && known) {
+    // each part is scanned as soon as this thread's copies of it have landed, while the later parts are in flight
+    const uint32_t thr = T::thr_of(F.s_theta);
+    T::template wait_part<0>();
+    sel_known |= x.template group_mask<true, 0, T::kPartGroups>(thr, &nan);
+    T::template wait_part<1>();
+    sel_known |= x.template group_mask<true, T::kPartGroups, 2 * T::kPartGroups>(thr, &nan);
+    T::template wait_part<2>();
+    sel_known |= x.template group_mask<true, 2 * T::kPartGroups, 3 * T::kPartGroups>(thr, &nan);
+    T::template wait_part<3>();
+    sel_known |= x.template group_mask<true, 3 * T::kPartGroups, T::kGroups>(thr, &nan);
+  } else {
+    T::template wait_part<T::kParts - 1>();
+    if (!kBf16) nan = x.any_nan_f32();
+  }
+  if (!known) {  // this chunk computes (and publishes) the bound
+    const uint32_t mk = x.max_key(nan);
+    if (M <= kThreads) {
+      __syncthreads();  // every thread has read s_theta
+      const uint32_t th = block_kth_key<T::kKeyBits, kThreads>(mk, M, F.tmax, F.s_sel);
+      if (t == 0) {
+        F.s_theta = th;
+        if (th) atomicMax(bounds + row, th);
+      }
+      __syncthreads();
+    }
+  }
+  const int n = chunk_keep(x, M, len, cap, kBf16 && known, sel_known, nan, hdr, F);
   CWord* out = static_cast<CWord*>(words) + (static_cast<size_t>(row) * chunks + chunk) * cap;
-  for (int i = t; i < n; i += kThreads) out[i] = cand[i];
+  for (int i = t; i < n; i += kThreads) out[i] = F.cand[i];
   if (t == 0) counts[static_cast<size_t>(row) * chunks + chunk] = n;
 }
 

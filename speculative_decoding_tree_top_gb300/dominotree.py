@@ -67,6 +67,7 @@ SIGNATURES = {
     "dt_build_stats_read": (_I, [_P, _P, _P]),
     "dt_set_barrier_timeout_ns": (None, [ctypes.c_uint64]),
     "dt_set_lookahead": (_I, [_I]),
+    "dt_set_topm_cluster": (_I, [_I]),
     "dt_status_string": (ctypes.c_char_p, [_I]),
     "dt_abi_version": (_I, []),
 }
@@ -164,6 +165,11 @@ def dt_set_barrier_timeout_ns(ns: int):
 def dt_set_lookahead(k: int):
     """Expansions per request per wave in dt_build_trees (0 = the library's choice); outputs do not depend on it."""
     _check(lib().dt_set_lookahead(int(k)), "dt_set_lookahead")
+
+
+def dt_set_topm_cluster(enable: bool):
+    """Whether small top-M launches run one thread-block cluster per row (the default); outputs do not depend on it."""
+    _check(lib().dt_set_topm_cluster(int(bool(enable))), "dt_set_topm_cluster")
 
 
 def dt_topm(logits: torch.Tensor, M: int, out_ids: Optional[torch.Tensor] = None,

@@ -175,6 +175,14 @@ def test_lookahead_setting_is_validated(dtlib):
         assert L.dt_set_lookahead(k) == OK
 
 
+def test_topm_cluster_setting_is_validated(dtlib):
+    L = dtlib.lib()
+    assert L.dt_set_topm_cluster(-1) == INVALID
+    assert L.dt_set_topm_cluster(2) == INVALID
+    for v in (0, 1):
+        assert L.dt_set_topm_cluster(v) == OK
+
+
 def test_marginal_rejects_bad_arguments(dtlib):
     L = dtlib.lib()
     f = L.dt_build_trees_marginal

@@ -8,6 +8,15 @@ from speculative_decoding_tree_top_gb300 import synth
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(autouse=True, params=["cluster", "lists"])
+def topm_kernel(dtlib, request):
+    """Every case runs twice: small launches through the one-cluster-per-row kernel, and with that kernel switched off
+    (per-chunk candidate lists and the row selection). Large launches take the lists either way."""
+    dtlib.dt_set_topm_cluster(request.param == "cluster")
+    yield request.param
+    dtlib.dt_set_topm_cluster(True)
+
+
 def _host(t):
     return synth.host_array(t)
 
@@ -33,7 +42,8 @@ def test_topm_parity_workloads(dtlib, orc, config):
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("B,K,V,M", [(2, 3, 1000, 17), (1, 2, 1001, 8), (2, 2, 8191, 64), (1, 3, 8193, 64),
                                      (1, 2, 16384, 128), (1, 2, 700, 700), (1, 1, 5000, 1024), (3, 2, 40000, 1),
-                                     (1, 2, 8, 3), (2, 2, 100003, 256)])
+                                     (1, 2, 8, 3), (2, 2, 100003, 256), (1, 4, 8200, 256), (2, 3, 16392, 100),
+                                     (1, 1, 2048, 256), (1, 16, 151936, 64)])
 def test_topm_ragged_shapes(dtlib, orc, dtype, B, K, V, M):
     g = torch.Generator(device="cuda").manual_seed(B * 7919 + V)
     x = (torch.randn((B, K, V), generator=g, device="cuda") * 3).to(dtype)
@@ -59,6 +69,29 @@ def test_topm_ties_zeros_infinities(dtlib, orc, dtype):
         ids, vals = _check(dtlib, orc, x, M)
     row0 = ids[0, 0].cpu().numpy()
     assert np.array_equal(row0, np.arange(200))
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_topm_rows_in_whole_groups(dtlib, orc, dtype):
+    """The same extremes with a row length that is a whole number of 16-byte groups (the cluster kernel's domain):
+    slices of ties, rows of ties, winners crowded into one slice, a slice of -inf."""
+    V = 3 * 8192 + 80
+    x = torch.randn((1, 7, V), device="cuda") * 2
+    x[0, 0] = 0.5
+    x[0, 1, ::2] = -0.0
+    x[0, 1, 1::2] = 0.0
+    x[0, 2, 100] = float("inf")
+    x[0, 2, 200] = float("-inf")
+    x[0, 2, 9000] = float("inf")
+    x[0, 3] = torch.round(x[0, 3] * 4) / 4
+    x[0, 4, :] = -1.0
+    x[0, 4, V - 300:] = 3.0                          # all the winners in the last slice
+    x[0, 5] = torch.where(torch.arange(V, device="cuda") % 3082 < 40, 7.0, -7.0)  # 40 winners in every slice
+    x[0, 6, : V // 2] = float("-inf")                # half the row at -inf
+    x = x.to(dtype)
+    for M in (1, 64, 200, 256):
+        ids, _ = _check(dtlib, orc, x, M)
+        assert np.array_equal(ids[0, 0].cpu().numpy(), np.arange(M))
 
 
 def test_topm_merge_with_many_candidates(dtlib, orc):
