@@ -204,11 +204,19 @@ dt_status dt_accept_paths(int B, int n, const int32_t* tokens, const int32_t* pa
  *   workspace    dt_lmhead_workspace_bytes(R,D,V,M) bytes (on the current device), header initialised by
  *                dt_workspace_init; the status word reports DT_ERR_NUMERIC for a NaN logit and DT_ERR_TIMEOUT if a
  *                grid-barrier or copy wait ran out (dt_get_error).
- * One persistent cooperative launch, one CTA per SM, each CTA's slice of the logits held in tensor memory; the
- * supported envelope: dtype DT_BF16, D a multiple of 64, R <= 64, M <= DT_MAX_M, and ceil(ceil(V/128)/SMs) * R
- * (R rounded up to 16) <= 512 (V = 151936 on 152 SMs: R <= 64). Outside it: DT_ERR_UNSUPPORTED, before any launch.
+ * Supported: dtype DT_BF16, D a multiple of 64, M <= DT_MAX_M, R <= DT_LMHEAD_MAX_ROWS. Outside it:
+ * DT_ERR_UNSUPPORTED, before any launch. Two designs, chosen by the host:
+ *   - when ceil(ceil(V/128)/SMs) * (R rounded up to 16) <= 512 (V = 151936 on 152 SMs: R <= 64): one persistent
+ *     cooperative launch, one CTA per SM, each CTA's slice of the logits held in tensor memory (bound from a pool of
+ *     every CTA's logits, filter and selection after grid barriers);
+ *   - otherwise four launches: a GEMM pass over every CTA's first vocabulary tile (a sample) whose epilogue fills
+ *     each row's pool; a bound per row from its pool; the full GEMM pass (blocks of 256 hidden rows, two TMEM
+ *     accumulators) whose epilogue keeps the logits at or above their row's bound; a selection per row.
+ * The workspace holds room for every logit of every row as a candidate (8 bytes each: R * V * 8 bytes and a little
+ * more), so that the result is exact whatever the data; only the candidates actually kept are written.
  * Pointers must be 16-byte aligned device pointers; argument errors return DT_ERR_INVALID_ARG before any launch.
  * ------------------------------------------------------------------------------------------------------------- */
+#define DT_LMHEAD_MAX_ROWS 8192
 size_t dt_lmhead_workspace_bytes(int R, int D, int V, int M);
 dt_status dt_lmhead_topm(int R, int D, int V, int M, const void* hidden, const void* w_head, dt_dtype dtype,
                          int32_t* out_ids, float* out_vals, void* workspace, size_t workspace_bytes,

@@ -374,6 +374,230 @@ __global__ void __launch_bounds__(kThreads, 1) lmhead_topm_kernel(LhParams p, co
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(cols) : "memory");
 }
 
+// ---- more than 64 rows: blocked passes -------------------------------------------------------------------------
+// Past 64 hidden rows a CTA's slice of the logits no longer fits its tensor memory, so the GEMM runs twice over
+// blocks of at most 256 hidden rows (the MMA's N), each work item (vocabulary tile of 128 head rows, hidden block)
+// accumulating in one of two TMEM buffers while the epilogue warps drain the other:
+//   1. pool pass: every CTA's first tile only (128 x G head rows, a sample of the vocabulary): every warp quarter
+//      offers each row's two largest logits to the row's pool, as above;
+//   2. lh_bound_kernel: a warp per row takes the M-th largest of the row's pool, to the top 16 key bits (a lower
+//      bound of the row's M-th largest logit: the pool is a subset of the row's logits);
+//   3. filter pass: every tile; the epilogue appends every logit at or above its row's bound to the CTA's list of
+//      the row (room for all of the CTA's values: exact whatever the data);
+//   4. lh_select_kernel: a CTA per row selects the row's top M from the G lists (the selection shared with dt_topm).
+constexpr int kNbMax = 256;  // hidden rows per block: the MMA's N
+
+struct LbParams {
+  int R, D, V, M, G, rpc, tpc, last, Nb, nblk, stages;
+  uint32_t* pool;   // [Rp][G * kPoolPerCta] value keys (0: none)
+  uint32_t* bounds; // [R]
+  uint64_t* cand;   // [R][G][rpc]
+  int* counts;      // [R][G]
+  WsHeader* hdr;
+};
+struct LbMaps {
+  CUtensorMap w;    // head [V][D] bf16, box 64 x 128
+  CUtensorMap wl;   // the same, box 64 x last (a CTA's last tile)
+  CUtensorMap h;    // hidden [R][D] bf16, box 64 x Nb
+};
+// One stage: one K block of the head tile (128 rows x 64) and of the hidden block (Nb rows x 64), 1 KB-aligned.
+__host__ __device__ inline size_t lb_stage_bytes(int Nb) {
+  return static_cast<size_t>(kTileV) * kBK * 2 + static_cast<size_t>(Nb) * kBK * 2;
+}
+// Dynamic shared memory: alignment slack, the ring, and (filter pass) every row's bound and candidate count.
+__host__ __device__ inline size_t lb_smem_bytes(int Nb, int stages, int R) {
+  return 1024 + static_cast<size_t>(stages) * lb_stage_bytes(Nb) + 8 * static_cast<size_t>(R);
+}
+
+template <bool kPool>
+__global__ void __launch_bounds__(kThreads, 1) lh_block_kernel(LbParams p, const __grid_constant__ LbMaps maps) {
+  extern __shared__ float4 smem_f4[];
+  unsigned char* base =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_f4) + 1023) & ~uintptr_t(1023));
+  const size_t stage = lb_stage_bytes(p.Nb);
+  uint32_t* s_bound = reinterpret_cast<uint32_t*>(base + static_cast<size_t>(p.stages) * stage);  // [R]
+  int* s_cnt = reinterpret_cast<int*>(s_bound + p.R);                                              // [R]
+  __shared__ uint64_t full[kMaxStages], empty[kMaxStages], tfull[2], tempty[2];
+  __shared__ uint32_t s_tmem;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int G = static_cast<int>(gridDim.x), bid = static_cast<int>(blockIdx.x);
+  const int R = p.R, Nb = p.Nb, nblk = p.nblk, S = p.stages, nkb = p.D / kBK;
+  const int row0 = bid * p.rpc, nrows = min(p.rpc, p.V - row0);
+  const int my_tiles = nrows > 0 ? (nrows + kTileV - 1) / kTileV : 0;
+  // the pool pass takes tile 0 even past the vocabulary (zero-filled rows, keys 0): every pool slot is written
+  const int tiles = kPool ? 1 : my_tiles;
+  const int items = tiles * nblk;
+  const uint32_t cols = 2u * static_cast<uint32_t>(Nb) <= 32u ? 32u
+                        : 2u * static_cast<uint32_t>(Nb) <= 64u ? 64u
+                        : 2u * static_cast<uint32_t>(Nb) <= 128u ? 128u
+                        : 2u * static_cast<uint32_t>(Nb) <= 256u ? 256u : 512u;
+  if (t == 0) {
+    for (int i = 0; i < kMaxStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 4);  // one arrival per epilogue warp
+    }
+    mbar_fence_init();
+  }
+  if (!kPool) {
+    for (int r = t; r < R; r += kThreads) {
+      s_bound[r] = __ldcg(p.bounds + r);
+      s_cnt[r] = 0;
+    }
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                 "r"(cols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = s_tmem;
+  bool ok = true, nan = false;
+
+  if (warp == 0 && lane == 0) {  // TMA producer: K block kb of item (tile i, hidden block b) into one stage
+    unsigned n = 0;
+    for (int it = 0; it < items && ok; ++it) {
+      const int i = it / nblk, b = it % nblk;
+      const bool lastt = !kPool && i == p.tpc - 1;  // the CTA's last tile reads `last` head rows
+      const CUtensorMap* wm = lastt ? &maps.wl : &maps.w;
+      const uint32_t tx = static_cast<uint32_t>(((lastt ? p.last : kTileV) + Nb) * kBK * 2);
+      for (int kb = 0; kb < nkb; ++kb, ++n) {
+        const unsigned st = n % S, use = n / S;
+        if (use > 0) ok = mbar_wait(&empty[st], (use - 1) & 1u, kBudgetNs);
+        if (!ok) break;
+        unsigned char* a = base + st * stage;
+        mbar_expect_tx(&full[st], tx);
+        tma_load_2d(a, wm, kb * kBK, row0 + i * kTileV, &full[st]);
+        tma_load_2d(a + kTileV * kBK * 2, &maps.h, kb * kBK, b * Nb, &full[st]);
+      }
+    }
+  } else if (warp == 1 && lane == 0) {  // MMA issuer: item it accumulates in TMEM buffer it % 2
+    const uint32_t idesc = umma_idesc(Nb, kTileV);
+    unsigned n = 0;
+    for (int it = 0; it < items && ok; ++it) {
+      const int buf = it & 1;
+      if (it >= 2) ok = mbar_wait(&tempty[buf], static_cast<unsigned>((it >> 1) - 1) & 1u, kBudgetNs);
+      if (!ok) break;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      for (int kb = 0; kb < nkb; ++kb, ++n) {
+        const unsigned st = n % S, use = n / S;
+        ok = mbar_wait(&full[st], use & 1u, kBudgetNs);
+        if (!ok) break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t a = smem_u32(base + st * stage), bb = a + kTileV * kBK * 2;
+#pragma unroll
+        for (int k = 0; k < kBK / 16; ++k)
+          umma_f16(tmem + static_cast<uint32_t>(buf * Nb), umma_desc_sw128(a + 32 * k), umma_desc_sw128(bb + 32 * k),
+                   idesc, (kb > 0 || k > 0) ? 1u : 0u);
+        umma_commit(&empty[st]);  // the stage is free once these MMAs have read it
+      }
+      if (ok) umma_commit(&tfull[buf]);  // the item's accumulator is complete after these MMAs
+    }
+  } else if (warp >= 4) {  // epilogue: warp 4 + q drains TMEM lanes 32 q .. 32 q + 31 (head rows of the tile)
+    const int q = warp & 3;
+    const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16);
+    const int np = G * kPoolPerCta;
+    for (int it = 0; it < items && ok; ++it) {
+      const int i = it / nblk, b = it % nblk, buf = it & 1;
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(&tfull[buf], static_cast<unsigned>(it >> 1) & 1u, kBudgetNs));
+      if (!ok) break;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const int loc = i * kTileV + 32 * q + lane;
+      const bool valid = loc < nrows;  // rows past the range hold stale shared memory (or zero fill)
+      for (int c0 = 0; c0 < Nb; c0 += 32) {
+        uint32_t v0[16], v1[16];
+        const uint32_t ta = tq + static_cast<uint32_t>(buf * Nb + c0);
+        tmem_ld16x2(ta, ta + 16u, v0, v1);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const uint32_t x = j < 16 ? v0[j] : v1[j - 16];
+          const int r = b * Nb + c0 + j;
+          const bool isnan = (x & 0x7FFFFFFFu) > 0x7F800000u;
+          if (kPool) {
+            const uint32_t k = valid && !isnan && r < R ? key_of_f32(x) : 0u;
+            const uint32_t m1 = __reduce_max_sync(0xFFFFFFFFu, k);
+            const int win = __ffs(__ballot_sync(0xFFFFFFFFu, k == m1)) - 1;
+            const uint32_t m2 = __reduce_max_sync(0xFFFFFFFFu, lane == win ? 0u : k);
+            if (lane == 0 && r < R) {
+              uint32_t* pr = p.pool + static_cast<size_t>(r) * np + bid * kPoolPerCta + q * kPoolPerQuarter;
+              pr[0] = m1;
+              pr[1] = m2;
+            }
+          } else if (valid && r < R) {
+            nan |= isnan;
+            const uint32_t k = key_of_f32(x);
+            if (!isnan && k >= s_bound[r]) {
+              const int pos = atomicAdd(&s_cnt[r], 1);  // < rpc: the CTA holds at most rpc logits of a row
+              p.cand[(static_cast<size_t>(r) * G + bid) * p.rpc + pos] =
+                  pack_candidate(k, static_cast<uint32_t>(row0 + loc));
+            }
+          }
+        }
+      }
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);  // the MMAs may overwrite this buffer
+    }
+  }
+  ok = __syncthreads_and(ok);
+  if (!ok && t == 0) {
+    record_error(p.hdr, DT_ERR_TIMEOUT);
+    atomicExch(&p.hdr->abort, 1u);
+  }
+  if (__syncthreads_or(nan) && t == 0) record_error(p.hdr, DT_ERR_NUMERIC);
+  if (!kPool)
+    for (int r = t; r < R; r += kThreads) p.counts[static_cast<size_t>(r) * G + bid] = s_cnt[r];
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(cols) : "memory");
+}
+
+// A warp per row: the M-th largest key of the row's pool (np keys, 0: none), to the top 16 bits (the largest v with
+// at least M pool keys whose top 16 bits are >= v, shifted back): a lower bound of the row's M-th largest logit. 0
+// (every logit a candidate) when the pool holds fewer than M values.
+constexpr int kBoundWarps = 8;
+constexpr int kBoundPerLane = 64;  // pool keys per lane at most: np <= 2048
+__global__ void __launch_bounds__(32 * kBoundWarps) lh_bound_kernel(const uint32_t* __restrict__ pool, int np, int R,
+                                                                     int M, uint32_t* __restrict__ bounds) {
+  __shared__ uint16_t s_pool[kBoundWarps][32 * kBoundPerLane];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x * kBoundWarps + warp;
+  if (r >= R) return;
+  const uint32_t* pr = pool + static_cast<size_t>(r) * np;
+  uint16_t* sp = s_pool[warp];
+  for (int i = lane; i < np; i += 32) sp[i] = static_cast<uint16_t>(__ldcg(pr + i) >> 16);
+  __syncwarp();
+  uint32_t v = 0;
+  for (int bit = 15; bit >= 0; --bit) {
+    const uint32_t cand = v | (1u << bit);
+    unsigned cnt = 0;
+    for (int i = lane; i < np; i += 32) cnt += sp[i] >= cand;
+    if (static_cast<int>(__reduce_add_sync(0xFFFFFFFFu, cnt)) >= M) v = cand;
+  }
+  if (lane == 0) bounds[r] = v << 16;
+}
+
+// A CTA per row: the row's top M from the G lists of the filter pass.
+__global__ void __launch_bounds__(kSelThreads) lh_select_kernel(const uint64_t* __restrict__ cand,
+                                                                const int* __restrict__ counts, int G, int rpc, int M,
+                                                                int32_t* __restrict__ ids, float* __restrict__ vals) {
+  extern __shared__ uint4 smem_u4[];
+  __shared__ int s_warp[kSelThreads / 32];
+  __shared__ int s_n;
+  const int r = blockIdx.x;
+  const uint64_t* rc = cand + static_cast<size_t>(r) * G * rpc;
+  const int* rn = counts + static_cast<size_t>(r) * G;
+  select_words<false, kSelThreads>(
+      [&](int c) { return __ldcg(rn + c); }, G, M,
+      [&](int c, int i) { return __ldcg(rc + static_cast<size_t>(c) * rpc + i); }, ids + static_cast<size_t>(r) * M,
+      vals + static_cast<size_t>(r) * M, *reinterpret_cast<SelectSmem*>(smem_u4), s_warp, &s_n);
+}
+
 constexpr int kLhKbps = 4;  // K blocks per stage (the largest divisor of D / 64 up to this): 512 bytes of a head row
 inline int lh_kbps_setting(int nkb) {
   int k = kLhKbps < nkb ? kLhKbps : nkb;
@@ -399,6 +623,47 @@ inline LhLayout lh_layout(int R, int V, int G) {
   return L;
 }
 
+// The blocked passes (more than 64 rows): four launches on the stream, none waiting on another CTA.
+dt_status lh_blocked(int R, int D, int V, int M, const void* hidden, const void* w_head, int32_t* out_ids,
+                     float* out_vals, char* ws, const LhLayout& L, const DeviceInfo& di, cudaStream_t stream) {
+  const int G = di.sms;
+  const int Nb = R < kNbMax ? (R + 15) / 16 * 16 : kNbMax;
+  const size_t stage = lb_stage_bytes(Nb);
+  const long long room =
+      static_cast<long long>(di.optin) - static_cast<long long>(kStaticReserve) - 1024 - 8LL * static_cast<long long>(R);
+  long long stages = room > 0 ? room / static_cast<long long>(stage) : 0;
+  stages = stages < kMaxStages ? stages : kMaxStages;
+  if (stages < 2) return DT_ERR_UNSUPPORTED;  // every row's bound and count must fit beside a two-stage ring
+  LbParams p{};
+  p.R = R; p.D = D; p.V = V; p.M = M; p.G = G; p.rpc = L.rpc; p.tpc = L.tpc; p.last = L.last;
+  p.Nb = Nb; p.nblk = (R + Nb - 1) / Nb; p.stages = static_cast<int>(stages);
+  p.pool = reinterpret_cast<uint32_t*>(ws + L.pool);
+  p.bounds = reinterpret_cast<uint32_t*>(ws + L.bounds);
+  p.counts = reinterpret_cast<int*>(ws + L.counts);
+  p.cand = reinterpret_cast<uint64_t*>(ws + L.cand);
+  p.hdr = reinterpret_cast<WsHeader*>(ws);
+  LbMaps maps{};
+  if (!encode_bf16_2d(&maps.w, w_head, static_cast<uint64_t>(D), static_cast<uint64_t>(V), static_cast<uint64_t>(D),
+                      kBK, kTileV) ||
+      !encode_bf16_2d(&maps.wl, w_head, static_cast<uint64_t>(D), static_cast<uint64_t>(V), static_cast<uint64_t>(D),
+                      kBK, static_cast<uint32_t>(L.last)) ||
+      !encode_bf16_2d(&maps.h, hidden, static_cast<uint64_t>(D), static_cast<uint64_t>(R), static_cast<uint64_t>(D),
+                      kBK, static_cast<uint32_t>(Nb)))
+    return DT_ERR_CUDA;
+  const size_t smem = lb_smem_bytes(Nb, p.stages, R);
+  const void* fpool = reinterpret_cast<const void*>(lh_block_kernel<true>);
+  const void* ffilt = reinterpret_cast<const void*>(lh_block_kernel<false>);
+  if (ensure_dynamic_smem(fpool, smem) != cudaSuccess || ensure_dynamic_smem(ffilt, smem) != cudaSuccess ||
+      ensure_dynamic_smem(reinterpret_cast<const void*>(lh_select_kernel), sizeof(SelectSmem)) != cudaSuccess)
+    return DT_ERR_CUDA;
+  lh_block_kernel<true><<<G, kThreads, smem, stream>>>(p, maps);
+  lh_bound_kernel<<<(R + kBoundWarps - 1) / kBoundWarps, 32 * kBoundWarps, 0, stream>>>(p.pool, G * kPoolPerCta, R, M,
+                                                                                         p.bounds);
+  lh_block_kernel<false><<<G, kThreads, smem, stream>>>(p, maps);
+  lh_select_kernel<<<R, kSelThreads, sizeof(SelectSmem), stream>>>(p.cand, p.counts, G, L.rpc, M, out_ids, out_vals);
+  return cuda_status(cudaGetLastError());
+}
+
 }  // namespace
 }  // namespace dt
 
@@ -419,14 +684,16 @@ extern "C" dt_status dt_lmhead_topm(int R, int D, int V, int M, const void* hidd
   const void* ptrs[] = {hidden, w_head, out_ids, out_vals, workspace};
   for (const void* q : ptrs)
     if (!q || !aligned16(q)) return DT_ERR_INVALID_ARG;
-  if (dtype != DT_BF16 || D % kBK != 0 || M > DT_MAX_M || R > kMaxRp) return DT_ERR_UNSUPPORTED;
+  if (dtype != DT_BF16 || D % kBK != 0 || M > DT_MAX_M || R > DT_LMHEAD_MAX_ROWS) return DT_ERR_UNSUPPORTED;
   if (static_cast<long long>(V) + kTileV > INT_MAX) return DT_ERR_UNSUPPORTED;
   DeviceInfo di{};
   if (current_device_info(&di) != cudaSuccess) return DT_ERR_CUDA;
   const LhLayout L = lh_layout(R, V, di.sms);
   if (workspace_bytes < L.bytes) return DT_ERR_INVALID_ARG;
-  if (L.tpc * L.Rp > kTmemMax) return DT_ERR_UNSUPPORTED;  // the CTA's slice of logits must fit its tensor memory
   if (di.sms * kPoolPerCta > kThreads * kPoolPerThread) return DT_ERR_UNSUPPORTED;  // the pool of a row in registers
+  // the CTA's slice of logits must fit its tensor memory for the one-launch kernel; otherwise the blocked passes
+  if (R > kMaxRp || L.tpc * L.Rp > kTmemMax)
+    return lh_blocked(R, D, V, M, hidden, w_head, out_ids, out_vals, static_cast<char*>(workspace), L, di, stream);
   // the ring: K blocks per stage and as many stages as the shared memory takes (a reserve for the kernel's static
   // shared memory, about 2 KB)
   const int nkb = D / kBK;

@@ -228,7 +228,7 @@ def test_lmhead_rejects_bad_arguments(dtlib):
     assert call(w=A + 8) == INVALID                   # misaligned
     assert call(dtype=F32) == UNSUPPORTED             # the tensor-core path takes bf16
     assert call(D=96) == UNSUPPORTED                  # K blocks of 64
-    assert call(R=65) == UNSUPPORTED                  # the rows must fit the tensor-memory slice
+    assert call(R=8193) == UNSUPPORTED                # every row's bound and count in shared memory
     assert call(M=2000, V=5000) == UNSUPPORTED
     assert call(R=0) == OK
 

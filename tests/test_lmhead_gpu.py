@@ -65,6 +65,32 @@ def test_lmhead_topm_parity(dtlib, R, D, V, M):
     check_rows(ids, vals, fp64_logits(hb, wb), o_ids, o_vals, M)
 
 
+@pytest.mark.parametrize("R,D,V,M", [
+    (65, 128, 30000, 64),      # one row past the one-launch kernel: one hidden block of 80 (rows 65..79 padding)
+    (300, 192, 20000, 128),    # two hidden blocks of 256, the second partial
+    (100, 64, 1000, 1000),     # M = V: the pool holds fewer than M values, the bound takes every logit
+    (129, 64, 3000, 1),        # the arg-max
+])
+def test_lmhead_topm_blocked_parity(dtlib, R, D, V, M):
+    """More rows than the tensor-memory slice takes: the blocked passes (pool, bound, filter, select)."""
+    ids, vals, hb, wb, status = run(dtlib, R, D, V, M)
+    assert status == dtlib.Status.OK
+    o_ids, o_vals = orc.lmhead_topm(hb, wb, M)
+    check_rows(ids, vals, fp64_logits(hb, wb), o_ids, o_vals, M)
+
+
+def test_lmhead_topm_batched_round_shape(dtlib):
+    """The batched round's projection, 64 requests x 16 block positions of the Qwen3-4B-shaped drafter (R = 1024, D =
+    2560, V = 151936, M = 64). A row's top M depends on that row alone, so the oracle checks sampled rows, one in
+    every hidden block and at both ends of each."""
+    R, D, V, M = 1024, 2560, 151936, 64
+    ids, vals, hb, wb, status = run(dtlib, R, D, V, M, seed=77)
+    assert status == dtlib.Status.OK
+    rows = np.array([0, 1, 255, 256, 511, 640, 767, 1023])
+    o_ids, o_vals = orc.lmhead_topm(np.ascontiguousarray(hb[rows]), wb, M)
+    check_rows(ids[rows], vals[rows], fp64_logits(hb[rows], wb), o_ids, o_vals, M)
+
+
 def test_lmhead_topm_equal_logits_go_to_the_lower_id(dtlib):
     """Duplicated head rows in different tiles (different CTAs) give bit-equal logits: the lower id comes first."""
     def prep(h, w):
@@ -91,3 +117,24 @@ def test_lmhead_topm_reports_nan(dtlib):
         return h, w
     *_, status = run(dtlib, 2, 64, 1000, 8, prep=prep)
     assert status == dtlib.Status.NUMERIC
+    *_, status = run(dtlib, 200, 64, 1000, 8, prep=prep)   # the blocked passes
+    assert status == dtlib.Status.NUMERIC
+
+
+def test_lmhead_topm_blocked_equal_logits_go_to_the_lower_id(dtlib):
+    """The tie rule through the blocked passes: duplicated head rows in different CTAs, 300 rows."""
+    def prep(h, w):
+        w = w.clone()
+        w[900] = w[5] = w[5] * 8
+        w[4100] = w[77] = w[77] * 8
+        return h, w
+    R, D, V, M = 300, 128, 5000, 16
+    ids, vals, hb, wb, status = run(dtlib, R, D, V, M, prep=prep)
+    assert status == dtlib.Status.OK
+    o_ids, o_vals = orc.lmhead_topm(hb, wb, M)
+    check_rows(ids, vals, fp64_logits(hb, wb), o_ids, o_vals, M)
+    for r in range(R):
+        pos = {int(i): m for m, i in enumerate(ids[r])}
+        for a, b in ((5, 900), (77, 4100)):
+            if a in pos and b in pos:
+                assert pos[a] < pos[b] and vals[r, pos[a]] == vals[r, pos[b]], (r, a, b)
