@@ -375,62 +375,68 @@ __global__ void __launch_bounds__(kThreads, 1) lmhead_topm_kernel(LhParams p, co
 }
 
 // ---- more than 64 rows: blocked passes -------------------------------------------------------------------------
-// Past 64 hidden rows a CTA's slice of the logits no longer fits its tensor memory, so the GEMM runs twice over
-// blocks of at most 256 hidden rows (the MMA's N), each work item (vocabulary tile of 128 head rows, hidden block)
-// accumulating in one of two TMEM buffers while the epilogue warps drain the other:
+// Past 64 hidden rows a CTA's slice of the logits no longer fits its tensor memory, so the GEMM runs twice, over
+// work items of (vocabulary tile of 128 head rows, up to W = 256 hidden rows), each accumulating in one of two TMEM
+// buffers while the epilogue warps drain the other:
 //   1. pool pass: every CTA's first tile only (128 x G head rows, a sample of the vocabulary): every warp quarter
 //      offers each row's two largest logits to the row's pool, as above;
 //   2. lh_bound_kernel: a warp per row takes the M-th largest of the row's pool, to the top 16 key bits (a lower
 //      bound of the row's M-th largest logit: the pool is a subset of the row's logits);
-//   3. filter pass: every tile; the epilogue appends every logit at or above its row's bound to the CTA's list of
-//      the row (room for all of the CTA's values: exact whatever the data);
+//   3. filter pass: every tile; the epilogue keeps every logit at or above its row's bound (one float compare per
+//      logit; NaNs take the rare path too) in the CTA's list of the row (room for all of the CTA's values: exact
+//      whatever the data);
 //   4. lh_select_kernel: a CTA per row selects the row's top M from the G lists (the selection shared with dt_topm).
-constexpr int kNbMax = 256;  // hidden rows per block: the MMA's N
+// The CTAs form groups of gs (a divisor of the hidden blocks and of the grid, at most 4) that walk the same
+// vocabulary tiles in step, CTA k of a group taking hidden blocks k, k + gs, ...: a head tile comes from HBM once
+// and from L2 for the group's other CTAs, at about the same time, and no CTA reads a tile twice unless it has more
+// than one hidden block. A row's candidates of a group are all found by one CTA: the lists are (row, group).
+constexpr int kItemMax = 256;                                      // hidden rows per work item: the MMA's N
+constexpr size_t kAStage = static_cast<size_t>(kTileV) * kBK * 2;  // 16 KB: one K block of the head tile
 
 struct LbParams {
-  int R, D, V, M, G, rpc, tpc, last, Nb, nblk, stages;
+  int R, D, V, M, G, rpc, tpc, last;  // rpc, tpc, last: head rows, tiles and rows of the last tile of a group
+  int W, nitem, gs, stages;  // hidden rows per block (a multiple of 16), blocks, CTAs per group, ring stages
   uint32_t* pool;   // [Rp][G * kPoolPerCta] value keys (0: none)
   uint32_t* bounds; // [R]
-  uint64_t* cand;   // [R][G][rpc]
-  int* counts;      // [R][G]
+  uint64_t* cand;   // [R][G / gs][rpc]
+  int* counts;      // [R][G / gs]
   WsHeader* hdr;
 };
 struct LbMaps {
   CUtensorMap w;    // head [V][D] bf16, box 64 x 128
   CUtensorMap wl;   // the same, box 64 x last (a CTA's last tile)
-  CUtensorMap h;    // hidden [R][D] bf16, box 64 x Nb
+  CUtensorMap h;    // hidden [R][D] bf16, box 64 x W
 };
-// One stage: one K block of the head tile (128 rows x 64) and of the hidden block (Nb rows x 64), 1 KB-aligned.
-__host__ __device__ inline size_t lb_stage_bytes(int Nb) {
-  return static_cast<size_t>(kTileV) * kBK * 2 + static_cast<size_t>(Nb) * kBK * 2;
+// One stage: one K block of the head tile (16 KB) and of the hidden block (W rows x 128 bytes), 1 KB-aligned.
+__host__ __device__ inline size_t lb_stage_bytes(int W) { return kAStage + static_cast<size_t>(W) * kBK * 2; }
+// Dynamic shared memory: alignment slack, the ring, and (filter pass) every row's threshold and count.
+__host__ __device__ inline size_t lb_smem_bytes(int W, int stages, int R) {
+  return 1024 + stages * lb_stage_bytes(W) + 8 * static_cast<size_t>(R);
 }
-// Dynamic shared memory: alignment slack, the ring, and (filter pass) every row's bound and candidate count.
-__host__ __device__ inline size_t lb_smem_bytes(int Nb, int stages, int R) {
-  return 1024 + static_cast<size_t>(stages) * lb_stage_bytes(Nb) + 8 * static_cast<size_t>(R);
-}
-
 template <bool kPool>
 __global__ void __launch_bounds__(kThreads, 1) lh_block_kernel(LbParams p, const __grid_constant__ LbMaps maps) {
   extern __shared__ float4 smem_f4[];
-  unsigned char* base =
+  unsigned char* ring =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_f4) + 1023) & ~uintptr_t(1023));
-  const size_t stage = lb_stage_bytes(p.Nb);
-  uint32_t* s_bound = reinterpret_cast<uint32_t*>(base + static_cast<size_t>(p.stages) * stage);  // [R]
-  int* s_cnt = reinterpret_cast<int*>(s_bound + p.R);                                              // [R]
+  const size_t stage = lb_stage_bytes(p.W);
+  float* s_thr = reinterpret_cast<float*>(ring + p.stages * stage);  // [R] each row's bound as a value
+  int* s_cnt = reinterpret_cast<int*>(s_thr + p.R);                  // [R]
   __shared__ uint64_t full[kMaxStages], empty[kMaxStages], tfull[2], tempty[2];
   __shared__ uint32_t s_tmem;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int G = static_cast<int>(gridDim.x), bid = static_cast<int>(blockIdx.x);
-  const int R = p.R, Nb = p.Nb, nblk = p.nblk, S = p.stages, nkb = p.D / kBK;
-  const int row0 = bid * p.rpc, nrows = min(p.rpc, p.V - row0);
+  const int R = p.R, W = p.W, S = p.stages, nkb = p.D / kBK, nitem = p.nitem, gs = p.gs;
+  const int grp = bid / gs, rk = bid % gs, ngroups = G / gs;
+  const int row0 = grp * p.rpc, nrows = min(p.rpc, p.V - row0);  // the group's head rows
   const int my_tiles = nrows > 0 ? (nrows + kTileV - 1) / kTileV : 0;
-  // the pool pass takes tile 0 even past the vocabulary (zero-filled rows, keys 0): every pool slot is written
-  const int tiles = kPool ? 1 : my_tiles;
-  const int items = tiles * nblk;
-  const uint32_t cols = 2u * static_cast<uint32_t>(Nb) <= 32u ? 32u
-                        : 2u * static_cast<uint32_t>(Nb) <= 64u ? 64u
-                        : 2u * static_cast<uint32_t>(Nb) <= 128u ? 128u
-                        : 2u * static_cast<uint32_t>(Nb) <= 256u ? 256u : 512u;
+  // Filter pass: item it is (tile it / nb, hidden block rk + gs (it % nb)), nb = nitem / gs blocks per CTA. Pool
+  // pass: the CTA's sample tile, the group's tile rk (zero-filled or another group's rows past the group's end: not
+  // valid, keys 0; every pool slot is written and no logit is offered twice), against every hidden block.
+  const int nb = kPool ? nitem : nitem / gs;
+  const int items = kPool ? nitem : my_tiles * nb;
+  auto tile_of = [&](int it) { return kPool ? rk : it / nb; };
+  auto block_of = [&](int it) { return kPool ? it : rk + gs * (it % nb); };
+  const uint32_t cols = 2 * W <= 32 ? 32u : 2 * W <= 64 ? 64u : 2 * W <= 128 ? 128u : 2 * W <= 256 ? 256u : 512u;
   if (t == 0) {
     for (int i = 0; i < kMaxStages; ++i) {
       mbar_init(&full[i], 1);
@@ -444,7 +450,8 @@ __global__ void __launch_bounds__(kThreads, 1) lh_block_kernel(LbParams p, const
   }
   if (!kPool) {
     for (int r = t; r < R; r += kThreads) {
-      s_bound[r] = __ldcg(p.bounds + r);
+      const uint32_t b = __ldcg(p.bounds + r);
+      s_thr[r] = b <= 0x007FFFFFu ? -INFINITY : value_of_key_f32(b);  // at or below the key of -inf: no bound
       s_cnt[r] = 0;
     }
   }
@@ -459,25 +466,25 @@ __global__ void __launch_bounds__(kThreads, 1) lh_block_kernel(LbParams p, const
   const uint32_t tmem = s_tmem;
   bool ok = true, nan = false;
 
-  if (warp == 0 && lane == 0) {  // TMA producer: K block kb of item (tile i, hidden block b) into one stage
+  if (warp == 0 && lane == 0) {  // TMA producer: K block kb of item it (its tile and its hidden block) into a stage
     unsigned n = 0;
     for (int it = 0; it < items && ok; ++it) {
-      const int i = it / nblk, b = it % nblk;
-      const bool lastt = !kPool && i == p.tpc - 1;  // the CTA's last tile reads `last` head rows
+      const int i = tile_of(it), j = block_of(it);
+      const bool lastt = !kPool && i == p.tpc - 1;  // the group's last tile reads `last` head rows
       const CUtensorMap* wm = lastt ? &maps.wl : &maps.w;
-      const uint32_t tx = static_cast<uint32_t>(((lastt ? p.last : kTileV) + Nb) * kBK * 2);
+      const uint32_t tx = static_cast<uint32_t>(((lastt ? p.last : kTileV) + W) * kBK * 2);
       for (int kb = 0; kb < nkb; ++kb, ++n) {
         const unsigned st = n % S, use = n / S;
         if (use > 0) ok = mbar_wait(&empty[st], (use - 1) & 1u, kBudgetNs);
         if (!ok) break;
-        unsigned char* a = base + st * stage;
+        unsigned char* a = ring + st * stage;
         mbar_expect_tx(&full[st], tx);
         tma_load_2d(a, wm, kb * kBK, row0 + i * kTileV, &full[st]);
-        tma_load_2d(a + kTileV * kBK * 2, &maps.h, kb * kBK, b * Nb, &full[st]);
+        tma_load_2d(a + kAStage, &maps.h, kb * kBK, j * W, &full[st]);
       }
     }
   } else if (warp == 1 && lane == 0) {  // MMA issuer: item it accumulates in TMEM buffer it % 2
-    const uint32_t idesc = umma_idesc(Nb, kTileV);
+    const uint32_t idesc = umma_idesc(W, kTileV);
     unsigned n = 0;
     for (int it = 0; it < items && ok; ++it) {
       const int buf = it & 1;
@@ -489,10 +496,10 @@ __global__ void __launch_bounds__(kThreads, 1) lh_block_kernel(LbParams p, const
         ok = mbar_wait(&full[st], use & 1u, kBudgetNs);
         if (!ok) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t a = smem_u32(base + st * stage), bb = a + kTileV * kBK * 2;
+        const uint32_t a = smem_u32(ring + st * stage), bb = a + static_cast<uint32_t>(kAStage);
 #pragma unroll
         for (int k = 0; k < kBK / 16; ++k)
-          umma_f16(tmem + static_cast<uint32_t>(buf * Nb), umma_desc_sw128(a + 32 * k), umma_desc_sw128(bb + 32 * k),
+          umma_f16(tmem + static_cast<uint32_t>(buf * W), umma_desc_sw128(a + 32 * k), umma_desc_sw128(bb + 32 * k),
                    idesc, (kb > 0 || k > 0) ? 1u : 0u);
         umma_commit(&empty[st]);  // the stage is free once these MMAs have read it
       }
@@ -503,38 +510,67 @@ __global__ void __launch_bounds__(kThreads, 1) lh_block_kernel(LbParams p, const
     const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16);
     const int np = G * kPoolPerCta;
     for (int it = 0; it < items && ok; ++it) {
-      const int i = it / nblk, b = it % nblk, buf = it & 1;
+      const int i = tile_of(it), j = block_of(it), buf = it & 1;
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(&tfull[buf], static_cast<unsigned>(it >> 1) & 1u, kBudgetNs));
       if (!ok) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const int loc = i * kTileV + 32 * q + lane;
       const bool valid = loc < nrows;  // rows past the range hold stale shared memory (or zero fill)
-      for (int c0 = 0; c0 < Nb; c0 += 32) {
+      const int r0 = j * W;            // hidden row of column 0
+      const uint32_t tb = tq + static_cast<uint32_t>(buf * W);
+      for (int c0 = 0; c0 < W; c0 += 32) {
         uint32_t v0[16], v1[16];
-        const uint32_t ta = tq + static_cast<uint32_t>(buf * Nb + c0);
-        tmem_ld16x2(ta, ta + 16u, v0, v1);
+        tmem_ld16x2(tb + static_cast<uint32_t>(c0), tb + static_cast<uint32_t>(c0 + 16), v0, v1);
+        if (kPool) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const uint32_t x = j < 16 ? v0[j] : v1[j - 16];
-          const int r = b * Nb + c0 + j;
-          const bool isnan = (x & 0x7FFFFFFFu) > 0x7F800000u;
-          if (kPool) {
-            const uint32_t k = valid && !isnan && r < R ? key_of_f32(x) : 0u;
+          for (int jj = 0; jj < 32; ++jj) {
+            const uint32_t x = jj < 16 ? v0[jj] : v1[jj - 16];
+            const int c = c0 + jj, r = r0 + c;
+            const bool isnan = (x & 0x7FFFFFFFu) > 0x7F800000u;
+            const uint32_t k = valid && !isnan && c < W && r < R ? key_of_f32(x) : 0u;
             const uint32_t m1 = __reduce_max_sync(0xFFFFFFFFu, k);
             const int win = __ffs(__ballot_sync(0xFFFFFFFFu, k == m1)) - 1;
             const uint32_t m2 = __reduce_max_sync(0xFFFFFFFFu, lane == win ? 0u : k);
-            if (lane == 0 && r < R) {
+            if (lane == 0 && c < W && r < R) {
               uint32_t* pr = p.pool + static_cast<size_t>(r) * np + bid * kPoolPerCta + q * kPoolPerQuarter;
               pr[0] = m1;
               pr[1] = m2;
             }
-          } else if (valid && r < R) {
-            nan |= isnan;
-            const uint32_t k = key_of_f32(x);
-            if (!isnan && k >= s_bound[r]) {
-              const int pos = atomicAdd(&s_cnt[r], 1);  // < rpc: the CTA holds at most rpc logits of a row
-              p.cand[(static_cast<size_t>(r) * G + bid) * p.rpc + pos] =
-                  pack_candidate(k, static_cast<uint32_t>(row0 + loc));
+          }
+        } else if (valid) {
+          // fast path: one compare per logit against its row's threshold (NaN fails `<` and takes the rare path)
+          unsigned hit = 0;
+#pragma unroll
+          for (int jj = 0; jj < 32; jj += 4) {
+            const int c = c0 + jj, r = r0 + c;
+            float4 th = make_float4(INFINITY, INFINITY, INFINITY, INFINITY);
+            if (c < W && r + 3 < R) {
+              th = *reinterpret_cast<const float4*>(s_thr + r);
+            } else {
+              if (c < W && r < R) th.x = s_thr[r];
+              if (c < W && r + 1 < R) th.y = s_thr[r + 1];
+              if (c < W && r + 2 < R) th.z = s_thr[r + 2];
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t x = jj + e < 16 ? v0[jj + e] : v1[jj + e - 16];
+              const float te = e == 0 ? th.x : e == 1 ? th.y : e == 2 ? th.z : th.w;
+              hit |= static_cast<unsigned>(!(__uint_as_float(x) < te)) << (jj + e);
+            }
+          }
+          if (hit) {  // rare: candidates (or NaNs) among these 32 logits
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+              const uint32_t x = jj < 16 ? v0[jj] : v1[jj - 16];
+              const int c = c0 + jj, r = r0 + c;
+              if (!((hit >> jj) & 1u) || c >= W || r >= R) continue;
+              if ((x & 0x7FFFFFFFu) > 0x7F800000u) {
+                nan = true;
+                continue;
+              }
+              const int pos = atomicAdd(&s_cnt[r], 1);  // < rpc: the group holds rpc logits of a row
+              p.cand[(static_cast<size_t>(r) * ngroups + grp) * p.rpc + pos] =
+                  pack_candidate(key_of_f32(x), static_cast<uint32_t>(row0 + loc));
             }
           }
         }
@@ -550,8 +586,9 @@ __global__ void __launch_bounds__(kThreads, 1) lh_block_kernel(LbParams p, const
     atomicExch(&p.hdr->abort, 1u);
   }
   if (__syncthreads_or(nan) && t == 0) record_error(p.hdr, DT_ERR_NUMERIC);
-  if (!kPool)
-    for (int r = t; r < R; r += kThreads) p.counts[static_cast<size_t>(r) * G + bid] = s_cnt[r];
+  if (!kPool)  // the rows of this CTA's hidden blocks: their lists of this group
+    for (int r = t; r < R; r += kThreads)
+      if ((r / W) % gs == rk) p.counts[static_cast<size_t>(r) * ngroups + grp] = s_cnt[r];
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(cols) : "memory");
@@ -627,16 +664,23 @@ inline LhLayout lh_layout(int R, int V, int G) {
 dt_status lh_blocked(int R, int D, int V, int M, const void* hidden, const void* w_head, int32_t* out_ids,
                      float* out_vals, char* ws, const LhLayout& L, const DeviceInfo& di, cudaStream_t stream) {
   const int G = di.sms;
-  const int Nb = R < kNbMax ? (R + 15) / 16 * 16 : kNbMax;
-  const size_t stage = lb_stage_bytes(Nb);
-  const long long room =
-      static_cast<long long>(di.optin) - static_cast<long long>(kStaticReserve) - 1024 - 8LL * static_cast<long long>(R);
-  long long stages = room > 0 ? room / static_cast<long long>(stage) : 0;
+  const int W = R < kItemMax ? (R + 15) / 16 * 16 : kItemMax;
+  // the ring: as many stages as the shared memory takes beside every row's threshold and count
+  const long long room = static_cast<long long>(di.optin) - static_cast<long long>(kStaticReserve) - 1024 -
+                         8LL * static_cast<long long>(R);
+  long long stages = room > 0 ? room / static_cast<long long>(lb_stage_bytes(W)) : 0;
   stages = stages < kMaxStages ? stages : kMaxStages;
-  if (stages < 2) return DT_ERR_UNSUPPORTED;  // every row's bound and count must fit beside a two-stage ring
+  if (stages < 2) return DT_ERR_UNSUPPORTED;
+  const int nitem = (R + W - 1) / W;
+  int gs = 4;  // CTAs per group: a divisor of the hidden blocks and of the grid
+  while (gs > 1 && (nitem % gs != 0 || G % gs != 0)) gs /= 2;
+  const int ngroups = G / gs;
   LbParams p{};
-  p.R = R; p.D = D; p.V = V; p.M = M; p.G = G; p.rpc = L.rpc; p.tpc = L.tpc; p.last = L.last;
-  p.Nb = Nb; p.nblk = (R + Nb - 1) / Nb; p.stages = static_cast<int>(stages);
+  p.R = R; p.D = D; p.V = V; p.M = M; p.G = G;
+  p.rpc = (V + ngroups - 1) / ngroups;                  // a group's head rows, contiguous
+  p.tpc = (p.rpc + kTileV - 1) / kTileV;
+  p.last = p.rpc - kTileV * (p.tpc - 1);
+  p.W = W; p.nitem = nitem; p.gs = gs; p.stages = static_cast<int>(stages);
   p.pool = reinterpret_cast<uint32_t*>(ws + L.pool);
   p.bounds = reinterpret_cast<uint32_t*>(ws + L.bounds);
   p.counts = reinterpret_cast<int*>(ws + L.counts);
@@ -646,11 +690,11 @@ dt_status lh_blocked(int R, int D, int V, int M, const void* hidden, const void*
   if (!encode_bf16_2d(&maps.w, w_head, static_cast<uint64_t>(D), static_cast<uint64_t>(V), static_cast<uint64_t>(D),
                       kBK, kTileV) ||
       !encode_bf16_2d(&maps.wl, w_head, static_cast<uint64_t>(D), static_cast<uint64_t>(V), static_cast<uint64_t>(D),
-                      kBK, static_cast<uint32_t>(L.last)) ||
+                      kBK, static_cast<uint32_t>(p.last)) ||
       !encode_bf16_2d(&maps.h, hidden, static_cast<uint64_t>(D), static_cast<uint64_t>(R), static_cast<uint64_t>(D),
-                      kBK, static_cast<uint32_t>(Nb)))
+                      kBK, static_cast<uint32_t>(W)))
     return DT_ERR_CUDA;
-  const size_t smem = lb_smem_bytes(Nb, p.stages, R);
+  const size_t smem = lb_smem_bytes(W, p.stages, R);
   const void* fpool = reinterpret_cast<const void*>(lh_block_kernel<true>);
   const void* ffilt = reinterpret_cast<const void*>(lh_block_kernel<false>);
   if (ensure_dynamic_smem(fpool, smem) != cudaSuccess || ensure_dynamic_smem(ffilt, smem) != cudaSuccess ||
@@ -660,7 +704,8 @@ dt_status lh_blocked(int R, int D, int V, int M, const void* hidden, const void*
   lh_bound_kernel<<<(R + kBoundWarps - 1) / kBoundWarps, 32 * kBoundWarps, 0, stream>>>(p.pool, G * kPoolPerCta, R, M,
                                                                                          p.bounds);
   lh_block_kernel<false><<<G, kThreads, smem, stream>>>(p, maps);
-  lh_select_kernel<<<R, kSelThreads, sizeof(SelectSmem), stream>>>(p.cand, p.counts, G, L.rpc, M, out_ids, out_vals);
+  lh_select_kernel<<<R, kSelThreads, sizeof(SelectSmem), stream>>>(p.cand, p.counts, ngroups, p.rpc, M, out_ids,
+                                                                   out_vals);
   return cuda_status(cudaGetLastError());
 }
 
