@@ -506,7 +506,7 @@ def run_ours(args, world, rank, local):
         Hq, Hkv, d, Lp = 32, 8, 128, args.prefix
         aq, ak, av, _ = (t.to(dev) for t in synth.make_attention_inputs(s.B, s.n, Lp, Hq, Hkv, d, seed=99 + rank))
         amask = rnd.out["mask"]
-        aws = torch.empty(dt.dt_tree_attention_workspace_bytes(s.B, s.n, Lp, Hq, Hkv, d), dtype=torch.uint8, device=dev)
+        aws = dt.new_workspace(dt.dt_tree_attention_workspace_bytes(s.B, s.n, Lp, Hq, Hkv, d), dev)
         aout = torch.empty((s.B, s.n, Hq, d), dtype=torch.float32, device=dev)
         scale = 1.0 / math.sqrt(d)
         bm = torch.ones((s.B, 1, s.n, Lp + s.n), dtype=torch.bool, device=dev)

@@ -235,7 +235,11 @@ dt_status dt_lmhead_topm(int R, int D, int V, int M, const void* hidden, const v
  * they multiply the value rows.
  *   q          [B,n,Hq,d] bf16;  k, v [B,Hkv,L+n,d] bf16 (the prefix's cache rows, then the tree's);
  *   mask       [B,n,n] uint8 (device);  out [B,n,Hq,d] fp32;
- *   workspace  dt_tree_attention_workspace_bytes(B,n,L,Hq,Hkv,d) bytes (partials of the key chunks).
+ *   workspace  dt_tree_attention_workspace_bytes(B,n,L,Hq,Hkv,d) bytes: a 256-byte header whose status word reports
+ *              DT_ERR_TIMEOUT if a copy or MMA wait ran out (dt_get_error; initialise it with dt_workspace_init),
+ *              then the partials of the key blocks.
+ * Two launches: the partials on the tensor cores (tcgen05: S = Q K^T and O += P V accumulated in tensor memory, one
+ * CTA per SM over an even share of the (request, key/value head, 64-key block) space), then their combination.
  * Supported: dtype DT_BF16, d = 128, (Hq / Hkv) * n <= 64. Outside it DT_ERR_UNSUPPORTED; argument errors (Hq not a
  * multiple of Hkv, scale not finite and positive, null or misaligned pointers) DT_ERR_INVALID_ARG; both before any
  * launch. Pointers are 16-byte aligned device pointers (mask: any alignment).

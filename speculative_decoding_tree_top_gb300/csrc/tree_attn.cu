@@ -6,14 +6,14 @@
 // i the visible keys are the L prefix positions and the tree positions L + t with mask[b][i][t] = 1;
 // out = softmax(scale q.k) v over them; query head h reads key/value head h / (Hq / Hkv).
 //
-// GB300 design (flash decoding): the n tree nodes of the G = Hq / Hkv query heads that share a key/value head are
-// one block of G n <= 64 query rows, so each key and value row is read once per (request, key/value head) and feeds
-// 64 rows of dot products: a dense contraction on the tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate).
-// The key blocks of all (request, key/value head) pairs, flattened, are split evenly over four CTAs per SM (a CTA's
-// share may span two pairs: one segment each); a CTA streams a segment's key and value rows through a two-stage
-// cp.async ring in blocks of 32 (55 KB, 128 registers), keeps the running max and sum of every query row
-// (online softmax, base 2) and its unnormalised output in registers, and writes them as the segment's partial; a
-// second launch combines the segments of each row. Memory bound: the key and value rows are the bytes.
+// GB300 design (flash decoding on the 5th-generation tensor cores): the n tree nodes of the G = Hq / Hkv query heads
+// that share a key/value head are one block of G n <= 64 query rows, so each key and value row is read once per
+// (request, key/value head) and feeds 64 rows of dot products. The key blocks of all (request, key/value head)
+// pairs, flattened, are split evenly over one CTA per SM (a CTA's share may span several pairs: one segment each).
+// A CTA streams its keys and values by TMA, computes S = Q K^T and O += P V with tcgen05 MMAs whose accumulators
+// live in tensor memory, and runs the softmax (base 2, running maximum raised lazily) from tensor memory, one thread
+// per query row (tree_attn_tc below); a second launch combines the segments of each row. Memory bound: the key and
+// value rows are the bytes.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -21,21 +21,18 @@
 #include <cmath>
 
 #include "dt_internal.cuh"
+#include "umma.cuh"
 
 namespace dt {
 namespace {
 
 constexpr int kD = 128;           // head dimension
 constexpr int kRows = 64;         // query rows per CTA: G x n, padded
-constexpr int kBlockKeys = 32;    // keys per ring stage (small: four CTAs fit an SM)
-constexpr int kThreadsA = 128;    // four warps, 16 query rows each
-constexpr int kPitch = kD + 8;    // shared-memory row pitch in bf16 (272 bytes: conflict-free ldmatrix)
 constexpr int kMaxNodes = 64;
-constexpr int kStagesA = 2;      // key/value ring stages: one block in flight while one is consumed
 
 struct TaParams {
   int B, n, L, T, Hq, Hkv, G, R;
-  int nb;              // key blocks of 32 per (request, key/value head)
+  int nb;              // key blocks of 64 per (request, key/value head)
   int grid, maxseg;    // CTAs of the partial launch; partial slots per (request, key/value head)
   long long work;      // all key blocks: (B Hkv) nb, split evenly over the CTAs
   const unsigned short* q;   // [B][n][Hq][kD] bf16
@@ -48,31 +45,6 @@ struct TaParams {
   float* out;                // [B][n][Hq][kD]
 };
 
-struct TaSmem {
-  __nv_bfloat16 q[kRows * kPitch];
-  __nv_bfloat16 k[kStagesA][kBlockKeys * kPitch];
-  __nv_bfloat16 v[kStagesA][kBlockKeys * kPitch];
-  uint8_t mask[kMaxNodes * kMaxNodes];
-};
-
-__device__ __forceinline__ void cp16(void* dst, const void* src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(valid ? 16 : 0)
-               : "memory");
-}
-__device__ __forceinline__ void ldsm_x4(const void* p, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(smem_u32(p)));
-}
-__device__ __forceinline__ void ldsm_x4_t(const void* p, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(smem_u32(p)));
-}
-__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -83,163 +55,318 @@ __host__ __device__ __forceinline__ int block_owner(long long x, long long W, in
   return static_cast<int>(((x + 1) * G - 1) / W);
 }
 
-// Key and value rows [k0, k0 + 32) of one (request, key/value head) into ring stage s; rows past T read as zero.
-__device__ __forceinline__ void load_kv(const TaParams& p, TaSmem& S, int s, size_t kvbase, int k0) {
-  for (int c = threadIdx.x; c < kBlockKeys * (kD / 8); c += kThreadsA) {
-    const int r = c >> 4, col = (c & 15) * 8, key = k0 + r;  // 16 chunks of 16 bytes per row
-    const bool ok = key < p.T;
-    const size_t off = (kvbase + (ok ? key : 0)) * kD + col;
-    cp16(&S.k[s][r * kPitch + col], p.k + off, ok);
-    cp16(&S.v[s][r * kPitch + col], p.v + off, ok);
-  }
+// ---- the partial launch on tcgen05 -------------------------------------------------------------------------------
+// One CTA per SM takes an even share of the flattened (request, key/value head, block of 64 keys) space, as above;
+// each run of its share within one (request, key/value head) is a segment. The roles run through all of the CTA's
+// segments without stopping between them:
+//   warp 2 (one thread) loads each segment's query rows by 4-D TMA (the box is the G heads x n nodes of the pair, so
+//     row r = i G + gi holds node i of query head kvh G + gi) into one of two Q buffers, and streams the segment's
+//     key and value blocks by 3-D TMA (rows past a pair's end read as zero) through a ring of five 32 KB stages;
+//   warp 3 (one thread) issues the MMAs;
+//   warps 4 and 5 run the softmax, thread r owning query row r (TMEM lane r; rows past G n are padding and are left
+//     to whatever their rows of Q and P hold), so no row statistic needs a shuffle.
+// Per block j:
+//   S_j = Q K_j^T     M = 128 (query rows), N = 64 keys, K = 128: TMEM columns [64 (j % 2), +64), double-buffered
+//                     so that S_{j+1} is computed while block j's softmax runs;
+//   softmax           visibility bits (prefix keys, the node's ancestor row for tree keys, nothing past the pair's
+//                     end), scale (base 2), P = 2^(s - m) rounded to bf16 into shared memory (one 128-byte swizzled
+//                     row per query row, double-buffered);
+//   O += P_j V_j      M = 128, N = 128 (the head dimension), K = 64 keys, V read as an MN-major operand straight
+//                     from its TMA tile: TMEM columns [128 + 128 (segment % 2), +128), double-buffered per segment so
+//                     that a segment's output is read out while the next one accumulates.
+// The running maximum m of a row is raised only when a block's maximum exceeds it by more than 2^8 (then O is
+// rescaled in TMEM, rarely): the weights stay below 2^8, and O and the row sum l are taken against the same m, which
+// is what the combine kernel reads with them. The segment's O, m and l go to its partial slot.
+constexpr int kTcKeys = 64;       // keys per block
+constexpr int kTcStages = 5;      // key/value ring stages
+constexpr int kTcThreads = 256;
+constexpr float kTcLazy = 8.f;    // log2 headroom before the running maximum is raised
+constexpr uint64_t kTcBudgetNs = 4000000000ull;
+constexpr uint32_t kTcBox = kTcKeys * 128;          // one 64-row x 64-dim box: 8 KB
+constexpr uint32_t kTcQBytes = 2 * kTcBox;          // one Q buffer: dims 0-63, then 64-127, 64 rows each
+constexpr uint32_t kTcStageBytes = 4 * kTcBox;      // K (2 boxes), then V (2 boxes)
+constexpr uint32_t kTcPBytes = 128 * kTcKeys * 2;   // 128 rows x 64 keys x 2 bytes
+// Q buffers first: an MMA reads 128 rows of a Q box, rows 64-127 (padding) from whatever follows it, all allocated
+constexpr size_t kTcSmem = 1024 + 2 * kTcQBytes + kTcStages * kTcStageBytes + 2 * kTcPBytes;
+
+struct TaMaps {
+  CUtensorMap q;     // [B][n][Hq][128] bf16, box 64 dims x G heads x n nodes x 1
+  CUtensorMap k, v;  // [B Hkv][T][128] bf16, box 64 dims x 64 keys x 1
+};
+
+// 2^x by the hardware's approximate exponential (relative error about 2^-22, far below the bf16 rounding of the
+// weights it feeds; subnormal results flush to zero: weights below 2^-126 of the row's maximum).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld16_ta(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
 }
 
-// CTA c takes an even share of the flattened (request, key/value head, key block) space; each run of its share
-// within one (request, key/value head) is a segment, whose partial attention for the 64 query rows goes to that
-// pair's slot (c - the owner of the pair's first block).
-__global__ void __launch_bounds__(kThreadsA, 4) tree_attn_partial(TaParams p) {
-  extern __shared__ float4 smem_f4[];
-  TaSmem& S = *reinterpret_cast<TaSmem*>(smem_f4);
-  const int t = threadIdx.x, warp = t >> 5, lane = t & 31, g = lane >> 2, tq = lane & 3;
-  const long long x1 = (static_cast<long long>(blockIdx.x) + 1) * p.work / p.grid;
-  for (long long x = static_cast<long long>(blockIdx.x) * p.work / p.grid; x < x1;) {
-  const int pair = static_cast<int>(x / p.nb), b = pair / p.Hkv, kvh = pair % p.Hkv;
-  const long long pfirst = static_cast<long long>(pair) * p.nb;
+// One segment of a CTA's share: (request, key/value head) pair, its blocks [j0, j0 + nblk), and its partial slot.
+struct TaSeg {
+  int pair, b, kvh, j0, nblk, slot;
+};
+__device__ __forceinline__ TaSeg ta_segment(const TaParams& p, long long& x, long long x1) {
+  TaSeg g;
+  g.pair = static_cast<int>(x / p.nb);
+  g.b = g.pair / p.Hkv;
+  g.kvh = g.pair % p.Hkv;
+  const long long pfirst = static_cast<long long>(g.pair) * p.nb;
   const int bend = static_cast<int>(min(x1, pfirst + p.nb) - pfirst);
-  const int k0 = static_cast<int>(x - pfirst) * kBlockKeys, k1 = min(bend * kBlockKeys, p.T);
-  const int slot = static_cast<int>(blockIdx.x) - block_owner(pfirst, p.work, p.grid);
+  g.j0 = static_cast<int>(x - pfirst);
+  g.nblk = bend - g.j0;
+  g.slot = static_cast<int>(blockIdx.x) - block_owner(pfirst, p.work, p.grid);
   x = pfirst + bend;
-  const size_t kvbase = (static_cast<size_t>(b) * p.Hkv + kvh) * p.T;
-  // query row r = gi n + i: query head kvh G + gi, tree node i (rows >= R read as zero)
-  for (int c = t; c < kRows * (kD / 8); c += kThreadsA) {
-    const int r = c >> 4, col = (c & 15) * 8;
-    const bool ok = r < p.R;
-    const int gi = ok ? r / p.n : 0, i = ok ? r % p.n : 0;
-    cp16(&S.q[r * kPitch + col], p.q + ((static_cast<size_t>(b) * p.n + i) * p.Hq + kvh * p.G + gi) * kD + col, ok);
-  }
-  for (int c = t; c < p.n * p.n; c += kThreadsA) S.mask[c] = p.mask[static_cast<size_t>(b) * p.n * p.n + c];
-  const int nblk = (k1 - k0 + kBlockKeys - 1) / kBlockKeys;
-  for (int j = 0; j < kStagesA - 1; ++j) {  // the first blocks (the queries' copies join the first group)
-    if (j < nblk) load_kv(p, S, j, kvbase, k0 + j * kBlockKeys);
-    asm volatile("cp.async.commit_group;" ::: "memory");
-  }
+  return g;
+}
 
-  const int rw0 = 16 * warp + g, rw1 = rw0 + 8;  // this thread's two query rows
-  const int node0 = rw0 < p.R ? rw0 % p.n : -1, node1 = rw1 < p.R ? rw1 % p.n : -1;
-  float o[16][4];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  for (int blk = 0; blk < nblk; ++blk) {
-    if (blk + kStagesA - 1 < nblk)
-      load_kv(p, S, (blk + kStagesA - 1) % kStagesA, kvbase, k0 + (blk + kStagesA - 1) * kBlockKeys);
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    asm volatile("cp.async.wait_group %0;" ::"n"(kStagesA - 1) : "memory");  // block blk has landed
-    __syncthreads();
-    const __nv_bfloat16* Ks = S.k[blk % kStagesA];
-    const __nv_bfloat16* Vs = S.v[blk % kStagesA];
-    // S = Q K^T for the block's keys: tiles of 8 keys; the warp's 16 query rows re-read as A fragments per K step
-    constexpr int kNT = kBlockKeys / 8;
-    float s[kNT][4];
-#pragma unroll
-    for (int j = 0; j < kNT; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < kD / 16; ++ks) {
-      uint32_t qa[4];
-      ldsm_x4(&S.q[(16 * warp + (lane & 15)) * kPitch + ks * 16 + (lane >> 4) * 8], qa[0], qa[1], qa[2], qa[3]);
-#pragma unroll
-      for (int np = 0; np < kNT / 2; ++np) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(&Ks[(np * 16 + (lane & 7) + ((lane >> 4) << 3)) * kPitch + ks * 16 + ((lane >> 3) & 1) * 8], b0, b1,
-                b2, b3);
-        mma_bf16(s[2 * np], qa, b0, b1);
-        mma_bf16(s[2 * np + 1], qa, b2, b3);
+__global__ void __launch_bounds__(kTcThreads, 1) tree_attn_tc(TaParams p, const __grid_constant__ TaMaps maps,
+                                                              WsHeader* hdr) {
+  extern __shared__ float4 smem_f4[];
+  unsigned char* sq =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_f4) + 1023) & ~uintptr_t(1023));
+  unsigned char* skv = sq + 2 * kTcQBytes;
+  unsigned char* sp = skv + kTcStages * kTcStageBytes;
+  __shared__ uint64_t kv_full[kTcStages], kv_empty[kTcStages], s_full[2], p_full[2], o_done[2];
+  __shared__ uint64_t q_full[2], q_empty[2], o_free[2];
+  __shared__ uint32_t s_tmem;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  if (t == 0) {
+    for (int i = 0; i < kTcStages; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 2);  // one arrival per softmax warp
+      mbar_init(&o_done[i], 1);
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+      mbar_init(&o_free[i], 2);
+    }
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                 "r"(512) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = s_tmem;
+  bool ok = true;
+  const long long x0 = static_cast<long long>(blockIdx.x) * p.work / p.grid;
+  const long long x1 = (static_cast<long long>(blockIdx.x) + 1) * p.work / p.grid;
+
+  if (warp == 2 && lane == 0) {  // TMA producer
+    unsigned g = 0;
+    const uint32_t qtx = static_cast<uint32_t>(2 * 128 * p.R);
+    int si = 0;
+    for (long long x = x0; x < x1 && ok; ++si) {
+      const TaSeg sg = ta_segment(p, x, x1);
+      const unsigned qb = static_cast<unsigned>(si) & 1u;
+      if (si >= 2) ok = mbar_wait(&q_empty[qb], static_cast<unsigned>((si >> 1) - 1) & 1u, kTcBudgetNs);
+      if (!ok) break;
+      unsigned char* qd = sq + qb * kTcQBytes;
+      mbar_expect_tx(&q_full[qb], qtx);
+      tma_load_4d(qd, &maps.q, 0, sg.kvh * p.G, 0, sg.b, &q_full[qb]);
+      tma_load_4d(qd + kTcBox, &maps.q, 64, sg.kvh * p.G, 0, sg.b, &q_full[qb]);
+      for (int j = 0; j < sg.nblk && ok; ++j, ++g) {
+        const unsigned st = g % kTcStages, use = g / kTcStages;
+        if (use > 0) ok = mbar_wait(&kv_empty[st], (use - 1) & 1u, kTcBudgetNs);
+        if (!ok) break;
+        unsigned char* d = skv + st * kTcStageBytes;
+        const int key = (sg.j0 + j) * kTcKeys;
+        mbar_expect_tx(&kv_full[st], kTcStageBytes);
+        tma_load_3d(d, &maps.k, 0, key, sg.pair, &kv_full[st]);
+        tma_load_3d(d + kTcBox, &maps.k, 64, key, sg.pair, &kv_full[st]);
+        tma_load_3d(d + 2 * kTcBox, &maps.v, 0, key, sg.pair, &kv_full[st]);
+        tma_load_3d(d + 3 * kTcBox, &maps.v, 64, key, sg.pair, &kv_full[st]);
       }
     }
-    // mask and scale (base 2), the rows' running maxima
-    const int kb = k0 + blk * kBlockKeys;
-    float mx0 = -INFINITY, mx1 = -INFINITY;
+  } else if (warp == 3 && lane == 0) {  // MMA issuer
+    const uint32_t id_s = umma_idesc(kTcKeys, 128), id_o = umma_idesc(kD, 128) | (1u << 16);  // O: V MN-major
+    unsigned g = 0;
+    int si = 0;
+    for (long long x = x0; x < x1 && ok; ++si) {
+      const TaSeg sg = ta_segment(p, x, x1);
+      const unsigned qb = static_cast<unsigned>(si) & 1u;
+      const uint32_t aq = smem_u32(sq + qb * kTcQBytes), to = tmem + 128u + 128u * qb;
+      ok = mbar_wait(&q_full[qb], static_cast<unsigned>(si >> 1) & 1u, kTcBudgetNs);
+      // this segment's O buffer was read out by the softmax of segment si - 2
+      if (ok && si >= 2) ok = mbar_wait(&o_free[qb], static_cast<unsigned>((si >> 1) - 1) & 1u, kTcBudgetNs);
+      if (!ok) break;
+      auto issue_s = [&](unsigned gs) {  // S = Q K^T of block gs into TMEM columns [64 (gs % 2), +64)
+        const unsigned st = gs % kTcStages;
+        if (!mbar_wait(&kv_full[st], (gs / kTcStages) & 1u, kTcBudgetNs)) return false;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t bk = smem_u32(skv + st * kTcStageBytes);
 #pragma unroll
-    for (int nt = 0; nt < kNT; ++nt) {
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kTcBox + (kk & 3) * 32u;
+          umma_f16(tmem + (gs & 1u) * kTcKeys, umma_desc_sw128(aq + off), umma_desc_sw128(bk + off), id_s,
+                   kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&s_full[gs & 1u]);
+        return true;
+      };
+      ok = issue_s(g);
+      if (ok && sg.nblk == 1) umma_commit(&q_empty[qb]);  // the segment's last S: Q may be reloaded after it
+      for (int j = 0; j < sg.nblk && ok; ++j, ++g) {
+        const unsigned st = g % kTcStages;
+        if (j + 1 < sg.nblk) {  // its S buffer was freed by block g - 1's softmax (waited for below, one block ago)
+          ok = issue_s(g + 1);
+          if (ok && j + 2 == sg.nblk) umma_commit(&q_empty[qb]);
+        }
+        if (ok) ok = mbar_wait(&p_full[g & 1u], (g >> 1) & 1u, kTcBudgetNs);  // P written, O rescaled if it had to be
+        if (!ok) break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t ap = smem_u32(sp + (g & 1u) * kTcPBytes), bv = smem_u32(skv + st * kTcStageBytes + 2 * kTcBox);
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int key = kb + nt * 8 + tq * 2 + e;
-        const bool in = key < k1;
-        const bool v0 = in && node0 >= 0 && (key < p.L || S.mask[node0 * p.n + (key - p.L)] != 0);
-        const bool v1 = in && node1 >= 0 && (key < p.L || S.mask[node1 * p.n + (key - p.L)] != 0);
-        s[nt][e] = v0 ? s[nt][e] * p.scale_log2 : -INFINITY;
-        s[nt][2 + e] = v1 ? s[nt][2 + e] * p.scale_log2 : -INFINITY;
-        mx0 = fmaxf(mx0, s[nt][e]);
-        mx1 = fmaxf(mx1, s[nt][2 + e]);
+        for (int kk = 0; kk < kTcKeys / 16; ++kk)
+          umma_f16(to, umma_desc_sw128(ap + 32u * kk), umma_desc_sw128_mn(bv + 2048u * kk, kTcBox, 1024u), id_o,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&kv_empty[st]);  // the block's keys and values have been read
+        umma_commit(&o_done[g & 1u]);
       }
     }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 2));
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float a0 = mn0 == -INFINITY ? 1.f : exp2f(m0 - mn0), a1 = mn1 == -INFINITY ? 1.f : exp2f(m1 - mn1);
-    float ls0 = 0.f, ls1 = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < kNT; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        s[nt][e] = mn0 == -INFINITY ? 0.f : exp2f(s[nt][e] - mn0);
-        s[nt][2 + e] = mn1 == -INFINITY ? 0.f : exp2f(s[nt][2 + e] - mn1);
-        ls0 += s[nt][e];
-        ls1 += s[nt][2 + e];
+  } else if (warp == 4 || warp == 5) {  // softmax: thread r owns query row r (TMEM lane r)
+    const int r = 32 * (warp & 3) + lane;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    const bool live = r < p.R;
+    const int node = live ? r / p.G : 0, gi = live ? r % p.G : 0;  // row r = node G + gi
+    unsigned g = 0;
+    int si = 0;
+    for (long long x = x0; x < x1 && ok; ++si) {
+      const TaSeg sg = ta_segment(p, x, x1);
+      const unsigned qb = static_cast<unsigned>(si) & 1u;
+      const uint32_t to = tl + 128u + 128u * qb;
+      unsigned long long mbits = 0;  // bit c: tree position c is on the node's ancestor row
+      if (live) {
+        const uint8_t* mr = p.mask + (static_cast<size_t>(sg.b) * p.n + node) * p.n;
+        for (int c = 0; c < p.n; ++c) mbits |= static_cast<unsigned long long>(mr[c] != 0) << c;
       }
-    }
-    l0 = l0 * a0 + ls0;  // this thread's share of the row sums (the quad adds them up at the end)
-    l1 = l1 * a1 + ls1;
-    m0 = mn0;
-    m1 = mn1;
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < sg.nblk && ok; ++j, ++g) {
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(&s_full[g & 1u], (g >> 1) & 1u, kTcBudgetNs));
+        if (!ok) break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        uint32_t sv[4][16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      o[j][0] *= a0;
-      o[j][1] *= a0;
-      o[j][2] *= a1;
-      o[j][3] *= a1;
-    }
-    // O += P V: P from the score registers (bf16), V by transposed ldmatrix
+        for (int h = 0; h < 4; ++h) tmem_ld16_ta(tl + (g & 1u) * kTcKeys + 16u * h, sv[h]);
+        // bit c: key kbase + c is visible to this row; then a branch-free pass over the 64 scores
+        const int kbase = (sg.j0 + j) * kTcKeys, pre = p.L - kbase, lim = p.T - kbase;
+        unsigned long long visb = 0;
+        if (live) {
+          const unsigned long long pbits = pre >= 64 ? ~0ull : pre <= 0 ? 0ull : (1ull << pre) - 1ull;
+          unsigned long long tbits = 0;
+          if (pre < 64) tbits = pre >= 0 ? mbits << pre : mbits >> (-pre);  // 0 <= -pre < n <= 64
+          const unsigned long long lbits = lim >= 64 ? ~0ull : lim <= 0 ? 0ull : (1ull << lim) - 1ull;
+          visb = (pbits | tbits) & lbits;
+        }
+        float s[64];
+        float bmax = -INFINITY;
 #pragma unroll
-    for (int kp = 0; kp < kBlockKeys / 16; ++kp) {
-      const uint32_t pa[4] = {pack_bf16(s[2 * kp][0], s[2 * kp][1]), pack_bf16(s[2 * kp][2], s[2 * kp][3]),
-                              pack_bf16(s[2 * kp + 1][0], s[2 * kp + 1][1]),
-                              pack_bf16(s[2 * kp + 1][2], s[2 * kp + 1][3])};
+        for (int c = 0; c < 64; ++c) {
+          s[c] = (visb >> c) & 1ull ? __uint_as_float(sv[c >> 4][c & 15]) * p.scale_log2 : -INFINITY;
+          bmax = fmaxf(bmax, s[c]);
+        }
+        // raise the running maximum only past the headroom; O is rescaled then, unless it holds nothing yet
+        const bool raise = bmax > m + kTcLazy || (m == -INFINITY && bmax > -INFINITY);
+        const bool rescale_o = raise && m > -INFINITY;
+        const float mn = raise ? bmax : m;
+        const float alpha = rescale_o ? fast_exp2(m - mn) : 1.f;
+        m = mn;
+        float ls = 0.f;
+        uint32_t pk[32];
 #pragma unroll
-      for (int dp = 0; dp < kD / 16; ++dp) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(&Vs[(kp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * kPitch + dp * 16 + (lane >> 4) * 8], b0, b1,
-                  b2, b3);
-        mma_bf16(o[2 * dp], pa, b0, b1);
-        mma_bf16(o[2 * dp + 1], pa, b2, b3);
+        for (int c = 0; c < 64; c += 2) {
+          const float a = m == -INFINITY ? 0.f : fast_exp2(s[c] - m), bb = m == -INFINITY ? 0.f : fast_exp2(s[c + 1] - m);
+          ls += a + bb;
+          pk[c >> 1] = pack_bf16(a, bb);
+        }
+        l = l * alpha + ls;
+        // P's buffer was last read by the O MMA of block g - 2; a rescale needs block g - 1's O MMA complete (it is
+        // of this segment: m was finite). Commits complete in order.
+        const bool any_rescale = __any_sync(0xFFFFFFFFu, rescale_o);
+        if (g >= 2 || any_rescale) {
+          const unsigned gw = any_rescale ? g - 1 : g - 2;
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait(&o_done[gw & 1u], (gw >> 1) & 1u, kTcBudgetNs));
+          if (!ok) break;
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        }
+        if (any_rescale) {
+#pragma unroll
+          for (int h = 0; h < 8; ++h) {
+            uint32_t ov[16];
+            tmem_ld16_ta(to + 16u * h, ov);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            tmem_st16(to + 16u * h, ov);
+          }
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        }
+        unsigned char* prow = sp + (g & 1u) * kTcPBytes + r * 128;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)
+          *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) =
+              make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the MMA reads P through the async proxy
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[g & 1u]);
       }
-    }
-    __syncthreads();  // the stage is refilled by a later load
-  }
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
-  l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 1);
-  l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 2);
-  l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 1);
-  l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 2);
-  const size_t unit = static_cast<size_t>(pair) * p.maxseg + slot;
-  float* po = p.part + unit * kRows * kD;
+      if (!ok) break;
+      // the segment's partial: O (unnormalised, against m), m and l of each live row, at row gi n + node
+      const unsigned gl = g - 1;
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(&o_done[gl & 1u], (gl >> 1) & 1u, kTcBudgetNs));
+      if (!ok) break;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const size_t unit = static_cast<size_t>(sg.pair) * p.maxseg + sg.slot;
+      const int prow_out = gi * p.n + node;
+      float* po = p.part + (unit * kRows + prow_out) * kD;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const int col = j * 8 + tq * 2;
-    *reinterpret_cast<float2*>(po + rw0 * kD + col) = make_float2(o[j][0], o[j][1]);
-    *reinterpret_cast<float2*>(po + rw1 * kD + col) = make_float2(o[j][2], o[j][3]);
+      for (int h = 0; h < 8; ++h) {
+        uint32_t ov[16];
+        tmem_ld16_ta(to + 16u * h, ov);
+        if (live)
+#pragma unroll
+          for (int e = 0; e < 16; e += 4)
+            *reinterpret_cast<float4*>(po + 16 * h + e) = make_float4(__uint_as_float(ov[e]), __uint_as_float(ov[e + 1]),
+                                                                      __uint_as_float(ov[e + 2]), __uint_as_float(ov[e + 3]));
+      }
+      if (live) {
+        float* pm = p.ml + (unit * kRows + prow_out) * 2;
+        pm[0] = m;
+        pm[1] = l;
+      }
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&o_free[qb]);  // the next segment but one may accumulate here
+    }
   }
-  if (tq == 0) {
-    float* pm = p.ml + unit * kRows * 2;
-    pm[rw0 * 2] = m0;
-    pm[rw0 * 2 + 1] = l0;
-    pm[rw1 * 2] = m1;
-    pm[rw1 * 2 + 1] = l1;
-  }
-  __syncthreads();  // the queries, mask and ring are reloaded for the next segment
-  }
+  ok = __syncthreads_and(ok);
+  if (!ok && t == 0) record_error(hdr, DT_ERR_TIMEOUT);
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
 }
 
 // The segments' partials of each (request, key/value head, query row), rescaled to the row's overall maximum and
@@ -350,14 +477,14 @@ struct TaPlan {
   long long work;
   size_t part, ml, bytes;
 };
-// Four CTAs per SM share all key blocks evenly (a CTA takes at least one block); maxseg is the most CTAs any
-// (request, key/value head) is spread over, found pair by pair.
-inline TaPlan ta_plan(int B, int T, int Hkv, int sms) {
+// The partial launch's CTAs (`per_sm` per SM) share all key blocks of `block` keys evenly (a CTA takes at least one
+// block); maxseg is the most CTAs any (request, key/value head) is spread over, found pair by pair.
+inline TaPlan ta_plan(int B, int T, int Hkv, int sms, int per_sm = 1, int block = kTcKeys) {
   TaPlan P{};
   const long long pairs = static_cast<long long>(B) * Hkv;
-  P.nb = (T + kBlockKeys - 1) / kBlockKeys;
+  P.nb = (T + block - 1) / block;
   P.work = pairs * P.nb;
-  const long long g = 4LL * sms;
+  const long long g = static_cast<long long>(per_sm) * sms;
   P.grid = static_cast<int>(g < P.work ? g : P.work);
   P.maxseg = 1;
   for (long long pr = 0; pr < pairs; ++pr) {
@@ -365,8 +492,8 @@ inline TaPlan ta_plan(int B, int T, int Hkv, int sms) {
     P.maxseg = segs > P.maxseg ? segs : P.maxseg;
   }
   const size_t slots = static_cast<size_t>(pairs) * P.maxseg;
-  P.part = 0;
-  P.ml = align_up(sizeof(float) * slots * kRows * kD);
+  P.part = align_up(sizeof(WsHeader));  // the status word first
+  P.ml = align_up(P.part + sizeof(float) * slots * kRows * kD);
   P.bytes = align_up(P.ml + sizeof(float) * slots * kRows * 2);
   return P;
 }
@@ -414,9 +541,17 @@ extern "C" dt_status dt_tree_attention(int B, int n, int L, int Hq, int Hkv, int
   p.part = reinterpret_cast<float*>(ws + P.part);
   p.ml = reinterpret_cast<float*>(ws + P.ml);
   p.out = out;
-  const void* fa = reinterpret_cast<const void*>(tree_attn_partial);
-  if (ensure_dynamic_smem(fa, sizeof(TaSmem)) != cudaSuccess) return DT_ERR_CUDA;
-  tree_attn_partial<<<static_cast<unsigned>(P.grid), kThreadsA, sizeof(TaSmem), stream>>>(p);
+  TaMaps maps{};
+  const uint64_t pairs = static_cast<uint64_t>(B) * static_cast<uint64_t>(Hkv);
+  if (!encode_bf16_4d(&maps.q, q, kD, static_cast<uint64_t>(Hq), static_cast<uint64_t>(n), static_cast<uint64_t>(B),
+                      64, static_cast<uint32_t>(G), static_cast<uint32_t>(n)) ||
+      !encode_bf16_3d(&maps.k, k, kD, static_cast<uint64_t>(T), pairs, 64, kTcKeys) ||
+      !encode_bf16_3d(&maps.v, v, kD, static_cast<uint64_t>(T), pairs, 64, kTcKeys))
+    return DT_ERR_CUDA;
+  const void* fa = reinterpret_cast<const void*>(tree_attn_tc);
+  if (ensure_dynamic_smem(fa, kTcSmem) != cudaSuccess) return DT_ERR_CUDA;
+  tree_attn_tc<<<static_cast<unsigned>(P.grid), kTcThreads, kTcSmem, stream>>>(p, maps,
+                                                                               reinterpret_cast<WsHeader*>(ws));
   const long long crows = static_cast<long long>(B) * Hkv * p.R, cper = P.maxseg <= kWarpRowSegs ? kCombineWarps : 1;
   const long long cgrid = (crows + cper - 1) / cper, ccap = static_cast<long long>(kCombinePerSm) * di.sms;
   tree_attn_combine<<<static_cast<unsigned>(cgrid < ccap ? cgrid : ccap), kCombineThreads, 0, stream>>>(p);

@@ -18,6 +18,13 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {  // K-majo
   return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
          (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) | (static_cast<uint64_t>(2) << 61);
 }
+// MN-major tile with 128-byte swizzle: 64 elements of M (or N) contiguous in a 128-byte row, eight K rows per 1 KB
+// atom; atoms `mn_stride` bytes apart along M (N) and `k_stride` bytes apart along K.
+__device__ __forceinline__ uint64_t umma_desc_sw128_mn(uint32_t saddr, uint32_t mn_stride, uint32_t k_stride) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>((mn_stride >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((k_stride >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
 __device__ __forceinline__ uint32_t umma_idesc(int n, int m = 128) {  // bf16 x bf16 -> fp32, both K-major
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
          (static_cast<uint32_t>(m >> 4) << 24);
@@ -34,6 +41,17 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
   asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
                ::"r"(smem_u32(dst)), "l"(map), "r"(c0), "r"(c1), "r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(smem_u32(dst)), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
+      ::"r"(smem_u32(dst)), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar)) : "memory");
 }
 // Four 32-lane x 8-column TMEM loads, `stride` columns apart, and the wait for them, in one statement (nothing can
 // read the registers before the wait).
@@ -57,32 +75,64 @@ __device__ __forceinline__ void tmem_ld4x8(uint32_t taddr, uint32_t stride, floa
     for (int j = 0; j < 8; ++j) v[g][j] = __uint_as_float(r[8 * g + j]);
 }
 
-// A 2-D bf16 tensor map (rows of `cols` elements, `pitch` elements apart) read in boxes of box_cols x box_rows with
-// 128-byte swizzle; elements outside the tensor read as zero. cuTensorMapEncodeTiled comes from the driver through
-// the runtime's entry-point query (no link to the driver library). False when the encoder is missing or refuses.
-inline bool encode_bf16_2d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint64_t pitch,
-                           uint32_t box_cols, uint32_t box_rows) {
+// cuTensorMapEncodeTiled, from the driver through the runtime's entry-point query (no link to the driver library);
+// null when it is missing.
+inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static std::mutex mu;
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   static bool looked = false;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (!looked) {
-      looked = true;
-      void* f = nullptr;
-      cudaDriverEntryPointQueryResult q{};
-      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-              cudaSuccess &&
-          q == cudaDriverEntryPointSuccess)
-        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!looked) {
+    looked = true;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
   }
+  return encode;
+}
+// A 2-D bf16 tensor map (rows of `cols` elements, `pitch` elements apart) read in boxes of box_cols x box_rows with
+// 128-byte swizzle; elements outside the tensor read as zero. False when the encoder is missing or refuses.
+inline bool encode_bf16_2d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint64_t pitch,
+                           uint32_t box_cols, uint32_t box_rows) {
+  const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode) return false;
   const cuuint64_t gdim[2] = {cols, rows};
   const cuuint64_t gstride[1] = {pitch * 2};
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estride[2] = {1, 1};
   return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), gdim, gstride, box, estride,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A 3-D bf16 tensor map: `planes` planes of `rows` rows of `cols` elements (dense), read in boxes of box_cols x
+// box_rows x 1 with 128-byte swizzle; elements outside the tensor (rows past a plane's end) read as zero.
+inline bool encode_bf16_3d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint64_t planes,
+                           uint32_t box_cols, uint32_t box_rows) {
+  const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return false;
+  const cuuint64_t gdim[3] = {cols, rows, planes};
+  const cuuint64_t gstride[2] = {cols * 2, cols * rows * 2};
+  const cuuint32_t box[3] = {box_cols, box_rows, 1};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), gdim, gstride, box, estride,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A 4-D bf16 tensor map over a dense [d3][d2][d1][d0] array (d0 innermost), read in boxes of b0 x b1 x b2 x 1 with
+// 128-byte swizzle: the box lands as b1 * b2 rows of b0 elements, b1 fastest.
+inline bool encode_bf16_4d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t d3,
+                           uint32_t b0, uint32_t b1, uint32_t b2) {
+  const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return false;
+  const cuuint64_t gdim[4] = {d0, d1, d2, d3};
+  const cuuint64_t gstride[3] = {d0 * 2, d0 * d1 * 2, d0 * d1 * d2 * 2};
+  const cuuint32_t box[4] = {b0, b1, b2, 1};
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), gdim, gstride, box, estride,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -228,8 +228,7 @@ def dt_tree_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: t
     if out is None:
         out = torch.empty((B, n, Hq, d), dtype=torch.float32, device=q.device)
     if workspace is None:
-        workspace = torch.empty(max(dt_tree_attention_workspace_bytes(B, n, L, Hq, Hkv, d), 256), dtype=torch.uint8,
-                                device=q.device)
+        workspace = new_workspace(dt_tree_attention_workspace_bytes(B, n, L, Hq, Hkv, d), q.device)
     _check(lib().dt_tree_attention(B, n, L, Hq, Hkv, d, _dev(q, "q", q.dtype, (B, n, Hq, d)),
                                    _dev(k, "k", q.dtype, (B, Hkv, T, d)), _dev(v, "v", q.dtype, (B, Hkv, T, d)),
                                    _code(q.dtype), _dev(mask, "mask", torch.uint8, (B, n, n)), float(scale),
