@@ -695,7 +695,7 @@ __device__ bool children_groups(const Params& p, int w, const Job* jl, unsigned 
   const int M4 = round4(M);
   const unsigned rb = static_cast<unsigned>(H * 2);
   const JobGroup* gl = p.grouplist + static_cast<size_t>(w & 1) * p.B * p.lookahead;
-  const bool own = p.B >= static_cast<int>(gridDim.x);
+  const bool own = p.own_groups;
   // the wave's group count and (spread mode) this CTA's first group, read together: the list's slot exists even when
   // the group does not (then it holds an older wave's entry, unused)
   JobGroup first_group{};
@@ -976,91 +976,112 @@ __device__ bool control_phase(const Params& p, int w, unsigned char* smem, uint6
   const int t = threadIdx.x, warp = t >> 5;
   const int M = p.M, n = p.n, X = p.xslots, KM = M < n ? M : n, kla = p.lookahead;
   const ReqLayout RL = req_layout(n, X, KM, kla);
-  const ReqView R = req_view(smem, RL);
-  Job* jobs = reinterpret_cast<Job*>(smem + RL.jobs);
+  const size_t rstride = (RL.bytes + 127) / 128 * 128;  // one shared-memory region per request of a batch
+  const int G = static_cast<int>(gridDim.x), C = p.ctl_conc;
   Job* next = p.joblist + static_cast<size_t>((w + 1) & 1) * p.B * kla;
   __shared__ int s_off;
-  for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
-    unsigned char* gstate = p.rstate + static_cast<size_t>(b) * RL.bytes;
-    __syncthreads();  // the previous request (or phase) is done with the shared buffers
+  __shared__ int s_done[kWarps];  // the request was finished in an earlier wave
+  // The requests this CTA owns (b = blockIdx.x + i G), up to C at a time: their state blocks come in by bulk copies
+  // on one barrier, warp i runs request i's best-first step, and the rest follows request by request.
+  for (int b0 = blockIdx.x; b0 < p.B; b0 += G * C) {
+    int nb = 0;
+    while (nb < C && b0 + nb * G < p.B) ++nb;
+    __syncthreads();  // the previous batch (or phase) is done with the shared buffers
     if (t == 0) {
       asm volatile("fence.proxy.async.global;" ::: "memory");
-      mbar_expect_tx(bar, static_cast<unsigned>(RL.bytes));
-      bulk_g2s(smem, gstate, static_cast<unsigned>(RL.bytes), bar);
+      mbar_expect_tx(bar, static_cast<unsigned>(RL.bytes * nb));
+      for (int i = 0; i < nb; ++i)
+        bulk_g2s(smem + i * rstride, p.rstate + static_cast<size_t>(b0 + i * G) * RL.bytes,
+                 static_cast<unsigned>(RL.bytes), bar);
     }
     if (!__syncthreads_and(wait_copies(p, bar, bar_uses))) return false;
-    if (R.ctl->s >= n) continue;  // finished in an earlier wave
-    if (warp == 0) request_step(R, b, n, M, p.max_depth, X, KM, kla, jobs, p.hdr);
-    __syncthreads();
-    const ReqCtl st = *R.ctl;
-    if (t == 0 && st.njobs > 0) {
-      // the picks in order of depth (stable): a request's expansions at one block position sit together in the packed
-      // list, and each such run is a group of the children phase
-      for (int i = 1; i < st.njobs; ++i)
-        for (int k = i; k > 0 && jobs[k - 1].depth > jobs[k].depth; --k) {
-          const Job tmp = jobs[k];
-          jobs[k] = jobs[k - 1];
-          jobs[k - 1] = tmp;
-        }
-      int ng = 1;
-      for (int i = 1; i < st.njobs; ++i) ng += jobs[i].depth != jobs[i - 1].depth;
-      s_off = atomicAdd(p.jobcount + w + 1, st.njobs);
-      int gi = atomicAdd(p.groupcount + w + 1, ng);
-      JobGroup* gnext = p.grouplist + static_cast<size_t>((w + 1) & 1) * p.B * kla;
-      for (int i = 0; i < st.njobs;) {
-        int e = i + 1;
-        while (e < st.njobs && jobs[e].depth == jobs[i].depth) ++e;
-        gnext[gi++] = JobGroup{s_off + i, e - i, b, jobs[i].depth};
-        i = e;
-      }
+    if (warp < nb) {
+      const ReqView R = req_view(smem + warp * rstride, RL);
+      const bool done = R.ctl->s >= n;
+      if ((t & 31) == 0) s_done[warp] = done;
+      if (!done)
+        request_step(R, b0 + warp * G, n, M, p.max_depth, X, KM, kla,
+                     reinterpret_cast<Job*>(smem + warp * rstride + RL.jobs), p.hdr);
     }
     __syncthreads();
-    for (int q = t; q < st.njobs; q += kThreads) next[s_off + q] = jobs[q];
-    if (p.xact_on) {  // the picks' GRU inputs as the tensor-core GRU reads them: [emb | hi(h_parent) | lo(h_parent)]
-      const int E = p.E, H = p.H, Kx = E + 2 * H;
-      for (int q = 0; q < st.njobs; ++q) {
-        const Job jb = jobs[q];
-        unsigned short* xr = p.xact + static_cast<size_t>(s_off + q) * Kx;
-        const uint4* er = reinterpret_cast<const uint4*>(static_cast<const unsigned short*>(p.emb) +
-                                                         static_cast<size_t>(jb.token) * E);
-        for (int i = t; i < E / 8; i += kThreads) reinterpret_cast<uint4*>(xr)[i] = __ldg(er + i);
-        const float2* hp = reinterpret_cast<const float2*>(p.hs + (static_cast<size_t>(b) * X + jb.pslot) * H);
-        for (int i = t; i < H / 2; i += kThreads) {
-          const float2 v = __ldcg(hp + i);
-          uint32_t hi, lo;
-          split_bf16x2(v.x, v.y, hi, lo);
-          reinterpret_cast<uint32_t*>(xr + E)[i] = hi;
-          reinterpret_cast<uint32_t*>(xr + E + H)[i] = lo;
+    for (int i = 0; i < nb; ++i) {
+      if (s_done[i]) continue;  // uniform
+      const int b = b0 + i * G;
+      unsigned char* base = smem + i * rstride;
+      const ReqView R = req_view(base, RL);
+      Job* jobs = reinterpret_cast<Job*>(base + RL.jobs);
+      const ReqCtl st = *R.ctl;
+      if (t == 0 && st.njobs > 0) {
+        // the picks in order of depth (stable): a request's expansions at one block position sit together in the
+        // packed list, and each such run is a group of the children phase
+        for (int q = 1; q < st.njobs; ++q)
+          for (int k = q; k > 0 && jobs[k - 1].depth > jobs[k].depth; --k) {
+            const Job tmp = jobs[k];
+            jobs[k] = jobs[k - 1];
+            jobs[k - 1] = tmp;
+          }
+        int ng = 1;
+        for (int q = 1; q < st.njobs; ++q) ng += jobs[q].depth != jobs[q - 1].depth;
+        s_off = atomicAdd(p.jobcount + w + 1, st.njobs);
+        int gi = atomicAdd(p.groupcount + w + 1, ng);
+        JobGroup* gnext = p.grouplist + static_cast<size_t>((w + 1) & 1) * p.B * kla;
+        for (int q = 0; q < st.njobs;) {
+          int e = q + 1;
+          while (e < st.njobs && jobs[e].depth == jobs[q].depth) ++e;
+          gnext[gi++] = JobGroup{s_off + q, e - q, b, jobs[q].depth};
+          q = e;
         }
       }
-      asm volatile("fence.proxy.async.global;" ::: "memory");  // read by TMA (async proxy) after the next barrier
-    }
-    if (st.s >= n) {  // finished: the outputs, and each node's ancestor-mask row by walking its parent chain
-      resolve_parents(R.pops, R.popidx, n, t, kThreads);
       __syncthreads();
-      const size_t o = static_cast<size_t>(b) * n;
-      for (int i = t; i < n; i += kThreads) {
-        const PopRec r = R.pops[i];
-        p.tokens[o + i] = r.token;
-        p.parents[o + i] = r.parent;
-        p.depth[o + i] = r.depth;
-        p.scores[o + i] = r.score;
+      for (int q = t; q < st.njobs; q += kThreads) next[s_off + q] = jobs[q];
+      if (p.xact_on) {  // the picks' GRU inputs as the tensor-core GRU reads them: [emb | hi(h_parent) | lo(h_parent)]
+        const int E = p.E, H = p.H, Kx = E + 2 * H;
+        for (int q = 0; q < st.njobs; ++q) {
+          const Job jb = jobs[q];
+          unsigned short* xr = p.xact + static_cast<size_t>(s_off + q) * Kx;
+          const uint4* er = reinterpret_cast<const uint4*>(static_cast<const unsigned short*>(p.emb) +
+                                                           static_cast<size_t>(jb.token) * E);
+          for (int k = t; k < E / 8; k += kThreads) reinterpret_cast<uint4*>(xr)[k] = __ldg(er + k);
+          const float2* hp = reinterpret_cast<const float2*>(p.hs + (static_cast<size_t>(b) * X + jb.pslot) * H);
+          for (int k = t; k < H / 2; k += kThreads) {
+            const float2 v = __ldcg(hp + k);
+            uint32_t hi, lo;
+            split_bf16x2(v.x, v.y, hi, lo);
+            reinterpret_cast<uint32_t*>(xr + E)[k] = hi;
+            reinterpret_cast<uint32_t*>(xr + E + H)[k] = lo;
+          }
+        }
+        asm volatile("fence.proxy.async.global;" ::: "memory");  // read by TMA (async proxy) after the next barrier
       }
-      for (int i = t; i < n * n; i += kThreads) {
-        const int row = i / n, c = i % n;
-        int a = row;
-        for (int hops = 0; a > c && hops < n; ++hops) a = R.pops[a].parent;  // parents precede their children
-        p.mask[(o + row) * n + c] = a == c;
+      if (st.s >= n) {  // finished: the outputs, and each node's ancestor-mask row by walking its parent chain
+        resolve_parents(R.pops, R.popidx, n, t, kThreads);
+        __syncthreads();
+        const size_t o = static_cast<size_t>(b) * n;
+        for (int k = t; k < n; k += kThreads) {
+          const PopRec r = R.pops[k];
+          p.tokens[o + k] = r.token;
+          p.parents[o + k] = r.parent;
+          p.depth[o + k] = r.depth;
+          p.scores[o + k] = r.score;
+        }
+        for (int k = t; k < n * n; k += kThreads) {
+          const int row = k / n, c = k % n;
+          int a = row;
+          for (int hops = 0; a > c && hops < n; ++hops) a = R.pops[a].parent;  // parents precede their children
+          p.mask[(o + row) * n + c] = a == c;
+        }
+      }
+      // the state block goes back (one bulk copy; all of the batch's complete before the buffers are reused)
+      __syncthreads();
+      if (t == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        bulk_s2g(p.rstate + static_cast<size_t>(b) * RL.bytes, base, static_cast<unsigned>(RL.bytes));
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
       }
     }
-    // the state block goes back (one bulk copy; complete before the shared buffers are reused)
-    __syncthreads();
     if (t == 0) {
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      bulk_s2g(gstate, smem, static_cast<unsigned>(RL.bytes));
-      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
       asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-      asm volatile("fence.proxy.async.global;" ::: "memory");  // other CTAs write new children lists into it next
+      asm volatile("fence.proxy.async.global;" ::: "memory");  // other CTAs write new children lists into them next
     }
   }
   return true;
@@ -1150,7 +1171,7 @@ __device__ void run_waves(const Params& p, const TmaMaps& maps, unsigned char* s
     ++waves;
     expansions += static_cast<unsigned>(rows);
     gather_bytes += static_cast<uint64_t>(p.group_mma ? __ldcg(p.groupcount + w) : rows) * p.M * p.H * (p.bf16 ? 2 : 4);
-    if (p.B < static_cast<int>(G)) {  // children computed by other CTAs: wait for all of them
+    if (p.group_mma ? !p.own_groups : p.B < static_cast<int>(G)) {  // children computed by other CTAs: wait for them
       target += G;
       if (!counter_barrier(p.hdr, target, p.timeout_ns, s_flag)) return;
     } else {
@@ -1367,6 +1388,19 @@ dt_status build_trees(int B, int K, int V, int M, int n, int max_depth, float T,
   size_t smem = smem_bytes(gemm, M, n, H, p.lookahead, p.bf16 ? 2 : 4, static_cast<size_t>(di.optin) - 2048,
                            &p.rows_smem);
   // the children phase by groups on the tensor cores when its buffers fit the same budget
+  // groups spread over all CTAs (g mod G) whatever the batch: a request's groups on its owner CTA left the CTAs that
+  // own two requests, and the tail waves' few groups, on one CTA each (c4: 75-85 us against a 50 us mean)
+  p.own_groups = false;
+  {  // requests a CTA steps at once in the control phase: the ones it owns, as many as the shared memory holds
+    const ReqLayout RL = req_layout(n, p.xslots, M < n ? M : n, p.lookahead);
+    const size_t rstride = (RL.bytes + 127) / 128 * 128;
+    const int owned = (B + di.sms - 1) / di.sms;
+    const int fit = static_cast<int>((static_cast<size_t>(di.optin) - 2048) / rstride);
+    p.ctl_conc = owned < fit ? owned : fit;
+    if (p.ctl_conc > kWarps) p.ctl_conc = kWarps;
+    if (p.ctl_conc < 1) p.ctl_conc = 1;
+    if (smem < rstride * p.ctl_conc) smem = rstride * p.ctl_conc;
+  }
   p.group_mma = p.bf16 && H % 16 == 0 && M <= 128 &&
                 group_smem(M, H).bytes + 2048 <= static_cast<size_t>(di.optin);
   if (p.group_mma && group_smem(M, H).bytes > smem) smem = group_smem(M, H).bytes;
