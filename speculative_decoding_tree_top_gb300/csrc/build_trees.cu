@@ -436,10 +436,13 @@ struct TmaMaps {
   CUtensorMap wih;  // [3H][E] bf16, box 64 x 32
   CUtensorMap whh;  // [3H][H] bf16, box 64 x 32
 };
-constexpr int kUmmaRows = 128, kUmmaUnits = 32, kUmmaBK = 64, kUmmaStages = 8;
+constexpr int kUmmaRows = 128, kUmmaUnits = 32, kUmmaBK = 64, kUmmaStages = 7;
 constexpr int kUmmaA = kUmmaRows * kUmmaBK * 2;            // 16 KB
-constexpr int kUmmaB = 3 * kUmmaUnits * kUmmaBK * 2;       // 12 KB
-constexpr int kUmmaStage = kUmmaA + kUmmaB;                // 28 KB (a multiple of 1024)
+// The B tile of a K block: the weight rows of the gate columns [r | z | n_in | n_h] of the tile's units, the set a
+// block does not touch (n_h for an embedding block, n_in for a hidden one) read as zeros, so that one MMA of N = 128
+// covers the block: the zeros add exact zeros to the other gate's sums.
+constexpr int kUmmaB = 4 * kUmmaUnits * kUmmaBK * 2;       // 16 KB
+constexpr int kUmmaStage = kUmmaA + kUmmaB;                // 32 KB (a multiple of 1024)
 constexpr size_t kUmmaSmem = static_cast<size_t>(kUmmaStages) * kUmmaStage + 1024;  // + alignment slack
 constexpr int kTmemCols = 512;  // kSplits partials of 128 columns
 
@@ -541,8 +544,13 @@ __device__ bool umma_gru_phase(const Params& p, const TmaMaps& maps, const Job* 
         const int acol = emb ? kb * kUmmaBK : E + (kb - nE) * kUmmaBK;                   // hi blocks, then lo blocks
         const int wcol = emb ? kb * kUmmaBK : ((kb - nE) % nH) * kUmmaBK;
         tma_load_2d(a, &maps.x, acol, row0, &ring.full[st]);
-        for (int g = 0; g < 3; ++g)
-          tma_load_2d(bsm + g * kUmmaUnits * 128, emb ? &maps.wih : &maps.whh, wcol, g * H + u0, &ring.full[st]);
+        // gate slot g of the tile takes weight rows g H + u0 (r, z, and n_in or n_h); the block's unused slot reads
+        // rows 3 H .. past the weights' end: zeros
+        const CUtensorMap* wm = emb ? &maps.wih : &maps.whh;
+        for (int g = 0; g < 4; ++g) {
+          const int src = g < 2 ? g : (g == 2) == emb ? 2 : 3;
+          tma_load_2d(bsm + g * kUmmaUnits * 128, wm, wcol, src * H + u0, &ring.full[st]);
+        }
       }
     } else if (warp == 1 && lane == 0) {  // MMA issuer: partial s into TMEM columns [128 (s - s_lo), +128)
       for (int kb = kb_lo; kb < kb_hi && ok; ++kb) {
@@ -552,21 +560,13 @@ __device__ bool umma_gru_phase(const Params& p, const TmaMaps& maps, const Job* 
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         int sp = s_lo;  // the partial this block belongs to
         while (sp + 1 < s_hi && kb >= split_begin(sp + 1, nkb)) ++sp;
-        const int sb = split_begin(sp, nkb), hb = sb > nE ? sb : nE;  // its first block, its first hidden block
+        const int sb = split_begin(sp, nkb);  // its first block
         const uint32_t d = ring.tmem + 128u * static_cast<uint32_t>(sp - s_lo);
         const uint32_t a = smem_u32(base + st * kUmmaStage), bsm = a + kUmmaA;
-        const bool emb = kb < nE;
 #pragma unroll
-        for (int k = 0; k < kUmmaBK / 16; ++k) {
-          const uint64_t da = umma_desc_sw128(a + 32 * k);
-          if (emb) {
-            umma_f16(d, da, umma_desc_sw128(bsm + 32 * k), umma_idesc(3 * kUmmaUnits), (kb > sb || k > 0) ? 1u : 0u);
-          } else {
-            umma_f16(d, da, umma_desc_sw128(bsm + 32 * k), umma_idesc(2 * kUmmaUnits), (kb > sb || k > 0) ? 1u : 0u);
-            umma_f16(d + 3 * kUmmaUnits, da, umma_desc_sw128(bsm + 2 * kUmmaUnits * 128 + 32 * k),
-                     umma_idesc(kUmmaUnits), (kb > hb || k > 0) ? 1u : 0u);
-          }
-        }
+        for (int k = 0; k < kUmmaBK / 16; ++k)
+          umma_f16(d, umma_desc_sw128(a + 32 * k), umma_desc_sw128(bsm + 32 * k), umma_idesc(4 * kUmmaUnits),
+                   (kb > sb || k > 0) ? 1u : 0u);
         umma_commit(&ring.empty[st]);  // the stage is free once these MMAs have read it
       }
       if (ok) umma_commit(ring.done);  // and the partials are complete after the last block's MMAs
