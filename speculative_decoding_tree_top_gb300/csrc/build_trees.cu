@@ -702,9 +702,23 @@ __device__ bool children_groups(const Params& p, int w, const Job* jl, unsigned 
   if (!own && static_cast<int>(blockIdx.x) < p.B * p.lookahead) first_group = gl[blockIdx.x];
   const int ngroups = __ldcg(p.groupcount + w);
   int* s_mine = reinterpret_cast<int*>(smem + GS.mine);
+  // the hidden states the bulk copies read were written by the GRU phase through the generic proxy, before the last
+  // grid barrier: one proxy fence for the whole phase
+  if (t == 0) asm volatile("fence.proxy.async.global;" ::: "memory");
+  // Spread mode: the ids and base logits of this CTA's next group are loaded into registers (thread m < M: candidate
+  // m) a group ahead, so that a group's row copies go out at once; its rows are asked of L2 one group ahead too.
+  const size_t ngs = static_cast<size_t>(gridDim.x);
+  auto cand_pos = [&](const JobGroup& g) { return (static_cast<size_t>(g.b) * p.K + g.depth) * M; };
+  int nid = 0;
+  float nval = 0.f;
+  if (!own && static_cast<int>(blockIdx.x) < ngroups && t < M) {
+    nid = __ldg(p.ids + cand_pos(first_group) + t);
+    nval = __ldg(p.vals + cand_pos(first_group) + t);
+  }
+  JobGroup next_group{};
   for (int g0 = own ? 0 : blockIdx.x; g0 < ngroups; g0 += own ? kThreads : gridDim.x) {
     int nmine = 1;
-    if (!own && g0 != static_cast<int>(blockIdx.x)) first_group = gl[g0];  // later rounds of the spread mode
+    if (!own && g0 != static_cast<int>(blockIdx.x)) first_group = next_group;  // later rounds of the spread mode
     if (own) {  // the groups of this CTA's requests in this batch, found by every thread at once
       __syncthreads();
       if (t == 0) s_mine[kThreads] = 0;
@@ -717,18 +731,30 @@ __device__ bool children_groups(const Params& p, int w, const Job* jl, unsigned 
     for (int k = 0; k < nmine; ++k) {
       const JobGroup gr = own ? gl[s_mine[k]] : first_group;
       const int J = gr.count;
-      const size_t pos = (static_cast<size_t>(gr.b) * p.K + gr.depth) * M;
+      const size_t pos = cand_pos(gr);
       __syncthreads();  // the previous group is done with the shared buffers
-      for (int m = t; m < M; m += kThreads) {  // ids and base logits of the group's block position
-        ids[m] = valid_id(p, __ldg(p.ids + pos + m));
-        vals[m] = __ldg(p.vals + pos + m);
+      if (own) {
+        for (int m = t; m < M; m += kThreads) {  // ids and base logits of the group's block position
+          ids[m] = valid_id(p, __ldg(p.ids + pos + m));
+          vals[m] = __ldg(p.vals + pos + m);
+        }
+      } else {
+        if (t < M) {  // loaded a group ahead
+          ids[t] = valid_id(p, nid);
+          vals[t] = nval;
+        }
+        const bool more = g0 + static_cast<int>(ngs) < ngroups;  // the next group's ids, for the next round
+        if (more) {
+          next_group = gl[g0 + ngs];
+          if (t < M) {
+            nid = __ldg(p.ids + cand_pos(next_group) + t);
+            nval = __ldg(p.vals + cand_pos(next_group) + t);
+          }
+        }
       }
       __syncthreads();
-      if (warp == 0) {  // the group's hidden states (written by the GRU phase through the generic proxy) and rows
-        if (lane == 0) {
-          asm volatile("fence.proxy.async.global;" ::: "memory");
-          mbar_expect_tx(bar, static_cast<unsigned>(J * H * 4) + rb * static_cast<unsigned>(M));
-        }
+      if (warp == 0) {  // the group's hidden states and rows
+        if (lane == 0) mbar_expect_tx(bar, static_cast<unsigned>(J * H * 4) + rb * static_cast<unsigned>(M));
         __syncwarp();
         if (lane < J)
           bulk_g2s(hbuf + static_cast<size_t>(lane) * H,
@@ -738,16 +764,10 @@ __device__ bool children_groups(const Params& p, int w, const Job* jl, unsigned 
           bulk_g2s(rows_s + static_cast<size_t>(m) * SW, static_cast<const char*>(p.w_c) + static_cast<size_t>(ids[m]) * rb,
                    rb, bar);
       }
-      if (!own && g0 + static_cast<int>(gridDim.x) < ngroups && warp == 1) {  // the next group's rows, into L2
-        const JobGroup ng = gl[g0 + gridDim.x];
-        const size_t npos = (static_cast<size_t>(ng.b) * p.K + ng.depth) * M;
-        for (int m = lane; m < M; m += 32) {
-          const int id = __ldg(p.ids + npos + m);
-          if (static_cast<unsigned>(id) < static_cast<unsigned>(p.V))
-            prefetch_l2(static_cast<const char*>(p.w_c) + static_cast<size_t>(id) * rb, rb);
-        }
-      }
       if (!__syncthreads_and(wait_copies(p, bar, bar_uses))) return false;
+      // the next group's rows into L2 while this one computes (its ids are in registers by now)
+      if (!own && g0 + static_cast<int>(ngs) < ngroups && t < M && static_cast<unsigned>(nid) < static_cast<unsigned>(p.V))
+        prefetch_l2(static_cast<const char*>(p.w_c) + static_cast<size_t>(nid) * rb, rb);
       // Z[M][8] = rows . [h_0 .. h_7], columns j >= J unused. The 16-row tiles times `ks` K parts make the warps'
       // work (ks = 8 / tiles, so every warp has a share when M < 128); each warp runs two accumulator chains (even
       // and odd k16 steps) and stores its partial tile; the partials are then added in a fixed order (part 0 first,
