@@ -999,8 +999,8 @@ __device__ bool control_phase(const Params& p, int w, unsigned char* smem, uint6
   const size_t rstride = (RL.bytes + 127) / 128 * 128;  // one shared-memory region per request of a batch
   const int G = static_cast<int>(gridDim.x), C = p.ctl_conc;
   Job* next = p.joblist + static_cast<size_t>((w + 1) & 1) * p.B * kla;
-  __shared__ int s_off;
-  __shared__ int s_done[kWarps];  // the request was finished in an earlier wave
+  __shared__ int s_off[kWarps], s_cnt[kWarps];  // a batch request's place in the next wave's list, its picks
+  __shared__ int s_done[kWarps];                  // the request was finished in an earlier wave
   // The requests this CTA owns (b = blockIdx.x + i G), up to C at a time: their state blocks come in by bulk copies
   // on one barrier, warp i runs request i's best-first step, and the rest follows request by request.
   for (int b0 = blockIdx.x; b0 < p.B; b0 += G * C) {
@@ -1024,65 +1024,111 @@ __device__ bool control_phase(const Params& p, int w, unsigned char* smem, uint6
                      reinterpret_cast<Job*>(smem + warp * rstride + RL.jobs), p.hdr);
     }
     __syncthreads();
-    for (int i = 0; i < nb; ++i) {
-      if (s_done[i]) continue;  // uniform
-      const int b = b0 + i * G;
-      unsigned char* base = smem + i * rstride;
-      const ReqView R = req_view(base, RL);
-      Job* jobs = reinterpret_cast<Job*>(base + RL.jobs);
-      const ReqCtl st = *R.ctl;
-      if (t == 0 && st.njobs > 0) {
-        // the picks in order of depth (stable): a request's expansions at one block position sit together in the
-        // packed list, and each such run is a group of the children phase
-        for (int q = 1; q < st.njobs; ++q)
+    // the batch's picks: thread 0 orders each request's picks by depth (stable: a request's expansions at one block
+    // position sit together in the packed list, and each such run is a group of the children phase) and reserves
+    // their places in the next wave's lists
+    if (t == 0)
+      for (int i = 0; i < nb; ++i) {
+        s_off[i] = 0;
+        s_cnt[i] = 0;
+        if (s_done[i]) continue;
+        unsigned char* base = smem + i * rstride;
+        Job* jobs = reinterpret_cast<Job*>(base + RL.jobs);
+        const int nj = req_view(base, RL).ctl->njobs;
+        if (nj <= 0) continue;
+        for (int q = 1; q < nj; ++q)
           for (int k = q; k > 0 && jobs[k - 1].depth > jobs[k].depth; --k) {
             const Job tmp = jobs[k];
             jobs[k] = jobs[k - 1];
             jobs[k - 1] = tmp;
           }
         int ng = 1;
-        for (int q = 1; q < st.njobs; ++q) ng += jobs[q].depth != jobs[q - 1].depth;
-        s_off = atomicAdd(p.jobcount + w + 1, st.njobs);
+        for (int q = 1; q < nj; ++q) ng += jobs[q].depth != jobs[q - 1].depth;
+        const int off = atomicAdd(p.jobcount + w + 1, nj);
         int gi = atomicAdd(p.groupcount + w + 1, ng);
         JobGroup* gnext = p.grouplist + static_cast<size_t>((w + 1) & 1) * p.B * kla;
-        for (int q = 0; q < st.njobs;) {
+        for (int q = 0; q < nj;) {
           int e = q + 1;
-          while (e < st.njobs && jobs[e].depth == jobs[q].depth) ++e;
-          gnext[gi++] = JobGroup{s_off + q, e - q, b, jobs[q].depth};
+          while (e < nj && jobs[e].depth == jobs[q].depth) ++e;
+          gnext[gi++] = JobGroup{off + q, e - q, b0 + i * G, jobs[q].depth};
           q = e;
         }
+        s_off[i] = off;
+        s_cnt[i] = nj;
       }
-      __syncthreads();
-      for (int q = t; q < st.njobs; q += kThreads) next[s_off + q] = jobs[q];
-      if (p.xact_on) {  // the picks' GRU inputs as the tensor-core GRU reads them: [emb | hi(h_parent) | lo(h_parent)]
-        const int E = p.E, H = p.H, Kx = E + 2 * H;
-        for (int q = 0; q < st.njobs; ++q) {
-          const Job jb = jobs[q];
-          unsigned short* xr = p.xact + static_cast<size_t>(s_off + q) * Kx;
-          const uint4* er = reinterpret_cast<const uint4*>(static_cast<const unsigned short*>(p.emb) +
-                                                           static_cast<size_t>(jb.token) * E);
-          for (int k = t; k < E / 8; k += kThreads) reinterpret_cast<uint4*>(xr)[k] = __ldg(er + k);
-          const float2* hp = reinterpret_cast<const float2*>(p.hs + (static_cast<size_t>(b) * X + jb.pslot) * H);
-          for (int k = t; k < H / 2; k += kThreads) {
-            const float2 v = __ldcg(hp + k);
-            uint32_t hi, lo;
-            split_bf16x2(v.x, v.y, hi, lo);
-            reinterpret_cast<uint32_t*>(xr + E)[k] = hi;
-            reinterpret_cast<uint32_t*>(xr + E + H)[k] = lo;
+    __syncthreads();
+    int total_jobs = 0;
+    for (int i = 0; i < nb; ++i) total_jobs += s_cnt[i];
+    // the picks into the next wave's packed list, and their GRU inputs as the tensor-core GRU reads them
+    // ([emb | hi(h_parent) | lo(h_parent)]): every pick of the batch at once, each thread's loads issued together
+    for (int q = t; q < total_jobs; q += kThreads) {
+      int i = 0, qq = q;
+      while (qq >= s_cnt[i]) qq -= s_cnt[i++];
+      next[s_off[i] + qq] = reinterpret_cast<const Job*>(smem + i * rstride + RL.jobs)[qq];
+    }
+    if (p.xact_on && total_jobs > 0) {
+      const int E = p.E, H = p.H, Kx = E + 2 * H, ne = E / 8, nh = H / 2, per = ne + nh;
+      const int items = total_jobs * per;
+      constexpr int kBatch = 8;
+      for (int i0 = t; i0 < items; i0 += kBatch * kThreads) {
+        uint4 ve[kBatch];
+        float2 vh[kBatch];
+        unsigned short* dst[kBatch];
+        int kind[kBatch];  // 0: none, 1: an embedding chunk, 2: a hidden-state pair
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int idx = i0 + u * kThreads;
+          kind[u] = 0;
+          if (idx < items) {
+            int qi = idx / per, r = 0;
+            const int k = idx % per;
+            while (qi >= s_cnt[r]) qi -= s_cnt[r++];
+            const Job jb = reinterpret_cast<const Job*>(smem + r * rstride + RL.jobs)[qi];
+            unsigned short* xr = p.xact + static_cast<size_t>(s_off[r] + qi) * Kx;
+            if (k < ne) {
+              ve[u] = __ldg(reinterpret_cast<const uint4*>(static_cast<const unsigned short*>(p.emb) +
+                                                           static_cast<size_t>(jb.token) * E) + k);
+              dst[u] = xr + 8 * k;
+              kind[u] = 1;
+            } else {
+              const int kk = k - ne;
+              vh[u] = __ldcg(reinterpret_cast<const float2*>(
+                                 p.hs + (static_cast<size_t>(b0 + r * G) * X + jb.pslot) * H) + kk);
+              dst[u] = xr + E + 2 * kk;
+              kind[u] = 2;
+            }
           }
         }
-        asm volatile("fence.proxy.async.global;" ::: "memory");  // read by TMA (async proxy) after the next barrier
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          if (kind[u] == 1) {
+            *reinterpret_cast<uint4*>(dst[u]) = ve[u];
+          } else if (kind[u] == 2) {
+            uint32_t hi, lo;
+            split_bf16x2(vh[u].x, vh[u].y, hi, lo);
+            *reinterpret_cast<uint32_t*>(dst[u]) = hi;
+            *reinterpret_cast<uint32_t*>(dst[u] + H) = lo;
+          }
+        }
       }
+      asm volatile("fence.proxy.async.global;" ::: "memory");  // read by TMA (async proxy) after the next barrier
+    }
+    for (int i = 0; i < nb; ++i) {
+      if (s_done[i]) continue;  // uniform
+      const int b = b0 + i * G;
+      unsigned char* base = smem + i * rstride;
+      const ReqView R = req_view(base, RL);
+      const ReqCtl st = *R.ctl;
       if (st.s >= n) {  // finished: the outputs, and each node's ancestor-mask row by walking its parent chain
         resolve_parents(R.pops, R.popidx, n, t, kThreads);
         __syncthreads();
         const size_t o = static_cast<size_t>(b) * n;
         for (int k = t; k < n; k += kThreads) {
-          const PopRec r = R.pops[k];
-          p.tokens[o + k] = r.token;
-          p.parents[o + k] = r.parent;
-          p.depth[o + k] = r.depth;
-          p.scores[o + k] = r.score;
+          const PopRec rr = R.pops[k];
+          p.tokens[o + k] = rr.token;
+          p.parents[o + k] = rr.parent;
+          p.depth[o + k] = rr.depth;
+          p.scores[o + k] = rr.score;
         }
         for (int k = t; k < n * n; k += kThreads) {
           const int row = k / n, c = k % n;
