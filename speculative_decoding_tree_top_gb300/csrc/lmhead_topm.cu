@@ -423,6 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) lh_block_kernel(LbParams p, const
   int* s_cnt = reinterpret_cast<int*>(s_thr + p.R);                  // [R]
   __shared__ uint64_t full[kMaxStages], empty[kMaxStages], tfull[2], tempty[2];
   __shared__ uint32_t s_tmem;
+  __shared__ unsigned s_issued, s_used;  // stage loads issued and waited for (failure drain)
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int G = static_cast<int>(gridDim.x), bid = static_cast<int>(blockIdx.x);
   const int R = p.R, W = p.W, S = p.stages, nkb = p.D / kBK, nitem = p.nitem, gs = p.gs;
@@ -447,6 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1) lh_block_kernel(LbParams p, const
       mbar_init(&tempty[i], 4);  // one arrival per epilogue warp
     }
     mbar_fence_init();
+    s_issued = s_used = 0u;
   }
   if (!kPool) {
     for (int r = t; r < R; r += kThreads) {
@@ -481,6 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1) lh_block_kernel(LbParams p, const
         mbar_expect_tx(&full[st], tx);
         tma_load_2d(a, wm, kb * kBK, row0 + i * kTileV, &full[st]);
         tma_load_2d(a + kAStage, &maps.h, kb * kBK, j * W, &full[st]);
+        s_issued = n + 1u;
       }
     }
   } else if (warp == 1 && lane == 0) {  // MMA issuer: item it accumulates in TMEM buffer it % 2
@@ -495,6 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1) lh_block_kernel(LbParams p, const
         const unsigned st = n % S, use = n / S;
         ok = mbar_wait(&full[st], use & 1u, kBudgetNs);
         if (!ok) break;
+        s_used = n + 1u;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t a = smem_u32(ring + st * stage), bb = a + static_cast<uint32_t>(kAStage);
 #pragma unroll
@@ -584,6 +588,8 @@ __global__ void __launch_bounds__(kThreads, 1) lh_block_kernel(LbParams p, const
   if (!ok && t == 0) {
     record_error(p.hdr, DT_ERR_TIMEOUT);
     atomicExch(&p.hdr->abort, 1u);
+    // stage loads issued but never waited for must land before the CTA leaves (bounded)
+    for (unsigned n = s_used; n < s_issued; ++n) mbar_wait(&full[n % S], (n / S) & 1u, kBudgetNs);
   }
   if (__syncthreads_or(nan) && t == 0) record_error(p.hdr, DT_ERR_NUMERIC);
   if (!kPool)  // the rows of this CTA's hidden blocks: their lists of this group

@@ -146,6 +146,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_attn_tc(TaParams p, const 
   __shared__ uint64_t kv_full[kTcStages], kv_empty[kTcStages], s_full[2], p_full[2], o_done[2];
   __shared__ uint64_t q_full[2], q_empty[2], o_free[2];
   __shared__ uint32_t s_tmem;
+  __shared__ unsigned s_kv_issued, s_kv_used, s_q_issued, s_q_used;  // copies issued and consumed (failure drain)
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   if (t == 0) {
     for (int i = 0; i < kTcStages; ++i) {
@@ -162,6 +163,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_attn_tc(TaParams p, const 
     }
     mbar_fence_init();
   }
+  if (t == 0) s_kv_issued = s_kv_used = s_q_issued = s_q_used = 0u;
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
                  "r"(512) : "memory");
@@ -188,6 +190,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_attn_tc(TaParams p, const 
       mbar_expect_tx(&q_full[qb], qtx);
       tma_load_4d(qd, &maps.q, 0, sg.kvh * p.G, 0, sg.b, &q_full[qb]);
       tma_load_4d(qd + kTcBox, &maps.q, 64, sg.kvh * p.G, 0, sg.b, &q_full[qb]);
+      s_q_issued = static_cast<unsigned>(si) + 1u;
       for (int j = 0; j < sg.nblk && ok; ++j, ++g) {
         const unsigned st = g % kTcStages, use = g / kTcStages;
         if (use > 0) ok = mbar_wait(&kv_empty[st], (use - 1) & 1u, kTcBudgetNs);
@@ -199,6 +202,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_attn_tc(TaParams p, const 
         tma_load_3d(d + kTcBox, &maps.k, 64, key, sg.pair, &kv_full[st]);
         tma_load_3d(d + 2 * kTcBox, &maps.v, 0, key, sg.pair, &kv_full[st]);
         tma_load_3d(d + 3 * kTcBox, &maps.v, 64, key, sg.pair, &kv_full[st]);
+        s_kv_issued = g + 1u;
       }
     }
   } else if (warp == 3 && lane == 0) {  // MMA issuer
@@ -210,12 +214,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_attn_tc(TaParams p, const 
       const unsigned qb = static_cast<unsigned>(si) & 1u;
       const uint32_t aq = smem_u32(sq + qb * kTcQBytes), to = tmem + 128u + 128u * qb;
       ok = mbar_wait(&q_full[qb], static_cast<unsigned>(si >> 1) & 1u, kTcBudgetNs);
+      if (ok) s_q_used = static_cast<unsigned>(si) + 1u;
       // this segment's O buffer was read out by the softmax of segment si - 2
       if (ok && si >= 2) ok = mbar_wait(&o_free[qb], static_cast<unsigned>((si >> 1) - 1) & 1u, kTcBudgetNs);
       if (!ok) break;
       auto issue_s = [&](unsigned gs) {  // S = Q K^T of block gs into TMEM columns [64 (gs % 2), +64)
         const unsigned st = gs % kTcStages;
         if (!mbar_wait(&kv_full[st], (gs / kTcStages) & 1u, kTcBudgetNs)) return false;
+        s_kv_used = gs + 1u;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t bk = smem_u32(skv + st * kTcStageBytes);
 #pragma unroll
@@ -363,7 +369,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_attn_tc(TaParams p, const 
     }
   }
   ok = __syncthreads_and(ok);
-  if (!ok && t == 0) record_error(hdr, DT_ERR_TIMEOUT);
+  if (!ok && t == 0) {
+    record_error(hdr, DT_ERR_TIMEOUT);
+    // copies issued but never waited for must land before the CTA leaves: wait for them too (bounded)
+    for (unsigned g = s_kv_used; g < s_kv_issued; ++g) mbar_wait(&kv_full[g % kTcStages], (g / kTcStages) & 1u, kTcBudgetNs);
+    for (unsigned q = s_q_used; q < s_q_issued; ++q) mbar_wait(&q_full[q & 1u], (q >> 1) & 1u, kTcBudgetNs);
+  }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
