@@ -340,8 +340,8 @@ struct Params {
   int* jobcount;    // [xslots + 2] expansions per wave (large-batch builder)
   JobGroup* grouplist;  // [2][B * lookahead] the wave's expansions of one request at one depth (large-batch builder)
   int* groupcount;      // [xslots + 2] groups per wave (large-batch builder)
-  bool own_groups;  // large-batch builder, group_mma: a group goes to its request's owner CTA (else CTA g mod G)
   int ctl_conc;     // large-batch builder: requests a CTA steps at once in the control phase
+  int ctl_stage;    // ... and its staging slots for the picks' activation rows (tcgen05 GRU)
   bool group_mma;   // large-batch builder: a group's corrections as one tensor-core product (bf16, H % 16 == 0,
                     // M <= 128, the group's rows in shared memory)
   unsigned short* xact;  // [B * lookahead][E + 2H] bf16 GRU inputs of the next wave's expansions (tensor-core GRU)

@@ -394,7 +394,7 @@ constexpr size_t kFrontierRowsCap = 160 * 1024;  // gathered rows kept in shared
 // row stride padded by 16 bytes, so the MMA's row fragments fall in distinct banks), the corrected logits [8][M], and
 // per expansion its children [8][M] and their sibling keys [8][M].
 struct GroupSmem {
-  size_t h, ids, vals, rows, z, zpart, kraw, keys, mine, bytes;
+  size_t bfrag, h, ids, vals, rows, z, zpart, kraw, keys, jobs, ctl, bytes;
 };
 __host__ __device__ inline GroupSmem group_smem(int M, int H) {
   GroupSmem L{};
@@ -404,15 +404,17 @@ __host__ __device__ inline GroupSmem group_smem(int M, int H) {
     o = (o + bytes + 15) / 16 * 16;
     return at;
   };
+  L.bfrag = take(sizeof(uint4) * 2 * static_cast<size_t>(H));  // [H / 16 k16 steps][32 lanes]
   L.h = take(sizeof(float) * kLargeLookahead * H);
-  L.ids = take(sizeof(int) * round4(M));
-  L.vals = take(sizeof(float) * round4(M));
+  L.ids = take(sizeof(int) * 2 * round4(M));
+  L.vals = take(sizeof(float) * 2 * round4(M));
   L.rows = take(sizeof(unsigned short) * static_cast<size_t>(M) * (H + 8));
   L.z = take(sizeof(float) * kLargeLookahead * round4(M));
   L.zpart = take(sizeof(float) * kWarps * kLargeLookahead * 16);  // one 16 x 8 partial tile per warp
   L.kraw = take(sizeof(Node) * kLargeLookahead * M);
   L.keys = take(sizeof(unsigned long long) * kLargeLookahead * M);
-  L.mine = take(sizeof(int) * (kThreads + 1));  // own mode: this CTA's groups among the next kThreads of the list
+  L.jobs = take(sizeof(Job) * 3 * kLargeLookahead);
+  L.ctl = take(sizeof(ReqCtl) * 3);
   L.bytes = o;
   return L;
 }
@@ -671,187 +673,218 @@ __device__ __forceinline__ bool wait_copies(const Params& p, uint64_t* bar, unsi
 }
 
 // ---- phase B1 by groups: one request's expansions at one block position share that position's correction rows --
-// The group's M rows W_c[ids] are gathered once (bulk copies on an mbarrier, with the group's hidden states) and the
-// corrections of all its J expansions come out of one tensor-core product Z[M][J] = W_c[ids] . [h_1 .. h_J]:
-// mma.sync m16n8k16, the rows as A (a warp per 16 rows), the hidden states as the n8 B tile, split into bf16 hi + lo
-// pairs (as the GRU's hidden side). Column j of Z depends on h_j alone, summed in a fixed order, so an expansion's
-// children do not depend on which expansions share its group. Then one warp per expansion: the restricted
-// log-softmax, and the children ranked by a warp sort (M <= 128) into the request's state block. Groups go to CTAs as
-// expansions do (own requests, or group g to CTA g mod G). Returns false when a copy wait ran out.
-__device__ bool children_groups(const Params& p, int w, const Job* jl, unsigned char* smem, uint64_t* bar,
-                                unsigned& bar_uses) {
+// The group's M rows W_c[ids] are gathered once and the corrections of all its J expansions come out of one
+// tensor-core product Z[M][J] = W_c[ids] . [h_1 .. h_J]: mma.sync m16n8k16, the rows as A (a warp per 16 rows), the
+// hidden states as the n8 B tile, split into bf16 hi + lo pairs (as the GRU's hidden side). Column j of Z depends on
+// h_j alone, summed in a fixed order, so an expansion's children do not depend on which expansions share its group.
+// Then one warp per expansion: the restricted log-softmax, and the children ranked by a warp sort (M <= 128) into the
+// request's state block. Group g goes to CTA g mod G.
+// A CTA's groups form a pipeline: once a group's product is formed, the next group's rows and hidden states are
+// copied in (16-byte cp.async by every thread: a bulk copy per 1 KB row would queue on the CTA's copy engine) while
+// its children are ranked. Ids and base logits are loaded a group ahead of that (registers, then one of two shared
+// buffers), jobs and control words two groups ahead (three buffers), and rows are asked of L2 a group ahead.
+__device__ __forceinline__ void prefetch_l2_line(const void* src) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
+}
+__device__ bool children_groups(const Params& p, int w, const Job* jl, unsigned char* smem) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int M = p.M, n = p.n, H = p.H, X = p.xslots, KM = M < n ? M : n;
   const ReqLayout RL = req_layout(n, X, KM, p.lookahead);
   const GroupSmem GS = group_smem(M, H);
+  uint4* bfrag = reinterpret_cast<uint4*>(smem + GS.bfrag);
   float* hbuf = reinterpret_cast<float*>(smem + GS.h);
-  int* ids = reinterpret_cast<int*>(smem + GS.ids);
-  float* vals = reinterpret_cast<float*>(smem + GS.vals);
+  int* ids2 = reinterpret_cast<int*>(smem + GS.ids);       // [2][M4]
+  float* vals2 = reinterpret_cast<float*>(smem + GS.vals);  // [2][M4]
   unsigned short* rows_s = reinterpret_cast<unsigned short*>(smem + GS.rows);
   float* z = reinterpret_cast<float*>(smem + GS.z);
   Node* kraw = reinterpret_cast<Node*>(smem + GS.kraw);
   unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem + GS.keys);
+  Job* s_jobs = reinterpret_cast<Job*>(smem + GS.jobs);     // [3][kLargeLookahead]
+  ReqCtl* s_ctl = reinterpret_cast<ReqCtl*>(smem + GS.ctl);  // [3]: the groups' requests' control words
   const int SW = H + 8;  // padded row stride of the gathered rows (elements)
   const int M4 = round4(M);
-  const unsigned rb = static_cast<unsigned>(H * 2);
+  const size_t rb = static_cast<size_t>(H) * 2;
+  const int G = static_cast<int>(gridDim.x);
   const JobGroup* gl = p.grouplist + static_cast<size_t>(w & 1) * p.B * p.lookahead;
-  const bool own = p.own_groups;
-  // the wave's group count and (spread mode) this CTA's first group, read together: the list's slot exists even when
-  // the group does not (then it holds an older wave's entry, unused)
-  JobGroup first_group{};
-  if (!own && static_cast<int>(blockIdx.x) < p.B * p.lookahead) first_group = gl[blockIdx.x];
   const int ngroups = __ldcg(p.groupcount + w);
-  int* s_mine = reinterpret_cast<int*>(smem + GS.mine);
-  // the hidden states the bulk copies read were written by the GRU phase through the generic proxy, before the last
-  // grid barrier: one proxy fence for the whole phase
-  if (t == 0) asm volatile("fence.proxy.async.global;" ::: "memory");
-  // Spread mode: the ids and base logits of this CTA's next group are loaded into registers (thread m < M: candidate
-  // m) a group ahead, so that a group's row copies go out at once; its rows are asked of L2 one group ahead too.
-  const size_t ngs = static_cast<size_t>(gridDim.x);
+  if (static_cast<int>(blockIdx.x) >= ngroups) return true;
   auto cand_pos = [&](const JobGroup& g) { return (static_cast<size_t>(g.b) * p.K + g.depth) * M; };
+  // a group's jobs (32 bytes each) and its request's control word, as 16-byte copies into buffer `slot`
+  static_assert(sizeof(Job) == 32 && sizeof(ReqCtl) % 16 == 0, "copied in 16-byte pieces");
+  auto copy_meta = [&](const JobGroup& g, int slot) {
+    if (t < 2 * g.count)
+      cp_async16(reinterpret_cast<char*>(s_jobs + slot * kLargeLookahead) + 16 * t,
+                 reinterpret_cast<const char*>(jl + g.start) + 16 * t);
+    else if (t == 2 * kLargeLookahead)
+      cp_async16(s_ctl + slot, p.rstate + static_cast<size_t>(g.b) * RL.bytes + RL.ctl);
+  };
+  // a group's rows (warp w: rows w, w + 8, ...; lane l: 16-byte pieces l, l + 32, ...) and its hidden states
+  auto copy_inputs = [&](const JobGroup& g, const int* ids, const Job* jobs) {
+    for (int m = warp; m < M; m += kWarps) {
+      const char* src = static_cast<const char*>(p.w_c) + static_cast<size_t>(ids[m]) * rb;
+      unsigned short* dst = rows_s + static_cast<size_t>(m) * SW;
+      for (int c = lane; c < H / 8; c += 32) cp_async16(dst + 8 * c, src + 16 * c);
+    }
+    for (int j = warp; j < g.count; j += kWarps) {
+      const float* src = p.hs + (static_cast<size_t>(g.b) * X + jobs[j].xslot) * H;
+      for (int c = lane; c < H / 4; c += 32) cp_async16(hbuf + static_cast<size_t>(j) * H + 4 * c, src + 4 * c);
+    }
+  };
+  // prologue: the first group's ids, jobs and inputs; the second's ids (registers) and jobs
+  JobGroup gr = gl[blockIdx.x];
   int nid = 0;
   float nval = 0.f;
-  if (!own && static_cast<int>(blockIdx.x) < ngroups && t < M) {
-    nid = __ldg(p.ids + cand_pos(first_group) + t);
-    nval = __ldg(p.vals + cand_pos(first_group) + t);
+  if (t < M) {
+    nid = __ldg(p.ids + cand_pos(gr) + t);
+    nval = __ldg(p.vals + cand_pos(gr) + t);
   }
-  JobGroup next_group{};
-  for (int g0 = own ? 0 : blockIdx.x; g0 < ngroups; g0 += own ? kThreads : gridDim.x) {
-    int nmine = 1;
-    if (!own && g0 != static_cast<int>(blockIdx.x)) first_group = next_group;  // later rounds of the spread mode
-    if (own) {  // the groups of this CTA's requests in this batch, found by every thread at once
-      __syncthreads();
-      if (t == 0) s_mine[kThreads] = 0;
-      __syncthreads();
-      if (g0 + t < ngroups && gl[g0 + t].b % static_cast<int>(gridDim.x) == static_cast<int>(blockIdx.x))
-        s_mine[atomicAdd(&s_mine[kThreads], 1)] = g0 + t;
-      __syncthreads();
-      nmine = s_mine[kThreads];
+  copy_meta(gr, 0);
+  cp_async_commit();
+  if (t < M) {
+    ids2[t] = valid_id(p, nid);
+    vals2[t] = nval;
+  }
+  JobGroup next{};
+  if (static_cast<int>(blockIdx.x) + G < ngroups) {
+    next = gl[blockIdx.x + G];
+    if (t < M) {
+      nid = __ldg(p.ids + cand_pos(next) + t);
+      nval = __ldg(p.vals + cand_pos(next) + t);
     }
-    for (int k = 0; k < nmine; ++k) {
-      const JobGroup gr = own ? gl[s_mine[k]] : first_group;
-      const int J = gr.count;
-      const size_t pos = cand_pos(gr);
-      __syncthreads();  // the previous group is done with the shared buffers
-      if (own) {
-        for (int m = t; m < M; m += kThreads) {  // ids and base logits of the group's block position
-          ids[m] = valid_id(p, __ldg(p.ids + pos + m));
-          vals[m] = __ldg(p.vals + pos + m);
-        }
-      } else {
-        if (t < M) {  // loaded a group ahead
-          ids[t] = valid_id(p, nid);
-          vals[t] = nval;
-        }
-        const bool more = g0 + static_cast<int>(ngs) < ngroups;  // the next group's ids, for the next round
-        if (more) {
-          next_group = gl[g0 + ngs];
-          if (t < M) {
-            nid = __ldg(p.ids + cand_pos(next_group) + t);
-            nval = __ldg(p.vals + cand_pos(next_group) + t);
-          }
-        }
-      }
-      __syncthreads();
-      if (warp == 0) {  // the group's hidden states and rows
-        if (lane == 0) mbar_expect_tx(bar, static_cast<unsigned>(J * H * 4) + rb * static_cast<unsigned>(M));
-        __syncwarp();
-        if (lane < J)
-          bulk_g2s(hbuf + static_cast<size_t>(lane) * H,
-                   p.hs + (static_cast<size_t>(gr.b) * X + jl[gr.start + lane].xslot) * H, static_cast<unsigned>(H * 4),
-                   bar);
-        for (int m = lane; m < M; m += 32)
-          bulk_g2s(rows_s + static_cast<size_t>(m) * SW, static_cast<const char*>(p.w_c) + static_cast<size_t>(ids[m]) * rb,
-                   rb, bar);
-      }
-      if (!__syncthreads_and(wait_copies(p, bar, bar_uses))) return false;
-      // the next group's rows into L2 while this one computes (its ids are in registers by now)
-      if (!own && g0 + static_cast<int>(ngs) < ngroups && t < M && static_cast<unsigned>(nid) < static_cast<unsigned>(p.V))
-        prefetch_l2(static_cast<const char*>(p.w_c) + static_cast<size_t>(nid) * rb, rb);
-      // Z[M][8] = rows . [h_0 .. h_7], columns j >= J unused. The 16-row tiles times `ks` K parts make the warps'
-      // work (ks = 8 / tiles, so every warp has a share when M < 128); each warp runs two accumulator chains (even
-      // and odd k16 steps) and stores its partial tile; the partials are then added in a fixed order (part 0 first,
-      // even chain before odd), the same for every group, so Z does not depend on how many columns are in use.
-      {
-        const int g = lane >> 2, tg = lane & 3;
-        const int tiles = (M + 15) / 16, ks = tiles >= kWarps ? 1 : kWarps / tiles, steps = H / 16;
-        const float* hb = hbuf + static_cast<size_t>(g < J ? g : 0) * H;
-        float* zp = reinterpret_cast<float*>(smem + GS.zpart);
-        for (int item = warp; item < tiles * ks; item += kWarps) {
-          const int mt = item / ks, part = item % ks;
-          const int s0 = steps * part / ks, s1 = steps * (part + 1) / ks;
-          const int r0 = min(mt * 16 + g, M - 1), r1 = min(mt * 16 + g + 8, M - 1);
-          const unsigned short* a_lo = rows_s + static_cast<size_t>(r0) * SW;
-          const unsigned short* a_hi = rows_s + static_cast<size_t>(r1) * SW;
-          float de[4] = {0.f, 0.f, 0.f, 0.f}, dodd[4] = {0.f, 0.f, 0.f, 0.f};
-          for (int st = s0; st < s1; ++st) {
-            const int kk = st * 16 + tg * 2;
-            const uint32_t a0 = *reinterpret_cast<const uint32_t*>(a_lo + kk), a1 = *reinterpret_cast<const uint32_t*>(a_hi + kk);
-            const uint32_t a2 = *reinterpret_cast<const uint32_t*>(a_lo + kk + 8);
-            const uint32_t a3 = *reinterpret_cast<const uint32_t*>(a_hi + kk + 8);
-            const float2 x0 = *reinterpret_cast<const float2*>(hb + kk), x1 = *reinterpret_cast<const float2*>(hb + kk + 8);
-            uint32_t h0, l0, h1, l1;
-            split_bf16x2(x0.x, x0.y, h0, l0);
-            split_bf16x2(x1.x, x1.y, h1, l1);
-            float (&d)[4] = ((st - s0) & 1) ? dodd : de;
-            mma_bf16_16816(d, a0, a1, a2, a3, h0, h1);
-            mma_bf16_16816(d, a0, a1, a2, a3, l0, l1);
-          }
-          // this item's partial tile: rows g, g + 8 and columns 2 tg, 2 tg + 1 of tile mt
-          float* zt = zp + static_cast<size_t>(item) * 16 * kLargeLookahead;
-          zt[g * kLargeLookahead + 2 * tg] = de[0] + dodd[0];
-          zt[g * kLargeLookahead + 2 * tg + 1] = de[1] + dodd[1];
-          zt[(g + 8) * kLargeLookahead + 2 * tg] = de[2] + dodd[2];
-          zt[(g + 8) * kLargeLookahead + 2 * tg + 1] = de[3] + dodd[3];
-        }
-        __syncthreads();
-        for (int i = t; i < J * M; i += kThreads) {  // the corrected logits: the parts added in order
-          const int j = i / M, m = i % M, mt = m / 16, r = m % 16;
-          float v = 0.f;
-          for (int part = 0; part < ks; ++part)
-            v += zp[static_cast<size_t>(mt * ks + part) * 16 * kLargeLookahead + r * kLargeLookahead + j];
-          z[j * M4 + m] = (vals[m] + v) / p.T_eff;
-        }
-      }
-      __syncthreads();
-      // one warp per expansion: restricted log-softmax, children, their ranking into the request's state block (kc:
-      // at most n - s - 1 of them can still be popped after the node itself, n for the root's; s from the request's
-      // state block, written back by its owner before the last barrier)
-      if (warp < J) {
-        const Job jb = jl[gr.start + warp];
-        const float* zj = z + warp * M4;
-        Node* kr = kraw + warp * M;
-        unsigned long long* kk = keys + warp * M;
-        float mx = -INFINITY;
-        for (int m = lane; m < M; m += 32) mx = fmaxf(mx, zj[m]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-        float sum = 0.f;
-        for (int m = lane; m < M; m += 32) sum += expf(zj[m] - mx);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-        const float lse = logf(sum);
-        for (int m = lane; m < M; m += 32) {
-          Node e;
-          e.score = jb.score + ((zj[m] - mx) - lse);
-          e.token = ids[m];
-          e.seq = m;  // the candidate index until the node is popped
-          e.pslot = static_cast<short>(jb.xslot);
-          e.xslot = -1;
-          kr[m] = e;
-          kk[m] = (static_cast<unsigned long long>(key_of_f32(__float_as_uint(e.score))) << 32) |
-                  static_cast<unsigned long long>(~static_cast<uint32_t>(e.token));
-        }
-        __syncwarp();
-        const ReqView R = req_view(p.rstate + static_cast<size_t>(jb.b) * RL.bytes, RL);
-        const int kc = min(KM, jb.pslot < 0 ? n : n - __ldcg(&R.ctl->s) - 1);
-        Node* out = R.kids + static_cast<size_t>(jb.xslot) * KM;
-        if (M <= 32) rank_children_warp<1>(kr, kk, M, out, kc);
-        else if (M <= 64) rank_children_warp<2>(kr, kk, M, out, kc);
-        else rank_children_warp<4>(kr, kk, M, out, kc);
-        if (lane == 0) R.kcount[jb.xslot] = kc;
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  copy_inputs(gr, ids2, s_jobs);
+  if (static_cast<int>(blockIdx.x) + G < ngroups) copy_meta(next, 1);
+  cp_async_commit();
+  for (int g0 = blockIdx.x, k = 0; g0 < ngroups; g0 += G, ++k) {
+    const int cb = k & 1, cm = k % 3, J = gr.count;
+    const bool more1 = g0 + G < ngroups, more2 = g0 + 2 * G < ngroups;
+    const int* ids = ids2 + cb * M4;
+    cp_async_wait_all();
+    __syncthreads();  // this group's rows and hidden states, the next group's jobs have landed
+    // the B fragments: for k16 step s and lane l (column g = l / 4, tg = l % 4) the hi and lo bf16 pairs of
+    // h_g[16 s + 2 tg, + 1] and h_g[16 s + 2 tg + 8, + 9]; columns g >= J are never read back
+    for (int e = t; e < 2 * H; e += kThreads) {
+      const int st = e >> 5, l = e & 31, g = l >> 2, tg = l & 3;
+      if (g < J) {
+        const float* hg = hbuf + static_cast<size_t>(g) * H + 16 * st + 2 * tg;
+        const float2 x0 = *reinterpret_cast<const float2*>(hg), x1 = *reinterpret_cast<const float2*>(hg + 8);
+        uint4 f;
+        split_bf16x2(x0.x, x0.y, f.x, f.z);
+        split_bf16x2(x1.x, x1.y, f.y, f.w);
+        bfrag[e] = f;
       }
     }
+    // the next group's rows into L2 (its ids are in registers)
+    if (more1 && t < M && static_cast<unsigned>(nid) < static_cast<unsigned>(p.V)) {
+      const char* src = static_cast<const char*>(p.w_c) + static_cast<size_t>(nid) * rb;
+      for (size_t c = 0; c < rb; c += 128) prefetch_l2_line(src + c);
+    }
+    __syncthreads();
+    // Z[M][8] = rows . [h_0 .. h_7], columns j >= J unused. The 16-row tiles times `ks` K parts make the warps' work
+    // (ks = 8 / tiles, so every warp has a share when M < 128); each warp runs two accumulator chains (even and odd
+    // k16 steps) and stores its partial tile; the partials are then added in a fixed order (part 0 first, even chain
+    // before odd), the same for every group, so Z does not depend on how many columns are in use.
+    {
+      const int g = lane >> 2, tg = lane & 3;
+      const int tiles = (M + 15) / 16, ks = tiles >= kWarps ? 1 : kWarps / tiles, steps = H / 16;
+      float* zp = reinterpret_cast<float*>(smem + GS.zpart);
+      for (int item = warp; item < tiles * ks; item += kWarps) {
+        const int mt = item / ks, part = item % ks;
+        const int s0 = steps * part / ks, s1 = steps * (part + 1) / ks;
+        const int r0 = min(mt * 16 + g, M - 1), r1 = min(mt * 16 + g + 8, M - 1);
+        const unsigned short* a_lo = rows_s + static_cast<size_t>(r0) * SW + tg * 2;
+        const unsigned short* a_hi = rows_s + static_cast<size_t>(r1) * SW + tg * 2;
+        float de[4] = {0.f, 0.f, 0.f, 0.f}, dodd[4] = {0.f, 0.f, 0.f, 0.f};
+        auto step = [&](int st, float (&d)[4]) {
+          const int kk = st * 16;
+          const uint32_t a0 = lds32(a_lo + kk), a1 = lds32(a_hi + kk), a2 = lds32(a_lo + kk + 8), a3 = lds32(a_hi + kk + 8);
+          const uint4 f = bfrag[st * 32 + lane];
+          mma_bf16_16816(d, a0, a1, a2, a3, f.x, f.y);
+          mma_bf16_16816(d, a0, a1, a2, a3, f.z, f.w);
+        };
+        int st = s0;
+        for (; st + 1 < s1; st += 2) {
+          step(st, de);
+          step(st + 1, dodd);
+        }
+        if (st < s1) step(st, de);
+        // this item's partial tile: rows g, g + 8 and columns 2 tg, 2 tg + 1 of tile mt
+        float* zt = zp + static_cast<size_t>(item) * 16 * kLargeLookahead;
+        zt[g * kLargeLookahead + 2 * tg] = de[0] + dodd[0];
+        zt[g * kLargeLookahead + 2 * tg + 1] = de[1] + dodd[1];
+        zt[(g + 8) * kLargeLookahead + 2 * tg] = de[2] + dodd[2];
+        zt[(g + 8) * kLargeLookahead + 2 * tg + 1] = de[3] + dodd[3];
+      }
+      __syncthreads();
+      const float* vals = vals2 + cb * M4;
+      for (int i = t; i < J * M; i += kThreads) {  // the corrected logits: the parts added in order
+        const int j = i / M, m = i % M, mt = m / 16, r = m % 16;
+        float v = 0.f;
+        for (int part = 0; part < ks; ++part)
+          v += zp[static_cast<size_t>(mt * ks + part) * 16 * kLargeLookahead + r * kLargeLookahead + j];
+        z[j * M4 + m] = (vals[m] + v) / p.T_eff;
+      }
+    }
+    // the next group's ids into the other buffer; the one after it into registers
+    if (more1 && t < M) {
+      ids2[(cb ^ 1) * M4 + t] = valid_id(p, nid);
+      vals2[(cb ^ 1) * M4 + t] = nval;
+    }
+    JobGroup next2{};
+    if (more2) {
+      next2 = gl[g0 + 2 * G];
+      if (t < M) {
+        nid = __ldg(p.ids + cand_pos(next2) + t);
+        nval = __ldg(p.vals + cand_pos(next2) + t);
+      }
+    }
+    __syncthreads();  // the rows, hidden states and fragments are free; the next group's ids are in place
+    if (more1) {
+      copy_inputs(next, ids2 + (cb ^ 1) * M4, s_jobs + ((k + 1) % 3) * kLargeLookahead);
+      if (more2) copy_meta(next2, (k + 2) % 3);
+      cp_async_commit();
+    }
+    // one warp per expansion: restricted log-softmax, children, their ranking into the request's state block (kc:
+    // at most n - s - 1 of them can still be popped after the node itself, n for the root's; s from the request's
+    // control word, written back by its owner before the last barrier)
+    if (warp < J) {
+      const Job jb = s_jobs[cm * kLargeLookahead + warp];
+      const float* zj = z + warp * M4;
+      Node* kr = kraw + warp * M;
+      unsigned long long* kk = keys + warp * M;
+      float mx = -INFINITY;
+      for (int m = lane; m < M; m += 32) mx = fmaxf(mx, zj[m]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+      float sum = 0.f;
+      for (int m = lane; m < M; m += 32) sum += expf(zj[m] - mx);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+      const float lse = logf(sum);
+      for (int m = lane; m < M; m += 32) {
+        Node e;
+        e.score = jb.score + ((zj[m] - mx) - lse);
+        e.token = ids[m];
+        e.seq = m;  // the candidate index until the node is popped
+        e.pslot = static_cast<short>(jb.xslot);
+        e.xslot = -1;
+        kr[m] = e;
+        kk[m] = (static_cast<unsigned long long>(key_of_f32(__float_as_uint(e.score))) << 32) |
+                static_cast<unsigned long long>(~static_cast<uint32_t>(e.token));
+      }
+      __syncwarp();
+      const ReqView R = req_view(p.rstate + static_cast<size_t>(jb.b) * RL.bytes, RL);
+      const int kc = min(KM, jb.pslot < 0 ? n : n - s_ctl[cm].s - 1);
+      Node* out = R.kids + static_cast<size_t>(jb.xslot) * KM;
+      if (M <= 32) rank_children_warp<1>(kr, kk, M, out, kc);
+      else if (M <= 64) rank_children_warp<2>(kr, kk, M, out, kc);
+      else rank_children_warp<4>(kr, kk, M, out, kc);
+      if (lane == 0) R.kcount[jb.xslot] = kc;
+    }
+    gr = next;
+    next = next2;
   }
   // the children lists are read back through the async proxy (the owner's bulk copy of the state block)
   asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -993,7 +1026,7 @@ __device__ bool children_phase(const Params& p, const Job* jl, int rows, unsigne
 // picks join the next wave's packed list; the block goes back as one bulk copy; a finished request writes its
 // outputs and ancestor-mask rows. Returns false when a copy wait ran out.
 __device__ bool control_phase(const Params& p, int w, unsigned char* smem, uint64_t* bar, unsigned& bar_uses) {
-  const int t = threadIdx.x, warp = t >> 5;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int M = p.M, n = p.n, X = p.xslots, KM = M < n ? M : n, kla = p.lookahead;
   const ReqLayout RL = req_layout(n, X, KM, kla);
   const size_t rstride = (RL.bytes + 127) / 128 * 128;  // one shared-memory region per request of a batch
@@ -1016,46 +1049,50 @@ __device__ bool control_phase(const Params& p, int w, unsigned char* smem, uint6
     }
     if (!__syncthreads_and(wait_copies(p, bar, bar_uses))) return false;
     if (warp < nb) {
-      const ReqView R = req_view(smem + warp * rstride, RL);
+      const int b = b0 + warp * G;
+      unsigned char* base = smem + warp * rstride;
+      const ReqView R = req_view(base, RL);
       const bool done = R.ctl->s >= n;
-      if ((t & 31) == 0) s_done[warp] = done;
-      if (!done)
-        request_step(R, b0 + warp * G, n, M, p.max_depth, X, KM, kla,
-                     reinterpret_cast<Job*>(smem + warp * rstride + RL.jobs), p.hdr);
-    }
-    __syncthreads();
-    // the batch's picks: thread 0 orders each request's picks by depth (stable: a request's expansions at one block
-    // position sit together in the packed list, and each such run is a group of the children phase) and reserves
-    // their places in the next wave's lists
-    if (t == 0)
-      for (int i = 0; i < nb; ++i) {
-        s_off[i] = 0;
-        s_cnt[i] = 0;
-        if (s_done[i]) continue;
-        unsigned char* base = smem + i * rstride;
-        Job* jobs = reinterpret_cast<Job*>(base + RL.jobs);
-        const int nj = req_view(base, RL).ctl->njobs;
-        if (nj <= 0) continue;
-        for (int q = 1; q < nj; ++q)
-          for (int k = q; k > 0 && jobs[k - 1].depth > jobs[k].depth; --k) {
-            const Job tmp = jobs[k];
-            jobs[k] = jobs[k - 1];
-            jobs[k - 1] = tmp;
-          }
-        int ng = 1;
-        for (int q = 1; q < nj; ++q) ng += jobs[q].depth != jobs[q - 1].depth;
-        const int off = atomicAdd(p.jobcount + w + 1, nj);
-        int gi = atomicAdd(p.groupcount + w + 1, ng);
-        JobGroup* gnext = p.grouplist + static_cast<size_t>((w + 1) & 1) * p.B * kla;
-        for (int q = 0; q < nj;) {
-          int e = q + 1;
-          while (e < nj && jobs[e].depth == jobs[q].depth) ++e;
-          gnext[gi++] = JobGroup{off + q, e - q, b0 + i * G, jobs[q].depth};
-          q = e;
-        }
-        s_off[i] = off;
-        s_cnt[i] = nj;
+      Job* jobs = reinterpret_cast<Job*>(base + RL.jobs);
+      if (!done) {
+        // each pick's embedding row is asked of L2 as soon as the pick is made: the activation rows below read it
+        const auto ask_l2 = [&](int, const Job& jb) {
+          if (p.xact_on) prefetch_l2(static_cast<const unsigned short*>(p.emb) + static_cast<size_t>(jb.token) * p.E,
+                                     static_cast<unsigned>(p.E * 2));
+        };
+        request_step(R, b, n, M, p.max_depth, X, KM, kla, jobs, p.hdr, ask_l2);
       }
+      // the request's picks: ordered by depth (stable: a request's expansions at one block position sit together
+      // in the packed list, and each such run is a group of the children phase), their places reserved in the next
+      // wave's lists; one lane per request, the batch's requests at once
+      if ((t & 31) == 0) {
+        s_done[warp] = done;
+        s_off[warp] = 0;
+        s_cnt[warp] = 0;
+        const int nj = done ? 0 : R.ctl->njobs;
+        if (nj > 0) {
+          for (int q = 1; q < nj; ++q)
+            for (int k = q; k > 0 && jobs[k - 1].depth > jobs[k].depth; --k) {
+              const Job tmp = jobs[k];
+              jobs[k] = jobs[k - 1];
+              jobs[k - 1] = tmp;
+            }
+          int ng = 1;
+          for (int q = 1; q < nj; ++q) ng += jobs[q].depth != jobs[q - 1].depth;
+          const int off = atomicAdd(p.jobcount + w + 1, nj);
+          int gi = atomicAdd(p.groupcount + w + 1, ng);
+          JobGroup* gnext = p.grouplist + static_cast<size_t>((w + 1) & 1) * p.B * kla;
+          for (int q = 0; q < nj;) {
+            int e = q + 1;
+            while (e < nj && jobs[e].depth == jobs[q].depth) ++e;
+            gnext[gi++] = JobGroup{off + q, e - q, b, jobs[q].depth};
+            q = e;
+          }
+          s_off[warp] = off;
+          s_cnt[warp] = nj;
+        }
+      }
+    }
     __syncthreads();
     int total_jobs = 0;
     for (int i = 0; i < nb; ++i) total_jobs += s_cnt[i];
@@ -1067,49 +1104,49 @@ __device__ bool control_phase(const Params& p, int w, unsigned char* smem, uint6
       next[s_off[i] + qq] = reinterpret_cast<const Job*>(smem + i * rstride + RL.jobs)[qq];
     }
     if (p.xact_on && total_jobs > 0) {
-      const int E = p.E, H = p.H, Kx = E + 2 * H, ne = E / 8, nh = H / 2, per = ne + nh;
-      const int items = total_jobs * per;
-      constexpr int kBatch = 8;
-      for (int i0 = t; i0 < items; i0 += kBatch * kThreads) {
-        uint4 ve[kBatch];
-        float2 vh[kBatch];
-        unsigned short* dst[kBatch];
-        int kind[kBatch];  // 0: none, 1: an embedding chunk, 2: a hidden-state pair
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          const int idx = i0 + u * kThreads;
-          kind[u] = 0;
-          if (idx < items) {
-            int qi = idx / per, r = 0;
-            const int k = idx % per;
-            while (qi >= s_cnt[r]) qi -= s_cnt[r++];
-            const Job jb = reinterpret_cast<const Job*>(smem + r * rstride + RL.jobs)[qi];
-            unsigned short* xr = p.xact + static_cast<size_t>(s_off[r] + qi) * Kx;
-            if (k < ne) {
-              ve[u] = __ldg(reinterpret_cast<const uint4*>(static_cast<const unsigned short*>(p.emb) +
-                                                           static_cast<size_t>(jb.token) * E) + k);
-              dst[u] = xr + 8 * k;
-              kind[u] = 1;
-            } else {
-              const int kk = k - ne;
-              vh[u] = __ldcg(reinterpret_cast<const float2*>(
-                                 p.hs + (static_cast<size_t>(b0 + r * G) * X + jb.pslot) * H) + kk);
-              dst[u] = xr + E + 2 * kk;
-              kind[u] = 2;
-            }
+      // each pick's embedding row and parent state come into a staging slot (16-byte cp.async by the warp that owns
+      // the slot, every slot of a round at once) and go out from there as its activation row; ctl_stage slots follow
+      // the batch's state blocks
+      const int E = p.E, H = p.H, Kx = E + 2 * H, ce = E / 8, per = ce + H / 4;
+      const size_t pick_bytes = static_cast<size_t>(E) * 2 + static_cast<size_t>(H) * 4;
+      unsigned char* stage = smem + static_cast<size_t>(C) * rstride;
+      auto locate = [&](int q, int& r, int& qi) {  // pick q of the batch: request r's job qi
+        r = 0;
+        qi = q;
+        while (qi >= s_cnt[r]) qi -= s_cnt[r++];
+      };
+      for (int q0 = 0; q0 < total_jobs; q0 += p.ctl_stage) {
+        const int np = min(p.ctl_stage, total_jobs - q0);
+        for (int pk = warp; pk < np; pk += kWarps) {
+          int r, qi;
+          locate(q0 + pk, r, qi);
+          const Job jb = reinterpret_cast<const Job*>(smem + r * rstride + RL.jobs)[qi];
+          const char* esrc = static_cast<const char*>(p.emb) + static_cast<size_t>(jb.token) * E * 2;
+          const char* hsrc =
+              reinterpret_cast<const char*>(p.hs + (static_cast<size_t>(b0 + r * G) * X + jb.pslot) * H);
+          unsigned char* slot = stage + pk * pick_bytes;
+          for (int c = lane; c < per; c += 32) cp_async16(slot + 16 * c, c < ce ? esrc + 16 * c : hsrc + 16 * (c - ce));
+        }
+        cp_async_commit();
+        cp_async_wait_all();
+        __syncwarp();
+        for (int pk = warp; pk < np; pk += kWarps) {
+          int r, qi;
+          locate(q0 + pk, r, qi);
+          unsigned short* xr = p.xact + static_cast<size_t>(s_off[r] + qi) * Kx;
+          const unsigned char* slot = stage + pk * pick_bytes;
+          for (int c = lane; c < ce; c += 32)
+            reinterpret_cast<uint4*>(xr)[c] = reinterpret_cast<const uint4*>(slot)[c];
+          for (int c = lane; c < H / 4; c += 32) {
+            const float4 h = reinterpret_cast<const float4*>(slot + static_cast<size_t>(E) * 2)[c];
+            uint2 hi, lo;
+            split_bf16x2(h.x, h.y, hi.x, lo.x);
+            split_bf16x2(h.z, h.w, hi.y, lo.y);
+            *reinterpret_cast<uint2*>(xr + E + 4 * c) = hi;
+            *reinterpret_cast<uint2*>(xr + E + H + 4 * c) = lo;
           }
         }
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          if (kind[u] == 1) {
-            *reinterpret_cast<uint4*>(dst[u]) = ve[u];
-          } else if (kind[u] == 2) {
-            uint32_t hi, lo;
-            split_bf16x2(vh[u].x, vh[u].y, hi, lo);
-            *reinterpret_cast<uint32_t*>(dst[u]) = hi;
-            *reinterpret_cast<uint32_t*>(dst[u] + H) = lo;
-          }
-        }
+        __syncwarp();  // a warp's slots are read out before its next round's copies land in them
       }
       asm volatile("fence.proxy.async.global;" ::: "memory");  // read by TMA (async proxy) after the next barrier
     }
@@ -1230,14 +1267,13 @@ __device__ void run_waves(const Params& p, const TmaMaps& maps, unsigned char* s
         for (int i = threadIdx.x; i < p.gru_tiles; i += kThreads) p.gru_ticket[i] = 0u;
     }
     const uint64_t c0 = global_timer_ns();
-    if (!(p.group_mma ? children_groups(p, w, jl, smem, bar, bar_uses) : children_phase(p, jl, rows, smem, bar, bar_uses)))
-      return;
+    if (!(p.group_mma ? children_groups(p, w, jl, smem) : children_phase(p, jl, rows, smem, bar, bar_uses))) return;
     __syncthreads();
     gather_ns += global_timer_ns() - c0;
     ++waves;
     expansions += static_cast<unsigned>(rows);
     gather_bytes += static_cast<uint64_t>(p.group_mma ? __ldcg(p.groupcount + w) : rows) * p.M * p.H * (p.bf16 ? 2 : 4);
-    if (p.group_mma ? !p.own_groups : p.B < static_cast<int>(G)) {  // children computed by other CTAs: wait for them
+    if (p.group_mma || p.B < static_cast<int>(G)) {  // children computed by other CTAs: wait for them
       target += G;
       if (!counter_barrier(p.hdr, target, p.timeout_ns, s_flag)) return;
     } else {
@@ -1456,7 +1492,6 @@ dt_status build_trees(int B, int K, int V, int M, int n, int max_depth, float T,
   // the children phase by groups on the tensor cores when its buffers fit the same budget
   // groups spread over all CTAs (g mod G) whatever the batch: a request's groups on its owner CTA left the CTAs that
   // own two requests, and the tail waves' few groups, on one CTA each (c4: 75-85 us against a 50 us mean)
-  p.own_groups = false;
   {  // requests a CTA steps at once in the control phase: the ones it owns, as many as the shared memory holds
     const ReqLayout RL = req_layout(n, p.xslots, M < n ? M : n, p.lookahead);
     const size_t rstride = (RL.bytes + 127) / 128 * 128;
@@ -1465,7 +1500,20 @@ dt_status build_trees(int B, int K, int V, int M, int n, int max_depth, float T,
     p.ctl_conc = owned < fit ? owned : fit;
     if (p.ctl_conc > kWarps) p.ctl_conc = kWarps;
     if (p.ctl_conc < 1) p.ctl_conc = 1;
-    if (smem < rstride * p.ctl_conc) smem = rstride * p.ctl_conc;
+    size_t need = rstride * p.ctl_conc;
+    p.ctl_stage = 0;
+    if (p.xact_on) {  // staging slots for the picks' activation rows after the state blocks: all of a batch's picks
+      // at once when they fit, else as many as fit (at least one)
+      const size_t pick = static_cast<size_t>(E) * 2 + static_cast<size_t>(H) * 4;
+      const size_t cap = static_cast<size_t>(di.optin) - 2048;
+      while (p.ctl_conc > 1 && rstride * p.ctl_conc + pick > cap) --p.ctl_conc;
+      if (rstride * p.ctl_conc + pick > cap) return DT_ERR_UNSUPPORTED;
+      const size_t room = (cap - rstride * p.ctl_conc) / pick;
+      const int want = p.ctl_conc * p.lookahead;
+      p.ctl_stage = room < static_cast<size_t>(want) ? static_cast<int>(room) : want;
+      need = rstride * p.ctl_conc + static_cast<size_t>(p.ctl_stage) * pick;
+    }
+    if (smem < need) smem = need;
   }
   p.group_mma = p.bf16 && H % 16 == 0 && M <= 128 &&
                 group_smem(M, H).bytes + 2048 <= static_cast<size_t>(di.optin);
