@@ -434,9 +434,11 @@ __device__ __forceinline__ void bulk_s2g(void* gdst, const void* ssrc, unsigned 
 // K partial (below) has its own 128 columns. All eight warps read the tile back (tcgen05.ld, one row per thread,
 // warps w and w + 4 on the same TMEM lanes with half of the units each) and finish the GRU step.
 struct TmaMaps {
-  CUtensorMap x;    // [rows cap][E + 2H] bf16, box 64 x 128
-  CUtensorMap wih;  // [3H][E] bf16, box 64 x 32
-  CUtensorMap whh;  // [3H][H] bf16, box 64 x 32
+  CUtensorMap x;      // [rows cap][E + 2H] bf16, box 64 x 128
+  CUtensorMap wih;    // [3H][E] bf16, box 64 x 32
+  CUtensorMap whh;    // [3H][H] bf16, box 64 x 32
+  CUtensorMap wih64;  // the same weights in boxes of 64 x 64 (wide tiles)
+  CUtensorMap whh64;
 };
 constexpr int kUmmaRows = 128, kUmmaUnits = 32, kUmmaBK = 64, kUmmaStages = 7;
 constexpr int kUmmaA = kUmmaRows * kUmmaBK * 2;            // 16 KB
@@ -447,15 +449,26 @@ constexpr int kUmmaB = 4 * kUmmaUnits * kUmmaBK * 2;       // 16 KB
 constexpr int kUmmaStage = kUmmaA + kUmmaB;                // 32 KB (a multiple of 1024)
 constexpr size_t kUmmaSmem = static_cast<size_t>(kUmmaStages) * kUmmaStage + 1024;  // + alignment slack
 constexpr int kTmemCols = 512;  // kSplits partials of 128 columns
+// Wide tiles (128 expansions x 64 units, N = 256) for waves of whole tiles: half the activation reads of two narrow
+// tiles. A 4-stage ring of 48 KB stages in the same shared memory; two TMEM regions of 256 columns.
+constexpr int kWideUnits = 64, kWideStages = 4;
+constexpr int kWideB = 4 * kWideUnits * kUmmaBK * 2;  // 32 KB
+constexpr int kWideStage = kUmmaA + kWideB;           // 48 KB
+static_assert(kWideStages * kWideStage <= kUmmaStages * kUmmaStage, "the wide ring fits the narrow one's memory");
 
 // Per-launch state of the tensor-core phase: the ring's barriers and how far each has gone (the same in every thread).
 struct UmmaRing {
-  uint64_t* full;   // [kUmmaStages]
-  uint64_t* empty;  // [kUmmaStages]
-  uint64_t* done;   // accumulator complete
+  uint64_t* full;    // [kUmmaStages]
+  uint64_t* empty;   // [kUmmaStages]
+  uint64_t* done;    // accumulator complete
+  uint64_t* wfull;   // [kWideStages] the wide ring's
+  uint64_t* wempty;  // [kWideStages]
+  uint64_t* mid;     // wide tiles: partial 1, then partial 2, complete in TMEM
+  uint64_t* r1free;  // wide tiles: the epilogue warps folded it into region 0 (4 arrivals)
   uint32_t tmem;
-  unsigned blocks;  // K blocks loaded so far (ring position)
-  unsigned tiles;   // tiles finished so far (done phase)
+  unsigned blocks;   // K blocks loaded so far (ring position)
+  unsigned wblocks;  // ... through the wide ring
+  unsigned tiles;    // tiles finished so far (done phase)
 };
 
 // The GRU pointwise of U consecutive units u .. u + U - 1 of one expansion from its gate sums d[r | z | n_in | n_h][U].
@@ -514,6 +527,147 @@ __device__ __forceinline__ void reduce_partials(const Params& p, const Job* jl, 
   gru_pointwise<U>(p, jl[q], u0 + c, dsum, X, H);
 }
 
+__device__ __forceinline__ void tmem_st4x8(uint32_t taddr, const float (&v)[4][8]) {  // 32 columns from taddr
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                 ::"r"(taddr + 8u * g), "r"(__float_as_uint(v[g][0])), "r"(__float_as_uint(v[g][1])),
+                 "r"(__float_as_uint(v[g][2])), "r"(__float_as_uint(v[g][3])), "r"(__float_as_uint(v[g][4])),
+                 "r"(__float_as_uint(v[g][5])), "r"(__float_as_uint(v[g][6])), "r"(__float_as_uint(v[g][7]))
+                 : "memory");
+}
+
+// What partial `sp` of nkb K blocks (nE of them embedding blocks) wrote: gate slot g of its accumulator counts only
+// when the partial has blocks feeding it (n_in: embedding blocks, n_h: hidden ones, r and z: any).
+__device__ __forceinline__ bool partial_feeds(int sp, int g, int nkb, int nE) {
+  const int sb = split_begin(sp, nkb), se = split_begin(sp + 1, nkb);
+  const bool any = se > sb;
+  return g < 2 ? any : g == 2 ? any && sb < nE : any && se > nE;
+}
+
+// Waves of whole tiles on wide tiles: tile = 128 expansions x 64 units, B = the four gate slots of the 64 units
+// (N = 256). The K partials are still summed in order 0..3, in TMEM: partial 0 into region 0, partials 1..3 one
+// after another into region 1; the four epilogue warps fold partials 1 and 2 into region 0 as each completes
+// ((0 + p0) + p1, then + p2) while the MMA lane waits to reuse region 1, and the final epilogue adds partial 3.
+// The sums and their order are those of the narrow tiles, so the result does not depend on the tile width.
+__device__ bool umma_gru_wide(const Params& p, const TmaMaps& maps, const Job* jl, int rows, unsigned char* smem,
+                              UmmaRing& ring) {
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int E = p.E, H = p.H, X = p.xslots;
+  const int nE = E / kUmmaBK, nH = H / kUmmaBK, nkb = nE + 2 * nH;
+  unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem) + 1023) & ~uintptr_t(1023));
+  const int rtiles = (rows + kUmmaRows - 1) / kUmmaRows, utiles = H / kWideUnits, tiles = rtiles * utiles;
+  const int G = static_cast<int>(gridDim.x);
+  constexpr uint32_t kR1 = 256;  // region 1's first column
+  bool ok = true;
+  for (int tile = blockIdx.x; tile < tiles; tile += G) {
+    const int row0 = (tile / utiles) * kUmmaRows, u0 = (tile % utiles) * kWideUnits;
+    if (warp == 0 && lane == 0) {  // TMA producer
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the other phases' shared-memory use came first
+      for (int kb = 0; kb < nkb && ok; ++kb) {
+        const unsigned n = ring.wblocks + kb, st = n % kWideStages, use = n / kWideStages;
+        if (use > 0) ok = mbar_wait(&ring.wempty[st], (use - 1) & 1u, kCopyBudgetNs);
+        if (!ok) break;
+        unsigned char* a = base + st * kWideStage;
+        unsigned char* bsm = a + kUmmaA;
+        mbar_expect_tx(&ring.wfull[st], kWideStage);
+        const bool emb = kb < nE;
+        const int acol = emb ? kb * kUmmaBK : E + (kb - nE) * kUmmaBK;
+        const int wcol = emb ? kb * kUmmaBK : ((kb - nE) % nH) * kUmmaBK;
+        tma_load_2d(a, &maps.x, acol, row0, &ring.wfull[st]);
+        const CUtensorMap* wm = emb ? &maps.wih64 : &maps.whh64;
+        for (int g = 0; g < 4; ++g) {
+          const int src = g < 2 ? g : (g == 2) == emb ? 2 : 3;
+          tma_load_2d(bsm + g * kWideUnits * 128, wm, wcol, src * H + u0, &ring.wfull[st]);
+        }
+      }
+    } else if (warp == 1 && lane == 0) {  // MMA issuer
+      int sp = 0;
+      for (int kb = 0; kb < nkb && ok; ++kb) {
+        while (sp + 1 < kSplits && kb >= split_begin(sp + 1, nkb)) ++sp;
+        const int sb = split_begin(sp, nkb);
+        if (kb == sb && sp >= 2) {  // region 1 is reused: wait until partial sp - 1 is folded into region 0
+          ok = mbar_wait(ring.r1free, static_cast<unsigned>(sp - 2) & 1u, kCopyBudgetNs);
+          if (!ok) break;
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        }
+        const unsigned n = ring.wblocks + kb, st = n % kWideStages, use = n / kWideStages;
+        ok = mbar_wait(&ring.wfull[st], use & 1u, kCopyBudgetNs);
+        if (!ok) break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t d = ring.tmem + (sp == 0 ? 0u : kR1);
+        const uint32_t a = smem_u32(base + st * kWideStage), bsm = a + kUmmaA;
+#pragma unroll
+        for (int k = 0; k < kUmmaBK / 16; ++k)
+          umma_f16(d, umma_desc_sw128(a + 32 * k), umma_desc_sw128(bsm + 32 * k), umma_idesc(4 * kWideUnits),
+                   (kb > sb || k > 0) ? 1u : 0u);
+        umma_commit(&ring.wempty[st]);
+        if ((sp == 1 || sp == 2) && kb + 1 == split_begin(sp + 1, nkb)) umma_commit(ring.mid);
+      }
+      if (ok) umma_commit(ring.done);
+    } else if (warp >= 4) {  // fold partials 1 and 2 into region 0 as each completes
+      const uint32_t trow = ring.tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+      for (int f = 0; f < 2 && ok; ++f) {
+        ok = mbar_wait(ring.mid, static_cast<unsigned>(f), kCopyBudgetNs);
+        if (!ok) break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        for (int c = 0; c < 4 * kWideUnits; c += 32) {
+          const int g = c / kWideUnits;  // the gate slot of these 32 columns
+          float a[4][8], b[4][8];
+          tmem_ld4x8(trow + c, 8, a);
+          tmem_ld4x8(trow + kR1 + c, 8, b);
+          const bool fb = partial_feeds(f + 1, g, nkb, nE), fa = f > 0 || partial_feeds(0, g, nkb, nE);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float pa = fa ? a[i][j] : 0.f, pb = fb ? b[i][j] : 0.f;
+              a[i][j] = f == 0 ? (0.f + pa) + pb : pa + pb;
+            }
+          tmem_st4x8(trow + c, a);
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ring.r1free);
+      }
+    }
+    ring.wblocks += nkb;
+    ok = __syncthreads_and(ok);
+    if (ok) {  // the last partial added, then the GRU pointwise: one row per thread, warps w and w + 4 half the units
+      ok = mbar_wait(ring.done, ring.tiles & 1u, kCopyBudgetNs);
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const int r = 32 * (warp & 3) + lane, q = row0 + r;
+      const uint32_t trow = ring.tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+      Job jb{};
+      if (q < rows) jb = jl[q];
+      bool f3[4];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) f3[g] = partial_feeds(3, g, nkb, nE);
+      const int c0 = (warp >> 2) * (kWideUnits / 2);
+      for (int c = c0; c < c0 + kWideUnits / 2; c += 8) {
+        float s3[4][8], p3[4][8];
+        tmem_ld4x8(trow + c, kWideUnits, s3);
+        tmem_ld4x8(trow + kR1 + c, kWideUnits, p3);
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) s3[g][j] += f3[g] ? p3[g][j] : 0.f;
+        if (q < rows && ok) gru_pointwise<8>(p, jb, u0 + c, s3, X, H);
+      }
+    }
+    ring.tiles += 1;
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    ok = __syncthreads_and(ok);  // the accumulators are read before the next tile's first MMA overwrites them
+    if (!ok) {
+      record_error(p.hdr, DT_ERR_TIMEOUT);
+      atomicExch(&p.hdr->abort, 1u);
+      return false;
+    }
+  }
+  return true;
+}
+
 // Returns false when a wait ran out (recorded, abort raised).
 __device__ bool umma_gru_phase(const Params& p, const TmaMaps& maps, const Job* jl, int rows, unsigned char* smem,
                                UmmaRing& ring) {
@@ -523,6 +677,7 @@ __device__ bool umma_gru_phase(const Params& p, const TmaMaps& maps, const Job* 
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem) + 1023) & ~uintptr_t(1023));
   const int rtiles = (rows + kUmmaRows - 1) / kUmmaRows, utiles = H / kUmmaUnits, tiles = rtiles * utiles;
   const int G = static_cast<int>(gridDim.x);
+  if (tiles > p.gru_tiles && H % kWideUnits == 0) return umma_gru_wide(p, maps, jl, rows, smem, ring);
   const int per = tiles > p.gru_tiles ? kSplits : tiles * kSplits <= G ? 1 : tiles * (kSplits / 2) <= G ? 2 : kSplits;
   const int cpt = kSplits / per;  // CTAs per tile
   const int units = tiles * cpt;
@@ -1305,6 +1460,7 @@ __global__ void __launch_bounds__(kThreads, 1) build_kernel(Params p, const __gr
   __shared__ unsigned long long s_base;
   __shared__ uint64_t bar;  // completion of the frontier phase's bulk copies
   __shared__ uint64_t ufull[kUmmaStages], uempty[kUmmaStages], udone;
+  __shared__ uint64_t wfull[kWideStages], wempty[kWideStages], umid, ur1free;
   __shared__ uint32_t s_tmem;
   if (threadIdx.x == 0) {
     s_base = ld_relaxed_gpu_u64(&p.hdr->sync_count);  // before anyone can pass the first barrier
@@ -1315,6 +1471,12 @@ __global__ void __launch_bounds__(kThreads, 1) build_kernel(Params p, const __gr
         mbar_init(&uempty[i], 1);
       }
       mbar_init(&udone, 1);
+      for (int i = 0; i < kWideStages; ++i) {
+        mbar_init(&wfull[i], 1);
+        mbar_init(&wempty[i], 1);
+      }
+      mbar_init(&umid, 1);
+      mbar_init(&ur1free, 4);  // one arrival per epilogue warp
     }
     mbar_fence_init();
   }
@@ -1326,7 +1488,7 @@ __global__ void __launch_bounds__(kThreads, 1) build_kernel(Params p, const __gr
   if (kGemm == 4) asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   if (kGemm == 4) asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  UmmaRing ring{ufull, uempty, &udone, kGemm == 4 ? s_tmem : 0u, 0u, 0u};
+  UmmaRing ring{ufull, uempty, &udone, wfull, wempty, &umid, &ur1free, kGemm == 4 ? s_tmem : 0u, 0u, 0u, 0u};
   run_waves<kGemm>(p, maps, smem, ring, s_base, &bar, &s_flag);
   if (kGemm == 4) {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -1355,7 +1517,9 @@ bool gru_tensor_maps(TmaMaps* out, const void* xact, uint64_t xrows, const void*
   TmaMaps m{};
   if (!map2d(&m.x, xact, static_cast<uint64_t>(E) + 2 * static_cast<uint64_t>(H), xrows, kUmmaRows) ||
       !map2d(&m.wih, w_ih, static_cast<uint64_t>(E), 3 * static_cast<uint64_t>(H), kUmmaUnits) ||
-      !map2d(&m.whh, w_hh, static_cast<uint64_t>(H), 3 * static_cast<uint64_t>(H), kUmmaUnits))
+      !map2d(&m.whh, w_hh, static_cast<uint64_t>(H), 3 * static_cast<uint64_t>(H), kUmmaUnits) ||
+      !map2d(&m.wih64, w_ih, static_cast<uint64_t>(E), 3 * static_cast<uint64_t>(H), kWideUnits) ||
+      !map2d(&m.whh64, w_hh, static_cast<uint64_t>(H), 3 * static_cast<uint64_t>(H), kWideUnits))
     return false;
   last = m;
   key[0] = xact; key[1] = w_ih; key[2] = w_hh;
