@@ -499,32 +499,80 @@ constexpr int kSplits = kGruSplits;
 static_assert(kUmmaRows == kGruTileRows && kUmmaUnits == kGruTileUnits, "workspace tiles are the MMA tiles");
 __device__ __forceinline__ int split_begin(int s, int nkb) { return s * nkb / kSplits; }
 
-// Adds up the kSplits partials of rows [row0, row0 + 128) x units [u0 + uoff, + 2 * U) of a tile from the workspace and
-// runs the GRU pointwise; thread t takes row t % 128 and U units from uoff + U * (t / 128).
-template <int U>
-__device__ __forceinline__ void reduce_partials(const Params& p, const Job* jl, int rows, const float* part, int row0,
-                                                int u0, int uoff, int X, int H) {
-  const int r = threadIdx.x & (kUmmaRows - 1), q = row0 + r, c = uoff + U * (threadIdx.x / kUmmaRows);
-  if (q >= rows) return;
-  float dsum[4][U];
+// The split tile's CTAs meet, then each adds up the kSplits partials of rows [row0, row0 + 128) x units
+// [u0 + uoff, + 2 U) from the workspace and runs the GRU pointwise; thread t takes row t % 128 and U units from
+// uoff + U (t / 128). The pointwise's other inputs (the row's job, its parent state, the biases) are loaded before
+// the meeting, and all of a thread's partials at once after it. Returns false when the meeting ran out of time.
+template <int U>  // U a multiple of 4
+__device__ bool split_meet_reduce(const Params& p, const Job* jl, int rows, const float* part, int row0, int u0,
+                                  int uoff, int X, int H, unsigned* ticket, int cpt, bool ok, int* s_ok) {
+  const int t = threadIdx.x, r = t & (kUmmaRows - 1), q = row0 + r, c = uoff + U * (t / kUmmaRows);
+  const bool mine = q < rows;
+  Job jb{};
+  float hp[U], bias[6][U];
+  if (mine) {
+    jb = jl[q];
+    const float* hprev = p.hs + (static_cast<size_t>(jb.b) * X + jb.pslot) * H + u0 + c;
 #pragma unroll
-  for (int g = 0; g < 4; ++g)
+    for (int j = 0; j < U; ++j) {
+      hp[j] = __ldcg(hprev + j);
 #pragma unroll
-    for (int j = 0; j < U; ++j) dsum[g][j] = 0.f;
-#pragma unroll
-  for (int sp = 0; sp < kSplits; ++sp) {  // in order 0 .. kSplits - 1
-    const float* pr = part + static_cast<size_t>(sp) * kUmmaRows * 128 + r;
-    float v[4][U];
-#pragma unroll
-    for (int g = 0; g < 4; ++g)
-#pragma unroll
-      for (int j = 0; j < U; ++j) v[g][j] = __ldcg(pr + static_cast<size_t>(g * kUmmaUnits + c + j) * kUmmaRows);
-#pragma unroll
-    for (int g = 0; g < 4; ++g)
-#pragma unroll
-      for (int j = 0; j < U; ++j) dsum[g][j] += v[g][j];
+      for (int g = 0; g < 3; ++g) {
+        const size_t gi = static_cast<size_t>(g) * H + u0 + c + j;
+        bias[g][j] = p.b_ih ? ldw(p.b_ih, true, gi) : 0.f;
+        bias[3 + g][j] = p.b_hh ? ldw(p.b_hh, true, gi) : 0.f;
+      }
+    }
   }
-  gru_pointwise<U>(p, jl[q], u0 + c, dsum, X, H);
+  // thread 0's release after the CTA barrier publishes every thread's partials; its acquire before the next barrier
+  // orders every thread's reads of the others'
+  ok = __syncthreads_and(ok);
+  if (t == 0) {
+    bool met = ok;
+    if (met) {
+      atom_add_acq_rel_gpu(ticket, 1u);
+      const uint64_t t0 = global_timer_ns();
+      while (ld_acquire_gpu(ticket) < static_cast<unsigned>(cpt)) {  // the others run now: one unit per CTA
+        if (global_timer_ns() - t0 > kCopyBudgetNs || ld_acquire_gpu(&p.hdr->abort) != 0u) {
+          met = false;
+          break;
+        }
+      }
+    }
+    *s_ok = met;
+  }
+  __syncthreads();
+  if (*s_ok == 0) return false;
+  if (!mine) return true;
+  float* hout = p.hs + (static_cast<size_t>(jb.b) * X + jb.xslot) * H + u0 + c;
+#pragma unroll
+  for (int j0 = 0; j0 < U; j0 += 4) {  // four units at a time: their 4 x 4 x kSplits partials loaded together
+    float v[kSplits][4][4];
+#pragma unroll
+    for (int sp = 0; sp < kSplits; ++sp)
+#pragma unroll
+      for (int g = 0; g < 4; ++g)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          v[sp][g][j] = __ldcg(part + static_cast<size_t>(sp) * kUmmaRows * 128 +
+                               static_cast<size_t>(g * kUmmaUnits + c + j0 + j) * kUmmaRows + r);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float d[4];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        d[g] = 0.f;
+#pragma unroll
+        for (int sp = 0; sp < kSplits; ++sp) d[g] += v[sp][g][j];  // partials in order 0 .. kSplits - 1
+      }
+      const int u = j0 + j;
+      const float rg = sigmoidf_(d[0] + bias[0][u] + bias[3][u]);
+      const float zg = sigmoidf_(d[1] + bias[1][u] + bias[4][u]);
+      const float ng = tanhf(d[2] + bias[2][u] + rg * (d[3] + bias[5][u]));
+      hout[u] = (1.f - zg) * ng + zg * hp[u];
+    }
+  }
+  return true;
 }
 
 __device__ __forceinline__ void tmem_st4x8(uint32_t taddr, const float (&v)[4][8]) {  // 32 columns from taddr
@@ -778,31 +826,11 @@ __device__ bool umma_gru_phase(const Params& p, const TmaMaps& maps, const Job* 
       }
     }
     if (per < kSplits) {  // the tile's CTAs meet, then each adds up all partials for its share of the units
-      __threadfence();
-      ok = __syncthreads_and(ok);
-      if (t == 0) {
-        bool met = ok;
-        if (met) {
-          unsigned* tk = p.gru_ticket + tile;
-          atom_add_acq_rel_gpu(tk, 1u);
-          const uint64_t t0 = global_timer_ns();
-          while (ld_acquire_gpu(tk) < static_cast<unsigned>(cpt)) {  // the others run now: one unit per CTA
-            if (global_timer_ns() - t0 > kCopyBudgetNs || ld_acquire_gpu(&p.hdr->abort) != 0u) {
-              met = false;
-              break;
-            }
-          }
-        }
-        s_ok = met;
-      }
-      __syncthreads();
-      ok = s_ok != 0;
-      if (ok) {
-        __threadfence();
-        const int share = kUmmaUnits / cpt;  // 8 or 16 units of this CTA, over two groups of 128 threads
-        if (share == 8) reduce_partials<4>(p, jl, rows, part, row0, u0, part_idx * share, X, H);
-        else reduce_partials<8>(p, jl, rows, part, row0, u0, part_idx * share, X, H);
-      }
+      const int share = kUmmaUnits / cpt;  // 8 or 16 units of this CTA, over two groups of 128 threads
+      ok = share == 8 ? split_meet_reduce<4>(p, jl, rows, part, row0, u0, part_idx * share, X, H, p.gru_ticket + tile,
+                                             cpt, ok, &s_ok)
+                      : split_meet_reduce<8>(p, jl, rows, part, row0, u0, part_idx * share, X, H, p.gru_ticket + tile,
+                                             cpt, ok, &s_ok);
     }
     ring.tiles += 1;
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -861,6 +889,10 @@ __device__ bool children_groups(const Params& p, int w, const Job* jl, unsigned 
   const size_t rb = static_cast<size_t>(H) * 2;
   const int G = static_cast<int>(gridDim.x);
   const JobGroup* gl = p.grouplist + static_cast<size_t>(w & 1) * p.B * p.lookahead;
+  // the wave's group count and this CTA's first group, read together: the list's slot exists even when the group
+  // does not (then it holds an older wave's entry, unused)
+  JobGroup gr{};
+  if (static_cast<int>(blockIdx.x) < p.B * p.lookahead) gr = gl[blockIdx.x];
   const int ngroups = __ldcg(p.groupcount + w);
   if (static_cast<int>(blockIdx.x) >= ngroups) return true;
   auto cand_pos = [&](const JobGroup& g) { return (static_cast<size_t>(g.b) * p.K + g.depth) * M; };
@@ -886,7 +918,6 @@ __device__ bool children_groups(const Params& p, int w, const Job* jl, unsigned 
     }
   };
   // prologue: the first group's ids, jobs and inputs; the second's ids (registers) and jobs
-  JobGroup gr = gl[blockIdx.x];
   int nid = 0;
   float nval = 0.f;
   if (t < M) {
