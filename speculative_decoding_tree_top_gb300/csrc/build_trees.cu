@@ -502,10 +502,12 @@ __device__ __forceinline__ int split_begin(int s, int nkb) { return s * nkb / kS
 // The split tile's CTAs meet, then each adds up the kSplits partials of rows [row0, row0 + 128) x units
 // [u0 + uoff, + 2 U) from the workspace and runs the GRU pointwise; thread t takes row t % 128 and U units from
 // uoff + U (t / 128). The pointwise's other inputs (the row's job, its parent state, the biases) are loaded before
-// the meeting, and all of a thread's partials at once after it. Returns false when the meeting ran out of time.
-template <int U>  // U a multiple of 4
+// `epilogue` (which stores this CTA's partials) runs, so that their latency hides behind it, and all of a thread's
+// partials at once after the meeting. Returns false when the epilogue or the meeting ran out of time.
+template <int U, class Epilogue>  // U a multiple of 4
 __device__ bool split_meet_reduce(const Params& p, const Job* jl, int rows, const float* part, int row0, int u0,
-                                  int uoff, int X, int H, unsigned* ticket, int cpt, bool ok, int* s_ok) {
+                                  int uoff, int X, int H, unsigned* ticket, int cpt, bool ok, int* s_ok,
+                                  const Epilogue& epilogue) {
   const int t = threadIdx.x, r = t & (kUmmaRows - 1), q = row0 + r, c = uoff + U * (t / kUmmaRows);
   const bool mine = q < rows;
   Job jb{};
@@ -524,6 +526,7 @@ __device__ bool split_meet_reduce(const Params& p, const Job* jl, int rows, cons
       }
     }
   }
+  ok = epilogue(ok);
   // thread 0's release after the CTA barrier publishes every thread's partials; its acquire before the next barrier
   // orders every thread's reads of the others'
   ok = __syncthreads_and(ok);
@@ -781,7 +784,9 @@ __device__ bool umma_gru_phase(const Params& p, const TmaMaps& maps, const Job* 
     const int r = 32 * (warp & 3) + lane, q = row0 + r;  // the epilogue warps' row (expansion)
     // a tile's partials in the workspace: [split][gate column][row], so that a warp's rows are adjacent words
     float* part = p.gru_part + static_cast<size_t>(tile) * kSplits * kUmmaRows * 128;
-    if (ok) {  // epilogue: one row per thread, warps w and w + 4 (the same TMEM lanes) half of the units each
+    // epilogue: one row per thread, warps w and w + 4 (the same TMEM lanes) half of the units each
+    auto epilogue = [&](bool ok) -> bool {
+      if (!ok) return false;
       ok = mbar_wait(ring.done, ring.tiles & 1u, kCopyBudgetNs);
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const uint32_t trow = ring.tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
@@ -824,13 +829,16 @@ __device__ bool umma_gru_phase(const Params& p, const TmaMaps& maps, const Job* 
         }
         if (per == kSplits && q < rows && ok) gru_pointwise<8>(p, jb, u0 + c, dsum, X, H);
       }
-    }
+      return ok;
+    };
     if (per < kSplits) {  // the tile's CTAs meet, then each adds up all partials for its share of the units
       const int share = kUmmaUnits / cpt;  // 8 or 16 units of this CTA, over two groups of 128 threads
       ok = share == 8 ? split_meet_reduce<4>(p, jl, rows, part, row0, u0, part_idx * share, X, H, p.gru_ticket + tile,
-                                             cpt, ok, &s_ok)
+                                             cpt, ok, &s_ok, epilogue)
                       : split_meet_reduce<8>(p, jl, rows, part, row0, u0, part_idx * share, X, H, p.gru_ticket + tile,
-                                             cpt, ok, &s_ok);
+                                             cpt, ok, &s_ok, epilogue);
+    } else {
+      ok = epilogue(ok);
     }
     ring.tiles += 1;
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
