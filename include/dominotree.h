@@ -239,7 +239,9 @@ dt_status dt_lmhead_topm(int R, int D, int V, int M, const void* hidden, const v
  *              DT_ERR_TIMEOUT if a copy or MMA wait ran out (dt_get_error; initialise it with dt_workspace_init),
  *              then the partials of the key blocks.
  * Two launches: the partials on the tensor cores (tcgen05: S = Q K^T and O += P V accumulated in tensor memory, one
- * CTA per SM over an even share of the (request, key/value head, 64-key block) space), then their combination.
+ * CTA per SM over an even share of the (request, key/value head, 64-key block) space; a (request, key/value head)
+ * inside one CTA's share is written out directly), then the combination of the pairs split over several CTAs, a
+ * programmatic dependent of the first launch (left out when no pair is split).
  * Supported: dtype DT_BF16, d = 128, (Hq / Hkv) * n <= 64. Outside it DT_ERR_UNSUPPORTED; argument errors (Hq not a
  * multiple of Hkv, scale not finite and positive, null or misaligned pointers) DT_ERR_INVALID_ARG; both before any
  * launch. Pointers are 16-byte aligned device pointers (mask: any alignment).

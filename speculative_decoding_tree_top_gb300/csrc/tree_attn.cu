@@ -12,8 +12,9 @@
 // pairs, flattened, are split evenly over one CTA per SM (a CTA's share may span several pairs: one segment each).
 // A CTA streams its keys and values by TMA, computes S = Q K^T and O += P V with tcgen05 MMAs whose accumulators
 // live in tensor memory, and runs the softmax (base 2, running maximum raised lazily) from tensor memory, one thread
-// per query row (tree_attn_tc below); a second launch combines the segments of each row. Memory bound: the key and
-// value rows are the bytes.
+// per query row (tree_attn_tc below). A segment that covers its whole (request, key/value head) writes the output
+// itself; a second launch, a programmatic dependent of the first, combines the segments of the rows of pairs split
+// over several CTAs. Memory bound: the key and value rows are the bytes.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -173,6 +174,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_attn_tc(TaParams p, const 
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = s_tmem;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the combination may launch (it waits for us)
   bool ok = true;
   const long long x0 = static_cast<long long>(blockIdx.x) * p.work / p.grid;
   const long long x1 = (static_cast<long long>(blockIdx.x) + 1) * p.work / p.grid;
@@ -345,9 +347,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_attn_tc(TaParams p, const 
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(&o_done[gl & 1u], (gl >> 1) & 1u, kTcBudgetNs));
       if (!ok) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      // A segment that covers its whole pair is the row's only one: it writes the normalised output itself (the
+      // combination of one segment: weight exp2(0) = 1, then the same reciprocal), and the combination skips it.
+      const bool whole = sg.nblk == p.nb;
       const size_t unit = static_cast<size_t>(sg.pair) * p.maxseg + sg.slot;
       const int prow_out = gi * p.n + node;
-      float* po = p.part + (unit * kRows + prow_out) * kD;
+      float* po = whole ? p.out + ((static_cast<size_t>(sg.b) * p.n + node) * p.Hq + sg.kvh * p.G + gi) * kD
+                        : p.part + (unit * kRows + prow_out) * kD;
+      const float inv = !whole ? 1.f : l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
       for (int h = 0; h < 8; ++h) {
         uint32_t ov[16];
@@ -355,10 +362,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_attn_tc(TaParams p, const 
         if (live)
 #pragma unroll
           for (int e = 0; e < 16; e += 4)
-            *reinterpret_cast<float4*>(po + 16 * h + e) = make_float4(__uint_as_float(ov[e]), __uint_as_float(ov[e + 1]),
-                                                                      __uint_as_float(ov[e + 2]), __uint_as_float(ov[e + 3]));
+            *reinterpret_cast<float4*>(po + 16 * h + e) =
+                make_float4(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv,
+                            __uint_as_float(ov[e + 2]) * inv, __uint_as_float(ov[e + 3]) * inv);
       }
-      if (live) {
+      if (live && !whole) {
         float* pm = p.ml + (unit * kRows + prow_out) * 2;
         pm[0] = m;
         pm[1] = l;
@@ -433,12 +441,14 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 __global__ void __launch_bounds__(kCombineThreads) tree_attn_combine(TaParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the partial launch has completed and its writes are visible
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const long long rows = static_cast<long long>(p.B) * p.Hkv * p.R;
   if (p.maxseg <= kWarpRowSegs) {  // a warp per row
     const long long stride = static_cast<long long>(gridDim.x) * kCombineWarps;
     for (long long u = static_cast<long long>(blockIdx.x) * kCombineWarps + warp; u < rows; u += stride) {
       const RowRef q = row_ref(p, u);
+      if (q.nseg == 1) continue;  // a whole pair: its one segment wrote the output
       const float mx = warp_max(lane < q.nseg ? p.ml[((q.u0 + lane) * kRows + q.r) * 2] : -INFINITY);
       float den = 0.f;
       float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -451,6 +461,7 @@ __global__ void __launch_bounds__(kCombineThreads) tree_attn_combine(TaParams p)
   __shared__ float4 s_num[kCombineWarps][32];
   for (long long u = blockIdx.x; u < rows; u += gridDim.x) {  // a CTA per row
     const RowRef q = row_ref(p, u);
+    if (q.nseg == 1) continue;  // a whole pair: its one segment wrote the output
     float mx = -INFINITY;
     for (int c = threadIdx.x; c < q.nseg; c += kCombineThreads) mx = fmaxf(mx, p.ml[((q.u0 + c) * kRows + q.r) * 2]);
     mx = warp_max(mx);
@@ -563,8 +574,19 @@ extern "C" dt_status dt_tree_attention(int B, int n, int L, int Hq, int Hkv, int
   if (ensure_dynamic_smem(fa, kTcSmem) != cudaSuccess) return DT_ERR_CUDA;
   tree_attn_tc<<<static_cast<unsigned>(P.grid), kTcThreads, kTcSmem, stream>>>(p, maps,
                                                                                reinterpret_cast<WsHeader*>(ws));
+  if (cudaGetLastError() != cudaSuccess) return DT_ERR_CUDA;
+  if (P.maxseg == 1) return DT_OK;  // every pair in one CTA's share: the partial launch wrote every output
+  // the rows of pairs split over several CTAs, as a programmatic dependent of the partial launch
   const long long crows = static_cast<long long>(B) * Hkv * p.R, cper = P.maxseg <= kWarpRowSegs ? kCombineWarps : 1;
   const long long cgrid = (crows + cper - 1) / cper, ccap = static_cast<long long>(kCombinePerSm) * di.sms;
-  tree_attn_combine<<<static_cast<unsigned>(cgrid < ccap ? cgrid : ccap), kCombineThreads, 0, stream>>>(p);
-  return cuda_status(cudaGetLastError());
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(cgrid < ccap ? cgrid : ccap));
+  cfg.blockDim = dim3(kCombineThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_status(cudaLaunchKernelEx(&cfg, tree_attn_combine, p));
 }

@@ -34,6 +34,8 @@ def run(dtlib, B, n, L, Hq, Hkv, d=128, seed=2468, mask=None):
     (3, 7, 100, 8, 2),        # odd sizes: rows 28 of 64, a partial key block
     (1, 16, 5000, 4, 1),      # one key/value head, a long prefix in many chunks
     (4, 1, 63, 2, 2),         # one node, no grouping
+    (64, 16, 100, 32, 8),     # pairs of two key blocks: most inside one CTA's share (written directly), the rest
+                              # split over two CTAs (combined)
 ])
 def test_tree_attention_parity(dtlib, B, n, L, Hq, Hkv):
     out, ref, _ = run(dtlib, B, n, L, Hq, Hkv)
