@@ -35,7 +35,8 @@ struct TaParams {
   int B, n, L, T, Hq, Hkv, G, R;
   int nb;              // key blocks of 64 per (request, key/value head)
   int grid, maxseg;    // CTAs of the partial launch; partial slots per (request, key/value head)
-  long long work;      // all key blocks: (B Hkv) nb, split evenly over the CTAs
+  int wpc;             // whole pairs per CTA: CTA c takes pairs [wpc c, wpc (c + 1)) whole
+  long long rwork;     // the other pairs' key blocks, (B Hkv - wpc grid) nb, split evenly over the CTAs
   const unsigned short* q;   // [B][n][Hq][kD] bf16
   const unsigned short* k;   // [B][Hkv][T][kD] bf16
   const unsigned short* v;   // [B][Hkv][T][kD] bf16
@@ -120,20 +121,41 @@ __device__ __forceinline__ void tmem_ld16_ta(uint32_t taddr, uint32_t (&r)[16]) 
 }
 
 // One segment of a CTA's share: (request, key/value head) pair, its blocks [j0, j0 + nblk), and its partial slot.
+// A CTA's share is its wpc whole pairs, then its even share [rx0, rx1) of the remaining pairs' blocks (flattened);
+// x runs over the share: [0, wpc nb) the whole pairs, then the rest.
 struct TaSeg {
   int pair, b, kvh, j0, nblk, slot;
 };
-__device__ __forceinline__ TaSeg ta_segment(const TaParams& p, long long& x, long long x1) {
+struct TaShare {
+  long long rx0, len;  // the share of the remaining blocks starts at rx0; x runs over [0, len)
+};
+__device__ __forceinline__ TaShare ta_share(const TaParams& p) {
+  const long long c = blockIdx.x;
+  const long long rx0 = c * p.rwork / p.grid, rx1 = (c + 1) * p.rwork / p.grid;
+  return TaShare{rx0, static_cast<long long>(p.wpc) * p.nb + (rx1 - rx0)};
+}
+__device__ __forceinline__ TaSeg ta_segment(const TaParams& p, const TaShare& sh, long long& x) {
   TaSeg g;
-  g.pair = static_cast<int>(x / p.nb);
+  const long long wx = static_cast<long long>(p.wpc) * p.nb;
+  if (x < wx) {  // a whole pair
+    g.pair = static_cast<int>(blockIdx.x) * p.wpc + static_cast<int>(x / p.nb);
+    g.j0 = 0;
+    g.nblk = p.nb;
+    g.slot = 0;
+    x += p.nb;
+  } else {  // a run of the remaining pairs' blocks
+    const long long rx = sh.rx0 + (x - wx), rx1 = sh.rx0 + (sh.len - wx);
+    const int rp = static_cast<int>(rx / p.nb);
+    const long long pfirst = static_cast<long long>(rp) * p.nb;
+    const int bend = static_cast<int>(min(rx1, pfirst + p.nb) - pfirst);
+    g.pair = p.wpc * p.grid + rp;
+    g.j0 = static_cast<int>(rx - pfirst);
+    g.nblk = bend - g.j0;
+    g.slot = static_cast<int>(blockIdx.x) - block_owner(pfirst, p.rwork, p.grid);
+    x += g.nblk;
+  }
   g.b = g.pair / p.Hkv;
   g.kvh = g.pair % p.Hkv;
-  const long long pfirst = static_cast<long long>(g.pair) * p.nb;
-  const int bend = static_cast<int>(min(x1, pfirst + p.nb) - pfirst);
-  g.j0 = static_cast<int>(x - pfirst);
-  g.nblk = bend - g.j0;
-  g.slot = static_cast<int>(blockIdx.x) - block_owner(pfirst, p.work, p.grid);
-  x = pfirst + bend;
   return g;
 }
 
@@ -176,15 +198,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_attn_tc(TaParams p, const 
   const uint32_t tmem = s_tmem;
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the combination may launch (it waits for us)
   bool ok = true;
-  const long long x0 = static_cast<long long>(blockIdx.x) * p.work / p.grid;
-  const long long x1 = (static_cast<long long>(blockIdx.x) + 1) * p.work / p.grid;
+  const TaShare sh = ta_share(p);
 
   if (warp == 2 && lane == 0) {  // TMA producer
     unsigned g = 0;
     const uint32_t qtx = static_cast<uint32_t>(2 * 128 * p.R);
     int si = 0;
-    for (long long x = x0; x < x1 && ok; ++si) {
-      const TaSeg sg = ta_segment(p, x, x1);
+    for (long long x = 0; x < sh.len && ok; ++si) {
+      const TaSeg sg = ta_segment(p, sh, x);
       const unsigned qb = static_cast<unsigned>(si) & 1u;
       if (si >= 2) ok = mbar_wait(&q_empty[qb], static_cast<unsigned>((si >> 1) - 1) & 1u, kTcBudgetNs);
       if (!ok) break;
@@ -211,8 +232,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_attn_tc(TaParams p, const 
     const uint32_t id_s = umma_idesc(kTcKeys, 128), id_o = umma_idesc(kD, 128) | (1u << 16);  // O: V MN-major
     unsigned g = 0;
     int si = 0;
-    for (long long x = x0; x < x1 && ok; ++si) {
-      const TaSeg sg = ta_segment(p, x, x1);
+    for (long long x = 0; x < sh.len && ok; ++si) {
+      const TaSeg sg = ta_segment(p, sh, x);
       const unsigned qb = static_cast<unsigned>(si) & 1u;
       const uint32_t aq = smem_u32(sq + qb * kTcQBytes), to = tmem + 128u + 128u * qb;
       ok = mbar_wait(&q_full[qb], static_cast<unsigned>(si >> 1) & 1u, kTcBudgetNs);
@@ -262,8 +283,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_attn_tc(TaParams p, const 
     const int node = live ? r / p.G : 0, gi = live ? r % p.G : 0;  // row r = node G + gi
     unsigned g = 0;
     int si = 0;
-    for (long long x = x0; x < x1 && ok; ++si) {
-      const TaSeg sg = ta_segment(p, x, x1);
+    for (long long x = 0; x < sh.len && ok; ++si) {
+      const TaSeg sg = ta_segment(p, sh, x);
       const unsigned qb = static_cast<unsigned>(si) & 1u;
       const uint32_t to = tl + 128u + 128u * qb;
       unsigned long long mbits = 0;  // bit c: tree position c is on the node's ancestor row
@@ -409,8 +430,12 @@ __device__ __forceinline__ RowRef row_ref(const TaParams& p, long long u) {
   q.b = pair / p.Hkv;
   q.kvh = pair % p.Hkv;
   q.u0 = static_cast<size_t>(pair) * p.maxseg;
-  const long long pfirst = static_cast<long long>(pair) * p.nb;
-  q.nseg = block_owner(pfirst + p.nb - 1, p.work, p.grid) - block_owner(pfirst, p.work, p.grid) + 1;
+  q.nseg = 1;  // a whole pair
+  const int rp = pair - p.wpc * p.grid;
+  if (rp >= 0) {
+    const long long pfirst = static_cast<long long>(rp) * p.nb;
+    q.nseg = block_owner(pfirst + p.nb - 1, p.rwork, p.grid) - block_owner(pfirst, p.rwork, p.grid) + 1;
+  }
   return q;
 }
 // Segments c0, c0 + step, ... of a row, weighted relative to the row's maximum `mx`: the weighted sum of the lane's
@@ -495,22 +520,26 @@ __global__ void __launch_bounds__(kCombineThreads) tree_attn_combine(TaParams p)
 }
 
 struct TaPlan {
-  int nb, grid, maxseg;
-  long long work;
+  int nb, grid, maxseg, wpc;
+  long long rwork;
   size_t part, ml, bytes;
 };
-// The partial launch's CTAs (`per_sm` per SM) share all key blocks of `block` keys evenly (a CTA takes at least one
-// block); maxseg is the most CTAs any (request, key/value head) is spread over, found pair by pair.
+// The partial launch's CTAs (`per_sm` per SM) each take wpc = pairs / CTAs whole (request, key/value head) pairs,
+// then an even share of the remaining pairs' blocks of `block` keys (a CTA takes at least one block); maxseg is the
+// most CTAs a remaining pair is spread over, found pair by pair.
 inline TaPlan ta_plan(int B, int T, int Hkv, int sms, int per_sm = 1, int block = kTcKeys) {
   TaPlan P{};
   const long long pairs = static_cast<long long>(B) * Hkv;
   P.nb = (T + block - 1) / block;
-  P.work = pairs * P.nb;
+  const long long work = pairs * P.nb;
   const long long g = static_cast<long long>(per_sm) * sms;
-  P.grid = static_cast<int>(g < P.work ? g : P.work);
+  P.grid = static_cast<int>(g < work ? g : work);
+  P.wpc = static_cast<int>(pairs / P.grid);
+  const long long rest = pairs - static_cast<long long>(P.wpc) * P.grid;
+  P.rwork = rest * P.nb;
   P.maxseg = 1;
-  for (long long pr = 0; pr < pairs; ++pr) {
-    const int segs = block_owner((pr + 1) * P.nb - 1, P.work, P.grid) - block_owner(pr * P.nb, P.work, P.grid) + 1;
+  for (long long pr = 0; pr < rest; ++pr) {
+    const int segs = block_owner((pr + 1) * P.nb - 1, P.rwork, P.grid) - block_owner(pr * P.nb, P.rwork, P.grid) + 1;
     P.maxseg = segs > P.maxseg ? segs : P.maxseg;
   }
   const size_t slots = static_cast<size_t>(pairs) * P.maxseg;
@@ -553,7 +582,7 @@ extern "C" dt_status dt_tree_attention(int B, int n, int L, int Hq, int Hkv, int
   if (static_cast<long long>(B) * Hkv * G * n > INT_MAX || P.maxseg > kMaxChunks) return DT_ERR_UNSUPPORTED;
   TaParams p{};
   p.B = B; p.n = n; p.L = L; p.T = T; p.Hq = Hq; p.Hkv = Hkv; p.G = G; p.R = G * n;
-  p.nb = P.nb; p.grid = P.grid; p.maxseg = P.maxseg; p.work = P.work;
+  p.nb = P.nb; p.grid = P.grid; p.maxseg = P.maxseg; p.wpc = P.wpc; p.rwork = P.rwork;
   p.q = static_cast<const unsigned short*>(q);
   p.k = static_cast<const unsigned short*>(k);
   p.v = static_cast<const unsigned short*>(v);
@@ -575,7 +604,7 @@ extern "C" dt_status dt_tree_attention(int B, int n, int L, int Hq, int Hkv, int
   tree_attn_tc<<<static_cast<unsigned>(P.grid), kTcThreads, kTcSmem, stream>>>(p, maps,
                                                                                reinterpret_cast<WsHeader*>(ws));
   if (cudaGetLastError() != cudaSuccess) return DT_ERR_CUDA;
-  if (P.maxseg == 1) return DT_OK;  // every pair in one CTA's share: the partial launch wrote every output
+  if (P.rwork == 0) return DT_OK;  // every pair whole in one CTA's share: the partial launch wrote every output
   // the rows of pairs split over several CTAs, as a programmatic dependent of the partial launch
   const long long crows = static_cast<long long>(B) * Hkv * p.R, cper = P.maxseg <= kWarpRowSegs ? kCombineWarps : 1;
   const long long cgrid = (crows + cper - 1) / cper, ccap = static_cast<long long>(kCombinePerSm) * di.sms;
