@@ -439,7 +439,11 @@ __device__ __forceinline__ void warp_dot_rows8(const void* rows, const void* w, 
 // A job's children ranked among themselves by one warp: a bitonic sort of their sibling keys (larger first; equal
 // keys, possible only when a row repeats an id, by the lower candidate index) over 32 * R elements, element i in
 // register i / 32 of lane i % 32; padding (index >= M) has key 0 and sorts last. The first kc go to out[0 .. kc).
-template <int R>
+// kPacked (token ids below 2^25, M <= 128): the candidate index rides in the key's low 7 bits, under the token's 25
+// (the key's order is unchanged: score, then token ascending, then index ascending), so the sort moves one 64-bit
+// word per element instead of a word and an index.
+constexpr int kPackTokenBits = 25;
+template <int R, bool kPacked = false>
 __device__ __forceinline__ void rank_children_warp(const Node* kr, const unsigned long long* kk, int M, Node* out,
                                                    int kc) {
   const int lane = threadIdx.x & 31;
@@ -449,9 +453,12 @@ __device__ __forceinline__ void rank_children_warp(const Node* kr, const unsigne
   for (int r = 0; r < R; ++r) {
     m[r] = 32 * r + lane;
     k[r] = m[r] < M ? kk[m[r]] : 0ull;
+    if (kPacked && m[r] < M)  // score bits, then 2^25 - 1 - token, then 127 - index
+      k[r] = (k[r] & 0xFFFFFFFF00000000ull) |
+             ((k[r] & ((1ull << kPackTokenBits) - 1ull)) << 7) | static_cast<unsigned long long>(127 - m[r]);
   }
   auto first = [](unsigned long long ka, int ma, unsigned long long kb, int mb) {
-    return (ka > kb) | ((ka == kb) & (ma < mb));
+    return kPacked ? ka > kb : (ka > kb) | ((ka == kb) & (ma < mb));
   };
 #pragma unroll
   for (int size = 2; size <= 32 * R; size <<= 1) {
@@ -468,30 +475,47 @@ __device__ __forceinline__ void rank_children_warp(const Node* kr, const unsigne
             const unsigned long long tk = k[r];
             k[r] = k[r2];
             k[r2] = tk;
-            const int tm = m[r];
-            m[r] = m[r2];
-            m[r2] = tm;
+            if (!kPacked) {
+              const int tm = m[r];
+              m[r] = m[r2];
+              m[r2] = tm;
+            }
           }
         }
       } else {  // the pair spans lanes lane and lane ^ j, same register
 #pragma unroll
         for (int r = 0; r < R; ++r) {
           const unsigned long long ok = __shfl_xor_sync(0xFFFFFFFFu, k[r], j);
-          const int om = __shfl_xor_sync(0xFFFFFFFFu, m[r], j);
+          const int om = kPacked ? 0 : __shfl_xor_sync(0xFFFFFFFFu, m[r], j);
           const bool desc = ((32 * r + lane) & size) == 0;
           const bool lower = (lane & j) == 0;
           const bool mine_first = first(k[r], m[r], ok, om);
           if (mine_first != (lower == desc)) {
             k[r] = ok;
-            m[r] = om;
+            if (!kPacked) m[r] = om;
           }
         }
       }
     }
   }
 #pragma unroll
-  for (int r = 0; r < R; ++r)
-    if (32 * r + lane < kc) out[32 * r + lane] = kr[m[r]];
+  for (int r = 0; r < R; ++r) {
+    const int mi = kPacked ? 127 - static_cast<int>(k[r] & 127ull) : m[r];
+    if (32 * r + lane < kc) out[32 * r + lane] = kr[mi];
+  }
+}
+// The ranking of M <= 128 children, packed when every token id fits the packed key.
+__device__ __forceinline__ void rank_children(const Node* kr, const unsigned long long* kk, int M, int V, Node* out,
+                                              int kc) {
+  if (V <= (1 << kPackTokenBits)) {
+    if (M <= 32) rank_children_warp<1, true>(kr, kk, M, out, kc);
+    else if (M <= 64) rank_children_warp<2, true>(kr, kk, M, out, kc);
+    else rank_children_warp<4, true>(kr, kk, M, out, kc);
+  } else {
+    if (M <= 32) rank_children_warp<1>(kr, kk, M, out, kc);
+    else if (M <= 64) rank_children_warp<2>(kr, kk, M, out, kc);
+    else rank_children_warp<4>(kr, kk, M, out, kc);
+  }
 }
 
 // A request's best-first state as one contiguous block (the large-batch builder keeps it in the workspace between

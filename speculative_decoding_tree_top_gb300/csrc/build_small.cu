@@ -681,9 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_builder(Params p, Plan P) {
         const int rem = jb.pslot < 0 ? n : n - ctl[jb.b].s - 1;
         const int kc = min(min(M, KM), rem);
         Node* out = kids + (static_cast<size_t>(jb.b) * X + jb.xslot) * KM;
-        if (M <= 32) rank_children_warp<1>(kraw + q * M, kkey + q * M, M, out, kc);
-        else if (M <= 64) rank_children_warp<2>(kraw + q * M, kkey + q * M, M, out, kc);
-        else rank_children_warp<4>(kraw + q * M, kkey + q * M, M, out, kc);
+        rank_children(kraw + q * M, kkey + q * M, M, p.V, out, kc);
         if (lane == 0) kcount[jb.b * X + jb.xslot] = kc;
       }
     }

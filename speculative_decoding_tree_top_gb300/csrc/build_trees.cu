@@ -1072,9 +1072,7 @@ __device__ bool children_groups(const Params& p, int w, const Job* jl, unsigned 
       const ReqView R = req_view(p.rstate + static_cast<size_t>(jb.b) * RL.bytes, RL);
       const int kc = min(KM, jb.pslot < 0 ? n : n - s_ctl[cm].s - 1);
       Node* out = R.kids + static_cast<size_t>(jb.xslot) * KM;
-      if (M <= 32) rank_children_warp<1>(kr, kk, M, out, kc);
-      else if (M <= 64) rank_children_warp<2>(kr, kk, M, out, kc);
-      else rank_children_warp<4>(kr, kk, M, out, kc);
+      rank_children(kr, kk, M, p.V, out, kc);
       if (lane == 0) R.kcount[jb.xslot] = kc;
     }
     gr = next;
