@@ -977,9 +977,10 @@ __device__ bool children_groups(const Params& p, int w, const Job* jl, unsigned 
     }
     __syncthreads();
     // Z[M][8] = rows . [h_0 .. h_7], columns j >= J unused. The 16-row tiles times `ks` K parts make the warps' work
-    // (ks = 8 / tiles, so every warp has a share when M < 128); each warp runs two accumulator chains (even and odd
-    // k16 steps) and stores its partial tile; the partials are then added in a fixed order (part 0 first, even chain
-    // before odd), the same for every group, so Z does not depend on how many columns are in use.
+    // (ks = 8 / tiles, so every warp has a share when M < 128); each warp runs four accumulator chains (even and odd
+    // k16 steps, hi and lo halves) and stores its partial tile; the partials are then added in a fixed order (part 0
+    // first; even chain before odd, hi before lo), the same for every group, so Z does not depend on how many columns
+    // are in use.
     {
       const int g = lane >> 2, tg = lane & 3;
       const int tiles = (M + 15) / 16, ks = tiles >= kWarps ? 1 : kWarps / tiles, steps = H / 16;
@@ -990,26 +991,28 @@ __device__ bool children_groups(const Params& p, int w, const Job* jl, unsigned 
         const int r0 = min(mt * 16 + g, M - 1), r1 = min(mt * 16 + g + 8, M - 1);
         const unsigned short* a_lo = rows_s + static_cast<size_t>(r0) * SW + tg * 2;
         const unsigned short* a_hi = rows_s + static_cast<size_t>(r1) * SW + tg * 2;
-        float de[4] = {0.f, 0.f, 0.f, 0.f}, dodd[4] = {0.f, 0.f, 0.f, 0.f};
-        auto step = [&](int st, float (&d)[4]) {
+        // four accumulator chains: even and odd k16 steps, each with the hi and the lo halves apart
+        float eh[4] = {0.f, 0.f, 0.f, 0.f}, el[4] = {0.f, 0.f, 0.f, 0.f};
+        float oh[4] = {0.f, 0.f, 0.f, 0.f}, ol[4] = {0.f, 0.f, 0.f, 0.f};
+        auto step = [&](int st, float (&dh)[4], float (&dl)[4]) {
           const int kk = st * 16;
           const uint32_t a0 = lds32(a_lo + kk), a1 = lds32(a_hi + kk), a2 = lds32(a_lo + kk + 8), a3 = lds32(a_hi + kk + 8);
           const uint4 f = bfrag[st * 32 + lane];
-          mma_bf16_16816(d, a0, a1, a2, a3, f.x, f.y);
-          mma_bf16_16816(d, a0, a1, a2, a3, f.z, f.w);
+          mma_bf16_16816(dh, a0, a1, a2, a3, f.x, f.y);
+          mma_bf16_16816(dl, a0, a1, a2, a3, f.z, f.w);
         };
         int st = s0;
         for (; st + 1 < s1; st += 2) {
-          step(st, de);
-          step(st + 1, dodd);
+          step(st, eh, el);
+          step(st + 1, oh, ol);
         }
-        if (st < s1) step(st, de);
-        // this item's partial tile: rows g, g + 8 and columns 2 tg, 2 tg + 1 of tile mt
+        if (st < s1) step(st, eh, el);
+        // this item's partial tile: rows g, g + 8 and columns 2 tg, 2 tg + 1 of tile mt, the chains added in order
         float* zt = zp + static_cast<size_t>(item) * 16 * kLargeLookahead;
-        zt[g * kLargeLookahead + 2 * tg] = de[0] + dodd[0];
-        zt[g * kLargeLookahead + 2 * tg + 1] = de[1] + dodd[1];
-        zt[(g + 8) * kLargeLookahead + 2 * tg] = de[2] + dodd[2];
-        zt[(g + 8) * kLargeLookahead + 2 * tg + 1] = de[3] + dodd[3];
+        zt[g * kLargeLookahead + 2 * tg] = (eh[0] + el[0]) + (oh[0] + ol[0]);
+        zt[g * kLargeLookahead + 2 * tg + 1] = (eh[1] + el[1]) + (oh[1] + ol[1]);
+        zt[(g + 8) * kLargeLookahead + 2 * tg] = (eh[2] + el[2]) + (oh[2] + ol[2]);
+        zt[(g + 8) * kLargeLookahead + 2 * tg + 1] = (eh[3] + el[3]) + (oh[3] + ol[3]);
       }
       __syncthreads();
       const float* vals = vals2 + cb * M4;
