@@ -41,7 +41,9 @@ struct Job {
   int depth;    // its depth: the children take block position `depth`
   float score;  // its cumulative score
   int aux[2];   // aux[0], small-batch builder: 1 + the node's candidate index among the root's children when wave 0
-                // expands it speculatively (its score is known only once the root's children are scored), else 0
+                // expands it speculatively (its score is known only once the root's children are scored), else 0;
+                // aux[1], a lookahead pick: 1 + the index of its entry in the request's children lists (its parent's
+                // list), 0 when it sits in the merged list
 };
 
 // Expansions of one request at one block position, consecutive in a wave's packed list: they share the M correction
@@ -283,7 +285,8 @@ __device__ inline void request_step(const ReqView& R, int b, int n, int M, int m
         R.sdepth[x] = depth;
         R.popidx[x] = -2;
         R.kcount[x] = 0;
-        const Job jb{b, x, sc.hd.pslot, sc.hd.token, depth, sc.hd.score, {0, 0}};
+        const int kid = ss.src >= 0 ? 1 + ss.src * KM + ss.idx : 0;
+        const Job jb{b, x, sc.hd.pslot, sc.hd.token, depth, sc.hd.score, {0, kid}};
         jobs_out[njobs] = jb;
         on_pick(njobs, jb);
       }

@@ -1285,6 +1285,12 @@ __device__ bool control_phase(const Params& p, int w, unsigned char* smem, uint6
           }
           s_off[warp] = off;
           s_cnt[warp] = nj;
+          // a pick marked in its parent's children list: the mark goes to the workspace copy directly, because the
+          // children lists are not written back with the rest of the block (they change only in those marks)
+          Node* kids_g = reinterpret_cast<Node*>(p.rstate + static_cast<size_t>(b) * RL.bytes + RL.kids);
+          for (int q = 0; q < nj; ++q)
+            if (jobs[q].aux[1] > 0) kids_g[jobs[q].aux[1] - 1].xslot = static_cast<short>(jobs[q].xslot);
+          asm volatile("fence.proxy.async.global;" ::: "memory");  // read back by the next wave's bulk copy
         }
       }
     }
@@ -1369,11 +1375,14 @@ __device__ bool control_phase(const Params& p, int w, unsigned char* smem, uint6
           p.mask[(o + row) * n + c] = a == c;
         }
       }
-      // the state block goes back (one bulk copy; all of the batch's complete before the buffers are reused)
+      // the state block goes back but for its children lists (two bulk copies; all of the batch's complete before
+      // the buffers are reused): the children phase writes the lists, and the picks' marks went out above
       __syncthreads();
       if (t == 0) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        bulk_s2g(p.rstate + static_cast<size_t>(b) * RL.bytes, base, static_cast<unsigned>(RL.bytes));
+        unsigned char* gb = p.rstate + static_cast<size_t>(b) * RL.bytes;
+        bulk_s2g(gb, base, static_cast<unsigned>(RL.kids));
+        bulk_s2g(gb + RL.kcount, base + RL.kcount, static_cast<unsigned>(RL.bytes - RL.kcount));
         asm volatile("cp.async.bulk.commit_group;" ::: "memory");
       }
     }
