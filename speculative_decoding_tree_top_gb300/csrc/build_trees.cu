@@ -1285,12 +1285,6 @@ __device__ bool control_phase(const Params& p, int w, unsigned char* smem, uint6
           }
           s_off[warp] = off;
           s_cnt[warp] = nj;
-          // a pick marked in its parent's children list: the mark goes to the workspace copy directly, because the
-          // children lists are not written back with the rest of the block (they change only in those marks)
-          Node* kids_g = reinterpret_cast<Node*>(p.rstate + static_cast<size_t>(b) * RL.bytes + RL.kids);
-          for (int q = 0; q < nj; ++q)
-            if (jobs[q].aux[1] > 0) kids_g[jobs[q].aux[1] - 1].xslot = static_cast<short>(jobs[q].xslot);
-          asm volatile("fence.proxy.async.global;" ::: "memory");  // read back by the next wave's bulk copy
         }
       }
     }
@@ -1375,14 +1369,21 @@ __device__ bool control_phase(const Params& p, int w, unsigned char* smem, uint6
           p.mask[(o + row) * n + c] = a == c;
         }
       }
-      // the state block goes back but for its children lists (two bulk copies; all of the batch's complete before
-      // the buffers are reused): the children phase writes the lists, and the picks' marks went out above
+      // the state block goes back but for its children lists (bulk copies; all of the batch's complete before the
+      // buffers are reused): the children phase writes the lists, and the lists change here only where a lookahead
+      // pick was marked as expanded, one 16-byte entry per such pick
       __syncthreads();
       if (t == 0) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         unsigned char* gb = p.rstate + static_cast<size_t>(b) * RL.bytes;
         bulk_s2g(gb, base, static_cast<unsigned>(RL.kids));
         bulk_s2g(gb + RL.kcount, base + RL.kcount, static_cast<unsigned>(RL.bytes - RL.kcount));
+        const Job* jobs = reinterpret_cast<const Job*>(base + RL.jobs);
+        for (int q = 0; q < s_cnt[i]; ++q)
+          if (jobs[q].aux[1] > 0) {
+            const size_t at = RL.kids + static_cast<size_t>(jobs[q].aux[1] - 1) * sizeof(Node);
+            bulk_s2g(gb + at, base + at, static_cast<unsigned>(sizeof(Node)));
+          }
         asm volatile("cp.async.bulk.commit_group;" ::: "memory");
       }
     }
