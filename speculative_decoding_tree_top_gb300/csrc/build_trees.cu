@@ -424,15 +424,51 @@ __device__ __forceinline__ void bulk_s2g(void* gdst, const void* ssrc, unsigned 
                : "memory");
 }
 
+// ---- the first children group of a CTA, loaded while the wave's GRU runs -------------------------------------------
+// During the tensor-core GRU phase warps 2 and 3 have no role; warp 2 loads this CTA's first group of the wave (its
+// entry, ids and base logits, jobs and the request's control word) into a static shared buffer, so that the
+// children phase starts on its row copies at once.
+struct GroupPrefetch {
+  int valid, ngroups;
+  JobGroup gr;
+  ReqCtl ctl;
+  Job jobs[kLargeLookahead];
+  int ids[128];
+  float vals[128];
+};
+__device__ void prefetch_first_group(const Params& p, int w, const Job* jl, GroupPrefetch* pf) {
+  const int lane = threadIdx.x & 31;
+  const int M = p.M, n = p.n, KM = M < n ? M : n;
+  const JobGroup* gl = p.grouplist + static_cast<size_t>(w & 1) * p.B * p.lookahead;
+  JobGroup gr{};
+  if (static_cast<int>(blockIdx.x) < p.B * p.lookahead) gr = gl[blockIdx.x];
+  const int ng = __ldcg(p.groupcount + w);
+  if (static_cast<int>(blockIdx.x) >= ng || M > 128) return;  // valid stays 0
+  const size_t pos = (static_cast<size_t>(gr.b) * p.K + gr.depth) * M;
+  for (int m = lane; m < M; m += 32) {
+    pf->ids[m] = valid_id(p, __ldg(p.ids + pos + m));
+    pf->vals[m] = __ldg(p.vals + pos + m);
+  }
+  if (lane < gr.count) pf->jobs[lane] = jl[gr.start + lane];
+  if (lane == 0) {
+    const ReqLayout RL = req_layout(n, p.xslots, KM, p.lookahead);
+    pf->ctl = *reinterpret_cast<const ReqCtl*>(p.rstate + static_cast<size_t>(gr.b) * RL.bytes + RL.ctl);
+    pf->gr = gr;
+    pf->ngroups = ng;
+  }
+  __syncwarp();
+  if (lane == 0) pf->valid = 1;
+}
+
 // ---- phase A on the 5th-generation tensor cores (tcgen05, TMEM, 2-D TMA) ---------------------------------------
-// One tile = 128 expansions (rows) x 32 hidden units. The A operand is the packed activations [emb | hi(h) | lo(h)]
-// of the wave (bf16, written by the control phase that picked the expansions), the B operand the r, z, n gate rows of
-// the tile's units in W_ih / W_hh, both K-major, moved by TMA in 64-column blocks with 128-byte swizzle through an
-// 8-stage ring of full / empty mbarriers. One lane issues the TMA loads, one lane the MMAs (kind::f16, fp32 accumulate
-// in TMEM): embedding blocks into TMEM columns [0, 96) = r | z | n_in (N = 96), hidden blocks (hi, then lo: the fp32
-// parent state to 2^-16) into [0, 64) = r | z (N = 64) and [96, 128) = n_h (N = 32), which the GRU keeps apart; each
-// K partial (below) has its own 128 columns. All eight warps read the tile back (tcgen05.ld, one row per thread,
-// warps w and w + 4 on the same TMEM lanes with half of the units each) and finish the GRU step.
+// One narrow tile = 128 expansions (rows) x 32 hidden units. The A operand is the packed activations
+// [emb | hi(h) | lo(h)] of the wave (bf16, written by the control phase that picked the expansions; hi + lo carry the
+// fp32 parent state to 2^-16), the B operand the gate rows [r | z | n_in | n_h] of the tile's units in W_ih / W_hh,
+// both K-major, moved by TMA in 64-column blocks with 128-byte swizzle through a 6-stage ring of full / empty
+// mbarriers. One lane issues the TMA loads, one lane the MMAs (kind::f16, N = 128, fp32 accumulate in TMEM); each K
+// partial (below) has its own 128 columns. All eight warps read the tile back (tcgen05.ld, one row per thread, warps
+// w and w + 4 on the same TMEM lanes with half of the units each) and finish the GRU step. Waves of whole tiles run
+// on wide tiles instead (umma_gru_wide).
 struct TmaMaps {
   CUtensorMap x;      // [rows cap][E + 2H] bf16, box 64 x 128
   CUtensorMap wih;    // [3H][E] bf16, box 64 x 32
@@ -440,7 +476,7 @@ struct TmaMaps {
   CUtensorMap wih64;  // the same weights in boxes of 64 x 64 (wide tiles)
   CUtensorMap whh64;
 };
-constexpr int kUmmaRows = 128, kUmmaUnits = 32, kUmmaBK = 64, kUmmaStages = 7;
+constexpr int kUmmaRows = 128, kUmmaUnits = 32, kUmmaBK = 64, kUmmaStages = 6;
 constexpr int kUmmaA = kUmmaRows * kUmmaBK * 2;            // 16 KB
 // The B tile of a K block: the weight rows of the gate columns [r | z | n_in | n_h] of the tile's units, the set a
 // block does not touch (n_h for an embedding block, n_in for a hidden one) read as zeros, so that one MMA of N = 128
@@ -721,13 +757,14 @@ __device__ bool umma_gru_wide(const Params& p, const TmaMaps& maps, const Job* j
 
 // Returns false when a wait ran out (recorded, abort raised).
 __device__ bool umma_gru_phase(const Params& p, const TmaMaps& maps, const Job* jl, int rows, unsigned char* smem,
-                               UmmaRing& ring) {
+                               UmmaRing& ring, int w, GroupPrefetch* pf) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int E = p.E, H = p.H, X = p.xslots;
   const int nE = E / kUmmaBK, nH = H / kUmmaBK, nkb = nE + 2 * nH;
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem) + 1023) & ~uintptr_t(1023));
   const int rtiles = (rows + kUmmaRows - 1) / kUmmaRows, utiles = H / kUmmaUnits, tiles = rtiles * utiles;
   const int G = static_cast<int>(gridDim.x);
+  if (p.group_mma && warp == 2) prefetch_first_group(p, w, jl, pf);  // a warp with no role in either path
   if (tiles > p.gru_tiles && H % kWideUnits == 0) return umma_gru_wide(p, maps, jl, rows, smem, ring);
   const int per = tiles > p.gru_tiles ? kSplits : tiles * kSplits <= G ? 1 : tiles * (kSplits / 2) <= G ? 2 : kSplits;
   const int cpt = kSplits / per;  // CTAs per tile
@@ -877,7 +914,7 @@ __device__ __forceinline__ bool wait_copies(const Params& p, uint64_t* bar, unsi
 __device__ __forceinline__ void prefetch_l2_line(const void* src) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
 }
-__device__ bool children_groups(const Params& p, int w, const Job* jl, unsigned char* smem) {
+__device__ bool children_groups(const Params& p, int w, const Job* jl, unsigned char* smem, GroupPrefetch* pf) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int M = p.M, n = p.n, H = p.H, X = p.xslots, KM = M < n ? M : n;
   const ReqLayout RL = req_layout(n, X, KM, p.lookahead);
@@ -897,11 +934,18 @@ __device__ bool children_groups(const Params& p, int w, const Job* jl, unsigned 
   const size_t rb = static_cast<size_t>(H) * 2;
   const int G = static_cast<int>(gridDim.x);
   const JobGroup* gl = p.grouplist + static_cast<size_t>(w & 1) * p.B * p.lookahead;
-  // the wave's group count and this CTA's first group, read together: the list's slot exists even when the group
-  // does not (then it holds an older wave's entry, unused)
+  // the wave's group count and this CTA's first group: loaded during the GRU phase (pf), else read together here
+  // (the list's slot exists even when the group does not: then it holds an older wave's entry, unused)
+  const bool pre = pf->valid != 0;
   JobGroup gr{};
-  if (static_cast<int>(blockIdx.x) < p.B * p.lookahead) gr = gl[blockIdx.x];
-  const int ngroups = __ldcg(p.groupcount + w);
+  int ngroups;
+  if (pre) {
+    gr = pf->gr;
+    ngroups = pf->ngroups;
+  } else {
+    if (static_cast<int>(blockIdx.x) < p.B * p.lookahead) gr = gl[blockIdx.x];
+    ngroups = __ldcg(p.groupcount + w);
+  }
   if (static_cast<int>(blockIdx.x) >= ngroups) return true;
   auto cand_pos = [&](const JobGroup& g) { return (static_cast<size_t>(g.b) * p.K + g.depth) * M; };
   // a group's jobs (32 bytes each) and its request's control word, as 16-byte copies into buffer `slot`
@@ -928,15 +972,24 @@ __device__ bool children_groups(const Params& p, int w, const Job* jl, unsigned 
   // prologue: the first group's ids, jobs and inputs; the second's ids (registers) and jobs
   int nid = 0;
   float nval = 0.f;
-  if (t < M) {
-    nid = __ldg(p.ids + cand_pos(gr) + t);
-    nval = __ldg(p.vals + cand_pos(gr) + t);
-  }
-  copy_meta(gr, 0);
-  cp_async_commit();
-  if (t < M) {
-    ids2[t] = valid_id(p, nid);
-    vals2[t] = nval;
+  if (pre) {
+    if (t < M) {
+      ids2[t] = pf->ids[t];
+      vals2[t] = pf->vals[t];
+    }
+    if (t < gr.count) s_jobs[t] = pf->jobs[t];
+    if (t == 0) s_ctl[0] = pf->ctl;
+  } else {
+    if (t < M) {
+      nid = __ldg(p.ids + cand_pos(gr) + t);
+      nval = __ldg(p.vals + cand_pos(gr) + t);
+    }
+    copy_meta(gr, 0);
+    cp_async_commit();
+    if (t < M) {
+      ids2[t] = valid_id(p, nid);
+      vals2[t] = nval;
+    }
   }
   JobGroup next{};
   if (static_cast<int>(blockIdx.x) + G < ngroups) {
@@ -1435,7 +1488,7 @@ __device__ void init_requests(const Params& p, unsigned char* smem) {
 
 // The waves of one launch; every way out (done, or a wait that ran out) returns here in every thread of the CTA.
 template <int kGemm>
-__device__ void run_waves(const Params& p, const TmaMaps& maps, unsigned char* smem, UmmaRing& ring,
+__device__ void run_waves(const Params& p, const TmaMaps& maps, unsigned char* smem, UmmaRing& ring, GroupPrefetch* pf,
                           unsigned long long base_count, uint64_t* bar, int* s_flag) {
   unsigned bar_uses = 0;
   const unsigned G = gridDim.x;
@@ -1455,7 +1508,7 @@ __device__ void run_waves(const Params& p, const TmaMaps& maps, unsigned char* s
     const Job* jl = p.joblist + static_cast<size_t>(w & 1) * p.B * p.lookahead;
     if (w > 0) {  // wave 0 expands the roots, whose hidden state is h0: no GRU step
       if (kGemm == 4) {
-        if (!umma_gru_phase(p, maps, jl, rows, smem, ring)) return;
+        if (!umma_gru_phase(p, maps, jl, rows, smem, ring, w, pf)) return;
       } else if (kGemm == 1) {
         gemm_gru_phase<TileS, 32, 8>(p, jl, rows, smem);
       } else if (kGemm == 2) {
@@ -1472,7 +1525,8 @@ __device__ void run_waves(const Params& p, const TmaMaps& maps, unsigned char* s
         for (int i = threadIdx.x; i < p.gru_tiles; i += kThreads) p.gru_ticket[i] = 0u;
     }
     const uint64_t c0 = global_timer_ns();
-    if (!(p.group_mma ? children_groups(p, w, jl, smem) : children_phase(p, jl, rows, smem, bar, bar_uses))) return;
+    if (!(p.group_mma ? children_groups(p, w, jl, smem, pf) : children_phase(p, jl, rows, smem, bar, bar_uses))) return;
+    if (threadIdx.x == 0) pf->valid = 0;  // used once (read before the barrier that follows)
     __syncthreads();
     gather_ns += global_timer_ns() - c0;
     ++waves;
@@ -1512,7 +1566,9 @@ __global__ void __launch_bounds__(kThreads, 1) build_kernel(Params p, const __gr
   __shared__ uint64_t ufull[kUmmaStages], uempty[kUmmaStages], udone;
   __shared__ uint64_t wfull[kWideStages], wempty[kWideStages], umid, ur1free;
   __shared__ uint32_t s_tmem;
+  __shared__ GroupPrefetch s_pf;
   if (threadIdx.x == 0) {
+    s_pf.valid = 0;
     s_base = ld_relaxed_gpu_u64(&p.hdr->sync_count);  // before anyone can pass the first barrier
     mbar_init(&bar, 1);
     if (kGemm == 4) {
@@ -1539,7 +1595,7 @@ __global__ void __launch_bounds__(kThreads, 1) build_kernel(Params p, const __gr
   __syncthreads();
   if (kGemm == 4) asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   UmmaRing ring{ufull, uempty, &udone, wfull, wempty, &umid, &ur1free, kGemm == 4 ? s_tmem : 0u, 0u, 0u, 0u};
-  run_waves<kGemm>(p, maps, smem, ring, s_base, &bar, &s_flag);
+  run_waves<kGemm>(p, maps, smem, ring, &s_pf, s_base, &bar, &s_flag);
   if (kGemm == 4) {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
@@ -1684,7 +1740,11 @@ dt_status build_trees(int B, int K, int V, int M, int n, int max_depth, float T,
   const long long max_rows = static_cast<long long>(B) * p.lookahead;
   // tcgen05 tiles (128 expansions x 32 units) for every bf16 wave whose widths fit them: the K split makes the sums
   // independent of the wave's size, so the tree does not depend on the lookahead width
-  const bool umma = p.bf16 && E % kUmmaBK == 0 && H % kUmmaBK == 0 && kUmmaSmem + 2048 <= static_cast<size_t>(di.optin);
+  // the kernel's static shared memory (flags, barriers, reductions, the children phase's first-group prefetch) is
+  // under kStaticSmem; one CTA per SM (launch bounds), so the shared memory alone decides whether a CTA fits
+  constexpr size_t kStaticSmem = 3072;
+  const bool umma =
+      p.bf16 && E % kUmmaBK == 0 && H % kUmmaBK == 0 && kUmmaSmem + kStaticSmem <= static_cast<size_t>(di.optin);
   const int gemm = !p.bf16 ? 0
                    : umma ? 4
                    : max_rows >= 128 ? (E % TileL::kKc == 0 && H % TileL::kKc == 0 ? 2 : 0)
@@ -1699,9 +1759,7 @@ dt_status build_trees(int B, int K, int V, int M, int n, int max_depth, float T,
   p.xact_on = gemm == 4;
   if (gemm == 4 && !gru_tensor_maps(&maps, p.xact, static_cast<uint64_t>(B) * kLargeLookahead, w->w_ih, w->w_hh, E, H))
     return DT_ERR_CUDA;
-  // static shared memory of the kernel (flags, barriers, reductions) is under 2 KB; one CTA per SM (launch bounds), so
-  // the shared memory alone decides whether a CTA fits
-  size_t smem = smem_bytes(gemm, M, n, H, p.lookahead, p.bf16 ? 2 : 4, static_cast<size_t>(di.optin) - 2048,
+  size_t smem = smem_bytes(gemm, M, n, H, p.lookahead, p.bf16 ? 2 : 4, static_cast<size_t>(di.optin) - kStaticSmem,
                            &p.rows_smem);
   // the children phase by groups on the tensor cores when its buffers fit the same budget
   // groups spread over all CTAs (g mod G) whatever the batch: a request's groups on its owner CTA left the CTAs that
@@ -1710,7 +1768,7 @@ dt_status build_trees(int B, int K, int V, int M, int n, int max_depth, float T,
     const ReqLayout RL = req_layout(n, p.xslots, M < n ? M : n, p.lookahead);
     const size_t rstride = (RL.bytes + 127) / 128 * 128;
     const int owned = (B + di.sms - 1) / di.sms;
-    const int fit = static_cast<int>((static_cast<size_t>(di.optin) - 2048) / rstride);
+    const int fit = static_cast<int>((static_cast<size_t>(di.optin) - kStaticSmem) / rstride);
     p.ctl_conc = owned < fit ? owned : fit;
     if (p.ctl_conc > kWarps) p.ctl_conc = kWarps;
     if (p.ctl_conc < 1) p.ctl_conc = 1;
@@ -1719,7 +1777,7 @@ dt_status build_trees(int B, int K, int V, int M, int n, int max_depth, float T,
     if (p.xact_on) {  // staging slots for the picks' activation rows after the state blocks: all of a batch's picks
       // at once when they fit, else as many as fit (at least one)
       const size_t pick = static_cast<size_t>(E) * 2 + static_cast<size_t>(H) * 4;
-      const size_t cap = static_cast<size_t>(di.optin) - 2048;
+      const size_t cap = static_cast<size_t>(di.optin) - kStaticSmem;
       while (p.ctl_conc > 1 && rstride * p.ctl_conc + pick > cap) --p.ctl_conc;
       if (rstride * p.ctl_conc + pick > cap) return DT_ERR_UNSUPPORTED;
       const size_t room = (cap - rstride * p.ctl_conc) / pick;
@@ -1730,9 +1788,9 @@ dt_status build_trees(int B, int K, int V, int M, int n, int max_depth, float T,
     if (smem < need) smem = need;
   }
   p.group_mma = p.bf16 && H % 16 == 0 && M <= 128 &&
-                group_smem(M, H).bytes + 2048 <= static_cast<size_t>(di.optin);
+                group_smem(M, H).bytes + kStaticSmem <= static_cast<size_t>(di.optin);
   if (p.group_mma && group_smem(M, H).bytes > smem) smem = group_smem(M, H).bytes;
-  if (smem + 2048 > static_cast<size_t>(di.optin)) return DT_ERR_UNSUPPORTED;
+  if (smem + kStaticSmem > static_cast<size_t>(di.optin)) return DT_ERR_UNSUPPORTED;
   if (mode == BuildMode::kCheck) return DT_OK;
   if (ensure_dynamic_smem(fn, smem) != cudaSuccess) return DT_ERR_CUDA;
   const unsigned grid = static_cast<unsigned>(di.sms);  // one CTA per SM; co-resident under a cooperative launch
