@@ -426,8 +426,8 @@ __device__ __forceinline__ void bulk_s2g(void* gdst, const void* ssrc, unsigned 
 
 // ---- the first children group of a CTA, loaded while the wave's GRU runs -------------------------------------------
 // During the tensor-core GRU phase warps 2 and 3 have no role; warp 2 loads this CTA's first group of the wave (its
-// entry, ids and base logits, jobs and the request's control word) into a static shared buffer, so that the
-// children phase starts on its row copies at once.
+// entry, ids and base logits, jobs and the request's control word) into a static shared buffer and asks L2 for the
+// group's correction rows, so that the children phase starts on its row copies at once.
 struct GroupPrefetch {
   int valid, ngroups;
   JobGroup gr;
@@ -445,9 +445,13 @@ __device__ void prefetch_first_group(const Params& p, int w, const Job* jl, Grou
   const int ng = __ldcg(p.groupcount + w);
   if (static_cast<int>(blockIdx.x) >= ng || M > 128) return;  // valid stays 0
   const size_t pos = (static_cast<size_t>(gr.b) * p.K + gr.depth) * M;
+  const size_t rb = static_cast<size_t>(p.H) * 2;
   for (int m = lane; m < M; m += 32) {
-    pf->ids[m] = valid_id(p, __ldg(p.ids + pos + m));
+    const int id = valid_id(p, __ldg(p.ids + pos + m));
+    pf->ids[m] = id;
     pf->vals[m] = __ldg(p.vals + pos + m);
+    const char* row = static_cast<const char*>(p.w_c) + static_cast<size_t>(id) * rb;  // its row, asked of L2
+    for (size_t c = 0; c < rb; c += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + c));
   }
   if (lane < gr.count) pf->jobs[lane] = jl[gr.start + lane];
   if (lane == 0) {
