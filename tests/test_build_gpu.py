@@ -63,6 +63,8 @@ def tiny(seed, **kw):
     dict(dtype="bf16", M=40, n=64, max_depth=5, K=5),    # a wide, deep frontier
     dict(B=3, V=9000, M=100, n=40, T=1.0, logit_scale=0.5),
     dict(dtype="bf16", B=20, E=64, H=64, n=20),          # tensor-core GRU with fewer K blocks than K splits
+    dict(dtype="bf16", B=153, E=128, H=64, M=16, n=20),  # tensor-core GRU, one CTA owning two requests (a batched
+                                                         # control phase and its staged activation rows)
 ])
 def test_build_edge_cases(dtlib, orc, kw):
     inp = tiny(abs(hash(str(sorted(kw.items())))) % 10000, **kw)
