@@ -1,5 +1,7 @@
 """dt_build_trees on the GPU against the CPU oracle: structure bit-exact up to the first near-tie (gap <= 1e-3),
 scores within 1e-3 of the oracle's fp64 rescoring of the GPU's own tree, tree invariants everywhere."""
+import zlib
+
 import numpy as np
 import pytest
 import torch
@@ -67,7 +69,7 @@ def tiny(seed, **kw):
                                                          # control phase and its staged activation rows)
 ])
 def test_build_edge_cases(dtlib, orc, kw):
-    inp = tiny(abs(hash(str(sorted(kw.items())))) % 10000, **kw)
+    inp = tiny(zlib.crc32(str(sorted(kw.items())).encode()) % 10000, **kw)  # a seed fixed by the case
     run_both(dtlib, orc, inp)
 
 
