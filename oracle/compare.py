@@ -5,6 +5,12 @@ score minus the best score left in the oracle's frontier) is at most ``tol``. Be
 same clear-cut decisions, so tokens, parents, depths and mask rows must be bit-identical and the scores within
 ``tol``. Every GPU score must be within ``tol`` of the oracle's fp64 rescoring of the GPU's own path, and from i* on
 the GPU tree must satisfy the tree invariants and its sorted scores must match the oracle's within ``tol``.
+
+Past i* the node sets are still compared, in a form ties cannot upset (``check_top_nodes``). Scores never rise along
+a path (a log-softmax is at most 0, in fp32 as in fp64), so best-first pops the n highest-scoring nodes of the tree:
+every node whose exact score is above the oracle's n-th score s_n is one of the oracle's pops, and every node whose
+exact score is above s_n + 2 tol is one of the GPU's too (were one missing, the GPU's n pops, each scoring at least
+that node's fp32 score and hence more than s_n exactly, would be n + 1 nodes above s_n with it).
 """
 from __future__ import annotations
 
@@ -32,6 +38,32 @@ def check_tree_invariants(tokens, parents, depth, scores, mask, n, max_depth):
     assert np.all(np.diff(scores) <= 0), "pops are not in best-first order"
 
 
+def _paths(tokens, parents):
+    paths = []
+    for i, t in enumerate(tokens):
+        p = int(parents[i])
+        paths.append((paths[p] if p >= 0 else ()) + (int(t),))
+    return paths
+
+
+def check_top_nodes(gpu_tokens, gpu_parents, rescored, ora_tokens, ora_parents, ora_scores, tol):
+    """The tie-robust node-set check (module docstring): nodes are token paths from the root. Every oracle node
+    scoring above s_n + 2 tol is in the GPU tree, and every GPU node whose fp64 rescoring is above s_n is in the
+    oracle tree. Returns the share of the oracle's nodes the first part covers."""
+    gp = _paths(gpu_tokens, gpu_parents)
+    op = _paths(ora_tokens, ora_parents)
+    s_n = float(np.min(ora_scores))
+    gset, oset = set(gp), set(op)
+    covered = 0
+    for path, s in zip(op, ora_scores):
+        if s > s_n + 2 * tol:
+            covered += 1
+            assert path in gset, f"the oracle's node {path} (score {s}, n-th {s_n}) is missing from the GPU tree"
+    for path, s in zip(gp, rescored):
+        assert s <= s_n + 1e-9 or path in oset, f"the GPU's node {path} scores {s} above the n-th {s_n} yet is not in the oracle tree"
+    return covered / len(op)
+
+
 def compare_request(gpu: dict, ora: dict, rescored: np.ndarray, n: int, max_depth: int, tol: float = 1e-3,
                     struct_tol=None) -> dict:
     """gpu/ora: per-request arrays; rescored: oracle fp64 scores of the GPU's tree. Returns a small report.
@@ -51,7 +83,8 @@ def compare_request(gpu: dict, ora: dict, rescored: np.ndarray, n: int, max_dept
     check_tree_invariants(gpu["tokens"], gpu["parents"], gpu["depth"], gpu["scores"], gpu["mask"], n, max_depth)
     err_sorted = float(np.max(np.abs(np.sort(gpu["scores"].astype(np.float64)) - np.sort(ora["scores"]))))
     assert err_sorted <= tol, f"sorted scores differ by {err_sorted}"
-    return dict(i_star=i_star, err_own=err_own, err_sorted=err_sorted)
+    top = check_top_nodes(gpu["tokens"], gpu["parents"], rescored, ora["tokens"], ora["parents"], ora["scores"], tol)
+    return dict(i_star=i_star, err_own=err_own, err_sorted=err_sorted, top_nodes=top)
 
 
 def compare_round(gpu: dict, ora: dict, rescored: np.ndarray, n: int, max_depth: int, tol: float = 1e-3,
@@ -69,5 +102,6 @@ def compare_round(gpu: dict, ora: dict, rescored: np.ndarray, n: int, max_depth:
     full = sum(r["i_star"] == n for r in reports)
     compared = sum(r["i_star"] for r in reports)
     return dict(requests=B, exact_structure=full, compared_pops=compared / (B * n),
+                top_nodes=sum(r["top_nodes"] for r in reports) / B,
                 min_i_star=min(r["i_star"] for r in reports),
                 max_err_own=max(r["err_own"] for r in reports), max_err_sorted=max(r["err_sorted"] for r in reports))

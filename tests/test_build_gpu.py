@@ -43,8 +43,10 @@ def test_build_parity_workloads(dtlib, orc, config):
     rep, *_ = run_both(dtlib, orc, inp)
     print(config, rep)
     # not vacuous: under the stricter pass most pops are compared bit-exactly (the rest follow a genuine
-    # near-tie of the oracle, where either choice is correct)
-    assert rep["compared_pops"] >= 0.5 and rep["compared_pops_strict"] >= 0.8
+    # near-tie of the oracle, where either choice is correct), and past the first near-tie every node clear of the
+    # n-th score is in both trees (on these workloads the node-set check covers all but the nodes at the boundary,
+    # 0.875-0.98 of them)
+    assert rep["compared_pops"] >= 0.5 and rep["compared_pops_strict"] >= 0.8 and rep["top_nodes"] >= 0.5
 
 
 def tiny(seed, **kw):

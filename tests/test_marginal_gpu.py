@@ -1,6 +1,6 @@
 """dt_build_trees_marginal (DDTree's factorised scoring) on the GPU: parity with the CPU oracle's marginal builder
-(structure bit-exact up to the first near-tie, scores within 1e-3 of the oracle's fp64 rescoring of the GPU's own
-tree), and bit-identity with dt_build_trees when the correction head is zero."""
+(structure bit-exact up to the first near-tie, the node sets alike past it, scores within 1e-3 of the oracle's fp64
+rescoring of the GPU's own tree), and bit-identity with dt_build_trees when the correction head is zero."""
 import numpy as np
 import pytest
 import torch
@@ -41,10 +41,11 @@ def test_marginal_parity_workloads(dtlib, orc, config):
     inp = synth.make_inputs(config, device="cuda")
     rep, *_ = run_marginal(dtlib, orc, inp)
     print(config, rep)
-    # marginals of bf16 logits tie exactly and often (equal logits, equal log-probabilities), so the structure is
-    # compared bit-exactly only up to the first tie; the bit-exact check of the whole tree is the one against the
-    # conditional builder at W_c = 0 below
-    assert rep["compared_pops"] > 0 and rep["max_err_own"] < TOL
+    # marginals of bf16 logits tie exactly and often (equal logits, equal log-probabilities), so pop order is
+    # compared bit-exactly only up to the first tie; past it the node-set check holds every node clear of the n-th
+    # score to be in both trees (0.9-0.96 of the nodes on these workloads), and the bit-exact check of the whole
+    # tree is the one against the conditional builder at W_c = 0 below
+    assert rep["compared_pops"] > 0 and rep["max_err_own"] < TOL and rep["top_nodes"] >= 0.5
 
 
 @pytest.mark.parametrize("kw", [
