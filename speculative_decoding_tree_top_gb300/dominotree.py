@@ -468,6 +468,22 @@ class Round:
         _check(lib().dt_round(*self._round_args), "dt_round")
         return self.out
 
+    def capture(self, logits: torch.Tensor, h0: torch.Tensor) -> torch.cuda.CUDAGraph:
+        """One dt_round call on these tensors, captured as a CUDA graph (its two launches, the cluster top-M and the
+        cooperative builder, as graph nodes). ``replay()`` reruns the round on whatever ``logits`` and ``h0`` then
+        hold, into this round's ids/vals and outputs, without the per-launch host work. The addresses are fixed at
+        capture: new inputs go into the same tensors."""
+        side = torch.cuda.Stream(device=self.workspace.device)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            self.round(logits, h0)  # marshalled for the capture stream; the library's one-time set-up done
+        side.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            self.round(logits, h0)
+        torch.cuda.current_stream().wait_stream(side)
+        return g
+
     def __call__(self, logits: torch.Tensor, h0: torch.Tensor, stream=None) -> dict:
         return self.round(logits, h0, stream)
 

@@ -223,6 +223,35 @@ def test_round_matches_the_two_calls(dtlib, case):
         assert torch.equal(ref[-1][0][k], out[k]), k
 
 
+@pytest.mark.parametrize("case", [dict(config=1), dict(config=2, B=16)])
+def test_captured_round_replays_new_inputs(dtlib, case):
+    """Round.capture: the CUDA graph of one dt_round call (the top-M and the cooperative builder as graph nodes),
+    replayed after each round's inputs are written into the captured tensors, gives that round's direct results bit
+    for bit."""
+    s = synth.shape(case["config"], **{k: v for k, v in case.items() if k != "config"})
+    inputs = [synth.make_inputs(s, device="cuda", seed=60 + i) for i in range(3)]
+    rnd = dtlib.Round(s.B, s.K, s.V, s.M, s.n, s.max_depth, s.T, dtlib.Weights.of(inputs[0]))
+    ref = []
+    for inp in inputs:
+        out = rnd.round(inp.logits, inp.h0)
+        ref.append(({k: v.clone() for k, v in out.items()}, rnd.ids.clone(), rnd.vals.clone()))
+    torch.cuda.synchronize()
+    rnd.check()
+    logits, h0 = inputs[0].logits.clone(), inputs[0].h0.clone()
+    graph = rnd.capture(logits, h0)
+    for (ro, ri, rv), inp in zip(ref, inputs):
+        logits.copy_(inp.logits)
+        h0.copy_(inp.h0)
+        for v in rnd.out.values():
+            v.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        rnd.check()
+        assert torch.equal(rnd.ids, ri) and torch.equal(rnd.vals, rv)
+        for k in ro:
+            assert torch.equal(rnd.out[k], ro[k]), k
+
+
 @pytest.mark.parametrize("config", [1, 0])
 def test_host_round_matches_the_device_round(dtlib, config):
     """HostRound (inputs and outputs in one pinned buffer each, one copy each way) gives the device round's outputs
