@@ -586,6 +586,23 @@ def run_ours(args, world, rank, local):
         e2e = {"value": round(world * s.B * args.steps / e2e_s, 2), "unit": "trees/s",
                "h2d_bytes_per_step": hr.h2d_bytes(), "d2h_bytes_per_step": hr.d2h_bytes(),
                "us_per_round": round(e2e_s / args.steps * 1e6, 2)}
+        # the same host rounds replayed from their captured CUDA graph (HostRound.capture: the copy in, the round's
+        # launches and the copy out as graph nodes), up to 100 of them, L2 flushed before each
+        hgraph = hr.capture()
+        hevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(min(args.steps, 100))]
+        for a, b in hevs:
+            flush_l2()
+            a.record(stream)
+            hgraph.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        hr.check()
+        assert np.array_equal(hr.host_out["tokens"].numpy(), out["tokens"]), "replayed host round differs"
+        hg_us = float(np.mean([a.elapsed_time(b) for a, b in hevs])) * 1e3
+        e2e["graph_replay"] = {"us_per_round": round(hg_us, 2), "trees_per_s": round(world * s.B / (hg_us / 1e6), 2),
+                               "rounds": len(hevs)}
+        del hgraph
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not marginal:

@@ -541,3 +541,18 @@ class HostRound(Round):
         self(self.d_logits, self.d_h0, stream)
         self._hout.copy_(self._dout, non_blocking=True)
         return self.host_out
+
+    def capture(self) -> torch.cuda.CUDAGraph:
+        """``run()`` captured as a CUDA graph: the copy in, the round's two launches and the copy out as graph nodes.
+        ``replay()`` then runs a round on whatever ``host_logits`` / ``host_h0`` hold and leaves its tree in
+        ``host_out`` once the stream has been synchronised."""
+        side = torch.cuda.Stream(device=self.workspace.device)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            self.run()  # marshalled for the capture stream
+        side.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            self.run()
+        torch.cuda.current_stream().wait_stream(side)
+        return g

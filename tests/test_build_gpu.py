@@ -270,6 +270,31 @@ def test_host_round_matches_the_device_round(dtlib, config):
             assert torch.equal(ref[k], out[k]), k
 
 
+def test_captured_host_round_replays_new_inputs(dtlib):
+    """HostRound.capture: the graph of one host round (pinned copy in, dt_round, copy out), replayed after each round's
+    inputs are written into the pinned buffers, leaves that round's device results in host_out bit for bit."""
+    s = synth.shape(1)
+    inputs = [synth.make_inputs(s, device="cuda", seed=80 + i) for i in range(3)]
+    w = dtlib.Weights.of(inputs[0])
+    rnd = dtlib.Round(s.B, s.K, s.V, s.M, s.n, s.max_depth, s.T, w)
+    refs = [{k: v.cpu() for k, v in rnd(inp.logits, inp.h0).items()} for inp in inputs]
+    hr = dtlib.HostRound(s.B, s.K, s.V, s.M, s.n, s.max_depth, s.T, w, inputs[0].logits.dtype)
+    hr.host_logits.copy_(inputs[0].logits)
+    hr.host_h0.copy_(inputs[0].h0)
+    graph = hr.capture()
+    torch.cuda.synchronize()
+    for ref, inp in zip(refs, inputs):
+        hr.host_logits.copy_(inp.logits)
+        hr.host_h0.copy_(inp.h0)
+        for v in hr.host_out.values():
+            v.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        hr.check()
+        for k in ref:
+            assert torch.equal(ref[k], hr.host_out[k]), k
+
+
 @pytest.mark.parametrize("config", [1, 2])
 def test_build_stats_describe_the_launch(dtlib, config):
     """The statistics a builder launch records: its waves and expansions, and the correction rows it gathered."""
