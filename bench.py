@@ -12,6 +12,8 @@ flushed between steps outside the events by a 256 MB memset followed by a 256 MB
 written lines are not written back inside the next timed call); barrier + synchronize on both sides; max over
 ranks. ``e2e`` runs the same rounds through the host-buffer API (pinned logits
 and h0 copied in, the tree copied out, every step). The SM clock is sampled through NVML during the timed region.
+``graph_replay`` (and ``e2e.graph_replay``) time the same round (the same host round) replayed from its captured
+CUDA graph, after the timed loop; the headline stays the direct call.
 
 ``configs`` measures every workload (c0-c4) briefly in the same run: µs per round, trees/s, the top-M's and the gather
 stage's bandwidth (the builder's own statistics: correction-row bytes gathered over the longest time one CTA spent
