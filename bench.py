@@ -75,6 +75,30 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of every rank's x (a job's time is its slowest replica's), by one all-reduce on `device` (the
+    process group's: a GPU for NCCL, the CPU for gloo); x itself when there is one rank."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_seed(config: int, rank: int) -> int:
+    """Seed of a replica's synthetic inputs: rank 0 draws the workload's own inputs (those of one GPU), every other
+    rank a batch of its own."""
+    return 1234 + 100 * config + 7919 * rank
+
+
+def job_throughput(world: int, trees_per_round: int, rounds: int, seconds: float) -> float:
+    """Whole-job trees per second: every replica builds `trees_per_round` trees per round (weak scaling), and the job
+    takes as long as its slowest replica (`seconds`, already the maximum over ranks)."""
+    return world * trees_per_round * rounds / seconds
+
+
 # ---------------------------------------------------------------------------------------------------------------
 class ClockSampler:
     """SM clock and throttle reasons of one GPU, sampled by NVML in a thread (read-only queries)."""
@@ -314,7 +338,7 @@ def run_ours(args, world, rank, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     s = synth.shape(args.config)
-    inp = synth.make_inputs(args.config, device=dev, seed=1234 + 100 * args.config + 7919 * rank)
+    inp = synth.make_inputs(args.config, device=dev, seed=replica_seed(args.config, rank))
     w = dt.Weights.of(inp)
     rnd = dt.Round(s.B, s.K, s.V, s.M, s.n, s.max_depth, s.T, w, device=dev)
     flush_w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -403,13 +427,8 @@ def run_ours(args, world, rank, local):
         rnd.check()
         graph_ms = np.array([a.elapsed_time(b) for a, b in gevs])
         del graph
-    total_s = float(round_ms.sum()) / 1e3
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_s], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_s = float(t.item())
-    value = world * s.B * args.steps / total_s
+    total_s = max_over_ranks(float(round_ms.sum()) / 1e3, world, dev)
+    value = job_throughput(world, s.B, args.steps, total_s)
 
     out = {k: v.cpu().numpy() for k, v in rnd.out.items()}
     topm_b, build_b, parts = algorithmic_bytes(s, out["tokens"], out["parents"], out["depth"])
@@ -579,13 +598,8 @@ def run_ours(args, world, rank, local):
         barrier()
         hr.check()
         assert np.array_equal(hr.host_out["tokens"].numpy(), out["tokens"]), "host-buffer round differs"
-        e2e_s = sum(a.elapsed_time(b) for a, b in ev2) / 1e3
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t.item())
-        e2e = {"value": round(world * s.B * args.steps / e2e_s, 2), "unit": "trees/s",
+        e2e_s = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev2) / 1e3, world, dev)
+        e2e = {"value": round(job_throughput(world, s.B, args.steps, e2e_s), 2), "unit": "trees/s",
                "h2d_bytes_per_step": hr.h2d_bytes(), "d2h_bytes_per_step": hr.d2h_bytes(),
                "us_per_round": round(e2e_s / args.steps * 1e6, 2)}
         # the same host rounds replayed from their captured CUDA graph (HostRound.capture: the copy in, the round's
