@@ -9,6 +9,7 @@ import subprocess
 import pytest
 
 import pins
+from oracle import compare
 from oracle import oracle as orc
 
 MUTANTS = {
@@ -63,15 +64,19 @@ def _mutant_source(name):
     return src.replace(old, new)
 
 
-@pytest.mark.parametrize("name", sorted(MUTANTS))
-def test_pins_catch_mutant(name, tmp_path):
+def _compile(name, tmp_path):
     src = tmp_path / "mutant.cpp"
     src.write_text(_mutant_source(name))
     out = tmp_path / "libmutant.so"
     cmd = orc.compile_command(src, out)
     cmd[1] = "-O1"
     subprocess.run(cmd, check=True)
-    L = orc.load(out)
+    return orc.load(out)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path):
+    L = _compile(name, tmp_path)
     caught = None
     for pin in pins.ALL_PINS:
         try:
@@ -80,3 +85,34 @@ def test_pins_catch_mutant(name, tmp_path):
             caught = (pin.__name__, type(e).__name__)
             break
     assert caught is not None, f"no pin detects the planted mistake {name!r}"
+
+
+# The mutants that change the trees themselves: the GPU-vs-oracle rule (oracle/compare.py) must reject their trees,
+# as it would a kernel's that made the same mistake (the tie-break mutants are left to the golden trees: ties are
+# rare on random inputs).
+TREE_MUTANTS = ["gru-drops-b_hh", "gru-reset-gate-wrong-row", "gru-update-gate-swapped", "gru-sigmoid-sign",
+                "correction-columns-reversed", "correction-after-temperature", "softmax-drops-normaliser",
+                "position-off-by-one", "hidden-state-not-carried", "score-not-cumulative", "mask-self-only",
+                "embedding-of-parent"]
+
+
+@pytest.mark.parametrize("name", TREE_MUTANTS)
+def test_parity_rule_rejects_mutant_trees(name, tmp_path):
+    L = _compile(name, tmp_path)
+    inp = pins.tiny_inputs(5, dtype="bf16", B=4, M=6, n=16, max_depth=4, T=0.5)
+    s = inp.shape
+    logits, h0, w = pins.host(inp)
+    ids, vals = orc.topm(logits, s.M)
+    ora = orc.build_trees(ids, vals, h0, w, s.n, s.max_depth, s.T)
+    bad = orc.build_trees(ids, vals, h0, w, s.n, s.max_depth, s.T, L=L)
+    resc = orc.rescore(ids, vals, h0, w, bad["tokens"], bad["parents"], bad["depth"], s.max_depth, s.T)
+    compare.compare_round(ora, ora, orc.rescore(ids, vals, h0, w, ora["tokens"], ora["parents"], ora["depth"],
+                                                s.max_depth, s.T), s.n, s.max_depth)  # the rule accepts the oracle
+    with pytest.raises(AssertionError):
+        compare.compare_round(bad, ora, resc, s.n, s.max_depth)
+    # and past the first near-tie too (no bit-exact prefix at all), with the mutant's own scores or with its tree
+    # given the true scores, so that only the tree's shape can tell
+    relabelled = dict(bad, scores=resc)
+    for tree in (bad, relabelled):
+        with pytest.raises(AssertionError):
+            compare.compare_round(tree, ora, resc, s.n, s.max_depth, struct_tol=float("inf"))
