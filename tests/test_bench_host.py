@@ -1,6 +1,7 @@
-"""bench.py's host-side arithmetic on the CPU: the roofline numerators (a launch's and a round's algorithmic bytes)
+"""bench.py's host-side logic on the CPU: the roofline numerators (a launch's and a round's algorithmic bytes)
 from hand-worked trees, the launch count, the peaks' fallback, and the rule that a committed ncu traffic figure
-counts only while the call's sources are the ones it was taken on."""
+counts only while the call's sources are the ones it was taken on, and the SM-clock sampler against a fake NVML
+(read-only queries: median clock, throttle reasons, no library)."""
 import json
 import os
 
@@ -97,3 +98,55 @@ def test_committed_traffic_is_keyed_by_workload_names():
         d = json.load(f)
     names = {w for call in ("dt_topm", "dt_build_trees") for w in d.get(call, {})}
     assert names and names <= {synth.shape(c).name for c in range(5)}
+
+
+class FakeNvml:
+    """Answers the read-only NVML queries the clock sampler makes: SM clocks from a list, one reasons word."""
+
+    def __init__(self, clocks, reasons, max_mhz=2070, init_rc=0):
+        self.clocks, self.reasons, self.max_mhz, self.init_rc, self.i = clocks, reasons, max_mhz, init_rc, 0
+
+    def nvmlInit_v2(self):
+        return self.init_rc
+
+    def nvmlDeviceGetHandleByIndex_v2(self, index, ref):
+        return 0
+
+    def nvmlDeviceGetMaxClockInfo(self, h, kind, ref):
+        ref._obj.value = self.max_mhz
+        return 0
+
+    def nvmlDeviceGetClockInfo(self, h, kind, ref):
+        ref._obj.value = self.clocks[self.i % len(self.clocks)]
+        self.i += 1
+        return 0
+
+    def nvmlDeviceGetCurrentClocksEventReasons(self, h, ref):
+        ref._obj.value = self.reasons
+        return 0
+
+
+def sample(monkeypatch, fake):
+    def cdll(name):
+        if fake is None:
+            raise OSError(name)
+        return fake
+    monkeypatch.setattr(bench.ctypes, "CDLL", cdll)
+    with bench.ClockSampler(0, period_s=0.001) as cs:
+        bench.time.sleep(0.05)
+    return cs.summary()
+
+
+def test_clock_sampler_reports_median_clock_and_reasons(monkeypatch):
+    s = sample(monkeypatch, FakeNvml([2070, 1950, 2070], 0x4 | 0x1))  # sw_power_cap while busy, idle in between
+    assert s["source"] == "nvml" and s["samples"] > 3
+    assert s["sm_mhz"] == 2070 and s["sm_max_mhz"] == 2070
+    assert s["reasons"] == ["sw_power_cap"]  # idle is not a throttle
+    s = sample(monkeypatch, FakeNvml([1500], 0x8 | 0x40))
+    assert s["sm_mhz"] == 1500 and s["reasons"] == ["hw_slowdown", "hw_thermal_slowdown"]
+
+
+def test_clock_sampler_without_nvml(monkeypatch):
+    for fake in (None, FakeNvml([2070], 0, init_rc=1)):  # no library; a library that does not start
+        s = sample(monkeypatch, fake)
+        assert s["source"] == "unavailable" and s["sm_mhz"] is None and s["samples"] == 0
