@@ -270,3 +270,24 @@ def test_packed_buffers_align_every_view(dtlib):
     assert spans[-1][1] <= buf.numel()
     v["c"][1, 2] = 1.5
     assert v["c"][1, 2].item() == 1.5 and v["a"].shape == (3, 5) and v["d"].dtype == torch.uint8
+
+
+def test_workspace_calls_reject_bad_arguments(dtlib):
+    """The workspace's own calls check their pointer and size on the host, before any CUDA call."""
+    L = dtlib.lib()
+    assert L.dt_workspace_init(None, 1 << 20, None) == INVALID
+    assert L.dt_workspace_init(A + 8, 1 << 20, None) == INVALID   # misaligned
+    assert L.dt_workspace_init(A, 16, None) == INVALID            # smaller than the status header
+    assert L.dt_get_error(None, None) == INVALID
+    assert L.dt_get_error(A + 4, None) == INVALID
+
+
+def test_device_sized_workspaces_reject_empty_shapes(dtlib):
+    """The projection's and the tree attention's workspace sizes depend on the device (its SM count); shapes with
+    nothing to compute get 0 before the device is asked."""
+    L = dtlib.lib()
+    for args in [(0, 64, 1000, 8), (16, 0, 1000, 8), (16, 64, 0, 8), (16, 64, 1000, 0)]:
+        assert L.dt_lmhead_workspace_bytes(*args) == 0, args
+    for args in [(0, 16, 128, 32, 8, 128), (1, 0, 128, 32, 8, 128), (1, 16, -1, 32, 8, 128), (1, 16, 128, 0, 8, 128),
+                 (1, 16, 128, 32, 0, 128), (1, 16, 128, 32, 8, 0)]:
+        assert L.dt_tree_attention_workspace_bytes(*args) == 0, args
