@@ -50,3 +50,20 @@ def test_oracle_includes_nothing_of_the_product():
     assert includes and all("/" not in i and not i.endswith((".cuh", ".cu")) and i != "dominotree.h"
                             for i in includes), includes
     assert "dt_" not in re.sub(r"//.*|/\*.*?\*/", "", text, flags=re.S).replace("std::", ""), "calls into the product"
+
+
+def test_the_binding_fails_loudly_without_its_library():
+    """No fallback: with the compiled library absent, the first call raises instead of computing anything else."""
+    code = (
+        "import pathlib\n"
+        "from speculative_decoding_tree_top_gb300 import buildlib, dominotree\n"
+        "buildlib.LIB = pathlib.Path('/nonexistent/libdominotree.so')\n"
+        "try:\n"
+        "    dominotree.lib()\n"
+        "except RuntimeError as e:\n"
+        "    assert 'must be built' in str(e)\n"
+        "else:\n"
+        "    raise SystemExit('no error without the library')\n"
+    )
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:] + r.stdout[-500:]
