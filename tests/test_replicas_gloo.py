@@ -20,7 +20,7 @@ def _free_port():
 
 def _replica(rank, world, port, seconds, queue):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
-                      LOCAL_RANK=str(rank))
+                      LOCAL_RANK=str(rank), GLOO_SOCKET_IFNAME="lo")  # loopback: no hostname lookup needed
     w, r, _ = bench.dist_env()
     dist.init_process_group("gloo", rank=r, world_size=w)
     try:
