@@ -19,7 +19,7 @@ def _sources(top, exts):
                 yield os.path.join(d, f)
 
 
-def test_loading_the_product_loads_no_oracle():
+def test_loading_the_product_loads_no_oracle(dtlib):  # dtlib: the library is built first
     code = (
         "import sys\n"
         "import speculative_decoding_tree_top_gb300 as pkg\n"
